@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Benchmark of mamba_mimo_bwd_fwd on the pages' timed shape
+(B=1, S=8192, H=16, G=1, R=4, N=P=64, C=16, rotary_dim_divisor=4, reduced
+dout, D and Z on; synthetic inputs).  Prints one JSON line.
+
+A step is one call of the C ABI entry point (all kernels of the op) on one
+input set already resident in HBM.  Four input/output sets rotate between
+steps (together larger than the 129 MB L2), so no step reuses the previous
+step's data from L2.  Time is taken with CUDA events on the launching stream,
+with a barrier and synchronize on both sides; under torchrun every rank runs
+its own replica and the slowest rank's time counts.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synthetic_inputs as si  # noqa: E402
+
+METRIC = "MIMO bwd_fwd tokens/s at B1 S8192 H16 N=P=64 R4 C16; HBM GB/s % of peak"
+WORKLOAD_INDEX = 2
+# The pages' own median for this shape (Ascend910, 53.849475 ms per call).
+PAGES_TOKENS_PER_S = 8192 / 0.053849475
+DOMINANT = "chunk_output"
+KERNEL_SOURCE = os.path.join(ROOT, "mamba_mimo_chunked_gb300", "csrc", "mmbf_kernels.cu")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--sets", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic():
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    sha = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for name in sorted(os.listdir(pdir)):
+        if not name.startswith(DOMINANT) or not name.endswith(".md"):
+            continue
+        vals = {}
+        for line in open(os.path.join(pdir, name)):
+            if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
+                k, v = line.strip().split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+        if vals.get("source_sha256") == sha and "traffic_bytes_per_launch" in vals:
+            return float(vals["traffic_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        except Exception:
+            self.uuid = None
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 7]
+        if self.uuid:
+            mine = [r for r in rows if self.uuid.replace("GPU-", "") in r[0]]
+            rows = mine or rows
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.strip() == "Active"})
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+def nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def cpu_baseline(inp_cpu, wl):
+    """The oracle as it stands, timed on this host's cores on the whole
+    workload (every (b,h) head of one input set, BF16-boundary mode)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.bwd_fwd(*si.args_of(inp_cpu))
+    dt = time.perf_counter() - t0
+    return {"value": wl.B * wl.S / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"one full pass over all B*H={wl.B * wl.H} heads of {wl.name} "
+                      f"(BF16-boundary oracle, OpenMP over heads), {dt:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle, timed on host cores.  Each step is a
+    bounded sample of the workload: one head over a prefix of the sequence."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl = si.WORKLOADS[WORKLOAD_INDEX]
+    inp = si.workload_inputs(WORKLOAD_INDEX)
+    cores = os.cpu_count() or 1
+    # Calibrate: seconds per chunk of one head.
+    probe = _prefix(si.head_slice(inp, 0, 0), wl.C * 8, wl.C)
+    t0 = time.perf_counter()
+    oracle.bwd_fwd(*si.args_of(probe))
+    per_chunk = max((time.perf_counter() - t0) / 8, 1e-6)
+    budget = 120.0 / max(args.steps + args.warmup, 1)
+    chunks = int(min(wl.nchunks, max(1, budget / per_chunk)))
+    tokens = chunks * wl.C
+    samples = [_prefix(si.head_slice(inp, 0, h), tokens, wl.C) for h in range(wl.H)]
+    for i in range(args.warmup):
+        oracle.bwd_fwd(*si.args_of(samples[i % wl.H]))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.bwd_fwd(*si.args_of(samples[i % wl.H]))
+    dt = time.perf_counter() - t0
+    value = tokens / wl.H * args.steps / dt      # one head-token is 1/H of a token
+    sample = f"per step: one (b,h) head of {wl.name}, first {tokens} tokens ({chunks} chunks)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / PAGES_TOKENS_PER_S, "dtype": "f64+bf16-rounding",
+            "data": "synthetic", "config": {"workload": wl.name},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _prefix(inp, tokens, C):
+    """The first `tokens` tokens (a multiple of C) of a one-head problem."""
+    out = dict(inp)
+    nc = tokens // C
+    for n in ("dout", "q", "k", "v", "z", "angles"):
+        if inp[n] is not None:
+            out[n] = inp[n][:, :tokens].contiguous()
+    for n in ("da_cs", "da_cs_rev", "dt", "trap"):
+        out[n] = inp[n][:, :, :tokens].contiguous()
+    out["segsum"] = inp["segsum"][:, :, :nc].contiguous()
+    return out
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import mamba_mimo_chunked_gb300 as mm
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mm.build()
+    lib = mm.load_library()
+    wl = si.WORKLOADS[WORKLOAD_INDEX]
+    stream = torch.cuda.current_stream(dev)
+
+    # Input/output sets, resident in HBM before timing starts.
+    sets = []
+    for s in range(args.sets):
+        inp = si.make_inputs(**wl.shape_kwargs(), seed=si.WORKLOAD_SEED_BASE + WORKLOAD_INDEX + 7919 * s
+                             + 104729 * rank, device=dev)
+        out = mm.mamba_mimo_bwd_fwd(*si.args_of(inp))  # allocates outputs, validates once
+        sets.append((inp, out))
+    torch.cuda.synchronize(dev)
+    in_bytes = sum(nbytes(sets[0][0][n]) for n in si.ARG_NAMES)
+    out_bytes = sum(nbytes(t) for t in sets[0][1])
+    alg_bytes = in_bytes + out_bytes
+    ws_bytes = mm.workspace_size(wl.B, wl.S, wl.H, wl.G, wl.R, wl.N, wl.P, wl.C, wl.div,
+                                 wl.reduced, wl.has_z)
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    dims = mm._Dims(wl.B, wl.S, wl.H, wl.G, wl.R, wl.N, wl.P)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+
+    def cargs(inp, out):
+        ptr = mm._ptr
+        return ([ctypes.byref(dims)] + [ptr(inp[n]) for n in si.ARG_NAMES] + [wl.C, wl.div]
+                + [ptr(o) for o in out] + [ptr(workspace), ws_bytes, sh])
+
+    call_args = [cargs(i, o) for i, o in sets]
+    call = lib.mamba_mimo_bwd_fwd
+
+    for i in range(args.warmup):
+        st = call(*call_args[i % len(call_args)])
+        if st:
+            mm._raise(lib, st)
+    launches_per_call = lib.mamba_mimo_last_launch_count()
+
+    # Per-kernel events on sampled steps of the timed region.
+    every = max(1, args.steps // 400)
+    n_samples = (args.steps + every - 1) // every
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n_samples)]
+    ev_arrays = [(ctypes.c_void_p * 8)(*[ctypes.c_void_p(e.cuda_event) for e in row]) for row in ev]
+    for row in ev:                                    # make the handles exist
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    start.record(stream)
+    bad = 0
+    for i in range(args.steps):
+        if i % every == 0:
+            lib.mamba_mimo_set_stage_events(ev_arrays[i // every], 8)
+            bad |= call(*call_args[i % len(call_args)])
+            lib.mamba_mimo_set_stage_events(None, 0)
+        else:
+            bad |= call(*call_args[i % len(call_args)])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world)
+    if bad:
+        raise RuntimeError("a timed call failed")
+    elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, dev)
+
+    stage_ms = {}
+    for k in range(4):
+        name = lib.mamba_mimo_stage_name(k)
+        name = name.decode() if isinstance(name, bytes) else ctypes.string_at(name).decode()
+        if k >= launches_per_call:
+            continue
+        stage_ms[name] = statistics.mean(row[2 * k].elapsed_time(row[2 * k + 1]) for row in ev)
+    dom_ms = stage_ms[DOMINANT]
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
+    ms_per_step = elapsed_s * 1e3 / args.steps
+    value = wl.B * wl.S * args.steps * world / elapsed_s
+
+    # End to end through the public API with host buffers.
+    inp0, out0 = sets[0]
+    host_in = {n: (inp0[n].cpu().pin_memory() if inp0[n] is not None else None) for n in si.ARG_NAMES}
+    host_out = [None if t is None else torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out0]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step():
+        for n in si.ARG_NAMES:
+            if host_in[n] is not None:
+                inp0[n].copy_(host_in[n], non_blocking=True)
+        res = mm.mamba_mimo_bwd_fwd(*si.args_of(inp0), out=out0, workspace=workspace)
+        for h, t in zip(host_out, res):
+            if h is not None:
+                h.copy_(t, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e_start.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(e_start.elapsed_time(e_end) / 1e3, world, dev)
+    e2e = {"value": wl.B * wl.S * args.e2e_steps * world / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+           "ms_per_step": e2e_s * 1e3 / args.e2e_steps}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / (PAGES_TOKENS_PER_S * world),
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "H": wl.H, "G": wl.G, "R": wl.R,
+                   "N": wl.N, "P": wl.P, "chunk_size": wl.C, "rotary_dim_divisor": wl.div,
+                   "reduced_dout": wl.reduced, "z": wl.has_z, "d": wl.has_d,
+                   "parallelism": f"replicas{world}",
+                   "l2": f"{args.sets} rotating input+output sets, "
+                         f"{args.sets * alg_bytes / 1e6:.0f} MB > 129 MB L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profile_traffic(),
+                     "kernel": DOMINANT, "algorithmic_bytes_per_launch": alg_bytes,
+                     "peak_source": peak_kind},
+        "op_hbm_frac": alg_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
+        "stage_ms": stage_ms,
+        "gpu_launches": launches_per_call * args.steps,
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp_cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in sets[0][0].items()}
+        line["cpu_baseline"] = cpu_baseline(inp_cpu, wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

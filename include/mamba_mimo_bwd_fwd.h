@@ -1,0 +1,153 @@
+/*
+ * mamba_mimo_bwd_fwd.h -- C ABI of the GB300 (sm_103a) implementation of the
+ * first backward stage of the Mamba-3 MIMO chunked state-space scan.
+ *
+ * The operation is the one defined on the page "feat: add Triton-Ascend
+ * implementation of Mamba-3 mamba_mimo_bwd_fwd #125" (MindSpeed-Ops):
+ *   - argument list and optional branches: docs/triton/mamba_mimo_bwd_fwd.md,
+ *     sections "使用方法" (usage) and "输入与输出" (input/output tables and
+ *     constraints);
+ *   - arithmetic and BF16 rounding boundaries: the BF16 PyTorch reference
+ *     tests/unit_tests/triton/mamba_mimo_bwd_fwd_bf16_reference.py;
+ *   - validation errors: mindspeed_ops/api/triton/mamba_mimo_bwd_fwd.py,
+ *     function _validate_inputs;
+ *   - meaning of `states` (state entering each chunk) and `qk_dot`
+ *     (same-token R x R q.k): page "MindSpeed-Ops PR #100", section
+ *     "输入缓存的语义".
+ *
+ * Symbols (the pages' notation): B batch, S sequence length, H value heads,
+ * G query/key groups (H % G == 0; head h reads group h / (H / G)), R MIMO
+ * rank, N state dimension, P value dimension, C = chunk_size,
+ * nchunks = ceil(S / C).
+ *
+ * Memory.  Every tensor pointer is a DEVICE pointer to a dense, row-major
+ * (contiguous) tensor in the layout below.  The caller owns all memory:
+ * inputs, outputs and the workspace.  The library never allocates, frees or
+ * synchronises; each call only enqueues kernels on `stream`.
+ *
+ *   input       shape                                 dtype
+ *   dout        reduced: [B,S,H,P]; per-rank: [B,S,R,H,P]  bf16
+ *   q, k        [B,S,R,G,N]                           bf16
+ *   v           [B,S,H,P]                             bf16
+ *   q_bias, k_bias [H,R,N]                            fp32
+ *   mimo_v      [H,R,P]                               fp32
+ *   mimo_o      [H,R,P] or NULL                       fp32   (NULL: dout is per-rank)
+ *   z           [B,S,H,P] or NULL                     bf16
+ *   mimo_z      [H,R,P] or NULL (NULL iff z is NULL)  fp32
+ *   angles      [B,S,H,N/rotary_dim_divisor]          fp32
+ *   da_cs, da_cs_rev, dt  [B,H,S]                     fp32
+ *   trap        [B,H,S]                               bf16
+ *   d           [H] or NULL                           fp32
+ *   segsum      [B,H,nchunks,C,C]                     fp32
+ *
+ *   output      shape                                 dtype
+ *   dmimo_o     [B,H,R,P]   (NULL iff mimo_o NULL)    fp32   per batch, not batch-reduced
+ *   states      [B,H,nchunks,N,P]                     bf16   state entering chunk c
+ *   dz          [B,S,H,P]   (NULL iff z NULL)         bf16
+ *   dmimo_z     [B,H,R,P]   (NULL iff z NULL)         fp32
+ *   qk_dot      [B,H,S,R,R]                           bf16   [r_out, r_in]
+ *
+ * bf16 is IEEE bfloat16 (1-8-7); fp32 is IEEE binary32.  All pointers must be
+ * 4-byte aligned; the workspace 256-byte aligned.  Outputs must not overlap
+ * inputs or each other.
+ *
+ * Envelope (checked; the pages' constraints plus this build's own):
+ *   B, S, H, G, R, N, P >= 1; H % G == 0; N even; N % rotary_dim_divisor == 0;
+ *   rotary_dim_divisor in {2, 4}; N <= 128; P <= 128; 1 <= C*R <= 128;
+ *   this build also requires R <= 16 (MMBF_ERR_UNSUPPORTED otherwise).
+ *
+ * Numerics.  BF16 rounding at the boundaries of the pages' BF16 reference,
+ * FP32 everywhere else (FP32 tensor-core accumulation, FP32 recurrent
+ * state).  Results are deterministic for a given device and input: no
+ * floating-point atomics.
+ */
+#ifndef MAMBA_MIMO_BWD_FWD_H
+#define MAMBA_MIMO_BWD_FWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MAMBA_MIMO_BWD_FWD_ABI_VERSION 1
+
+/* Status codes.  SHAPE/ARG/DTYPE correspond to the pages' ValueError /
+ * TypeError cases; UNSUPPORTED to NotImplementedError. */
+typedef enum {
+  MMBF_OK = 0,
+  MMBF_ERR_SHAPE = 1,       /* a dimension is non-positive or violates a constraint */
+  MMBF_ERR_ARG = 2,         /* a required pointer is NULL, or optional pointers are
+                               inconsistent (z vs mimo_z vs dz/dmimo_z, mimo_o vs dmimo_o) */
+  MMBF_ERR_UNSUPPORTED = 3, /* allowed by the pages, outside this build's envelope */
+  MMBF_ERR_ALIGN = 4,       /* a pointer is not aligned as required */
+  MMBF_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than the size query says */
+  MMBF_ERR_CUDA = 6         /* a CUDA runtime error while enqueuing */
+} mmbf_status;
+
+/* Problem dimensions (see the symbol list above). */
+typedef struct {
+  int64_t B, S, H, G, R, N, P;
+} mmbf_dims;
+
+/* Bytes of device workspace mamba_mimo_bwd_fwd needs for this problem.
+ * `reduced_dout` = (mimo_o != NULL), `has_z` = (z != NULL).  Depends only on
+ * its arguments.  Returns MMBF_OK and writes *bytes, or the validation error
+ * mamba_mimo_bwd_fwd would return for the same shape. */
+mmbf_status mamba_mimo_bwd_fwd_workspace_size(const mmbf_dims* dims, int64_t chunk_size,
+                                              int64_t rotary_dim_divisor, int reduced_dout,
+                                              int has_z, size_t* bytes);
+
+/* Enqueue the first backward stage on `stream` (a cudaStream_t; NULL for the
+ * legacy default stream).  Arguments 2-18 follow the pages' positional order
+ * (dout ... segsum), then chunk_size and rotary_dim_divisor, then the five
+ * outputs in the pages' output order, then the workspace.
+ *
+ * Branches: mimo_o != NULL selects reduced dout and produces dmimo_o;
+ * z != NULL (with mimo_z) produces dz and dmimo_z; d != NULL adds the skip
+ * term d[h] * PsiV to the chunk output.
+ *
+ * On any validation failure nothing is enqueued and an error code is
+ * returned; mamba_mimo_last_error() then describes it.  MMBF_ERR_CUDA
+ * reports a launch error (the stream may hold part of the work).
+ * Asynchronous: outputs are valid once `stream` reaches this point.
+ * Calls that share a workspace must be ordered on one stream. */
+mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const void* q,
+                               const void* k, const void* v, const float* q_bias,
+                               const float* k_bias, const float* mimo_v, const float* mimo_o,
+                               const void* z, const float* mimo_z, const float* angles,
+                               const float* da_cs, const float* da_cs_rev, const float* dt,
+                               const void* trap, const float* d, const float* segsum,
+                               int64_t chunk_size, int64_t rotary_dim_divisor, float* dmimo_o,
+                               void* states, void* dz, float* dmimo_z, void* qk_dot,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Message of the last failed call on the calling thread ("" if none). */
+const char* mamba_mimo_last_error(void);
+
+/* MAMBA_MIMO_BWD_FWD_ABI_VERSION of the loaded library. */
+int mamba_mimo_abi_version(void);
+
+/* Number of kernel launches the last successful mamba_mimo_bwd_fwd call on
+ * this thread enqueued. */
+int mamba_mimo_last_launch_count(void);
+
+/* Optional per-kernel timing (host-side setting of the calling thread).
+ * While set, each mamba_mimo_bwd_fwd call on this thread records
+ * events[2*i] just before and events[2*i+1] just after its i-th kernel
+ * launch, on the call's stream, for every i < count / 2.  `events` holds
+ * cudaEvent_t handles (created with timing enabled) cast to void*; the array
+ * must stay valid while set.  Pass NULL, 0 to stop.  Kernel i is named by
+ * mamba_mimo_stage_name(i). */
+void mamba_mimo_set_stage_events(void* const* events, int count);
+
+/* Name of the i-th kernel a call may launch (0 <= i < 4), or NULL:
+ * "segment_state", "segment_prefix", "chunk_output", "grad_reduce". */
+const char* mamba_mimo_stage_name(int i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_MIMO_BWD_FWD_H */

@@ -1,0 +1,1011 @@
+// GB300 (sm_103a) kernels and C ABI for the first backward stage of the
+// Mamba-3 MIMO chunked scan (`mamba_mimo_bwd_fwd`).
+//
+// What is computed is defined on the page "feat: add Triton-Ascend
+// implementation of Mamba-3 mamba_mimo_bwd_fwd #125": the op document's
+// input/output tables and the BF16-boundary reference
+// (tests/unit_tests/triton/mamba_mimo_bwd_fwd_bf16_reference.py).  The
+// decomposition below is this library's own:
+//
+//   segment_state_kernel   grid (p-slice, segment, b*h)
+//       For a segment of L consecutive chunks, the chunk-local state
+//       contributions U_c = k_state_c^T PsiV_c (BF16 tensor-core GEMM, FP32
+//       accumulate) folded as  local = exp(da_cs[last_c]) * local + U_c,
+//       plus the segment's total decay.  Inputs: k, k_bias, angles, dt, trap,
+//       da_cs, da_cs_rev, v, mimo_v.
+//   segment_prefix_kernel  grid (N*P / 256, b*h)
+//       Exclusive scan over segments: the FP32 state entering each segment.
+//   chunk_output_kernel    grid (p-slice, segment, b*h)
+//       Walks its segment's chunks with the FP32 state resident in shared
+//       memory.  Per chunk: states[c] = bf16(state); biased Q/K (BF16 add);
+//       same-token qk_dot (tensor cores, diagonal tiles only); rotary;
+//       trapezoid factors; the strictly causal (C*R)^2 matrix A, inter =
+//       Q bf16(state) exp(da_cs), intra = A PsiV (tensor cores); the rank-
+//       ordered BF16 diagonal term; out; the Z / projection-gradient branch
+//       (dz, and per-thread partial sums of dmimo_o / dmimo_z); then the
+//       state update.
+//   grad_reduce_kernel     grid (b*h)
+//       Fixed-order sum of the per-segment dmimo_o / dmimo_z partials.
+//
+// Rows of a chunk tile are j = t*R + r (token-major), as in the reference's
+// flatten of the token and rank axes.  BF16 products and sums of two BF16
+// values use mul.rn.bf16x2 / add.rn.bf16x2: the exact product of two BF16
+// values fits FP32, and FP32 (24 bits) >= 2*8+2 bits makes FP32-then-BF16
+// rounding of a sum equal to direct BF16 rounding, so these equal the
+// reference's FP32-op-then-round steps bit for bit.
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "mamba_mimo_bwd_fwd.h"
+
+namespace mmbf {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTargetCtas = 608;  // ~4 per SM on a 152-SM GB300; device-independent
+
+// ---------------------------------------------------------------------------
+// Number formats
+
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+__device__ __forceinline__ float bf_f(uint16_t u) { return __uint_as_float(((uint32_t)u) << 16); }
+__device__ __forceinline__ uint16_t f_bf(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ float round_bf(float x) { return bf_f(f_bf(x)); }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  return (uint32_t)f_bf(lo) | ((uint32_t)f_bf(hi) << 16);
+}
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t badd2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// ---------------------------------------------------------------------------
+// Tensor-core fragments (mma.sync m16n8k16, BF16 in, FP32 accumulate).
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                        const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                          const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// acc[2][4] += A[m0:m0+16, 0:K] * B[0:K, n0:n0+16] for one warp.
+//   A_T = false: A stored row-major [M][K] (leading dim lda)
+//   A_T = true : A stored as its transpose, row-major [K][M]
+//   B_KN = false: B stored as its transpose, row-major [N][K]
+//   B_KN = true : B stored row-major [K][N]
+// All tiles are padded to multiples of 16 rows/cols with zeros, and every
+// row stride is an odd multiple of 16 bytes (ldmatrix rows hit distinct banks).
+template <bool A_T, bool B_KN>
+__device__ __forceinline__ void warp_mma_16x16(float (&acc)[2][4], const uint16_t* A, int lda,
+                                               int m0, const uint16_t* B, int ldb, int n0, int K) {
+  const int lane = threadIdx.x & 31;
+  const int mi = lane >> 3, li = lane & 7;
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+    if (!A_T) {
+      ldsm_x4(a0, a1, a2, a3, A + (m0 + (lane & 15)) * lda + k0 + (lane >> 4) * 8);
+    } else {
+      ldsm_x4_t(a0, a1, a2, a3, A + (k0 + (mi >> 1) * 8 + li) * lda + m0 + (mi & 1) * 8);
+    }
+    if (!B_KN) {
+      ldsm_x4(b0, b1, b2, b3, B + (n0 + (mi >> 1) * 8 + li) * ldb + k0 + (mi & 1) * 8);
+    } else {
+      ldsm_x4_t(b0, b1, b2, b3, B + (k0 + (mi & 1) * 8 + li) * ldb + n0 + (mi >> 1) * 8);
+    }
+    mma16816(acc[0], a0, a1, a2, a3, b0, b1);
+    mma16816(acc[1], a0, a1, a2, a3, b2, b3);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Problem description shared by host and device.
+
+struct Params {
+  int B, S, H, G, R, N, P, C, div, w, half;
+  int nc, CR, MP, NP, PS, npslice, L, nseg;
+  int reduced, has_z, has_d, vec_p;  // vec_p: P even (pairs of p are 4-byte aligned)
+  const uint16_t *dout, *q, *k, *v, *z, *trap;
+  const float *q_bias, *k_bias, *mimo_v, *mimo_o, *mimo_z, *angles, *da_cs, *da_cs_rev, *dt,
+      *d, *segsum;
+  float *dmimo_o, *dmimo_z;
+  uint16_t *states, *dz, *qk_dot;
+  float *ws_state, *ws_decay, *ws_grad;
+};
+
+__host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+// Shared-memory carve-up of chunk_output_kernel (byte offsets).
+struct OutLayout {
+  size_t Qt, Kt, Pt, At, Sb, X, st, qkS, eseg, qbb, kbb, mvb, mob, mzf, tok, red, total;
+};
+__host__ __device__ inline OutLayout out_layout(const Params& p) {
+  OutLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align16(o + bytes); return at; };
+  L.Qt = take((size_t)p.MP * (p.NP + 8) * 2);
+  L.Kt = take((size_t)p.MP * (p.NP + 8) * 2);
+  L.Pt = take((size_t)p.MP * (p.PS + 8) * 2);
+  L.At = take((size_t)p.MP * (p.MP + 8) * 2);
+  L.Sb = take((size_t)p.NP * (p.PS + 8) * 2);
+  L.X = take((size_t)p.MP * (p.PS + 4) * 4);
+  L.st = take((size_t)p.NP * (p.PS + 4) * 4);
+  const size_t tiles_end = o;
+  L.qkS = take((size_t)p.C * p.R * p.R * 4);
+  L.eseg = take(p.C <= 64 ? (size_t)p.C * p.C * 4 : 0);
+  L.qbb = take((size_t)p.R * p.NP * 2);
+  L.kbb = take((size_t)p.R * p.NP * 2);
+  L.mvb = take((size_t)p.R * p.PS * 2);
+  L.mob = take((size_t)p.R * p.PS * 2);
+  L.mzf = take((size_t)p.R * p.PS * 4);
+  L.tok = take((size_t)p.C * 4 * 4);
+  // End-of-segment reduction scratch: reuses the tile region when it fits.
+  const size_t red_bytes = (size_t)(kThreads / (p.PS / 2)) * 2 * p.R * p.PS * 4;
+  if (red_bytes <= tiles_end) {
+    L.red = 0;
+  } else {
+    L.red = take(red_bytes);
+  }
+  L.total = o;
+  return L;
+}
+
+struct StateLayout {
+  size_t Kt, Pt, st, kbb, mvb, tok, total;
+};
+__host__ __device__ inline StateLayout state_layout(const Params& p) {
+  StateLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align16(o + bytes); return at; };
+  L.Kt = take((size_t)p.MP * (p.NP + 8) * 2);
+  L.Pt = take((size_t)p.MP * (p.PS + 8) * 2);
+  L.st = take((size_t)p.NP * (p.PS + 4) * 4);
+  L.kbb = take((size_t)p.R * p.NP * 2);
+  L.mvb = take((size_t)p.R * p.PS * 2);
+  L.tok = take((size_t)p.C * 4 * 4);
+  L.total = o;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Per-chunk building blocks (shared by the state and output kernels).
+
+// Per-token scalars of chunk c: gamma (FP32), factor (BF16 value), exp(da_cs),
+// exp(da_cs_rev).  Trapezoid rule of the reference: gamma = bf16(dt)
+// sigmoid(trap); shifted = bf16(bf16(dt[t+1]) sigmoid(-trap[t+1])) (0 past the
+// padded end); factor = bf16(gamma + shifted).  Padded tokens read dt = trap =
+// da_cs = da_cs_rev = 0.
+__device__ void token_scalars(const Params& p, int bh, int c, float* tok) {
+  const int64_t row = (int64_t)bh * p.S;
+  const int Sp = p.nc * p.C;
+  for (int t = threadIdx.x; t < p.C; t += blockDim.x) {
+    const int tg = c * p.C + t;
+    float gam = 0.f, fac, eda = 1.f, edr = 1.f;
+    float dtv = 0.f, trv = 0.f;
+    if (tg < p.S) {
+      dtv = p.dt[row + tg];
+      trv = bf_f(p.trap[row + tg]);
+      eda = expf(p.da_cs[row + tg]);
+      edr = expf(p.da_cs_rev[row + tg]);
+    }
+    gam = __fmul_rn(round_bf(dtv), sigmoid_f(trv));
+    float sh = 0.f;
+    if (tg + 1 < Sp) {
+      float dtn = 0.f, trn = 0.f;
+      if (tg + 1 < p.S) {
+        dtn = p.dt[row + tg + 1];
+        trn = bf_f(p.trap[row + tg + 1]);
+      }
+      sh = round_bf(__fmul_rn(round_bf(dtn), 1.0f / (1.0f + expf(trn))));
+    }
+    fac = round_bf(__fadd_rn(gam, sh));
+    tok[t] = gam;
+    tok[p.C + t] = fac;
+    tok[2 * p.C + t] = eda;
+    tok[3 * p.C + t] = edr;
+  }
+}
+
+// BF16(x) of FP32 parameter rows [R][len] into a padded [R][ld] table.
+__device__ void param_bf16(const float* src, int R, int len, uint16_t* dst, int ld, int col0,
+                           int total_cols) {
+  for (int e = threadIdx.x; e < R * ld; e += blockDim.x) {
+    const int r = e / ld, x = e % ld;
+    const int col = col0 + x;
+    dst[e] = (x < len && col < total_cols) ? f_bf(src[r * total_cols + col]) : (uint16_t)0;
+  }
+}
+
+// T[j][n] = bf16(src[b,t,r,g,n] + bf16(bias[h,r,n])) for the chunk's rows
+// (pairs of n; N is even).  Padded tokens read q/k = 0.
+__device__ void biased_tile(const Params& p, const uint16_t* src, const uint16_t* biasb,
+                            uint16_t* T, int b, int g, int c) {
+  const int ld = p.NP + 8, npairs = p.N / 2;
+  for (int e = threadIdx.x; e < p.CR * npairs; e += blockDim.x) {
+    const int j = e / npairs, n = 2 * (e % npairs);
+    const int t = j / p.R, r = j % p.R;
+    const int tg = c * p.C + t;
+    uint32_t x = 0;
+    if (tg < p.S)
+      x = __ldg(reinterpret_cast<const uint32_t*>(
+          src + ((((int64_t)b * p.S + tg) * p.R + r) * p.G + g) * p.N + n));
+    const uint32_t bb = *reinterpret_cast<const uint32_t*>(biasb + r * p.NP + n);
+    *reinterpret_cast<uint32_t*>(T + j * ld + n) = badd2(x, bb);
+  }
+}
+
+// Rotary on the pairs (m, N/2 + m), m < N/div, in FP32 with the reference's
+// operation order, each result rounded to BF16; applied to Q (if given) and K.
+// Then K is scaled by the token's factor (BF16 x BF16 product, rounded):
+// k_scaled = bf16(k_rot * factor).  One work item per (token, m < N/2).
+__device__ void rotate_and_scale(const Params& p, uint16_t* Qt, uint16_t* Kt, const float* fac,
+                                 int b, int h, int c) {
+  const int ld = p.NP + 8;
+  const int items = p.C * p.half;
+  for (int e = threadIdx.x; e < items; e += blockDim.x) {
+    const int t = e / p.half, m = e % p.half;
+    const int tg = c * p.C + t;
+    const uint16_t fb = f_bf(fac[t]);
+    const float ff = bf_f(fb);
+    float cs = 1.f, sn = 0.f;
+    const bool rot = m < p.w;
+    if (rot && tg < p.S) {
+      const float th = p.angles[(((int64_t)b * p.S + tg) * p.H + h) * p.w + m];
+      sincosf(th, &sn, &cs);
+    }
+    for (int r = 0; r < p.R; r++) {
+      const int j = t * p.R + r;
+      if (rot && Qt) {
+        const float a = bf_f(Qt[j * ld + m]), x = bf_f(Qt[j * ld + p.half + m]);
+        Qt[j * ld + m] = f_bf(__fsub_rn(__fmul_rn(cs, a), __fmul_rn(sn, x)));
+        Qt[j * ld + p.half + m] = f_bf(__fadd_rn(__fmul_rn(sn, a), __fmul_rn(cs, x)));
+      }
+      float a = bf_f(Kt[j * ld + m]), x = bf_f(Kt[j * ld + p.half + m]);
+      if (rot) {
+        const float a2 = round_bf(__fsub_rn(__fmul_rn(cs, a), __fmul_rn(sn, x)));
+        const float x2 = round_bf(__fadd_rn(__fmul_rn(sn, a), __fmul_rn(cs, x)));
+        a = a2;
+        x = x2;
+      }
+      Kt[j * ld + m] = f_bf(__fmul_rn(a, ff));
+      Kt[j * ld + p.half + m] = f_bf(__fmul_rn(x, ff));
+    }
+  }
+}
+
+// k_state = bf16(k_scaled * exp(da_cs_rev[t])), in place.
+__device__ void k_state_tile(const Params& p, uint16_t* Kt, const float* edr) {
+  const int ld = p.NP + 8;
+  for (int e = threadIdx.x; e < p.CR * p.N; e += blockDim.x) {
+    const int j = e / p.N, n = e % p.N;
+    Kt[j * ld + n] = f_bf(__fmul_rn(bf_f(Kt[j * ld + n]), edr[j / p.R]));
+  }
+}
+
+// PsiV[j][pp] = bf16(v[b,t,h,p0+pp] * bf16(mimo_v[h,r,p0+pp])) for the p-slice.
+__device__ void psi_tile(const Params& p, const uint16_t* mvb, uint16_t* Pt, int b, int h, int c,
+                         int p0, int pw) {
+  const int ld = p.PS + 8;
+  if (p.vec_p) {
+    const int npairs = (pw + 1) / 2;
+    for (int e = threadIdx.x; e < p.CR * npairs; e += blockDim.x) {
+      const int j = e / npairs, pp = 2 * (e % npairs);
+      const int t = j / p.R, r = j % p.R, tg = c * p.C + t;
+      uint32_t x = 0;
+      if (tg < p.S)
+        x = __ldg(reinterpret_cast<const uint32_t*>(
+            p.v + (((int64_t)b * p.S + tg) * p.H + h) * p.P + p0 + pp));
+      const uint32_t m = *reinterpret_cast<const uint32_t*>(mvb + r * p.PS + pp);
+      *reinterpret_cast<uint32_t*>(Pt + j * ld + pp) = bmul2(x, m);
+    }
+  } else {
+    for (int e = threadIdx.x; e < p.CR * pw; e += blockDim.x) {
+      const int j = e / pw, pp = e % pw;
+      const int t = j / p.R, r = j % p.R, tg = c * p.C + t;
+      float x = 0.f;
+      if (tg < p.S) x = bf_f(p.v[(((int64_t)b * p.S + tg) * p.H + h) * p.P + p0 + pp]);
+      Pt[j * ld + pp] = f_bf(__fmul_rn(x, bf_f(mvb[r * p.PS + pp])));
+    }
+  }
+}
+
+// state <- alpha * state + Kt^T Pt  over the (NP x PS) tile (one GEMM, K = MP).
+__device__ void state_update(const Params& p, float* st, const uint16_t* Kt, const uint16_t* Pt,
+                             float alpha) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q4 = lane & 3;
+  const int ldst = p.PS + 4;
+  const int nmb = p.NP / 16, npb = p.PS / 16;
+  for (int task = warp; task < nmb * npb; task += kWarps) {
+    const int m0 = (task / npb) * 16, n0 = (task % npb) * 16;
+    float acc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; nt++) {
+      const int col = n0 + nt * 8 + 2 * q4;
+      acc[nt][0] = st[(m0 + g) * ldst + col] * alpha;
+      acc[nt][1] = st[(m0 + g) * ldst + col + 1] * alpha;
+      acc[nt][2] = st[(m0 + g + 8) * ldst + col] * alpha;
+      acc[nt][3] = st[(m0 + g + 8) * ldst + col + 1] * alpha;
+    }
+    warp_mma_16x16<true, true>(acc, Kt, p.NP + 8, m0, Pt, p.PS + 8, n0, p.MP);
+#pragma unroll
+    for (int nt = 0; nt < 2; nt++) {
+      const int col = n0 + nt * 8 + 2 * q4;
+      st[(m0 + g) * ldst + col] = acc[nt][0];
+      st[(m0 + g) * ldst + col + 1] = acc[nt][1];
+      st[(m0 + g + 8) * ldst + col] = acc[nt][2];
+      st[(m0 + g + 8) * ldst + col + 1] = acc[nt][3];
+    }
+  }
+}
+
+__device__ void zero_smem(unsigned char* base, size_t bytes) {
+  uint4* p = reinterpret_cast<uint4*>(base);
+  const size_t n = bytes / 16;
+  for (size_t i = threadIdx.x; i < n; i += blockDim.x) p[i] = make_uint4(0, 0, 0, 0);
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 1: segment-local state sums.
+
+__global__ void __launch_bounds__(kThreads) segment_state_kernel(Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const StateLayout Ly = state_layout(p);
+  uint16_t* Kt = reinterpret_cast<uint16_t*>(smem + Ly.Kt);
+  uint16_t* Pt = reinterpret_cast<uint16_t*>(smem + Ly.Pt);
+  float* st = reinterpret_cast<float*>(smem + Ly.st);
+  uint16_t* kbb = reinterpret_cast<uint16_t*>(smem + Ly.kbb);
+  uint16_t* mvb = reinterpret_cast<uint16_t*>(smem + Ly.mvb);
+  float* tok = reinterpret_cast<float*>(smem + Ly.tok);
+
+  const int ps = blockIdx.x, seg = blockIdx.y, bh = blockIdx.z;
+  const int b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
+  const int p0 = ps * p.PS, pw = min(p.PS, p.P - p0);
+  const int c0 = seg * p.L, c1 = min(p.nc, c0 + p.L);
+
+  zero_smem(smem, Ly.total);
+  __syncthreads();
+  param_bf16(p.k_bias + (int64_t)h * p.R * p.N, p.R, p.N, kbb, p.NP, 0, p.N);
+  param_bf16(p.mimo_v + (int64_t)h * p.R * p.P, p.R, pw, mvb, p.PS, p0, p.P);
+  float decay = 1.f;
+  for (int c = c0; c < c1; c++) {
+    __syncthreads();
+    token_scalars(p, bh, c, tok);
+    __syncthreads();
+    biased_tile(p, p.k, kbb, Kt, b, g, c);
+    psi_tile(p, mvb, Pt, b, h, c, p0, pw);
+    __syncthreads();
+    rotate_and_scale(p, nullptr, Kt, tok + p.C, b, h, c);
+    __syncthreads();
+    k_state_tile(p, Kt, tok + 3 * p.C);
+    __syncthreads();
+    const int last = min(c * p.C + p.C, p.S) - 1;
+    const float alpha = expf(p.da_cs[(int64_t)bh * p.S + last]);
+    state_update(p, st, Kt, Pt, alpha);
+    decay *= alpha;
+  }
+  __syncthreads();
+  float* dst = p.ws_state + ((int64_t)bh * p.nseg + seg) * p.N * p.P;
+  for (int e = threadIdx.x; e < p.N * pw; e += blockDim.x) {
+    const int n = e / pw, pp = e % pw;
+    dst[n * p.P + p0 + pp] = st[n * (p.PS + 4) + pp];
+  }
+  if (ps == 0 && threadIdx.x == 0) p.ws_decay[(int64_t)bh * p.nseg + seg] = decay;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 2: exclusive prefix over segments (in place): entering state.
+
+__global__ void segment_prefix_kernel(Params p) {
+  const int bh = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= p.N * p.P) return;
+  float acc = 0.f;
+  float* base = p.ws_state + (int64_t)bh * p.nseg * p.N * p.P + e;
+  const float* dec = p.ws_decay + (int64_t)bh * p.nseg;
+  for (int s = 0; s < p.nseg; s++) {
+    const float loc = base[(int64_t)s * p.N * p.P];
+    base[(int64_t)s * p.N * p.P] = acc;
+    acc = acc * dec[s] + loc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 3: per-chunk outputs and gradients.
+
+template <int RMAX>
+__global__ void __launch_bounds__(kThreads) chunk_output_kernel(Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const OutLayout Ly = out_layout(p);
+  uint16_t* Qt = reinterpret_cast<uint16_t*>(smem + Ly.Qt);
+  uint16_t* Kt = reinterpret_cast<uint16_t*>(smem + Ly.Kt);
+  uint16_t* Pt = reinterpret_cast<uint16_t*>(smem + Ly.Pt);
+  uint16_t* At = reinterpret_cast<uint16_t*>(smem + Ly.At);
+  uint16_t* Sb = reinterpret_cast<uint16_t*>(smem + Ly.Sb);
+  float* X = reinterpret_cast<float*>(smem + Ly.X);
+  float* st = reinterpret_cast<float*>(smem + Ly.st);
+  float* qkS = reinterpret_cast<float*>(smem + Ly.qkS);
+  float* eseg = reinterpret_cast<float*>(smem + Ly.eseg);
+  uint16_t* qbb = reinterpret_cast<uint16_t*>(smem + Ly.qbb);
+  uint16_t* kbb = reinterpret_cast<uint16_t*>(smem + Ly.kbb);
+  uint16_t* mvb = reinterpret_cast<uint16_t*>(smem + Ly.mvb);
+  uint16_t* mob = reinterpret_cast<uint16_t*>(smem + Ly.mob);
+  float* mzf = reinterpret_cast<float*>(smem + Ly.mzf);
+  float* tok = reinterpret_cast<float*>(smem + Ly.tok);
+  float* red = reinterpret_cast<float*>(smem + Ly.red);
+
+  const int ps = blockIdx.x, seg = blockIdx.y, bh = blockIdx.z;
+  const int b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
+  const int p0 = ps * p.PS, pw = min(p.PS, p.P - p0);
+  const int c0 = seg * p.L, c1 = min(p.nc, c0 + p.L);
+  const int R = p.R, C = p.C, CR = p.CR;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lg = lane >> 2, lq = lane & 3;
+  const int ldQ = p.NP + 8, ldP = p.PS + 8, ldA = p.MP + 8, ldX = p.PS + 4;
+  const float dval = p.has_d ? p.d[h] : 0.f;
+
+  zero_smem(smem, Ly.total);
+  __syncthreads();
+  param_bf16(p.q_bias + (int64_t)h * R * p.N, R, p.N, qbb, p.NP, 0, p.N);
+  param_bf16(p.k_bias + (int64_t)h * R * p.N, R, p.N, kbb, p.NP, 0, p.N);
+  param_bf16(p.mimo_v + (int64_t)h * R * p.P, R, pw, mvb, p.PS, p0, p.P);
+  if (p.reduced) param_bf16(p.mimo_o + (int64_t)h * R * p.P, R, pw, mob, p.PS, p0, p.P);
+  if (p.has_z)
+    for (int e = threadIdx.x; e < R * p.PS; e += blockDim.x) {
+      const int r = e / p.PS, x = e % p.PS;
+      mzf[e] = (x < pw) ? p.mimo_z[((int64_t)h * R + r) * p.P + p0 + x] : 0.f;
+    }
+  {  // entering state of the segment
+    const float* src = p.ws_state + ((int64_t)bh * p.nseg + seg) * p.N * p.P;
+    for (int e = threadIdx.x; e < p.N * pw; e += blockDim.x) {
+      const int n = e / pw, pp = e % pw;
+      st[n * ldX + pp] = src[n * p.P + p0 + pp];
+    }
+  }
+
+  // Epilogue work assignment: thread -> fixed pair of columns (pp, pp+1) of the
+  // slice, tokens t = slot, slot + nslots, ...
+  const int npairs = p.PS / 2, nslots = kThreads / npairs;
+  const int my_pair = threadIdx.x % npairs, my_slot = threadIdx.x / npairs;
+  const int pp = 2 * my_pair;
+  const bool col0_ok = pp < pw, col1_ok = pp + 1 < pw;
+  float dmo[RMAX][2], dmz[RMAX][2];
+#pragma unroll
+  for (int r = 0; r < RMAX; r++) dmo[r][0] = dmo[r][1] = dmz[r][0] = dmz[r][1] = 0.f;
+
+  for (int c = c0; c < c1; c++) {
+    __syncthreads();
+    token_scalars(p, bh, c, tok);
+    if (C <= 64) {
+      const float* sg = p.segsum + (((int64_t)bh * p.nc + c) * C) * C;
+      for (int e = threadIdx.x; e < C * C; e += blockDim.x) {
+        const int ti = e / C, tj = e % C;
+        eseg[e] = (tj < ti) ? expf(sg[e]) : 0.f;
+      }
+    }
+    // (1) biased Q/K, PsiV, bf16(state) (+ the states output)
+    biased_tile(p, p.q, qbb, Qt, b, g, c);
+    biased_tile(p, p.k, kbb, Kt, b, g, c);
+    psi_tile(p, mvb, Pt, b, h, c, p0, pw);
+    {
+      uint16_t* so = p.states + (((int64_t)bh * p.nc + c) * p.N) * p.P + p0;
+      for (int e = threadIdx.x; e < p.N * pw; e += blockDim.x) {
+        const int n = e / pw, x = e % pw;
+        const uint16_t u = f_bf(st[n * ldX + x]);
+        Sb[n * ldP + x] = u;
+        so[(int64_t)n * p.P + x] = u;
+      }
+    }
+    __syncthreads();
+    // (2) same-token qk_dot on the diagonal tiles of Qh Kh^T
+    for (int rb = warp; rb * 16 < CR; rb += kWarps) {
+      const int tlo = (rb * 16) / R, thi = min((rb * 16 + 15) / R, C - 1);
+      const int cb0 = (tlo * R) / 16, cb1 = (min((thi + 1) * R, CR) + 15) / 16;
+      for (int cb = cb0; cb < cb1; cb++) {
+        float acc[2][4] = {};
+        warp_mma_16x16<false, false>(acc, Qt, ldQ, rb * 16, Kt, ldQ, cb * 16, p.NP);
+#pragma unroll
+        for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+          for (int x = 0; x < 4; x++) {
+            const int row = rb * 16 + lg + ((x >> 1) << 3);
+            const int col = cb * 16 + nt * 8 + 2 * lq + (x & 1);
+            if (row < CR && col < CR && row / R == col / R)
+              qkS[row * R + col % R] = round_bf(acc[nt][x]);
+          }
+      }
+    }
+    __syncthreads();
+    if (ps == 0) {  // qk_dot output: [B,H,S,R,R], contiguous per chunk
+      const int tcount = min(C, p.S - c * C);
+      uint16_t* qo = p.qk_dot + (((int64_t)bh * p.S) + (int64_t)c * C) * R * R;
+      for (int e = threadIdx.x; e < tcount * R * R; e += blockDim.x) qo[e] = f_bf(qkS[e]);
+    }
+    // (3) rotary (Q and K), k_scaled = bf16(k_rot * factor)
+    rotate_and_scale(p, Qt, Kt, tok + C, b, h, c);
+    __syncthreads();
+    // Without mimo_o and z the chunk output feeds nothing: only the state
+    // update remains.
+    if (!(p.reduced || p.has_z)) {
+      k_state_tile(p, Kt, tok + 3 * C);
+      __syncthreads();
+      const int last = min(c * C + C, p.S) - 1;
+      state_update(p, st, Kt, Pt, expf(p.da_cs[(int64_t)bh * p.S + last]));
+      continue;
+    }
+    // (4) causal A = bf16(mask(Q Ks^T) exp(segsum)) and inter = (Q bf16(state)) exp(da_cs)
+    {
+      const int nrb = (CR + 15) / 16;
+      // tasks: A strips (rb, cb < klim/16), then inter strips (rb, pb < PS/16)
+      int ntask_a = 0;
+      for (int rb = 0; rb < nrb; rb++) {
+        const int thi = min((rb * 16 + 15) / R, C - 1);
+        ntask_a += round16(min(thi * R, CR)) / 16;
+      }
+      const int npb = p.PS / 16;
+      const int ntask = ntask_a + nrb * npb;
+      for (int task = warp; task < ntask; task += kWarps) {
+        if (task < ntask_a) {
+          int rb = 0, rem = task;
+          for (;; rb++) {
+            const int thi = min((rb * 16 + 15) / R, C - 1);
+            const int nk = round16(min(thi * R, CR)) / 16;
+            if (rem < nk) break;
+            rem -= nk;
+          }
+          const int cb = rem;
+          float acc[2][4] = {};
+          warp_mma_16x16<false, false>(acc, Qt, ldQ, rb * 16, Kt, ldQ, cb * 16, p.NP);
+#pragma unroll
+          for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+            for (int x = 0; x < 4; x++) {
+              const int row = rb * 16 + lg + ((x >> 1) << 3);
+              const int col = cb * 16 + nt * 8 + 2 * lq + (x & 1);
+              float val = 0.f;
+              if (row < CR && col < CR) {
+                const int ti = row / R, tj = col / R;
+                if (ti > tj) {
+                  const float e = (C <= 64)
+                                      ? eseg[ti * C + tj]
+                                      : expf(p.segsum[(((int64_t)bh * p.nc + c) * C + ti) * C + tj]);
+                  val = __fmul_rn(acc[nt][x], e);
+                }
+              }
+              At[row * ldA + col] = f_bf(val);
+            }
+        } else {
+          const int t2 = task - ntask_a;
+          const int rb = t2 / npb, n0 = (t2 % npb) * 16;
+          float acc[2][4] = {};
+          warp_mma_16x16<false, true>(acc, Qt, ldQ, rb * 16, Sb, ldP, n0, p.NP);
+#pragma unroll
+          for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+            for (int x = 0; x < 4; x++) {
+              const int row = rb * 16 + lg + ((x >> 1) << 3);
+              const int col = n0 + nt * 8 + 2 * lq + (x & 1);
+              const float e = row < CR ? tok[2 * C + row / R] : 0.f;
+              X[row * ldX + col] = __fmul_rn(acc[nt][x], e);
+            }
+        }
+      }
+    }
+    __syncthreads();
+    // (5) intra = A PsiV added to X; k_state in place
+    {
+      const int nrb = (CR + 15) / 16, npb = p.PS / 16;
+      for (int task = warp; task < nrb * npb; task += kWarps) {
+        const int rb = task / npb, n0 = (task % npb) * 16;
+        const int thi = min((rb * 16 + 15) / R, C - 1);
+        const int klim = round16(min(thi * R, CR));
+        if (klim == 0) continue;
+        float acc[2][4] = {};
+        warp_mma_16x16<false, true>(acc, At, ldA, rb * 16, Pt, ldP, n0, klim);
+#pragma unroll
+        for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+          for (int x = 0; x < 4; x++) {
+            const int row = rb * 16 + lg + ((x >> 1) << 3);
+            const int col = n0 + nt * 8 + 2 * lq + (x & 1);
+            X[row * ldX + col] = __fadd_rn(X[row * ldX + col], acc[nt][x]);
+          }
+      }
+    }
+    k_state_tile(p, Kt, tok + 3 * C);
+    __syncthreads();
+    // (6) state update (tensor cores) and the per-element epilogue
+    {
+      const int last = min(c * C + C, p.S) - 1;
+      const float alpha = expf(p.da_cs[(int64_t)bh * p.S + last]);
+      state_update(p, st, Kt, Pt, alpha);
+    }
+    for (int t = my_slot; t < C; t += nslots) {
+      const int tg = c * C + t;
+      const bool valid = tg < p.S;
+      const float gam = tok[t];
+      float zt[2] = {0.f, 0.f}, dov[2] = {0.f, 0.f};
+      const int64_t rowbase = (((int64_t)b * p.S + tg) * p.H + h) * p.P + p0 + pp;
+      if (valid) {
+        if (p.has_z) {
+          if (col0_ok) zt[0] = bf_f(p.z[rowbase]);
+          if (col1_ok) zt[1] = bf_f(p.z[rowbase + 1]);
+        }
+        if (p.reduced) {
+          if (col0_ok) dov[0] = bf_f(p.dout[rowbase]);
+          if (col1_ok) dov[1] = bf_f(p.dout[rowbase + 1]);
+        }
+      }
+      float dzacc[2] = {0.f, 0.f};
+#pragma unroll 1
+      for (int o = 0; o < R; o++) {
+        const int jo = t * R + o;
+        // diagonal: rank-ordered BF16 products and sums, then * gamma
+        uint32_t dg2 = 0;
+        for (int r = 0; r < R; r++) {
+          const uint32_t qb = f_bf(qkS[jo * R + r]);
+          const uint32_t q2 = qb | (qb << 16);
+          const uint32_t ps2 = *reinterpret_cast<const uint32_t*>(Pt + (t * R + r) * ldP + pp);
+          dg2 = badd2(dg2, bmul2(q2, ps2));
+        }
+        const uint32_t psi2 = *reinterpret_cast<const uint32_t*>(Pt + jo * ldP + pp);
+        float outv[2];
+#pragma unroll
+        for (int x = 0; x < 2; x++) {
+          const float dg = round_bf(__fmul_rn(x ? bf_hi(dg2) : bf_lo(dg2), gam));
+          float acc = __fadd_rn(X[jo * ldX + pp + x], dg);
+          if (p.has_d) acc = __fadd_rn(acc, __fmul_rn(dval, x ? bf_hi(psi2) : bf_lo(psi2)));
+          outv[x] = round_bf(acc);
+        }
+#pragma unroll
+        for (int x = 0; x < 2; x++) {
+          if (!(x ? col1_ok : col0_ok)) continue;
+          const float o_ = outv[x];
+          float pz = 0.f, sg = 0.5f, pre = 0.f;
+          if (p.has_z) {
+            pz = __fmul_rn(zt[x], mzf[o * p.PS + pp + x]);
+            sg = sigmoid_f(pz);
+          }
+          if (p.reduced) {
+            const float dv = dov[x];
+            if (p.has_z) {
+              dmo[o][x] += __fmul_rn(__fmul_rn(o_, __fmul_rn(pz, sg)), dv);
+              pre = round_bf(__fmul_rn(round_bf(__fmul_rn(dv, bf_f(mob[o * p.PS + pp + x]))), o_));
+            } else {
+              dmo[o][x] += __fmul_rn(o_, dv);
+            }
+          } else if (p.has_z && valid) {
+            const float dr = bf_f(p.dout[((((int64_t)b * p.S + tg) * R + o) * p.H + h) * p.P + p0 +
+                                         pp + x]);
+            pre = round_bf(__fmul_rn(dr, o_));
+          }
+          if (p.has_z) {
+            const float gzp =
+                __fmul_rn(__fmul_rn(pre, sg), __fadd_rn(1.f, __fmul_rn(pz, 1.0f / (1.0f + expf(pz)))));
+            dzacc[x] = round_bf(__fadd_rn(dzacc[x], __fmul_rn(gzp, mzf[o * p.PS + pp + x])));
+            dmz[o][x] += __fmul_rn(gzp, zt[x]);
+          }
+        }
+      }
+      if (p.has_z && valid) {
+        if (col0_ok) p.dz[rowbase] = f_bf(dzacc[0]);
+        if (col1_ok) p.dz[rowbase + 1] = f_bf(dzacc[1]);
+      }
+    }
+  }
+  // End of segment: fixed-order reduction of dmimo_o / dmimo_z partials over the
+  // threads that share a column pair, into this segment's workspace slot.
+  if (p.reduced || p.has_z) {
+    __syncthreads();
+    for (int r = 0; r < R; r++)
+      for (int x = 0; x < 2; x++) {
+        red[((my_slot * 2 + 0) * R + r) * p.PS + pp + x] = (r < RMAX) ? dmo[r][x] : 0.f;
+        red[((my_slot * 2 + 1) * R + r) * p.PS + pp + x] = (r < RMAX) ? dmz[r][x] : 0.f;
+      }
+    __syncthreads();
+    float* dst = p.ws_grad + ((int64_t)bh * p.nseg + seg) * 2 * R * p.P;
+    for (int e = threadIdx.x; e < 2 * R * pw; e += blockDim.x) {
+      const int which = e / (R * pw), r = (e / pw) % R, x = e % pw;
+      float s = 0.f;
+      for (int sl = 0; sl < nslots; sl++) s += red[((sl * 2 + which) * R + r) * p.PS + x];
+      dst[((int64_t)which * R + r) * p.P + p0 + x] = s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 4: dmimo_o / dmimo_z = sum over segments (fixed order).
+
+__global__ void grad_reduce_kernel(Params p) {
+  const int bh = blockIdx.x;
+  const int RP = p.R * p.P;
+  for (int e = threadIdx.x; e < 2 * RP; e += blockDim.x) {
+    const int which = e / RP, x = e % RP;
+    if (which == 0 && !p.reduced) continue;
+    if (which == 1 && !p.has_z) continue;
+    float s = 0.f;
+    const float* src = p.ws_grad + (int64_t)bh * p.nseg * 2 * RP + (int64_t)which * RP + x;
+    for (int sgm = 0; sgm < p.nseg; sgm++) s += src[(int64_t)sgm * 2 * RP];
+    (which == 0 ? p.dmimo_o : p.dmimo_z)[(int64_t)bh * RP + x] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: planning, validation, launch.
+
+static thread_local char g_err[512] = "";
+static thread_local int g_launches = 0;
+static thread_local void* const* g_stage_events = nullptr;
+static thread_local int g_stage_count = 0;
+static thread_local cudaError_t g_stage_error = cudaSuccess;
+static const char* const kStageNames[4] = {"segment_state", "segment_prefix", "chunk_output",
+                                           "grad_reduce"};
+
+// Records the optional timing event around kernel `i` (before: which = 0).
+static void stage_event(int i, int which, cudaStream_t s) {
+  const int k = 2 * i + which;
+  if (g_stage_events && k < (g_stage_count / 2) * 2 && g_stage_events[k]) {
+    const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(g_stage_events[k]), s);
+    if (e != cudaSuccess && g_stage_error == cudaSuccess) g_stage_error = e;
+  }
+}
+
+// cudaFuncSetAttribute once per kernel and size (kept out of stream capture).
+template <typename K>
+static cudaError_t ensure_smem(K kern, size_t smem, int* cached) {
+  if ((int)smem <= *cached) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) *cached = (int)smem;
+  return e;
+}
+
+static mmbf_status fail(mmbf_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+static size_t out_smem_bytes(Params p, int PS) {
+  p.PS = PS;
+  return out_layout(p).total;
+}
+
+static const size_t kSmemLimit = 227 * 1024;
+
+// Shape validation (the pages' checks in their order, then this build's
+// envelope) and the launch plan: tile sizes, p-slices, segment length.
+static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduced, int has_z,
+                        Params* out) {
+  if (!dims) return fail(MMBF_ERR_ARG, "dims is NULL");
+  const int64_t B = dims->B, S = dims->S, H = dims->H, G = dims->G, R = dims->R, N = dims->N,
+                P = dims->P;
+  if (B < 1 || S < 1 || R < 1 || G < 1)
+    return fail(MMBF_ERR_SHAPE, "B, S, R and G must be positive");
+  if (C < 1 || C * R > 128) return fail(MMBF_ERR_SHAPE, "chunk_size * R must be in [1, 128]");
+  if (div != 2 && div != 4) return fail(MMBF_ERR_SHAPE, "rotary_dim_divisor must be 2 or 4");
+  if (N < 1 || N % div || N % 2)
+    return fail(MMBF_ERR_SHAPE, "N must be even and divisible by rotary_dim_divisor");
+  if (N > 128) return fail(MMBF_ERR_SHAPE, "N greater than 128 is not supported");
+  if (H < 1 || P < 1) return fail(MMBF_ERR_SHAPE, "H and P must be positive");
+  if (H % G) return fail(MMBF_ERR_SHAPE, "H must be divisible by G");
+  if (P > 128) return fail(MMBF_ERR_SHAPE, "P greater than 128 is not supported");
+  if (R > 16) return fail(MMBF_ERR_UNSUPPORTED, "R > 16 is outside this build's envelope");
+  if (S > (int64_t)1 << 30 || B * H > 65535)
+    return fail(MMBF_ERR_UNSUPPORTED, "S > 2^30 or B*H > 65535 is outside this build's envelope");
+  Params p;
+  memset(&p, 0, sizeof p);
+  p.B = (int)B; p.S = (int)S; p.H = (int)H; p.G = (int)G; p.R = (int)R; p.N = (int)N;
+  p.P = (int)P; p.C = (int)C; p.div = (int)div;
+  p.w = p.N / p.div;
+  p.half = p.N / 2;
+  p.nc = (int)((S + C - 1) / C);
+  p.CR = (int)(C * R);
+  p.MP = round16(p.CR);
+  p.NP = round16(p.N);
+  p.reduced = reduced ? 1 : 0;
+  p.has_z = has_z ? 1 : 0;
+  p.vec_p = (P % 2 == 0);
+  int PS = std::min(round16(p.P), 64);
+  while (PS > 16 && out_smem_bytes(p, PS) > kSmemLimit) PS /= 2;
+  if (out_smem_bytes(p, PS) > kSmemLimit)
+    return fail(MMBF_ERR_UNSUPPORTED, "tile does not fit in shared memory");
+  p.PS = PS;
+  p.npslice = (p.P + PS - 1) / PS;
+  const int64_t per_seg = (int64_t)B * H * p.npslice;
+  int nseg = (int)std::min<int64_t>(p.nc, std::max<int64_t>(1, (kTargetCtas + per_seg - 1) / per_seg));
+  p.L = (p.nc + nseg - 1) / nseg;
+  p.nseg = (p.nc + p.L - 1) / p.L;
+  *out = p;
+  return MMBF_OK;
+}
+
+static size_t workspace_bytes_of(const Params& p) {
+  const size_t st = align16((size_t)p.B * p.H * p.nseg * p.N * p.P * 4);
+  const size_t dec = align16((size_t)p.B * p.H * p.nseg * 4);
+  const size_t gr = align16((size_t)p.B * p.H * p.nseg * 2 * p.R * p.P * 4);
+  return st + dec + gr + 256;
+}
+
+template <int RMAX>
+static cudaError_t launch_output(const Params& p, size_t smem, cudaStream_t s) {
+  static int cached = 48 * 1024;
+  auto kern = chunk_output_kernel<RMAX>;
+  cudaError_t e = ensure_smem(kern, smem, &cached);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(p.npslice, p.nseg, p.B * p.H), kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mmbf
+
+using namespace mmbf;
+
+extern "C" {
+
+mmbf_status mamba_mimo_bwd_fwd_workspace_size(const mmbf_dims* dims, int64_t chunk_size,
+                                              int64_t rotary_dim_divisor, int reduced_dout,
+                                              int has_z, size_t* bytes) {
+  Params p;
+  mmbf_status s = plan(dims, chunk_size, rotary_dim_divisor, reduced_dout, has_z, &p);
+  if (s != MMBF_OK) return s;
+  if (!bytes) return fail(MMBF_ERR_ARG, "bytes is NULL");
+  *bytes = workspace_bytes_of(p);
+  return MMBF_OK;
+}
+
+mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const void* q,
+                               const void* k, const void* v, const float* q_bias,
+                               const float* k_bias, const float* mimo_v, const float* mimo_o,
+                               const void* z, const float* mimo_z, const float* angles,
+                               const float* da_cs, const float* da_cs_rev, const float* dt,
+                               const void* trap, const float* d, const float* segsum,
+                               int64_t chunk_size, int64_t rotary_dim_divisor, float* dmimo_o,
+                               void* states, void* dz, float* dmimo_z, void* qk_dot,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = '\0';
+  Params p;
+  mmbf_status s = plan(dims, chunk_size, rotary_dim_divisor, mimo_o != nullptr, z != nullptr, &p);
+  if (s != MMBF_OK) return s;
+  if (!dout || !q || !k || !v || !q_bias || !k_bias || !mimo_v || !angles || !da_cs ||
+      !da_cs_rev || !dt || !trap || !segsum)
+    return fail(MMBF_ERR_ARG, "a required input pointer is NULL");
+  if (!states || !qk_dot) return fail(MMBF_ERR_ARG, "states and qk_dot must not be NULL");
+  if ((z == nullptr) != (mimo_z == nullptr))
+    return fail(MMBF_ERR_ARG, z ? "mimo_z is required when z is present"
+                                : "mimo_z must be None when z is None");
+  if ((mimo_o == nullptr) != (dmimo_o == nullptr))
+    return fail(MMBF_ERR_ARG, "dmimo_o must be given exactly when mimo_o is given");
+  if ((z == nullptr) != (dz == nullptr) || (z == nullptr) != (dmimo_z == nullptr))
+    return fail(MMBF_ERR_ARG, "dz and dmimo_z must be given exactly when z is given");
+  const void* ptrs[] = {dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs,
+                        da_cs_rev, dt, trap, d, segsum, dmimo_o, states, dz, dmimo_z, qk_dot};
+  for (const void* x : ptrs)
+    if (x && (reinterpret_cast<uintptr_t>(x) & 3))
+      return fail(MMBF_ERR_ALIGN, "tensor pointers must be 4-byte aligned");
+  const size_t need = workspace_bytes_of(p);
+  if (!workspace || workspace_bytes < need)
+    return fail(MMBF_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255)
+    return fail(MMBF_ERR_ALIGN, "workspace must be 256-byte aligned");
+
+  p.has_d = d != nullptr;
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.z = static_cast<const uint16_t*>(z);
+  p.trap = static_cast<const uint16_t*>(trap);
+  p.q_bias = q_bias; p.k_bias = k_bias; p.mimo_v = mimo_v; p.mimo_o = mimo_o; p.mimo_z = mimo_z;
+  p.angles = angles; p.da_cs = da_cs; p.da_cs_rev = da_cs_rev; p.dt = dt; p.d = d;
+  p.segsum = segsum;
+  p.dmimo_o = dmimo_o; p.dmimo_z = dmimo_z;
+  p.states = static_cast<uint16_t*>(states);
+  p.dz = static_cast<uint16_t*>(dz);
+  p.qk_dot = static_cast<uint16_t*>(qk_dot);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.ws_state = reinterpret_cast<float*>(ws);
+  ws += align16((size_t)p.B * p.H * p.nseg * p.N * p.P * 4);
+  p.ws_decay = reinterpret_cast<float*>(ws);
+  ws += align16((size_t)p.B * p.H * p.nseg * 4);
+  p.ws_grad = reinterpret_cast<float*>(ws);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  cudaError_t e;
+  {
+    static int cached = 48 * 1024;
+    const size_t smem = state_layout(p).total;
+    e = ensure_smem(segment_state_kernel, smem, &cached);
+    if (e == cudaSuccess) {
+      stage_event(0, 0, st);
+      segment_state_kernel<<<dim3(p.npslice, p.nseg, p.B * p.H), kThreads, smem, st>>>(p);
+      e = cudaGetLastError();
+      stage_event(0, 1, st);
+      launches++;
+    }
+  }
+  if (e == cudaSuccess) {
+    stage_event(1, 0, st);
+    segment_prefix_kernel<<<dim3((p.N * p.P + 255) / 256, p.B * p.H), 256, 0, st>>>(p);
+    e = cudaGetLastError();
+    stage_event(1, 1, st);
+    launches++;
+  }
+  if (e == cudaSuccess) {
+    const size_t smem = out_layout(p).total;
+    stage_event(2, 0, st);
+    if (p.R <= 4)
+      e = launch_output<4>(p, smem, st);
+    else if (p.R <= 8)
+      e = launch_output<8>(p, smem, st);
+    else
+      e = launch_output<16>(p, smem, st);
+    stage_event(2, 1, st);
+    launches++;
+  }
+  if (e == cudaSuccess && (p.reduced || p.has_z)) {
+    stage_event(3, 0, st);
+    grad_reduce_kernel<<<p.B * p.H, 256, 0, st>>>(p);
+    e = cudaGetLastError();
+    stage_event(3, 1, st);
+    launches++;
+  }
+  if (e == cudaSuccess && g_stage_error != cudaSuccess) {
+    e = g_stage_error;
+    g_stage_error = cudaSuccess;
+  }
+  if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
+  g_launches = launches;
+  return MMBF_OK;
+}
+
+const char* mamba_mimo_last_error(void) { return g_err; }
+int mamba_mimo_abi_version(void) { return MAMBA_MIMO_BWD_FWD_ABI_VERSION; }
+int mamba_mimo_last_launch_count(void) { return g_launches; }
+
+void mamba_mimo_set_stage_events(void* const* events, int count) {
+  g_stage_events = (events && count > 0) ? events : nullptr;
+  g_stage_count = g_stage_events ? count : 0;
+}
+
+const char* mamba_mimo_stage_name(int i) { return (i >= 0 && i < 4) ? kStageNames[i] : nullptr; }
+
+}  // extern "C"
