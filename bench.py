@@ -275,11 +275,12 @@ def main():
     every = max(1, args.steps // 400)
     n_samples = (args.steps + every - 1) // every
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n_samples)]
-    ev_arrays = [(ctypes.c_void_p * 8)(*[ctypes.c_void_p(e.cuda_event) for e in row]) for row in ev]
-    for row in ev:                                    # make the handles exist
+    for row in ev:                      # torch creates the CUDA event on first record
         for e in row:
             e.record(stream)
     torch.cuda.synchronize(dev)
+    ev_arrays = [(ctypes.c_void_p * 8)(*[ctypes.c_void_p(e.cuda_event) for e in row]) for row in ev]
+    assert all(e.cuda_event for row in ev for e in row)
 
     sampler = ClockSampler(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
