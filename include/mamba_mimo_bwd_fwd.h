@@ -142,6 +142,11 @@ int mamba_mimo_last_launch_count(void);
  * mamba_mimo_stage_name(i). */
 void mamba_mimo_set_stage_events(void* const* events, int count);
 
+/* Kernel family the last successful mamba_mimo_bwd_fwd call on this thread
+ * used: -1 for the generic kernels (any shape of the envelope), k >= 0 for
+ * the k-th shape-specialised family. */
+int mamba_mimo_last_kernel_variant(void);
+
 /* Name of the i-th kernel a call may launch (0 <= i < 4), or NULL:
  * "segment_state", "segment_prefix", "chunk_output", "grad_reduce". */
 const char* mamba_mimo_stage_name(int i);

@@ -75,6 +75,7 @@ def load_library():
         lib.mamba_mimo_last_launch_count.restype = ctypes.c_int
         lib.mamba_mimo_set_stage_events.restype = None
         lib.mamba_mimo_set_stage_events.argtypes = [ctypes.c_void_p, ctypes.c_int]
+        lib.mamba_mimo_last_kernel_variant.restype = ctypes.c_int
         lib.mamba_mimo_stage_name.restype = ctypes.c_char_p
         lib.mamba_mimo_stage_name.argtypes = [ctypes.c_int]
         _lib = lib
@@ -85,6 +86,12 @@ def load_library():
 def _raise(lib, status: int):
     msg = lib.mamba_mimo_last_error().decode(errors="replace")
     raise MMBF_ERRORS.get(status, RuntimeError)(f"mamba_mimo_bwd_fwd: {msg} (status {status})")
+
+
+def last_kernel_variant() -> int:
+    """-1 if the last call on this thread used the generic kernels, else the
+    index of the shape-specialised kernel family it used."""
+    return load_library().mamba_mimo_last_kernel_variant()
 
 
 def last_launch_count() -> int:

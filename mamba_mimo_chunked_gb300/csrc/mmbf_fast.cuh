@@ -1,0 +1,973 @@
+// Shape-specialised kernels of mamba_mimo_bwd_fwd (included by mmbf_kernels.cu
+// inside namespace mmbf; uses its Params, number-format and mma helpers).
+//
+// Same decomposition and the same arithmetic as the generic kernels, with all
+// tile sizes compile-time and every per-element step kept in registers:
+//
+// * One CTA per (b*h, segment) walks the segment's chunks; one warp per
+//   16-row block of the chunk's (C*R) rows j = t*R + r ("j-block").
+// * The chunk output is produced transposed, X^T[p][j] = inter^T + intra^T,
+//   so each thread owns p-row pairs (p, p+8) and packed f32x2 / bf16x2
+//   instructions act on both.  Inside every j-block the rows are visited in a
+//   fixed permutation (see perm()) chosen so that for R = 4 a thread owns all
+//   four ranks of one token: the rank-ordered BF16 diagonal and dz sums then
+//   need no cross-lane traffic.  The permutation only reorders the summation
+//   index of the contractions; what is computed is unchanged.
+// * The FP32 state is register resident as the transposed tile state^T[p][n]
+//   (an MMA accumulator), split over the warps by p-block.
+// * Raw inputs of chunk c+1 stream into shared memory with cp.async while
+//   chunk c is computed.
+
+namespace fast {
+
+template <int R_, int C_, int N_, int P_, int DIV_>
+struct Cfg {
+  static constexpr int R = R_, C = C_, N = N_, P = P_, DIV = DIV_;
+  static constexpr int CR = C * R;            // rows per chunk
+  static constexpr int NW = CR / 16;          // warps (one per j-block)
+  static constexpr int NT = NW * 32;          // threads
+  static constexpr int TPW = 16 / R;          // tokens per j-block
+  static constexpr int W = N / DIV;           // rotated pairs
+  static constexpr int HALF = N / 2;
+  static constexpr int NKT = N / 16;          // 16-wide k tiles over N
+  static constexpr int NMT = P / 16;          // 16-row p blocks of X^T / state^T
+  static constexpr int LDN = N + 8;           // padded smem row strides (elements)
+  static constexpr int LDP = P + 8;
+  static constexpr int WPM = NW / NMT;        // warps sharing one p-block of the state
+  static constexpr int NCW = N / WPM;         // state columns (n) per warp
+  static constexpr int NN8 = NCW / 8;         // n8 tiles of the state per warp
+  static constexpr int SLOTS = 4;             // X^T columns per thread: (tile nt, bit b)
+  static_assert(R == 2 || R == 4 || R == 8, "fast path: R in {2,4,8}");
+  static_assert(CR % 16 == 0 && NW >= 1 && NW <= 8, "fast path: C*R in {16..128}, multiple of 16");
+  static_assert(N % 32 == 0 && N <= 128 && P % 16 == 0 && P <= 64, "fast path tile sizes");
+  static_assert(NW % NMT == 0 && NCW % 16 == 0, "state split over warps");
+  static_assert(W % 8 == 0, "rotated width multiple of 8");
+};
+
+// Row visited at fragment position i (0..15) of a j-block.  Fragment rows
+// g (< 8) and g + 8 become mma output columns (tile nt = i/8, column i%8);
+// a thread (g, c) owns columns 2c and 2c+1 of both tiles.  The permutation
+// places (R = 4) token c's ranks 0,1 at tile 0 and 2,3 at tile 1; (R = 8)
+// token c/2's ranks 4(c%2) + {0,1} / {2,3}; (R = 2) identity.
+template <int R>
+__device__ __forceinline__ int perm(int i) {
+  const int nt = i >> 3, cc = i & 7;
+  if (R == 4) return 4 * (cc >> 1) + 2 * nt + (cc & 1);
+  if (R == 8) return 8 * (cc >> 2) + 4 * ((cc >> 1) & 1) + 2 * nt + (cc & 1);
+  return i;
+}
+
+// ---------------------------------------------------------------------------
+// Small device helpers
+
+__device__ __forceinline__ void cp16(void* s, const void* g, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(s)), "l"(g),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int NPEND>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(NPEND) : "memory");
+}
+__device__ __forceinline__ void stsm_x4(void* p, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(smem_u32(p)),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+__device__ __forceinline__ void stsm_x4_t(void* p, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(
+                   smem_u32(p)),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+__device__ __forceinline__ float2 unpack2(uint32_t x) {
+  return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t pack2(float2 v) {
+  __nv_bfloat162 b = __float22bfloat162_rn(v);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+__device__ __forceinline__ uint32_t dup_bf(float x) {  // BF16(x) in both halves
+  const uint32_t u = f_bf(x);
+  return u | (u << 16);
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// (a.lo, b.lo) and (a.hi, b.hi) of two BF16 pairs
+__device__ __forceinline__ uint32_t lo_lo(uint32_t a, uint32_t b) { return prmt(a, b, 0x5410); }
+__device__ __forceinline__ uint32_t hi_hi(uint32_t a, uint32_t b) { return prmt(a, b, 0x7632); }
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void st_cs_16(void* g, uint4 v) {
+  asm volatile("st.global.cs.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"l"(g), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory carve-up (byte offsets; every piece 128-byte aligned).
+
+struct Stage {  // raw inputs of one chunk
+  uint32_t q, k, v, dout, z, ang, seg, bytes;
+};
+struct Smem {
+  Stage st[2];
+  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, cosT, sinT, tok, scr, dzs, mvb, mzp, mop, qbs, kbs, red;
+  uint32_t total;
+};
+
+__device__ __host__ inline uint32_t a128(uint32_t x) { return (x + 127u) & ~127u; }
+
+// Stage buffer s (0 or 1): the second buffer is the first shifted by its size
+// (computed, so the layout never needs dynamic indexing).
+__device__ __forceinline__ Stage stage_at(const Stage& s0, int s) {
+  const uint32_t d = s ? s0.bytes : 0u;
+  Stage r = s0;
+  r.q += d; r.k += d; r.v += d; r.dout += d; r.z += d; r.ang += d; r.seg += d;
+  return r;
+}
+
+template <class K>
+__device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool has_z) {
+  Smem L;
+  uint32_t o = 0;
+  auto take = [&](uint32_t bytes) { uint32_t at = o; o = a128(o + bytes); return at; };
+  const bool need_out = out_kernel && (reduced || has_z);
+  for (int s = 0; s < 2; s++) {
+    const uint32_t base = o;
+    L.st[s].q = out_kernel ? take(K::CR * K::LDN * 2) : 0;
+    L.st[s].k = take(K::CR * K::LDN * 2);
+    L.st[s].v = take(K::C * K::LDP * 2);
+    L.st[s].dout = need_out ? take((reduced ? K::C : K::CR) * K::LDP * 2) : 0;
+    L.st[s].z = (need_out && has_z) ? take(K::C * K::LDP * 2) : 0;
+    L.st[s].ang = take(K::C * K::W * 4);
+    L.st[s].seg = need_out ? take(K::C * K::C * 4) : 0;
+    L.st[s].bytes = o - base;
+  }
+  L.Ks = out_kernel ? take(K::CR * K::LDN * 2) : 0;
+  L.Kst = take(K::CR * K::LDN * 2);
+  L.Psi = take(K::CR * K::LDP * 2);
+  L.Sb = out_kernel ? take(K::N * K::LDP * 2) : 0;
+  L.qkd = out_kernel ? take(K::C * K::R * K::R * 4) : 0;
+  L.eseg = need_out ? take(K::C * K::C * 4) : 0;
+  L.cosT = take(K::C * K::W * 4);
+  L.sinT = take(K::C * K::W * 4);
+  L.tok = take(K::C * 4 * 4 + 16);
+  L.scr = take(4 * (K::C + 1) * 4);
+  L.dzs = (need_out && has_z) ? take(K::C * K::LDP * 2) : 0;
+  L.mvb = take(K::R * K::P * 2);
+  L.mzp = (need_out && has_z) ? take(K::R * K::NMT * 8 * 8) : 0;
+  L.mop = (need_out && reduced) ? take(K::R * K::NMT * 8 * 4) : 0;
+  L.qbs = out_kernel ? take(K::R * K::N * 2) : 0;
+  L.kbs = take(K::R * K::N * 2);
+  // end-of-segment reduction scratch reuses the stage buffers when they fit
+  const uint32_t red_bytes = need_out ? (uint32_t)K::NT * 2 * K::SLOTS * K::NMT * 2 * 4 : 0;
+  L.red = (red_bytes <= L.st[0].bytes + L.st[1].bytes) ? 0 : take(red_bytes);
+  L.total = o;
+  return L;
+}
+
+}  // namespace fast
+
+namespace fast {
+
+// Raw inputs of chunk c -> stage buffer (cp.async, 16-byte pieces; rows of
+// tokens past S are zero-filled, which is the reference's zero padding).
+template <class K>
+__device__ void load_stage(const Params& p, const Stage& S, unsigned char* sm, int bh, int c,
+                           bool out_kernel, bool need_out) {
+  const int b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
+  const int t0 = c * K::C;
+  constexpr int GN = K::N / 8, GP = K::P / 8, GA = K::W / 4;
+  for (int e = threadIdx.x; e < K::CR * GN; e += K::NT) {
+    const int j = e / GN, gr = e % GN;
+    const int t = j / K::R, r = j % K::R, tg = t0 + t;
+    const bool ok = tg < p.S;
+    const int64_t off = ((((int64_t)b * p.S + (ok ? tg : 0)) * K::R + r) * p.G + g) * K::N + gr * 8;
+    if (out_kernel) cp16(sm + S.q + (j * K::LDN + gr * 8) * 2, p.q + off, ok);
+    cp16(sm + S.k + (j * K::LDN + gr * 8) * 2, p.k + off, ok);
+  }
+  for (int e = threadIdx.x; e < K::C * GP; e += K::NT) {
+    const int t = e / GP, gr = e % GP, tg = t0 + t;
+    const bool ok = tg < p.S;
+    const int64_t off = (((int64_t)b * p.S + (ok ? tg : 0)) * p.H + h) * K::P + gr * 8;
+    const uint32_t so = (t * K::LDP + gr * 8) * 2;
+    cp16(sm + S.v + so, p.v + off, ok);
+    if (need_out && p.reduced) cp16(sm + S.dout + so, p.dout + off, ok);
+    if (need_out && p.has_z) cp16(sm + S.z + so, p.z + off, ok);
+  }
+  if (need_out && !p.reduced) {  // per-rank dout, rows j = t*R + r
+    for (int e = threadIdx.x; e < K::CR * GP; e += K::NT) {
+      const int j = e / GP, gr = e % GP;
+      const int t = j / K::R, r = j % K::R, tg = t0 + t;
+      const bool ok = tg < p.S;
+      const int64_t off =
+          ((((int64_t)b * p.S + (ok ? tg : 0)) * K::R + r) * p.H + h) * K::P + gr * 8;
+      cp16(sm + S.dout + (j * K::LDP + gr * 8) * 2, p.dout + off, ok);
+    }
+  }
+  for (int e = threadIdx.x; e < K::C * GA; e += K::NT) {
+    const int t = e / GA, gr = e % GA, tg = t0 + t;
+    const bool ok = tg < p.S;
+    const int64_t off = (((int64_t)b * p.S + (ok ? tg : 0)) * p.H + h) * K::W + gr * 4;
+    cp16(sm + S.ang + (t * K::W + gr * 4) * 4, p.angles + off, ok);
+  }
+  if (need_out) {
+    const float* src = p.segsum + ((int64_t)bh * p.nc + c) * K::C * K::C;
+    for (int e = threadIdx.x; e < K::C * K::C / 4; e += K::NT) cp16(sm + S.seg + e * 16, src + e * 4, true);
+  }
+}
+
+// dt, trap, da_cs, da_cs_rev of token c*C + threadIdx.x (threads 0..C; C is the
+// next chunk's first token, for the shifted gamma).  Zero past S.
+template <class K>
+__device__ __forceinline__ float4 load_scalars(const Params& p, int bh, int c) {
+  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int t = threadIdx.x, tg = c * K::C + t;
+  if (t <= K::C && tg < p.S) {
+    const int64_t i = (int64_t)bh * p.S + tg;
+    r.x = __ldg(p.dt + i);
+    r.y = bf_f(__ldg(p.trap + i));
+    r.z = __ldg(p.da_cs + i);
+    r.w = __ldg(p.da_cs_rev + i);
+  }
+  return r;
+}
+template <class K>
+__device__ __forceinline__ void store_scalars(float* scr, float4 v) {
+  const int t = threadIdx.x;
+  if (t <= K::C) {
+    scr[t] = v.x;
+    scr[(K::C + 1) + t] = v.y;
+    scr[2 * (K::C + 1) + t] = v.z;
+    scr[3 * (K::C + 1) + t] = v.w;
+  }
+}
+
+// Token scalars of chunk c: gamma = bf16(dt) sigmoid(trap) (FP32), factor =
+// bf16(gamma + bf16(bf16(dt[t+1]) sigmoid(-trap[t+1]))) (as a BF16 pair),
+// exp(da_cs), exp(da_cs_rev); and the chunk's state decay exp(da_cs[last]).
+// tok layout: gam[C] | facd[C] (u32) | eda[C] | edr[C] | alpha.
+template <class K>
+__device__ void token_scalars(const Params& p, const float* scr, float* tok, int c) {
+  const int t = threadIdx.x;
+  const int Sp = p.nc * K::C;
+  constexpr int C1 = K::C + 1;
+  if (t < K::C) {
+    const int tg = c * K::C + t;
+    const float gam = __fmul_rn(round_bf(scr[t]), sigmoid_f(scr[C1 + t]));
+    float sh = 0.f;
+    if (tg + 1 < Sp)
+      sh = round_bf(__fmul_rn(round_bf(scr[t + 1]), 1.0f / (1.0f + expf(scr[C1 + t + 1]))));
+    tok[t] = gam;
+    reinterpret_cast<uint32_t*>(tok)[K::C + t] = dup_bf(__fadd_rn(gam, sh));
+    tok[2 * K::C + t] = expf(scr[2 * C1 + t]);
+    tok[3 * K::C + t] = expf(scr[3 * C1 + t]);
+  }
+  if (t == K::C) {
+    const int last = min(c * K::C + K::C, p.S) - 1 - c * K::C;
+    tok[4 * K::C] = expf(scr[2 * C1 + last]);
+  }
+}
+
+// sin and cos of x: Cody-Waite reduction of x by 2*pi (2*pi split into the
+// nearest float and the float nearest the remainder) to r in about
+// [-pi, pi], then the sin.approx / cos.approx instructions (absolute error
+// about 2^-20 there; the results only enter BF16-rounded products).
+__device__ __forceinline__ void sincos_fast(float x, float* s, float* c) {
+  const float k = rintf(x * 0.159154943091895336f);
+  float r = fmaf(-k, 6.28318548202514648f, x);
+  r = fmaf(-k, -1.74845560007448e-07f, r);
+  asm("sin.approx.f32 %0, %1;" : "=f"(*s) : "f"(r));
+  asm("cos.approx.f32 %0, %1;" : "=f"(*c) : "f"(r));
+}
+// e^x as 2^(x log2 e) with the ex2.approx instruction.
+__device__ __forceinline__ float exp_fast(float x) { return ex2_approx(x * 1.44269504088896341f); }
+
+// cos/sin of the chunk's angles, [C][W] each.
+template <class K>
+__device__ void sincos_table(const float* ang, float* cosT, float* sinT) {
+  for (int e = threadIdx.x; e < K::C * K::W; e += K::NT) sincos_fast(ang[e], &sinT[e], &cosT[e]);
+}
+
+// This warp's 16 rows of a [CR][LDN] tile as MMA A fragments, rows visited in
+// perm order.
+template <class K>
+__device__ __forceinline__ void load_rows(uint32_t (&f)[K::NKT][4], const uint16_t* tile, int j0) {
+  const int lane = threadIdx.x & 31;
+  const uint16_t* row = tile + (j0 + perm<K::R>(lane & 15)) * K::LDN + (lane >> 4) * 8;
+#pragma unroll
+  for (int kt = 0; kt < K::NKT; kt++) ldsm_x4(f[kt][0], f[kt][1], f[kt][2], f[kt][3], row + kt * 16);
+}
+template <class K>
+__device__ __forceinline__ void store_rows(const uint32_t (&f)[K::NKT][4], uint16_t* tile, int j0) {
+  const int lane = threadIdx.x & 31;
+  uint16_t* row = tile + (j0 + perm<K::R>(lane & 15)) * K::LDN + (lane >> 4) * 8;
+#pragma unroll
+  for (int kt = 0; kt < K::NKT; kt++) stsm_x4(row + kt * 16, f[kt][0], f[kt][1], f[kt][2], f[kt][3]);
+}
+
+// Fragment register (kt, e) holds row i = g + 8 (e & 1), columns
+// kt*16 + 8 (e >> 1) + 2c, +1.
+template <class K>
+__device__ __forceinline__ int frag_row(int e) {
+  return perm<K::R>(((threadIdx.x & 31) >> 2) + 8 * (e & 1));
+}
+
+// x = bf16(x + bf16(bias[r])) on every fragment register (BF16 pair add).
+template <class K>
+__device__ __forceinline__ void add_bias(uint32_t (&f)[K::NKT][4], const uint16_t* bias) {
+  const int c2 = 2 * (threadIdx.x & 3);
+#pragma unroll
+  for (int e = 0; e < 4; e++) {
+    const int r = frag_row<K>(e) % K::R;
+#pragma unroll
+    for (int kt = 0; kt < K::NKT; kt++)
+      f[kt][e] = badd2(f[kt][e], *reinterpret_cast<const uint32_t*>(bias + r * K::N + kt * 16 + 8 * (e >> 1) + c2));
+  }
+}
+
+// Rotary on the pairs (m, N/2 + m), m < W: both partners sit in the same
+// register slot of k tiles kt and kt + NKT/2.  FP32 with the reference's
+// operation order (products, then sum), each result rounded to BF16.
+template <class K>
+__device__ __forceinline__ void rotate_regs(uint32_t& lo, uint32_t& hi, float2 cs, float2 sn) {
+  const float2 a = unpack2(lo), x = unpack2(hi);
+  const float2 sx = __fmul2_rn(sn, x);
+  lo = pack2(__fadd2_rn(__fmul2_rn(cs, a), make_float2(-sx.x, -sx.y)));
+  hi = pack2(__fadd2_rn(__fmul2_rn(sn, a), __fmul2_rn(cs, x)));
+}
+template <class K, bool WITH_Q>
+__device__ __forceinline__ void rotate(uint32_t (&fq)[K::NKT][4], uint32_t (&fk)[K::NKT][4],
+                                       const float* cosT, const float* sinT, int j0) {
+  const int c2 = 2 * (threadIdx.x & 3);
+#pragma unroll
+  for (int kt = 0; kt < K::NKT / 2; kt++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      if (kt * 16 + 8 * (e >> 1) >= K::W) continue;
+      const int tl = (j0 + frag_row<K>(e)) / K::R;
+      const int m = kt * 16 + 8 * (e >> 1) + c2;
+      const float2 cs = *reinterpret_cast<const float2*>(cosT + tl * K::W + m);
+      const float2 sn = *reinterpret_cast<const float2*>(sinT + tl * K::W + m);
+      if (WITH_Q) rotate_regs<K>(fq[kt][e], fq[kt + K::NKT / 2][e], cs, sn);
+      rotate_regs<K>(fk[kt][e], fk[kt + K::NKT / 2][e], cs, sn);
+    }
+}
+
+// k_scaled = bf16(k_rot * factor[t]) (BF16 x BF16), then optionally store it,
+// then k_state = bf16(k_scaled * exp(da_cs_rev[t])) in place.
+template <class K>
+__device__ __forceinline__ void scale_k(uint32_t (&f)[K::NKT][4], const uint32_t* facd, int j0) {
+#pragma unroll
+  for (int e = 0; e < 4; e++) {
+    const uint32_t fd = facd[(j0 + frag_row<K>(e)) / K::R];
+#pragma unroll
+    for (int kt = 0; kt < K::NKT; kt++) f[kt][e] = bmul2(f[kt][e], fd);
+  }
+}
+template <class K>
+__device__ __forceinline__ void k_state(uint32_t (&f)[K::NKT][4], const float* edr, int j0) {
+#pragma unroll
+  for (int e = 0; e < 4; e++) {
+    const float x = edr[(j0 + frag_row<K>(e)) / K::R];
+    const float2 x2 = make_float2(x, x);
+#pragma unroll
+    for (int kt = 0; kt < K::NKT; kt++) f[kt][e] = pack2(__fmul2_rn(unpack2(f[kt][e]), x2));
+  }
+}
+
+// PsiV rows of this warp's j-block (natural order): bf16(v[t] * bf16(mimo_v[r])).
+template <class K>
+__device__ __forceinline__ void psi_rows(const uint16_t* vraw, const uint16_t* mvb, uint16_t* Psi,
+                                         int j0) {
+  constexpr int GP = K::P / 8;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int it = 0; it < GP / 2; it++) {
+    const int q = lane + 32 * it, i = q / GP, gr = q % GP;
+    const int j = j0 + i, tl = j / K::R, r = j % K::R;
+    const uint4 v = *reinterpret_cast<const uint4*>(vraw + tl * K::LDP + gr * 8);
+    const uint4 m = *reinterpret_cast<const uint4*>(mvb + r * K::P + gr * 8);
+    uint4 o;
+    o.x = bmul2(v.x, m.x);
+    o.y = bmul2(v.y, m.y);
+    o.z = bmul2(v.z, m.z);
+    o.w = bmul2(v.w, m.w);
+    *reinterpret_cast<uint4*>(Psi + j * K::LDP + gr * 8) = o;
+  }
+}
+
+// state^T[p][n] (this warp's p-block pm, columns nbase..) = alpha * state^T +
+// PsiV^T Kst over all C*R rows j.
+template <class K>
+__device__ __forceinline__ void state_mma(float (&st)[K::NN8][4], const uint16_t* Psi,
+                                          const uint16_t* Kst, float alpha, int pm, int nbase) {
+  const int lane = threadIdx.x & 31, mi = lane >> 3, li = lane & 7;
+  const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+  for (int nn = 0; nn < K::NN8; nn++) {
+    const float2 x = __fmul2_rn(make_float2(st[nn][0], st[nn][1]), a2);
+    const float2 y = __fmul2_rn(make_float2(st[nn][2], st[nn][3]), a2);
+    st[nn][0] = x.x; st[nn][1] = x.y; st[nn][2] = y.x; st[nn][3] = y.y;
+  }
+#pragma unroll
+  for (int kb = 0; kb < K::NW; kb++) {
+    uint32_t a0, a1, a2_, a3;
+    ldsm_x4_t(a0, a1, a2_, a3, Psi + (kb * 16 + (mi >> 1) * 8 + li) * K::LDP + pm * 16 + (mi & 1) * 8);
+#pragma unroll
+    for (int nn = 0; nn < K::NN8 / 2; nn++) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(b0, b1, b2, b3,
+                Kst + (kb * 16 + (mi & 1) * 8 + li) * K::LDN + nbase + nn * 16 + (mi >> 1) * 8);
+      mma16816(st[2 * nn], a0, a1, a2_, a3, b0, b1);
+      mma16816(st[2 * nn + 1], a0, a1, a2_, a3, b2, b3);
+    }
+  }
+}
+
+// Parameter tables of head h: bf16(mimo_v) [R][P], bf16 biases [R][N].
+template <class K>
+__device__ void param_tables(const Params& p, int h, uint16_t* mvb, uint16_t* qbs, uint16_t* kbs) {
+  for (int e = threadIdx.x; e < K::R * K::P; e += K::NT) mvb[e] = f_bf(p.mimo_v[(int64_t)h * K::R * K::P + e]);
+  for (int e = threadIdx.x; e < K::R * K::N; e += K::NT) {
+    if (qbs) qbs[e] = f_bf(p.q_bias[(int64_t)h * K::R * K::N + e]);
+    kbs[e] = f_bf(p.k_bias[(int64_t)h * K::R * K::N + e]);
+  }
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+}  // namespace fast
+
+namespace fast {
+
+// Segment-local state sums (fast path of segment_state_kernel).
+template <class K>
+__global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  const Smem L = smem_layout<K>(false, p.reduced, p.has_z);
+  const int bh = blockIdx.x, unit = blockIdx.y;
+  const int h = bh % p.H;
+  const int seg = unit / p.UA, sub = unit % p.UA;
+  const int c0 = seg * p.L + sub * p.LA;
+  const int c1 = min(min(c0 + p.LA, seg * p.L + p.L), p.nc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j0 = warp * 16;
+  const int pm = warp % K::NMT, nbase = (warp / K::NMT) * K::NCW;
+  uint16_t* Kst = reinterpret_cast<uint16_t*>(sm + L.Kst);
+  uint16_t* Psi = reinterpret_cast<uint16_t*>(sm + L.Psi);
+  float* cosT = reinterpret_cast<float*>(sm + L.cosT);
+  float* sinT = reinterpret_cast<float*>(sm + L.sinT);
+  float* tok = reinterpret_cast<float*>(sm + L.tok);
+  float* scr = reinterpret_cast<float*>(sm + L.scr);
+  uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
+  uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
+
+  pdl_trigger();  // the prefix kernel may launch; it waits for this grid's results
+  param_tables<K>(p, h, mvb, nullptr, kbs);
+  if (c0 < c1) load_stage<K>(p, L.st[0], sm, bh, c0, false, false);
+  cp_commit();
+  float4 scal = load_scalars<K>(p, bh, c0);
+  float st[K::NN8][4];
+#pragma unroll
+  for (int nn = 0; nn < K::NN8; nn++) st[nn][0] = st[nn][1] = st[nn][2] = st[nn][3] = 0.f;
+  float decay = 1.f;
+  for (int c = c0; c < c1; c++) {
+    const int s = (c - c0) & 1;
+    if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, false, false);
+    const Stage S = stage_at(L.st[0], s);
+    cp_commit();
+    store_scalars<K>(scr, scal);
+    if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
+    cp_wait<1>();
+    __syncthreads();  // (1) chunk c raw inputs and scalars visible
+    token_scalars<K>(p, scr, tok, c);
+    sincos_table<K>(reinterpret_cast<const float*>(sm + S.ang), cosT, sinT);
+    __syncthreads();  // (2)
+    {
+      uint32_t kf[K::NKT][4];
+      load_rows<K>(kf, reinterpret_cast<const uint16_t*>(sm + S.k), j0);
+      add_bias<K>(kf, kbs);
+      rotate<K, false>(kf, kf, cosT, sinT, j0);
+      scale_k<K>(kf, reinterpret_cast<const uint32_t*>(tok) + K::C, j0);
+      k_state<K>(kf, tok + 3 * K::C, j0);
+      store_rows<K>(kf, Kst, j0);
+      psi_rows<K>(reinterpret_cast<const uint16_t*>(sm + S.v), mvb, Psi, j0);
+    }
+    __syncthreads();  // (3)
+    const float alpha = tok[4 * K::C];
+    state_mma<K>(st, Psi, Kst, alpha, pm, nbase);
+    decay *= alpha;
+  }
+  const int g = lane >> 2, cq = lane & 3;
+  float* dst = p.ws_state + ((int64_t)bh * p.nunit + unit) * K::N * K::P;
+#pragma unroll
+  for (int nn = 0; nn < K::NN8; nn++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const int n = nbase + nn * 8 + 2 * cq + (e & 1), pp = pm * 16 + g + 8 * (e >> 1);
+      dst[n * K::P + pp] = st[nn][e];
+    }
+  if (threadIdx.x == 0) p.ws_decay[(int64_t)bh * p.nunit + unit] = decay;
+}
+
+}  // namespace fast
+
+// Exclusive scan over segments, in place: the FP32 state entering each
+// segment.  VEC consecutive elements per thread; the loads of a group of
+// segments are issued before the dependent FMA chain consumes them.
+template <int VEC>
+__global__ void segment_prefix_vec_kernel(Params p) {
+  fast::pdl_trigger();  // the output kernel may launch and prefetch; it waits for this grid
+  fast::pdl_wait();
+  const int bh = blockIdx.y;
+  const int64_t NPe = (int64_t)p.N * p.P;
+  const int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * VEC;
+  if (e < NPe) {
+    float* base = p.ws_state + (int64_t)bh * p.nunit * NPe + e;
+    const float* dec = p.ws_decay + (int64_t)bh * p.nunit;
+    float acc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; v++) acc[v] = 0.f;
+    constexpr int GRP = 8;
+    for (int s0 = 0; s0 < p.nunit; s0 += GRP) {
+      float loc[GRP][VEC];
+#pragma unroll
+      for (int q = 0; q < GRP; q++) {
+        if (s0 + q < p.nunit) {
+          if (VEC == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(base + (int64_t)(s0 + q) * NPe);
+            loc[q][0] = x.x; loc[q][VEC > 1 ? 1 : 0] = x.y;
+            loc[q][VEC > 2 ? 2 : 0] = x.z; loc[q][VEC > 3 ? 3 : 0] = x.w;
+          } else {
+            loc[q][0] = base[(int64_t)(s0 + q) * NPe];
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < GRP; q++) {
+        if (s0 + q < p.nunit) {
+          const float d = dec[s0 + q];
+          float* dstp = base + (int64_t)(s0 + q) * NPe;
+          if (VEC == 4) {
+            *reinterpret_cast<float4*>(dstp) = make_float4(acc[0], acc[VEC > 1 ? 1 : 0],
+                                                           acc[VEC > 2 ? 2 : 0], acc[VEC > 3 ? 3 : 0]);
+          } else {
+            dstp[0] = acc[0];
+          }
+#pragma unroll
+          for (int v = 0; v < VEC; v++) acc[v] = acc[v] * d + loc[q][v];
+        }
+      }
+    }
+  }
+}
+
+namespace fast {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Per-chunk outputs and gradients (fast path of chunk_output_kernel).
+template <class K>
+__global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
+  constexpr int R = K::R, C = K::C, N = K::N, P = K::P, NMT = K::NMT, LDN = K::LDN, LDP = K::LDP;
+  extern __shared__ __align__(128) unsigned char sm[];
+  const bool need_out = p.reduced || p.has_z;
+  const Smem L = smem_layout<K>(true, p.reduced, p.has_z);
+  const int bh = blockIdx.x, seg = blockIdx.y;
+  const int b = bh / p.H, h = bh % p.H;
+  const int c0 = seg * p.L, c1 = min(p.nc, c0 + p.L);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, cq = lane & 3, mi = lane >> 3, li = lane & 7;
+  const int j0 = warp * 16;
+  const int pm = warp % NMT, nbase = (warp / NMT) * K::NCW;
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(sm + L.Ks);
+  uint16_t* Kst = reinterpret_cast<uint16_t*>(sm + L.Kst);
+  uint16_t* Psi = reinterpret_cast<uint16_t*>(sm + L.Psi);
+  uint16_t* Sb = reinterpret_cast<uint16_t*>(sm + L.Sb);
+  uint32_t* qkd = reinterpret_cast<uint32_t*>(sm + L.qkd);
+  float* eseg = reinterpret_cast<float*>(sm + L.eseg);
+  float* cosT = reinterpret_cast<float*>(sm + L.cosT);
+  float* sinT = reinterpret_cast<float*>(sm + L.sinT);
+  float* tok = reinterpret_cast<float*>(sm + L.tok);
+  float* scr = reinterpret_cast<float*>(sm + L.scr);
+  uint16_t* dzs = reinterpret_cast<uint16_t*>(sm + L.dzs);
+  uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
+  float2* mzp = reinterpret_cast<float2*>(sm + L.mzp);
+  uint32_t* mop = reinterpret_cast<uint32_t*>(sm + L.mop);
+  uint16_t* qbs = reinterpret_cast<uint16_t*>(sm + L.qbs);
+  uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
+  const uint32_t* facd = reinterpret_cast<const uint32_t*>(tok) + C;
+  const float* eda = tok + 2 * C;
+  const float* edr = tok + 3 * C;
+
+  // ---- once per CTA: parameters of head h, first chunk's inputs in flight
+  param_tables<K>(p, h, mvb, qbs, kbs);
+  if (need_out && p.has_z)
+    for (int e = threadIdx.x; e < R * NMT * 8; e += K::NT) {
+      const int o = e / (NMT * 8), mt = (e / 8) % NMT, gg = e % 8;
+      const float* mz = p.mimo_z + ((int64_t)h * R + o) * P + mt * 16 + gg;
+      mzp[e] = make_float2(mz[0], mz[8]);
+    }
+  if (need_out && p.reduced)
+    for (int e = threadIdx.x; e < R * NMT * 8; e += K::NT) {
+      const int o = e / (NMT * 8), mt = (e / 8) % NMT, gg = e % 8;
+      const float* mo = p.mimo_o + ((int64_t)h * R + o) * P + mt * 16 + gg;
+      mop[e] = (uint32_t)f_bf(mo[0]) | ((uint32_t)f_bf(mo[8]) << 16);
+    }
+  const float dval = p.has_d ? p.d[h] : 0.f;
+  load_stage<K>(p, L.st[0], sm, bh, c0, true, need_out);
+  cp_commit();
+  float4 scal = load_scalars<K>(p, bh, c0);
+
+  // ---- entering state of the segment (written by the prefix kernel)
+  pdl_wait();
+  float st[K::NN8][4];
+  {
+    const float* src = p.ws_state + ((int64_t)bh * p.nunit + (int64_t)seg * p.UA) * N * P;
+#pragma unroll
+    for (int nn = 0; nn < K::NN8; nn++)
+#pragma unroll
+      for (int e = 0; e < 4; e++)
+        st[nn][e] = src[(nbase + nn * 8 + 2 * cq + (e & 1)) * P + pm * 16 + g + 8 * (e >> 1)];
+  }
+  pdl_trigger();
+
+  float2 dmo[4][NMT], dmz[4][NMT];
+#pragma unroll
+  for (int sl = 0; sl < 4; sl++)
+#pragma unroll
+    for (int mt = 0; mt < NMT; mt++) dmo[sl][mt] = dmz[sl][mt] = make_float2(0.f, 0.f);
+
+  for (int c = c0; c < c1; c++) {
+    const int s = (c - c0) & 1;
+    const Stage S = stage_at(L.st[0], s);
+    if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, true, need_out);
+    cp_commit();
+    store_scalars<K>(scr, scal);
+    if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
+    cp_wait<1>();
+    __syncthreads();  // (1) chunk c raw inputs and scalars visible
+    token_scalars<K>(p, scr, tok, c);
+    if (need_out) {
+      const float* sg = reinterpret_cast<const float*>(sm + S.seg);
+      for (int e = threadIdx.x; e < C * C; e += K::NT)
+        eseg[e] = ((e % C) < (e / C)) ? exp_fast(sg[e]) : 0.f;
+    }
+    sincos_table<K>(reinterpret_cast<const float*>(sm + S.ang), cosT, sinT);
+    __syncthreads();  // (2)
+
+    // ---- warp prologue: Q/K of this j-block, same-token qk_dot, rotary,
+    //      k_scaled / k_state tiles, PsiV rows, bf16(state) tile
+    uint32_t qf[K::NKT][4];
+    {
+      uint32_t kf[K::NKT][4];
+      load_rows<K>(qf, reinterpret_cast<const uint16_t*>(sm + S.q), j0);
+      load_rows<K>(kf, reinterpret_cast<const uint16_t*>(sm + S.k), j0);
+      add_bias<K>(qf, qbs);
+      add_bias<K>(kf, kbs);
+      float qa[2][4];
+#pragma unroll
+      for (int ht = 0; ht < 2; ht++) qa[ht][0] = qa[ht][1] = qa[ht][2] = qa[ht][3] = 0.f;
+#pragma unroll
+      for (int kt = 0; kt < K::NKT; kt++) {
+        mma16816(qa[0], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], kf[kt][0], kf[kt][2]);
+        mma16816(qa[1], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], kf[kt][1], kf[kt][3]);
+      }
+#pragma unroll
+      for (int ht = 0; ht < 2; ht++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int pi = perm<R>(g + 8 * hh), pi2 = perm<R>(ht * 8 + 2 * cq);
+          if (pi / R == pi2 / R) {
+            const int tl = (j0 + pi) / R, o = pi % R, s0 = pi2 % R;
+            const float v0 = round_bf(qa[ht][2 * hh]), v1 = round_bf(qa[ht][2 * hh + 1]);
+            qkd[(tl * R + o) * R + s0] = dup_bf(v0);
+            qkd[(tl * R + o) * R + s0 + 1] = dup_bf(v1);
+            const int tg = c * C + tl;
+            if (tg < p.S)
+              *reinterpret_cast<uint32_t*>(p.qk_dot + (((int64_t)bh * p.S + tg) * R + o) * R + s0) =
+                  (uint32_t)f_bf(v0) | ((uint32_t)f_bf(v1) << 16);
+          }
+        }
+      rotate<K, true>(qf, kf, cosT, sinT, j0);
+      scale_k<K>(kf, facd, j0);
+      store_rows<K>(kf, Ks, j0);
+      k_state<K>(kf, edr, j0);
+      store_rows<K>(kf, Kst, j0);
+    }
+    psi_rows<K>(reinterpret_cast<const uint16_t*>(sm + S.v), mvb, Psi, j0);
+#pragma unroll
+    for (int nn = 0; nn < K::NN8 / 2; nn++) {
+      const uint32_t r0 = pack2(make_float2(st[2 * nn][0], st[2 * nn][1]));
+      const uint32_t r1 = pack2(make_float2(st[2 * nn][2], st[2 * nn][3]));
+      const uint32_t r2 = pack2(make_float2(st[2 * nn + 1][0], st[2 * nn + 1][1]));
+      const uint32_t r3 = pack2(make_float2(st[2 * nn + 1][2], st[2 * nn + 1][3]));
+      stsm_x4_t(Sb + (nbase + nn * 16 + (mi >> 1) * 8 + li) * LDP + pm * 16 + (mi & 1) * 8, r0, r1, r2, r3);
+    }
+    __syncthreads();  // (3) Ks, Kst, PsiV, Sb, qkd complete
+
+    {  // states[c] = bf16(state entering chunk c)
+      constexpr int GP = P / 8;
+      uint16_t* so = p.states + ((int64_t)bh * p.nc + c) * N * P;
+      for (int e = threadIdx.x; e < N * GP; e += K::NT) {
+        const int n = e / GP, gr = e % GP;
+        st_cs_16(so + n * P + gr * 8, *reinterpret_cast<const uint4*>(Sb + n * LDP + gr * 8));
+      }
+    }
+
+    float X[NMT][2][4];
+    if (need_out) {
+      // inter^T = bf16(state)^T q_rot^T, then * exp(da_cs[t]) per column
+#pragma unroll
+      for (int mt = 0; mt < NMT; mt++) {
+#pragma unroll
+        for (int nt = 0; nt < 2; nt++) X[mt][nt][0] = X[mt][nt][1] = X[mt][nt][2] = X[mt][nt][3] = 0.f;
+#pragma unroll
+        for (int kt = 0; kt < K::NKT; kt++) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(a0, a1, a2, a3, Sb + (kt * 16 + (mi >> 1) * 8 + li) * LDP + mt * 16 + (mi & 1) * 8);
+          mma16816(X[mt][0], a0, a1, a2, a3, qf[kt][0], qf[kt][2]);
+          mma16816(X[mt][1], a0, a1, a2, a3, qf[kt][1], qf[kt][3]);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; nt++) {
+        const float ed = eda[(j0 + perm<R>(nt * 8 + 2 * cq)) / R];
+        const float2 e2 = make_float2(ed, ed);
+#pragma unroll
+        for (int mt = 0; mt < NMT; mt++) {
+          const float2 x = __fmul2_rn(make_float2(X[mt][nt][0], X[mt][nt][1]), e2);
+          const float2 y = __fmul2_rn(make_float2(X[mt][nt][2], X[mt][nt][3]), e2);
+          X[mt][nt][0] = x.x; X[mt][nt][1] = x.y; X[mt][nt][2] = y.x; X[mt][nt][3] = y.y;
+        }
+      }
+      // causal blocks jb <= this warp's block: A = bf16(mask(Q Ks^T) exp(segsum)),
+      // intra^T += PsiV^T A^T
+#pragma unroll
+      for (int jb = 0; jb < K::NW; jb++) {
+        if (jb > warp) continue;
+        float sa[2][4];
+#pragma unroll
+        for (int ht = 0; ht < 2; ht++) sa[ht][0] = sa[ht][1] = sa[ht][2] = sa[ht][3] = 0.f;
+        const uint16_t* krow = Ks + (jb * 16 + perm<R>((mi >> 1) * 8 + li)) * LDN + (mi & 1) * 8;
+#pragma unroll
+        for (int kt = 0; kt < K::NKT; kt++) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(b0, b1, b2, b3, krow + kt * 16);
+          mma16816(sa[0], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], b0, b1);
+          mma16816(sa[1], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], b2, b3);
+        }
+        uint32_t bi[2][2];
+#pragma unroll
+        for (int ht = 0; ht < 2; ht++) {
+          const int tcol = (jb * 16 + perm<R>(ht * 8 + 2 * cq)) / R;
+#pragma unroll
+          for (int hh = 0; hh < 2; hh++) {
+            const int trow = (j0 + perm<R>(g + 8 * hh)) / R;
+            const bool on = trow > tcol;
+            const float ex = on ? eseg[trow * C + tcol] : 0.f;
+            const float v0 = on ? __fmul_rn(sa[ht][2 * hh], ex) : 0.f;
+            const float v1 = on ? __fmul_rn(sa[ht][2 * hh + 1], ex) : 0.f;
+            bi[hh][ht] = pack2(make_float2(v0, v1));
+          }
+        }
+        const uint16_t* prow = Psi + (jb * 16 + perm<R>((mi >> 1) * 8 + li)) * LDP + (mi & 1) * 8;
+#pragma unroll
+        for (int mt = 0; mt < NMT; mt++) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(a0, a1, a2, a3, prow + mt * 16);
+          mma16816(X[mt][0], a0, a1, a2, a3, bi[0][0], bi[0][1]);
+          mma16816(X[mt][1], a0, a1, a2, a3, bi[1][0], bi[1][1]);
+        }
+      }
+    }
+    // state update: state^T = exp(da_cs[last]) state^T + PsiV^T k_state
+    state_mma<K>(st, Psi, Kst, tok[4 * C], pm, nbase);
+
+    // ---- per-element epilogue on X^T (p-row pairs (p, p+8), four columns
+    //      per thread).  Column slot (nt, bb) is row j0 + perm(nt*8 + 2c + bb).
+    if (need_out) {
+      constexpr int NTOK = (R == 2) ? 2 : 1;  // tokens per thread
+      constexpr int NS = (R == 2) ? 2 : 4;    // slots per token
+      const uint16_t* zraw = reinterpret_cast<const uint16_t*>(sm + S.z);
+      const uint16_t* draw = reinterpret_cast<const uint16_t*>(sm + S.dout);
+#pragma unroll
+      for (int tt = 0; tt < NTOK; tt++) {
+        const int tl = (j0 + perm<R>(tt * 8 + 2 * cq)) / R;
+        const int tg = c * C + tl;
+        const float gam = tok[tl];
+        const float2 gam2 = make_float2(gam, gam);
+        int oo[NS], slo[NS], nto[NS], bbo[NS];
+#pragma unroll
+        for (int k = 0; k < NS; k++) {
+          nto[k] = (R == 2) ? tt : (k >> 1);
+          bbo[k] = (R == 2) ? k : (k & 1);
+          slo[k] = nto[k] * 2 + bbo[k];
+          oo[k] = perm<R>(nto[k] * 8 + 2 * cq + bbo[k]) % R;
+        }
+        uint32_t qrow[NS][R];
+#pragma unroll
+        for (int k = 0; k < NS; k++)
+#pragma unroll
+          for (int r = 0; r < R; r++) qrow[k][r] = qkd[(tl * R + oo[k]) * R + r];
+#pragma unroll
+        for (int mt = 0; mt < NMT; mt++) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(a0, a1, a2, a3,
+                    Psi + (j0 + perm<R>((mi >> 1) * 8 + li)) * LDP + mt * 16 + (mi & 1) * 8);
+          uint32_t pso[NS];
+#pragma unroll
+          for (int k = 0; k < NS; k++) {
+            const uint32_t xp = nto[k] ? a2 : a0, xp8 = nto[k] ? a3 : a1;
+            pso[k] = bbo[k] ? hi_hi(xp, xp8) : lo_lo(xp, xp8);
+          }
+          uint32_t psiP[R];
+          if (R == 8) {
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+              const uint32_t own = pso[k & (NS - 1)];
+              const uint32_t oth = __shfl_xor_sync(0xffffffffu, own, 1);
+              psiP[k] = (cq & 1) ? oth : own;
+              psiP[(4 + k) % R] = (cq & 1) ? own : oth;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < NS; k++) psiP[k % R] = pso[k];
+          }
+          float2 z2 = make_float2(0.f, 0.f), do2 = make_float2(0.f, 0.f);
+          uint32_t dob = 0;
+          if (p.has_z) {
+            const uint16_t* zr = zraw + tl * LDP + mt * 16 + g;
+            z2 = unpack2((uint32_t)zr[0] | ((uint32_t)zr[8] << 16));
+          }
+          if (p.reduced) {
+            const uint16_t* dr = draw + tl * LDP + mt * 16 + g;
+            dob = (uint32_t)dr[0] | ((uint32_t)dr[8] << 16);
+            do2 = unpack2(dob);
+          }
+          float2 prodz[NS];
+#pragma unroll
+          for (int k = 0; k < NS; k++) {
+            const int o = oo[k], nt = nto[k], bb = bbo[k], sl = slo[k];
+            // diagonal: rank-ordered BF16 products and sums, then * gamma, rounded
+            uint32_t dacc = 0u;
+#pragma unroll
+            for (int r = 0; r < R; r++) dacc = badd2(dacc, bmul2(qrow[k][r], psiP[r]));
+            const float2 dg = unpack2(pack2(__fmul2_rn(unpack2(dacc), gam2)));
+            // out = bf16(inter + intra + diag + d * PsiV)
+            float2 x = __fadd2_rn(make_float2(X[mt][nt][bb], X[mt][nt][bb + 2]), dg);
+            if (p.has_d) x = __fadd2_rn(x, __fmul2_rn(make_float2(dval, dval), unpack2(pso[k])));
+            const uint32_t ob = pack2(x);
+            const float2 of = unpack2(ob);
+            float2 pz = make_float2(0.f, 0.f), sg = make_float2(0.5f, 0.5f), mz = make_float2(0.f, 0.f);
+            if (p.has_z) {
+              mz = mzp[(o * NMT + mt) * 8 + g];
+              pz = __fmul2_rn(z2, mz);
+              const float2 tq = __fmul2_rn(pz, make_float2(-kLog2e, -kLog2e));
+              const float2 den = __fadd2_rn(make_float2(ex2_approx(tq.x), ex2_approx(tq.y)),
+                                            make_float2(1.f, 1.f));
+              sg = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+            }
+            uint32_t preb = 0u;
+            if (p.reduced) {
+              if (p.has_z) {
+                dmo[sl][mt] = __ffma2_rn(__fmul2_rn(of, __fmul2_rn(pz, sg)), do2, dmo[sl][mt]);
+                preb = bmul2(bmul2(dob, mop[(o * NMT + mt) * 8 + g]), ob);
+              } else {
+                dmo[sl][mt] = __ffma2_rn(of, do2, dmo[sl][mt]);
+              }
+            } else if (p.has_z) {
+              const uint16_t* dr = draw + (tl * R + o) * LDP + mt * 16 + g;
+              preb = bmul2((uint32_t)dr[0] | ((uint32_t)dr[8] << 16), ob);
+            }
+            prodz[k] = make_float2(0.f, 0.f);
+            if (p.has_z) {
+              const float2 pre = unpack2(preb);
+              const float2 om = __fadd2_rn(make_float2(1.f, 1.f), make_float2(-sg.x, -sg.y));
+              const float2 gg = __ffma2_rn(pz, om, make_float2(1.f, 1.f));
+              const float2 gz = __fmul2_rn(__fmul2_rn(pre, sg), gg);
+              dmz[sl][mt] = __ffma2_rn(gz, z2, dmz[sl][mt]);
+              prodz[k] = __fmul2_rn(gz, mz);
+            }
+          }
+          if (p.has_z) {  // dz: BF16 running sum over the ranks in order
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < NS; k++) acc = unpack2(pack2(__fadd2_rn(acc, prodz[k])));
+            if (R == 8) {  // ranks 0..3 in the even lane, 4..7 in the odd lane
+              float2 acc2 = unpack2(__shfl_xor_sync(0xffffffffu, pack2(acc), 1));
+#pragma unroll
+              for (int k = 0; k < NS; k++) acc2 = unpack2(pack2(__fadd2_rn(acc2, prodz[k])));
+              if (cq & 1) acc = acc2;
+            }
+            const bool writer = (R == 8) ? ((cq & 1) != 0) : true;
+            if (writer && tg < p.S) {
+              const uint32_t v = pack2(acc);
+              dzs[tl * LDP + mt * 16 + g] = (uint16_t)(v & 0xffffu);
+              dzs[tl * LDP + mt * 16 + g + 8] = (uint16_t)(v >> 16);
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();  // (4)
+    if (need_out && p.has_z) {
+      constexpr int GP = P / 8;
+      for (int e = threadIdx.x; e < C * GP; e += K::NT) {
+        const int t = e / GP, gr = e % GP, tg = c * C + t;
+        if (tg < p.S)
+          st_cs_16(p.dz + (((int64_t)b * p.S + tg) * p.H + h) * P + gr * 8,
+                   *reinterpret_cast<const uint4*>(dzs + t * LDP + gr * 8));
+      }
+    }
+  }  // chunk loop
+
+  // ---- end of segment: fixed-order sum of the dmimo_o / dmimo_z partials
+  if (need_out) {
+    cp_wait<0>();
+    __syncthreads();
+    constexpr int PER = 2 * 4 * NMT * 2;
+    float* red = reinterpret_cast<float*>(sm + L.red);
+    float* mine = red + threadIdx.x * PER;
+#pragma unroll
+    for (int sl = 0; sl < 4; sl++)
+#pragma unroll
+      for (int mt = 0; mt < NMT; mt++) {
+        mine[((0 * 4 + sl) * NMT + mt) * 2 + 0] = dmo[sl][mt].x;
+        mine[((0 * 4 + sl) * NMT + mt) * 2 + 1] = dmo[sl][mt].y;
+        mine[((1 * 4 + sl) * NMT + mt) * 2 + 0] = dmz[sl][mt].x;
+        mine[((1 * 4 + sl) * NMT + mt) * 2 + 1] = dmz[sl][mt].y;
+      }
+    __syncthreads();
+    float* dst = p.ws_grad + ((int64_t)bh * p.nseg + seg) * 2 * R * P;
+    for (int e = threadIdx.x; e < 2 * R * P; e += K::NT) {
+      const int which = e / (R * P), r = (e / P) % R, pp = e % P;
+      const int mt = pp / 16, gg = pp % 8, hh = (pp % 16) / 8;
+      float sum = 0.f;
+      for (int w = 0; w < K::NW; w++)
+        for (int cc = 0; cc < 4; cc++)
+#pragma unroll
+          for (int sl = 0; sl < 4; sl++)
+            if (perm<R>((sl >> 1) * 8 + 2 * cc + (sl & 1)) % R == r)
+              sum += red[(w * 32 + gg * 4 + cc) * PER + ((which * 4 + sl) * NMT + mt) * 2 + hh];
+      dst[e] = sum;
+    }
+  }
+}
+
+}  // namespace fast

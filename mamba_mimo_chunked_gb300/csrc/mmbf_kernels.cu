@@ -140,6 +140,8 @@ struct Params {
   int B, S, H, G, R, N, P, C, div, w, half;
   int nc, CR, MP, NP, PS, npslice, L, nseg;
   int reduced, has_z, has_d, vec_p;  // vec_p: P even (pairs of p are 4-byte aligned)
+  int fast;                          // index of the shape-specialised kernels, or -1
+  int UA, LA, nunit;                 // state units per segment, chunks per unit, units per head
   const uint16_t *dout, *q, *k, *v, *z, *trap;
   const float *q_bias, *k_bias, *mimo_v, *mimo_o, *mimo_z, *angles, *da_cs, *da_cs_rev, *dt,
       *d, *segsum;
@@ -753,6 +755,7 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(Params p) {
 // Kernel 4: dmimo_o / dmimo_z = sum over segments (fixed order).
 
 __global__ void grad_reduce_kernel(Params p) {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // no-op unless launched as a dependent
   const int bh = blockIdx.x;
   const int RP = p.R * p.P;
   for (int e = threadIdx.x; e < 2 * RP; e += blockDim.x) {
@@ -766,6 +769,8 @@ __global__ void grad_reduce_kernel(Params p) {
   }
 }
 
+#include "mmbf_fast.cuh"
+
 // ---------------------------------------------------------------------------
 // Host side: planning, validation, launch.
 
@@ -774,6 +779,8 @@ static thread_local int g_launches = 0;
 static thread_local void* const* g_stage_events = nullptr;
 static thread_local int g_stage_count = 0;
 static thread_local cudaError_t g_stage_error = cudaSuccess;
+static thread_local int g_failed_stage = -1;  // kernel index of a failed launch
+static thread_local int g_variant = -1;       // kernel family of the last call
 static const char* const kStageNames[4] = {"segment_state", "segment_prefix", "chunk_output",
                                            "grad_reduce"};
 
@@ -809,6 +816,96 @@ static size_t out_smem_bytes(Params p, int PS) {
 }
 
 static const size_t kSmemLimit = 227 * 1024;
+
+// ---- shape-specialised kernels: instantiated shapes and launch plan
+using FastA = fast::Cfg<4, 16, 64, 64, 4>;  // R4 C16 N=P=64 (the pages' timed and unit-test shape)
+using FastB = fast::Cfg<8, 16, 64, 64, 4>;  // R8 C16 N=P=64
+using FastC = fast::Cfg<4, 16, 32, 32, 4>;  // R4 C16 N=P=32
+constexpr int kNumFast = 3;
+
+template <class K>
+static bool fast_fits(const Params& p) {
+  return p.R == K::R && p.C == K::C && p.N == K::N && p.P == K::P && p.div == K::DIV;
+}
+static int fast_index(const Params& p) {
+  if (fast_fits<FastA>(p)) return 0;
+  if (fast_fits<FastB>(p)) return 1;
+  if (fast_fits<FastC>(p)) return 2;
+  return -1;
+}
+template <class K>
+static size_t fast_out_smem(const Params& p) {
+  return fast::smem_layout<K>(true, p.reduced, p.has_z).total;
+}
+template <class K>
+static size_t fast_state_smem(const Params& p) {
+  return fast::smem_layout<K>(false, p.reduced, p.has_z).total;
+}
+
+// Resident output-kernel CTAs on the current device (SMs x CTAs per SM), or a
+// GB300-sized default when no device can be queried.
+template <class K>
+static int fast_slots_of(const Params& p) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 2 * 152;
+  }
+  const size_t smem = fast_out_smem<K>(p);
+  if (cudaFuncSetAttribute(fast::output_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    cudaGetLastError();
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fast::output_kernel<K>, K::NT, smem) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  return sms * per_sm;
+}
+static int fast_slots(const Params& p) {
+  // cached per device and specialisation (the occupancy query is not free)
+  static int cache[16][kNumFast][2][2];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = 0;
+  }
+  int* slot = (dev >= 0 && dev < 16) ? &cache[dev][p.fast][p.reduced][p.has_z] : nullptr;
+  if (slot && *slot > 0) return *slot;
+  int v;
+  switch (p.fast) {
+    case 0: v = fast_slots_of<FastA>(p); break;
+    case 1: v = fast_slots_of<FastB>(p); break;
+    default: v = fast_slots_of<FastC>(p); break;
+  }
+  if (slot) *slot = v;
+  return v;
+}
+// Chunks per segment: the length that minimises (waves x (L + per-CTA setup)),
+// with every segment a CTA of the output kernel.
+static int fast_segment_length(const Params& p, int slots) {
+  static thread_local int64_t key[3] = {-1, -1, -1};
+  static thread_local int val = 1;
+  const int64_t heads = (int64_t)p.B * p.H;
+  if (key[0] == p.nc && key[1] == heads && key[2] == slots) return val;
+  double best = 1e300;
+  int bestL = p.nc;
+  for (int L = 1; L <= p.nc; L++) {
+    const int64_t nseg = (p.nc + L - 1) / L;
+    if (nseg > 4096 || heads * nseg > (int64_t)1 << 30) continue;
+    const int64_t waves = (heads * nseg + slots - 1) / slots;
+    const double cost = (double)waves * (L + 2.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      bestL = L;
+    }
+  }
+  key[0] = p.nc; key[1] = heads; key[2] = slots;
+  val = bestL;
+  return bestL;
+}
 
 // Shape validation (the pages' checks in their order, then this build's
 // envelope) and the launch plan: tile sizes, p-slices, segment length.
@@ -853,14 +950,41 @@ static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduc
   int nseg = (int)std::min<int64_t>(p.nc, std::max<int64_t>(1, (kTargetCtas + per_seg - 1) / per_seg));
   p.L = (p.nc + nseg - 1) / nseg;
   p.nseg = (p.nc + p.L - 1) / p.L;
+  p.UA = 1;
+  p.LA = p.L;
+  p.nunit = p.nseg;
+  p.fast = fast_index(p);
+  if (p.fast >= 0) {
+    p.L = fast_segment_length(p, fast_slots(p));
+    p.nseg = (p.nc + p.L - 1) / p.L;
+    // The state-sum kernel works on units of about L/UA chunks: enough CTAs to
+    // fill the GPU several times over, short chains that hide load latency.
+    const int64_t heads = (int64_t)p.B * p.H;
+    int ua = (int)std::max<int64_t>(1, std::min<int64_t>(8, (8 * 152 + heads * p.nseg - 1) / (heads * p.nseg)));
+    ua = std::min(ua, p.L);
+    p.LA = (p.L + ua - 1) / ua;
+    p.UA = (p.L + p.LA - 1) / p.LA;
+    p.nunit = p.nseg * p.UA;
+  }
   *out = p;
   return MMBF_OK;
 }
 
+// Workspace: per (b,h) and segment, the FP32 [N][P] state sum, the decay
+// product and the [2][R][P] gradient partials.  Sized for the larger of the
+// generic and the specialised plan, so one size serves both.
+static int ws_units(const Params& p) {
+  int n = std::max(p.nunit, p.nseg);
+  const int64_t per_seg = (int64_t)p.B * p.H * p.npslice;
+  const int ng = (int)std::min<int64_t>(p.nc, std::max<int64_t>(1, (kTargetCtas + per_seg - 1) / per_seg));
+  const int Lg = (p.nc + ng - 1) / ng;
+  return std::max(n, (p.nc + Lg - 1) / Lg);
+}
 static size_t workspace_bytes_of(const Params& p) {
-  const size_t st = align16((size_t)p.B * p.H * p.nseg * p.N * p.P * 4);
-  const size_t dec = align16((size_t)p.B * p.H * p.nseg * 4);
-  const size_t gr = align16((size_t)p.B * p.H * p.nseg * 2 * p.R * p.P * 4);
+  const int n = ws_units(p);
+  const size_t st = align16((size_t)p.B * p.H * n * p.N * p.P * 4);
+  const size_t dec = align16((size_t)p.B * p.H * n * 4);
+  const size_t gr = align16((size_t)p.B * p.H * n * 2 * p.R * p.P * 4);
   return st + dec + gr + 256;
 }
 
@@ -872,6 +996,66 @@ static cudaError_t launch_output(const Params& p, size_t smem, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   kern<<<dim3(p.npslice, p.nseg, p.B * p.H), kThreads, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+// Launch with programmatic dependent launch (the kernel waits with
+// griddepcontrol.wait before it reads its predecessor's results).
+template <typename Kern>
+static cudaError_t launch_ex(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                             const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+static bool aligned16(const void* x) { return x == nullptr || (reinterpret_cast<uintptr_t>(x) & 15) == 0; }
+
+template <class K>
+static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) {
+  static int cached_s = 48 * 1024, cached_o = 48 * 1024;
+  const size_t ss = fast_state_smem<K>(p), so = fast_out_smem<K>(p);
+  cudaError_t e = ensure_smem(fast::state_kernel<K>, ss, &cached_s);
+  if (e == cudaSuccess) e = ensure_smem(fast::output_kernel<K>, so, &cached_o);
+  if (e != cudaSuccess) return e;
+  const bool vec = (p.N * p.P) % 4 == 0;
+  const int npe = vec ? (p.N * p.P) / 4 : p.N * p.P;
+  g_failed_stage = 0;
+  stage_event(0, 0, st);
+  e = launch_ex(fast::state_kernel<K>, dim3(p.B * p.H, p.nunit), dim3(K::NT), ss, st, false, p);
+  stage_event(0, 1, st);
+  (*launches)++;
+  if (e != cudaSuccess) return e;
+  g_failed_stage = 1;
+  stage_event(1, 0, st);
+  e = vec ? launch_ex(segment_prefix_vec_kernel<4>, dim3((npe + 127) / 128, p.B * p.H), dim3(128), 0, st,
+                      true, p)
+          : launch_ex(segment_prefix_vec_kernel<1>, dim3((npe + 127) / 128, p.B * p.H), dim3(128), 0, st,
+                      true, p);
+  stage_event(1, 1, st);
+  (*launches)++;
+  if (e != cudaSuccess) return e;
+  g_failed_stage = 2;
+  stage_event(2, 0, st);
+  e = launch_ex(fast::output_kernel<K>, dim3(p.B * p.H, p.nseg), dim3(K::NT), so, st, true, p);
+  stage_event(2, 1, st);
+  (*launches)++;
+  if (e != cudaSuccess) return e;
+  if (p.reduced || p.has_z) {
+    g_failed_stage = 3;
+    stage_event(3, 0, st);
+    e = launch_ex(grad_reduce_kernel, dim3(p.B * p.H), dim3(256), 0, st, true, p);
+    stage_event(3, 1, st);
+    (*launches)++;
+  }
+  return e;
 }
 
 }  // namespace mmbf
@@ -941,15 +1125,49 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
   p.dz = static_cast<uint16_t*>(dz);
   p.qk_dot = static_cast<uint16_t*>(qk_dot);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
+  const int wsn = ws_units(p);
   p.ws_state = reinterpret_cast<float*>(ws);
-  ws += align16((size_t)p.B * p.H * p.nseg * p.N * p.P * 4);
+  ws += align16((size_t)p.B * p.H * wsn * p.N * p.P * 4);
   p.ws_decay = reinterpret_cast<float*>(ws);
-  ws += align16((size_t)p.B * p.H * p.nseg * 4);
+  ws += align16((size_t)p.B * p.H * wsn * 4);
   p.ws_grad = reinterpret_cast<float*>(ws);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int launches = 0;
   cudaError_t e;
+  cudaGetLastError();  // a stale error from elsewhere must not be reported as ours
+  const bool fast_ok = p.fast >= 0 && aligned16(q) && aligned16(k) && aligned16(v) &&
+                       aligned16(dout) && aligned16(z) && aligned16(angles) && aligned16(segsum) &&
+                       aligned16(states) && aligned16(dz);
+  if (fast_ok) {
+    switch (p.fast) {
+      case 0: e = launch_fast<FastA>(p, st, &launches); break;
+      case 1: e = launch_fast<FastB>(p, st, &launches); break;
+      default: e = launch_fast<FastC>(p, st, &launches); break;
+    }
+    if (e == cudaSuccess && g_stage_error != cudaSuccess) {
+      e = g_stage_error;
+      g_stage_error = cudaSuccess;
+    }
+    g_variant = p.fast;
+    if (e != cudaSuccess)
+      return fail(MMBF_ERR_CUDA, "CUDA error in %s (fast %d, grid %d x %d/%d): %s",
+                  g_failed_stage >= 0 ? kStageNames[g_failed_stage] : "setup", p.fast, p.B * p.H,
+                  p.nseg, p.nunit, cudaGetErrorString(e));
+    g_launches = launches;
+    return MMBF_OK;
+  }
+  // Generic kernels (any shape of the envelope).  Their segmentation is the
+  // generic one, one state unit per segment.
+  {
+    const int64_t per_seg = (int64_t)p.B * p.H * p.npslice;
+    const int ng = (int)std::min<int64_t>(p.nc, std::max<int64_t>(1, (kTargetCtas + per_seg - 1) / per_seg));
+    p.L = (p.nc + ng - 1) / ng;
+    p.nseg = (p.nc + p.L - 1) / p.L;
+    p.UA = 1;
+    p.LA = p.L;
+    p.nunit = p.nseg;
+  }
   {
     static int cached = 48 * 1024;
     const size_t smem = state_layout(p).total;
@@ -964,7 +1182,10 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
   }
   if (e == cudaSuccess) {
     stage_event(1, 0, st);
-    segment_prefix_kernel<<<dim3((p.N * p.P + 255) / 256, p.B * p.H), 256, 0, st>>>(p);
+    if ((p.N * p.P) % 4 == 0)
+      segment_prefix_vec_kernel<4><<<dim3((p.N * p.P / 4 + 127) / 128, p.B * p.H), 128, 0, st>>>(p);
+    else
+      segment_prefix_vec_kernel<1><<<dim3((p.N * p.P + 127) / 128, p.B * p.H), 128, 0, st>>>(p);
     e = cudaGetLastError();
     stage_event(1, 1, st);
     launches++;
@@ -992,14 +1213,20 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
     e = g_stage_error;
     g_stage_error = cudaSuccess;
   }
-  if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess)
+    return fail(MMBF_ERR_CUDA,
+                "CUDA error in generic kernel %d (fast=%d, grid %d/%d/%d, smem state %zu out %zu): %s",
+                launches, p.fast, p.npslice, p.nseg, p.B * p.H, state_layout(p).total,
+                out_layout(p).total, cudaGetErrorString(e));
   g_launches = launches;
+  g_variant = -1;
   return MMBF_OK;
 }
 
 const char* mamba_mimo_last_error(void) { return g_err; }
 int mamba_mimo_abi_version(void) { return MAMBA_MIMO_BWD_FWD_ABI_VERSION; }
 int mamba_mimo_last_launch_count(void) { return g_launches; }
+int mamba_mimo_last_kernel_variant(void) { return g_variant; }
 
 void mamba_mimo_set_stage_events(void* const* events, int count) {
   g_stage_events = (events && count > 0) ? events : nullptr;

@@ -121,6 +121,10 @@ def test_shapes(N, P, R, C):
     dict(seqlen=37, chunk_size=5, rank=3, state_dim=12, value_dim=5, div=2),    # odd P, N not /16
     dict(seqlen=50, chunk_size=7, rank=2, state_dim=20, value_dim=33, heads=3, groups=3),
     dict(seqlen=17, chunk_size=16, rank=4, state_dim=8, value_dim=130 - 2),     # two p-slices
+    # shapes of the specialised kernels, with tails and GQA
+    dict(seqlen=200, chunk_size=16, rank=4, state_dim=64, value_dim=64, heads=4, groups=2),
+    dict(seqlen=77, chunk_size=16, rank=8, state_dim=64, value_dim=64, heads=2, groups=1),
+    dict(seqlen=90, chunk_size=16, rank=4, state_dim=32, value_dim=32, heads=3, groups=1),
 ])
 @pytest.mark.parametrize("branches", [(True, True, True), (False, True, False), (True, False, True)])
 def test_edge_shapes(kw, branches):
@@ -143,6 +147,9 @@ def sampled_heads(index, pairs):
     inp = si.make_inputs(**wl.shape_kwargs(), seed=si.WORKLOAD_SEED_BASE + index, device="cuda")
     got = mm.mamba_mimo_bwd_fwd(*si.args_of(inp))
     torch.cuda.synchronize()
+    variant = mm.last_kernel_variant()
+    if index in (2, 4):   # shapes with specialised kernels must use them
+        assert variant >= 0, f"{wl.name} ran the generic kernels"
     for (b, h) in pairs:
         sl = si.head_slice(inp, b, h)
         sl_cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in sl.items()}
@@ -172,22 +179,22 @@ def test_throughput_workload_sampled_heads():
 
 # --- layout, determinism, coverage -------------------------------------------
 
-def test_qk_dot_layout_bit_exact():
-    # q[t,r] = (2^(4r + 16 (t%2) - 40), 0, ...), k[t,s] = (2^s, 0, ...), biases 0:
+@pytest.mark.parametrize("C,R,N,P,S", [(8, 4, 8, 8, 19), (16, 4, 64, 64, 37), (16, 8, 64, 64, 21)])
+def test_qk_dot_layout_bit_exact(C, R, N, P, S):
+    # q[t,r] = (2^(8r + 16 (t%2) - 60), 0, ...), k[t,s] = (2^s, 0, ...), biases 0:
     # every same-token product is a distinct power of two, exact in BF16.
-    inp = unit_inputs(seqlen=19, chunk_size=8, rank=4, state_dim=8, value_dim=8, recipe="workload")
-    S, R = 19, 4
+    inp = unit_inputs(seqlen=S, chunk_size=C, rank=R, state_dim=N, value_dim=P, recipe="workload")
     q = torch.zeros_like(inp["q"])
     k = torch.zeros_like(inp["k"])
     for t in range(S):
         for r in range(R):
-            q[0, t, r, 0, 0] = 2.0 ** (4 * r + 16 * (t % 2) - 40)
+            q[0, t, r, 0, 0] = 2.0 ** (8 * r + 16 * (t % 2) - 60)
             k[0, t, r, 0, 0] = 2.0 ** r
     inp.update(q=q, k=k, q_bias=torch.zeros_like(inp["q_bias"]), k_bias=torch.zeros_like(inp["k_bias"]))
     got = run_gpu(inp).qk_dot.float().cpu()
     want = torch.tensor(oracle.bwd_fwd(*si.args_of(inp))["qk_dot"], dtype=torch.float32)
     assert torch.equal(got, want)
-    assert got[0, 0, 3, 2, 1] == 2.0 ** (4 * 2 + 16 - 40 + 1)
+    assert got[0, 0, 3, 2, 1] == 2.0 ** (8 * 2 + 16 - 60 + 1)
 
 
 def test_deterministic_and_every_output_written():
