@@ -842,6 +842,20 @@ static size_t fast_state_smem(const Params& p) {
   return fast::smem_layout<K>(false, p.reduced, p.has_z).total;
 }
 
+// Largest dynamic shared memory each fast kernel has been opened for.  The
+// limit is only ever raised (a lower request must never shrink it, or a later
+// launch with a larger layout would fail).
+template <class K>
+static int& fast_out_smem_set() {
+  static int v = 48 * 1024;
+  return v;
+}
+template <class K>
+static int& fast_state_smem_set() {
+  static int v = 48 * 1024;
+  return v;
+}
+
 // Resident output-kernel CTAs on the current device (SMs x CTAs per SM), or a
 // GB300-sized default when no device can be queried.
 template <class K>
@@ -853,8 +867,7 @@ static int fast_slots_of(const Params& p) {
     return 2 * 152;
   }
   const size_t smem = fast_out_smem<K>(p);
-  if (cudaFuncSetAttribute(fast::output_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  if (ensure_smem(fast::output_kernel<K>, smem, &fast_out_smem_set<K>()) != cudaSuccess)
     cudaGetLastError();
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fast::output_kernel<K>, K::NT, smem) !=
           cudaSuccess ||
@@ -1020,10 +1033,9 @@ static bool aligned16(const void* x) { return x == nullptr || (reinterpret_cast<
 
 template <class K>
 static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) {
-  static int cached_s = 48 * 1024, cached_o = 48 * 1024;
   const size_t ss = fast_state_smem<K>(p), so = fast_out_smem<K>(p);
-  cudaError_t e = ensure_smem(fast::state_kernel<K>, ss, &cached_s);
-  if (e == cudaSuccess) e = ensure_smem(fast::output_kernel<K>, so, &cached_o);
+  cudaError_t e = ensure_smem(fast::state_kernel<K>, ss, &fast_state_smem_set<K>());
+  if (e == cudaSuccess) e = ensure_smem(fast::output_kernel<K>, so, &fast_out_smem_set<K>());
   if (e != cudaSuccess) return e;
   const bool vec = (p.N * p.P) % 4 == 0;
   const int npe = vec ? (p.N * p.P) / 4 : p.N * p.P;
