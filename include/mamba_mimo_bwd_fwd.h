@@ -123,6 +123,36 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
                                void* states, void* dz, float* dmimo_z, void* qk_dot,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of the built-in scratch area used by
+ * mamba_mimo_bwd_fwd_fixed_scratch (one area per GPU, held until exit). */
+#define MAMBA_MIMO_FIXED_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* The same operation as mamba_mimo_bwd_fwd, for callers that cannot
+ * allocate device memory themselves -- for example code running under a host
+ * framework that owns every device allocation through its own pool, or code
+ * that must not call cudaMalloc because it can synchronise the device -- and
+ * so cannot provide a workspace.  (The pages define no such call; it exists
+ * for these callers.)  Arguments are those of mamba_mimo_bwd_fwd without the
+ * workspace; inputs and outputs are still the caller's device buffers.
+ *
+ * The workspace is a built-in device array of MAMBA_MIMO_FIXED_SCRATCH_BYTES
+ * bytes on each GPU.  A problem whose workspace (the size query above) is
+ * larger is rejected with MMBF_ERR_WORKSPACE and nothing is enqueued.  This
+ * call allocates nothing.  Its first call on a device looks up the array's
+ * device address on the current device (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  Every call on a device shares the
+ * one array and leaves its contents behind; nothing in it needs to start at
+ * zero.  Calls whose kernels overlap on the GPU (different streams without
+ * ordering between them) race on the array and give wrong results: order
+ * them on one stream. */
+mmbf_status mamba_mimo_bwd_fwd_fixed_scratch(
+    const mmbf_dims* dims, const void* dout, const void* q, const void* k, const void* v,
+    const float* q_bias, const float* k_bias, const float* mimo_v, const float* mimo_o,
+    const void* z, const float* mimo_z, const float* angles, const float* da_cs,
+    const float* da_cs_rev, const float* dt, const void* trap, const float* d,
+    const float* segsum, int64_t chunk_size, int64_t rotary_dim_divisor, float* dmimo_o,
+    void* states, void* dz, float* dmimo_z, void* qk_dot, void* stream);
+
 /* Message of the last failed call on the calling thread ("" if none). */
 const char* mamba_mimo_last_error(void);
 

@@ -43,6 +43,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "mamba_mimo_bwd_fwd.h"
 
@@ -1070,6 +1071,32 @@ static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) 
   return e;
 }
 
+// Built-in scratch area of mamba_mimo_bwd_fwd_fixed_scratch: a file-scope
+// device array (every GPU that loads the library holds it until exit).  Host
+// code must not use the name as an address; the device address is looked up
+// once per device with that device current.
+static __device__ __align__(256) unsigned char g_fixed_scratch[MAMBA_MIMO_FIXED_SCRATCH_BYTES];
+static std::mutex g_fixed_scratch_mu;
+static void* g_fixed_scratch_addr[256];
+
+static mmbf_status fixed_scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 256) return fail(MMBF_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_fixed_scratch_mu);
+  if (!g_fixed_scratch_addr[dev]) {
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_fixed_scratch);
+    if (e != cudaSuccess || addr == nullptr)
+      return fail(MMBF_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch area: %s",
+                  cudaGetErrorString(e));
+    g_fixed_scratch_addr[dev] = addr;
+  }
+  *out = g_fixed_scratch_addr[dev];
+  return MMBF_OK;
+}
+
 }  // namespace mmbf
 
 using namespace mmbf;
@@ -1233,6 +1260,32 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
   g_launches = launches;
   g_variant = -1;
   return MMBF_OK;
+}
+
+mmbf_status mamba_mimo_bwd_fwd_fixed_scratch(
+    const mmbf_dims* dims, const void* dout, const void* q, const void* k, const void* v,
+    const float* q_bias, const float* k_bias, const float* mimo_v, const float* mimo_o,
+    const void* z, const float* mimo_z, const float* angles, const float* da_cs,
+    const float* da_cs_rev, const float* dt, const void* trap, const float* d,
+    const float* segsum, int64_t chunk_size, int64_t rotary_dim_divisor, float* dmimo_o,
+    void* states, void* dz, float* dmimo_z, void* qk_dot, void* stream) {
+  g_err[0] = '\0';
+  size_t need = 0;
+  mmbf_status s = mamba_mimo_bwd_fwd_workspace_size(dims, chunk_size, rotary_dim_divisor,
+                                                    mimo_o != nullptr, z != nullptr, &need);
+  if (s != MMBF_OK) return s;
+  if (need > MAMBA_MIMO_FIXED_SCRATCH_BYTES)
+    return fail(MMBF_ERR_WORKSPACE,
+                "this problem needs %zu bytes of workspace; the built-in scratch area holds %zu "
+                "(use mamba_mimo_bwd_fwd with a caller-provided workspace)",
+                need, (size_t)MAMBA_MIMO_FIXED_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  s = fixed_scratch_address(&scratch);
+  if (s != MMBF_OK) return s;
+  return mamba_mimo_bwd_fwd(dims, dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles,
+                            da_cs, da_cs_rev, dt, trap, d, segsum, chunk_size, rotary_dim_divisor,
+                            dmimo_o, states, dz, dmimo_z, qk_dot, scratch,
+                            (size_t)MAMBA_MIMO_FIXED_SCRATCH_BYTES, stream);
 }
 
 const char* mamba_mimo_last_error(void) { return g_err; }
