@@ -20,27 +20,41 @@
 
 namespace fast {
 
-template <int R_, int C_, int N_, int P_, int DIV_>
+template <int R_, int C_, int N_, int P_, int DIV_, int SPLIT_ = 1>
 struct Cfg {
   static constexpr int R = R_, C = C_, N = N_, P = P_, DIV = DIV_;
+  static constexpr int SPLIT = SPLIT_;        // warps per j-block (they split the p-blocks)
   static constexpr int CR = C * R;            // rows per chunk
-  static constexpr int NW = CR / 16;          // warps (one per j-block)
+  static constexpr int NWJ = CR / 16;         // j-blocks
+  static constexpr int NW = NWJ * SPLIT;      // warps
   static constexpr int NT = NW * 32;          // threads
   static constexpr int TPW = 16 / R;          // tokens per j-block
   static constexpr int W = N / DIV;           // rotated pairs
   static constexpr int HALF = N / 2;
   static constexpr int NKT = N / 16;          // 16-wide k tiles over N
   static constexpr int NMT = P / 16;          // 16-row p blocks of X^T / state^T
+  static constexpr int NMTH = NMT / SPLIT;    // p blocks per warp in the output stage
   static constexpr int LDN = N + 8;           // padded smem row strides (elements)
   static constexpr int LDP = P + 8;
   static constexpr int WPM = NW / NMT;        // warps sharing one p-block of the state
   static constexpr int NCW = N / WPM;         // state columns (n) per warp
   static constexpr int NN8 = NCW / 8;         // n8 tiles of the state per warp
   static constexpr int SLOTS = 4;             // X^T columns per thread: (tile nt, bit b)
+  // Tensor memory of the output kernel, per warp: the FP32 state slice and
+  // the dmimo_o / dmimo_z accumulators (16 columns per p-block).  Warps w and
+  // w + 4 share a lane quarter and use different column groups.
+  static constexpr int TM_ST = NN8 * 4;
+  static constexpr int TM_DM = NMTH * 16;
+  static constexpr int TM_WARP = TM_ST + TM_DM;
+  static constexpr int TM_GROUPS = (NW + 3) / 4;
+  static constexpr int TM_NEED = TM_GROUPS * TM_WARP;
+  static constexpr int TM_COLS = TM_NEED <= 32 ? 32 : TM_NEED <= 64 ? 64 : TM_NEED <= 128 ? 128
+                                 : TM_NEED <= 256 ? 256 : 512;
+  static_assert(TM_NEED <= 512 && TM_ST % 8 == 0, "tensor memory budget");
   static_assert(R == 2 || R == 4 || R == 8, "fast path: R in {2,4,8}");
-  static_assert(CR % 16 == 0 && NW >= 1 && NW <= 8, "fast path: C*R in {16..128}, multiple of 16");
+  static_assert(CR % 16 == 0 && NWJ >= 1 && NWJ <= 8, "fast path: C*R in {16..128}, multiple of 16");
   static_assert(N % 32 == 0 && N <= 128 && P % 16 == 0 && P <= 64, "fast path tile sizes");
-  static_assert(NW % NMT == 0 && NCW % 16 == 0, "state split over warps");
+  static_assert(NMT % SPLIT == 0 && NW % NMT == 0 && NCW % 16 == 0, "work split over warps");
   static_assert(W % 8 == 0, "rotated width multiple of 8");
 };
 
@@ -59,6 +73,15 @@ __device__ __forceinline__ int perm(int i) {
 
 // ---------------------------------------------------------------------------
 // Small device helpers
+
+// Element offset of (row, col) in a row-major tile with row stride LD whose
+// 16-byte chunks are XOR-swizzled by row bit 3 (col is a multiple of 8).  With
+// the +8-element padding, any 8 rows that share bit 3 and any set of rows
+// visited through perm() hit 8 different bank groups.
+template <int LD>
+__device__ __forceinline__ int swz(int row, int col) {
+  return row * LD + (col ^ ((row & 8) << 1));
+}
 
 __device__ __forceinline__ void cp16(void* s, const void* g, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(s)), "l"(g),
@@ -124,7 +147,7 @@ struct Stage {  // raw inputs of one chunk
 };
 struct Smem {
   Stage st[2];
-  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, cosT, sinT, tok, scr, dzs, mvb, mzp, mop, qbs, kbs, red;
+  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, cosT, sinT, tok, scr, dzs, mvb, mzp, mop, qbs, kbs, red, tm;
   uint32_t total;
 };
 
@@ -172,8 +195,9 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   L.mop = (need_out && reduced) ? take(K::R * K::NMT * 8 * 4) : 0;
   L.qbs = out_kernel ? take(K::R * K::N * 2) : 0;
   L.kbs = take(K::R * K::N * 2);
+  L.tm = take(16);
   // end-of-segment reduction scratch reuses the stage buffers when they fit
-  const uint32_t red_bytes = need_out ? (uint32_t)K::NT * 2 * K::SLOTS * K::NMT * 2 * 4 : 0;
+  const uint32_t red_bytes = need_out ? (uint32_t)K::NT * 2 * K::SLOTS * K::NMTH * 2 * 4 : 0;
   L.red = (red_bytes <= L.st[0].bytes + L.st[1].bytes) ? 0 : take(red_bytes);
   L.total = o;
   return L;
@@ -196,8 +220,8 @@ __device__ void load_stage(const Params& p, const Stage& S, unsigned char* sm, i
     const int t = j / K::R, r = j % K::R, tg = t0 + t;
     const bool ok = tg < p.S;
     const int64_t off = ((((int64_t)b * p.S + (ok ? tg : 0)) * K::R + r) * p.G + g) * K::N + gr * 8;
-    if (out_kernel) cp16(sm + S.q + (j * K::LDN + gr * 8) * 2, p.q + off, ok);
-    cp16(sm + S.k + (j * K::LDN + gr * 8) * 2, p.k + off, ok);
+    if (out_kernel) cp16(sm + S.q + swz<K::LDN>(j, gr * 8) * 2, p.q + off, ok);
+    cp16(sm + S.k + swz<K::LDN>(j, gr * 8) * 2, p.k + off, ok);
   }
   for (int e = threadIdx.x; e < K::C * GP; e += K::NT) {
     const int t = e / GP, gr = e % GP, tg = t0 + t;
@@ -307,16 +331,18 @@ __device__ void sincos_table(const float* ang, float* cosT, float* sinT) {
 template <class K>
 __device__ __forceinline__ void load_rows(uint32_t (&f)[K::NKT][4], const uint16_t* tile, int j0) {
   const int lane = threadIdx.x & 31;
-  const uint16_t* row = tile + (j0 + perm<K::R>(lane & 15)) * K::LDN + (lane >> 4) * 8;
+  const int r = j0 + perm<K::R>(lane & 15);
 #pragma unroll
-  for (int kt = 0; kt < K::NKT; kt++) ldsm_x4(f[kt][0], f[kt][1], f[kt][2], f[kt][3], row + kt * 16);
+  for (int kt = 0; kt < K::NKT; kt++)
+    ldsm_x4(f[kt][0], f[kt][1], f[kt][2], f[kt][3], tile + swz<K::LDN>(r, kt * 16 + (lane >> 4) * 8));
 }
 template <class K>
 __device__ __forceinline__ void store_rows(const uint32_t (&f)[K::NKT][4], uint16_t* tile, int j0) {
   const int lane = threadIdx.x & 31;
-  uint16_t* row = tile + (j0 + perm<K::R>(lane & 15)) * K::LDN + (lane >> 4) * 8;
+  const int r = j0 + perm<K::R>(lane & 15);
 #pragma unroll
-  for (int kt = 0; kt < K::NKT; kt++) stsm_x4(row + kt * 16, f[kt][0], f[kt][1], f[kt][2], f[kt][3]);
+  for (int kt = 0; kt < K::NKT; kt++)
+    stsm_x4(tile + swz<K::LDN>(r, kt * 16 + (lane >> 4) * 8), f[kt][0], f[kt][1], f[kt][2], f[kt][3]);
 }
 
 // Fragment register (kt, e) holds row i = g + 8 (e & 1), columns
@@ -390,13 +416,13 @@ __device__ __forceinline__ void k_state(uint32_t (&f)[K::NKT][4], const float* e
 }
 
 // PsiV rows of this warp's j-block (natural order): bf16(v[t] * bf16(mimo_v[r])).
-template <class K>
+template <class K, int ROWS = 16>
 __device__ __forceinline__ void psi_rows(const uint16_t* vraw, const uint16_t* mvb, uint16_t* Psi,
                                          int j0) {
   constexpr int GP = K::P / 8;
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int it = 0; it < GP / 2; it++) {
+  for (int it = 0; it < ROWS * GP / 32; it++) {
     const int q = lane + 32 * it, i = q / GP, gr = q % GP;
     const int j = j0 + i, tl = j / K::R, r = j % K::R;
     const uint4 v = *reinterpret_cast<const uint4*>(vraw + tl * K::LDP + gr * 8);
@@ -406,7 +432,7 @@ __device__ __forceinline__ void psi_rows(const uint16_t* vraw, const uint16_t* m
     o.y = bmul2(v.y, m.y);
     o.z = bmul2(v.z, m.z);
     o.w = bmul2(v.w, m.w);
-    *reinterpret_cast<uint4*>(Psi + j * K::LDP + gr * 8) = o;
+    *reinterpret_cast<uint4*>(Psi + swz<K::LDP>(j, gr * 8)) = o;
   }
 }
 
@@ -424,14 +450,14 @@ __device__ __forceinline__ void state_mma(float (&st)[K::NN8][4], const uint16_t
     st[nn][0] = x.x; st[nn][1] = x.y; st[nn][2] = y.x; st[nn][3] = y.y;
   }
 #pragma unroll
-  for (int kb = 0; kb < K::NW; kb++) {
+  for (int kb = 0; kb < K::NWJ; kb++) {
     uint32_t a0, a1, a2_, a3;
-    ldsm_x4_t(a0, a1, a2_, a3, Psi + (kb * 16 + (mi >> 1) * 8 + li) * K::LDP + pm * 16 + (mi & 1) * 8);
+    ldsm_x4_t(a0, a1, a2_, a3, Psi + swz<K::LDP>(kb * 16 + (mi >> 1) * 8 + li, pm * 16 + (mi & 1) * 8));
 #pragma unroll
     for (int nn = 0; nn < K::NN8 / 2; nn++) {
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(b0, b1, b2, b3,
-                Kst + (kb * 16 + (mi & 1) * 8 + li) * K::LDN + nbase + nn * 16 + (mi >> 1) * 8);
+                Kst + swz<K::LDN>(kb * 16 + (mi & 1) * 8 + li, nbase + nn * 16 + (mi >> 1) * 8));
       mma16816(st[2 * nn], a0, a1, a2_, a3, b0, b1);
       mma16816(st[2 * nn + 1], a0, a1, a2_, a3, b2, b3);
     }
@@ -446,6 +472,60 @@ __device__ void param_tables(const Params& p, int h, uint16_t* mvb, uint16_t* qb
     if (qbs) qbs[e] = f_bf(p.q_bias[(int64_t)h * K::R * K::N + e]);
     kbs[e] = f_bf(p.k_bias[(int64_t)h * K::R * K::N + e]);
   }
+}
+
+// ---- tensor memory (tcgen05) helpers: 32x32b accesses, 8 columns each.
+// Each thread reaches its own lane; the wait is fused with the load and
+// carries the registers, so no use can be scheduled before it.
+__device__ __forceinline__ void tm_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r0, r1, r2, r3, r4, r5, r6, r7;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5), "=r"(r6), "=r"(r7)
+               : "r"(taddr)
+               : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(r0), "+r"(r1), "+r"(r2), "+r"(r3), "+r"(r4), "+r"(r5), "+r"(r6), "+r"(r7)
+               :
+               : "memory");
+  v[0] = __uint_as_float(r0); v[1] = __uint_as_float(r1); v[2] = __uint_as_float(r2);
+  v[3] = __uint_as_float(r3); v[4] = __uint_as_float(r4); v[5] = __uint_as_float(r5);
+  v[6] = __uint_as_float(r6); v[7] = __uint_as_float(r7);
+}
+__device__ __forceinline__ void tm_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
+}
+__device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tm_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tm_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// State slice st[NN8][4] <-> its TMEM columns (col0 = first column).
+template <class K>
+__device__ __forceinline__ void tm_load_state(uint32_t taddr, float (&st)[K::NN8][4]) {
+#pragma unroll
+  for (int q = 0; q < K::TM_ST / 8; q++) {
+    float v[8];
+    tm_ld8(taddr + q * 8, v);
+#pragma unroll
+    for (int i = 0; i < 8; i++) st[(q * 8 + i) / 4][(q * 8 + i) % 4] = v[i];
+  }
+}
+template <class K>
+__device__ __forceinline__ void tm_store_state(uint32_t taddr, const float (&st)[K::NN8][4]) {
+#pragma unroll
+  for (int q = 0; q < K::TM_ST / 8; q++) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = st[(q * 8 + i) / 4][(q * 8 + i) % 4];
+    tm_st8(taddr + q * 8, v);
+  }
+  tm_wait_st();
 }
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
@@ -582,18 +662,25 @@ namespace fast {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Per-chunk outputs and gradients (fast path of chunk_output_kernel).
-template <class K>
-__global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
-  constexpr int R = K::R, C = K::C, N = K::N, P = K::P, NMT = K::NMT, LDN = K::LDN, LDP = K::LDP;
+// MODE >= 0 fixes the branches at compile time (bit 0: reduced dout, bit 1: z,
+// bit 2: d); MODE = -1 reads them from Params.
+template <class K, int MODE>
+__global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(Params p) {
+  const bool RED = MODE >= 0 ? (MODE & 1) != 0 : p.reduced != 0;
+  const bool HZ = MODE >= 0 ? (MODE & 2) != 0 : p.has_z != 0;
+  const bool HD = MODE >= 0 ? (MODE & 4) != 0 : p.has_d != 0;
+  constexpr int R = K::R, C = K::C, N = K::N, P = K::P, NMT = K::NMT, NMTH = K::NMTH, LDN = K::LDN,
+                LDP = K::LDP;
   extern __shared__ __align__(128) unsigned char sm[];
-  const bool need_out = p.reduced || p.has_z;
-  const Smem L = smem_layout<K>(true, p.reduced, p.has_z);
+  const bool need_out = RED || HZ;
+  const Smem L = smem_layout<K>(true, RED, HZ);
   const int bh = blockIdx.x, seg = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H;
   const int c0 = seg * p.L, c1 = min(p.nc, c0 + p.L);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, cq = lane & 3, mi = lane >> 3, li = lane & 7;
-  const int j0 = warp * 16;
+  const int jw = warp % K::NWJ, half = warp / K::NWJ;  // j-block, p-block group
+  const int j0 = jw * 16, mt0 = half * NMTH;
   const int pm = warp % NMT, nbase = (warp / NMT) * K::NCW;
   uint16_t* Ks = reinterpret_cast<uint16_t*>(sm + L.Ks);
   uint16_t* Kst = reinterpret_cast<uint16_t*>(sm + L.Kst);
@@ -617,41 +704,56 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
 
   // ---- once per CTA: parameters of head h, first chunk's inputs in flight
   param_tables<K>(p, h, mvb, qbs, kbs);
-  if (need_out && p.has_z)
+  if (need_out && HZ)
     for (int e = threadIdx.x; e < R * NMT * 8; e += K::NT) {
       const int o = e / (NMT * 8), mt = (e / 8) % NMT, gg = e % 8;
       const float* mz = p.mimo_z + ((int64_t)h * R + o) * P + mt * 16 + gg;
       mzp[e] = make_float2(mz[0], mz[8]);
     }
-  if (need_out && p.reduced)
+  if (need_out && RED)
     for (int e = threadIdx.x; e < R * NMT * 8; e += K::NT) {
       const int o = e / (NMT * 8), mt = (e / 8) % NMT, gg = e % 8;
       const float* mo = p.mimo_o + ((int64_t)h * R + o) * P + mt * 16 + gg;
       mop[e] = (uint32_t)f_bf(mo[0]) | ((uint32_t)f_bf(mo[8]) << 16);
     }
-  const float dval = p.has_d ? p.d[h] : 0.f;
+  const float dval = HD ? p.d[h] : 0.f;
+  // Tensor memory: warp 0 allocates the CTA's columns; each warp uses its lane
+  // quarter (warp % 4) and column group (warp / 4).
+  uint32_t* tm_slot = reinterpret_cast<uint32_t*>(sm + L.tm);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     smem_u32(tm_slot)),
+                 "r"((uint32_t)K::TM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  tm_fence_before();
+  __syncthreads();
+  tm_fence_after();
+  const uint32_t tm_alloc = *tm_slot;
+  const uint32_t tm_st = tm_alloc + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * K::TM_WARP);
+  const uint32_t tm_dm = tm_st + K::TM_ST;
   load_stage<K>(p, L.st[0], sm, bh, c0, true, need_out);
   cp_commit();
   float4 scal = load_scalars<K>(p, bh, c0);
 
   // ---- entering state of the segment (written by the prefix kernel)
   pdl_wait();
-  float st[K::NN8][4];
   {
+    float st[K::NN8][4];
     const float* src = p.ws_state + ((int64_t)bh * p.nunit + (int64_t)seg * p.UA) * N * P;
 #pragma unroll
     for (int nn = 0; nn < K::NN8; nn++)
 #pragma unroll
       for (int e = 0; e < 4; e++)
         st[nn][e] = src[(nbase + nn * 8 + 2 * cq + (e & 1)) * P + pm * 16 + g + 8 * (e >> 1)];
+    tm_store_state<K>(tm_st, st);
+    const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < K::TM_DM / 8; q++) tm_st8(tm_dm + q * 8, zero8);
+    tm_wait_st();
   }
   pdl_trigger();
-
-  float2 dmo[4][NMT], dmz[4][NMT];
-#pragma unroll
-  for (int sl = 0; sl < 4; sl++)
-#pragma unroll
-    for (int mt = 0; mt < NMT; mt++) dmo[sl][mt] = dmz[sl][mt] = make_float2(0.f, 0.f);
 
   for (int c = c0; c < c1; c++) {
     const int s = (c - c0) & 1;
@@ -680,6 +782,7 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
       load_rows<K>(kf, reinterpret_cast<const uint16_t*>(sm + S.k), j0);
       add_bias<K>(qf, qbs);
       add_bias<K>(kf, kbs);
+      if (half == 0) {
       float qa[2][4];
 #pragma unroll
       for (int ht = 0; ht < 2; ht++) qa[ht][0] = qa[ht][1] = qa[ht][2] = qa[ht][3] = 0.f;
@@ -704,13 +807,21 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
                   (uint32_t)f_bf(v0) | ((uint32_t)f_bf(v1) << 16);
           }
         }
+      }
       rotate<K, true>(qf, kf, cosT, sinT, j0);
       scale_k<K>(kf, facd, j0);
-      store_rows<K>(kf, Ks, j0);
-      k_state<K>(kf, edr, j0);
-      store_rows<K>(kf, Kst, j0);
+      if (half == 0) {
+        store_rows<K>(kf, Ks, j0);
+      }
+      if (half == K::SPLIT - 1) {
+        k_state<K>(kf, edr, j0);
+        store_rows<K>(kf, Kst, j0);
+      }
     }
-    psi_rows<K>(reinterpret_cast<const uint16_t*>(sm + S.v), mvb, Psi, j0);
+    psi_rows<K, 16 / K::SPLIT>(reinterpret_cast<const uint16_t*>(sm + S.v), mvb, Psi,
+                               j0 + half * (16 / K::SPLIT));
+    float st[K::NN8][4];
+    tm_load_state<K>(tm_st, st);
 #pragma unroll
     for (int nn = 0; nn < K::NN8 / 2; nn++) {
       const uint32_t r0 = pack2(make_float2(st[2 * nn][0], st[2 * nn][1]));
@@ -730,17 +841,18 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
       }
     }
 
-    float X[NMT][2][4];
+    float X[NMTH][2][4];
     if (need_out) {
       // inter^T = bf16(state)^T q_rot^T, then * exp(da_cs[t]) per column
 #pragma unroll
-      for (int mt = 0; mt < NMT; mt++) {
+      for (int mt = 0; mt < NMTH; mt++) {
 #pragma unroll
         for (int nt = 0; nt < 2; nt++) X[mt][nt][0] = X[mt][nt][1] = X[mt][nt][2] = X[mt][nt][3] = 0.f;
 #pragma unroll
         for (int kt = 0; kt < K::NKT; kt++) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(a0, a1, a2, a3, Sb + (kt * 16 + (mi >> 1) * 8 + li) * LDP + mt * 16 + (mi & 1) * 8);
+          ldsm_x4_t(a0, a1, a2, a3,
+                    Sb + (kt * 16 + (mi >> 1) * 8 + li) * LDP + (mt0 + mt) * 16 + (mi & 1) * 8);
           mma16816(X[mt][0], a0, a1, a2, a3, qf[kt][0], qf[kt][2]);
           mma16816(X[mt][1], a0, a1, a2, a3, qf[kt][1], qf[kt][3]);
         }
@@ -750,7 +862,7 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
         const float ed = eda[(j0 + perm<R>(nt * 8 + 2 * cq)) / R];
         const float2 e2 = make_float2(ed, ed);
 #pragma unroll
-        for (int mt = 0; mt < NMT; mt++) {
+        for (int mt = 0; mt < NMTH; mt++) {
           const float2 x = __fmul2_rn(make_float2(X[mt][nt][0], X[mt][nt][1]), e2);
           const float2 y = __fmul2_rn(make_float2(X[mt][nt][2], X[mt][nt][3]), e2);
           X[mt][nt][0] = x.x; X[mt][nt][1] = x.y; X[mt][nt][2] = y.x; X[mt][nt][3] = y.y;
@@ -759,16 +871,16 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
       // causal blocks jb <= this warp's block: A = bf16(mask(Q Ks^T) exp(segsum)),
       // intra^T += PsiV^T A^T
 #pragma unroll
-      for (int jb = 0; jb < K::NW; jb++) {
-        if (jb > warp) continue;
+      for (int jb = 0; jb < K::NWJ; jb++) {
+        if (jb > jw) continue;
         float sa[2][4];
 #pragma unroll
         for (int ht = 0; ht < 2; ht++) sa[ht][0] = sa[ht][1] = sa[ht][2] = sa[ht][3] = 0.f;
-        const uint16_t* krow = Ks + (jb * 16 + perm<R>((mi >> 1) * 8 + li)) * LDN + (mi & 1) * 8;
+        const int krow = jb * 16 + perm<R>((mi >> 1) * 8 + li);
 #pragma unroll
         for (int kt = 0; kt < K::NKT; kt++) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(b0, b1, b2, b3, krow + kt * 16);
+          ldsm_x4(b0, b1, b2, b3, Ks + swz<LDN>(krow, kt * 16 + (mi & 1) * 8));
           mma16816(sa[0], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], b0, b1);
           mma16816(sa[1], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], b2, b3);
         }
@@ -786,18 +898,20 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
             bi[hh][ht] = pack2(make_float2(v0, v1));
           }
         }
-        const uint16_t* prow = Psi + (jb * 16 + perm<R>((mi >> 1) * 8 + li)) * LDP + (mi & 1) * 8;
+        const int prow = jb * 16 + perm<R>((mi >> 1) * 8 + li);
 #pragma unroll
-        for (int mt = 0; mt < NMT; mt++) {
+        for (int mt = 0; mt < NMTH; mt++) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(a0, a1, a2, a3, prow + mt * 16);
+          ldsm_x4_t(a0, a1, a2, a3, Psi + swz<LDP>(prow, (mt0 + mt) * 16 + (mi & 1) * 8));
           mma16816(X[mt][0], a0, a1, a2, a3, bi[0][0], bi[0][1]);
           mma16816(X[mt][1], a0, a1, a2, a3, bi[1][0], bi[1][1]);
         }
       }
     }
     // state update: state^T = exp(da_cs[last]) state^T + PsiV^T k_state
+    tm_load_state<K>(tm_st, st);
     state_mma<K>(st, Psi, Kst, tok[4 * C], pm, nbase);
+    tm_store_state<K>(tm_st, st);
 
     // ---- per-element epilogue on X^T (p-row pairs (p, p+8), four columns
     //      per thread).  Column slot (nt, bb) is row j0 + perm(nt*8 + 2c + bb).
@@ -826,10 +940,10 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
 #pragma unroll
           for (int r = 0; r < R; r++) qrow[k][r] = qkd[(tl * R + oo[k]) * R + r];
 #pragma unroll
-        for (int mt = 0; mt < NMT; mt++) {
+        for (int mtl = 0; mtl < NMTH; mtl++) {
+          const int mt = mt0 + mtl;
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(a0, a1, a2, a3,
-                    Psi + (j0 + perm<R>((mi >> 1) * 8 + li)) * LDP + mt * 16 + (mi & 1) * 8);
+          ldsm_x4_t(a0, a1, a2, a3, Psi + swz<LDP>(j0 + perm<R>((mi >> 1) * 8 + li), mt * 16 + (mi & 1) * 8));
           uint32_t pso[NS];
 #pragma unroll
           for (int k = 0; k < NS; k++) {
@@ -851,16 +965,19 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
           }
           float2 z2 = make_float2(0.f, 0.f), do2 = make_float2(0.f, 0.f);
           uint32_t dob = 0;
-          if (p.has_z) {
+          if (HZ) {
             const uint16_t* zr = zraw + tl * LDP + mt * 16 + g;
             z2 = unpack2((uint32_t)zr[0] | ((uint32_t)zr[8] << 16));
           }
-          if (p.reduced) {
+          if (RED) {
             const uint16_t* dr = draw + tl * LDP + mt * 16 + g;
             dob = (uint32_t)dr[0] | ((uint32_t)dr[8] << 16);
             do2 = unpack2(dob);
           }
           float2 prodz[NS];
+          float2 cdmo[4], cdmz[4];
+#pragma unroll
+          for (int sl = 0; sl < 4; sl++) cdmo[sl] = cdmz[sl] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < NS; k++) {
             const int o = oo[k], nt = nto[k], bb = bbo[k], sl = slo[k];
@@ -870,12 +987,12 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
             for (int r = 0; r < R; r++) dacc = badd2(dacc, bmul2(qrow[k][r], psiP[r]));
             const float2 dg = unpack2(pack2(__fmul2_rn(unpack2(dacc), gam2)));
             // out = bf16(inter + intra + diag + d * PsiV)
-            float2 x = __fadd2_rn(make_float2(X[mt][nt][bb], X[mt][nt][bb + 2]), dg);
-            if (p.has_d) x = __fadd2_rn(x, __fmul2_rn(make_float2(dval, dval), unpack2(pso[k])));
+            float2 x = __fadd2_rn(make_float2(X[mtl][nt][bb], X[mtl][nt][bb + 2]), dg);
+            if (HD) x = __fadd2_rn(x, __fmul2_rn(make_float2(dval, dval), unpack2(pso[k])));
             const uint32_t ob = pack2(x);
             const float2 of = unpack2(ob);
             float2 pz = make_float2(0.f, 0.f), sg = make_float2(0.5f, 0.5f), mz = make_float2(0.f, 0.f);
-            if (p.has_z) {
+            if (HZ) {
               mz = mzp[(o * NMT + mt) * 8 + g];
               pz = __fmul2_rn(z2, mz);
               const float2 tq = __fmul2_rn(pz, make_float2(-kLog2e, -kLog2e));
@@ -884,28 +1001,46 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
               sg = make_float2(rcp_approx(den.x), rcp_approx(den.y));
             }
             uint32_t preb = 0u;
-            if (p.reduced) {
-              if (p.has_z) {
-                dmo[sl][mt] = __ffma2_rn(__fmul2_rn(of, __fmul2_rn(pz, sg)), do2, dmo[sl][mt]);
+            if (RED) {
+              if (HZ) {
+                cdmo[sl] = __ffma2_rn(__fmul2_rn(of, __fmul2_rn(pz, sg)), do2, cdmo[sl]);
                 preb = bmul2(bmul2(dob, mop[(o * NMT + mt) * 8 + g]), ob);
               } else {
-                dmo[sl][mt] = __ffma2_rn(of, do2, dmo[sl][mt]);
+                cdmo[sl] = __ffma2_rn(of, do2, cdmo[sl]);
               }
-            } else if (p.has_z) {
+            } else if (HZ) {
               const uint16_t* dr = draw + (tl * R + o) * LDP + mt * 16 + g;
               preb = bmul2((uint32_t)dr[0] | ((uint32_t)dr[8] << 16), ob);
             }
             prodz[k] = make_float2(0.f, 0.f);
-            if (p.has_z) {
+            if (HZ) {
               const float2 pre = unpack2(preb);
               const float2 om = __fadd2_rn(make_float2(1.f, 1.f), make_float2(-sg.x, -sg.y));
               const float2 gg = __ffma2_rn(pz, om, make_float2(1.f, 1.f));
               const float2 gz = __fmul2_rn(__fmul2_rn(pre, sg), gg);
-              dmz[sl][mt] = __ffma2_rn(gz, z2, dmz[sl][mt]);
+              cdmz[sl] = __ffma2_rn(gz, z2, cdmz[sl]);
               prodz[k] = __fmul2_rn(gz, mz);
             }
           }
-          if (p.has_z) {  // dz: BF16 running sum over the ranks in order
+          {  // this p-block's dmimo partials accumulate in tensor memory
+            float v[8];
+            tm_ld8(tm_dm + mtl * 16, v);
+#pragma unroll
+            for (int sl = 0; sl < 4; sl++) {
+              v[2 * sl] += cdmo[sl].x;
+              v[2 * sl + 1] += cdmo[sl].y;
+            }
+            tm_st8(tm_dm + mtl * 16, v);
+            tm_ld8(tm_dm + mtl * 16 + 8, v);
+#pragma unroll
+            for (int sl = 0; sl < 4; sl++) {
+              v[2 * sl] += cdmz[sl].x;
+              v[2 * sl + 1] += cdmz[sl].y;
+            }
+            tm_st8(tm_dm + mtl * 16 + 8, v);
+            tm_wait_st();
+          }
+          if (HZ) {  // dz: BF16 running sum over the ranks in order
             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < NS; k++) acc = unpack2(pack2(__fadd2_rn(acc, prodz[k])));
@@ -926,7 +1061,7 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
       }
     }
     __syncthreads();  // (4)
-    if (need_out && p.has_z) {
+    if (need_out && HZ) {
       constexpr int GP = P / 8;
       for (int e = threadIdx.x; e < C * GP; e += K::NT) {
         const int t = e / GP, gr = e % GP, tg = c * C + t;
@@ -938,33 +1073,53 @@ __global__ void __launch_bounds__(K::NT) output_kernel(Params p) {
   }  // chunk loop
 
   // ---- end of segment: fixed-order sum of the dmimo_o / dmimo_z partials
+  float2 dmo[4][NMTH], dmz[4][NMTH];
+  if (need_out) {
+#pragma unroll
+    for (int mt = 0; mt < NMTH; mt++) {
+      float v[8];
+      tm_ld8(tm_dm + mt * 16, v);
+#pragma unroll
+      for (int sl = 0; sl < 4; sl++) dmo[sl][mt] = make_float2(v[2 * sl], v[2 * sl + 1]);
+      tm_ld8(tm_dm + mt * 16 + 8, v);
+#pragma unroll
+      for (int sl = 0; sl < 4; sl++) dmz[sl][mt] = make_float2(v[2 * sl], v[2 * sl + 1]);
+    }
+  }
+  tm_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tm_alloc),
+                 "r"((uint32_t)K::TM_COLS)
+                 : "memory");
   if (need_out) {
     cp_wait<0>();
     __syncthreads();
-    constexpr int PER = 2 * 4 * NMT * 2;
+    constexpr int PER = 2 * 4 * NMTH * 2;
     float* red = reinterpret_cast<float*>(sm + L.red);
     float* mine = red + threadIdx.x * PER;
 #pragma unroll
     for (int sl = 0; sl < 4; sl++)
 #pragma unroll
-      for (int mt = 0; mt < NMT; mt++) {
-        mine[((0 * 4 + sl) * NMT + mt) * 2 + 0] = dmo[sl][mt].x;
-        mine[((0 * 4 + sl) * NMT + mt) * 2 + 1] = dmo[sl][mt].y;
-        mine[((1 * 4 + sl) * NMT + mt) * 2 + 0] = dmz[sl][mt].x;
-        mine[((1 * 4 + sl) * NMT + mt) * 2 + 1] = dmz[sl][mt].y;
+      for (int mt = 0; mt < NMTH; mt++) {
+        mine[((0 * 4 + sl) * NMTH + mt) * 2 + 0] = dmo[sl][mt].x;
+        mine[((0 * 4 + sl) * NMTH + mt) * 2 + 1] = dmo[sl][mt].y;
+        mine[((1 * 4 + sl) * NMTH + mt) * 2 + 0] = dmz[sl][mt].x;
+        mine[((1 * 4 + sl) * NMTH + mt) * 2 + 1] = dmz[sl][mt].y;
       }
     __syncthreads();
     float* dst = p.ws_grad + ((int64_t)bh * p.nseg + seg) * 2 * R * P;
     for (int e = threadIdx.x; e < 2 * R * P; e += K::NT) {
       const int which = e / (R * P), r = (e / P) % R, pp = e % P;
       const int mt = pp / 16, gg = pp % 8, hh = (pp % 16) / 8;
+      const int hf = mt / NMTH, mtl = mt % NMTH;
       float sum = 0.f;
-      for (int w = 0; w < K::NW; w++)
+      for (int w = hf * K::NWJ; w < (hf + 1) * K::NWJ; w++)
         for (int cc = 0; cc < 4; cc++)
 #pragma unroll
           for (int sl = 0; sl < 4; sl++)
             if (perm<R>((sl >> 1) * 8 + 2 * cc + (sl & 1)) % R == r)
-              sum += red[(w * 32 + gg * 4 + cc) * PER + ((which * 4 + sl) * NMT + mt) * 2 + hh];
+              sum += red[(w * 32 + gg * 4 + cc) * PER + ((which * 4 + sl) * NMTH + mtl) * 2 + hh];
       dst[e] = sum;
     }
   }

@@ -819,9 +819,9 @@ static size_t out_smem_bytes(Params p, int PS) {
 static const size_t kSmemLimit = 227 * 1024;
 
 // ---- shape-specialised kernels: instantiated shapes and launch plan
-using FastA = fast::Cfg<4, 16, 64, 64, 4>;  // R4 C16 N=P=64 (the pages' timed and unit-test shape)
-using FastB = fast::Cfg<8, 16, 64, 64, 4>;  // R8 C16 N=P=64
-using FastC = fast::Cfg<4, 16, 32, 32, 4>;  // R4 C16 N=P=32
+using FastA = fast::Cfg<4, 16, 64, 64, 4, 1>;  // R4 C16 N=P=64 (the pages' timed and unit-test shape)
+using FastB = fast::Cfg<8, 16, 64, 64, 4, 2>;  // R8 C16 N=P=64
+using FastC = fast::Cfg<4, 16, 32, 32, 4, 1>;  // R4 C16 N=P=32
 constexpr int kNumFast = 3;
 
 template <class K>
@@ -838,15 +838,18 @@ template <class K>
 static size_t fast_out_smem(const Params& p) {
   return fast::smem_layout<K>(true, p.reduced, p.has_z).total;
 }
+// The state-sum kernel always runs one warp per j-block.
+template <class K>
+using StateCfg = fast::Cfg<K::R, K::C, K::N, K::P, K::DIV, 1>;
 template <class K>
 static size_t fast_state_smem(const Params& p) {
-  return fast::smem_layout<K>(false, p.reduced, p.has_z).total;
+  return fast::smem_layout<StateCfg<K>>(false, p.reduced, p.has_z).total;
 }
 
 // Largest dynamic shared memory each fast kernel has been opened for.  The
 // limit is only ever raised (a lower request must never shrink it, or a later
 // launch with a larger layout would fail).
-template <class K>
+template <class K, int MODE = -1>
 static int& fast_out_smem_set() {
   static int v = 48 * 1024;
   return v;
@@ -868,9 +871,9 @@ static int fast_slots_of(const Params& p) {
     return 2 * 152;
   }
   const size_t smem = fast_out_smem<K>(p);
-  if (ensure_smem(fast::output_kernel<K>, smem, &fast_out_smem_set<K>()) != cudaSuccess)
+  if (ensure_smem(fast::output_kernel<K, -1>, smem, &fast_out_smem_set<K>()) != cudaSuccess)
     cudaGetLastError();
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fast::output_kernel<K>, K::NT, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fast::output_kernel<K, -1>, K::NT, smem) !=
           cudaSuccess ||
       per_sm < 1) {
     cudaGetLastError();
@@ -1035,14 +1038,20 @@ static bool aligned16(const void* x) { return x == nullptr || (reinterpret_cast<
 template <class K>
 static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) {
   const size_t ss = fast_state_smem<K>(p), so = fast_out_smem<K>(p);
-  cudaError_t e = ensure_smem(fast::state_kernel<K>, ss, &fast_state_smem_set<K>());
-  if (e == cudaSuccess) e = ensure_smem(fast::output_kernel<K>, so, &fast_out_smem_set<K>());
+  // All branches on (the benchmarked combination) has its own instantiation
+  // with the branches resolved at compile time.
+  const bool all_on = p.reduced && p.has_z && p.has_d;
+  cudaError_t e = ensure_smem(fast::state_kernel<StateCfg<K>>, ss, &fast_state_smem_set<K>());
+  if (e == cudaSuccess)
+    e = all_on ? ensure_smem(fast::output_kernel<K, 7>, so, &fast_out_smem_set<K, 7>())
+               : ensure_smem(fast::output_kernel<K, -1>, so, &fast_out_smem_set<K, -1>());
   if (e != cudaSuccess) return e;
   const bool vec = (p.N * p.P) % 4 == 0;
   const int npe = vec ? (p.N * p.P) / 4 : p.N * p.P;
   g_failed_stage = 0;
   stage_event(0, 0, st);
-  e = launch_ex(fast::state_kernel<K>, dim3(p.B * p.H, p.nunit), dim3(K::NT), ss, st, false, p);
+  e = launch_ex(fast::state_kernel<StateCfg<K>>, dim3(p.B * p.H, p.nunit), dim3(StateCfg<K>::NT), ss,
+                st, false, p);
   stage_event(0, 1, st);
   (*launches)++;
   if (e != cudaSuccess) return e;
@@ -1057,7 +1066,8 @@ static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) 
   if (e != cudaSuccess) return e;
   g_failed_stage = 2;
   stage_event(2, 0, st);
-  e = launch_ex(fast::output_kernel<K>, dim3(p.B * p.H, p.nseg), dim3(K::NT), so, st, true, p);
+  e = all_on ? launch_ex(fast::output_kernel<K, 7>, dim3(p.B * p.H, p.nseg), dim3(K::NT), so, st, true, p)
+             : launch_ex(fast::output_kernel<K, -1>, dim3(p.B * p.H, p.nseg), dim3(K::NT), so, st, true, p);
   stage_event(2, 1, st);
   (*launches)++;
   if (e != cudaSuccess) return e;
