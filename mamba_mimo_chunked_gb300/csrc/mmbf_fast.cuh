@@ -147,7 +147,7 @@ struct Stage {  // raw inputs of one chunk
 };
 struct Smem {
   Stage st[2];
-  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, cosT, sinT, tok, scr, dzs, mvb, mzp, mop, qbs, kbs, red, tm;
+  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, cosT, sinT, tok, dzs, mvb, mzp, mop, qbs, kbs, red, tm;
   uint32_t total;
 };
 
@@ -187,8 +187,7 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   L.eseg = need_out ? take(K::C * K::C * 4) : 0;
   L.cosT = take(K::C * K::W * 4);
   L.sinT = take(K::C * K::W * 4);
-  L.tok = take(K::C * 4 * 4 + 16);
-  L.scr = take(4 * (K::C + 1) * 4);
+  L.tok = take(2 * (K::C * 4 * 4 + 16));
   L.dzs = (need_out && has_z) ? take(K::C * K::LDP * 2) : 0;
   L.mvb = take(K::R * K::P * 2);
   L.mzp = (need_out && has_z) ? take(K::R * K::NMT * 8 * 8) : 0;
@@ -269,43 +268,6 @@ __device__ __forceinline__ float4 load_scalars(const Params& p, int bh, int c) {
   }
   return r;
 }
-template <class K>
-__device__ __forceinline__ void store_scalars(float* scr, float4 v) {
-  const int t = threadIdx.x;
-  if (t <= K::C) {
-    scr[t] = v.x;
-    scr[(K::C + 1) + t] = v.y;
-    scr[2 * (K::C + 1) + t] = v.z;
-    scr[3 * (K::C + 1) + t] = v.w;
-  }
-}
-
-// Token scalars of chunk c: gamma = bf16(dt) sigmoid(trap) (FP32), factor =
-// bf16(gamma + bf16(bf16(dt[t+1]) sigmoid(-trap[t+1]))) (as a BF16 pair),
-// exp(da_cs), exp(da_cs_rev); and the chunk's state decay exp(da_cs[last]).
-// tok layout: gam[C] | facd[C] (u32) | eda[C] | edr[C] | alpha.
-template <class K>
-__device__ void token_scalars(const Params& p, const float* scr, float* tok, int c) {
-  const int t = threadIdx.x;
-  const int Sp = p.nc * K::C;
-  constexpr int C1 = K::C + 1;
-  if (t < K::C) {
-    const int tg = c * K::C + t;
-    const float gam = __fmul_rn(round_bf(scr[t]), sigmoid_f(scr[C1 + t]));
-    float sh = 0.f;
-    if (tg + 1 < Sp)
-      sh = round_bf(__fmul_rn(round_bf(scr[t + 1]), 1.0f / (1.0f + expf(scr[C1 + t + 1]))));
-    tok[t] = gam;
-    reinterpret_cast<uint32_t*>(tok)[K::C + t] = dup_bf(__fadd_rn(gam, sh));
-    tok[2 * K::C + t] = expf(scr[2 * C1 + t]);
-    tok[3 * K::C + t] = expf(scr[3 * C1 + t]);
-  }
-  if (t == K::C) {
-    const int last = min(c * K::C + K::C, p.S) - 1 - c * K::C;
-    tok[4 * K::C] = expf(scr[2 * C1 + last]);
-  }
-}
-
 // sin and cos of x: Cody-Waite reduction of x by 2*pi (2*pi split into the
 // nearest float and the float nearest the remainder) to r in about
 // [-pi, pi], then the sin.approx / cos.approx instructions (absolute error
@@ -319,6 +281,37 @@ __device__ __forceinline__ void sincos_fast(float x, float* s, float* c) {
 }
 // e^x as 2^(x log2 e) with the ex2.approx instruction.
 __device__ __forceinline__ float exp_fast(float x) { return ex2_approx(x * 1.44269504088896341f); }
+
+// Token scalars of chunk c computed by warp 0 from its prefetched registers
+// (thread t holds token c*C + t; lane C the next chunk's first token), the
+// next token's dt / trap by a shuffle: gamma = bf16(dt) sigmoid(trap) (FP32),
+// factor = bf16(gamma + bf16(bf16(dt[t+1]) sigmoid(-trap[t+1]))) (as a BF16
+// pair), exp(da_cs), exp(da_cs_rev).
+// tok layout: gam[C] | facd[C] (u32) | eda[C] | edr[C].
+template <class K>
+__device__ __forceinline__ void token_scalars_regs(const Params& p, float4 v, float* tok, int c) {
+  static_assert(K::C + 1 <= 32, "token scalars of one chunk must sit in one warp");
+  if (threadIdx.x < 32) {
+    const int t = threadIdx.x;
+    const float dtn = __shfl_down_sync(0xffffffffu, v.x, 1);
+    const float trn = __shfl_down_sync(0xffffffffu, v.y, 1);
+    if (t < K::C) {
+      const int tg = c * K::C + t;
+      const float gam = __fmul_rn(round_bf(v.x), sigmoid_f(v.y));
+      float sh = 0.f;
+      if (tg + 1 < p.nc * K::C) sh = round_bf(__fmul_rn(round_bf(dtn), 1.0f / (1.0f + expf(trn))));
+      tok[t] = gam;
+      reinterpret_cast<uint32_t*>(tok)[K::C + t] = dup_bf(__fadd_rn(gam, sh));
+      tok[2 * K::C + t] = expf(v.z);
+      tok[3 * K::C + t] = expf(v.w);
+    }
+  }
+}
+// The chunk's state decay exp(da_cs[last valid token]) from the token table.
+template <class K>
+__device__ __forceinline__ float chunk_decay(const Params& p, const float* tok, int c) {
+  return tok[2 * K::C + min(c * K::C + K::C, p.S) - 1 - c * K::C];
+}
 
 // cos/sin of the chunk's angles, [C][W] each.
 template <class K>
@@ -552,8 +545,7 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
   uint16_t* Psi = reinterpret_cast<uint16_t*>(sm + L.Psi);
   float* cosT = reinterpret_cast<float*>(sm + L.cosT);
   float* sinT = reinterpret_cast<float*>(sm + L.sinT);
-  float* tok = reinterpret_cast<float*>(sm + L.tok);
-  float* scr = reinterpret_cast<float*>(sm + L.scr);
+  float* tokb = reinterpret_cast<float*>(sm + L.tok);
   uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
   uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
 
@@ -571,11 +563,11 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
     if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, false, false);
     const Stage S = stage_at(L.st[0], s);
     cp_commit();
-    store_scalars<K>(scr, scal);
+    float* tok = tokb + s * (4 * K::C + 4);
+    token_scalars_regs<K>(p, scal, tok, c);
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
     cp_wait<1>();
-    __syncthreads();  // (1) chunk c raw inputs and scalars visible
-    token_scalars<K>(p, scr, tok, c);
+    __syncthreads();  // (1) chunk c raw inputs and token scalars visible
     sincos_table<K>(reinterpret_cast<const float*>(sm + S.ang), cosT, sinT);
     __syncthreads();  // (2)
     {
@@ -589,7 +581,7 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
       psi_rows<K>(reinterpret_cast<const uint16_t*>(sm + S.v), mvb, Psi, j0);
     }
     __syncthreads();  // (3)
-    const float alpha = tok[4 * K::C];
+    const float alpha = chunk_decay<K>(p, tok, c);
     state_mma<K>(st, Psi, Kst, alpha, pm, nbase);
     decay *= alpha;
   }
@@ -690,17 +682,13 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
   float* eseg = reinterpret_cast<float*>(sm + L.eseg);
   float* cosT = reinterpret_cast<float*>(sm + L.cosT);
   float* sinT = reinterpret_cast<float*>(sm + L.sinT);
-  float* tok = reinterpret_cast<float*>(sm + L.tok);
-  float* scr = reinterpret_cast<float*>(sm + L.scr);
+  float* tokb = reinterpret_cast<float*>(sm + L.tok);
   uint16_t* dzs = reinterpret_cast<uint16_t*>(sm + L.dzs);
   uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
   float2* mzp = reinterpret_cast<float2*>(sm + L.mzp);
   uint32_t* mop = reinterpret_cast<uint32_t*>(sm + L.mop);
   uint16_t* qbs = reinterpret_cast<uint16_t*>(sm + L.qbs);
   uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
-  const uint32_t* facd = reinterpret_cast<const uint32_t*>(tok) + C;
-  const float* eda = tok + 2 * C;
-  const float* edr = tok + 3 * C;
 
   // ---- once per CTA: parameters of head h, first chunk's inputs in flight
   param_tables<K>(p, h, mvb, qbs, kbs);
@@ -760,11 +748,14 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
     const Stage S = stage_at(L.st[0], s);
     if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, true, need_out);
     cp_commit();
-    store_scalars<K>(scr, scal);
+    float* tok = tokb + s * (4 * C + 4);
+    const uint32_t* facd = reinterpret_cast<const uint32_t*>(tok) + C;
+    const float* eda = tok + 2 * C;
+    const float* edr = tok + 3 * C;
+    token_scalars_regs<K>(p, scal, tok, c);
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
     cp_wait<1>();
-    __syncthreads();  // (1) chunk c raw inputs and scalars visible
-    token_scalars<K>(p, scr, tok, c);
+    __syncthreads();  // (1) chunk c raw inputs and token scalars visible
     if (need_out) {
       const float* sg = reinterpret_cast<const float*>(sm + S.seg);
       for (int e = threadIdx.x; e < C * C; e += K::NT)
@@ -910,7 +901,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
     }
     // state update: state^T = exp(da_cs[last]) state^T + PsiV^T k_state
     tm_load_state<K>(tm_st, st);
-    state_mma<K>(st, Psi, Kst, tok[4 * C], pm, nbase);
+    state_mma<K>(st, Psi, Kst, chunk_decay<K>(p, tok, c), pm, nbase);
     tm_store_state<K>(tm_st, st);
 
     // ---- per-element epilogue on X^T (p-row pairs (p, p+8), four columns
