@@ -38,7 +38,16 @@ WORKLOAD_INDEX = 2
 # The pages' own median for this shape (Ascend910, 53.849475 ms per call).
 PAGES_TOKENS_PER_S = 8192 / 0.053849475
 DOMINANT = "chunk_output"
-KERNEL_SOURCE = os.path.join(ROOT, "mamba_mimo_chunked_gb300", "csrc", "mmbf_kernels.cu")
+KERNEL_DIR = os.path.join(ROOT, "mamba_mimo_chunked_gb300", "csrc")
+
+
+def kernel_source_sha256():
+    """sha256 over the CUDA sources (sorted by name, concatenated)."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(KERNEL_DIR)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(KERNEL_DIR, name), "rb").read())
+    return h.hexdigest()
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -92,7 +101,7 @@ def measured_peaks():
 def profile_traffic():
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
-    sha = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    sha = kernel_source_sha256()
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
