@@ -315,11 +315,11 @@ def main():
     elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, dev)
 
     stage_ms = {}
-    for k in range(4):
+    for k in range(min(4, launches_per_call)):
         name = lib.mamba_mimo_stage_name(k)
-        name = name.decode() if isinstance(name, bytes) else ctypes.string_at(name).decode()
-        if k >= launches_per_call:
+        if not name:
             continue
+        name = name.decode() if isinstance(name, bytes) else ctypes.string_at(name).decode()
         stage_ms[name] = statistics.mean(row[2 * k].elapsed_time(row[2 * k + 1]) for row in ev)
     dom_ms = stage_ms[DOMINANT]
     peak, peak_kind = measured_peaks()

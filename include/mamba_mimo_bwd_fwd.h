@@ -177,8 +177,11 @@ void mamba_mimo_set_stage_events(void* const* events, int count);
  * the k-th shape-specialised family. */
 int mamba_mimo_last_kernel_variant(void);
 
-/* Name of the i-th kernel a call may launch (0 <= i < 4), or NULL:
- * "segment_state", "segment_prefix", "chunk_output", "grad_reduce". */
+/* Name of the i-th kernel the last mamba_mimo_bwd_fwd call on this thread
+ * launched (0 <= i < 4), or NULL past its last kernel.  The generic kernels
+ * are "segment_state", "segment_prefix", "chunk_output", "grad_reduce"; the
+ * shape-specialised ones "segment_state", "chunk_output" (the segment scan
+ * and the gradient sum are folded into those two). */
 const char* mamba_mimo_stage_name(int i);
 
 #ifdef __cplusplus

@@ -148,6 +148,7 @@ struct Stage {  // raw inputs of one chunk
 struct Smem {
   Stage st[2];
   uint32_t Ks, Kst, Psi, Sb, qkd, eseg, cosT, sinT, tok, dzs, mvb, mzp, mop, qbs, kbs, red, tm;
+  uint32_t xch;  // state exchange: the cluster fold (state kernel), the entering state (output kernel)
   uint32_t total;
 };
 
@@ -198,6 +199,16 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   // end-of-segment reduction scratch reuses the stage buffers when they fit
   const uint32_t red_bytes = need_out ? (uint32_t)K::NT * 2 * K::SLOTS * K::NMTH * 2 * 4 : 0;
   L.red = (red_bytes <= L.st[0].bytes + L.st[1].bytes) ? 0 : take(red_bytes);
+  // Stage buffers are idle where the exchange is used: after the chunk loop in
+  // the state kernel (both stages), before the loop's first prefetch into
+  // stage 1 in the output kernel.
+  if (out_kernel) {
+    const uint32_t x = (uint32_t)K::N * K::P * 4;
+    L.xch = (x <= L.st[1].bytes) ? L.st[0].bytes : take(x);
+  } else {
+    const uint32_t x = (uint32_t)K::NT * K::NN8 * 16;
+    L.xch = (x <= L.st[0].bytes + L.st[1].bytes) ? 0 : take(x);
+  }
   L.total = o;
   return L;
 }
@@ -549,7 +560,7 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
   uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
   uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
 
-  pdl_trigger();  // the prefix kernel may launch; it waits for this grid's results
+  if (unit == 0 && threadIdx.x == 0) p.ws_count[bh] = 0u;  // read by this call's output kernel
   param_tables<K>(p, h, mvb, nullptr, kbs);
   if (c0 < c1) load_stage<K>(p, L.st[0], sm, bh, c0, false, false);
   cp_commit();
@@ -585,16 +596,63 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
     state_mma<K>(st, Psi, Kst, alpha, pm, nbase);
     decay *= alpha;
   }
+  // ---- segment sum.  The UA units of a segment run as one thread-block
+  //      cluster; its last CTA folds the units' sums in unit order
+  //      (sum = sum * decay_u + S_u, the chunk recurrence regrouped by unit)
+  //      and writes the segment's FP32 [N][P] sum and decay product.
   const int g = lane >> 2, cq = lane & 3;
-  float* dst = p.ws_state + ((int64_t)bh * p.nunit + unit) * K::N * K::P;
+  float* dst = p.ws_state + ((int64_t)bh * p.nseg + seg) * K::N * K::P;
+  float* dsts = p.ws_decay + (int64_t)bh * p.nseg + seg;
+  if (p.UA > 1) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    float4* xch = reinterpret_cast<float4*>(sm + L.xch);
+    float* xdec = reinterpret_cast<float*>(sm + L.tm);
+    __syncthreads();  // every warp is past its last read of the stage buffers
 #pragma unroll
-  for (int nn = 0; nn < K::NN8; nn++)
+    for (int nn = 0; nn < K::NN8; nn++)
+      xch[nn * K::NT + threadIdx.x] = make_float4(st[nn][0], st[nn][1], st[nn][2], st[nn][3]);
+    if (threadIdx.x == 0) *xdec = decay;
+    cl.sync();
+    if ((int)cl.block_rank() == p.UA - 1) {
+      float acc[K::NN8][4];
+      float dseg = 1.f;
 #pragma unroll
-    for (int e = 0; e < 4; e++) {
-      const int n = nbase + nn * 8 + 2 * cq + (e & 1), pp = pm * 16 + g + 8 * (e >> 1);
-      dst[n * K::P + pp] = st[nn][e];
+      for (int nn = 0; nn < K::NN8; nn++) acc[nn][0] = acc[nn][1] = acc[nn][2] = acc[nn][3] = 0.f;
+      for (int u = 0; u < p.UA; u++) {
+        const float4* src = cl.map_shared_rank(xch, u);
+        const float du = *cl.map_shared_rank(xdec, u);
+#pragma unroll
+        for (int nn = 0; nn < K::NN8; nn++) {
+          const float4 x = src[nn * K::NT + threadIdx.x];
+          acc[nn][0] = acc[nn][0] * du + x.x;
+          acc[nn][1] = acc[nn][1] * du + x.y;
+          acc[nn][2] = acc[nn][2] * du + x.z;
+          acc[nn][3] = acc[nn][3] * du + x.w;
+        }
+        dseg = u ? dseg * du : du;
+      }
+#pragma unroll
+      for (int nn = 0; nn < K::NN8; nn++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const int n = nbase + nn * 8 + 2 * cq + (e & 1), pp = pm * 16 + g + 8 * (e >> 1);
+          dst[n * K::P + pp] = acc[nn][e];
+        }
+      if (threadIdx.x == 0) *dsts = dseg;
     }
-  if (threadIdx.x == 0) p.ws_decay[(int64_t)bh * p.nunit + unit] = decay;
+    cl.sync();  // the other CTAs' shared memory stays valid until it has been read
+  } else {
+#pragma unroll
+    for (int nn = 0; nn < K::NN8; nn++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        const int n = nbase + nn * 8 + 2 * cq + (e & 1), pp = pm * 16 + g + 8 * (e >> 1);
+        dst[n * K::P + pp] = st[nn][e];
+      }
+    if (threadIdx.x == 0) *dsts = decay;
+  }
+  pdl_trigger();  // the output kernel may launch; it waits for this grid's results
 }
 
 }  // namespace fast
@@ -728,8 +786,46 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
   // ---- entering state of the segment (written by the prefix kernel)
   pdl_wait();
   {
+    // the state entering this segment: the earlier segments' sums folded in
+    // segment order (state = state * decay_s + sum_s), staged in shared memory
+    constexpr int NV4 = N * P / 4 / K::NT;
+    static_assert((N * P) % (4 * K::NT) == 0, "state elements must split evenly over the threads");
+    float4 acc[NV4];
+#pragma unroll
+    for (int i = 0; i < NV4; i++) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* A = reinterpret_cast<const float4*>(p.ws_state + (int64_t)bh * p.nseg * N * P);
+    const float* D = p.ws_decay + (int64_t)bh * p.nseg;
+    auto fold = [&](float4& a, float4 x, float d) {
+      a.x = a.x * d + x.x; a.y = a.y * d + x.y; a.z = a.z * d + x.z; a.w = a.w * d + x.w;
+    };
+    int s2 = 0;
+    for (; s2 + 1 < seg; s2 += 2) {
+      float4 x0[NV4], x1[NV4];
+#pragma unroll
+      for (int i = 0; i < NV4; i++) {
+        x0[i] = __ldcg(A + (int64_t)s2 * (N * P / 4) + i * K::NT + threadIdx.x);
+        x1[i] = __ldcg(A + (int64_t)(s2 + 1) * (N * P / 4) + i * K::NT + threadIdx.x);
+      }
+      const float d0 = __ldcg(D + s2), d1 = __ldcg(D + s2 + 1);
+#pragma unroll
+      for (int i = 0; i < NV4; i++) {
+        fold(acc[i], x0[i], d0);
+        fold(acc[i], x1[i], d1);
+      }
+    }
+    if (s2 < seg) {
+      const float d0 = __ldcg(D + s2);
+#pragma unroll
+      for (int i = 0; i < NV4; i++) fold(acc[i], __ldcg(A + (int64_t)s2 * (N * P / 4) + i * K::NT + threadIdx.x), d0);
+    }
+    float4* xs = reinterpret_cast<float4*>(sm + L.xch);
+#pragma unroll
+    for (int i = 0; i < NV4; i++) xs[i * K::NT + threadIdx.x] = acc[i];
+  }
+  __syncthreads();
+  {
     float st[K::NN8][4];
-    const float* src = p.ws_state + ((int64_t)bh * p.nunit + (int64_t)seg * p.UA) * N * P;
+    const float* src = reinterpret_cast<const float*>(sm + L.xch);
 #pragma unroll
     for (int nn = 0; nn < K::NN8; nn++)
 #pragma unroll
@@ -741,6 +837,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
     for (int q = 0; q < K::TM_DM / 8; q++) tm_st8(tm_dm + q * 8, zero8);
     tm_wait_st();
   }
+  __syncthreads();  // every thread has its entering state before stage 1 is refilled
   pdl_trigger();
 
   for (int c = c0; c < c1; c++) {
@@ -1112,6 +1209,25 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
             if (perm<R>((sl >> 1) * 8 + 2 * cc + (sl & 1)) % R == r)
               sum += red[(w * 32 + gg * 4 + cc) * PER + ((which * 4 + sl) * NMTH + mtl) * 2 + hh];
       dst[e] = sum;
+    }
+    // The last CTA of this (b,h) to finish sums the segments' partials in
+    // segment order (the result does not depend on which CTA is last).
+    __threadfence();
+    __syncthreads();
+    unsigned int* last = reinterpret_cast<unsigned int*>(sm + L.tm);
+    if (threadIdx.x == 0) *last = (atomicAdd(p.ws_count + bh, 1u) == (unsigned int)p.nseg - 1u) ? 1u : 0u;
+    __syncthreads();
+    if (*last) {
+      __threadfence();
+      const float* src = p.ws_grad + (int64_t)bh * p.nseg * 2 * R * P;
+      for (int e = threadIdx.x; e < 2 * R * P; e += K::NT) {
+        const int which = e / (R * P), x = e % (R * P);
+        if (which == 0 && !RED) continue;
+        if (which == 1 && !HZ) continue;
+        float sum = 0.f;
+        for (int sgm = 0; sgm < p.nseg; sgm++) sum += __ldcg(src + (int64_t)sgm * 2 * R * P + e);
+        (which == 0 ? p.dmimo_o : p.dmimo_z)[(int64_t)bh * R * P + x] = sum;
+      }
     }
   }
 }

@@ -27,6 +27,11 @@
 //   grad_reduce_kernel     grid (b*h)
 //       Fixed-order sum of the per-segment dmimo_o / dmimo_z partials.
 //
+// Shapes with specialised kernels (mmbf_fast.cuh) run three launches:
+// fast::state_kernel over state units of LA chunks, unit_prefix_kernel (the
+// state entering each segment), and fast::output_kernel, whose last CTA per
+// (b,h) -- found with an atomic counter -- does the fixed-order gradient sum.
+//
 // Rows of a chunk tile are j = t*R + r (token-major), as in the reference's
 // flatten of the token and rank axes.  BF16 products and sums of two BF16
 // values use mul.rn.bf16x2 / add.rn.bf16x2: the exact product of two BF16
@@ -34,6 +39,7 @@
 // rounding of a sum equal to direct BF16 rounding, so these equal the
 // reference's FP32-op-then-round steps bit for bit.
 
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -149,6 +155,7 @@ struct Params {
   float *dmimo_o, *dmimo_z;
   uint16_t *states, *dz, *qk_dot;
   float *ws_state, *ws_decay, *ws_grad;
+  unsigned int* ws_count;  // per (b,h): output CTAs done (specialised kernels)
 };
 
 __host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
@@ -784,6 +791,9 @@ static thread_local int g_failed_stage = -1;  // kernel index of a failed launch
 static thread_local int g_variant = -1;       // kernel family of the last call
 static const char* const kStageNames[4] = {"segment_state", "segment_prefix", "chunk_output",
                                            "grad_reduce"};
+static const char* const kFastStageNames[2] = {"segment_state", "chunk_output"};
+static thread_local const char* const* g_stage_names = kStageNames;  // kernels of the last call
+static thread_local int g_stage_names_n = 4;
 
 // Records the optional timing event around kernel `i` (before: which = 0).
 static void stage_event(int i, int which, cudaStream_t s) {
@@ -974,10 +984,12 @@ static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduc
   if (p.fast >= 0) {
     p.L = fast_segment_length(p, fast_slots(p));
     p.nseg = (p.nc + p.L - 1) / p.L;
-    // The state-sum kernel works on units of about L/UA chunks: enough CTAs to
-    // fill the GPU several times over, short chains that hide load latency.
+    // The state-sum kernel works on units of about L/UA chunks, the UA units
+    // of a segment one thread-block cluster: more CTAs in flight, shorter
+    // chains.  Clusters of more than two CTAs measured slower (co-scheduling
+    // of the whole cluster leaves slots idle).
     const int64_t heads = (int64_t)p.B * p.H;
-    int ua = (int)std::max<int64_t>(1, std::min<int64_t>(8, (8 * 152 + heads * p.nseg - 1) / (heads * p.nseg)));
+    int ua = (int)std::max<int64_t>(1, std::min<int64_t>(2, (8 * 152 + heads * p.nseg - 1) / (heads * p.nseg)));
     ua = std::min(ua, p.L);
     p.LA = (p.L + ua - 1) / ua;
     p.UA = (p.L + p.LA - 1) / p.LA;
@@ -1002,7 +1014,8 @@ static size_t workspace_bytes_of(const Params& p) {
   const size_t st = align16((size_t)p.B * p.H * n * p.N * p.P * 4);
   const size_t dec = align16((size_t)p.B * p.H * n * 4);
   const size_t gr = align16((size_t)p.B * p.H * n * 2 * p.R * p.P * 4);
-  return st + dec + gr + 256;
+  const size_t cnt = align16((size_t)p.B * p.H * 4);
+  return st + dec + gr + cnt + 256;
 }
 
 template <int RMAX>
@@ -1017,19 +1030,31 @@ static cudaError_t launch_output(const Params& p, size_t smem, cudaStream_t s) {
 
 // Launch with programmatic dependent launch (the kernel waits with
 // griddepcontrol.wait before it reads its predecessor's results).
+// cluster_y > 1 groups consecutive blockIdx.y into thread-block clusters.
 template <typename Kern>
 static cudaError_t launch_ex(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                             const Params& p) {
+                             const Params& p, int cluster_y = 1) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    n++;
+  }
+  if (cluster_y > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = (unsigned)cluster_y;
+    attr[n].val.clusterDim.z = 1;
+    n++;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -1046,39 +1071,23 @@ static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) 
     e = all_on ? ensure_smem(fast::output_kernel<K, 7>, so, &fast_out_smem_set<K, 7>())
                : ensure_smem(fast::output_kernel<K, -1>, so, &fast_out_smem_set<K, -1>());
   if (e != cudaSuccess) return e;
-  const bool vec = (p.N * p.P) % 4 == 0;
-  const int npe = vec ? (p.N * p.P) / 4 : p.N * p.P;
+  g_stage_names = kFastStageNames;
+  g_stage_names_n = 2;
   g_failed_stage = 0;
   stage_event(0, 0, st);
+  // the UA units of a segment form one cluster (UA <= 8)
   e = launch_ex(fast::state_kernel<StateCfg<K>>, dim3(p.B * p.H, p.nunit), dim3(StateCfg<K>::NT), ss,
-                st, false, p);
+                st, false, p, p.UA);
   stage_event(0, 1, st);
   (*launches)++;
   if (e != cudaSuccess) return e;
   g_failed_stage = 1;
   stage_event(1, 0, st);
-  e = vec ? launch_ex(segment_prefix_vec_kernel<4>, dim3((npe + 127) / 128, p.B * p.H), dim3(128), 0, st,
-                      true, p)
-          : launch_ex(segment_prefix_vec_kernel<1>, dim3((npe + 127) / 128, p.B * p.H), dim3(128), 0, st,
-                      true, p);
-  stage_event(1, 1, st);
-  (*launches)++;
-  if (e != cudaSuccess) return e;
-  g_failed_stage = 2;
-  stage_event(2, 0, st);
   e = all_on ? launch_ex(fast::output_kernel<K, 7>, dim3(p.B * p.H, p.nseg), dim3(K::NT), so, st, true, p)
              : launch_ex(fast::output_kernel<K, -1>, dim3(p.B * p.H, p.nseg), dim3(K::NT), so, st, true, p);
-  stage_event(2, 1, st);
+  stage_event(1, 1, st);
   (*launches)++;
-  if (e != cudaSuccess) return e;
-  if (p.reduced || p.has_z) {
-    g_failed_stage = 3;
-    stage_event(3, 0, st);
-    e = launch_ex(grad_reduce_kernel, dim3(p.B * p.H), dim3(256), 0, st, true, p);
-    stage_event(3, 1, st);
-    (*launches)++;
-  }
-  return e;
+  return e;  // the output kernel's last CTA per (b,h) also sums the dmimo partials
 }
 
 // Built-in scratch area of mamba_mimo_bwd_fwd_fixed_scratch: a file-scope
@@ -1180,6 +1189,8 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
   p.ws_decay = reinterpret_cast<float*>(ws);
   ws += align16((size_t)p.B * p.H * wsn * 4);
   p.ws_grad = reinterpret_cast<float*>(ws);
+  ws += align16((size_t)p.B * p.H * wsn * 2 * p.R * p.P * 4);
+  p.ws_count = reinterpret_cast<unsigned int*>(ws);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int launches = 0;
@@ -1201,13 +1212,15 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
     g_variant = p.fast;
     if (e != cudaSuccess)
       return fail(MMBF_ERR_CUDA, "CUDA error in %s (fast %d, grid %d x %d/%d): %s",
-                  g_failed_stage >= 0 ? kStageNames[g_failed_stage] : "setup", p.fast, p.B * p.H,
+                  g_failed_stage >= 0 ? g_stage_names[g_failed_stage] : "setup", p.fast, p.B * p.H,
                   p.nseg, p.nunit, cudaGetErrorString(e));
     g_launches = launches;
     return MMBF_OK;
   }
   // Generic kernels (any shape of the envelope).  Their segmentation is the
   // generic one, one state unit per segment.
+  g_stage_names = kStageNames;
+  g_stage_names_n = 4;
   {
     const int64_t per_seg = (int64_t)p.B * p.H * p.npslice;
     const int ng = (int)std::min<int64_t>(p.nc, std::max<int64_t>(1, (kTargetCtas + per_seg - 1) / per_seg));
@@ -1308,6 +1321,8 @@ void mamba_mimo_set_stage_events(void* const* events, int count) {
   g_stage_count = g_stage_events ? count : 0;
 }
 
-const char* mamba_mimo_stage_name(int i) { return (i >= 0 && i < 4) ? kStageNames[i] : nullptr; }
+const char* mamba_mimo_stage_name(int i) {
+  return (i >= 0 && i < g_stage_names_n) ? g_stage_names[i] : nullptr;
+}
 
 }  // extern "C"
