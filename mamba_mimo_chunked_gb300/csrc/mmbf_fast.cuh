@@ -147,7 +147,7 @@ struct Stage {  // raw inputs of one chunk
 };
 struct Smem {
   Stage st[2];
-  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, cosT, sinT, tok, dzs, mvb, mzp, mop, qbs, kbs, red, tm;
+  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, tok, dzs, mvb, mzp, mop, qbs, kbs, red, tm;
   uint32_t xch;  // state exchange: the cluster fold (state kernel), the entering state (output kernel)
   uint32_t total;
 };
@@ -186,8 +186,6 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   L.Sb = out_kernel ? take(K::N * K::LDP * 2) : 0;
   L.qkd = out_kernel ? take(K::C * K::R * K::R * 4) : 0;
   L.eseg = need_out ? take(K::C * K::C * 4) : 0;
-  L.cosT = take(K::C * K::W * 4);
-  L.sinT = take(K::C * K::W * 4);
   L.tok = take(2 * (K::C * 4 * 4 + 16));
   L.dzs = (need_out && has_z) ? take(K::C * K::LDP * 2) : 0;
   L.mvb = take(K::R * K::P * 2);
@@ -324,12 +322,6 @@ __device__ __forceinline__ float chunk_decay(const Params& p, const float* tok, 
   return tok[2 * K::C + min(c * K::C + K::C, p.S) - 1 - c * K::C];
 }
 
-// cos/sin of the chunk's angles, [C][W] each.
-template <class K>
-__device__ void sincos_table(const float* ang, float* cosT, float* sinT) {
-  for (int e = threadIdx.x; e < K::C * K::W; e += K::NT) sincos_fast(ang[e], &sinT[e], &cosT[e]);
-}
-
 // This warp's 16 rows of a [CR][LDN] tile as MMA A fragments, rows visited in
 // perm order.
 template <class K>
@@ -379,21 +371,32 @@ __device__ __forceinline__ void rotate_regs(uint32_t& lo, uint32_t& hi, float2 c
   lo = pack2(__fadd2_rn(__fmul2_rn(cs, a), make_float2(-sx.x, -sx.y)));
   hi = pack2(__fadd2_rn(__fmul2_rn(sn, a), __fmul2_rn(cs, x)));
 }
+// The same rotary with each thread taking the sines and cosines it needs from
+// the chunk's raw angles [C][W] (no shared table, no barrier).  For R = 4 and
+// 8 the two rows of a fragment register pair belong to one token.
 template <class K, bool WITH_Q>
-__device__ __forceinline__ void rotate(uint32_t (&fq)[K::NKT][4], uint32_t (&fk)[K::NKT][4],
-                                       const float* cosT, const float* sinT, int j0) {
+__device__ __forceinline__ void rotate_direct(uint32_t (&fq)[K::NKT][4], uint32_t (&fk)[K::NKT][4],
+                                              const float* ang, int j0) {
+  constexpr bool SAME = (K::R == 4 || K::R == 8);
   const int c2 = 2 * (threadIdx.x & 3);
 #pragma unroll
   for (int kt = 0; kt < K::NKT / 2; kt++)
 #pragma unroll
-    for (int e = 0; e < 4; e++) {
-      if (kt * 16 + 8 * (e >> 1) >= K::W) continue;
-      const int tl = (j0 + frag_row<K>(e)) / K::R;
-      const int m = kt * 16 + 8 * (e >> 1) + c2;
-      const float2 cs = *reinterpret_cast<const float2*>(cosT + tl * K::W + m);
-      const float2 sn = *reinterpret_cast<const float2*>(sinT + tl * K::W + m);
-      if (WITH_Q) rotate_regs<K>(fq[kt][e], fq[kt + K::NKT / 2][e], cs, sn);
-      rotate_regs<K>(fk[kt][e], fk[kt + K::NKT / 2][e], cs, sn);
+    for (int hc = 0; hc < 2; hc++) {
+      if (kt * 16 + 8 * hc >= K::W) continue;
+      const int m = kt * 16 + 8 * hc + c2;
+      float2 cs, sn;
+#pragma unroll
+      for (int hr = 0; hr < 2; hr++) {
+        const int e = 2 * hc + hr;
+        if (hr == 0 || !SAME) {
+          const float2 a = *reinterpret_cast<const float2*>(ang + ((j0 + frag_row<K>(e)) / K::R) * K::W + m);
+          sincos_fast(a.x, &sn.x, &cs.x);
+          sincos_fast(a.y, &sn.y, &cs.y);
+        }
+        if (WITH_Q) rotate_regs<K>(fq[kt][e], fq[kt + K::NKT / 2][e], cs, sn);
+        rotate_regs<K>(fk[kt][e], fk[kt + K::NKT / 2][e], cs, sn);
+      }
     }
 }
 
@@ -554,8 +557,6 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
   const int pm = warp % K::NMT, nbase = (warp / K::NMT) * K::NCW;
   uint16_t* Kst = reinterpret_cast<uint16_t*>(sm + L.Kst);
   uint16_t* Psi = reinterpret_cast<uint16_t*>(sm + L.Psi);
-  float* cosT = reinterpret_cast<float*>(sm + L.cosT);
-  float* sinT = reinterpret_cast<float*>(sm + L.sinT);
   float* tokb = reinterpret_cast<float*>(sm + L.tok);
   uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
   uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
@@ -579,13 +580,11 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
     cp_wait<1>();
     __syncthreads();  // (1) chunk c raw inputs and token scalars visible
-    sincos_table<K>(reinterpret_cast<const float*>(sm + S.ang), cosT, sinT);
-    __syncthreads();  // (2)
     {
       uint32_t kf[K::NKT][4];
       load_rows<K>(kf, reinterpret_cast<const uint16_t*>(sm + S.k), j0);
       add_bias<K>(kf, kbs);
-      rotate<K, false>(kf, kf, cosT, sinT, j0);
+      rotate_direct<K, false>(kf, kf, reinterpret_cast<const float*>(sm + S.ang), j0);
       scale_k<K>(kf, reinterpret_cast<const uint32_t*>(tok) + K::C, j0);
       k_state<K>(kf, tok + 3 * K::C, j0);
       store_rows<K>(kf, Kst, j0);
@@ -738,8 +737,6 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
   uint16_t* Sb = reinterpret_cast<uint16_t*>(sm + L.Sb);
   uint32_t* qkd = reinterpret_cast<uint32_t*>(sm + L.qkd);
   float* eseg = reinterpret_cast<float*>(sm + L.eseg);
-  float* cosT = reinterpret_cast<float*>(sm + L.cosT);
-  float* sinT = reinterpret_cast<float*>(sm + L.sinT);
   float* tokb = reinterpret_cast<float*>(sm + L.tok);
   uint16_t* dzs = reinterpret_cast<uint16_t*>(sm + L.dzs);
   uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
@@ -798,25 +795,24 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
     auto fold = [&](float4& a, float4 x, float d) {
       a.x = a.x * d + x.x; a.y = a.y * d + x.y; a.z = a.z * d + x.z; a.w = a.w * d + x.w;
     };
-    int s2 = 0;
-    for (; s2 + 1 < seg; s2 += 2) {
-      float4 x0[NV4], x1[NV4];
+    // four segments' loads in flight per round trip; past the last segment
+    // the fold is the identity (decay 1, sum 0)
+    for (int s2 = 0; s2 < seg; s2 += 4) {
+      float4 x[4][NV4];
+      float d[4];
 #pragma unroll
-      for (int i = 0; i < NV4; i++) {
-        x0[i] = __ldcg(A + (int64_t)s2 * (N * P / 4) + i * K::NT + threadIdx.x);
-        x1[i] = __ldcg(A + (int64_t)(s2 + 1) * (N * P / 4) + i * K::NT + threadIdx.x);
+      for (int k = 0; k < 4; k++) {
+        const bool in = s2 + k < seg;
+        d[k] = in ? __ldcg(D + s2 + k) : 1.f;
+#pragma unroll
+        for (int i = 0; i < NV4; i++)
+          x[k][i] = in ? __ldcg(A + (int64_t)(s2 + k) * (N * P / 4) + i * K::NT + threadIdx.x)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      const float d0 = __ldcg(D + s2), d1 = __ldcg(D + s2 + 1);
 #pragma unroll
-      for (int i = 0; i < NV4; i++) {
-        fold(acc[i], x0[i], d0);
-        fold(acc[i], x1[i], d1);
-      }
-    }
-    if (s2 < seg) {
-      const float d0 = __ldcg(D + s2);
+      for (int k = 0; k < 4; k++)
 #pragma unroll
-      for (int i = 0; i < NV4; i++) fold(acc[i], __ldcg(A + (int64_t)s2 * (N * P / 4) + i * K::NT + threadIdx.x), d0);
+        for (int i = 0; i < NV4; i++) fold(acc[i], x[k][i], d[k]);
     }
     float4* xs = reinterpret_cast<float4*>(sm + L.xch);
 #pragma unroll
@@ -853,13 +849,6 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
     cp_wait<1>();
     __syncthreads();  // (1) chunk c raw inputs and token scalars visible
-    if (need_out) {
-      const float* sg = reinterpret_cast<const float*>(sm + S.seg);
-      for (int e = threadIdx.x; e < C * C; e += K::NT)
-        eseg[e] = ((e % C) < (e / C)) ? exp_fast(sg[e]) : 0.f;
-    }
-    sincos_table<K>(reinterpret_cast<const float*>(sm + S.ang), cosT, sinT);
-    __syncthreads();  // (2)
 
     // ---- warp prologue: Q/K of this j-block, same-token qk_dot, rotary,
     //      k_scaled / k_state tiles, PsiV rows, bf16(state) tile
@@ -896,7 +885,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
           }
         }
       }
-      rotate<K, true>(qf, kf, cosT, sinT, j0);
+      rotate_direct<K, true>(qf, kf, reinterpret_cast<const float*>(sm + S.ang), j0);
       scale_k<K>(kf, facd, j0);
       if (half == 0) {
         store_rows<K>(kf, Ks, j0);
@@ -918,7 +907,12 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
       const uint32_t r3 = pack2(make_float2(st[2 * nn + 1][2], st[2 * nn + 1][3]));
       stsm_x4_t(Sb + (nbase + nn * 16 + (mi >> 1) * 8 + li) * LDP + pm * 16 + (mi & 1) * 8, r0, r1, r2, r3);
     }
-    __syncthreads();  // (3) Ks, Kst, PsiV, Sb, qkd complete
+    if (need_out) {  // exp(segsum) below the diagonal (read after the barrier)
+      const float* sg = reinterpret_cast<const float*>(sm + S.seg);
+      for (int e = threadIdx.x; e < C * C; e += K::NT)
+        eseg[e] = ((e % C) < (e / C)) ? exp_fast(sg[e]) : 0.f;
+    }
+    __syncthreads();  // (3) Ks, Kst, PsiV, Sb, qkd, eseg complete
 
     {  // states[c] = bf16(state entering chunk c)
       constexpr int GP = P / 8;
@@ -1219,14 +1213,31 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
     __syncthreads();
     if (*last) {
       __threadfence();
-      const float* src = p.ws_grad + (int64_t)bh * p.nseg * 2 * R * P;
-      for (int e = threadIdx.x; e < 2 * R * P; e += K::NT) {
-        const int which = e / (R * P), x = e % (R * P);
-        if (which == 0 && !RED) continue;
-        if (which == 1 && !HZ) continue;
-        float sum = 0.f;
-        for (int sgm = 0; sgm < p.nseg; sgm++) sum += __ldcg(src + (int64_t)sgm * 2 * R * P + e);
-        (which == 0 ? p.dmimo_o : p.dmimo_z)[(int64_t)bh * R * P + x] = sum;
+      // element e = threadIdx.x + i*NT; four segments' loads in flight
+      constexpr int NE = 2 * R * P / K::NT;
+      static_assert((2 * R * P) % K::NT == 0, "gradient partials must split evenly over the threads");
+      const float* src = p.ws_grad + (int64_t)bh * p.nseg * 2 * R * P + threadIdx.x;
+      float sum[NE];
+#pragma unroll
+      for (int i = 0; i < NE; i++) sum[i] = 0.f;
+      for (int s0 = 0; s0 < p.nseg; s0 += 4) {
+        float x[4][NE];
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+#pragma unroll
+          for (int i = 0; i < NE; i++)
+            x[k][i] = (s0 + k < p.nseg) ? __ldcg(src + (int64_t)(s0 + k) * 2 * R * P + i * K::NT) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+#pragma unroll
+          for (int i = 0; i < NE; i++)
+            if (s0 + k < p.nseg) sum[i] += x[k][i];
+      }
+#pragma unroll
+      for (int i = 0; i < NE; i++) {
+        const int e = threadIdx.x + i * K::NT, which = e / (R * P), x = e % (R * P);
+        if (which == 0 && RED) p.dmimo_o[(int64_t)bh * R * P + x] = sum[i];
+        if (which == 1 && HZ) p.dmimo_z[(int64_t)bh * R * P + x] = sum[i];
       }
     }
   }
