@@ -177,6 +177,13 @@ void mamba_mimo_set_stage_events(void* const* events, int count);
  * the k-th shape-specialised family. */
 int mamba_mimo_last_kernel_variant(void);
 
+/* Launch plan of the last successful mamba_mimo_bwd_fwd call on this thread
+ * (diagnostic): writes min(n, 5) ints to out -- chunks per segment, segments
+ * per (b,h), state units per segment, chunks per unit, and the resident
+ * output-kernel CTAs the segment length was sized for (0 for the generic
+ * kernels) -- and returns how many it wrote (0 if out is NULL or n < 0). */
+int mamba_mimo_last_plan(int* out, int n);
+
 /* Name of the i-th kernel the last mamba_mimo_bwd_fwd call on this thread
  * launched (0 <= i < 4), or NULL past its last kernel.  The generic kernels
  * are "segment_state", "segment_prefix", "chunk_output", "grad_reduce"; the

@@ -76,6 +76,8 @@ def load_library():
         lib.mamba_mimo_set_stage_events.restype = None
         lib.mamba_mimo_set_stage_events.argtypes = [ctypes.c_void_p, ctypes.c_int]
         lib.mamba_mimo_last_kernel_variant.restype = ctypes.c_int
+        lib.mamba_mimo_last_plan.restype = ctypes.c_int
+        lib.mamba_mimo_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         lib.mamba_mimo_stage_name.restype = ctypes.c_char_p
         lib.mamba_mimo_stage_name.argtypes = [ctypes.c_int]
         _lib = lib
@@ -92,6 +94,14 @@ def last_kernel_variant() -> int:
     """-1 if the last call on this thread used the generic kernels, else the
     index of the shape-specialised kernel family it used."""
     return load_library().mamba_mimo_last_kernel_variant()
+
+
+def last_plan() -> dict:
+    """Launch plan of the last successful call on this thread."""
+    buf = (ctypes.c_int * 5)()
+    n = load_library().mamba_mimo_last_plan(buf, 5)
+    keys = ("chunks_per_segment", "segments", "units_per_segment", "chunks_per_unit", "output_slots")
+    return dict(zip(keys, list(buf)[:n]))
 
 
 def last_launch_count() -> int:

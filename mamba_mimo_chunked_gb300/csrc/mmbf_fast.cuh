@@ -34,8 +34,12 @@ struct Cfg {
   static constexpr int NKT = N / 16;          // 16-wide k tiles over N
   static constexpr int NMT = P / 16;          // 16-row p blocks of X^T / state^T
   static constexpr int NMTH = NMT / SPLIT;    // p blocks per warp in the output stage
-  static constexpr int LDN = N + 8;           // padded smem row strides (elements)
-  static constexpr int LDP = P + 8;
+  // smem row strides (elements): 128-byte rows unpadded, others padded by 8
+  static constexpr int LDN = (N == 64) ? 64 : N + 8;
+  static constexpr int LDP = (P == 64) ? 64 : P + 8;
+  // one warp per j-block: k_scaled / k_state go over the warp's own rows of
+  // the raw k / q stage tiles (output kernel), k_state over raw k (state kernel)
+  static constexpr bool ALIAS_K = (SPLIT == 1);
   static constexpr int WPM = NW / NMT;        // warps sharing one p-block of the state
   static constexpr int NCW = N / WPM;         // state columns (n) per warp
   static constexpr int NN8 = NCW / 8;         // n8 tiles of the state per warp
@@ -74,12 +78,15 @@ __device__ __forceinline__ int perm(int i) {
 // ---------------------------------------------------------------------------
 // Small device helpers
 
-// Element offset of (row, col) in a row-major tile with row stride LD whose
-// 16-byte chunks are XOR-swizzled by row bit 3 (col is a multiple of 8).  With
-// the +8-element padding, any 8 rows that share bit 3 and any set of rows
-// visited through perm() hit 8 different bank groups.
+// Element offset of (row, col) in a row-major BF16 tile with row stride LD
+// whose 16-byte chunks are XOR-swizzled (the XOR touches col bits 3..5 only).
+// LD = 64 (128-byte rows, no padding): chunk ^ ((row & 7) ^ (bit 3 of row
+// moved to bit 1)).  Padded strides (LD = width + 8): chunk ^ (bit 3 of row).
+// Either way any 8 consecutive rows, and the row sets {0,1,4,5,8,9,12,13} and
+// {2,3,6,7,10,11,14,15} that perm() visits, hit 8 different bank groups.
 template <int LD>
 __device__ __forceinline__ int swz(int row, int col) {
+  if (LD == 64) return row * 64 + (col ^ ((((row & 7) ^ ((row >> 2) & 2))) << 3));
   return row * LD + (col ^ ((row & 8) << 1));
 }
 
@@ -147,7 +154,7 @@ struct Stage {  // raw inputs of one chunk
 };
 struct Smem {
   Stage st[2];
-  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, tok, dzs, mvb, mzp, mop, qbs, kbs, red, tm;
+  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, tok, mvb, mzp, mop, qbs, kbs, red, tm;
   uint32_t xch;  // state exchange: the cluster fold (state kernel), the entering state (output kernel)
   uint32_t total;
 };
@@ -180,14 +187,13 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
     L.st[s].seg = need_out ? take(K::C * K::C * 4) : 0;
     L.st[s].bytes = o - base;
   }
-  L.Ks = out_kernel ? take(K::CR * K::LDN * 2) : 0;
-  L.Kst = take(K::CR * K::LDN * 2);
+  L.Ks = (out_kernel && !K::ALIAS_K) ? take(K::CR * K::LDN * 2) : 0;
+  L.Kst = K::ALIAS_K ? 0 : take(K::CR * K::LDN * 2);
   L.Psi = take(K::CR * K::LDP * 2);
   L.Sb = out_kernel ? take(K::N * K::LDP * 2) : 0;
   L.qkd = out_kernel ? take(K::C * K::R * K::R * 4) : 0;
   L.eseg = need_out ? take(K::C * K::C * 4) : 0;
   L.tok = take(2 * (K::C * 4 * 4 + 16));
-  L.dzs = (need_out && has_z) ? take(K::C * K::LDP * 2) : 0;
   L.mvb = take(K::R * K::P * 2);
   L.mzp = (need_out && has_z) ? take(K::R * K::NMT * 8 * 8) : 0;
   L.mop = (need_out && reduced) ? take(K::R * K::NMT * 8 * 4) : 0;
@@ -235,7 +241,7 @@ __device__ void load_stage(const Params& p, const Stage& S, unsigned char* sm, i
     const int t = e / GP, gr = e % GP, tg = t0 + t;
     const bool ok = tg < p.S;
     const int64_t off = (((int64_t)b * p.S + (ok ? tg : 0)) * p.H + h) * K::P + gr * 8;
-    const uint32_t so = (t * K::LDP + gr * 8) * 2;
+    const uint32_t so = swz<K::LDP>(t, gr * 8) * 2;
     cp16(sm + S.v + so, p.v + off, ok);
     if (need_out && p.reduced) cp16(sm + S.dout + so, p.dout + off, ok);
     if (need_out && p.has_z) cp16(sm + S.z + so, p.z + off, ok);
@@ -247,7 +253,7 @@ __device__ void load_stage(const Params& p, const Stage& S, unsigned char* sm, i
       const bool ok = tg < p.S;
       const int64_t off =
           ((((int64_t)b * p.S + (ok ? tg : 0)) * K::R + r) * p.H + h) * K::P + gr * 8;
-      cp16(sm + S.dout + (j * K::LDP + gr * 8) * 2, p.dout + off, ok);
+      cp16(sm + S.dout + swz<K::LDP>(j, gr * 8) * 2, p.dout + off, ok);
     }
   }
   for (int e = threadIdx.x; e < K::C * GA; e += K::NT) {
@@ -432,7 +438,7 @@ __device__ __forceinline__ void psi_rows(const uint16_t* vraw, const uint16_t* m
   for (int it = 0; it < ROWS * GP / 32; it++) {
     const int q = lane + 32 * it, i = q / GP, gr = q % GP;
     const int j = j0 + i, tl = j / K::R, r = j % K::R;
-    const uint4 v = *reinterpret_cast<const uint4*>(vraw + tl * K::LDP + gr * 8);
+    const uint4 v = *reinterpret_cast<const uint4*>(vraw + swz<K::LDP>(tl, gr * 8));
     const uint4 m = *reinterpret_cast<const uint4*>(mvb + r * K::P + gr * 8);
     uint4 o;
     o.x = bmul2(v.x, m.x);
@@ -544,7 +550,7 @@ namespace fast {
 
 // Segment-local state sums (fast path of segment_state_kernel).
 template <class K>
-__global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
+__global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char sm[];
   const Smem L = smem_layout<K>(false, p.reduced, p.has_z);
   const int bh = blockIdx.x, unit = blockIdx.y;
@@ -555,7 +561,7 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j0 = warp * 16;
   const int pm = warp % K::NMT, nbase = (warp / K::NMT) * K::NCW;
-  uint16_t* Kst = reinterpret_cast<uint16_t*>(sm + L.Kst);
+  static_assert(K::ALIAS_K, "the state kernel runs one warp per j-block");
   uint16_t* Psi = reinterpret_cast<uint16_t*>(sm + L.Psi);
   float* tokb = reinterpret_cast<float*>(sm + L.tok);
   uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
@@ -572,14 +578,16 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
   float decay = 1.f;
   for (int c = c0; c < c1; c++) {
     const int s = (c - c0) & 1;
-    if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, false, false);
     const Stage S = stage_at(L.st[0], s);
-    cp_commit();
     float* tok = tokb + s * (4 * K::C + 4);
     token_scalars_regs<K>(p, scal, tok, c);
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
-    cp_wait<1>();
-    __syncthreads();  // (1) chunk c raw inputs and token scalars visible
+    cp_wait<0>();
+    __syncthreads();  // (1) chunk c raw inputs and token scalars visible; all warps past chunk c-1
+    // the other stage (chunk c-1's inputs and k_state) is free now
+    if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, false, false);
+    cp_commit();
+    uint16_t* const Kst = reinterpret_cast<uint16_t*>(sm + S.k);
     {
       uint32_t kf[K::NKT][4];
       load_rows<K>(kf, reinterpret_cast<const uint16_t*>(sm + S.k), j0);
@@ -587,6 +595,7 @@ __global__ void __launch_bounds__(K::NT) state_kernel(Params p) {
       rotate_direct<K, false>(kf, kf, reinterpret_cast<const float*>(sm + S.ang), j0);
       scale_k<K>(kf, reinterpret_cast<const uint32_t*>(tok) + K::C, j0);
       k_state<K>(kf, tok + 3 * K::C, j0);
+      __syncwarp();  // this warp's raw k rows are read before k_state overwrites them
       store_rows<K>(kf, Kst, j0);
       psi_rows<K>(reinterpret_cast<const uint16_t*>(sm + S.v), mvb, Psi, j0);
     }
@@ -714,7 +723,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // MODE >= 0 fixes the branches at compile time (bit 0: reduced dout, bit 1: z,
 // bit 2: d); MODE = -1 reads them from Params.
 template <class K, int MODE>
-__global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(Params p) {
+__global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 : 1))) output_kernel(Params p) {
   const bool RED = MODE >= 0 ? (MODE & 1) != 0 : p.reduced != 0;
   const bool HZ = MODE >= 0 ? (MODE & 2) != 0 : p.has_z != 0;
   const bool HD = MODE >= 0 ? (MODE & 4) != 0 : p.has_d != 0;
@@ -731,14 +740,13 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
   const int jw = warp % K::NWJ, half = warp / K::NWJ;  // j-block, p-block group
   const int j0 = jw * 16, mt0 = half * NMTH;
   const int pm = warp % NMT, nbase = (warp / NMT) * K::NCW;
-  uint16_t* Ks = reinterpret_cast<uint16_t*>(sm + L.Ks);
-  uint16_t* Kst = reinterpret_cast<uint16_t*>(sm + L.Kst);
+  uint16_t* Ks_sep = reinterpret_cast<uint16_t*>(sm + L.Ks);   // unused when ALIAS_K
+  uint16_t* Kst_sep = reinterpret_cast<uint16_t*>(sm + L.Kst);
   uint16_t* Psi = reinterpret_cast<uint16_t*>(sm + L.Psi);
   uint16_t* Sb = reinterpret_cast<uint16_t*>(sm + L.Sb);
   uint32_t* qkd = reinterpret_cast<uint32_t*>(sm + L.qkd);
   float* eseg = reinterpret_cast<float*>(sm + L.eseg);
   float* tokb = reinterpret_cast<float*>(sm + L.tok);
-  uint16_t* dzs = reinterpret_cast<uint16_t*>(sm + L.dzs);
   uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
   float2* mzp = reinterpret_cast<float2*>(sm + L.mzp);
   uint32_t* mop = reinterpret_cast<uint32_t*>(sm + L.mop);
@@ -839,6 +847,8 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
   for (int c = c0; c < c1; c++) {
     const int s = (c - c0) & 1;
     const Stage S = stage_at(L.st[0], s);
+    uint16_t* const Ks = K::ALIAS_K ? reinterpret_cast<uint16_t*>(sm + S.k) : Ks_sep;
+    uint16_t* const Kst = K::ALIAS_K ? reinterpret_cast<uint16_t*>(sm + S.q) : Kst_sep;
     if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, true, need_out);
     cp_commit();
     float* tok = tokb + s * (4 * C + 4);
@@ -887,6 +897,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
       }
       rotate_direct<K, true>(qf, kf, reinterpret_cast<const float*>(sm + S.ang), j0);
       scale_k<K>(kf, facd, j0);
+      if (K::ALIAS_K) __syncwarp();  // raw q / k rows read before they are overwritten
       if (half == 0) {
         store_rows<K>(kf, Ks, j0);
       }
@@ -905,7 +916,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
       const uint32_t r1 = pack2(make_float2(st[2 * nn][2], st[2 * nn][3]));
       const uint32_t r2 = pack2(make_float2(st[2 * nn + 1][0], st[2 * nn + 1][1]));
       const uint32_t r3 = pack2(make_float2(st[2 * nn + 1][2], st[2 * nn + 1][3]));
-      stsm_x4_t(Sb + (nbase + nn * 16 + (mi >> 1) * 8 + li) * LDP + pm * 16 + (mi & 1) * 8, r0, r1, r2, r3);
+      stsm_x4_t(Sb + swz<LDP>(nbase + nn * 16 + (mi >> 1) * 8 + li, pm * 16 + (mi & 1) * 8), r0, r1, r2, r3);
     }
     if (need_out) {  // exp(segsum) below the diagonal (read after the barrier)
       const float* sg = reinterpret_cast<const float*>(sm + S.seg);
@@ -919,7 +930,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
       uint16_t* so = p.states + ((int64_t)bh * p.nc + c) * N * P;
       for (int e = threadIdx.x; e < N * GP; e += K::NT) {
         const int n = e / GP, gr = e % GP;
-        st_cs_16(so + n * P + gr * 8, *reinterpret_cast<const uint4*>(Sb + n * LDP + gr * 8));
+        st_cs_16(so + n * P + gr * 8, *reinterpret_cast<const uint4*>(Sb + swz<LDP>(n, gr * 8)));
       }
     }
 
@@ -934,7 +945,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
         for (int kt = 0; kt < K::NKT; kt++) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(a0, a1, a2, a3,
-                    Sb + (kt * 16 + (mi >> 1) * 8 + li) * LDP + (mt0 + mt) * 16 + (mi & 1) * 8);
+                    Sb + swz<LDP>(kt * 16 + (mi >> 1) * 8 + li, (mt0 + mt) * 16 + (mi & 1) * 8));
           mma16816(X[mt][0], a0, a1, a2, a3, qf[kt][0], qf[kt][2]);
           mma16816(X[mt][1], a0, a1, a2, a3, qf[kt][1], qf[kt][3]);
         }
@@ -1048,12 +1059,11 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
           float2 z2 = make_float2(0.f, 0.f), do2 = make_float2(0.f, 0.f);
           uint32_t dob = 0;
           if (HZ) {
-            const uint16_t* zr = zraw + tl * LDP + mt * 16 + g;
-            z2 = unpack2((uint32_t)zr[0] | ((uint32_t)zr[8] << 16));
+            z2 = unpack2((uint32_t)zraw[swz<LDP>(tl, mt * 16 + g)] |
+                         ((uint32_t)zraw[swz<LDP>(tl, mt * 16 + g + 8)] << 16));
           }
           if (RED) {
-            const uint16_t* dr = draw + tl * LDP + mt * 16 + g;
-            dob = (uint32_t)dr[0] | ((uint32_t)dr[8] << 16);
+            dob = (uint32_t)draw[swz<LDP>(tl, mt * 16 + g)] | ((uint32_t)draw[swz<LDP>(tl, mt * 16 + g + 8)] << 16);
             do2 = unpack2(dob);
           }
           float2 prodz[NS];
@@ -1091,8 +1101,10 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
                 cdmo[sl] = __ffma2_rn(of, do2, cdmo[sl]);
               }
             } else if (HZ) {
-              const uint16_t* dr = draw + (tl * R + o) * LDP + mt * 16 + g;
-              preb = bmul2((uint32_t)dr[0] | ((uint32_t)dr[8] << 16), ob);
+              const int jr = tl * R + o;
+              preb = bmul2((uint32_t)draw[swz<LDP>(jr, mt * 16 + g)] |
+                               ((uint32_t)draw[swz<LDP>(jr, mt * 16 + g + 8)] << 16),
+                           ob);
             }
             prodz[k] = make_float2(0.f, 0.f);
             if (HZ) {
@@ -1135,23 +1147,15 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 256 ? 2 : 1)) output_kernel(P
             const bool writer = (R == 8) ? ((cq & 1) != 0) : true;
             if (writer && tg < p.S) {
               const uint32_t v = pack2(acc);
-              dzs[tl * LDP + mt * 16 + g] = (uint16_t)(v & 0xffffu);
-              dzs[tl * LDP + mt * 16 + g + 8] = (uint16_t)(v >> 16);
+              uint16_t* dzp = p.dz + (((int64_t)b * p.S + tg) * p.H + h) * P + mt * 16 + g;
+              dzp[0] = (uint16_t)(v & 0xffffu);
+              dzp[8] = (uint16_t)(v >> 16);
             }
           }
         }
       }
     }
     __syncthreads();  // (4)
-    if (need_out && HZ) {
-      constexpr int GP = P / 8;
-      for (int e = threadIdx.x; e < C * GP; e += K::NT) {
-        const int t = e / GP, gr = e % GP, tg = c * C + t;
-        if (tg < p.S)
-          st_cs_16(p.dz + (((int64_t)b * p.S + tg) * p.H + h) * P + gr * 8,
-                   *reinterpret_cast<const uint4*>(dzs + t * LDP + gr * 8));
-      }
-    }
   }  // chunk loop
 
   // ---- end of segment: fixed-order sum of the dmimo_o / dmimo_z partials

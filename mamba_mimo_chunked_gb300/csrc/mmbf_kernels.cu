@@ -789,6 +789,7 @@ static thread_local int g_stage_count = 0;
 static thread_local cudaError_t g_stage_error = cudaSuccess;
 static thread_local int g_failed_stage = -1;  // kernel index of a failed launch
 static thread_local int g_variant = -1;       // kernel family of the last call
+static thread_local int g_plan[5] = {0, 0, 0, 0, 0};  // L, nseg, UA, LA, resident output CTAs
 static const char* const kStageNames[4] = {"segment_state", "segment_prefix", "chunk_output",
                                            "grad_reduce"};
 static const char* const kFastStageNames[2] = {"segment_state", "chunk_output"};
@@ -809,6 +810,10 @@ template <typename K>
 static cudaError_t ensure_smem(K kern, size_t smem, int* cached) {
   if ((int)smem <= *cached) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the whole unified L1 / shared array as shared memory, so occupancy
+  // queries and launches both see every CTA that fits
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) *cached = (int)smem;
   return e;
 }
@@ -870,11 +875,41 @@ static int& fast_state_smem_set() {
   return v;
 }
 
+// CTAs of `kern` (NT threads, `smem` dynamic bytes, `tmem_cols` tensor-memory
+// columns each) resident on one SM of device `dev`, from the function's
+// register count and the SM's limits: registers per scheduler (a warp's
+// registers rounded to 256), shared memory incl. the per-CTA reservation,
+// threads, CTAs, and the 512 tensor-memory columns.  (The runtime occupancy
+// query reports one CTA per SM for kernels that allocate tensor memory, which
+// is not what the hardware runs.)
+template <typename Kern>
+static int resident_ctas(Kern kern, int dev, int NT, size_t smem, int tmem_cols) {
+  cudaFuncAttributes fa;
+  int regs_sm = 0, smem_sm = 0, reserved = 0, thr_sm = 0, blk_sm = 0;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess ||
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  const int warps = (NT + 31) / 32;
+  const int regs_warp = ((std::max(fa.numRegs, 1) * 32 + 255) / 256) * 256;
+  const int warps_smsp = (regs_sm / 4) / regs_warp;
+  int n = std::min(4 * warps_smsp / warps, blk_sm);
+  n = std::min(n, (int)(smem_sm / (smem + fa.sharedSizeBytes + (size_t)reserved)));
+  n = std::min(n, thr_sm / NT);
+  if (tmem_cols > 0) n = std::min(n, 512 / tmem_cols);
+  return std::max(n, 1);
+}
+
 // Resident output-kernel CTAs on the current device (SMs x CTAs per SM), or a
 // GB300-sized default when no device can be queried.
 template <class K>
 static int fast_slots_of(const Params& p) {
-  int dev = 0, sms = 0, per_sm = 0;
+  int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
@@ -883,13 +918,39 @@ static int fast_slots_of(const Params& p) {
   const size_t smem = fast_out_smem<K>(p);
   if (ensure_smem(fast::output_kernel<K, -1>, smem, &fast_out_smem_set<K>()) != cudaSuccess)
     cudaGetLastError();
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fast::output_kernel<K, -1>, K::NT, smem) !=
-          cudaSuccess ||
-      per_sm < 1) {
+  return sms * resident_ctas(fast::output_kernel<K, -1>, dev, K::NT, smem, K::TM_COLS);
+}
+// Resident state-kernel CTAs on the current device.
+template <class K>
+static int fast_state_slots_of(const Params& p) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
-    per_sm = 1;
+    return 4 * 152;
   }
-  return sms * per_sm;
+  const size_t smem = fast_state_smem<K>(p);
+  if (ensure_smem(fast::state_kernel<StateCfg<K>>, smem, &fast_state_smem_set<K>()) != cudaSuccess)
+    cudaGetLastError();
+  return sms * resident_ctas(fast::state_kernel<StateCfg<K>>, dev, StateCfg<K>::NT, smem, 0);
+}
+static int fast_state_slots(const Params& p) {
+  static int cache[16][kNumFast];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = 0;
+  }
+  int* slot = (dev >= 0 && dev < 16) ? &cache[dev][p.fast] : nullptr;
+  if (slot && *slot > 0) return *slot;
+  int v;
+  switch (p.fast) {
+    case 0: v = fast_state_slots_of<FastA>(p); break;
+    case 1: v = fast_state_slots_of<FastB>(p); break;
+    default: v = fast_state_slots_of<FastC>(p); break;
+  }
+  if (slot) *slot = v;
+  return v;
 }
 static int fast_slots(const Params& p) {
   // cached per device and specialisation (the occupancy query is not free)
@@ -986,11 +1047,22 @@ static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduc
     p.nseg = (p.nc + p.L - 1) / p.L;
     // The state-sum kernel works on units of about L/UA chunks, the UA units
     // of a segment one thread-block cluster: more CTAs in flight, shorter
-    // chains.  Clusters of more than two CTAs measured slower (co-scheduling
-    // of the whole cluster leaves slots idle).
+    // chains.  UA minimises (waves x (chunks per unit + setup)) over the
+    // resident state CTAs; clusters of more than two CTAs measured slower
+    // (co-scheduling of the whole cluster leaves slots idle).
     const int64_t heads = (int64_t)p.B * p.H;
-    int ua = (int)std::max<int64_t>(1, std::min<int64_t>(2, (8 * 152 + heads * p.nseg - 1) / (heads * p.nseg)));
-    ua = std::min(ua, p.L);
+    const int64_t sslots = fast_state_slots(p);
+    int ua = 1;
+    double best = 1e300;
+    for (int u = 1; u <= std::min(2, p.L); u++) {
+      const int la = (p.L + u - 1) / u;
+      const int64_t ctas = heads * p.nseg * ((p.L + la - 1) / la);
+      const double cost = (double)((ctas + sslots - 1) / sslots) * (la + 2.0);
+      if (cost < best - 1e-9) {
+        best = cost;
+        ua = u;
+      }
+    }
     p.LA = (p.L + ua - 1) / ua;
     p.UA = (p.L + p.LA - 1) / p.LA;
     p.nunit = p.nseg * p.UA;
@@ -1210,6 +1282,7 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
       g_stage_error = cudaSuccess;
     }
     g_variant = p.fast;
+    g_plan[0] = p.L; g_plan[1] = p.nseg; g_plan[2] = p.UA; g_plan[3] = p.LA; g_plan[4] = fast_slots(p);
     if (e != cudaSuccess)
       return fail(MMBF_ERR_CUDA, "CUDA error in %s (fast %d, grid %d x %d/%d): %s",
                   g_failed_stage >= 0 ? g_stage_names[g_failed_stage] : "setup", p.fast, p.B * p.H,
@@ -1282,6 +1355,7 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
                 out_layout(p).total, cudaGetErrorString(e));
   g_launches = launches;
   g_variant = -1;
+  g_plan[0] = p.L; g_plan[1] = p.nseg; g_plan[2] = 1; g_plan[3] = p.L; g_plan[4] = 0;
   return MMBF_OK;
 }
 
@@ -1315,6 +1389,13 @@ const char* mamba_mimo_last_error(void) { return g_err; }
 int mamba_mimo_abi_version(void) { return MAMBA_MIMO_BWD_FWD_ABI_VERSION; }
 int mamba_mimo_last_launch_count(void) { return g_launches; }
 int mamba_mimo_last_kernel_variant(void) { return g_variant; }
+
+int mamba_mimo_last_plan(int* out, int n) {
+  if (!out || n < 0) return 0;
+  const int k = n < 5 ? n : 5;
+  for (int i = 0; i < k; i++) out[i] = g_plan[i];
+  return k;
+}
 
 void mamba_mimo_set_stage_events(void* const* events, int count) {
   g_stage_events = (events && count > 0) ? events : nullptr;
