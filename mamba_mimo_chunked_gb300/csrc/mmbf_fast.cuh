@@ -849,16 +849,17 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     const Stage S = stage_at(L.st[0], s);
     uint16_t* const Ks = K::ALIAS_K ? reinterpret_cast<uint16_t*>(sm + S.k) : Ks_sep;
     uint16_t* const Kst = K::ALIAS_K ? reinterpret_cast<uint16_t*>(sm + S.q) : Kst_sep;
-    if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, true, need_out);
-    cp_commit();
     float* tok = tokb + s * (4 * C + 4);
     const uint32_t* facd = reinterpret_cast<const uint32_t*>(tok) + C;
     const float* eda = tok + 2 * C;
     const float* edr = tok + 3 * C;
     token_scalars_regs<K>(p, scal, tok, c);
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
-    cp_wait<1>();
-    __syncthreads();  // (1) chunk c raw inputs and token scalars visible
+    cp_wait<0>();
+    __syncthreads();  // (1) chunk c raw inputs and token scalars visible; all warps past chunk c-1
+    // the other stage (chunk c-1's inputs, k_scaled, k_state) is free now
+    if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, true, need_out);
+    cp_commit();
 
     // ---- warp prologue: Q/K of this j-block, same-token qk_dot, rotary,
     //      k_scaled / k_state tiles, PsiV rows, bf16(state) tile
@@ -1074,13 +1075,13 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
           for (int k = 0; k < NS; k++) {
             const int o = oo[k], nt = nto[k], bb = bbo[k], sl = slo[k];
             // diagonal: rank-ordered BF16 products and sums, then * gamma, rounded
-            uint32_t dacc = 0u;
+            uint32_t dacc = bmul2(qrow[k][0], psiP[0]);
 #pragma unroll
-            for (int r = 0; r < R; r++) dacc = badd2(dacc, bmul2(qrow[k][r], psiP[r]));
+            for (int r = 1; r < R; r++) dacc = badd2(dacc, bmul2(qrow[k][r], psiP[r]));
             const float2 dg = unpack2(pack2(__fmul2_rn(unpack2(dacc), gam2)));
             // out = bf16(inter + intra + diag + d * PsiV)
             float2 x = __fadd2_rn(make_float2(X[mtl][nt][bb], X[mtl][nt][bb + 2]), dg);
-            if (HD) x = __fadd2_rn(x, __fmul2_rn(make_float2(dval, dval), unpack2(pso[k])));
+            if (HD) x = __ffma2_rn(make_float2(dval, dval), unpack2(pso[k]), x);
             const uint32_t ob = pack2(x);
             const float2 of = unpack2(ob);
             float2 pz = make_float2(0.f, 0.f), sg = make_float2(0.5f, 0.5f), mz = make_float2(0.f, 0.f);
@@ -1155,7 +1156,6 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
         }
       }
     }
-    __syncthreads();  // (4)
   }  // chunk loop
 
   // ---- end of segment: fixed-order sum of the dmimo_o / dmimo_z partials
