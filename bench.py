@@ -98,6 +98,28 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_tflops():
+    """Sustained dense bf16 tensor throughput of this machine's GPUs (the
+    output kernel runs inside a long step), or the fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured sustained"
+    except Exception:
+        return 1700.0, "fallback sustained"
+
+
+def algorithmic_flop(wl):
+    """Dense contraction FLOP per call, masked upper triangle not counted:
+    per chunk and (b,h), 4*CR*N*P (state GEMM + inter) + R^2*C*(C-1)*(N+P)
+    (strictly causal Q K^T and A PsiV) + 2*C*R^2*(N+P) (qk_dot + diagonal)."""
+    nc = -(-wl.S // wl.C)
+    CR = wl.C * wl.R
+    per = 4 * CR * wl.N * wl.P + wl.R ** 2 * wl.C * (wl.C - 1) * (wl.N + wl.P) \
+        + 2 * wl.C * wl.R ** 2 * (wl.N + wl.P)
+    return per * nc * wl.B * wl.H
+
+
 def profile_traffic():
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
@@ -324,6 +346,9 @@ def main():
     dom_ms = stage_ms[DOMINANT]
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
+    alg_flop = algorithmic_flop(wl)
+    tpeak, tpeak_kind = measured_bf16_tflops()
+    tflops = alg_flop / (dom_ms * 1e-3) / 1e12
     ms_per_step = elapsed_s * 1e3 / args.steps
     value = wl.B * wl.S * args.steps * world / elapsed_s
 
@@ -373,6 +398,9 @@ def main():
                      "kernel": DOMINANT, "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": peak_kind},
         "op_hbm_frac": alg_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
+        "tensor": {"achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
+                   "kernel": DOMINANT, "algorithmic_flop_per_launch": alg_flop,
+                   "peak_source": tpeak_kind, "path": "mma.sync m16n8k16 bf16"},
         "stage_ms": stage_ms,
         "gpu_launches": launches_per_call * args.steps,
         "e2e": e2e,

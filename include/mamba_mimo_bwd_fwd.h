@@ -83,7 +83,8 @@ typedef enum {
   MMBF_ERR_UNSUPPORTED = 3, /* allowed by the pages, outside this build's envelope */
   MMBF_ERR_ALIGN = 4,       /* a pointer is not aligned as required */
   MMBF_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than the size query says */
-  MMBF_ERR_CUDA = 6         /* a CUDA runtime error while enqueuing */
+  MMBF_ERR_CUDA = 6,        /* a CUDA runtime error while enqueuing */
+  MMBF_ERR_DEVICE_TIMEOUT = 7 /* a kernel's bounded wait ran out (see mamba_mimo_device_status) */
 } mmbf_status;
 
 /* Problem dimensions (see the symbol list above). */
@@ -176,6 +177,17 @@ void mamba_mimo_set_stage_events(void* const* events, int count);
  * used: -1 for the generic kernels (any shape of the envelope), k >= 0 for
  * the k-th shape-specialised family. */
 int mamba_mimo_last_kernel_variant(void);
+
+/* Failure detection for the last mamba_mimo_bwd_fwd call on this thread.
+ * Every wait inside the kernels (the shared-memory barriers that the TMA
+ * input loads complete) is bounded to about a second; when one runs out the
+ * kernel records an error word tagged with the call in the first bytes of
+ * the call's workspace, lets its copies in flight land, and returns early
+ * (its outputs are then incomplete).  This function synchronises `stream`,
+ * reads that word, and returns MMBF_OK or MMBF_ERR_DEVICE_TIMEOUT (message
+ * in mamba_mimo_last_error).  The workspace must still be valid.  MMBF_OK if
+ * no call has been made on this thread. */
+mmbf_status mamba_mimo_device_status(void* stream);
 
 /* Launch plan of the last successful mamba_mimo_bwd_fwd call on this thread
  * (diagnostic): writes min(n, 5) ints to out -- chunks per segment, segments

@@ -76,6 +76,8 @@ def load_library():
         lib.mamba_mimo_set_stage_events.restype = None
         lib.mamba_mimo_set_stage_events.argtypes = [ctypes.c_void_p, ctypes.c_int]
         lib.mamba_mimo_last_kernel_variant.restype = ctypes.c_int
+        lib.mamba_mimo_device_status.restype = ctypes.c_int
+        lib.mamba_mimo_device_status.argtypes = [ctypes.c_void_p]
         lib.mamba_mimo_last_plan.restype = ctypes.c_int
         lib.mamba_mimo_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         lib.mamba_mimo_stage_name.restype = ctypes.c_char_p
@@ -94,6 +96,17 @@ def last_kernel_variant() -> int:
     """-1 if the last call on this thread used the generic kernels, else the
     index of the shape-specialised kernel family it used."""
     return load_library().mamba_mimo_last_kernel_variant()
+
+
+def device_status(stream=None) -> None:
+    """Synchronise the stream and raise if a bounded wait inside a kernel of
+    this thread's last call ran out (its outputs are then incomplete)."""
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    st = lib.mamba_mimo_device_status(ctypes.c_void_p(stream))
+    if st:
+        _raise(lib, st)
 
 
 def last_plan() -> dict:

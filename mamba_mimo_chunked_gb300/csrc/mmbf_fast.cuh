@@ -40,6 +40,9 @@ struct Cfg {
   // one warp per j-block: k_scaled / k_state go over the warp's own rows of
   // the raw k / q stage tiles (output kernel), k_state over raw k (state kernel)
   static constexpr bool ALIAS_K = (SPLIT == 1);
+  // 128-byte rows: raw inputs arrive by TMA (tensor maps, 128-byte swizzle)
+  // into 1024-byte aligned stage tiles; other widths use cp.async
+  static constexpr bool TMA = (N == 64 && P == 64);
   static constexpr int WPM = NW / NMT;        // warps sharing one p-block of the state
   static constexpr int NCW = N / WPM;         // state columns (n) per warp
   static constexpr int NN8 = NCW / 8;         // n8 tiles of the state per warp
@@ -89,6 +92,71 @@ __device__ __forceinline__ int swz(int row, int col) {
   if (LD == 64) return row * 64 + (col ^ ((((row & 7) ^ ((row >> 2) & 2))) << 3));
   return row * LD + (col ^ ((row & 8) << 1));
 }
+
+// ---- mbarrier and bulk-copy (TMA) helpers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+// Wait for phase `parity` of the barrier for at most about a second; false
+// if it did not complete (the caller reports the error and stops).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+// Generic-proxy shared-memory writes before later async-proxy (TMA) writes
+// to the same bytes.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* map, int c0, int c1, int c2, int c3, int c4,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+      : "memory");
+}
+// Contiguous global -> shared copy (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Element offset of (row, col) in a [rows][64] BF16 tile written by a TMA
+// load with the 128-byte swizzle (tile base 1024-byte aligned): 16-byte
+// chunk ^ (row & 7).
+__device__ __forceinline__ int swz128(int row, int col) { return row * 64 + (col ^ ((row & 7) << 3)); }
 
 __device__ __forceinline__ void cp16(void* s, const void* g, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(s)), "l"(g),
@@ -156,6 +224,7 @@ struct Smem {
   Stage st[2];
   uint32_t Ks, Kst, Psi, Sb, qkd, eseg, tok, mvb, mzp, mop, qbs, kbs, red, tm;
   uint32_t xch;  // state exchange: the cluster fold (state kernel), the entering state (output kernel)
+  uint32_t mbar;  // two stage barriers (TMA loads)
   uint32_t total;
 };
 
@@ -200,6 +269,7 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   L.qbs = out_kernel ? take(K::R * K::N * 2) : 0;
   L.kbs = take(K::R * K::N * 2);
   L.tm = take(16);
+  L.mbar = take(16);
   // end-of-segment reduction scratch reuses the stage buffers when they fit
   const uint32_t red_bytes = need_out ? (uint32_t)K::NT * 2 * K::SLOTS * K::NMTH * 2 * 4 : 0;
   L.red = (red_bytes <= L.st[0].bytes + L.st[1].bytes) ? 0 : take(red_bytes);
@@ -213,8 +283,18 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
     const uint32_t x = (uint32_t)K::NT * K::NN8 * 16;
     L.xch = (x <= L.st[0].bytes + L.st[1].bytes) ? 0 : take(x);
   }
-  L.total = o;
+  // TMA kernels align the dynamic shared memory base to 1024 bytes at run time
+  L.total = o + (K::TMA ? 1024u : 0u);
   return L;
+}
+
+// Dynamic shared memory base of a kernel with layout K (1024-byte aligned for
+// TMA stage tiles; the layout's total includes the slack).
+template <class K>
+__device__ __forceinline__ unsigned char* smem_base(unsigned char* raw) {
+  if (!K::TMA) return raw;
+  const uint32_t a = smem_u32(raw);
+  return raw + (((a + 1023u) & ~1023u) - a);
 }
 
 }  // namespace fast
@@ -266,6 +346,42 @@ __device__ void load_stage(const Params& p, const Stage& S, unsigned char* sm, i
     const float* src = p.segsum + ((int64_t)bh * p.nc + c) * K::C * K::C;
     for (int e = threadIdx.x; e < K::C * K::C / 4; e += K::NT) cp16(sm + S.seg + e * 16, src + e * 4, true);
   }
+}
+
+// Raw inputs of chunk c -> stage buffer by TMA (issued by one thread): q, k
+// as [C*R][N] rows, v / z / reduced dout as [C][P], per-rank dout [C*R][P]
+// (128-byte swizzle), angles [C][W], segsum by a plain bulk copy.  Tokens
+// past S are zero-filled by the tensor maps' bounds (the reference's zero
+// padding).  The barrier completes when every byte has landed.
+template <class K>
+__device__ void load_stage_tma(const Params& p, const Stage& S, uint32_t sbase, uint32_t bar, int bh, int c,
+                               bool out_kernel, bool need_out) {
+  const int b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
+  const int t0 = c * K::C;
+  uint32_t bytes = K::CR * K::N * 2 + K::C * K::P * 2 + K::C * K::W * 4;
+  if (out_kernel) bytes += K::CR * K::N * 2;
+  if (need_out) bytes += (p.reduced ? K::C : K::CR) * K::P * 2 + K::C * K::C * 4;
+  if (need_out && p.has_z) bytes += K::C * K::P * 2;
+  mbar_expect_tx(bar, bytes);
+  if (out_kernel) tma_load_5d(sbase + S.q, &p.tm_q, 0, g, 0, t0, b, bar);
+  tma_load_5d(sbase + S.k, &p.tm_k, 0, g, 0, t0, b, bar);
+  tma_load_4d(sbase + S.v, &p.tm_v, 0, h, t0, b, bar);
+  if (need_out) {
+    if (p.reduced)
+      tma_load_4d(sbase + S.dout, &p.tm_dout, 0, h, t0, b, bar);
+    else
+      tma_load_5d(sbase + S.dout, &p.tm_dout, 0, h, 0, t0, b, bar);
+    if (p.has_z) tma_load_4d(sbase + S.z, &p.tm_z, 0, h, t0, b, bar);
+    bulk_load(sbase + S.seg, p.segsum + ((int64_t)bh * p.nc + c) * K::C * K::C, K::C * K::C * 4, bar);
+  }
+  tma_load_4d(sbase + S.ang, &p.tm_ang, 0, h, t0, b, bar);
+}
+
+// Offset of (row, col) in a raw BF16 stage tile: the TMA swizzle, or the
+// cp.async layout.
+template <class K, int LD>
+__device__ __forceinline__ int raw_off(int row, int col) {
+  return K::TMA ? swz128(row, col) : swz<LD>(row, col);
 }
 
 // dt, trap, da_cs, da_cs_rev of token c*C + threadIdx.x (threads 0..C; C is the
@@ -336,7 +452,7 @@ __device__ __forceinline__ void load_rows(uint32_t (&f)[K::NKT][4], const uint16
   const int r = j0 + perm<K::R>(lane & 15);
 #pragma unroll
   for (int kt = 0; kt < K::NKT; kt++)
-    ldsm_x4(f[kt][0], f[kt][1], f[kt][2], f[kt][3], tile + swz<K::LDN>(r, kt * 16 + (lane >> 4) * 8));
+    ldsm_x4(f[kt][0], f[kt][1], f[kt][2], f[kt][3], tile + raw_off<K, K::LDN>(r, kt * 16 + (lane >> 4) * 8));
 }
 template <class K>
 __device__ __forceinline__ void store_rows(const uint32_t (&f)[K::NKT][4], uint16_t* tile, int j0) {
@@ -438,7 +554,7 @@ __device__ __forceinline__ void psi_rows(const uint16_t* vraw, const uint16_t* m
   for (int it = 0; it < ROWS * GP / 32; it++) {
     const int q = lane + 32 * it, i = q / GP, gr = q % GP;
     const int j = j0 + i, tl = j / K::R, r = j % K::R;
-    const uint4 v = *reinterpret_cast<const uint4*>(vraw + swz<K::LDP>(tl, gr * 8));
+    const uint4 v = *reinterpret_cast<const uint4*>(vraw + raw_off<K, K::LDP>(tl, gr * 8));
     const uint4 m = *reinterpret_cast<const uint4*>(mvb + r * K::P + gr * 8);
     uint4 o;
     o.x = bmul2(v.x, m.x);
@@ -548,10 +664,52 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 namespace fast {
 
+// Stage pipeline of both kernels.  TMA kernels: thread 0 issues a chunk's
+// loads against the stage's barrier; every thread waits (bounded) on the
+// barrier's phase.  Otherwise: every thread issues cp.async, waits for its
+// own groups, and the next barrier publishes them.
+template <class K>
+__device__ __forceinline__ void stage_issue(const Params& p, const Smem& L, unsigned char* sm, int s, int bh, int c,
+                                            bool out_kernel, bool need_out) {
+  if (K::TMA) {
+    if (threadIdx.x == 0)
+      load_stage_tma<K>(p, stage_at(L.st[0], s), smem_u32(sm), smem_u32(sm) + L.mbar + 8 * s, bh, c, out_kernel,
+                        need_out);
+  } else {
+    load_stage<K>(p, stage_at(L.st[0], s), sm, bh, c, out_kernel, need_out);
+  }
+}
+// Chunk c of a CTA whose first chunk is c0 sits in stage (c - c0) & 1; its
+// barrier's phase parity is ((c - c0) >> 1) & 1.
+template <class K>
+__device__ __forceinline__ bool stage_wait(const Smem& L, unsigned char* sm, int c, int c0) {
+  if (K::TMA) return mbar_wait(smem_u32(sm) + L.mbar + 8 * ((c - c0) & 1), ((c - c0) >> 1) & 1);
+  cp_wait<0>();
+  return true;
+}
+template <class K>
+__device__ __forceinline__ void stage_init(const Smem& L, unsigned char* sm) {
+  if (K::TMA && threadIdx.x == 0) {
+    mbar_init(smem_u32(sm) + L.mbar, 1);
+    mbar_init(smem_u32(sm) + L.mbar + 8, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+}
+// After a barrier wait ran out: record the error (tagged with this call) and
+// give the copies in flight for chunk c a bounded time to land before the
+// shared memory is reused or released.
+template <class K>
+__device__ __forceinline__ void stage_abort(const Params& p, const Smem& L, unsigned char* sm, int c, int c0) {
+  if (K::TMA) (void)stage_wait<K>(L, sm, c, c0);
+  if (threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 1u);
+}
+
 // Segment-local state sums (fast path of segment_state_kernel).
 template <class K>
-__global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(Params p) {
-  extern __shared__ __align__(128) unsigned char sm[];
+__global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) unsigned char sm_raw[];
+  unsigned char* sm = smem_base<K>(sm_raw);
   const Smem L = smem_layout<K>(false, p.reduced, p.has_z);
   const int bh = blockIdx.x, unit = blockIdx.y;
   const int h = bh % p.H;
@@ -568,9 +726,10 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(Pa
   uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
 
   if (unit == 0 && threadIdx.x == 0) p.ws_count[bh] = 0u;  // read by this call's output kernel
-  param_tables<K>(p, h, mvb, nullptr, kbs);
-  if (c0 < c1) load_stage<K>(p, L.st[0], sm, bh, c0, false, false);
+  stage_init<K>(L, sm);
+  if (c0 < c1) stage_issue<K>(p, L, sm, 0, bh, c0, false, false);
   cp_commit();
+  param_tables<K>(p, h, mvb, nullptr, kbs);
   float4 scal = load_scalars<K>(p, bh, c0);
   float st[K::NN8][4];
 #pragma unroll
@@ -582,10 +741,14 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(Pa
     float* tok = tokb + s * (4 * K::C + 4);
     token_scalars_regs<K>(p, scal, tok, c);
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
-    cp_wait<0>();
-    __syncthreads();  // (1) chunk c raw inputs and token scalars visible; all warps past chunk c-1
+    const bool ok = stage_wait<K>(L, sm, c, c0);
+    if (K::TMA) fence_proxy_async();  // k_state written over stage rows precedes their refill
+    if (__syncthreads_or(!ok)) {  // (1) chunk c raw inputs, token scalars visible; all warps past c-1
+      stage_abort<K>(p, L, sm, c, c0);
+      break;
+    }
     // the other stage (chunk c-1's inputs and k_state) is free now
-    if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, false, false);
+    if (c + 1 < c1) stage_issue<K>(p, L, sm, s ^ 1, bh, c + 1, false, false);
     cp_commit();
     uint16_t* const Kst = reinterpret_cast<uint16_t*>(sm + S.k);
     {
@@ -723,13 +886,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 // MODE >= 0 fixes the branches at compile time (bit 0: reduced dout, bit 1: z,
 // bit 2: d); MODE = -1 reads them from Params.
 template <class K, int MODE>
-__global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 : 1))) output_kernel(Params p) {
+__global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 : 1)))
+    output_kernel(const __grid_constant__ Params p) {
   const bool RED = MODE >= 0 ? (MODE & 1) != 0 : p.reduced != 0;
   const bool HZ = MODE >= 0 ? (MODE & 2) != 0 : p.has_z != 0;
   const bool HD = MODE >= 0 ? (MODE & 4) != 0 : p.has_d != 0;
   constexpr int R = K::R, C = K::C, N = K::N, P = K::P, NMT = K::NMT, NMTH = K::NMTH, LDN = K::LDN,
                 LDP = K::LDP;
-  extern __shared__ __align__(128) unsigned char sm[];
+  extern __shared__ __align__(128) unsigned char sm_raw[];
+  unsigned char* sm = smem_base<K>(sm_raw);
   const bool need_out = RED || HZ;
   const Smem L = smem_layout<K>(true, RED, HZ);
   const int bh = blockIdx.x, seg = blockIdx.y;
@@ -753,7 +918,10 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
   uint16_t* qbs = reinterpret_cast<uint16_t*>(sm + L.qbs);
   uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
 
-  // ---- once per CTA: parameters of head h, first chunk's inputs in flight
+  // ---- once per CTA: first chunk's inputs in flight, parameters of head h
+  stage_init<K>(L, sm);
+  stage_issue<K>(p, L, sm, 0, bh, c0, true, need_out);
+  cp_commit();
   param_tables<K>(p, h, mvb, qbs, kbs);
   if (need_out && HZ)
     for (int e = threadIdx.x; e < R * NMT * 8; e += K::NT) {
@@ -784,8 +952,6 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
   const uint32_t tm_alloc = *tm_slot;
   const uint32_t tm_st = tm_alloc + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * K::TM_WARP);
   const uint32_t tm_dm = tm_st + K::TM_ST;
-  load_stage<K>(p, L.st[0], sm, bh, c0, true, need_out);
-  cp_commit();
   float4 scal = load_scalars<K>(p, bh, c0);
 
   // ---- entering state of the segment (written by the prefix kernel)
@@ -855,10 +1021,14 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     const float* edr = tok + 3 * C;
     token_scalars_regs<K>(p, scal, tok, c);
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
-    cp_wait<0>();
-    __syncthreads();  // (1) chunk c raw inputs and token scalars visible; all warps past chunk c-1
+    const bool ok = stage_wait<K>(L, sm, c, c0);
+    if (K::TMA) fence_proxy_async();  // k_scaled / k_state over stage rows precede their refill
+    if (__syncthreads_or(!ok)) {  // (1) chunk c raw inputs, token scalars visible; all warps past c-1
+      stage_abort<K>(p, L, sm, c, c0);
+      break;
+    }
     // the other stage (chunk c-1's inputs, k_scaled, k_state) is free now
-    if (c + 1 < c1) load_stage<K>(p, stage_at(L.st[0], s ^ 1), sm, bh, c + 1, true, need_out);
+    if (c + 1 < c1) stage_issue<K>(p, L, sm, s ^ 1, bh, c + 1, true, need_out);
     cp_commit();
 
     // ---- warp prologue: Q/K of this j-block, same-token qk_dot, rotary,
@@ -1060,11 +1230,12 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
           float2 z2 = make_float2(0.f, 0.f), do2 = make_float2(0.f, 0.f);
           uint32_t dob = 0;
           if (HZ) {
-            z2 = unpack2((uint32_t)zraw[swz<LDP>(tl, mt * 16 + g)] |
-                         ((uint32_t)zraw[swz<LDP>(tl, mt * 16 + g + 8)] << 16));
+            z2 = unpack2((uint32_t)zraw[raw_off<K, LDP>(tl, mt * 16 + g)] |
+                         ((uint32_t)zraw[raw_off<K, LDP>(tl, mt * 16 + g + 8)] << 16));
           }
           if (RED) {
-            dob = (uint32_t)draw[swz<LDP>(tl, mt * 16 + g)] | ((uint32_t)draw[swz<LDP>(tl, mt * 16 + g + 8)] << 16);
+            dob = (uint32_t)draw[raw_off<K, LDP>(tl, mt * 16 + g)] |
+                  ((uint32_t)draw[raw_off<K, LDP>(tl, mt * 16 + g + 8)] << 16);
             do2 = unpack2(dob);
           }
           float2 prodz[NS];
@@ -1103,8 +1274,8 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
               }
             } else if (HZ) {
               const int jr = tl * R + o;
-              preb = bmul2((uint32_t)draw[swz<LDP>(jr, mt * 16 + g)] |
-                               ((uint32_t)draw[swz<LDP>(jr, mt * 16 + g + 8)] << 16),
+              preb = bmul2((uint32_t)draw[raw_off<K, LDP>(jr, mt * 16 + g)] |
+                               ((uint32_t)draw[raw_off<K, LDP>(jr, mt * 16 + g + 8)] << 16),
                            ob);
             }
             prodz[k] = make_float2(0.f, 0.f);

@@ -40,6 +40,8 @@
 // reference's FP32-op-then-round steps bit for bit.
 
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -49,6 +51,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "mamba_mimo_bwd_fwd.h"
@@ -156,6 +159,12 @@ struct Params {
   uint16_t *states, *dz, *qk_dot;
   float *ws_state, *ws_decay, *ws_grad;
   unsigned int* ws_count;  // per (b,h): output CTAs done (specialised kernels)
+  unsigned int* ws_err;    // device-side error word: (tag << 8) | code of the failing call
+  unsigned int tag;        // call tag (24 bits) for ws_err
+  // Tensor maps of the specialised kernels with 128-byte rows (TMA loads):
+  // q, k [N,G,R,S,B]; v, z, reduced dout [P,H,S,B]; per-rank dout
+  // [P,H,R,S,B]; angles [W,H,S,B].  Unused maps are left zero.
+  CUtensorMap tm_q, tm_k, tm_v, tm_dout, tm_z, tm_ang;
 };
 
 __host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
@@ -790,6 +799,18 @@ static thread_local cudaError_t g_stage_error = cudaSuccess;
 static thread_local int g_failed_stage = -1;  // kernel index of a failed launch
 static thread_local int g_variant = -1;       // kernel family of the last call
 static thread_local int g_plan[5] = {0, 0, 0, 0, 0};  // L, nseg, UA, LA, resident output CTAs
+static thread_local unsigned int g_last_tag = 0;           // tag of this thread's last call
+static thread_local const unsigned int* g_last_err_word = nullptr;
+// 24-bit call tags, never 0, so a stale or uninitialised error word is
+// unlikely to carry the tag of the call being checked.
+static unsigned int next_call_tag() {
+  static std::atomic<unsigned int> n{0};
+  unsigned int t;
+  do {
+    t = (n.fetch_add(1, std::memory_order_relaxed) + 1) & 0xffffffu;
+  } while (t == 0);
+  return t;
+}
 static const char* const kStageNames[4] = {"segment_state", "segment_prefix", "chunk_output",
                                            "grad_reduce"};
 static const char* const kFastStageNames[2] = {"segment_state", "chunk_output"};
@@ -1081,13 +1102,82 @@ static int ws_units(const Params& p) {
   const int Lg = (p.nc + ng - 1) / ng;
   return std::max(n, (p.nc + Lg - 1) / Lg);
 }
+// Workspace header: the device error word (first 4 bytes of 256).
+constexpr size_t kWsHeader = 256;
+
 static size_t workspace_bytes_of(const Params& p) {
   const int n = ws_units(p);
   const size_t st = align16((size_t)p.B * p.H * n * p.N * p.P * 4);
   const size_t dec = align16((size_t)p.B * p.H * n * 4);
   const size_t gr = align16((size_t)p.B * p.H * n * 2 * p.R * p.P * 4);
   const size_t cnt = align16((size_t)p.B * p.H * 4);
-  return st + dec + gr + cnt + 256;
+  return kWsHeader + st + dec + gr + cnt + 256;
+}
+
+// ---- tensor maps of the TMA kernels (cuTensorMapEncodeTiled through the
+// runtime's driver entry point; no link against the driver library)
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+// dims[0] innermost; strides[i] (bytes) of dims[i+1]; box[rank].
+static bool encode_map(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint32_t ones[5] = {1, 1, 1, 1, 1};
+  return enc(m, type, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, ones,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// The maps the TMA stage loads read (layouts as in Params); false if any
+// cannot be encoded (the call then takes the generic kernels).
+template <class K>
+static bool encode_stage_maps(Params& p) {
+  if (!K::TMA) return true;
+  const cuuint64_t B = p.B, S = p.S, H = p.H, G = p.G, R = p.R, N = p.N, P = p.P, W = p.w;
+  const cuuint32_t C = (cuuint32_t)K::C, Rb = (cuuint32_t)K::R;
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  {  // q, k [B,S,R,G,N]
+    const cuuint64_t d[5] = {N, G, R, S, B};
+    const cuuint64_t st[4] = {N * 2, G * N * 2, R * G * N * 2, S * R * G * N * 2};
+    const cuuint32_t box[5] = {(cuuint32_t)N, 1, Rb, C, 1};
+    if (!encode_map(&p.tm_q, bf, 5, p.q, d, st, box, true)) return false;
+    if (!encode_map(&p.tm_k, bf, 5, p.k, d, st, box, true)) return false;
+  }
+  {  // v, z, reduced dout [B,S,H,P]
+    const cuuint64_t d[4] = {P, H, S, B};
+    const cuuint64_t st[3] = {P * 2, H * P * 2, S * H * P * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)P, 1, C, 1};
+    if (!encode_map(&p.tm_v, bf, 4, p.v, d, st, box, true)) return false;
+    if (p.has_z && !encode_map(&p.tm_z, bf, 4, p.z, d, st, box, true)) return false;
+    if (p.dout && p.reduced && !encode_map(&p.tm_dout, bf, 4, p.dout, d, st, box, true)) return false;
+  }
+  if (p.dout && !p.reduced) {  // per-rank dout [B,S,R,H,P]
+    const cuuint64_t d[5] = {P, H, R, S, B};
+    const cuuint64_t st[4] = {P * 2, H * P * 2, R * H * P * 2, S * R * H * P * 2};
+    const cuuint32_t box[5] = {(cuuint32_t)P, 1, Rb, C, 1};
+    if (!encode_map(&p.tm_dout, bf, 5, p.dout, d, st, box, true)) return false;
+  }
+  {  // angles [B,S,H,W] fp32
+    const cuuint64_t d[4] = {W, H, S, B};
+    const cuuint64_t st[3] = {W * 4, H * W * 4, S * H * W * 4};
+    const cuuint32_t box[4] = {(cuuint32_t)W, 1, C, 1};
+    if (!encode_map(&p.tm_ang, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.angles, d, st, box, false)) return false;
+  }
+  return true;
 }
 
 template <int RMAX>
@@ -1256,6 +1346,8 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
   p.qk_dot = static_cast<uint16_t*>(qk_dot);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   const int wsn = ws_units(p);
+  p.ws_err = reinterpret_cast<unsigned int*>(ws);
+  ws += kWsHeader;
   p.ws_state = reinterpret_cast<float*>(ws);
   ws += align16((size_t)p.B * p.H * wsn * p.N * p.P * 4);
   p.ws_decay = reinterpret_cast<float*>(ws);
@@ -1268,9 +1360,18 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
   int launches = 0;
   cudaError_t e;
   cudaGetLastError();  // a stale error from elsewhere must not be reported as ours
-  const bool fast_ok = p.fast >= 0 && aligned16(q) && aligned16(k) && aligned16(v) &&
-                       aligned16(dout) && aligned16(z) && aligned16(angles) && aligned16(segsum) &&
-                       aligned16(states) && aligned16(dz);
+  p.tag = next_call_tag();
+  g_last_tag = p.tag;
+  g_last_err_word = p.ws_err;
+  bool fast_ok = p.fast >= 0 && aligned16(q) && aligned16(k) && aligned16(v) && aligned16(dout) &&
+                 aligned16(z) && aligned16(angles) && aligned16(segsum) && aligned16(states) && aligned16(dz);
+  if (fast_ok) {
+    switch (p.fast) {
+      case 0: fast_ok = encode_stage_maps<FastA>(p); break;
+      case 1: fast_ok = encode_stage_maps<FastB>(p); break;
+      default: fast_ok = encode_stage_maps<FastC>(p); break;
+    }
+  }
   if (fast_ok) {
     switch (p.fast) {
       case 0: e = launch_fast<FastA>(p, st, &launches); break;
@@ -1389,6 +1490,19 @@ const char* mamba_mimo_last_error(void) { return g_err; }
 int mamba_mimo_abi_version(void) { return MAMBA_MIMO_BWD_FWD_ABI_VERSION; }
 int mamba_mimo_last_launch_count(void) { return g_launches; }
 int mamba_mimo_last_kernel_variant(void) { return g_variant; }
+
+mmbf_status mamba_mimo_device_status(void* stream) {
+  if (!g_last_err_word) return MMBF_OK;
+  unsigned int w = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&w, g_last_err_word, sizeof w, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "reading the device status: %s", cudaGetErrorString(e));
+  if ((w >> 8) == g_last_tag && (w & 0xffu) != 0)
+    return fail(MMBF_ERR_DEVICE_TIMEOUT, "a kernel of the last call stopped: a shared-memory barrier wait ran out (code %u)",
+                w & 0xffu);
+  return MMBF_OK;
+}
 
 int mamba_mimo_last_plan(int* out, int n) {
   if (!out || n < 0) return 0;

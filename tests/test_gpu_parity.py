@@ -222,4 +222,16 @@ def test_all_outputs_written_with_z_and_reduced():
 
 def test_launch_count_reported():
     run_gpu(si.workload_inputs(0))
-    assert mm.last_launch_count() >= 3
+    assert mm.last_launch_count() >= 2
+
+
+def test_device_status_clean_after_calls():
+    # every wait inside the kernels is bounded; a completed call reports no timeout
+    for index in (0, 1):
+        run_gpu(si.workload_inputs(index))
+        mm.device_status()
+    wl = si.WORKLOADS[2]
+    inp = si.make_inputs(**wl.shape_kwargs(), seed=7, device="cuda")
+    mm.mamba_mimo_bwd_fwd(*si.args_of(inp))
+    assert mm.last_kernel_variant() == 0
+    mm.device_status()
