@@ -189,6 +189,14 @@ int mamba_mimo_last_kernel_variant(void);
  * no call has been made on this thread. */
 mmbf_status mamba_mimo_device_status(void* stream);
 
+/* Test hooks for this thread's later calls (0 = off, the default).  Bit 0:
+ * in the kernels that load their inputs by TMA, each CTA's first barrier
+ * expects 16 bytes more than its loads deliver, so its bounded wait runs
+ * out and the call reports MMBF_ERR_DEVICE_TIMEOUT through
+ * mamba_mimo_device_status.  Nothing faults or hangs; outputs of such a
+ * call are incomplete.  For tests of the failure path only. */
+void mamba_mimo_set_test_hooks(int flags);
+
 /* Launch plan of the last successful mamba_mimo_bwd_fwd call on this thread
  * (diagnostic): writes min(n, 5) ints to out -- chunks per segment, segments
  * per (b,h), state units per segment, chunks per unit, and the resident

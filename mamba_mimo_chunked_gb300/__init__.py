@@ -36,6 +36,7 @@ MMBF_ERRORS = {
     4: ValueError,          # alignment
     5: ValueError,          # workspace
     6: RuntimeError,        # CUDA
+    7: TimeoutError,        # a bounded wait inside a kernel ran out
 }
 
 
@@ -78,6 +79,8 @@ def load_library():
         lib.mamba_mimo_last_kernel_variant.restype = ctypes.c_int
         lib.mamba_mimo_device_status.restype = ctypes.c_int
         lib.mamba_mimo_device_status.argtypes = [ctypes.c_void_p]
+        lib.mamba_mimo_set_test_hooks.restype = None
+        lib.mamba_mimo_set_test_hooks.argtypes = [ctypes.c_int]
         lib.mamba_mimo_last_plan.restype = ctypes.c_int
         lib.mamba_mimo_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         lib.mamba_mimo_stage_name.restype = ctypes.c_char_p

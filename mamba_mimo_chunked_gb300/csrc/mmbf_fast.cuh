@@ -355,13 +355,16 @@ __device__ void load_stage(const Params& p, const Stage& S, unsigned char* sm, i
 // padding).  The barrier completes when every byte has landed.
 template <class K>
 __device__ void load_stage_tma(const Params& p, const Stage& S, uint32_t sbase, uint32_t bar, int bh, int c,
-                               bool out_kernel, bool need_out) {
+                               bool out_kernel, bool need_out, bool first) {
   const int b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
   const int t0 = c * K::C;
   uint32_t bytes = K::CR * K::N * 2 + K::C * K::P * 2 + K::C * K::W * 4;
   if (out_kernel) bytes += K::CR * K::N * 2;
   if (need_out) bytes += (p.reduced ? K::C : K::CR) * K::P * 2 + K::C * K::C * 4;
   if (need_out && p.has_z) bytes += K::C * K::P * 2;
+  // test hook 1: each CTA's first chunk expects 16 bytes that never arrive,
+  // so its bounded wait runs out (exercises the failure path; nothing faults)
+  if (first && (p.test_flags & 1)) bytes += 16;
   mbar_expect_tx(bar, bytes);
   if (out_kernel) tma_load_5d(sbase + S.q, &p.tm_q, 0, g, 0, t0, b, bar);
   tma_load_5d(sbase + S.k, &p.tm_k, 0, g, 0, t0, b, bar);
@@ -670,11 +673,11 @@ namespace fast {
 // own groups, and the next barrier publishes them.
 template <class K>
 __device__ __forceinline__ void stage_issue(const Params& p, const Smem& L, unsigned char* sm, int s, int bh, int c,
-                                            bool out_kernel, bool need_out) {
+                                            bool out_kernel, bool need_out, bool first = false) {
   if (K::TMA) {
     if (threadIdx.x == 0)
       load_stage_tma<K>(p, stage_at(L.st[0], s), smem_u32(sm), smem_u32(sm) + L.mbar + 8 * s, bh, c, out_kernel,
-                        need_out);
+                        need_out, first);
   } else {
     load_stage<K>(p, stage_at(L.st[0], s), sm, bh, c, out_kernel, need_out);
   }
@@ -727,7 +730,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
 
   if (unit == 0 && threadIdx.x == 0) p.ws_count[bh] = 0u;  // read by this call's output kernel
   stage_init<K>(L, sm);
-  if (c0 < c1) stage_issue<K>(p, L, sm, 0, bh, c0, false, false);
+  if (c0 < c1) stage_issue<K>(p, L, sm, 0, bh, c0, false, false, true);
   cp_commit();
   param_tables<K>(p, h, mvb, nullptr, kbs);
   float4 scal = load_scalars<K>(p, bh, c0);
@@ -920,7 +923,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
 
   // ---- once per CTA: first chunk's inputs in flight, parameters of head h
   stage_init<K>(L, sm);
-  stage_issue<K>(p, L, sm, 0, bh, c0, true, need_out);
+  stage_issue<K>(p, L, sm, 0, bh, c0, true, need_out, true);
   cp_commit();
   param_tables<K>(p, h, mvb, qbs, kbs);
   if (need_out && HZ)

@@ -161,6 +161,7 @@ struct Params {
   unsigned int* ws_count;  // per (b,h): output CTAs done (specialised kernels)
   unsigned int* ws_err;    // device-side error word: (tag << 8) | code of the failing call
   unsigned int tag;        // call tag (24 bits) for ws_err
+  int test_flags;          // test hooks (mamba_mimo_set_test_hooks); 0 in normal use
   // Tensor maps of the specialised kernels with 128-byte rows (TMA loads):
   // q, k [N,G,R,S,B]; v, z, reduced dout [P,H,S,B]; per-rank dout
   // [P,H,R,S,B]; angles [W,H,S,B].  Unused maps are left zero.
@@ -800,6 +801,7 @@ static thread_local int g_failed_stage = -1;  // kernel index of a failed launch
 static thread_local int g_variant = -1;       // kernel family of the last call
 static thread_local int g_plan[5] = {0, 0, 0, 0, 0};  // L, nseg, UA, LA, resident output CTAs
 static thread_local unsigned int g_last_tag = 0;           // tag of this thread's last call
+static thread_local int g_test_flags = 0;                  // mamba_mimo_set_test_hooks
 static thread_local const unsigned int* g_last_err_word = nullptr;
 // 24-bit call tags, never 0, so a stale or uninitialised error word is
 // unlikely to carry the tag of the call being checked.
@@ -1361,6 +1363,7 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
   cudaError_t e;
   cudaGetLastError();  // a stale error from elsewhere must not be reported as ours
   p.tag = next_call_tag();
+  p.test_flags = g_test_flags;
   g_last_tag = p.tag;
   g_last_err_word = p.ws_err;
   bool fast_ok = p.fast >= 0 && aligned16(q) && aligned16(k) && aligned16(v) && aligned16(dout) &&
@@ -1490,6 +1493,8 @@ const char* mamba_mimo_last_error(void) { return g_err; }
 int mamba_mimo_abi_version(void) { return MAMBA_MIMO_BWD_FWD_ABI_VERSION; }
 int mamba_mimo_last_launch_count(void) { return g_launches; }
 int mamba_mimo_last_kernel_variant(void) { return g_variant; }
+
+void mamba_mimo_set_test_hooks(int flags) { g_test_flags = flags; }
 
 mmbf_status mamba_mimo_device_status(void* stream) {
   if (!g_last_err_word) return MMBF_OK;

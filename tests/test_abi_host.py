@@ -126,3 +126,13 @@ def test_python_binding_invalid_q_dtype():
 def test_python_binding_requires_cuda_tensors():
     with pytest.raises(ValueError, match="CUDA tensors"):
         mm.mamba_mimo_bwd_fwd(*_unit_args())
+
+
+def test_device_status_without_a_call_is_ok(lib):
+    # nothing enqueued on this thread yet: no stream is touched
+    import threading
+    res = []
+    t = threading.Thread(target=lambda: res.append(lib.mamba_mimo_device_status(None)))
+    t.start()
+    t.join()
+    assert res == [0]
