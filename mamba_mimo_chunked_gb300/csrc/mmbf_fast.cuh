@@ -43,6 +43,9 @@ struct Cfg {
   // 128-byte rows: raw inputs arrive by TMA (tensor maps, 128-byte swizzle)
   // into 1024-byte aligned stage tiles; other widths use cp.async
   static constexpr bool TMA = (N == 64 && P == 64);
+  // ... and the state update on tcgen05.mma (M = P = 64, N = 64): PsiV and
+  // k_state in the 128-byte-swizzled layout the MMA reads
+  static constexpr bool UMMA = TMA;
   static constexpr int WPM = NW / NMT;        // warps sharing one p-block of the state
   static constexpr int NCW = N / WPM;         // state columns (n) per warp
   static constexpr int NN8 = NCW / 8;         // n8 tiles of the state per warp
@@ -54,7 +57,9 @@ struct Cfg {
   static constexpr int TM_DM = NMTH * 16;
   static constexpr int TM_WARP = TM_ST + TM_DM;
   static constexpr int TM_GROUPS = (NW + 3) / 4;
-  static constexpr int TM_NEED = TM_GROUPS * TM_WARP;
+  // UMMA: the state accumulator takes columns [0, 64) (M = 64 layout), the
+  // dmimo accumulators follow per column group
+  static constexpr int TM_NEED = (N == 64 && P == 64) ? 64 + TM_GROUPS * TM_DM : TM_GROUPS * TM_WARP;
   static constexpr int TM_COLS = TM_NEED <= 32 ? 32 : TM_NEED <= 64 ? 64 : TM_NEED <= 128 ? 128
                                  : TM_NEED <= 256 ? 256 : 512;
   static_assert(TM_NEED <= 512 && TM_ST % 8 == 0, "tensor memory budget");
@@ -76,6 +81,14 @@ __device__ __forceinline__ int perm(int i) {
   if (R == 4) return 4 * (cc >> 1) + 2 * nt + (cc & 1);
   if (R == 8) return 8 * (cc >> 2) + 4 * ((cc >> 1) & 1) + 2 * nt + (cc & 1);
   return i;
+}
+
+// Inverse of perm<R> on 0..15.
+template <int R>
+__device__ __forceinline__ int perm_inv(int r) {
+  if (R == 4) return ((r >> 1) & 1) * 8 + ((r >> 2) << 1) + (r & 1);
+  if (R == 8) return ((r >> 1) & 1) * 8 + ((r >> 3) << 2) + (((r >> 2) & 1) << 1) + (r & 1);
+  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -257,7 +270,9 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
     L.st[s].bytes = o - base;
   }
   L.Ks = (out_kernel && !K::ALIAS_K) ? take(K::CR * K::LDN * 2) : 0;
+  if (K::UMMA && !K::ALIAS_K) o = (o + 1023u) & ~1023u;
   L.Kst = K::ALIAS_K ? 0 : take(K::CR * K::LDN * 2);
+  if (K::UMMA) o = (o + 1023u) & ~1023u;
   L.Psi = take(K::CR * K::LDP * 2);
   L.Sb = out_kernel ? take(K::N * K::LDP * 2) : 0;
   L.qkd = out_kernel ? take(K::C * K::R * K::R * 4) : 0;
@@ -269,7 +284,7 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   L.qbs = out_kernel ? take(K::R * K::N * 2) : 0;
   L.kbs = take(K::R * K::N * 2);
   L.tm = take(16);
-  L.mbar = take(16);
+  L.mbar = take(24);  // stage 0, stage 1, MMA completion
   // end-of-segment reduction scratch reuses the stage buffers when they fit
   const uint32_t red_bytes = need_out ? (uint32_t)K::NT * 2 * K::SLOTS * K::NMTH * 2 * 4 : 0;
   L.red = (red_bytes <= L.st[0].bytes + L.st[1].bytes) ? 0 : take(red_bytes);
@@ -380,6 +395,25 @@ __device__ void load_stage_tma(const Params& p, const Stage& S, uint32_t sbase, 
   tma_load_4d(sbase + S.ang, &p.tm_ang, 0, h, t0, b, bar);
 }
 
+// Offset of (row, col) in the PsiV tile [C*R][P] and in k_state [C*R][N]:
+// the MMA operand layout (128-byte swizzle) or the padded layout.  In the
+// MMA layout each 16-row block is stored in fragment order (logical row
+// j0 + perm(i) at physical row j0 + i), so the perm() row sets that
+// fragment loads and stores visit are 8 consecutive rows (conflict-free);
+// the MMA's sum over rows is order-free as both operands use the same order.
+template <class K>
+__device__ __forceinline__ int op_row(int j) {
+  return K::UMMA ? ((j & ~15) | perm_inv<K::R>(j & 15)) : j;
+}
+template <class K>
+__device__ __forceinline__ int psi_off(int row, int col) {
+  return K::UMMA ? swz128(op_row<K>(row), col) : swz<K::LDP>(row, col);
+}
+template <class K>
+__device__ __forceinline__ int kst_off(int row, int col) {
+  return K::UMMA ? swz128(op_row<K>(row), col) : swz<K::LDN>(row, col);
+}
+
 // Offset of (row, col) in a raw BF16 stage tile: the TMA swizzle, or the
 // cp.async layout.
 template <class K, int LD>
@@ -457,13 +491,14 @@ __device__ __forceinline__ void load_rows(uint32_t (&f)[K::NKT][4], const uint16
   for (int kt = 0; kt < K::NKT; kt++)
     ldsm_x4(f[kt][0], f[kt][1], f[kt][2], f[kt][3], tile + raw_off<K, K::LDN>(r, kt * 16 + (lane >> 4) * 8));
 }
-template <class K>
+template <class K, bool KSTATE = false>
 __device__ __forceinline__ void store_rows(const uint32_t (&f)[K::NKT][4], uint16_t* tile, int j0) {
   const int lane = threadIdx.x & 31;
   const int r = j0 + perm<K::R>(lane & 15);
 #pragma unroll
   for (int kt = 0; kt < K::NKT; kt++)
-    stsm_x4(tile + swz<K::LDN>(r, kt * 16 + (lane >> 4) * 8), f[kt][0], f[kt][1], f[kt][2], f[kt][3]);
+    stsm_x4(tile + (KSTATE ? kst_off<K>(r, kt * 16 + (lane >> 4) * 8) : swz<K::LDN>(r, kt * 16 + (lane >> 4) * 8)),
+            f[kt][0], f[kt][1], f[kt][2], f[kt][3]);
 }
 
 // Fragment register (kt, e) holds row i = g + 8 (e & 1), columns
@@ -564,7 +599,7 @@ __device__ __forceinline__ void psi_rows(const uint16_t* vraw, const uint16_t* m
     o.y = bmul2(v.y, m.y);
     o.z = bmul2(v.z, m.z);
     o.w = bmul2(v.w, m.w);
-    *reinterpret_cast<uint4*>(Psi + swz<K::LDP>(j, gr * 8)) = o;
+    *reinterpret_cast<uint4*>(Psi + psi_off<K>(j, gr * 8)) = o;
   }
 }
 
@@ -584,12 +619,12 @@ __device__ __forceinline__ void state_mma(float (&st)[K::NN8][4], const uint16_t
 #pragma unroll
   for (int kb = 0; kb < K::NWJ; kb++) {
     uint32_t a0, a1, a2_, a3;
-    ldsm_x4_t(a0, a1, a2_, a3, Psi + swz<K::LDP>(kb * 16 + (mi >> 1) * 8 + li, pm * 16 + (mi & 1) * 8));
+    ldsm_x4_t(a0, a1, a2_, a3, Psi + psi_off<K>(kb * 16 + (mi >> 1) * 8 + li, pm * 16 + (mi & 1) * 8));
 #pragma unroll
     for (int nn = 0; nn < K::NN8 / 2; nn++) {
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(b0, b1, b2, b3,
-                Kst + swz<K::LDN>(kb * 16 + (mi & 1) * 8 + li, nbase + nn * 16 + (mi >> 1) * 8));
+                Kst + kst_off<K>(kb * 16 + (mi & 1) * 8 + li, nbase + nn * 16 + (mi >> 1) * 8));
       mma16816(st[2 * nn], a0, a1, a2_, a3, b0, b1);
       mma16816(st[2 * nn + 1], a0, a1, a2_, a3, b2, b3);
     }
@@ -660,6 +695,103 @@ __device__ __forceinline__ void tm_store_state(uint32_t taddr, const float (&st)
   tm_wait_st();
 }
 
+// ---- tcgen05.mma for the state update (kernels with 128-byte rows).
+// The FP32 state^T [P][N] is the accumulator of an M=64 MMA: its row m = 16w
+// + i sits in tensor-memory lane 32w + i, column n in column n, so a
+// tcgen05.ld / st of shape 16x256b gives warp w's threads their rows 16w..
+// 16w+15 in the mma.sync accumulator layout (rows g, g+8; columns 2c, 2c+1
+// of each 8-column group).
+template <int NN8>
+__device__ __forceinline__ void tm_ld_frag(uint32_t taddr, float (&st)[NN8][4]) {
+  static_assert(NN8 == 1 || NN8 == 2 || NN8 == 4 || NN8 == 8, "16x256b repetitions");
+  uint32_t r[NN8 * 4];
+  if constexpr (NN8 == 8) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+  } else if constexpr (NN8 == 4) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+  } else {
+#pragma unroll
+    for (int q = 0; q < NN8; q++)
+      asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];\n"
+                   : "=r"(r[4 * q]), "=r"(r[4 * q + 1]), "=r"(r[4 * q + 2]), "=r"(r[4 * q + 3])
+                   : "r"(taddr + 8 * q)
+                   : "memory");
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < NN8 * 4; i++) st[i / 4][i % 4] = __uint_as_float(r[i]);
+}
+template <int NN8>
+__device__ __forceinline__ void tm_st_frag(uint32_t taddr, const float (&st)[NN8][4]) {
+  static_assert(NN8 == 1 || NN8 == 2 || NN8 == 4 || NN8 == 8, "16x256b repetitions");
+  uint32_t r[NN8 * 4];
+#pragma unroll
+  for (int i = 0; i < NN8 * 4; i++) r[i] = __float_as_uint(st[i / 4][i % 4]);
+  if constexpr (NN8 == 8) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+  } else if constexpr (NN8 == 4) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+  } else {
+#pragma unroll
+    for (int q = 0; q < NN8; q++)
+      asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr + 8 * q),
+                   "r"(r[4 * q]), "r"(r[4 * q + 1]), "r"(r[4 * q + 2]), "r"(r[4 * q + 3])
+                   : "memory");
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+// Shared-memory matrix descriptor: MN-major operand stored as [K rows][64]
+// BF16 with the 128-byte swizzle (tile base 1024-byte aligned); 8-row groups
+// 1024 bytes apart along K.
+__device__ __forceinline__ uint64_t umma_desc_mn128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
+         ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+// D[64][64] (+)= A^T B over K = 16 * ksteps rows, A = [K][64] (A's M
+// contiguous), B = [K][64] (N contiguous), BF16 in, FP32 accumulate.  Issued
+// by one thread; completion is signalled on `bar` by tcgen05.commit.
+__device__ __forceinline__ void umma_64x64_mn(uint32_t tmem_d, uint32_t a_saddr, uint32_t b_saddr, int ksteps,
+                                              bool accumulate, uint32_t bar) {
+  constexpr uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((64u >> 3) << 17) |
+                             ((64u >> 4) << 24);
+  for (int ks = 0; ks < ksteps; ks++) {
+    const uint64_t da = umma_desc_mn128(a_saddr + ks * 2048), db = umma_desc_mn128(b_saddr + ks * 2048);
+    const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(da), "l"(db), "r"(idesc), "r"(acc)
+        : "memory");
+  }
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
@@ -708,6 +840,21 @@ __device__ __forceinline__ void stage_abort(const Params& p, const Smem& L, unsi
   if (threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 1u);
 }
 
+// state^T = state^T * alpha + U, U = the chunk's PsiV^T k_state read from
+// tensor memory (this warp's rows, 16x256b fragments).
+template <class K>
+__device__ __forceinline__ void fold_u(float (&st)[K::NN8][4], uint32_t taddr, float alpha) {
+  float u[K::NN8][4];
+  tm_ld_frag<K::NN8>(taddr, u);
+  const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+  for (int nn = 0; nn < K::NN8; nn++) {
+    const float2 x = __ffma2_rn(make_float2(st[nn][0], st[nn][1]), a2, make_float2(u[nn][0], u[nn][1]));
+    const float2 y = __ffma2_rn(make_float2(st[nn][2], st[nn][3]), a2, make_float2(u[nn][2], u[nn][3]));
+    st[nn][0] = x.x; st[nn][1] = x.y; st[nn][2] = y.x; st[nn][3] = y.y;
+  }
+}
+
 // Segment-local state sums (fast path of segment_state_kernel).
 template <class K>
 __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(const __grid_constant__ Params p) {
@@ -732,6 +879,28 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
   stage_init<K>(L, sm);
   if (c0 < c1) stage_issue<K>(p, L, sm, 0, bh, c0, false, false, true);
   cp_commit();
+  // UMMA: each chunk's U = PsiV^T k_state goes to tensor memory (64 columns,
+  // M = 64 layout) and is folded into the register state one chunk later
+  uint32_t tm_u = 0, tm_uw = 0;
+  const uint32_t bar_mma = smem_u32(sm) + L.mbar + 16;
+  if constexpr (K::UMMA) {
+    uint32_t* slot = reinterpret_cast<uint32_t*>(sm + L.tm);
+    if (warp == 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 64;\n" ::"r"(smem_u32(slot))
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+      mbar_init(bar_mma, 1);
+      mbar_fence_init();
+    }
+    tm_fence_before();
+    __syncthreads();
+    tm_fence_after();
+    tm_u = *slot;
+    tm_uw = tm_u + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)nbase;
+  }
+  int last_mma = -1;
   param_tables<K>(p, h, mvb, nullptr, kbs);
   float4 scal = load_scalars<K>(p, bh, c0);
   float st[K::NN8][4];
@@ -750,6 +919,13 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
       stage_abort<K>(p, L, sm, c, c0);
       break;
     }
+    if constexpr (K::UMMA) {
+      if (c > c0) {  // chunk c-1's U (its MMA has also finished reading PsiV and k_state)
+        if (!mbar_wait(bar_mma, (c - 1 - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
+        tm_fence_after();
+        fold_u<K>(st, tm_uw, chunk_decay<K>(p, tokb + ((c - 1 - c0) & 1) * (4 * K::C + 4), c - 1));
+      }
+    }
     // the other stage (chunk c-1's inputs and k_state) is free now
     if (c + 1 < c1) stage_issue<K>(p, L, sm, s ^ 1, bh, c + 1, false, false);
     cp_commit();
@@ -762,13 +938,33 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
       scale_k<K>(kf, reinterpret_cast<const uint32_t*>(tok) + K::C, j0);
       k_state<K>(kf, tok + 3 * K::C, j0);
       __syncwarp();  // this warp's raw k rows are read before k_state overwrites them
-      store_rows<K>(kf, Kst, j0);
+      store_rows<K, true>(kf, Kst, j0);
       psi_rows<K>(reinterpret_cast<const uint16_t*>(sm + S.v), mvb, Psi, j0);
     }
+    if (K::UMMA) fence_proxy_async();  // PsiV and k_state stores before the MMA reads them
     __syncthreads();  // (3)
     const float alpha = chunk_decay<K>(p, tok, c);
-    state_mma<K>(st, Psi, Kst, alpha, pm, nbase);
+    if constexpr (K::UMMA) {
+      if (threadIdx.x == 0) {
+        tm_fence_after();
+        umma_64x64_mn(tm_u, smem_u32(Psi), smem_u32(Kst), K::CR / 16, false, bar_mma);
+      }
+      last_mma = c;
+    } else {
+      state_mma<K>(st, Psi, Kst, alpha, pm, nbase);
+    }
     decay *= alpha;
+  }
+  if constexpr (K::UMMA) {  // the last chunk's U, then release the tensor memory
+    if (last_mma >= 0) {
+      if (!mbar_wait(bar_mma, (last_mma - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
+      tm_fence_after();
+      fold_u<K>(st, tm_uw, chunk_decay<K>(p, tokb + ((last_mma - c0) & 1) * (4 * K::C + 4), last_mma));
+    }
+    tm_fence_before();
+    __syncthreads();
+    if (warp == 0)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 64;\n" ::"r"(tm_u) : "memory");
   }
   // ---- segment sum.  The UA units of a segment run as one thread-block
   //      cluster; its last CTA folds the units' sums in unit order
@@ -953,8 +1149,18 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
   __syncthreads();
   tm_fence_after();
   const uint32_t tm_alloc = *tm_slot;
-  const uint32_t tm_st = tm_alloc + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * K::TM_WARP);
-  const uint32_t tm_dm = tm_st + K::TM_ST;
+  // UMMA: state accumulator in columns [0, 64) (this warp's rows at its lane
+  // quarter, columns nbase..), dmimo accumulators after it; otherwise each
+  // warp's state slice and accumulators side by side in its column group
+  const uint32_t tm_lane = (uint32_t)(32 * (warp & 3)) << 16;
+  const uint32_t tm_st = K::UMMA ? tm_alloc + tm_lane + (uint32_t)nbase
+                                 : tm_alloc + tm_lane + (uint32_t)((warp >> 2) * K::TM_WARP);
+  const uint32_t tm_dm = K::UMMA ? tm_alloc + tm_lane + 64u + (uint32_t)((warp >> 2) * K::TM_DM) : tm_st + K::TM_ST;
+  const uint32_t bar_mma = smem_u32(sm) + L.mbar + 16;
+  if (K::UMMA && threadIdx.x == 0) {
+    mbar_init(bar_mma, 1);
+    mbar_fence_init();
+  }
   float4 scal = load_scalars<K>(p, bh, c0);
 
   // ---- entering state of the segment (written by the prefix kernel)
@@ -1004,7 +1210,10 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
 #pragma unroll
       for (int e = 0; e < 4; e++)
         st[nn][e] = src[(nbase + nn * 8 + 2 * cq + (e & 1)) * P + pm * 16 + g + 8 * (e >> 1)];
-    tm_store_state<K>(tm_st, st);
+    if constexpr (K::UMMA)
+      tm_st_frag<K::NN8>(tm_st, st);
+    else
+      tm_store_state<K>(tm_st, st);
     const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < K::TM_DM / 8; q++) tm_st8(tm_dm + q * 8, zero8);
@@ -1012,6 +1221,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
   }
   __syncthreads();  // every thread has its entering state before stage 1 is refilled
   pdl_trigger();
+  int last_mma = -1;  // chunk whose state MMA is in flight (UMMA)
 
   for (int c = c0; c < c1; c++) {
     const int s = (c - c0) & 1;
@@ -1029,6 +1239,10 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     if (__syncthreads_or(!ok)) {  // (1) chunk c raw inputs, token scalars visible; all warps past c-1
       stage_abort<K>(p, L, sm, c, c0);
       break;
+    }
+    if (K::UMMA && c > c0) {  // chunk c-1's state MMA has read PsiV and k_state
+      if (!mbar_wait(bar_mma, (c - 1 - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
+      tm_fence_after();
     }
     // the other stage (chunk c-1's inputs, k_scaled, k_state) is free now
     if (c + 1 < c1) stage_issue<K>(p, L, sm, s ^ 1, bh, c + 1, true, need_out);
@@ -1077,13 +1291,16 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       }
       if (half == K::SPLIT - 1) {
         k_state<K>(kf, edr, j0);
-        store_rows<K>(kf, Kst, j0);
+        store_rows<K, true>(kf, Kst, j0);
       }
     }
     psi_rows<K, 16 / K::SPLIT>(reinterpret_cast<const uint16_t*>(sm + S.v), mvb, Psi,
                                j0 + half * (16 / K::SPLIT));
     float st[K::NN8][4];
-    tm_load_state<K>(tm_st, st);
+    if constexpr (K::UMMA)
+      tm_ld_frag<K::NN8>(tm_st, st);
+    else
+      tm_load_state<K>(tm_st, st);
 #pragma unroll
     for (int nn = 0; nn < K::NN8 / 2; nn++) {
       const uint32_t r0 = pack2(make_float2(st[2 * nn][0], st[2 * nn][1]));
@@ -1092,12 +1309,29 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       const uint32_t r3 = pack2(make_float2(st[2 * nn + 1][2], st[2 * nn + 1][3]));
       stsm_x4_t(Sb + swz<LDP>(nbase + nn * 16 + (mi >> 1) * 8 + li, pm * 16 + (mi & 1) * 8), r0, r1, r2, r3);
     }
+    if constexpr (K::UMMA) {  // state^T * exp(da_cs[last]) back into the accumulator
+      const float2 a2 = make_float2(chunk_decay<K>(p, tok, c), chunk_decay<K>(p, tok, c));
+#pragma unroll
+      for (int nn = 0; nn < K::NN8; nn++) {
+        const float2 x = __fmul2_rn(make_float2(st[nn][0], st[nn][1]), a2);
+        const float2 y = __fmul2_rn(make_float2(st[nn][2], st[nn][3]), a2);
+        st[nn][0] = x.x; st[nn][1] = x.y; st[nn][2] = y.x; st[nn][3] = y.y;
+      }
+      tm_st_frag<K::NN8>(tm_st, st);
+      fence_proxy_async();  // PsiV and k_state stores before the MMA reads them
+      tm_fence_before();
+    }
     if (need_out) {  // exp(segsum) below the diagonal (read after the barrier)
       const float* sg = reinterpret_cast<const float*>(sm + S.seg);
       for (int e = threadIdx.x; e < C * C; e += K::NT)
         eseg[e] = ((e % C) < (e / C)) ? exp_fast(sg[e]) : 0.f;
     }
     __syncthreads();  // (3) Ks, Kst, PsiV, Sb, qkd, eseg complete
+    if (K::UMMA && threadIdx.x == 0) {  // state^T += PsiV^T k_state, asynchronous
+      tm_fence_after();
+      umma_64x64_mn(tm_alloc, smem_u32(Psi), smem_u32(Kst), K::CR / 16, true, bar_mma);
+    }
+    if (K::UMMA) last_mma = c;
 
     {  // states[c] = bf16(state entering chunk c)
       constexpr int GP = P / 8;
@@ -1169,16 +1403,18 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
 #pragma unroll
         for (int mt = 0; mt < NMTH; mt++) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(a0, a1, a2, a3, Psi + swz<LDP>(prow, (mt0 + mt) * 16 + (mi & 1) * 8));
+          ldsm_x4_t(a0, a1, a2, a3, Psi + psi_off<K>(prow, (mt0 + mt) * 16 + (mi & 1) * 8));
           mma16816(X[mt][0], a0, a1, a2, a3, bi[0][0], bi[0][1]);
           mma16816(X[mt][1], a0, a1, a2, a3, bi[1][0], bi[1][1]);
         }
       }
     }
     // state update: state^T = exp(da_cs[last]) state^T + PsiV^T k_state
-    tm_load_state<K>(tm_st, st);
-    state_mma<K>(st, Psi, Kst, chunk_decay<K>(p, tok, c), pm, nbase);
-    tm_store_state<K>(tm_st, st);
+    if (!K::UMMA) {
+      tm_load_state<K>(tm_st, st);
+      state_mma<K>(st, Psi, Kst, chunk_decay<K>(p, tok, c), pm, nbase);
+      tm_store_state<K>(tm_st, st);
+    }
 
     // ---- per-element epilogue on X^T (p-row pairs (p, p+8), four columns
     //      per thread).  Column slot (nt, bb) is row j0 + perm(nt*8 + 2c + bb).
@@ -1210,7 +1446,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
         for (int mtl = 0; mtl < NMTH; mtl++) {
           const int mt = mt0 + mtl;
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(a0, a1, a2, a3, Psi + swz<LDP>(j0 + perm<R>((mi >> 1) * 8 + li), mt * 16 + (mi & 1) * 8));
+          ldsm_x4_t(a0, a1, a2, a3, Psi + psi_off<K>(j0 + perm<R>((mi >> 1) * 8 + li), mt * 16 + (mi & 1) * 8));
           uint32_t pso[NS];
 #pragma unroll
           for (int k = 0; k < NS; k++) {
@@ -1331,6 +1567,10 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       }
     }
   }  // chunk loop
+  if (K::UMMA && last_mma >= 0) {  // the last state MMA completes before tensor memory is released
+    if (!mbar_wait(bar_mma, (last_mma - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
+    tm_fence_after();
+  }
 
   // ---- end of segment: fixed-order sum of the dmimo_o / dmimo_z partials
   float2 dmo[4][NMTH], dmz[4][NMTH];

@@ -955,7 +955,7 @@ static int fast_state_slots_of(const Params& p) {
   const size_t smem = fast_state_smem<K>(p);
   if (ensure_smem(fast::state_kernel<StateCfg<K>>, smem, &fast_state_smem_set<K>()) != cudaSuccess)
     cudaGetLastError();
-  return sms * resident_ctas(fast::state_kernel<StateCfg<K>>, dev, StateCfg<K>::NT, smem, 0);
+  return sms * resident_ctas(fast::state_kernel<StateCfg<K>>, dev, StateCfg<K>::NT, smem, K::UMMA ? 64 : 0);
 }
 static int fast_state_slots(const Params& p) {
   static int cache[16][kNumFast];
