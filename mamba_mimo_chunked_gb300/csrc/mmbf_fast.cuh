@@ -50,6 +50,10 @@ struct Cfg {
   static constexpr int NCW = N / WPM;         // state columns (n) per warp
   static constexpr int NN8 = NCW / 8;         // n8 tiles of the state per warp
   static constexpr int SLOTS = 4;             // X^T columns per thread: (tile nt, bit b)
+  // padded strides of small tables (bank spread): bias rows [R][N + 8] BF16,
+  // same-token qk_dot [C][R*R + QKP] words
+  static constexpr int LDB = N + 8;
+  static constexpr int QKS = R * R + (R * R % 32 == 16 ? 4 : (R * R % 32 == 0 ? 4 : 0));
   // Tensor memory of the output kernel, per warp: the FP32 state slice and
   // the dmimo_o / dmimo_z accumulators (16 columns per p-block).  Warps w and
   // w + 4 share a lane quarter and use different column groups.
@@ -275,14 +279,14 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   if (K::UMMA) o = (o + 1023u) & ~1023u;
   L.Psi = take(K::CR * K::LDP * 2);
   L.Sb = out_kernel ? take(K::N * K::LDP * 2) : 0;
-  L.qkd = out_kernel ? take(K::C * K::R * K::R * 4) : 0;
+  L.qkd = out_kernel ? take(K::C * K::QKS * 4) : 0;
   L.eseg = need_out ? take(K::C * K::C * 4) : 0;
   L.tok = take(2 * (K::C * 4 * 4 + 16));
   L.mvb = take(K::R * K::P * 2);
   L.mzp = (need_out && has_z) ? take(K::R * K::NMT * 8 * 8) : 0;
   L.mop = (need_out && reduced) ? take(K::R * K::NMT * 8 * 4) : 0;
-  L.qbs = out_kernel ? take(K::R * K::N * 2) : 0;
-  L.kbs = take(K::R * K::N * 2);
+  L.qbs = out_kernel ? take(K::R * K::LDB * 2) : 0;
+  L.kbs = take(K::R * K::LDB * 2);
   L.tm = take(16);
   L.mbar = take(24);  // stage 0, stage 1, MMA completion
   // end-of-segment reduction scratch reuses the stage buffers when they fit
@@ -517,7 +521,7 @@ __device__ __forceinline__ void add_bias(uint32_t (&f)[K::NKT][4], const uint16_
     const int r = frag_row<K>(e) % K::R;
 #pragma unroll
     for (int kt = 0; kt < K::NKT; kt++)
-      f[kt][e] = badd2(f[kt][e], *reinterpret_cast<const uint32_t*>(bias + r * K::N + kt * 16 + 8 * (e >> 1) + c2));
+      f[kt][e] = badd2(f[kt][e], *reinterpret_cast<const uint32_t*>(bias + r * K::LDB + kt * 16 + 8 * (e >> 1) + c2));
   }
 }
 
@@ -631,13 +635,14 @@ __device__ __forceinline__ void state_mma(float (&st)[K::NN8][4], const uint16_t
   }
 }
 
-// Parameter tables of head h: bf16(mimo_v) [R][P], bf16 biases [R][N].
+// Parameter tables of head h: bf16(mimo_v) [R][P], bf16 biases [R][N] (rows N + 8 apart).
 template <class K>
 __device__ void param_tables(const Params& p, int h, uint16_t* mvb, uint16_t* qbs, uint16_t* kbs) {
   for (int e = threadIdx.x; e < K::R * K::P; e += K::NT) mvb[e] = f_bf(p.mimo_v[(int64_t)h * K::R * K::P + e]);
   for (int e = threadIdx.x; e < K::R * K::N; e += K::NT) {
-    if (qbs) qbs[e] = f_bf(p.q_bias[(int64_t)h * K::R * K::N + e]);
-    kbs[e] = f_bf(p.k_bias[(int64_t)h * K::R * K::N + e]);
+    const int at = (e / K::N) * K::LDB + e % K::N;
+    if (qbs) qbs[at] = f_bf(p.q_bias[(int64_t)h * K::R * K::N + e]);
+    kbs[at] = f_bf(p.k_bias[(int64_t)h * K::R * K::N + e]);
   }
 }
 
@@ -1274,8 +1279,8 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
           if (pi / R == pi2 / R) {
             const int tl = (j0 + pi) / R, o = pi % R, s0 = pi2 % R;
             const float v0 = round_bf(qa[ht][2 * hh]), v1 = round_bf(qa[ht][2 * hh + 1]);
-            qkd[(tl * R + o) * R + s0] = dup_bf(v0);
-            qkd[(tl * R + o) * R + s0 + 1] = dup_bf(v1);
+            qkd[tl * K::QKS + o * R + s0] = dup_bf(v0);
+            qkd[tl * K::QKS + o * R + s0 + 1] = dup_bf(v1);
             const int tg = c * C + tl;
             if (tg < p.S)
               *reinterpret_cast<uint32_t*>(p.qk_dot + (((int64_t)bh * p.S + tg) * R + o) * R + s0) =
@@ -1441,7 +1446,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
 #pragma unroll
         for (int k = 0; k < NS; k++)
 #pragma unroll
-          for (int r = 0; r < R; r++) qrow[k][r] = qkd[(tl * R + oo[k]) * R + r];
+          for (int r = 0; r < R; r++) qrow[k][r] = qkd[tl * K::QKS + oo[k] * R + r];
 #pragma unroll
         for (int mtl = 0; mtl < NMTH; mtl++) {
           const int mt = mt0 + mtl;
