@@ -163,6 +163,18 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* map, int c
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
       : "memory");
 }
+// Shared -> global tile store through a tensor map (bulk async group).
+__device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// This thread's bulk stores have finished reading shared memory / completed.
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // Contiguous global -> shared copy (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
@@ -278,6 +290,7 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   L.Kst = K::ALIAS_K ? 0 : take(K::CR * K::LDN * 2);
   if (K::UMMA) o = (o + 1023u) & ~1023u;
   L.Psi = take(K::CR * K::LDP * 2);
+  if (K::TMA && out_kernel) o = (o + 1023u) & ~1023u;  // TMA store source
   L.Sb = out_kernel ? take(K::N * K::LDP * 2) : 0;
   L.qkd = out_kernel ? take(K::C * K::QKS * 4) : 0;
   L.eseg = need_out ? take(K::C * K::C * 4) : 0;
@@ -416,6 +429,13 @@ __device__ __forceinline__ int psi_off(int row, int col) {
 template <class K>
 __device__ __forceinline__ int kst_off(int row, int col) {
   return K::UMMA ? swz128(op_row<K>(row), col) : swz<K::LDN>(row, col);
+}
+
+// Offset of (n, p) in the BF16 state tile [N][P]: the TMA swizzle when it is
+// stored by TMA, else the conflict-free swizzle.
+template <class K>
+__device__ __forceinline__ int sb_off(int row, int col) {
+  return K::TMA ? swz128(row, col) : swz<K::LDP>(row, col);
 }
 
 // Offset of (row, col) in a raw BF16 stage tile: the TMA swizzle, or the
@@ -1241,6 +1261,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
     const bool ok = stage_wait<K>(L, sm, c, c0);
     if (K::TMA) fence_proxy_async();  // k_scaled / k_state over stage rows precede their refill
+    if (K::TMA && threadIdx.x == 0) tma_store_wait_read();  // chunk c-1's states store has read the state tile
     if (__syncthreads_or(!ok)) {  // (1) chunk c raw inputs, token scalars visible; all warps past c-1
       stage_abort<K>(p, L, sm, c, c0);
       break;
@@ -1312,7 +1333,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       const uint32_t r1 = pack2(make_float2(st[2 * nn][2], st[2 * nn][3]));
       const uint32_t r2 = pack2(make_float2(st[2 * nn + 1][0], st[2 * nn + 1][1]));
       const uint32_t r3 = pack2(make_float2(st[2 * nn + 1][2], st[2 * nn + 1][3]));
-      stsm_x4_t(Sb + swz<LDP>(nbase + nn * 16 + (mi >> 1) * 8 + li, pm * 16 + (mi & 1) * 8), r0, r1, r2, r3);
+      stsm_x4_t(Sb + sb_off<K>(nbase + nn * 16 + (mi >> 1) * 8 + li, pm * 16 + (mi & 1) * 8), r0, r1, r2, r3);
     }
     if constexpr (K::UMMA) {  // state^T * exp(da_cs[last]) back into the accumulator
       const float2 a2 = make_float2(chunk_decay<K>(p, tok, c), chunk_decay<K>(p, tok, c));
@@ -1338,12 +1359,14 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     }
     if (K::UMMA) last_mma = c;
 
-    {  // states[c] = bf16(state entering chunk c)
+    if constexpr (K::TMA) {  // states[c] = bf16(state entering chunk c): one tile store
+      if (threadIdx.x == 0) tma_store_2d(&p.tm_states, smem_u32(Sb), 0, (int)(((int64_t)bh * p.nc + c) * N));
+    } else {
       constexpr int GP = P / 8;
       uint16_t* so = p.states + ((int64_t)bh * p.nc + c) * N * P;
       for (int e = threadIdx.x; e < N * GP; e += K::NT) {
         const int n = e / GP, gr = e % GP;
-        st_cs_16(so + n * P + gr * 8, *reinterpret_cast<const uint4*>(Sb + swz<LDP>(n, gr * 8)));
+        st_cs_16(so + n * P + gr * 8, *reinterpret_cast<const uint4*>(Sb + sb_off<K>(n, gr * 8)));
       }
     }
 
@@ -1358,7 +1381,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
         for (int kt = 0; kt < K::NKT; kt++) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(a0, a1, a2, a3,
-                    Sb + swz<LDP>(kt * 16 + (mi >> 1) * 8 + li, (mt0 + mt) * 16 + (mi & 1) * 8));
+                    Sb + sb_off<K>(kt * 16 + (mi >> 1) * 8 + li, (mt0 + mt) * 16 + (mi & 1) * 8));
           mma16816(X[mt][0], a0, a1, a2, a3, qf[kt][0], qf[kt][2]);
           mma16816(X[mt][1], a0, a1, a2, a3, qf[kt][1], qf[kt][3]);
         }
@@ -1572,6 +1595,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       }
     }
   }  // chunk loop
+  if (K::TMA && threadIdx.x == 0) tma_store_wait_all();  // the states tile stores are complete
   if (K::UMMA && last_mma >= 0) {  // the last state MMA completes before tensor memory is released
     if (!mbar_wait(bar_mma, (last_mma - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
     tm_fence_after();

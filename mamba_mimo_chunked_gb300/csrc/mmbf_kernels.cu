@@ -166,6 +166,7 @@ struct Params {
   // q, k [N,G,R,S,B]; v, z, reduced dout [P,H,S,B]; per-rank dout
   // [P,H,R,S,B]; angles [W,H,S,B].  Unused maps are left zero.
   CUtensorMap tm_q, tm_k, tm_v, tm_dout, tm_z, tm_ang;
+  CUtensorMap tm_states;   // states as [B*H*nc*N][P] (TMA tile stores)
 };
 
 __host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
@@ -1172,6 +1173,12 @@ static bool encode_stage_maps(Params& p) {
     const cuuint64_t st[4] = {P * 2, H * P * 2, R * H * P * 2, S * R * H * P * 2};
     const cuuint32_t box[5] = {(cuuint32_t)P, 1, Rb, C, 1};
     if (!encode_map(&p.tm_dout, bf, 5, p.dout, d, st, box, true)) return false;
+  }
+  {  // states [B,H,nc,N,P] as rows of P
+    const cuuint64_t d[2] = {P, (cuuint64_t)p.B * p.H * p.nc * N};
+    const cuuint64_t st[1] = {P * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)P, (cuuint32_t)N};
+    if (!encode_map(&p.tm_states, bf, 2, p.states, d, st, box, true)) return false;
   }
   {  // angles [B,S,H,W] fp32
     const cuuint64_t d[4] = {W, H, S, B};
