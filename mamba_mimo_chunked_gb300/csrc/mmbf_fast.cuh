@@ -824,15 +824,21 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 namespace fast {
 
-// Stage pipeline of both kernels.  TMA kernels: thread 0 issues a chunk's
+// Single-thread duties sit on different warps, so no warp carries them all
+// into the barriers: warp 0 the token scalars, warp 1 the TMA loads, warp 2
+// the tcgen05.mma issue, warp 3 the states tile store (its bulk group).
+constexpr int kTmaThread = 32, kMmaThread = 64, kStoreThread = 96;
+
+// Stage pipeline of both kernels.  TMA kernels: one thread issues a chunk's
 // loads against the stage's barrier; every thread waits (bounded) on the
 // barrier's phase.  Otherwise: every thread issues cp.async, waits for its
 // own groups, and the next barrier publishes them.
 template <class K>
 __device__ __forceinline__ void stage_issue(const Params& p, const Smem& L, unsigned char* sm, int s, int bh, int c,
                                             bool out_kernel, bool need_out, bool first = false) {
+  static_assert(K::NT >= 128, "duty threads");
   if (K::TMA) {
-    if (threadIdx.x == 0)
+    if (threadIdx.x == kTmaThread)
       load_stage_tma<K>(p, stage_at(L.st[0], s), smem_u32(sm), smem_u32(sm) + L.mbar + 8 * s, bh, c, out_kernel,
                         need_out, first);
   } else {
@@ -970,7 +976,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
     __syncthreads();  // (3)
     const float alpha = chunk_decay<K>(p, tok, c);
     if constexpr (K::UMMA) {
-      if (threadIdx.x == 0) {
+      if (threadIdx.x == kMmaThread) {
         tm_fence_after();
         umma_64x64_mn(tm_u, smem_u32(Psi), smem_u32(Kst), K::CR / 16, false, bar_mma);
       }
@@ -1261,7 +1267,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
     const bool ok = stage_wait<K>(L, sm, c, c0);
     if (K::TMA) fence_proxy_async();  // k_scaled / k_state over stage rows precede their refill
-    if (K::TMA && threadIdx.x == 0) tma_store_wait_read();  // chunk c-1's states store has read the state tile
+    if (K::TMA && threadIdx.x == kStoreThread) tma_store_wait_read();  // chunk c-1's states store has read the tile
     if (__syncthreads_or(!ok)) {  // (1) chunk c raw inputs, token scalars visible; all warps past c-1
       stage_abort<K>(p, L, sm, c, c0);
       break;
@@ -1353,14 +1359,15 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
         eseg[e] = ((e % C) < (e / C)) ? exp_fast(sg[e]) : 0.f;
     }
     __syncthreads();  // (3) Ks, Kst, PsiV, Sb, qkd, eseg complete
-    if (K::UMMA && threadIdx.x == 0) {  // state^T += PsiV^T k_state, asynchronous
+    if (K::UMMA && threadIdx.x == kMmaThread) {  // state^T += PsiV^T k_state, asynchronous
       tm_fence_after();
       umma_64x64_mn(tm_alloc, smem_u32(Psi), smem_u32(Kst), K::CR / 16, true, bar_mma);
     }
     if (K::UMMA) last_mma = c;
 
     if constexpr (K::TMA) {  // states[c] = bf16(state entering chunk c): one tile store
-      if (threadIdx.x == 0) tma_store_2d(&p.tm_states, smem_u32(Sb), 0, (int)(((int64_t)bh * p.nc + c) * N));
+      if (threadIdx.x == kStoreThread)
+        tma_store_2d(&p.tm_states, smem_u32(Sb), 0, (int)(((int64_t)bh * p.nc + c) * N));
     } else {
       constexpr int GP = P / 8;
       uint16_t* so = p.states + ((int64_t)bh * p.nc + c) * N * P;
@@ -1595,7 +1602,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       }
     }
   }  // chunk loop
-  if (K::TMA && threadIdx.x == 0) tma_store_wait_all();  // the states tile stores are complete
+  if (K::TMA && threadIdx.x == kStoreThread) tma_store_wait_all();  // the states tile stores are complete
   if (K::UMMA && last_mma >= 0) {  // the last state MMA completes before tensor memory is released
     if (!mbar_wait(bar_mma, (last_mma - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
     tm_fence_after();
