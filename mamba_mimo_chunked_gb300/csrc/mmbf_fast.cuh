@@ -691,6 +691,32 @@ __device__ __forceinline__ void tm_st8(uint32_t taddr, const float (&v)[8]) {
                : "memory");
 }
 __device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+// 16 columns of this thread's lane: load issued now, registers valid only
+// after tm_ld16_wait on the same array; store without waiting.
+__device__ __forceinline__ void tm_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tm_ld16_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tm_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tm_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
 }
@@ -1480,6 +1506,9 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
 #pragma unroll
         for (int mtl = 0; mtl < NMTH; mtl++) {
           const int mt = mt0 + mtl;
+          // this p-block's running dmimo partials: load now, used at the end of the block
+          uint32_t dmv[16];
+          tm_ld16_issue(tm_dm + mtl * 16, dmv);
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(a0, a1, a2, a3, Psi + psi_off<K>(j0 + perm<R>((mi >> 1) * 8 + li), mt * 16 + (mi & 1) * 8));
           uint32_t pso[NS];
@@ -1563,22 +1592,15 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
             }
           }
           {  // this p-block's dmimo partials accumulate in tensor memory
-            float v[8];
-            tm_ld8(tm_dm + mtl * 16, v);
+            tm_ld16_wait(dmv);
 #pragma unroll
             for (int sl = 0; sl < 4; sl++) {
-              v[2 * sl] += cdmo[sl].x;
-              v[2 * sl + 1] += cdmo[sl].y;
+              dmv[2 * sl] = __float_as_uint(__uint_as_float(dmv[2 * sl]) + cdmo[sl].x);
+              dmv[2 * sl + 1] = __float_as_uint(__uint_as_float(dmv[2 * sl + 1]) + cdmo[sl].y);
+              dmv[8 + 2 * sl] = __float_as_uint(__uint_as_float(dmv[8 + 2 * sl]) + cdmz[sl].x);
+              dmv[8 + 2 * sl + 1] = __float_as_uint(__uint_as_float(dmv[8 + 2 * sl + 1]) + cdmz[sl].y);
             }
-            tm_st8(tm_dm + mtl * 16, v);
-            tm_ld8(tm_dm + mtl * 16 + 8, v);
-#pragma unroll
-            for (int sl = 0; sl < 4; sl++) {
-              v[2 * sl] += cdmz[sl].x;
-              v[2 * sl + 1] += cdmz[sl].y;
-            }
-            tm_st8(tm_dm + mtl * 16 + 8, v);
-            tm_wait_st();
+            tm_st16(tm_dm + mtl * 16, dmv);
           }
           if (HZ) {  // dz: BF16 running sum over the ranks in order
             float2 acc = make_float2(0.f, 0.f);
@@ -1601,6 +1623,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
         }
       }
     }
+    tm_wait_st();  // this chunk's dmimo partials are stored before the next chunk reloads them
   }  // chunk loop
   if (K::TMA && threadIdx.x == kStoreThread) tma_store_wait_all();  // the states tile stores are complete
   if (K::UMMA && last_mma >= 0) {  // the last state MMA completes before tensor memory is released
