@@ -171,6 +171,13 @@ __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int 
                : "memory");
   asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
 }
+__device__ __forceinline__ void tma_store_4d(const void* map, uint32_t src, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
 // This thread's bulk stores have finished reading shared memory / completed.
 __device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
@@ -1279,6 +1286,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
   __syncthreads();  // every thread has its entering state before stage 1 is refilled
   pdl_trigger();
   int last_mma = -1;  // chunk whose state MMA is in flight (UMMA)
+  int last_done = -1;  // last chunk whose epilogue completed
 
   for (int c = c0; c < c1; c++) {
     const int s = (c - c0) & 1;
@@ -1301,6 +1309,11 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     if (K::UMMA && c > c0) {  // chunk c-1's state MMA has read PsiV and k_state
       if (!mbar_wait(bar_mma, (c - 1 - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
       tm_fence_after();
+    }
+    // chunk c-1's dz (in its z tile) leaves by TMA before that stage is refilled
+    if (K::TMA && HZ && c > c0 && threadIdx.x == kTmaThread) {
+      tma_store_4d(&p.tm_dz, smem_u32(sm) + stage_at(L.st[0], s ^ 1).z, 0, h, (c - 1) * C, b);
+      tma_store_wait_read();
     }
     // the other stage (chunk c-1's inputs, k_scaled, k_state) is free now
     if (c + 1 < c1) stage_issue<K>(p, L, sm, s ^ 1, bh, c + 1, true, need_out);
@@ -1613,7 +1626,12 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
               if (cq & 1) acc = acc2;
             }
             const bool writer = (R == 8) ? ((cq & 1) != 0) : true;
-            if (writer && tg < p.S) {
+            if (K::TMA && writer) {  // over the z values this lane pair has read; stored by TMA
+              const uint32_t v = pack2(acc);
+              uint16_t* zw = const_cast<uint16_t*>(zraw);
+              zw[raw_off<K, LDP>(tl, mt * 16 + g)] = (uint16_t)(v & 0xffffu);
+              zw[raw_off<K, LDP>(tl, mt * 16 + g + 8)] = (uint16_t)(v >> 16);
+            } else if (writer && tg < p.S) {
               const uint32_t v = pack2(acc);
               uint16_t* dzp = p.dz + (((int64_t)b * p.S + tg) * p.H + h) * P + mt * 16 + g;
               dzp[0] = (uint16_t)(v & 0xffffu);
@@ -1624,6 +1642,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       }
     }
     tm_wait_st();  // this chunk's dmimo partials are stored before the next chunk reloads them
+    last_done = c;
   }  // chunk loop
   if (K::TMA && threadIdx.x == kStoreThread) tma_store_wait_all();  // the states tile stores are complete
   if (K::UMMA && last_mma >= 0) {  // the last state MMA completes before tensor memory is released
@@ -1643,6 +1662,14 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       tm_ld8(tm_dm + mt * 16 + 8, v);
 #pragma unroll
       for (int sl = 0; sl < 4; sl++) dmz[sl][mt] = make_float2(v[2 * sl], v[2 * sl + 1]);
+    }
+  }
+  if (K::TMA && HZ) {  // the last chunk's dz, before the stage memory is reused
+    fence_proxy_async();
+    __syncthreads();
+    if (threadIdx.x == kTmaThread && last_done >= 0) {
+      tma_store_4d(&p.tm_dz, smem_u32(sm) + stage_at(L.st[0], (last_done - c0) & 1).z, 0, h, last_done * C, b);
+      tma_store_wait_all();
     }
   }
   tm_fence_before();

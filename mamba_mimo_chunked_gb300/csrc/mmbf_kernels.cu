@@ -167,6 +167,7 @@ struct Params {
   // [P,H,R,S,B]; angles [W,H,S,B].  Unused maps are left zero.
   CUtensorMap tm_q, tm_k, tm_v, tm_dout, tm_z, tm_ang;
   CUtensorMap tm_states;   // states as [B*H*nc*N][P] (TMA tile stores)
+  CUtensorMap tm_dz;       // dz [P,H,S,B] (TMA tile stores)
 };
 
 __host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
@@ -1166,6 +1167,7 @@ static bool encode_stage_maps(Params& p) {
     const cuuint32_t box[4] = {(cuuint32_t)P, 1, C, 1};
     if (!encode_map(&p.tm_v, bf, 4, p.v, d, st, box, true)) return false;
     if (p.has_z && !encode_map(&p.tm_z, bf, 4, p.z, d, st, box, true)) return false;
+    if (p.has_z && !encode_map(&p.tm_dz, bf, 4, p.dz, d, st, box, true)) return false;
     if (p.dout && p.reduced && !encode_map(&p.tm_dout, bf, 4, p.dout, d, st, box, true)) return false;
   }
   if (p.dout && !p.reduced) {  // per-rank dout [B,S,R,H,P]
