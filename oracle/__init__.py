@@ -15,6 +15,9 @@ layouts of the op document's output table:
     dz      [B,S,H,P]     | None     dmimo_z [B,H,R,P]  | None
     qk_dot  [B,H,S,R,R]              out [B,H,Sp,R,P]   (optional, never an
                                                           output of the op)
+
+and, on request, the layer's forward output y (``forward_y``), laid out like
+dout: [B,S,H,P] with mimo_o, [B,S,R,H,P] without.
 """
 
 from __future__ import annotations
@@ -88,14 +91,25 @@ def _ptr(a: np.ndarray | None):
 
 def bwd_fwd(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs,
             da_cs_rev, dt, trap, d, segsum, chunk_size=16, rotary_dim_divisor=4, *,
-            round_bf16: bool = True, pairs=None, want_out: bool = False) -> dict:
+            round_bf16: bool = True, pairs=None, want_out: bool = False, want_y: bool = False) -> dict:
     """Run the oracle.  Arguments follow the pages' positional order.
 
     ``pairs``: None for every (b,h) pair (results in full layouts), or a list
     of (b,h) pairs (results compact, leading axis = pair index:
     states [n,nc,N,P], qk_dot [n,S,R,R], dz [n,S,P], dmimo_o/dmimo_z [n,R,P],
     out [n,Sp,R,P]).  Values are float64; with ``round_bf16`` the BF16
-    outputs hold BF16 values."""
+    outputs hold BF16 values.  ``want_y`` adds the forward output "y"
+    (see forward_y; full layouts only)."""
+    if want_y:
+        if pairs is not None:
+            raise ValueError("want_y needs the full problem (pairs=None)")
+        res = bwd_fwd(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs,
+                      da_cs_rev, dt, trap, d, segsum, chunk_size, rotary_dim_divisor,
+                      round_bf16=round_bf16, want_out=True)
+        res["y"] = forward_y(res["out"], mimo_o, z, mimo_z, q.shape[1], round_bf16=round_bf16)
+        if not want_out:
+            res["out"] = None
+        return res
     B, S, R, G, N = q.shape
     H, P = v.shape[2], v.shape[3]
     C = int(chunk_size)
@@ -140,3 +154,44 @@ def bwd_fwd(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da
 
 
 OUTPUT_NAMES = ("dmimo_o", "states", "dz", "dmimo_z", "qk_dot")
+
+
+def forward_y(out, mimo_o, z, mimo_z, S: int, *, round_bf16: bool = True):
+    """The layer's forward output y, from the chunk output ``out`` [B,H,Sp,R,P]
+    (BF16 values in BF16 mode) of a problem of length S.  It is the function
+    whose gradients with respect to mimo_o, z and mimo_z the op returns (op
+    document, gradient formulas of the Z / projection branch):
+
+        gate  g[t,r,p] = silu(z[t,p] * mimo_z[r,p])   (1 without z)
+        y[t,p]         = sum over r, in rank order, of mimo_o[r,p] out[t,r,p] g[t,r,p]
+                                                      (with mimo_o: [B,S,H,P])
+        y[t,r,p]       = out[t,r,p] g[t,r,p]          (without:     [B,S,R,H,P])
+
+    In double; with ``round_bf16`` the result is rounded to BF16 once (the
+    activations' type)."""
+    B, H, Sp, R, P = out.shape
+    o = out[:, :, :S]                                            # [B,H,S,R,P]
+    if z is not None:
+        zd = z.double().numpy()                                  # [B,S,H,P]
+        mz = mimo_z.double().numpy()                             # [H,R,P]
+        pz = zd.transpose(0, 2, 1, 3)[:, :, :, None, :] * mz[None, :, None, :, :]
+        g = pz / (1.0 + np.exp(-pz))                             # silu, [B,H,S,R,P]
+    else:
+        g = np.ones_like(o)
+    if mimo_o is not None:
+        mo = mimo_o.double().numpy()                             # [H,R,P]
+        y = np.zeros((B, H, S, P))
+        for r in range(R):                                       # rank order
+            y = y + mo[None, :, None, r, :] * o[:, :, :, r, :] * g[:, :, :, r, :]
+        y = y.transpose(0, 2, 1, 3)                              # [B,S,H,P]
+    else:
+        y = (o * g).transpose(0, 2, 3, 1, 4)                     # [B,S,R,H,P]
+    y = np.ascontiguousarray(y)
+    return bf16_nearest_array(y) if round_bf16 else y
+
+
+def bf16_nearest_array(x: np.ndarray) -> np.ndarray:
+    """bf16_nearest applied to every element."""
+    f = _load().oracle_bf16_nearest
+    flat = np.asarray(x, dtype=np.float64).ravel()
+    return np.fromiter((f(float(v)) for v in flat), dtype=np.float64, count=flat.size).reshape(np.shape(x))

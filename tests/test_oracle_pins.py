@@ -797,3 +797,56 @@ def test_worked_example_pre_gate_dout_projection_is_rounded():
     rb, re_ = both(x)
     assert rb["dmimo_z"][0, 0, 0, 0] == 1.265625
     assert re_["dmimo_z"][0, 0, 0, 0] == pytest.approx((1 + 2 ** -7) ** 2 * 1.25, abs=1e-15)
+
+
+# --- the layer's forward output y ---------------------------------------------
+# y is pinned to the op's own gradients (themselves pinned by the token
+# recurrence above): y is linear in mimo_o, and its derivative along mimo_z is
+# what dmimo_z accumulates.
+
+@pytest.mark.parametrize("has_z", [True, False])
+def test_forward_y_pairs_with_dmimo_o(has_z):
+    # <dout, y> = sum_t,p dout sum_r mimo_o out g = sum_r,p mimo_o dmimo_o  (exact)
+    inp, _ = small_inputs(2, 37, 3, 3, 4, 8, 12, 8, 4, True, has_z, True, seed=11)
+    r = oracle.bwd_fwd(*si.args_of(inp), round_bf16=False, want_y=True)
+    assert r["y"].shape == tuple(inp["dout"].shape)
+    lhs = float((f64(inp["dout"]) * r["y"]).sum())
+    rhs = float((f64(inp["mimo_o"])[None] * r["dmimo_o"]).sum())
+    assert abs(lhs - rhs) <= 1e-11 * max(abs(rhs), 1.0)
+
+
+@pytest.mark.parametrize("reduced", [True, False])
+def test_forward_y_gate_derivative_along_mimo_z(reduced):
+    # d/ds <dout, y(mimo_z (1 + s))> at s = 0 equals sum_r,p mimo_z dmimo_z  (exact)
+    inp, _ = small_inputs(1, 29, 2, 1, 3, 8, 10, 8, 4, reduced, True, False, seed=5)
+    # mimo_z with 8 significant bits, so mimo_z * (1 +- 2^-12) is exact in FP32
+    inp["mimo_z"] = inp["mimo_z"].to(torch.bfloat16).float()
+
+    def f(scale):
+        x = dict(inp)
+        x["mimo_z"] = inp["mimo_z"] * scale
+        r = oracle.bwd_fwd(*si.args_of(x), round_bf16=False, want_y=True)
+        return float((f64(inp["dout"]) * r["y"]).sum()), r
+
+    eps = 2.0 ** -12
+    fp, _ = f(1.0 + eps)
+    fm, _ = f(1.0 - eps)
+    _, r0 = f(1.0)
+    fd = (fp - fm) / (2 * eps)
+    want = float((f64(inp["mimo_z"])[None] * r0["dmimo_z"]).sum())
+    assert abs(fd - want) <= 1e-6 * max(abs(want), 1.0)
+
+
+def test_forward_y_layout_and_bf16_rounding():
+    # per-rank dout layout [B,S,R,H,P] without mimo_o; BF16 mode rounds y once
+    inp, _ = small_inputs(1, 19, 2, 2, 2, 8, 6, 8, 2, False, True, True, seed=9)
+    ex = oracle.bwd_fwd(*si.args_of(inp), round_bf16=True, want_y=True, want_out=True)
+    y = ex["y"]
+    assert y.shape == tuple(inp["dout"].shape)
+    assert np.array_equal(y, oracle.bf16_nearest_array(y))
+    # y[b,t,r,h,p] has out[b,h,t,r,p] as a factor: zero out -> zero y
+    inp0 = dict(inp)
+    inp0["mimo_v"] = torch.zeros_like(inp["mimo_v"])
+    inp0["d"] = None
+    y0 = oracle.bwd_fwd(*si.args_of(inp0), round_bf16=True, want_y=True)["y"]
+    assert np.count_nonzero(y0) == 0
