@@ -124,6 +124,28 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
                                void* states, void* dz, float* dmimo_z, void* qk_dot,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same operation, also writing the layer's forward output `y` (BF16, in
+ * dout's layout: [B,S,H,P] when mimo_o != NULL, [B,S,R,H,P] otherwise) to the
+ * caller-owned, 4-byte aligned buffer `y` (MMBF_ERR_ARG if NULL).  y is the
+ * function whose gradients the op returns (op document, gradient formulas of
+ * the Z / projection branch): with the chunk output out[t,r,p] (BF16) and the
+ * gate g = silu(z[t,p] * mimo_z[r,p]) (g = 1 without z),
+ *   y[t,p]   = sum over r in rank order of mimo_o[r,p] * out[t,r,p] * g[t,r,p]
+ *   y[t,r,p] = out[t,r,p] * g[t,r,p]                  (without mimo_o)
+ * computed in FP32 and rounded to BF16 once.  The pages' op has no y
+ * output; every other argument and output is as for mamba_mimo_bwd_fwd
+ * (the outputs equal that call's up to FP32 summation order, since the
+ * launch plan may differ). */
+mmbf_status mamba_mimo_bwd_fwd_y(const mmbf_dims* dims, const void* dout, const void* q,
+                                 const void* k, const void* v, const float* q_bias,
+                                 const float* k_bias, const float* mimo_v, const float* mimo_o,
+                                 const void* z, const float* mimo_z, const float* angles,
+                                 const float* da_cs, const float* da_cs_rev, const float* dt,
+                                 const void* trap, const float* d, const float* segsum,
+                                 int64_t chunk_size, int64_t rotary_dim_divisor, float* dmimo_o,
+                                 void* states, void* dz, float* dmimo_z, void* qk_dot, void* y,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of the built-in scratch area used by
  * mamba_mimo_bwd_fwd_fixed_scratch (one area per GPU, held until exit). */
 #define MAMBA_MIMO_FIXED_SCRATCH_BYTES ((size_t)32 << 20)

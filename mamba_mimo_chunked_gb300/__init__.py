@@ -68,6 +68,9 @@ def load_library():
         lib.mamba_mimo_bwd_fwd.restype = ctypes.c_int
         lib.mamba_mimo_bwd_fwd.argtypes = (
             [ctypes.POINTER(_Dims)] + [vp] * 17 + [i64, i64] + [vp] * 6 + [ctypes.c_size_t, vp])
+        lib.mamba_mimo_bwd_fwd_y.restype = ctypes.c_int
+        lib.mamba_mimo_bwd_fwd_y.argtypes = (
+            [ctypes.POINTER(_Dims)] + [vp] * 17 + [i64, i64] + [vp] * 7 + [ctypes.c_size_t, vp])
         lib.mamba_mimo_bwd_fwd_workspace_size.restype = ctypes.c_int
         lib.mamba_mimo_bwd_fwd_workspace_size.argtypes = [
             ctypes.POINTER(_Dims), i64, i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
@@ -235,6 +238,27 @@ def mamba_mimo_bwd_fwd(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z,
     pass preallocated outputs (same shapes/dtypes as returned); ``workspace``
     a uint8 device buffer of at least ``workspace_size(...)`` bytes.
     """
+    return _run(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs, da_cs_rev,
+                dt, trap, d, segsum, chunk_size, rotary_dim_divisor, out, workspace, None)
+
+
+def mamba_mimo_bwd_fwd_with_y(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles,
+                              da_cs, da_cs_rev, dt, trap, d, segsum, chunk_size: int = 16,
+                              rotary_dim_divisor: int = 4, *,
+                              out: MambaMimoBwdFwdOutputs | None = None,
+                              workspace: torch.Tensor | None = None, y: torch.Tensor | None = None):
+    """mamba_mimo_bwd_fwd plus the layer's forward output ``y`` (BF16, shaped
+    like ``dout``): sum over ranks of mimo_o * out * silu(z * mimo_z), or per
+    rank without ``mimo_o`` (no gate without ``z``).  Returns (outputs, y)."""
+    if y is None:
+        y = torch.empty(dout.shape, dtype=torch.bfloat16, device=q.device)
+    res = _run(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs, da_cs_rev,
+               dt, trap, d, segsum, chunk_size, rotary_dim_divisor, out, workspace, y)
+    return res, y
+
+
+def _run(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs, da_cs_rev, dt,
+         trap, d, segsum, chunk_size, rotary_dim_divisor, out, workspace, y):
     args = (dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs, da_cs_rev,
             dt, trap, d, segsum)
     B, S, H, G, R, N, P = _validate(*args, chunk_size, rotary_dim_divisor)
@@ -254,11 +278,21 @@ def mamba_mimo_bwd_fwd(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z,
     if workspace is None:
         workspace = _workspace(dev, nbytes)
     stream = torch.cuda.current_stream(dev).cuda_stream
+    if y is not None:
+        if y.dtype != torch.bfloat16 or tuple(y.shape) != tuple(dout.shape) or not y.is_contiguous() \
+                or y.device != dev:
+            raise ValueError("y must be a contiguous bf16 tensor shaped like dout on the inputs' device")
     with torch.cuda.device(dev):
-        st = lib.mamba_mimo_bwd_fwd(
-            ctypes.byref(_Dims(B, S, H, G, R, N, P)), *[_ptr(a) for a in args], chunk_size,
-            rotary_dim_divisor, *[_ptr(o) for o in out], _ptr(workspace),
-            workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream))
+        if y is None:
+            st = lib.mamba_mimo_bwd_fwd(
+                ctypes.byref(_Dims(B, S, H, G, R, N, P)), *[_ptr(a) for a in args], chunk_size,
+                rotary_dim_divisor, *[_ptr(o) for o in out], _ptr(workspace),
+                workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream))
+        else:
+            st = lib.mamba_mimo_bwd_fwd_y(
+                ctypes.byref(_Dims(B, S, H, G, R, N, P)), *[_ptr(a) for a in args], chunk_size,
+                rotary_dim_divisor, *[_ptr(o) for o in out], _ptr(y), _ptr(workspace),
+                workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream))
     if st:
         _raise(lib, st)
     return out

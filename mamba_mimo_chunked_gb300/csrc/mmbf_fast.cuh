@@ -178,6 +178,13 @@ __device__ __forceinline__ void tma_store_4d(const void* map, uint32_t src, int 
                : "memory");
   asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
 }
+__device__ __forceinline__ void tma_store_5d(const void* map, uint32_t src, int c0, int c1, int c2, int c3, int c4) {
+  asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
 // This thread's bulk stores have finished reading shared memory / completed.
 __device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
@@ -258,7 +265,7 @@ struct Stage {  // raw inputs of one chunk
 };
 struct Smem {
   Stage st[2];
-  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, tok, mvb, mzp, mop, qbs, kbs, red, tm;
+  uint32_t Ks, Kst, Psi, Sb, qkd, eseg, tok, mvb, mzp, mop, mof, qbs, kbs, red, tm;
   uint32_t xch;  // state exchange: the cluster fold (state kernel), the entering state (output kernel)
   uint32_t mbar;  // two stage barriers (TMA loads)
   uint32_t total;
@@ -276,11 +283,11 @@ __device__ __forceinline__ Stage stage_at(const Stage& s0, int s) {
 }
 
 template <class K>
-__device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool has_z) {
+__device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool has_z, bool want_y = false) {
   Smem L;
   uint32_t o = 0;
   auto take = [&](uint32_t bytes) { uint32_t at = o; o = a128(o + bytes); return at; };
-  const bool need_out = out_kernel && (reduced || has_z);
+  const bool need_out = out_kernel && (reduced || has_z || want_y);
   for (int s = 0; s < 2; s++) {
     const uint32_t base = o;
     L.st[s].q = out_kernel ? take(K::CR * K::LDN * 2) : 0;
@@ -305,6 +312,7 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   L.mvb = take(K::R * K::P * 2);
   L.mzp = (need_out && has_z) ? take(K::R * K::NMT * 8 * 8) : 0;
   L.mop = (need_out && reduced) ? take(K::R * K::NMT * 8 * 4) : 0;
+  L.mof = (need_out && reduced && want_y) ? take(K::R * K::NMT * 8 * 8) : 0;  // FP32 mimo_o pairs (y)
   L.qbs = out_kernel ? take(K::R * K::LDB * 2) : 0;
   L.kbs = take(K::R * K::LDB * 2);
   L.tm = take(16);
@@ -1154,12 +1162,13 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
   const bool RED = MODE >= 0 ? (MODE & 1) != 0 : p.reduced != 0;
   const bool HZ = MODE >= 0 ? (MODE & 2) != 0 : p.has_z != 0;
   const bool HD = MODE >= 0 ? (MODE & 4) != 0 : p.has_d != 0;
+  const bool WY = MODE >= 0 ? false : p.want_y != 0;  // the forward output y (runtime flag only)
   constexpr int R = K::R, C = K::C, N = K::N, P = K::P, NMT = K::NMT, NMTH = K::NMTH, LDN = K::LDN,
                 LDP = K::LDP;
   extern __shared__ __align__(128) unsigned char sm_raw[];
   unsigned char* sm = smem_base<K>(sm_raw);
-  const bool need_out = RED || HZ;
-  const Smem L = smem_layout<K>(true, RED, HZ);
+  const bool need_out = RED || HZ || WY;
+  const Smem L = smem_layout<K>(true, RED, HZ, WY);
   const int bh = blockIdx.x, seg = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H;
   const int c0 = seg * p.L, c1 = min(p.nc, c0 + p.L);
@@ -1178,6 +1187,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
   uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + L.mvb);
   float2* mzp = reinterpret_cast<float2*>(sm + L.mzp);
   uint32_t* mop = reinterpret_cast<uint32_t*>(sm + L.mop);
+  float2* mof = reinterpret_cast<float2*>(sm + L.mof);
   uint16_t* qbs = reinterpret_cast<uint16_t*>(sm + L.qbs);
   uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
 
@@ -1197,6 +1207,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       const int o = e / (NMT * 8), mt = (e / 8) % NMT, gg = e % 8;
       const float* mo = p.mimo_o + ((int64_t)h * R + o) * P + mt * 16 + gg;
       mop[e] = (uint32_t)f_bf(mo[0]) | ((uint32_t)f_bf(mo[8]) << 16);
+      if (WY) mof[e] = make_float2(mo[0], mo[8]);
     }
   const float dval = HD ? p.d[h] : 0.f;
   // Tensor memory: warp 0 allocates the CTA's columns; each warp uses its lane
@@ -1310,9 +1321,13 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       if (!mbar_wait(bar_mma, (c - 1 - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
       tm_fence_after();
     }
-    // chunk c-1's dz (in its z tile) leaves by TMA before that stage is refilled
-    if (K::TMA && HZ && c > c0 && threadIdx.x == kTmaThread) {
-      tma_store_4d(&p.tm_dz, smem_u32(sm) + stage_at(L.st[0], s ^ 1).z, 0, h, (c - 1) * C, b);
+    // chunk c-1's dz (in its z tile) and y (in its dout tile) leave by TMA
+    // before that stage is refilled
+    if (K::TMA && (HZ || WY) && c > c0 && threadIdx.x == kTmaThread) {
+      const Stage Sp = stage_at(L.st[0], s ^ 1);
+      if (HZ) tma_store_4d(&p.tm_dz, smem_u32(sm) + Sp.z, 0, h, (c - 1) * C, b);
+      if (WY && RED) tma_store_4d(&p.tm_y, smem_u32(sm) + Sp.dout, 0, h, (c - 1) * C, b);
+      if (WY && !RED) tma_store_5d(&p.tm_y, smem_u32(sm) + Sp.dout, 0, h, 0, (c - 1) * C, b);
       tma_store_wait_read();
     }
     // the other stage (chunk c-1's inputs, k_scaled, k_state) is free now
@@ -1556,6 +1571,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
           }
           float2 prodz[NS];
           float2 cdmo[4], cdmz[4];
+          float2 yacc = make_float2(0.f, 0.f);  // y over this thread's ranks (with mimo_o)
 #pragma unroll
           for (int sl = 0; sl < 4; sl++) cdmo[sl] = cdmz[sl] = make_float2(0.f, 0.f);
 #pragma unroll
@@ -1594,6 +1610,24 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
                                ((uint32_t)draw[raw_off<K, LDP>(jr, mt * 16 + g + 8)] << 16),
                            ob);
             }
+            if (WY) {  // y: out silu(pz), weighted by mimo_o and summed over ranks, or per rank
+              const float2 og = HZ ? __fmul2_rn(of, __fmul2_rn(pz, sg)) : of;
+              if (RED) {
+                yacc = __ffma2_rn(mof[(o * NMT + mt) * 8 + g], og, yacc);
+              } else {
+                const uint32_t yb = pack2(og);
+                const int jr = tl * R + o;
+                if (K::TMA) {  // over this rank's dout row (read above), stored by TMA
+                  uint16_t* dw = const_cast<uint16_t*>(draw);
+                  dw[raw_off<K, LDP>(jr, mt * 16 + g)] = (uint16_t)(yb & 0xffffu);
+                  dw[raw_off<K, LDP>(jr, mt * 16 + g + 8)] = (uint16_t)(yb >> 16);
+                } else if (tg < p.S) {
+                  uint16_t* yp = p.y + ((((int64_t)b * p.S + tg) * R + o) * p.H + h) * P + mt * 16 + g;
+                  yp[0] = (uint16_t)(yb & 0xffffu);
+                  yp[8] = (uint16_t)(yb >> 16);
+                }
+              }
+            }
             prodz[k] = make_float2(0.f, 0.f);
             if (HZ) {
               const float2 pre = unpack2(preb);
@@ -1614,6 +1648,25 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
               dmv[8 + 2 * sl + 1] = __float_as_uint(__uint_as_float(dmv[8 + 2 * sl + 1]) + cdmz[sl].y);
             }
             tm_st16(tm_dm + mtl * 16, dmv);
+          }
+          if (WY && RED) {  // y of this token and p pair
+            float2 yv = yacc;
+            if (R == 8) {  // ranks 0..3 in the even lane, 4..7 in the odd lane
+              const float2 oth = make_float2(__shfl_xor_sync(0xffffffffu, yv.x, 1), __shfl_xor_sync(0xffffffffu, yv.y, 1));
+              if (cq & 1) yv = __fadd2_rn(oth, yv);
+            }
+            if ((R == 8) ? ((cq & 1) != 0) : true) {
+              const uint32_t yb = pack2(yv);
+              if (K::TMA) {  // over the dout values read above, stored by TMA
+                uint16_t* dw = const_cast<uint16_t*>(draw);
+                dw[raw_off<K, LDP>(tl, mt * 16 + g)] = (uint16_t)(yb & 0xffffu);
+                dw[raw_off<K, LDP>(tl, mt * 16 + g + 8)] = (uint16_t)(yb >> 16);
+              } else if (tg < p.S) {
+                uint16_t* yp = p.y + (((int64_t)b * p.S + tg) * p.H + h) * P + mt * 16 + g;
+                yp[0] = (uint16_t)(yb & 0xffffu);
+                yp[8] = (uint16_t)(yb >> 16);
+              }
+            }
           }
           if (HZ) {  // dz: BF16 running sum over the ranks in order
             float2 acc = make_float2(0.f, 0.f);
@@ -1664,11 +1717,14 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       for (int sl = 0; sl < 4; sl++) dmz[sl][mt] = make_float2(v[2 * sl], v[2 * sl + 1]);
     }
   }
-  if (K::TMA && HZ) {  // the last chunk's dz, before the stage memory is reused
+  if (K::TMA && (HZ || WY)) {  // the last chunk's dz and y, before the stage memory is reused
     fence_proxy_async();
     __syncthreads();
     if (threadIdx.x == kTmaThread && last_done >= 0) {
-      tma_store_4d(&p.tm_dz, smem_u32(sm) + stage_at(L.st[0], (last_done - c0) & 1).z, 0, h, last_done * C, b);
+      const Stage Sp = stage_at(L.st[0], (last_done - c0) & 1);
+      if (HZ) tma_store_4d(&p.tm_dz, smem_u32(sm) + Sp.z, 0, h, last_done * C, b);
+      if (WY && RED) tma_store_4d(&p.tm_y, smem_u32(sm) + Sp.dout, 0, h, last_done * C, b);
+      if (WY && !RED) tma_store_5d(&p.tm_y, smem_u32(sm) + Sp.dout, 0, h, 0, last_done * C, b);
       tma_store_wait_all();
     }
   }

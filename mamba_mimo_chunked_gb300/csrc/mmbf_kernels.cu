@@ -157,6 +157,8 @@ struct Params {
       *d, *segsum;
   float *dmimo_o, *dmimo_z;
   uint16_t *states, *dz, *qk_dot;
+  uint16_t* y;  // the layer's forward output (layout of dout) or NULL
+  int want_y;
   float *ws_state, *ws_decay, *ws_grad;
   unsigned int* ws_count;  // per (b,h): output CTAs done (specialised kernels)
   unsigned int* ws_err;    // device-side error word: (tag << 8) | code of the failing call
@@ -168,6 +170,7 @@ struct Params {
   CUtensorMap tm_q, tm_k, tm_v, tm_dout, tm_z, tm_ang;
   CUtensorMap tm_states;   // states as [B*H*nc*N][P] (TMA tile stores)
   CUtensorMap tm_dz;       // dz [P,H,S,B] (TMA tile stores)
+  CUtensorMap tm_y;        // y in dout's layout (TMA tile stores)
 };
 
 __host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
@@ -582,9 +585,9 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(Params p) {
     // (3) rotary (Q and K), k_scaled = bf16(k_rot * factor)
     rotate_and_scale(p, Qt, Kt, tok + C, b, h, c);
     __syncthreads();
-    // Without mimo_o and z the chunk output feeds nothing: only the state
+    // Without mimo_o, z and y the chunk output feeds nothing: only the state
     // update remains.
-    if (!(p.reduced || p.has_z)) {
+    if (!(p.reduced || p.has_z || p.want_y)) {
       k_state_tile(p, Kt, tok + 3 * C);
       __syncthreads();
       const int last = min(c * C + C, p.S) - 1;
@@ -694,7 +697,7 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(Params p) {
           if (col1_ok) dov[1] = bf_f(p.dout[rowbase + 1]);
         }
       }
-      float dzacc[2] = {0.f, 0.f};
+      float dzacc[2] = {0.f, 0.f}, yacc[2] = {0.f, 0.f};
 #pragma unroll 1
       for (int o = 0; o < R; o++) {
         const int jo = t * R + o;
@@ -724,6 +727,13 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(Params p) {
             pz = __fmul_rn(zt[x], mzf[o * p.PS + pp + x]);
             sg = sigmoid_f(pz);
           }
+          if (p.want_y) {  // y: mimo_o out silu(pz) summed over ranks, or per rank
+            const float g_ = p.has_z ? __fmul_rn(pz, sg) : 1.f;
+            if (p.reduced)
+              yacc[x] = __fmaf_rn(__fmul_rn(p.mimo_o[((int64_t)h * R + o) * p.P + p0 + pp + x], o_), g_, yacc[x]);
+            else if (valid)
+              p.y[((((int64_t)b * p.S + tg) * R + o) * p.H + h) * p.P + p0 + pp + x] = f_bf(__fmul_rn(o_, g_));
+          }
           if (p.reduced) {
             const float dv = dov[x];
             if (p.has_z) {
@@ -748,6 +758,10 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(Params p) {
       if (p.has_z && valid) {
         if (col0_ok) p.dz[rowbase] = f_bf(dzacc[0]);
         if (col1_ok) p.dz[rowbase + 1] = f_bf(dzacc[1]);
+      }
+      if (p.want_y && p.reduced && valid) {
+        if (col0_ok) p.y[rowbase] = f_bf(yacc[0]);
+        if (col1_ok) p.y[rowbase + 1] = f_bf(yacc[1]);
       }
     }
   }
@@ -876,7 +890,7 @@ static int fast_index(const Params& p) {
 }
 template <class K>
 static size_t fast_out_smem(const Params& p) {
-  return fast::smem_layout<K>(true, p.reduced, p.has_z).total;
+  return fast::smem_layout<K>(true, p.reduced, p.has_z, p.want_y).total;
 }
 // The state-sum kernel always runs one warp per j-block.
 template <class K>
@@ -979,13 +993,13 @@ static int fast_state_slots(const Params& p) {
 }
 static int fast_slots(const Params& p) {
   // cached per device and specialisation (the occupancy query is not free)
-  static int cache[16][kNumFast][2][2];
+  static int cache[16][kNumFast][2][2][2];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     dev = 0;
   }
-  int* slot = (dev >= 0 && dev < 16) ? &cache[dev][p.fast][p.reduced][p.has_z] : nullptr;
+  int* slot = (dev >= 0 && dev < 16) ? &cache[dev][p.fast][p.reduced][p.has_z][p.want_y ? 1 : 0] : nullptr;
   if (slot && *slot > 0) return *slot;
   int v;
   switch (p.fast) {
@@ -1169,12 +1183,14 @@ static bool encode_stage_maps(Params& p) {
     if (p.has_z && !encode_map(&p.tm_z, bf, 4, p.z, d, st, box, true)) return false;
     if (p.has_z && !encode_map(&p.tm_dz, bf, 4, p.dz, d, st, box, true)) return false;
     if (p.dout && p.reduced && !encode_map(&p.tm_dout, bf, 4, p.dout, d, st, box, true)) return false;
+    if (p.want_y && p.reduced && !encode_map(&p.tm_y, bf, 4, p.y, d, st, box, true)) return false;
   }
   if (p.dout && !p.reduced) {  // per-rank dout [B,S,R,H,P]
     const cuuint64_t d[5] = {P, H, R, S, B};
     const cuuint64_t st[4] = {P * 2, H * P * 2, R * H * P * 2, S * R * H * P * 2};
     const cuuint32_t box[5] = {(cuuint32_t)P, 1, Rb, C, 1};
     if (!encode_map(&p.tm_dout, bf, 5, p.dout, d, st, box, true)) return false;
+    if (p.want_y && !encode_map(&p.tm_y, bf, 5, p.y, d, st, box, true)) return false;
   }
   {  // states [B,H,nc,N,P] as rows of P
     const cuuint64_t d[2] = {P, (cuuint64_t)p.B * p.H * p.nc * N};
@@ -1238,7 +1254,7 @@ static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) 
   const size_t ss = fast_state_smem<K>(p), so = fast_out_smem<K>(p);
   // All branches on (the benchmarked combination) has its own instantiation
   // with the branches resolved at compile time.
-  const bool all_on = p.reduced && p.has_z && p.has_d;
+  const bool all_on = p.reduced && p.has_z && p.has_d && !p.want_y;
   cudaError_t e = ensure_smem(fast::state_kernel<StateCfg<K>>, ss, &fast_state_smem_set<K>());
   if (e == cudaSuccess)
     e = all_on ? ensure_smem(fast::output_kernel<K, 7>, so, &fast_out_smem_set<K, 7>())
@@ -1306,15 +1322,17 @@ mmbf_status mamba_mimo_bwd_fwd_workspace_size(const mmbf_dims* dims, int64_t chu
   return MMBF_OK;
 }
 
-mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const void* q,
-                               const void* k, const void* v, const float* q_bias,
-                               const float* k_bias, const float* mimo_v, const float* mimo_o,
-                               const void* z, const float* mimo_z, const float* angles,
-                               const float* da_cs, const float* da_cs_rev, const float* dt,
-                               const void* trap, const float* d, const float* segsum,
-                               int64_t chunk_size, int64_t rotary_dim_divisor, float* dmimo_o,
-                               void* states, void* dz, float* dmimo_z, void* qk_dot,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+// The op, with the optional forward output y (NULL: not computed).
+static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q, const void* k,
+                          const void* v, const float* q_bias, const float* k_bias,
+                          const float* mimo_v, const float* mimo_o, const void* z,
+                          const float* mimo_z, const float* angles, const float* da_cs,
+                          const float* da_cs_rev, const float* dt, const void* trap, const float* d,
+                          const float* segsum, int64_t chunk_size, int64_t rotary_dim_divisor,
+                          float* dmimo_o, void* states, void* dz, float* dmimo_z, void* qk_dot,
+                          void* y, void* workspace, size_t workspace_bytes, void* stream) {
   g_err[0] = '\0';
   Params p;
   mmbf_status s = plan(dims, chunk_size, rotary_dim_divisor, mimo_o != nullptr, z != nullptr, &p);
@@ -1331,7 +1349,7 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
   if ((z == nullptr) != (dz == nullptr) || (z == nullptr) != (dmimo_z == nullptr))
     return fail(MMBF_ERR_ARG, "dz and dmimo_z must be given exactly when z is given");
   const void* ptrs[] = {dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs,
-                        da_cs_rev, dt, trap, d, segsum, dmimo_o, states, dz, dmimo_z, qk_dot};
+                        da_cs_rev, dt, trap, d, segsum, dmimo_o, states, dz, dmimo_z, qk_dot, y};
   for (const void* x : ptrs)
     if (x && (reinterpret_cast<uintptr_t>(x) & 3))
       return fail(MMBF_ERR_ALIGN, "tensor pointers must be 4-byte aligned");
@@ -1342,6 +1360,8 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
     return fail(MMBF_ERR_ALIGN, "workspace must be 256-byte aligned");
 
   p.has_d = d != nullptr;
+  p.y = static_cast<uint16_t*>(y);
+  p.want_y = y != nullptr;
   p.dout = static_cast<const uint16_t*>(dout);
   p.q = static_cast<const uint16_t*>(q);
   p.k = static_cast<const uint16_t*>(k);
@@ -1470,6 +1490,40 @@ mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const vo
   g_variant = -1;
   g_plan[0] = p.L; g_plan[1] = p.nseg; g_plan[2] = 1; g_plan[3] = p.L; g_plan[4] = 0;
   return MMBF_OK;
+}
+
+extern "C" {
+
+mmbf_status mamba_mimo_bwd_fwd(const mmbf_dims* dims, const void* dout, const void* q,
+                               const void* k, const void* v, const float* q_bias,
+                               const float* k_bias, const float* mimo_v, const float* mimo_o,
+                               const void* z, const float* mimo_z, const float* angles,
+                               const float* da_cs, const float* da_cs_rev, const float* dt,
+                               const void* trap, const float* d, const float* segsum,
+                               int64_t chunk_size, int64_t rotary_dim_divisor, float* dmimo_o,
+                               void* states, void* dz, float* dmimo_z, void* qk_dot,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return run_op(dims, dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs,
+                da_cs_rev, dt, trap, d, segsum, chunk_size, rotary_dim_divisor, dmimo_o, states, dz,
+                dmimo_z, qk_dot, nullptr, workspace, workspace_bytes, stream);
+}
+
+mmbf_status mamba_mimo_bwd_fwd_y(const mmbf_dims* dims, const void* dout, const void* q,
+                                 const void* k, const void* v, const float* q_bias,
+                                 const float* k_bias, const float* mimo_v, const float* mimo_o,
+                                 const void* z, const float* mimo_z, const float* angles,
+                                 const float* da_cs, const float* da_cs_rev, const float* dt,
+                                 const void* trap, const float* d, const float* segsum,
+                                 int64_t chunk_size, int64_t rotary_dim_divisor, float* dmimo_o,
+                                 void* states, void* dz, float* dmimo_z, void* qk_dot, void* y,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!y) {
+    g_err[0] = '\0';
+    return fail(MMBF_ERR_ARG, "y must not be NULL");
+  }
+  return run_op(dims, dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs,
+                da_cs_rev, dt, trap, d, segsum, chunk_size, rotary_dim_divisor, dmimo_o, states, dz,
+                dmimo_z, qk_dot, y, workspace, workspace_bytes, stream);
 }
 
 mmbf_status mamba_mimo_bwd_fwd_fixed_scratch(
