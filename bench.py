@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--sets", type=int, default=4)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--with-y", action="store_true",
+                    help="time mamba_mimo_bwd_fwd_y (the op plus the layer's forward output y)")
     return ap.parse_args()
 
 
@@ -280,7 +282,11 @@ def main():
     for s in range(args.sets):
         inp = si.make_inputs(**wl.shape_kwargs(), seed=si.WORKLOAD_SEED_BASE + WORKLOAD_INDEX + 7919 * s
                              + 104729 * rank, device=dev)
-        out = mm.mamba_mimo_bwd_fwd(*si.args_of(inp))  # allocates outputs, validates once
+        if args.with_y:  # y travels with the outputs (last field)
+            out, y = mm.mamba_mimo_bwd_fwd_with_y(*si.args_of(inp))
+            out = tuple(out) + (y,)
+        else:
+            out = mm.mamba_mimo_bwd_fwd(*si.args_of(inp))  # allocates outputs, validates once
         sets.append((inp, out))
     torch.cuda.synchronize(dev)
     in_bytes = sum(nbytes(sets[0][0][n]) for n in si.ARG_NAMES)
@@ -298,7 +304,7 @@ def main():
                 + [ptr(o) for o in out] + [ptr(workspace), ws_bytes, sh])
 
     call_args = [cargs(i, o) for i, o in sets]
-    call = lib.mamba_mimo_bwd_fwd
+    call = lib.mamba_mimo_bwd_fwd_y if args.with_y else lib.mamba_mimo_bwd_fwd
 
     for i in range(args.warmup):
         st = call(*call_args[i % len(call_args)])
@@ -388,7 +394,7 @@ def main():
         inp.update(dict(zip(in_names, dviews)))
         obuf, oviews = packed(out_list, device=dev)
         it = iter(oviews)
-        out = mm.MambaMimoBwdFwdOutputs(*[None if t is None else next(it) for t in src_out])
+        out = tuple(None if t is None else next(it) for t in src_out)
         bufs.append((dbuf, inp, obuf, out))
     host_out = [packed(out_list, pin_memory=True)[0] for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -408,7 +414,12 @@ def main():
             ev_in[k].record(s_in)
         stream.wait_event(ev_in[k])
         stream.wait_event(ev_out[k])             # step i-2's outputs have been downloaded
-        mm.mamba_mimo_bwd_fwd(*si.args_of(inp), out=out, workspace=workspace)
+        if args.with_y:
+            mm.mamba_mimo_bwd_fwd_with_y(*si.args_of(inp), out=mm.MambaMimoBwdFwdOutputs(*out[:5]),
+                                         workspace=workspace, y=out[5])
+        else:
+            mm.mamba_mimo_bwd_fwd(*si.args_of(inp), out=mm.MambaMimoBwdFwdOutputs(*out),
+                                  workspace=workspace)
         ev_comp[k].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[k])
@@ -440,7 +451,7 @@ def main():
         "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "H": wl.H, "G": wl.G, "R": wl.R,
                    "N": wl.N, "P": wl.P, "chunk_size": wl.C, "rotary_dim_divisor": wl.div,
                    "reduced_dout": wl.reduced, "z": wl.has_z, "d": wl.has_d,
-                   "parallelism": f"replicas{world}",
+                   "parallelism": f"replicas{world}", "with_y": bool(args.with_y),
                    "l2": f"{args.sets} rotating input+output sets, "
                          f"{args.sets * alg_bytes / 1e6:.0f} MB > 129 MB L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

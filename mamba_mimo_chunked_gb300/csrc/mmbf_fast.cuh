@@ -1155,14 +1155,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Per-chunk outputs and gradients (fast path of chunk_output_kernel).
 // MODE >= 0 fixes the branches at compile time (bit 0: reduced dout, bit 1: z,
-// bit 2: d); MODE = -1 reads them from Params.
+// bit 2: d, bit 3: the forward output y); MODE = -1 reads them from Params.
 template <class K, int MODE>
 __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 : 1)))
     output_kernel(const __grid_constant__ Params p) {
   const bool RED = MODE >= 0 ? (MODE & 1) != 0 : p.reduced != 0;
   const bool HZ = MODE >= 0 ? (MODE & 2) != 0 : p.has_z != 0;
   const bool HD = MODE >= 0 ? (MODE & 4) != 0 : p.has_d != 0;
-  const bool WY = MODE >= 0 ? false : p.want_y != 0;  // the forward output y (runtime flag only)
+  const bool WY = MODE >= 0 ? (MODE & 8) != 0 : p.want_y != 0;  // the forward output y
   constexpr int R = K::R, C = K::C, N = K::N, P = K::P, NMT = K::NMT, NMTH = K::NMTH, LDN = K::LDN,
                 LDP = K::LDP;
   extern __shared__ __align__(128) unsigned char sm_raw[];

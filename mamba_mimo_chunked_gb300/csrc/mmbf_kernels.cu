@@ -1252,13 +1252,15 @@ static bool aligned16(const void* x) { return x == nullptr || (reinterpret_cast<
 template <class K>
 static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) {
   const size_t ss = fast_state_smem<K>(p), so = fast_out_smem<K>(p);
-  // All branches on (the benchmarked combination) has its own instantiation
-  // with the branches resolved at compile time.
-  const bool all_on = p.reduced && p.has_z && p.has_d && !p.want_y;
+  // All branches on (the benchmarked combination), without and with the
+  // forward output y, have their own instantiations with the branches
+  // resolved at compile time; other combinations read them at run time.
+  const int mode = (p.reduced && p.has_z && p.has_d) ? (p.want_y ? 15 : 7) : -1;
   cudaError_t e = ensure_smem(fast::state_kernel<StateCfg<K>>, ss, &fast_state_smem_set<K>());
   if (e == cudaSuccess)
-    e = all_on ? ensure_smem(fast::output_kernel<K, 7>, so, &fast_out_smem_set<K, 7>())
-               : ensure_smem(fast::output_kernel<K, -1>, so, &fast_out_smem_set<K, -1>());
+    e = mode == 7    ? ensure_smem(fast::output_kernel<K, 7>, so, &fast_out_smem_set<K, 7>())
+        : mode == 15 ? ensure_smem(fast::output_kernel<K, 15>, so, &fast_out_smem_set<K, 15>())
+                     : ensure_smem(fast::output_kernel<K, -1>, so, &fast_out_smem_set<K, -1>());
   if (e != cudaSuccess) return e;
   g_stage_names = kFastStageNames;
   g_stage_names_n = 2;
@@ -1272,8 +1274,10 @@ static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) 
   if (e != cudaSuccess) return e;
   g_failed_stage = 1;
   stage_event(1, 0, st);
-  e = all_on ? launch_ex(fast::output_kernel<K, 7>, dim3(p.B * p.H, p.nseg), dim3(K::NT), so, st, true, p)
-             : launch_ex(fast::output_kernel<K, -1>, dim3(p.B * p.H, p.nseg), dim3(K::NT), so, st, true, p);
+  const dim3 og(p.B * p.H, p.nseg);
+  e = mode == 7    ? launch_ex(fast::output_kernel<K, 7>, og, dim3(K::NT), so, st, true, p)
+      : mode == 15 ? launch_ex(fast::output_kernel<K, 15>, og, dim3(K::NT), so, st, true, p)
+                   : launch_ex(fast::output_kernel<K, -1>, og, dim3(K::NT), so, st, true, p);
   stage_event(1, 1, st);
   (*launches)++;
   return e;  // the output kernel's last CTA per (b,h) also sums the dmimo partials
