@@ -13,10 +13,17 @@
 //   four ranks of one token: the rank-ordered BF16 diagonal and dz sums then
 //   need no cross-lane traffic.  The permutation only reorders the summation
 //   index of the contractions; what is computed is unchanged.
-// * The FP32 state is register resident as the transposed tile state^T[p][n]
-//   (an MMA accumulator), split over the warps by p-block.
-// * Raw inputs of chunk c+1 stream into shared memory with cp.async while
-//   chunk c is computed.
+// * Two launches per call: state_kernel (segment sums, the units of a
+//   segment folded inside a thread-block cluster) and output_kernel (each
+//   CTA folds the earlier segments' sums into its entering state; its last
+//   CTA per (b,h) sums the gradient partials).
+// * The FP32 state is the transposed tile state^T[p][n], split over the warps
+//   by p-block.  For N = P = 64 it lives in tensor memory as the accumulator
+//   of an M = 64 tcgen05.mma that adds PsiV^T k_state each chunk; otherwise
+//   it is updated with mma.sync from registers.
+// * Raw inputs of chunk c+1 stream into shared memory while chunk c is
+//   computed: TMA tensor loads against an mbarrier for N = P = 64 (128-byte
+//   rows), cp.async otherwise; states, dz and y leave by TMA tile stores.
 
 namespace fast {
 
@@ -1238,7 +1245,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
   }
   float4 scal = load_scalars<K>(p, bh, c0);
 
-  // ---- entering state of the segment (written by the prefix kernel)
+  // ---- entering state of the segment (folded from the state kernel's sums)
   pdl_wait();
   {
     // the state entering this segment: the earlier segments' sums folded in

@@ -27,10 +27,12 @@
 //   grad_reduce_kernel     grid (b*h)
 //       Fixed-order sum of the per-segment dmimo_o / dmimo_z partials.
 //
-// Shapes with specialised kernels (mmbf_fast.cuh) run three launches:
-// fast::state_kernel over state units of LA chunks, unit_prefix_kernel (the
-// state entering each segment), and fast::output_kernel, whose last CTA per
-// (b,h) -- found with an atomic counter -- does the fixed-order gradient sum.
+// Shapes with specialised kernels (mmbf_fast.cuh) run two launches:
+// fast::state_kernel over state units of LA chunks (the units of a segment
+// form a thread-block cluster and fold their sums into the segment's sum),
+// and fast::output_kernel, whose CTAs fold the earlier segments' sums into
+// their entering state and whose last CTA per (b,h) -- found with an atomic
+// counter -- does the fixed-order gradient sum.
 //
 // Rows of a chunk tile are j = t*R + r (token-major), as in the reference's
 // flatten of the token and rank axes.  BF16 products and sums of two BF16
