@@ -57,6 +57,10 @@ struct Cfg {
   static constexpr int NCW = N / WPM;         // state columns (n) per warp
   static constexpr int NN8 = NCW / 8;         // n8 tiles of the state per warp
   static constexpr int SLOTS = 4;             // X^T columns per thread: (tile nt, bit b)
+  // token tables: a window of TW chunks, one token per thread, filled at the
+  // window's first chunk; two windows in shared memory (TS floats per chunk)
+  static constexpr int TW = (NT / C < 8) ? NT / C : 8;
+  static constexpr int TS = 4 * C;
   // padded strides of small tables (bank spread): bias rows [R][N + 8] BF16,
   // same-token qk_dot [C][R*R + QKP] words
   static constexpr int LDB = N + 8;
@@ -315,7 +319,7 @@ __device__ __host__ inline Smem smem_layout(bool out_kernel, bool reduced, bool 
   L.Sb = out_kernel ? take(K::N * K::LDP * 2) : 0;
   L.qkd = out_kernel ? take(K::C * K::QKS * 4) : 0;
   L.eseg = need_out ? take(K::C * K::C * 4) : 0;
-  L.tok = take(2 * (K::C * 4 * 4 + 16));
+  L.tok = take(2 * K::TW * K::TS * 4);
   L.mvb = take(K::R * K::P * 2);
   L.mzp = (need_out && has_z) ? take(K::R * K::NMT * 8 * 8) : 0;
   L.mop = (need_out && reduced) ? take(K::R * K::NMT * 8 * 4) : 0;
@@ -467,18 +471,29 @@ __device__ __forceinline__ int raw_off(int row, int col) {
   return K::TMA ? swz128(row, col) : swz<LD>(row, col);
 }
 
-// dt, trap, da_cs, da_cs_rev of token c*C + threadIdx.x (threads 0..C; C is the
-// next chunk's first token, for the shifted gamma).  Zero past S.
+// Raw token inputs of a window of TW chunks starting at chunk cw, one token
+// per thread (thread e < TW*C: token cw*C + e): dt, trap, the next token's
+// dt and trap (for the shifted gamma), da_cs, da_cs_rev.  Zero past S (the
+// reference's zero padding).
+struct TokRaw {
+  float dt, tr, dtn, trn, a, ar;
+};
 template <class K>
-__device__ __forceinline__ float4 load_scalars(const Params& p, int bh, int c) {
-  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int t = threadIdx.x, tg = c * K::C + t;
-  if (t <= K::C && tg < p.S) {
+__device__ __forceinline__ TokRaw load_tok_window(const Params& p, int bh, int cw) {
+  TokRaw r = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int e = threadIdx.x, tg = cw * K::C + e;
+  if (e < K::TW * K::C) {
     const int64_t i = (int64_t)bh * p.S + tg;
-    r.x = __ldg(p.dt + i);
-    r.y = bf_f(__ldg(p.trap + i));
-    r.z = __ldg(p.da_cs + i);
-    r.w = __ldg(p.da_cs_rev + i);
+    if (tg < p.S) {
+      r.dt = __ldg(p.dt + i);
+      r.tr = bf_f(__ldg(p.trap + i));
+      r.a = __ldg(p.da_cs + i);
+      r.ar = __ldg(p.da_cs_rev + i);
+    }
+    if (tg + 1 < p.S) {
+      r.dtn = __ldg(p.dt + i + 1);
+      r.trn = bf_f(__ldg(p.trap + i + 1));
+    }
   }
   return r;
 }
@@ -496,30 +511,44 @@ __device__ __forceinline__ void sincos_fast(float x, float* s, float* c) {
 // e^x as 2^(x log2 e) with the ex2.approx instruction.
 __device__ __forceinline__ float exp_fast(float x) { return ex2_approx(x * 1.44269504088896341f); }
 
-// Token scalars of chunk c computed by warp 0 from its prefetched registers
-// (thread t holds token c*C + t; lane C the next chunk's first token), the
-// next token's dt / trap by a shuffle: gamma = bf16(dt) sigmoid(trap) (FP32),
-// factor = bf16(gamma + bf16(bf16(dt[t+1]) sigmoid(-trap[t+1]))) (as a BF16
-// pair), exp(da_cs), exp(da_cs_rev).
-// tok layout: gam[C] | facd[C] (u32) | eda[C] | edr[C].
+// Token tables of the window starting at chunk cw from the raw inputs (one
+// token per thread; chunk cw + i at tab + i*TS): gamma = bf16(dt) sigmoid(trap)
+// (FP32), factor = bf16(gamma + bf16(bf16(dt[t+1]) sigmoid(-trap[t+1]))) as a
+// BF16 pair (the shifted term is 0 at the last padded position), exp(da_cs),
+// exp(da_cs_rev).  Layout per chunk: gam[C] | facd[C] (u32) | eda[C] | edr[C].
 template <class K>
-__device__ __forceinline__ void token_scalars_regs(const Params& p, float4 v, float* tok, int c) {
-  static_assert(K::C + 1 <= 32, "token scalars of one chunk must sit in one warp");
-  if (threadIdx.x < 32) {
-    const int t = threadIdx.x;
-    const float dtn = __shfl_down_sync(0xffffffffu, v.x, 1);
-    const float trn = __shfl_down_sync(0xffffffffu, v.y, 1);
-    if (t < K::C) {
-      const int tg = c * K::C + t;
-      const float gam = __fmul_rn(round_bf(v.x), sigmoid_f(v.y));
-      float sh = 0.f;
-      if (tg + 1 < p.nc * K::C) sh = round_bf(__fmul_rn(round_bf(dtn), 1.0f / (1.0f + expf(trn))));
-      tok[t] = gam;
-      reinterpret_cast<uint32_t*>(tok)[K::C + t] = dup_bf(__fadd_rn(gam, sh));
-      tok[2 * K::C + t] = expf(v.z);
-      tok[3 * K::C + t] = expf(v.w);
-    }
+__device__ __forceinline__ void token_window(const Params& p, const TokRaw& v, float* tab, int cw) {
+  const int e = threadIdx.x;
+  if (e < K::TW * K::C) {
+    const int tg = cw * K::C + e;
+    float* tok = tab + (e / K::C) * K::TS;
+    const int t = e % K::C;
+    const float gam = __fmul_rn(round_bf(v.dt), sigmoid_f(v.tr));
+    float sh = 0.f;
+    if (tg + 1 < p.nc * K::C) sh = round_bf(__fmul_rn(round_bf(v.dtn), 1.0f / (1.0f + expf(v.trn))));
+    tok[t] = gam;
+    reinterpret_cast<uint32_t*>(tok)[K::C + t] = dup_bf(__fadd_rn(gam, sh));
+    tok[2 * K::C + t] = expf(v.a);
+    tok[3 * K::C + t] = expf(v.ar);
   }
+}
+// At a window's first chunk c (relative to the CTA's first chunk c0): fill
+// that window's half of the two-window table from the prefetched raw inputs
+// and prefetch the next window.  The other half holds the window before, which
+// warps still finishing chunk c - 1 may read.  Published by the chunk's first
+// barrier.
+template <class K>
+__device__ __forceinline__ void token_window_step(const Params& p, TokRaw& raw, float* tokb, int bh, int c,
+                                                  int c0, int c1) {
+  if ((c - c0) % K::TW == 0) {
+    token_window<K>(p, raw, tokb + (((c - c0) / K::TW) & 1) * K::TW * K::TS, c);
+    if (c + K::TW < c1) raw = load_tok_window<K>(p, bh, c + K::TW);
+  }
+}
+// Token table of chunk c.
+template <class K>
+__device__ __forceinline__ float* token_slot(float* tokb, int c, int c0) {
+  return tokb + ((c - c0) % (2 * K::TW)) * K::TS;
 }
 // The chunk's state decay exp(da_cs[last valid token]) from the token table.
 template <class K>
@@ -981,7 +1010,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
   }
   int last_mma = -1;
   param_tables<K>(p, h, mvb, nullptr, kbs);
-  float4 scal = load_scalars<K>(p, bh, c0);
+  TokRaw traw = load_tok_window<K>(p, bh, c0);
   float st[K::NN8][4];
 #pragma unroll
   for (int nn = 0; nn < K::NN8; nn++) st[nn][0] = st[nn][1] = st[nn][2] = st[nn][3] = 0.f;
@@ -989,9 +1018,8 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
   for (int c = c0; c < c1; c++) {
     const int s = (c - c0) & 1;
     const Stage S = stage_at(L.st[0], s);
-    float* tok = tokb + s * (4 * K::C + 4);
-    token_scalars_regs<K>(p, scal, tok, c);
-    if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
+    token_window_step<K>(p, traw, tokb, bh, c, c0, c1);
+    float* tok = token_slot<K>(tokb, c, c0);
     const bool ok = stage_wait<K>(L, sm, c, c0);
     if (K::TMA) fence_proxy_async();  // k_state written over stage rows precedes their refill
     if (__syncthreads_or(!ok)) {  // (1) chunk c raw inputs, token scalars visible; all warps past c-1
@@ -1002,7 +1030,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
       if (c > c0) {  // chunk c-1's U (its MMA has also finished reading PsiV and k_state)
         if (!mbar_wait(bar_mma, (c - 1 - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
         tm_fence_after();
-        fold_u<K>(st, tm_uw, chunk_decay<K>(p, tokb + ((c - 1 - c0) & 1) * (4 * K::C + 4), c - 1));
+        fold_u<K>(st, tm_uw, chunk_decay<K>(p, token_slot<K>(tokb, c - 1, c0), c - 1));
       }
     }
     // the other stage (chunk c-1's inputs and k_state) is free now
@@ -1038,7 +1066,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
     if (last_mma >= 0) {
       if (!mbar_wait(bar_mma, (last_mma - c0) & 1) && threadIdx.x == 0) atomicExch(p.ws_err, (p.tag << 8) | 2u);
       tm_fence_after();
-      fold_u<K>(st, tm_uw, chunk_decay<K>(p, tokb + ((last_mma - c0) & 1) * (4 * K::C + 4), last_mma));
+      fold_u<K>(st, tm_uw, chunk_decay<K>(p, token_slot<K>(tokb, last_mma, c0), last_mma));
     }
     tm_fence_before();
     __syncthreads();
@@ -1243,7 +1271,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     mbar_init(bar_mma, 1);
     mbar_fence_init();
   }
-  float4 scal = load_scalars<K>(p, bh, c0);
+  TokRaw traw = load_tok_window<K>(p, bh, c0);
 
   // ---- entering state of the segment (folded from the state kernel's sums)
   pdl_wait();
@@ -1311,12 +1339,11 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     const Stage S = stage_at(L.st[0], s);
     uint16_t* const Ks = K::ALIAS_K ? reinterpret_cast<uint16_t*>(sm + S.k) : Ks_sep;
     uint16_t* const Kst = K::ALIAS_K ? reinterpret_cast<uint16_t*>(sm + S.q) : Kst_sep;
-    float* tok = tokb + s * (4 * C + 4);
+    token_window_step<K>(p, traw, tokb, bh, c, c0, c1);
+    float* tok = token_slot<K>(tokb, c, c0);
     const uint32_t* facd = reinterpret_cast<const uint32_t*>(tok) + C;
     const float* eda = tok + 2 * C;
     const float* edr = tok + 3 * C;
-    token_scalars_regs<K>(p, scal, tok, c);
-    if (c + 1 < c1) scal = load_scalars<K>(p, bh, c + 1);
     const bool ok = stage_wait<K>(L, sm, c, c0);
     if (K::TMA) fence_proxy_async();  // k_scaled / k_state over stage rows precede their refill
     if (K::TMA && threadIdx.x == kStoreThread) tma_store_wait_read();  // chunk c-1's states store has read the tile
@@ -1758,17 +1785,29 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
       }
     __syncthreads();
     float* dst = p.ws_grad + ((int64_t)bh * p.nseg + seg) * 2 * R * P;
+    // Thread (g, cc) slot sl holds rank perm(8 (sl >> 1) + 2 cc + (sl & 1)) % R:
+    // sl itself (R = 4), 4 (cc & 1) + sl (R = 8), sl & 1 (R = 2).  Each sum
+    // visits only its rank's (warp, cc, sl) entries, in that order.
     for (int e = threadIdx.x; e < 2 * R * P; e += K::NT) {
       const int which = e / (R * P), r = (e / P) % R, pp = e % P;
       const int mt = pp / 16, gg = pp % 8, hh = (pp % 16) / 8;
       const int hf = mt / NMTH, mtl = mt % NMTH;
+      const float* col = red + gg * 4 * PER + ((which * 4) * NMTH + mtl) * 2 + hh;
       float sum = 0.f;
-      for (int w = hf * K::NWJ; w < (hf + 1) * K::NWJ; w++)
-        for (int cc = 0; cc < 4; cc++)
+      for (int w = hf * K::NWJ; w < (hf + 1) * K::NWJ; w++) {
+        const float* cw = col + w * 32 * PER;
 #pragma unroll
-          for (int sl = 0; sl < 4; sl++)
-            if (perm<R>((sl >> 1) * 8 + 2 * cc + (sl & 1)) % R == r)
-              sum += red[(w * 32 + gg * 4 + cc) * PER + ((which * 4 + sl) * NMTH + mtl) * 2 + hh];
+        for (int cc = 0; cc < 4; cc++) {
+          if (R == 4) {
+            sum += cw[cc * PER + (r * NMTH) * 2];
+          } else if (R == 8) {
+            if ((cc & 1) == (r >> 2)) sum += cw[cc * PER + ((r & 3) * NMTH) * 2];
+          } else {
+            sum += cw[cc * PER + (r * NMTH) * 2];
+            sum += cw[cc * PER + ((r + 2) * NMTH) * 2];
+          }
+        }
+      }
       dst[e] = sum;
     }
     // The last CTA of this (b,h) to finish sums the segments' partials in
@@ -1780,22 +1819,22 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
     __syncthreads();
     if (*last) {
       __threadfence();
-      // element e = threadIdx.x + i*NT; four segments' loads in flight
+      // element e = threadIdx.x + i*NT
       constexpr int NE = 2 * R * P / K::NT;
       static_assert((2 * R * P) % K::NT == 0, "gradient partials must split evenly over the threads");
       const float* src = p.ws_grad + (int64_t)bh * p.nseg * 2 * R * P + threadIdx.x;
       float sum[NE];
 #pragma unroll
       for (int i = 0; i < NE; i++) sum[i] = 0.f;
-      for (int s0 = 0; s0 < p.nseg; s0 += 4) {
-        float x[4][NE];
+      for (int s0 = 0; s0 < p.nseg; s0 += 8) {  // eight segments' loads in flight
+        float x[8][NE];
 #pragma unroll
-        for (int k = 0; k < 4; k++)
+        for (int k = 0; k < 8; k++)
 #pragma unroll
           for (int i = 0; i < NE; i++)
             x[k][i] = (s0 + k < p.nseg) ? __ldcg(src + (int64_t)(s0 + k) * 2 * R * P + i * K::NT) : 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; k++)
+        for (int k = 0; k < 8; k++)
 #pragma unroll
           for (int i = 0; i < NE; i++)
             if (s0 + k < p.nseg) sum[i] += x[k][i];
