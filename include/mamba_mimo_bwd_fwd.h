@@ -229,8 +229,8 @@ int mamba_mimo_last_plan(int* out, int n);
 /* Name of the i-th kernel the last mamba_mimo_bwd_fwd call on this thread
  * launched (0 <= i < 4), or NULL past its last kernel.  The generic kernels
  * are "segment_state", "segment_prefix", "chunk_output", "grad_reduce"; the
- * shape-specialised ones "segment_state", "chunk_output" (the segment scan
- * and the gradient sum are folded into those two). */
+ * shape-specialised ones "segment_state", "segment_prefix", "chunk_output"
+ * (the gradient sum is folded into the output kernel). */
 const char* mamba_mimo_stage_name(int i);
 
 #ifdef __cplusplus

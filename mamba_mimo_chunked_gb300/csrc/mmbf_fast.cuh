@@ -1184,6 +1184,40 @@ __global__ void segment_prefix_vec_kernel(Params p) {
   }
 }
 
+// The same exclusive scan for the shape-specialised kernels: one state
+// element per thread and all of a group of 32 segments' loads in flight, so
+// a (b,h) with up to 32 segments takes one round trip to memory.
+// Segment s of (b,h) then holds the FP32 state entering it (sum_s' of
+// decay(s'+1..s-1) * sum_s', in segment order).
+__global__ void __launch_bounds__(128) segment_prefix_fast_kernel(Params p) {
+  fast::pdl_trigger();  // the output kernel may launch and set up; it waits for this grid
+  fast::pdl_wait();
+  const int bh = blockIdx.y;
+  const int64_t NPe = (int64_t)p.N * p.P;
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= NPe) return;
+  float* base = p.ws_state + (int64_t)bh * p.nseg * NPe + e;
+  const float* dec = p.ws_decay + (int64_t)bh * p.nseg;
+  constexpr int GRP = 32;
+  float acc = 0.f;
+  for (int s0 = 0; s0 < p.nseg; s0 += GRP) {
+    float x[GRP], d[GRP];
+#pragma unroll
+    for (int q = 0; q < GRP; q++) {
+      const bool in = s0 + q < p.nseg;
+      x[q] = in ? __ldcg(base + (int64_t)(s0 + q) * NPe) : 0.f;
+      d[q] = in ? __ldcg(dec + s0 + q) : 1.f;
+    }
+#pragma unroll
+    for (int q = 0; q < GRP; q++) {
+      if (s0 + q < p.nseg) {
+        base[(int64_t)(s0 + q) * NPe] = acc;
+        acc = acc * d[q] + x[q];
+      }
+    }
+  }
+}
+
 namespace fast {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -1273,40 +1307,16 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
   }
   TokRaw traw = load_tok_window<K>(p, bh, c0);
 
-  // ---- entering state of the segment (folded from the state kernel's sums)
+  // ---- entering state of the segment (the exclusive prefix over the
+  //      state kernel's segment sums, one FP32 [N][P] tile)
   pdl_wait();
   {
-    // the state entering this segment: the earlier segments' sums folded in
-    // segment order (state = state * decay_s + sum_s), staged in shared memory
     constexpr int NV4 = N * P / 4 / K::NT;
     static_assert((N * P) % (4 * K::NT) == 0, "state elements must split evenly over the threads");
     float4 acc[NV4];
+    const float4* A = reinterpret_cast<const float4*>(p.ws_state + ((int64_t)bh * p.nseg + seg) * N * P);
 #pragma unroll
-    for (int i = 0; i < NV4; i++) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4* A = reinterpret_cast<const float4*>(p.ws_state + (int64_t)bh * p.nseg * N * P);
-    const float* D = p.ws_decay + (int64_t)bh * p.nseg;
-    auto fold = [&](float4& a, float4 x, float d) {
-      a.x = a.x * d + x.x; a.y = a.y * d + x.y; a.z = a.z * d + x.z; a.w = a.w * d + x.w;
-    };
-    // four segments' loads in flight per round trip; past the last segment
-    // the fold is the identity (decay 1, sum 0)
-    for (int s2 = 0; s2 < seg; s2 += 4) {
-      float4 x[4][NV4];
-      float d[4];
-#pragma unroll
-      for (int k = 0; k < 4; k++) {
-        const bool in = s2 + k < seg;
-        d[k] = in ? __ldcg(D + s2 + k) : 1.f;
-#pragma unroll
-        for (int i = 0; i < NV4; i++)
-          x[k][i] = in ? __ldcg(A + (int64_t)(s2 + k) * (N * P / 4) + i * K::NT + threadIdx.x)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; k++)
-#pragma unroll
-        for (int i = 0; i < NV4; i++) fold(acc[i], x[k][i], d[k]);
-    }
+    for (int i = 0; i < NV4; i++) acc[i] = __ldcg(A + i * K::NT + threadIdx.x);
     float4* xs = reinterpret_cast<float4*>(sm + L.xch);
 #pragma unroll
     for (int i = 0; i < NV4; i++) xs[i * K::NT + threadIdx.x] = acc[i];

@@ -833,7 +833,7 @@ static unsigned int next_call_tag() {
 }
 static const char* const kStageNames[4] = {"segment_state", "segment_prefix", "chunk_output",
                                            "grad_reduce"};
-static const char* const kFastStageNames[2] = {"segment_state", "chunk_output"};
+static const char* const kFastStageNames[3] = {"segment_state", "segment_prefix", "chunk_output"};
 static thread_local const char* const* g_stage_names = kStageNames;  // kernels of the last call
 static thread_local int g_stage_names_n = 4;
 
@@ -1265,7 +1265,7 @@ static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) 
                      : ensure_smem(fast::output_kernel<K, -1>, so, &fast_out_smem_set<K, -1>());
   if (e != cudaSuccess) return e;
   g_stage_names = kFastStageNames;
-  g_stage_names_n = 2;
+  g_stage_names_n = 3;
   g_failed_stage = 0;
   stage_event(0, 0, st);
   // the UA units of a segment form one cluster (UA <= 8)
@@ -1274,13 +1274,21 @@ static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) 
   stage_event(0, 1, st);
   (*launches)++;
   if (e != cudaSuccess) return e;
+  // exclusive prefix over the segment sums: the state entering each segment
   g_failed_stage = 1;
   stage_event(1, 0, st);
+  e = launch_ex(segment_prefix_fast_kernel, dim3((unsigned)((p.N * p.P + 127) / 128), p.B * p.H), dim3(128), 0,
+                st, true, p);
+  stage_event(1, 1, st);
+  (*launches)++;
+  if (e != cudaSuccess) return e;
+  g_failed_stage = 2;
+  stage_event(2, 0, st);
   const dim3 og(p.B * p.H, p.nseg);
   e = mode == 7    ? launch_ex(fast::output_kernel<K, 7>, og, dim3(K::NT), so, st, true, p)
       : mode == 15 ? launch_ex(fast::output_kernel<K, 15>, og, dim3(K::NT), so, st, true, p)
                    : launch_ex(fast::output_kernel<K, -1>, og, dim3(K::NT), so, st, true, p);
-  stage_event(1, 1, st);
+  stage_event(2, 1, st);
   (*launches)++;
   return e;  // the output kernel's last CTA per (b,h) also sums the dmimo partials
 }
