@@ -249,6 +249,26 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
+// Mixed-precision pair arithmetic (sm_100 and later): BF16 operands widened
+// exactly inside the FP32 operation, so no separate unpack.
+// (a.lo + c.x, a.hi + c.y), one FP32 rounding each
+__device__ __forceinline__ float2 add_bf2_f32(uint32_t a, float2 c) {
+  float2 d;
+  asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %4;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "r"(a), "f"(c.x), "f"(c.y));
+  return d;
+}
+// (a.lo * b.lo + c.x, a.hi * b.hi + c.y), one FP32 rounding each (the BF16
+// products are exact in FP32)
+__device__ __forceinline__ float2 fma_bf2_f32(uint32_t a, uint32_t b, float2 c) {
+  float2 d;
+  asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %4;\n\tfma.rn.f32.bf16 %1, ah, bh, %5;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "r"(a), "r"(b), "f"(c.x), "f"(c.y));
+  return d;
+}
 // (a.lo, b.lo) and (a.hi, b.hi) of two BF16 pairs
 __device__ __forceinline__ uint32_t lo_lo(uint32_t a, uint32_t b) { return prmt(a, b, 0x5410); }
 __device__ __forceinline__ uint32_t hi_hi(uint32_t a, uint32_t b) { return prmt(a, b, 0x7632); }
@@ -1602,7 +1622,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
 #pragma unroll
             for (int k = 0; k < NS; k++) psiP[k % R] = pso[k];
           }
-          float2 z2 = make_float2(0.f, 0.f), do2 = make_float2(0.f, 0.f);
+          float2 z2 = make_float2(0.f, 0.f);
           uint32_t dob = 0;
           if (HZ) {
             z2 = unpack2((uint32_t)zraw[raw_off<K, LDP>(tl, mt * 16 + g)] |
@@ -1611,7 +1631,6 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
           if (RED) {
             dob = (uint32_t)draw[raw_off<K, LDP>(tl, mt * 16 + g)] |
                   ((uint32_t)draw[raw_off<K, LDP>(tl, mt * 16 + g + 8)] << 16);
-            do2 = unpack2(dob);
           }
           float2 prodz[NS];
           float2 cdmo[4], cdmz[4];
@@ -1625,12 +1644,11 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
             uint32_t dacc = bmul2(qrow[k][0], psiP[0]);
 #pragma unroll
             for (int r = 1; r < R; r++) dacc = badd2(dacc, bmul2(qrow[k][r], psiP[r]));
-            const float2 dg = unpack2(pack2(__fmul2_rn(unpack2(dacc), gam2)));
+            const uint32_t dgb = pack2(__fmul2_rn(unpack2(dacc), gam2));
             // out = bf16(inter + intra + diag + d * PsiV)
-            float2 x = __fadd2_rn(make_float2(X[mtl][nt][bb], X[mtl][nt][bb + 2]), dg);
+            float2 x = add_bf2_f32(dgb, make_float2(X[mtl][nt][bb], X[mtl][nt][bb + 2]));
             if (HD) x = __ffma2_rn(make_float2(dval, dval), unpack2(pso[k]), x);
             const uint32_t ob = pack2(x);
-            const float2 of = unpack2(ob);
             float2 pz = make_float2(0.f, 0.f), sg = make_float2(0.5f, 0.5f), mz = make_float2(0.f, 0.f);
             if (HZ) {
               mz = mzp[(o * NMT + mt) * 8 + g];
@@ -1641,12 +1659,13 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
               sg = make_float2(rcp_approx(den.x), rcp_approx(den.y));
             }
             uint32_t preb = 0u;
-            if (RED) {
+            if (RED) {  // dmimo_o partials: out * dout (exact) * silu(pz)
               if (HZ) {
-                cdmo[sl] = __ffma2_rn(__fmul2_rn(of, __fmul2_rn(pz, sg)), do2, cdmo[sl]);
+                const float2 od = fma_bf2_f32(ob, dob, make_float2(-0.f, -0.f));
+                cdmo[sl] = __ffma2_rn(od, __fmul2_rn(pz, sg), cdmo[sl]);
                 preb = bmul2(bmul2(dob, mop[(o * NMT + mt) * 8 + g]), ob);
               } else {
-                cdmo[sl] = __ffma2_rn(of, do2, cdmo[sl]);
+                cdmo[sl] = fma_bf2_f32(ob, dob, cdmo[sl]);
               }
             } else if (HZ) {
               const int jr = tl * R + o;
@@ -1655,6 +1674,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
                            ob);
             }
             if (WY) {  // y: out silu(pz), weighted by mimo_o and summed over ranks, or per rank
+              const float2 of = unpack2(ob);
               const float2 og = HZ ? __fmul2_rn(of, __fmul2_rn(pz, sg)) : of;
               if (RED) {
                 yacc = __ffma2_rn(mof[(o * NMT + mt) * 8 + g], og, yacc);
@@ -1686,10 +1706,14 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
             tm_ld16_wait(dmv);
 #pragma unroll
             for (int sl = 0; sl < 4; sl++) {
-              dmv[2 * sl] = __float_as_uint(__uint_as_float(dmv[2 * sl]) + cdmo[sl].x);
-              dmv[2 * sl + 1] = __float_as_uint(__uint_as_float(dmv[2 * sl + 1]) + cdmo[sl].y);
-              dmv[8 + 2 * sl] = __float_as_uint(__uint_as_float(dmv[8 + 2 * sl]) + cdmz[sl].x);
-              dmv[8 + 2 * sl + 1] = __float_as_uint(__uint_as_float(dmv[8 + 2 * sl + 1]) + cdmz[sl].y);
+              const float2 a = __fadd2_rn(make_float2(__uint_as_float(dmv[2 * sl]), __uint_as_float(dmv[2 * sl + 1])),
+                                          cdmo[sl]);
+              const float2 z = __fadd2_rn(
+                  make_float2(__uint_as_float(dmv[8 + 2 * sl]), __uint_as_float(dmv[8 + 2 * sl + 1])), cdmz[sl]);
+              dmv[2 * sl] = __float_as_uint(a.x);
+              dmv[2 * sl + 1] = __float_as_uint(a.y);
+              dmv[8 + 2 * sl] = __float_as_uint(z.x);
+              dmv[8 + 2 * sl + 1] = __float_as_uint(z.y);
             }
             tm_st16(tm_dm + mtl * 16, dmv);
           }
@@ -1712,24 +1736,24 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
               }
             }
           }
-          if (HZ) {  // dz: BF16 running sum over the ranks in order
-            float2 acc = make_float2(0.f, 0.f);
+          if (HZ) {  // dz: BF16 running sum over the ranks in order (BF16 pair + FP32 pair)
+            uint32_t acc = 0u;
 #pragma unroll
-            for (int k = 0; k < NS; k++) acc = unpack2(pack2(__fadd2_rn(acc, prodz[k])));
+            for (int k = 0; k < NS; k++) acc = pack2(add_bf2_f32(acc, prodz[k]));
             if (R == 8) {  // ranks 0..3 in the even lane, 4..7 in the odd lane
-              float2 acc2 = unpack2(__shfl_xor_sync(0xffffffffu, pack2(acc), 1));
+              uint32_t acc2 = __shfl_xor_sync(0xffffffffu, acc, 1);
 #pragma unroll
-              for (int k = 0; k < NS; k++) acc2 = unpack2(pack2(__fadd2_rn(acc2, prodz[k])));
+              for (int k = 0; k < NS; k++) acc2 = pack2(add_bf2_f32(acc2, prodz[k]));
               if (cq & 1) acc = acc2;
             }
             const bool writer = (R == 8) ? ((cq & 1) != 0) : true;
             if (K::TMA && writer) {  // over the z values this lane pair has read; stored by TMA
-              const uint32_t v = pack2(acc);
+              const uint32_t v = acc;
               uint16_t* zw = const_cast<uint16_t*>(zraw);
               zw[raw_off<K, LDP>(tl, mt * 16 + g)] = (uint16_t)(v & 0xffffu);
               zw[raw_off<K, LDP>(tl, mt * 16 + g + 8)] = (uint16_t)(v >> 16);
             } else if (writer && tg < p.S) {
-              const uint32_t v = pack2(acc);
+              const uint32_t v = acc;
               uint16_t* dzp = p.dz + (((int64_t)b * p.S + tg) * p.H + h) * P + mt * 16 + g;
               dzp[0] = (uint16_t)(v & 0xffffu);
               dzp[8] = (uint16_t)(v >> 16);
