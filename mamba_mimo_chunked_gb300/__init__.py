@@ -22,7 +22,8 @@ import torch
 from . import _build
 
 __all__ = ["MambaMimoBwdFwdOutputs", "mamba_mimo_bwd_fwd", "workspace_size", "load_library",
-           "last_launch_count", "build"]
+           "last_launch_count", "build", "mamba_mimo_bwd_bwd", "bwd_bwd_workspace_size",
+           "BWD_BWD_OUTPUTS"]
 
 build = _build.build
 
@@ -88,6 +89,12 @@ def load_library():
         lib.mamba_mimo_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         lib.mamba_mimo_stage_name.restype = ctypes.c_char_p
         lib.mamba_mimo_stage_name.argtypes = [ctypes.c_int]
+        lib.mamba_mimo_bwd_bwd.restype = ctypes.c_int
+        lib.mamba_mimo_bwd_bwd.argtypes = (
+            [ctypes.POINTER(_Dims)] + [vp] * 17 + [i64, i64] + [vp] * 12 + [vp, ctypes.c_size_t, vp])
+        lib.mamba_mimo_bwd_bwd_workspace_size.restype = ctypes.c_int
+        lib.mamba_mimo_bwd_bwd_workspace_size.argtypes = [
+            ctypes.POINTER(_Dims), i64, i64, ctypes.POINTER(ctypes.c_size_t)]
         _lib = lib
         del f32p
     return _lib
@@ -296,3 +303,100 @@ def _run(dout, q, k, v, q_bias, k_bias, mimo_v, mimo_o, z, mimo_z, angles, da_cs
     if st:
         _raise(lib, st)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Second backward stage (include/mamba_mimo_bwd_bwd.h)
+
+BWD_BWD_OUTPUTS = ("DQ", "DK", "DV", "DMIMO_V", "DANGLES", "DFACTOR", "DGAMMA", "DDA", "DSSDA",
+                   "DDA_CS_REV", "DDA_CS", "DD")
+
+
+def bwd_bwd_workspace_size(B, S, H, G, R, N, P, chunk_size=16, rotary_dim_divisor=4) -> int:
+    """Device workspace bytes of mamba_mimo_bwd_bwd (a query; no GPU needed)."""
+    lib = load_library()
+    nbytes = ctypes.c_size_t(0)
+    st = lib.mamba_mimo_bwd_bwd_workspace_size(ctypes.byref(_Dims(B, S, H, G, R, N, P)), chunk_size,
+                                               rotary_dim_divisor, ctypes.byref(nbytes))
+    if st:
+        _raise(lib, st)
+    return nbytes.value
+
+
+def mamba_mimo_bwd_bwd(dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt,
+                       trap, segsum, angles, mimo_o=None, d=None, chunk_size: int = 16,
+                       rotary_dim_divisor: int = 4, *, workspace: torch.Tensor | None = None) -> dict:
+    """Second Mamba-3 MIMO backward stage on the current CUDA stream.
+
+    Arguments in the pages' order (the first stage's ``states`` and
+    ``qk_dot`` caches among them); ``mimo_o`` selects reduce-O ``dout``
+    ([B,S,H,P]), ``d`` adds the D-skip gradient.  Returns a dict of the 12
+    FP32 gradients (``DD`` is None without ``d``)."""
+    if q.dim() != 5:
+        raise ValueError("q must have shape [B, S, R, G, N]")
+    B, S, R, G, N = q.shape
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q, k, v, dout, states, qk_dot and trap must use torch.bfloat16")
+    if q.device.type != "cuda":
+        raise ValueError("mamba_mimo_bwd_bwd requires CUDA tensors")
+    if rotary_dim_divisor not in (2, 4):
+        raise ValueError("rotary_dim_divisor must be 2 or 4")
+    if N % 2 or N % rotary_dim_divisor:
+        raise ValueError("N must be even and divisible by rotary_dim_divisor")
+    if v.dim() != 4 or tuple(v.shape[:2]) != (B, S):
+        raise ValueError("v must have shape [B, S, H, P]")
+    H, P = v.shape[2:]
+    if H % G:
+        raise ValueError("H must be divisible by G")
+    dev = q.device
+    bf16, f32 = torch.bfloat16, torch.float32
+    nc = (S + chunk_size - 1) // chunk_size
+    _check("k", k, q.shape, bf16, dev)
+    _check("v", v, (B, S, H, P), bf16, dev)
+    _check("q_bias", q_bias, (H, R, N), f32, dev)
+    _check("k_bias", k_bias, (H, R, N), f32, dev)
+    _check("mimo_v", mimo_v, (H, R, P), f32, dev)
+    _check("states", states, (B, H, nc, N, P), bf16, dev)
+    _check("qk_dot", qk_dot, (B, H, S, R, R), bf16, dev)
+    for name, t in (("da_cs", da_cs), ("da_cs_rev", da_cs_rev), ("dt", dt)):
+        _check(name, t, (B, H, S), f32, dev)
+    _check("trap", trap, (B, H, S), bf16, dev)
+    _check("segsum", segsum, (B, H, nc, chunk_size, chunk_size), f32, dev)
+    _check("angles", angles, (B, S, H, N // rotary_dim_divisor), f32, dev)
+    if mimo_o is not None:
+        _check("mimo_o", mimo_o, (H, R, P), f32, dev)
+        _check("dout", dout, (B, S, H, P), bf16, dev)
+    else:
+        _check("dout", dout, (B, S, R, H, P), bf16, dev)
+    if d is not None:
+        _check("d", d, (H,), f32, dev)
+    args = tuple(None if a is None else a.contiguous() for a in (
+        dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt, trap, segsum,
+        angles, mimo_o, d))
+    lib = load_library()
+    outs = {
+        "DQ": torch.empty((B, S * R, H, N), dtype=f32, device=dev),
+        "DK": torch.empty((B, S * R, H, N), dtype=f32, device=dev),
+        "DV": torch.empty((B, S, H, P), dtype=f32, device=dev),
+        "DMIMO_V": torch.empty((B, H, R, P), dtype=f32, device=dev),
+        "DANGLES": torch.empty((B, S, H, N // rotary_dim_divisor), dtype=f32, device=dev),
+        "DFACTOR": torch.empty((B, H, S), dtype=f32, device=dev),
+        "DGAMMA": torch.empty((B, H, S), dtype=f32, device=dev),
+        "DDA": torch.empty((B, H, S), dtype=f32, device=dev),
+        "DSSDA": torch.empty((B, H, nc, chunk_size, chunk_size), dtype=f32, device=dev),
+        "DDA_CS_REV": torch.empty((B, H, S), dtype=f32, device=dev),
+        "DDA_CS": torch.empty((B, H, S), dtype=f32, device=dev),
+        "DD": torch.empty((B, H), dtype=f32, device=dev) if d is not None else None,
+    }
+    nbytes = bwd_bwd_workspace_size(B, S, H, G, R, N, P, chunk_size, rotary_dim_divisor)
+    if workspace is None:
+        workspace = _workspace(dev, nbytes)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        st = lib.mamba_mimo_bwd_bwd(
+            ctypes.byref(_Dims(B, S, H, G, R, N, P)), *[_ptr(a) for a in args], chunk_size,
+            rotary_dim_divisor, *[_ptr(outs[n]) for n in BWD_BWD_OUTPUTS], _ptr(workspace),
+            workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream))
+    if st:
+        _raise(lib, st)
+    return outs

@@ -8,7 +8,10 @@ import subprocess
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 REPO_DIR = os.path.dirname(PKG_DIR)
 SOURCES = [os.path.join(PKG_DIR, "csrc", "mmbf_kernels.cu")]
-HEADERS = [os.path.join(REPO_DIR, "include", "mamba_mimo_bwd_fwd.h")]
+HEADERS = [os.path.join(REPO_DIR, "include", "mamba_mimo_bwd_fwd.h"),
+           os.path.join(REPO_DIR, "include", "mamba_mimo_bwd_bwd.h"),
+           os.path.join(PKG_DIR, "csrc", "mmbf_fast.cuh"),
+           os.path.join(PKG_DIR, "csrc", "mmbb.cuh")]
 LIB_PATH = os.path.join(PKG_DIR, "libmmbf.so")
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -1,0 +1,629 @@
+// Second backward stage of the Mamba-3 MIMO chunked scan (mamba_mimo_bwd_bwd):
+// the reverse scan over chunks and its 12 gradients.  Definition: the page
+// "MindSpeed-Ops PR #100" (op document "mamba3_mimo_bwd_bwd 算子迁移说明" for
+// the interface, dPhiO and PsiV; practice document, sections "输入缓存的语义"
+// for the state and dstates recurrences and the caches, "非整 chunk" for the
+// padding of a partial last chunk); each output is the exact derivative of
+// L = sum dPhiO * out of the first stage's chunk output (readings in
+// include/mamba_mimo_bwd_bwd.h).
+//
+// Four launches per call:
+//   seed_kernel   (chunk, b*h)  G_c = sum_i exp(da_cs[t_i]) q_rot[i]^T dPhiO[i]
+//                               and the chunk decay alpha_c = exp(da_cs[last]);
+//   scan_kernel   (N*P slice, b*h)  D_c = alpha_c D_{c+1} + G_c in reverse
+//                               chunk order; chunk c's slot then holds
+//                               D_{c+1}, the gradient of the state leaving it;
+//   grad_kernel   (chunk, b*h)  every gradient of the chunk from its inputs,
+//                               the state entering it (the states cache) and
+//                               D_{c+1}: 9 products of at most 64 x 64 x 64
+//                               in FP32 tiles in shared memory;
+//   reduce_kernel (b*h)         DMIMO_V and DD: the chunks' partial sums in
+//                               chunk order.
+// FP32 throughout, deterministic (no floating-point atomics).
+
+#include "mamba_mimo_bwd_bwd.h"
+
+namespace mmbf {
+namespace bb {
+
+struct BBParams {
+  int B, S, H, G, R, N, P, C, w, nc, CR, reduced, has_d;
+  const uint16_t *dout, *q, *k, *v, *states, *qk, *trap;
+  const float *q_bias, *k_bias, *mimo_v, *mimo_o, *d, *da_cs, *da_cs_rev, *dt, *segsum, *angles;
+  float *DQ, *DK, *DV, *DMIMO_V, *DANGLES, *DFACTOR, *DGAMMA, *DDA, *DSSDA, *DDA_CS_REV, *DDA_CS, *DD;
+  float* ws_D;      // [BH][nc][N][P]: seeds G_c, then D_{c+1}
+  float* ws_alpha;  // [BH][nc]
+  float* ws_mv;     // [BH][nc][R][P]: DMIMO_V partials
+  float* ws_dd;     // [BH][nc]: DD partials
+};
+
+constexpr int kT = 256;             // threads per CTA
+constexpr int kMax = 64;            // N, P and C*R limit of this path
+constexpr int kLD = kMax + 1;       // FP32 tile row stride
+constexpr int kTile = kMax * kLD;   // floats per tile
+constexpr int kSmall = 4224;        // segsum [C][C], qk [C][R][R], dqk (C*R <= 64, R <= 16)
+constexpr int kRedCols = 16;        // per-row partial sums, one per column block
+
+__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// acc[u][v] += sum_k a(i0+u, k) * b(k, j0+v): a 4 x 4 block of a product of
+// shared-memory tiles (rows and columns past the operands' extents are
+// computed on whatever the tile holds there and never used).
+template <class FA, class FB>
+__device__ __forceinline__ void mm4(float (&acc)[4][4], int i0, int j0, int K, FA a, FB b) {
+  for (int kk = 0; kk < K; kk++) {
+    float av[4], bv[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      av[u] = a(i0 + u, kk);
+      bv[u] = b(kk, j0 + u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int v = 0; v < 4; v++) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+  }
+}
+__device__ __forceinline__ void zero4(float (&acc)[4][4]) {
+#pragma unroll
+  for (int u = 0; u < 4; u++)
+#pragma unroll
+    for (int v = 0; v < 4; v++) acc[u][v] = 0.f;
+}
+
+// Token scalars of chunk c (reading of the op header): gamma, factor,
+// exp(da_cs), exp(da_cs_rev), and whether the token is inside S.
+__device__ void load_tokens(const BBParams& p, int bh, int c, float* gam, float* fac, float* ea, float* er,
+                            float* valid) {
+  for (int t = threadIdx.x; t < p.C; t += kT) {
+    const int tg = c * p.C + t;
+    const int64_t i = (int64_t)bh * p.S + tg;
+    const bool in = tg < p.S, in1 = tg + 1 < p.S;
+    const float dtv = in ? p.dt[i] : 0.f, trv = in ? bf_f(p.trap[i]) : 0.f;
+    const float dtn = in1 ? p.dt[i + 1] : 0.f, trn = in1 ? bf_f(p.trap[i + 1]) : 0.f;
+    const float g = dtv * sigm(trv);
+    gam[t] = g;
+    fac[t] = g + dtn * sigm(-trn);  // 0 shifted part past S and at the last padded position
+    ea[t] = expf(in ? p.da_cs[i] : 0.f);
+    er[t] = expf(in ? p.da_cs_rev[i] : 0.f);
+    valid[t] = in ? 1.f : 0.f;
+  }
+}
+
+// Biased rows of q (or k) of chunk c, then the rotary on the pairs (m, N/2+m),
+// m < w, in place: rows j = t*R + r of a [C*R][N] tile (zero input past S,
+// plus the bias, as the padded reference).
+__device__ void load_rotated(const BBParams& p, int b, int h, int c, const uint16_t* src, const float* bias,
+                             float* T) {
+  const int g = h / (p.H / p.G);
+  for (int e = threadIdx.x; e < p.CR * p.N; e += kT) {
+    const int j = e / p.N, n = e % p.N, t = j / p.R, r = j % p.R, tg = c * p.C + t;
+    float x = bias[((int64_t)h * p.R + r) * p.N + n];
+    if (tg < p.S) x += bf_f(src[((((int64_t)b * p.S + tg) * p.R + r) * p.G + g) * p.N + n]);
+    T[j * kLD + n] = x;
+  }
+  __syncthreads();
+  const int half = p.N / 2;
+  for (int e = threadIdx.x; e < p.CR * p.w; e += kT) {
+    const int j = e / p.w, m = e % p.w, t = j / p.R, tg = c * p.C + t;
+    const float th = tg < p.S ? p.angles[(((int64_t)b * p.S + tg) * p.H + h) * p.w + m] : 0.f;
+    float sn, cs;
+    sincosf(th, &sn, &cs);
+    const float lo = T[j * kLD + m], hi = T[j * kLD + half + m];
+    T[j * kLD + m] = cs * lo - sn * hi;
+    T[j * kLD + half + m] = sn * lo + cs * hi;
+  }
+}
+
+// dPhiO rows [C*R][P] (zero past S) [op document: reduce-O or per rank].
+__device__ void load_dphio(const BBParams& p, int b, int h, int c, float* T) {
+  for (int e = threadIdx.x; e < p.CR * p.P; e += kT) {
+    const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
+    float x = 0.f;
+    if (tg < p.S) {
+      if (p.reduced)
+        x = bf_f(p.dout[(((int64_t)b * p.S + tg) * p.H + h) * p.P + pp]) * p.mimo_o[((int64_t)h * p.R + r) * p.P + pp];
+      else
+        x = bf_f(p.dout[((((int64_t)b * p.S + tg) * p.R + r) * p.H + h) * p.P + pp]);
+    }
+    T[j * kLD + pp] = x;
+  }
+}
+
+// PsiV rows [C*R][P] = v[t,p] * mimo_v[r,p] (zero past S).
+__device__ void load_psi(const BBParams& p, int b, int h, int c, float* T) {
+  for (int e = threadIdx.x; e < p.CR * p.P; e += kT) {
+    const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
+    float x = 0.f;
+    if (tg < p.S)
+      x = bf_f(p.v[(((int64_t)b * p.S + tg) * p.H + h) * p.P + pp]) * p.mimo_v[((int64_t)h * p.R + r) * p.P + pp];
+    T[j * kLD + pp] = x;
+  }
+}
+
+// ---- 1. seeds: G_c[n][p] = sum_i exp(da_cs[t_i]) q_rot[i][n] dPhiO[i][p]
+__global__ void __launch_bounds__(kT, 2) seed_kernel(const BBParams p) {
+  extern __shared__ float smf[];
+  float* Qr = smf;
+  float* Gp = Qr + kTile;
+  float* tk = Gp + kTile;  // gam, fac, ea, er, valid: 5 x kMax
+  const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+  load_tokens(p, bh, c, tk, tk + kMax, tk + 2 * kMax, tk + 3 * kMax, tk + 4 * kMax);
+  load_dphio(p, b, h, c, Gp);
+  load_rotated(p, b, h, c, p.q, p.q_bias, Qr);
+  __syncthreads();
+  const float* ea = tk + 2 * kMax;
+  const int i0 = (threadIdx.x >> 4) * 4, j0 = (threadIdx.x & 15) * 4;
+  float acc[4][4];
+  zero4(acc);
+  mm4(acc, i0, j0, p.CR, [&](int n, int i) { return Qr[i * kLD + n] * ea[i / p.R]; },
+      [&](int i, int pp) { return Gp[i * kLD + pp]; });
+  float* dst = p.ws_D + ((int64_t)bh * p.nc + c) * p.N * p.P;
+#pragma unroll
+  for (int u = 0; u < 4; u++)
+#pragma unroll
+    for (int v = 0; v < 4; v++)
+      if (i0 + u < p.N && j0 + v < p.P) dst[(i0 + u) * p.P + j0 + v] = acc[u][v];
+  if (threadIdx.x == 0) {
+    const int last = min(c * p.C + p.C, p.S) - 1;
+    p.ws_alpha[(int64_t)bh * p.nc + c] = expf(p.da_cs[(int64_t)bh * p.S + last]);
+  }
+}
+
+// ---- 2. reverse scan, one state element per thread: slot c becomes D_{c+1}
+__global__ void __launch_bounds__(128) scan_kernel(const BBParams p) {
+  const int bh = blockIdx.y;
+  const int64_t NP = (int64_t)p.N * p.P;
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= NP) return;
+  float* base = p.ws_D + (int64_t)bh * p.nc * NP + e;
+  const float* al = p.ws_alpha + (int64_t)bh * p.nc;
+  constexpr int GRP = 16;
+  float acc = 0.f;
+  for (int c1 = p.nc - 1; c1 >= 0; c1 -= GRP) {
+    float x[GRP], a[GRP];
+#pragma unroll
+    for (int q = 0; q < GRP; q++) {
+      const int c = c1 - q;
+      x[q] = c >= 0 ? base[(int64_t)c * NP] : 0.f;
+      a[q] = c >= 0 ? al[c] : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < GRP; q++) {
+      const int c = c1 - q;
+      if (c >= 0) {
+        base[(int64_t)c * NP] = acc;
+        acc = fmaf(a[q], acc, x[q]);
+      }
+    }
+  }
+}
+
+// ---- 3. every gradient of one chunk
+__global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
+  extern __shared__ float smf[];
+  float* Qr = smf;              // rotated q rows
+  float* Kr = Qr + kTile;       // rotated k rows
+  float* Ps = Kr + kTile;       // PsiV
+  float* Gp = Ps + kTile;       // dPhiO
+  float* Hc = Gp + kTile;       // state entering the chunk [N][P]
+  float* Dn = Hc + kTile;       // gradient of the state leaving it [N][P]
+  float* M1 = Dn + kTile;       // A, then (kept) for the segsum gradient
+  float* M2 = M1 + kTile;       // dA, then dS
+  float* dQ = M2 + kTile;       // gradient of q_rot
+  float* dK = dQ + kTile;       // gradient of k_scaled
+  float* dP = dK + kTile;       // gradient of PsiV
+  float* sm = dP + kTile;       // segsum [C][C] | qk [C][R][R] | dqk [C][R][R]
+  float* tk = sm + kSmall;      // gam | fac | ea | er | valid, kMax each
+  float* red = tk + 5 * kMax;   // [kMax][kRedCols] row partials
+  float* gam = tk;
+  float* fac = tk + kMax;
+  float* ea = tk + 2 * kMax;
+  float* er = tk + 3 * kMax;
+  float* valid = tk + 4 * kMax;
+  const int C = p.C, R = p.R, N = p.N, P = p.P, CR = p.CR;
+  float* seg = sm;
+  float* qk = sm + C * C;
+  float* dqk = qk + C * R * R;
+  const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+  const int tid = threadIdx.x, i0 = (tid >> 4) * 4, j0 = (tid & 15) * 4;
+
+  // ---- inputs of the chunk
+  load_tokens(p, bh, c, gam, fac, ea, er, valid);
+  for (int e = tid; e < C * C; e += kT) seg[e] = p.segsum[((int64_t)bh * p.nc + c) * C * C + e];
+  for (int e = tid; e < C * R * R; e += kT) {
+    const int tg = c * C + e / (R * R);
+    qk[e] = tg < p.S ? bf_f(p.qk[((int64_t)bh * p.S + tg) * R * R + e % (R * R)]) : 0.f;
+  }
+  for (int e = tid; e < N * P; e += kT) {
+    Hc[(e / P) * kLD + e % P] = bf_f(p.states[((int64_t)bh * p.nc + c) * N * P + e]);
+    Dn[(e / P) * kLD + e % P] = p.ws_D[((int64_t)bh * p.nc + c) * N * P + e];
+  }
+  load_psi(p, b, h, c, Ps);
+  load_dphio(p, b, h, c, Gp);
+  load_rotated(p, b, h, c, p.q, p.q_bias, Qr);
+  load_rotated(p, b, h, c, p.k, p.k_bias, Kr);
+  __syncthreads();
+
+  // ---- A = mask(q_rot k_scaled^T) exp(segsum): selected, never multiplied by
+  //      a mask (padded rows and the upper triangle never reach a product)
+  auto tok_ok = [&](int i, int j) { return (i / R) > (j / R) && valid[i / R] != 0.f; };
+  {
+    float acc[4][4];
+    zero4(acc);
+    mm4(acc, i0, j0, N, [&](int i, int n) { return Qr[i * kLD + n]; }, [&](int n, int j) { return Kr[j * kLD + n]; });
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int v = 0; v < 4; v++) {
+        const int i = i0 + u, j = j0 + v;
+        if (i < CR && j < CR)
+          M1[i * kLD + j] = tok_ok(i, j) ? acc[u][v] * fac[j / R] * expf(seg[(i / R) * C + j / R]) : 0.f;
+      }
+  }
+  __syncthreads();
+
+  // ---- dPsiV = A^T dPhiO + k_state D_{c+1} + d dPhiO + gamma qk^T dPhiO (diagonal);
+  //      dA = dPhiO PsiV^T
+  {
+    float acc[4][4];
+    zero4(acc);
+    mm4(acc, i0, j0, CR, [&](int j, int i) { return M1[i * kLD + j]; }, [&](int i, int pp) { return Gp[i * kLD + pp]; });
+    float acc2[4][4];
+    zero4(acc2);
+    mm4(acc2, i0, j0, N, [&](int j, int n) { return Kr[j * kLD + n]; }, [&](int n, int pp) { return Dn[n * kLD + pp]; });
+    const float dv = p.has_d ? p.d[h] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int v = 0; v < 4; v++) {
+        const int j = i0 + u, pp = j0 + v;
+        if (j < CR && pp < P) {
+          const int t = j / R, r = j % R;
+          float x = acc[u][v] + acc2[u][v] * fac[t] * er[t] + dv * Gp[j * kLD + pp];
+          float dg = 0.f;
+          for (int o = 0; o < R; o++) dg = fmaf(qk[(t * R + o) * R + r], Gp[(t * R + o) * kLD + pp], dg);
+          dP[j * kLD + pp] = fmaf(gam[t], dg, x);
+        }
+      }
+    zero4(acc);
+    mm4(acc, i0, j0, P, [&](int i, int pp) { return Gp[i * kLD + pp]; }, [&](int pp, int j) { return Ps[j * kLD + pp]; });
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int v = 0; v < 4; v++)
+        if (i0 + u < CR && j0 + v < CR) M2[(i0 + u) * kLD + j0 + v] = acc[u][v];
+  }
+  __syncthreads();
+
+  // ---- DSSDA[ti][tj] = sum over the token pair's rank pairs of dA * A
+  for (int e = tid; e < C * C; e += kT) {
+    const int ti = e / C, tj = e % C;
+    float s = 0.f;
+    if (ti > tj && valid[ti] != 0.f)
+      for (int o = 0; o < R; o++)
+        for (int r = 0; r < R; r++) s = fmaf(M2[(ti * R + o) * kLD + tj * R + r], M1[(ti * R + o) * kLD + tj * R + r], s);
+    p.DSSDA[((int64_t)bh * p.nc + c) * C * C + e] = (valid[tj] != 0.f) ? s : 0.f;
+  }
+  __syncthreads();
+  // dS = dA exp(segsum) on the causal entries (in place)
+  for (int e = tid; e < CR * CR; e += kT) {
+    const int i = e / CR, j = e % CR;
+    M2[i * kLD + j] = tok_ok(i, j) ? M2[i * kLD + j] * expf(seg[(i / R) * C + j / R]) : 0.f;
+  }
+  __syncthreads();
+
+  // ---- dq_rot = dS k_scaled + exp(da_cs) dPhiO Hc^T;
+  //      dk_scaled = dS^T q_rot + exp(da_cs_rev) dk_state, dk_state = PsiV Dn^T;
+  //      row sums for DDA_CS_REV (dk_state * k_state) and DDA_CS (inter * dPhiO)
+  {
+    float acc[4][4];
+    zero4(acc);
+    mm4(acc, i0, j0, CR, [&](int i, int j) { return M2[i * kLD + j] * fac[j / R]; },
+        [&](int j, int n) { return Kr[j * kLD + n]; });
+    float acc2[4][4];
+    zero4(acc2);
+    mm4(acc2, i0, j0, P, [&](int i, int pp) { return Gp[i * kLD + pp]; }, [&](int pp, int n) { return Hc[n * kLD + pp]; });
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+#pragma unroll
+      for (int v = 0; v < 4; v++)
+        if (i0 + u < CR && j0 + v < N) dQ[(i0 + u) * kLD + j0 + v] = fmaf(ea[(i0 + u) / R], acc2[u][v], acc[u][v]);
+    // dk_state and its row sums with k_state = k_rot * factor * exp(da_cs_rev)
+    zero4(acc);
+    mm4(acc, i0, j0, P, [&](int j, int pp) { return Ps[j * kLD + pp]; }, [&](int pp, int n) { return Dn[n * kLD + pp]; });
+    zero4(acc2);
+    mm4(acc2, i0, j0, CR, [&](int j, int i) { return M2[i * kLD + j]; }, [&](int i, int n) { return Qr[i * kLD + n]; });
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int j = i0 + u;
+      float rs = 0.f;
+#pragma unroll
+      for (int v = 0; v < 4; v++) {
+        const int n = j0 + v;
+        if (j < CR && n < N) {
+          const int t = j / R;
+          rs = fmaf(acc[u][v], Kr[j * kLD + n] * fac[t] * er[t], rs);
+          dK[j * kLD + n] = fmaf(er[t], acc[u][v], acc2[u][v]);
+        }
+      }
+      if (j < kMax) red[j * kRedCols + (tid & 15)] = rs;
+    }
+  }
+  __syncthreads();
+  for (int t = tid; t < C; t += kT) {  // DDA_CS_REV
+    float s = 0.f;
+    for (int r = 0; r < R; r++)
+      for (int q = 0; q < kRedCols; q++) s += red[(t * R + r) * kRedCols + q];
+    const int tg = c * C + t;
+    if (tg < p.S) p.DDA_CS_REV[(int64_t)bh * p.S + tg] = s;
+  }
+  __syncthreads();
+  {  // inter = exp(da_cs) q_rot Hc and its row sums with dPhiO (DDA_CS)
+    float acc[4][4];
+    zero4(acc);
+    mm4(acc, i0, j0, N, [&](int i, int n) { return Qr[i * kLD + n]; }, [&](int n, int pp) { return Hc[n * kLD + pp]; });
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int i = i0 + u;
+      float rs = 0.f;
+#pragma unroll
+      for (int v = 0; v < 4; v++)
+        if (i < CR && j0 + v < P) rs = fmaf(acc[u][v] * ea[i / R], Gp[i * kLD + j0 + v], rs);
+      if (i < kMax) red[i * kRedCols + (tid & 15)] = rs;
+    }
+  }
+  // same-token terms: dot[t,o,r] = dPhiO[(t,o)] . PsiV[(t,r)] -> dqk = gamma dot,
+  // DGAMMA = sum qk * dot
+  for (int e = tid; e < C * R * R; e += kT) {
+    const int t = e / (R * R), o = (e / R) % R, r = e % R;
+    float s = 0.f;
+    for (int pp = 0; pp < P; pp++) s = fmaf(Gp[(t * R + o) * kLD + pp], Ps[(t * R + r) * kLD + pp], s);
+    dqk[e] = s;  // gamma applied below
+  }
+  __syncthreads();
+  for (int t = tid; t < C; t += kT) {
+    float s = 0.f, g = 0.f;
+    for (int r = 0; r < R; r++)
+      for (int q = 0; q < kRedCols; q++) s += red[(t * R + r) * kRedCols + q];
+    for (int e = 0; e < R * R; e++) g = fmaf(qk[t * R * R + e], dqk[t * R * R + e], g);
+    const int tg = c * C + t;
+    if (tg < p.S) {
+      p.DDA_CS[(int64_t)bh * p.S + tg] = s;
+      p.DGAMMA[(int64_t)bh * p.S + tg] = g;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < C * R * R; e += kT) dqk[e] *= gam[e / (R * R)];
+  // DFACTOR = sum dk_scaled * k_rot per token
+  for (int t = tid; t < C; t += kT) {
+    float s = 0.f;
+    for (int r = 0; r < R; r++)
+      for (int n = 0; n < N; n++) s = fmaf(dK[(t * R + r) * kLD + n], Kr[(t * R + r) * kLD + n], s);
+    const int tg = c * C + t;
+    if (tg < p.S) p.DFACTOR[(int64_t)bh * p.S + tg] = s;
+  }
+  // DDA at the chunk's last valid token: alpha_c * <Hc, D_{c+1}>; DD partial
+  if (tid < 32) {
+    float s = 0.f, dd = 0.f;
+    for (int e = tid; e < N * P; e += 32) s = fmaf(Hc[(e / P) * kLD + e % P], Dn[(e / P) * kLD + e % P], s);
+    for (int e = tid; e < CR * P; e += 32) dd = fmaf(Gp[(e / P) * kLD + e % P], Ps[(e / P) * kLD + e % P], dd);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, o);
+      dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    }
+    if (tid == 0) {
+      const int last = min(c * C + C, p.S) - 1;
+      for (int t = 0; t < C; t++) {
+        const int tg = c * C + t;
+        if (tg < p.S)
+          p.DDA[(int64_t)bh * p.S + tg] = (tg == last) ? p.ws_alpha[(int64_t)bh * p.nc + c] * s : 0.f;
+      }
+      p.ws_dd[(int64_t)bh * p.nc + c] = dd;
+    }
+  }
+  __syncthreads();
+
+  // ---- rotary post-pass: DQ / DK (transposed rotation + the diagonal's
+  //      same-token q.k terms on the un-rotated biased rows), DANGLES
+  const int half = N / 2, g = h / (p.H / p.G);
+  for (int e = tid; e < CR * N; e += kT) {
+    const int j = e / N, n = e % N, t = j / R, r = j % R, tg = c * C + t;
+    if (tg >= p.S) continue;
+    int m = -1;
+    bool lo = false;
+    if (n < p.w) { m = n; lo = true; }
+    else if (n >= half && n < half + p.w) { m = n - half; }
+    float dq = dQ[j * kLD + n], dk = dK[j * kLD + n] * fac[t];
+    if (m >= 0) {
+      float sn, cs;
+      sincosf(p.angles[(((int64_t)b * p.S + tg) * p.H + h) * p.w + m], &sn, &cs);
+      const float qlo = dQ[j * kLD + m], qhi = dQ[j * kLD + half + m];
+      const float klo = dK[j * kLD + m] * fac[t], khi = dK[j * kLD + half + m] * fac[t];
+      dq = lo ? cs * qlo + sn * qhi : -sn * qlo + cs * qhi;
+      dk = lo ? cs * klo + sn * khi : -sn * klo + cs * khi;
+    }
+    // diagonal: qk[t,o,r] = qh[(t,o)] . kh[(t,r)]
+    for (int x = 0; x < R; x++) {
+      const int64_t src = ((((int64_t)b * p.S + tg) * R + x) * p.G + g) * N + n;
+      const float kh = bf_f(p.k[src]) + p.k_bias[((int64_t)h * R + x) * N + n];
+      const float qh = bf_f(p.q[src]) + p.q_bias[((int64_t)h * R + x) * N + n];
+      dq = fmaf(dqk[(t * R + r) * R + x], kh, dq);   // row j = (t, o = r) of q
+      dk = fmaf(dqk[(t * R + x) * R + r], qh, dk);   // row j = (t, r) of k
+    }
+    const int64_t o = (((int64_t)b * p.S + tg) * R + r) * p.H + h;
+    p.DQ[o * N + n] = dq;
+    p.DK[o * N + n] = dk;
+  }
+  for (int e = tid; e < C * p.w; e += kT) {
+    const int t = e / p.w, m = e % p.w, tg = c * C + t;
+    if (tg >= p.S) continue;
+    float s = 0.f;
+    for (int r = 0; r < R; r++) {
+      const int j = t * R + r;
+      s += dQ[j * kLD + m] * (-Qr[j * kLD + half + m]) + dQ[j * kLD + half + m] * Qr[j * kLD + m];
+      s += dK[j * kLD + m] * fac[t] * (-Kr[j * kLD + half + m]) + dK[j * kLD + half + m] * fac[t] * Kr[j * kLD + m];
+    }
+    p.DANGLES[(((int64_t)b * p.S + tg) * p.H + h) * p.w + m] = s;
+  }
+  // DV and the DMIMO_V partial of the chunk
+  for (int e = tid; e < C * P; e += kT) {
+    const int t = e / P, pp = e % P, tg = c * C + t;
+    if (tg >= p.S) continue;
+    float s = 0.f;
+    for (int r = 0; r < R; r++) s = fmaf(dP[(t * R + r) * kLD + pp], p.mimo_v[((int64_t)h * R + r) * P + pp], s);
+    p.DV[(((int64_t)b * p.S + tg) * p.H + h) * P + pp] = s;
+  }
+  for (int e = tid; e < R * P; e += kT) {
+    const int r = e / P, pp = e % P;
+    float s = 0.f;
+    for (int t = 0; t < C; t++) {
+      const int tg = c * C + t;
+      if (tg < p.S) s = fmaf(dP[(t * R + r) * kLD + pp], bf_f(p.v[(((int64_t)b * p.S + tg) * p.H + h) * P + pp]), s);
+    }
+    p.ws_mv[((int64_t)bh * p.nc + c) * R * P + e] = s;
+  }
+}
+
+// ---- 4. DMIMO_V and DD: the chunks' partials in chunk order
+__global__ void __launch_bounds__(kT) reduce_kernel(const BBParams p) {
+  const int bh = blockIdx.x;
+  for (int e = threadIdx.x; e < p.R * p.P; e += kT) {
+    float s = 0.f;
+    for (int c = 0; c < p.nc; c++) s += p.ws_mv[((int64_t)bh * p.nc + c) * p.R * p.P + e];
+    p.DMIMO_V[(int64_t)bh * p.R * p.P + e] = s;
+  }
+  if (p.has_d && threadIdx.x == 0) {
+    float s = 0.f;
+    for (int c = 0; c < p.nc; c++) s += p.ws_dd[(int64_t)bh * p.nc + c];
+    p.DD[bh] = s;
+  }
+}
+
+constexpr size_t kSeedSmem = (2 * kTile + 5 * kMax) * sizeof(float);
+constexpr size_t kGradSmem = (11 * kTile + kSmall + 5 * kMax + kMax * kRedCols) * sizeof(float);
+
+static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace carve-up (bytes): D, alpha, DMIMO_V partials, DD partials.
+static size_t bb_workspace(const BBParams& p, size_t* off) {
+  const size_t BH = (size_t)p.B * p.H, nc = (size_t)p.nc;
+  size_t o = 0;
+  off[0] = o; o += a256(BH * nc * p.N * p.P * 4);
+  off[1] = o; o += a256(BH * nc * 4);
+  off[2] = o; o += a256(BH * nc * p.R * p.P * 4);
+  off[3] = o; o += a256(BH * nc * 4);
+  return o;
+}
+
+static mmbf_status bb_plan(const mmbf_dims* dims, int64_t chunk_size, int64_t div, BBParams* out) {
+  if (!dims) return fail(MMBF_ERR_ARG, "dims is NULL");
+  const mmbf_dims& d = *dims;
+  if (d.B < 1 || d.S < 1 || d.H < 1 || d.G < 1 || d.R < 1 || d.N < 1 || d.P < 1 || chunk_size < 1)
+    return fail(MMBF_ERR_SHAPE, "every dimension and chunk_size must be positive");
+  if (d.H % d.G) return fail(MMBF_ERR_SHAPE, "H (%lld) must be a multiple of G (%lld)", (long long)d.H, (long long)d.G);
+  if (div != 2 && div != 4) return fail(MMBF_ERR_SHAPE, "rotary_dim_divisor must be 2 or 4");
+  if (d.N % 2 || d.N % div) return fail(MMBF_ERR_SHAPE, "N must be even and a multiple of rotary_dim_divisor");
+  if (d.N > kMax || d.P > kMax || chunk_size * d.R > kMax || d.R > 16)
+    return fail(MMBF_ERR_UNSUPPORTED, "this build of the second stage needs N, P, C*R <= %d and R <= 16", kMax);
+  if (d.S > (1 << 30) || d.B * d.H > 65535) return fail(MMBF_ERR_UNSUPPORTED, "S > 2^30 or B*H > 65535");
+  BBParams p = {};
+  p.B = (int)d.B; p.S = (int)d.S; p.H = (int)d.H; p.G = (int)d.G; p.R = (int)d.R; p.N = (int)d.N; p.P = (int)d.P;
+  p.C = (int)chunk_size;
+  p.w = (int)(d.N / div);
+  p.nc = (int)((d.S + chunk_size - 1) / chunk_size);
+  p.CR = p.C * p.R;
+  *out = p;
+  return MMBF_OK;
+}
+
+}  // namespace bb
+}  // namespace mmbf
+
+extern "C" {
+
+mmbf_status mamba_mimo_bwd_bwd_workspace_size(const mmbf_dims* dims, int64_t chunk_size, int64_t rotary_dim_divisor,
+                                              size_t* bytes) {
+  using namespace mmbf::bb;
+  BBParams p;
+  mmbf_status s = bb_plan(dims, chunk_size, rotary_dim_divisor, &p);
+  if (s != MMBF_OK) return s;
+  if (!bytes) return fail(MMBF_ERR_ARG, "bytes is NULL");
+  size_t off[4];
+  *bytes = bb_workspace(p, off);
+  return MMBF_OK;
+}
+
+mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const void* q, const void* k, const void* v,
+                               const float* q_bias, const float* k_bias, const float* mimo_v, const void* states,
+                               const void* qk_dot, const float* da_cs, const float* da_cs_rev, const float* dt,
+                               const void* trap, const float* segsum, const float* angles, const float* mimo_o,
+                               const float* d, int64_t chunk_size, int64_t rotary_dim_divisor, float* DQ, float* DK,
+                               float* DV, float* DMIMO_V, float* DANGLES, float* DFACTOR, float* DGAMMA, float* DDA,
+                               float* DSSDA, float* DDA_CS_REV, float* DDA_CS, float* DD, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  using namespace mmbf::bb;
+  BBParams p;
+  mmbf_status s = bb_plan(dims, chunk_size, rotary_dim_divisor, &p);
+  if (s != MMBF_OK) return s;
+  const void* req[] = {dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt, trap, segsum, angles,
+                       DQ, DK, DV, DMIMO_V, DANGLES, DFACTOR, DGAMMA, DDA, DSSDA, DDA_CS_REV, DDA_CS};
+  for (const void* x : req)
+    if (!x) return fail(MMBF_ERR_ARG, "a required pointer is NULL");
+  if ((d == nullptr) != (DD == nullptr)) return fail(MMBF_ERR_ARG, "DD must be given exactly when d is");
+  const void* all[] = {dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt, trap, segsum,
+                       angles, mimo_o, d, DQ, DK, DV, DMIMO_V, DANGLES, DFACTOR, DGAMMA, DDA, DSSDA, DDA_CS_REV, DDA_CS, DD};
+  for (const void* x : all)
+    if (x && (reinterpret_cast<uintptr_t>(x) & 3)) return fail(MMBF_ERR_ALIGN, "tensor pointers must be 4-byte aligned");
+  size_t off[4];
+  const size_t need = bb_workspace(p, off);
+  if (!workspace || workspace_bytes < need)
+    return fail(MMBF_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(MMBF_ERR_ALIGN, "workspace must be 256-byte aligned");
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.states = static_cast<const uint16_t*>(states);
+  p.qk = static_cast<const uint16_t*>(qk_dot);
+  p.trap = static_cast<const uint16_t*>(trap);
+  p.q_bias = q_bias; p.k_bias = k_bias; p.mimo_v = mimo_v; p.mimo_o = mimo_o; p.d = d;
+  p.da_cs = da_cs; p.da_cs_rev = da_cs_rev; p.dt = dt; p.segsum = segsum; p.angles = angles;
+  p.reduced = mimo_o != nullptr;
+  p.has_d = d != nullptr;
+  p.DQ = DQ; p.DK = DK; p.DV = DV; p.DMIMO_V = DMIMO_V; p.DANGLES = DANGLES; p.DFACTOR = DFACTOR;
+  p.DGAMMA = DGAMMA; p.DDA = DDA; p.DSSDA = DSSDA; p.DDA_CS_REV = DDA_CS_REV; p.DDA_CS = DDA_CS; p.DD = DD;
+  p.ws_D = reinterpret_cast<float*>(ws + off[0]);
+  p.ws_alpha = reinterpret_cast<float*>(ws + off[1]);
+  p.ws_mv = reinterpret_cast<float*>(ws + off[2]);
+  p.ws_dd = reinterpret_cast<float*>(ws + off[3]);
+
+  static int smem_set = 0;
+  cudaError_t e = cudaSuccess;
+  if (!smem_set) {
+    e = cudaFuncSetAttribute(seed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeedSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
+    if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "shared-memory attribute: %s", cudaGetErrorString(e));
+    smem_set = 1;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = p.B * p.H;
+  int launches = 0;
+  seed_kernel<<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
+  launches++;
+  scan_kernel<<<dim3((p.N * p.P + 127) / 128, BH), 128, 0, st>>>(p);
+  launches++;
+  grad_kernel<<<dim3(p.nc, BH), kT, kGradSmem, st>>>(p);
+  launches++;
+  reduce_kernel<<<BH, kT, 0, st>>>(p);
+  launches++;
+  e = cudaGetLastError();
+  g_launches = launches;
+  if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "launching the second stage: %s", cudaGetErrorString(e));
+  return MMBF_OK;
+}
+
+}  // extern "C"

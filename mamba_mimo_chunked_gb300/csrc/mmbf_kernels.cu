@@ -1603,3 +1603,6 @@ const char* mamba_mimo_stage_name(int i) {
 }
 
 }  // extern "C"
+
+// The second backward stage (its own kernels and C entry points).
+#include "mmbb.cuh"

@@ -192,3 +192,17 @@ def head_slice(inputs: dict, b: int, h: int) -> dict:
         if inputs[n] is not None:
             out[n] = inputs[n][h:h + 1].contiguous()
     return out
+
+
+def make_stage1_caches(*, B, S, H, R, N, P, C, seed, device="cpu") -> tuple:
+    """Seeded stand-ins for the first stage's caches that the second stage
+    reads as given inputs: states [B,H,nchunks,N,P] ~ N(0, 1) and qk_dot
+    [B,H,S,R,R] ~ N(0, N), both stored as BF16 (the first stage's output
+    dtype).  For tests and benchmarks at sizes where the caches are not
+    derived from a forward pass."""
+    dev = torch.device(device)
+    g = _gen(seed, dev)
+    nc = (S + C - 1) // C
+    states = torch.randn((B, H, nc, N, P), generator=g, device=dev).to(torch.bfloat16)
+    qk = (torch.randn((B, H, S, R, R), generator=g, device=dev) * math.sqrt(N)).to(torch.bfloat16)
+    return states, qk

@@ -13,7 +13,7 @@ import mamba_mimo_chunked_gb300 as mm
 import synthetic_inputs as si
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mamba_mimo_bwd_fwd.h")
+HEADERS = [os.path.join(ROOT, "include", n) for n in ("mamba_mimo_bwd_fwd.h", "mamba_mimo_bwd_bwd.h")]
 
 
 @pytest.fixture(scope="module")
@@ -23,14 +23,17 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mamba_mimo_\w+)\s*\(", text)))
+    names = set()
+    for path in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names |= set(re.findall(r"\b(mamba_mimo_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert "mamba_mimo_bwd_fwd" in names and "mamba_mimo_bwd_fwd_workspace_size" in names
+    assert "mamba_mimo_bwd_bwd" in names and "mamba_mimo_bwd_bwd_workspace_size" in names
     for name in names:
         assert hasattr(lib, name), name
     assert lib.mamba_mimo_abi_version() == 1
@@ -136,3 +139,54 @@ def test_device_status_without_a_call_is_ok(lib):
     t.start()
     t.join()
     assert res == [0]
+
+
+# ---- second backward stage: host-side validation (nothing reaches a GPU)
+
+def bb_ws(lib, d, C=16, div=4):
+    n = ctypes.c_size_t(0)
+    st = lib.mamba_mimo_bwd_bwd_workspace_size(ctypes.byref(d), C, div, ctypes.byref(n))
+    return st, n.value, lib.mamba_mimo_last_error().decode()
+
+
+def test_bwd_bwd_workspace_query_and_envelope(lib):
+    st, n, _ = bb_ws(lib, dims())
+    # dstates [BH][nc][N][P] + decays + DMIMO_V and DD partials, FP32
+    nc = 8192 // 16
+    assert st == 0 and n >= 16 * nc * (64 * 64 + 1 + 4 * 64 + 1) * 4
+    for d, C, div, code, msg in [
+        (dims(B=0), 16, 4, 1, "must be positive"),
+        (dims(H=6, G=4), 16, 4, 1, "multiple of G"),
+        (dims(), 16, 3, 1, "rotary_dim_divisor"),
+        (dims(N=66), 16, 4, 1, "N must be even"),
+        (dims(N=128), 16, 4, 3, "N, P, C*R <= 64"),
+        (dims(), 32, 4, 3, "N, P, C*R <= 64"),
+    ]:
+        st, _, err = bb_ws(lib, d, C, div)
+        assert st == code and msg in err, (st, err)
+
+
+def test_bwd_bwd_rejects_bad_pointer_patterns_without_gpu(lib):
+    d = dims(S=64, H=2, R=2, N=16, P=16)
+    fake = ctypes.c_void_p(0x1000)
+
+    def call(ins, outs, ws_bytes=1 << 30, ws_ptr=fake):
+        return lib.mamba_mimo_bwd_bwd(ctypes.byref(d), *ins, 16, 4, *outs, ws_ptr, ws_bytes, None)
+
+    ins = [fake] * 17
+    outs = [fake] * 12
+    # DD without d
+    ins2 = list(ins)
+    ins2[16] = None
+    assert call(ins2, outs) == 2 and "DD must be given" in lib.mamba_mimo_last_error().decode()
+    # a required input missing
+    ins2 = list(ins)
+    ins2[7] = None
+    assert call(ins2, outs) == 2
+    # misaligned pointer
+    ins2 = list(ins)
+    ins2[3] = ctypes.c_void_p(0x1002)
+    assert call(ins2, outs) == 4
+    # workspace too small / misaligned
+    assert call(ins, outs, ws_bytes=16) == 5
+    assert call(ins, outs, ws_ptr=ctypes.c_void_p(0x1010)) == 4

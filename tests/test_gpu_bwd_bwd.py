@@ -1,0 +1,110 @@
+"""GPU parity of the second backward stage (mamba_mimo_bwd_bwd) against the
+float64 oracle (oracle/bwd_bwd.py), through the C ABI and its binding.
+
+Both sides read the same inputs (BF16 q/k/v/dout/trap and caches, FP32 the
+rest).  The oracle computes in float64, the kernels in FP32 (products of at
+most 64 terms, a reverse scan over chunks with decays below one), so every
+output is held to a relative RMS error below 1e-4; DDA and DANGLES, whose
+entries can sit near zero, also to a max-abs error below 1e-3 of their
+largest entry (the pages' global relative criterion for those two).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import mamba_mimo_chunked_gb300 as mm
+import synthetic_inputs as si
+from oracle import bwd_bwd as bb
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ("dout", "q", "k", "v", "q_bias", "k_bias", "mimo_v", "mimo_o", "d", "da_cs", "da_cs_rev", "dt",
+        "trap", "segsum", "angles")
+
+
+def _problem(B, S, H, G, R, N, P, C, div=4, reduced=True, has_d=True, seed=0, caches="forward"):
+    inp = si.make_inputs(B=B, S=S, H=H, G=G, R=R, N=N, P=P, C=C, div=div, reduced=reduced, has_z=False,
+                         has_d=has_d, seed=seed, recipe="workload")
+    if caches == "forward":  # the caches a forward pass leaves (float64, stored as BF16)
+        a = {k: bb._f64(inp[k]) for k in KEYS}
+        nc = (S + C - 1) // C
+        st = np.zeros((B, H, nc, N, P))
+        qk = np.zeros((B, H, S, R, R))
+        for b in range(B):
+            for h in range(H):
+                _, s_, q_, _ = bb.forward(a, b, h, C, div)
+                st[b, h], qk[b, h] = s_, q_[:S]
+        states = torch.from_numpy(st).to(torch.bfloat16)
+        qk_dot = torch.from_numpy(qk).to(torch.bfloat16)
+    else:
+        states, qk_dot = si.make_stage1_caches(B=B, S=S, H=H, R=R, N=N, P=P, C=C, seed=seed + 1)
+    args = (inp["dout"], inp["q"], inp["k"], inp["v"], inp["q_bias"], inp["k_bias"], inp["mimo_v"], states,
+            qk_dot, inp["da_cs"], inp["da_cs_rev"], inp["dt"], inp["trap"], inp["segsum"], inp["angles"])
+    kw = dict(mimo_o=inp["mimo_o"], d=inp["d"], chunk_size=C, rotary_dim_divisor=div)
+    return args, kw
+
+
+def _run_gpu(args, kw):
+    dev = torch.device("cuda:0")
+    g = mm.mamba_mimo_bwd_bwd(*[a.to(dev) for a in args],
+                              **{k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in kw.items()})
+    torch.cuda.synchronize(dev)
+    return g
+
+
+def _compare(got, want):
+    for name in bb.OUTPUT_NAMES:
+        w = want[name]
+        if w is None:
+            assert got[name] is None, name
+            continue
+        g = got[name].double().cpu().numpy()
+        assert g.shape == w.shape, (name, g.shape, w.shape)
+        assert np.all(np.isfinite(g)), name
+        scale = np.sqrt(np.mean(w ** 2))
+        err = np.sqrt(np.mean((g - w) ** 2)) / max(scale, 1e-30)
+        assert err < 1e-4, f"{name}: relative RMS {err:.3e}"
+        if name in ("DDA", "DANGLES"):
+            m = np.max(np.abs(g - w)) / max(np.max(np.abs(w)), 1e-30)
+            assert m < 1e-3, f"{name}: max-abs relative {m:.3e}"
+
+
+CASES = [
+    dict(B=1, S=40, H=2, G=1, R=4, N=64, P=64, C=16, div=4, reduced=True, has_d=True),    # the timed family, tail 8
+    dict(B=2, S=33, H=2, G=2, R=2, N=32, P=32, C=16, div=2, reduced=False, has_d=False),  # per-rank dout, no D
+    dict(B=1, S=100, H=1, G=1, R=1, N=16, P=16, C=64, div=4, reduced=True, has_d=True),   # R = 1, C*R = 64
+    dict(B=1, S=20, H=2, G=1, R=8, N=32, P=16, C=8, div=4, reduced=True, has_d=True),     # R = 8
+    dict(B=1, S=9, H=2, G=1, R=16, N=16, P=8, C=4, div=2, reduced=False, has_d=True),     # R = 16
+    dict(B=1, S=48, H=4, G=2, R=4, N=32, P=32, C=16, div=4, reduced=True, has_d=True),    # GQA
+    dict(B=1, S=1, H=1, G=1, R=4, N=64, P=64, C=16, div=4, reduced=True, has_d=True),     # one token
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"S{c['S']}_R{c['R']}_N{c['N']}_C{c['C']}")
+def test_parity_with_forward_caches(case):
+    args, kw = _problem(**case, seed=21)
+    want = bb.bwd_bwd(*args, **kw)
+    _compare(_run_gpu(args, kw), want)
+
+
+def test_parity_timed_shape_all_heads():
+    # B1 S8192 H16 R4 N=P=64 C16: given caches (seeded stand-ins); every head
+    args, kw = _problem(B=1, S=8192, H=16, G=1, R=4, N=64, P=64, C=16, seed=5, caches="random")
+    want = bb.bwd_bwd(*args, **kw)
+    _compare(_run_gpu(args, kw), want)
+
+
+def test_deterministic_and_four_launches():
+    args, kw = _problem(B=1, S=200, H=2, G=1, R=4, N=64, P=64, C=16, seed=3, caches="random")
+    g1 = _run_gpu(args, kw)
+    assert mm.last_launch_count() == 4
+    g2 = _run_gpu(args, kw)
+    for name in bb.OUTPUT_NAMES:
+        assert torch.equal(g1[name], g2[name]), name
+
+
+def test_outside_the_envelope_raises():
+    args, kw = _problem(B=1, S=16, H=1, G=1, R=2, N=128, P=16, C=16, seed=1, caches="random")
+    with pytest.raises(NotImplementedError):
+        _run_gpu(args, kw)
