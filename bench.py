@@ -11,6 +11,10 @@ with a barrier and synchronize on both sides; under torchrun every rank runs
 its own replica and the slowest rank's time counts.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
+
+``--op bwd_bwd`` instead times the second backward stage (mamba_mimo_bwd_bwd)
+on the same shape and prints its own line (metric, FP32-ALU roofline of its
+gradient kernel, CPU-oracle baseline on a sample of heads).
 """
 
 from __future__ import annotations
@@ -62,6 +66,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--with-y", action="store_true",
                     help="time mamba_mimo_bwd_fwd_y (the op plus the layer's forward output y)")
+    ap.add_argument("--op", choices=["bwd_fwd", "bwd_bwd"], default="bwd_fwd",
+                    help="bwd_bwd: time the second backward stage instead (its own JSON line)")
     return ap.parse_args()
 
 
@@ -262,11 +268,156 @@ def _prefix(inp, tokens, C):
     return out
 
 
+BB_METRIC = "MIMO bwd_bwd tokens/s at B1 S8192 H16 N=P=64 R4 C16"
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)
+
+
+def bb_grad_flop(wl):
+    """Algorithmic FP32 FLOP of the second stage's gradient kernel per call:
+    per chunk and (b,h), the five strictly causal products (Q Ks^T, A^T dPhiO,
+    dPhiO PsiV^T, dS Ks, dS^T Q: R^2 C(C-1)/2 x (3N + 2P) multiply-adds) and
+    the four state products (dPhiO Hc^T, k_state D, PsiV D^T, Q Hc: 4 CR N P)."""
+    nc = -(-wl.S // wl.C)
+    CR = wl.C * wl.R
+    macs = wl.R ** 2 * wl.C * (wl.C - 1) // 2 * (3 * wl.N + 2 * wl.P) + 4 * CR * wl.N * wl.P
+    return 2 * macs * nc * wl.B * wl.H
+
+
+def _bb_inputs(wl, seed, device):
+    inp = si.make_inputs(B=wl.B, S=wl.S, H=wl.H, G=wl.G, R=wl.R, N=wl.N, P=wl.P, C=wl.C, div=wl.div,
+                         reduced=True, has_z=False, has_d=True, seed=seed, device=device)
+    states, qk = si.make_stage1_caches(B=wl.B, S=wl.S, H=wl.H, R=wl.R, N=wl.N, P=wl.P, C=wl.C, seed=seed + 1,
+                                       device=device)
+    args = [inp["dout"], inp["q"], inp["k"], inp["v"], inp["q_bias"], inp["k_bias"], inp["mimo_v"], states, qk,
+            inp["da_cs"], inp["da_cs_rev"], inp["dt"], inp["trap"], inp["segsum"], inp["angles"],
+            inp["mimo_o"], inp["d"]]
+    return args
+
+
+def run_bwd_bwd(args, world, rank, local):
+    """Second backward stage: C-ABI calls on resident input/output sets."""
+    import mamba_mimo_chunked_gb300 as mm
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mm.build()
+    lib = mm.load_library()
+    wl = si.WORKLOADS[WORKLOAD_INDEX]
+    stream = torch.cuda.current_stream(dev)
+    steps = args.steps if args.steps != 20000 else 300   # the default count is the first stage's
+    nsets = 2                                            # each set ~0.45 GB, over the L2
+    sets = []
+    for s in range(nsets):
+        a = _bb_inputs(wl, si.WORKLOAD_SEED_BASE + 31 * s + 104729 * rank, dev)
+        outs = mm.mamba_mimo_bwd_bwd(*a[:15], mimo_o=a[15], d=a[16], chunk_size=wl.C, rotary_dim_divisor=wl.div)
+        sets.append((a, outs))
+    torch.cuda.synchronize(dev)
+    in_bytes = sum(nbytes(t) for t in sets[0][0])
+    out_bytes = sum(nbytes(t) for t in sets[0][1].values())
+    ws_bytes = mm.bwd_bwd_workspace_size(wl.B, wl.S, wl.H, wl.G, wl.R, wl.N, wl.P, wl.C, wl.div)
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    dims = mm._Dims(wl.B, wl.S, wl.H, wl.G, wl.R, wl.N, wl.P)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    call_args = [[ctypes.byref(dims)] + [mm._ptr(t) for t in a] + [wl.C, wl.div]
+                 + [mm._ptr(o[n]) for n in mm.BWD_BWD_OUTPUTS] + [mm._ptr(workspace), ws_bytes, sh]
+                 for a, o in sets]
+    for i in range(args.warmup):
+        st = lib.mamba_mimo_bwd_bwd(*call_args[i % nsets])
+        if st:
+            mm._raise(lib, st)
+    launches = lib.mamba_mimo_last_launch_count()
+    every = max(1, steps // 100)
+    n_samples = (steps + every - 1) // every
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n_samples)]
+    for row in ev:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    ev_arrays = [(ctypes.c_void_p * 8)(*[ctypes.c_void_p(e.cuda_event) for e in row]) for row in ev]
+    sampler = ClockSampler(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    start.record(stream)
+    bad = 0
+    for i in range(steps):
+        if i % every == 0:
+            lib.mamba_mimo_set_stage_events(ev_arrays[i // every], 8)
+            bad |= lib.mamba_mimo_bwd_bwd(*call_args[i % nsets])
+            lib.mamba_mimo_set_stage_events(None, 0)
+        else:
+            bad |= lib.mamba_mimo_bwd_bwd(*call_args[i % nsets])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world)
+    if bad:
+        raise RuntimeError("a timed call failed")
+    elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, dev)
+    stage_ms = {}
+    for k in range(launches):
+        name = lib.mamba_mimo_stage_name(k)
+        if name:
+            stage_ms[name.decode()] = statistics.mean(row[2 * k].elapsed_time(row[2 * k + 1]) for row in ev)
+    grad_ms = stage_ms["bb_grad"]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    alu_peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    flop = bb_grad_flop(wl)
+    achieved = flop / (grad_ms * 1e-3) / 1e12
+    hbm, hbm_kind = measured_peaks()
+    ms_per_step = elapsed_s * 1e3 / steps
+    value = wl.B * wl.S * steps * world / elapsed_s
+    line = {
+        "metric": BB_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name + "_bwd_bwd", "B": wl.B, "S": wl.S, "H": wl.H, "G": wl.G, "R": wl.R,
+                   "N": wl.N, "P": wl.P, "chunk_size": wl.C, "rotary_dim_divisor": wl.div, "reduced_dout": True,
+                   "d": True, "caches": "seeded stand-ins for states / qk_dot",
+                   "parallelism": f"replicas{world}",
+                   "l2": f"{nsets} rotating input+output sets, {nsets * (in_bytes + out_bytes) / 1e6:.0f} MB > 129 MB L2"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                     "frac": achieved / alu_peak, "traffic": None, "kernel": "bb_grad",
+                     "algorithmic_flop_per_launch": flop,
+                     "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {mhz:.0f} MHz"},
+        "op_hbm_frac": (in_bytes + out_bytes) / (ms_per_step * 1e-3) / 1e9 / hbm,
+        "algorithmic_bytes_per_call": in_bytes + out_bytes,
+        "stage_ms": stage_ms, "gpu_launches": launches * steps, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = bb_cpu_baseline(sets[0][0], wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bb_cpu_baseline(a, wl, heads=2):
+    """The second-stage oracle as it stands (numpy, float64), timed on a
+    sample of `heads` heads of the workload and scaled to tokens/s of the
+    whole problem."""
+    from oracle import bwd_bwd as bb
+    cpu = [None if t is None else t.cpu() for t in a]
+    hs = slice(0, heads)
+    dout, q, k, v, qb, kb, mv, st, qk, dcs, dcr, dt, tr, seg, ang, mo, d = cpu
+    t0 = time.perf_counter()
+    bb.bwd_bwd(dout[:, :, hs], q, k, v[:, :, hs], qb[hs], kb[hs], mv[hs], st[:, hs], qk[:, hs], dcs[:, hs],
+               dcr[:, hs], dt[:, hs], tr[:, hs], seg[:, hs], ang[:, :, hs], mimo_o=mo[hs], d=d[hs],
+               chunk_size=wl.C, rotary_dim_divisor=wl.div)
+    dt_s = time.perf_counter() - t0
+    return {"value": wl.B * wl.S / (dt_s * wl.H / heads), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{heads} of {wl.H} heads of {wl.name} (numpy float64, one thread), {dt_s:.2f} s"}
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.op == "bwd_bwd":
+        run_bwd_bwd(args, world, rank, local)
         return
     import mamba_mimo_chunked_gb300 as mm
 

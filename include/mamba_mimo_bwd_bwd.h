@@ -89,7 +89,9 @@ mmbf_status mamba_mimo_bwd_bwd_workspace_size(const mmbf_dims* dims, int64_t chu
  * MMBF_ERR_CUDA reports a launch error.  Asynchronous; calls sharing a
  * workspace must be ordered on one stream.  Four kernels: the per-chunk
  * dstates seeds, the reverse scan, the per-chunk gradients, the per-(b,h)
- * sums of DMIMO_V and DD (mamba_mimo_last_launch_count reports them). */
+ * sums of DMIMO_V and DD (mamba_mimo_last_launch_count reports them;
+ * mamba_mimo_stage_name names them "bb_seed", "bb_scan", "bb_grad",
+ * "bb_reduce", and mamba_mimo_set_stage_events times them). */
 mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const void* q, const void* k,
                                const void* v, const float* q_bias, const float* k_bias,
                                const float* mimo_v, const void* states, const void* qk_dot,

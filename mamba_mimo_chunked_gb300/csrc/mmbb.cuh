@@ -501,6 +501,8 @@ __global__ void __launch_bounds__(kT) reduce_kernel(const BBParams p) {
   }
 }
 
+static const char* const kBBStageNames[4] = {"bb_seed", "bb_scan", "bb_grad", "bb_reduce"};
+
 constexpr size_t kSeedSmem = (2 * kTile + 5 * kMax) * sizeof(float);
 constexpr size_t kGradSmem = (11 * kTile + kSmall + 5 * kMax + kMax * kRedCols) * sizeof(float);
 
@@ -612,13 +614,23 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = p.B * p.H;
   int launches = 0;
+  g_stage_names = kBBStageNames;
+  g_stage_names_n = 4;
+  stage_event(0, 0, st);
   seed_kernel<<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
+  stage_event(0, 1, st);
   launches++;
+  stage_event(1, 0, st);
   scan_kernel<<<dim3((p.N * p.P + 127) / 128, BH), 128, 0, st>>>(p);
+  stage_event(1, 1, st);
   launches++;
+  stage_event(2, 0, st);
   grad_kernel<<<dim3(p.nc, BH), kT, kGradSmem, st>>>(p);
+  stage_event(2, 1, st);
   launches++;
+  stage_event(3, 0, st);
   reduce_kernel<<<BH, kT, 0, st>>>(p);
+  stage_event(3, 1, st);
   launches++;
   e = cudaGetLastError();
   g_launches = launches;
