@@ -37,7 +37,9 @@ struct BBParams {
   float* ws_dd;     // [BH][nc]: DD partials
 };
 
-constexpr int kT = 256;             // threads per CTA
+constexpr int kT = 256;             // threads per CTA (seed kernel: 4 x 4 blocks of a 64 x 64 product)
+constexpr int kTG = 512;            // threads per CTA of the gradient kernel (2 x 4 blocks)
+constexpr int kTM = 2;              // rows per thread block of the gradient kernel's products
 constexpr int kMax = 64;            // N, P and C*R limit of this path
 constexpr int kLD = kMax + 1;       // FP32 tile row stride
 constexpr int kTile = kMax * kLD;   // floats per tile
@@ -49,33 +51,34 @@ __device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x))
 // acc[u][v] += sum_k a(i0+u, k) * b(k, j0+v): a 4 x 4 block of a product of
 // shared-memory tiles (rows and columns past the operands' extents are
 // computed on whatever the tile holds there and never used).
-template <class FA, class FB>
-__device__ __forceinline__ void mm4(float (&acc)[4][4], int i0, int j0, int K, FA a, FB b) {
+template <int TM, int TN, class FA, class FB>
+__device__ __forceinline__ void mm4(float (&acc)[TM][TN], int i0, int j0, int K, FA a, FB b) {
+#pragma unroll 4
   for (int kk = 0; kk < K; kk++) {
-    float av[4], bv[4];
+    float av[TM], bv[TN];
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      av[u] = a(i0 + u, kk);
-      bv[u] = b(kk, j0 + u);
-    }
+    for (int u = 0; u < TM; u++) av[u] = a(i0 + u, kk);
 #pragma unroll
-    for (int u = 0; u < 4; u++)
+    for (int v = 0; v < TN; v++) bv[v] = b(kk, j0 + v);
 #pragma unroll
-      for (int v = 0; v < 4; v++) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+    for (int u = 0; u < TM; u++)
+#pragma unroll
+      for (int v = 0; v < TN; v++) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
   }
 }
-__device__ __forceinline__ void zero4(float (&acc)[4][4]) {
+template <int TM, int TN>
+__device__ __forceinline__ void zero4(float (&acc)[TM][TN]) {
 #pragma unroll
-  for (int u = 0; u < 4; u++)
+  for (int u = 0; u < TM; u++)
 #pragma unroll
-    for (int v = 0; v < 4; v++) acc[u][v] = 0.f;
+    for (int v = 0; v < TN; v++) acc[u][v] = 0.f;
 }
 
 // Token scalars of chunk c (reading of the op header): gamma, factor,
 // exp(da_cs), exp(da_cs_rev), and whether the token is inside S.
 __device__ void load_tokens(const BBParams& p, int bh, int c, float* gam, float* fac, float* ea, float* er,
                             float* valid) {
-  for (int t = threadIdx.x; t < p.C; t += kT) {
+  for (int t = threadIdx.x; t < p.C; t += blockDim.x) {
     const int tg = c * p.C + t;
     const int64_t i = (int64_t)bh * p.S + tg;
     const bool in = tg < p.S, in1 = tg + 1 < p.S;
@@ -96,7 +99,7 @@ __device__ void load_tokens(const BBParams& p, int bh, int c, float* gam, float*
 __device__ void load_rotated(const BBParams& p, int b, int h, int c, const uint16_t* src, const float* bias,
                              float* T) {
   const int g = h / (p.H / p.G);
-  for (int e = threadIdx.x; e < p.CR * p.N; e += kT) {
+  for (int e = threadIdx.x; e < p.CR * p.N; e += blockDim.x) {
     const int j = e / p.N, n = e % p.N, t = j / p.R, r = j % p.R, tg = c * p.C + t;
     float x = bias[((int64_t)h * p.R + r) * p.N + n];
     if (tg < p.S) x += bf_f(src[((((int64_t)b * p.S + tg) * p.R + r) * p.G + g) * p.N + n]);
@@ -104,7 +107,7 @@ __device__ void load_rotated(const BBParams& p, int b, int h, int c, const uint1
   }
   __syncthreads();
   const int half = p.N / 2;
-  for (int e = threadIdx.x; e < p.CR * p.w; e += kT) {
+  for (int e = threadIdx.x; e < p.CR * p.w; e += blockDim.x) {
     const int j = e / p.w, m = e % p.w, t = j / p.R, tg = c * p.C + t;
     const float th = tg < p.S ? p.angles[(((int64_t)b * p.S + tg) * p.H + h) * p.w + m] : 0.f;
     float sn, cs;
@@ -117,7 +120,7 @@ __device__ void load_rotated(const BBParams& p, int b, int h, int c, const uint1
 
 // dPhiO rows [C*R][P] (zero past S) [op document: reduce-O or per rank].
 __device__ void load_dphio(const BBParams& p, int b, int h, int c, float* T) {
-  for (int e = threadIdx.x; e < p.CR * p.P; e += kT) {
+  for (int e = threadIdx.x; e < p.CR * p.P; e += blockDim.x) {
     const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
     float x = 0.f;
     if (tg < p.S) {
@@ -132,7 +135,7 @@ __device__ void load_dphio(const BBParams& p, int b, int h, int c, float* T) {
 
 // PsiV rows [C*R][P] = v[t,p] * mimo_v[r,p] (zero past S).
 __device__ void load_psi(const BBParams& p, int b, int h, int c, float* T) {
-  for (int e = threadIdx.x; e < p.CR * p.P; e += kT) {
+  for (int e = threadIdx.x; e < p.CR * p.P; e += blockDim.x) {
     const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
     float x = 0.f;
     if (tg < p.S)
@@ -153,11 +156,11 @@ __global__ void __launch_bounds__(kT, 2) seed_kernel(const BBParams p) {
   load_rotated(p, b, h, c, p.q, p.q_bias, Qr);
   __syncthreads();
   const float* ea = tk + 2 * kMax;
-  const int i0 = (threadIdx.x >> 4) * 4, j0 = (threadIdx.x & 15) * 4;
+  const int i0 = (threadIdx.x >> 4) * 4, j0 = (threadIdx.x & 15) * 4, R = p.R;
   float acc[4][4];
   zero4(acc);
-  mm4(acc, i0, j0, p.CR, [&](int n, int i) { return Qr[i * kLD + n] * ea[i / p.R]; },
-      [&](int i, int pp) { return Gp[i * kLD + pp]; });
+  mm4(acc, i0, j0, p.CR, [=](int n, int i) { return Qr[i * kLD + n] * ea[i / R]; },
+      [=](int i, int pp) { return Gp[i * kLD + pp]; });
   float* dst = p.ws_D + ((int64_t)bh * p.nc + c) * p.N * p.P;
 #pragma unroll
   for (int u = 0; u < 4; u++)
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(128) scan_kernel(const BBParams p) {
 }
 
 // ---- 3. every gradient of one chunk
-__global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
+__global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   extern __shared__ float smf[];
   float* Qr = smf;              // rotated q rows
   float* Kr = Qr + kTile;       // rotated k rows
@@ -215,7 +218,10 @@ __global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
   float* dP = dK + kTile;       // gradient of PsiV
   float* sm = dP + kTile;       // segsum [C][C] | qk [C][R][R] | dqk [C][R][R]
   float* tk = sm + kSmall;      // gam | fac | ea | er | valid, kMax each
-  float* red = tk + 5 * kMax;   // [kMax][kRedCols] row partials
+  float* red = tk + 5 * kMax;   // three [kMax][kRedCols] row-partial buffers
+  float* red2 = red + kMax * kRedCols;
+  float* red3 = red2 + kMax * kRedCols;
+  float* wsum = red3 + kMax * kRedCols;  // [2][kTG / 32] per-warp sums
   float* gam = tk;
   float* fac = tk + kMax;
   float* ea = tk + 2 * kMax;
@@ -226,16 +232,16 @@ __global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
   float* qk = sm + C * C;
   float* dqk = qk + C * R * R;
   const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  const int tid = threadIdx.x, i0 = (tid >> 4) * 4, j0 = (tid & 15) * 4;
+  const int tid = threadIdx.x, i0 = (tid >> 4) * kTM, j0 = (tid & 15) * 4;
 
   // ---- inputs of the chunk
   load_tokens(p, bh, c, gam, fac, ea, er, valid);
-  for (int e = tid; e < C * C; e += kT) seg[e] = p.segsum[((int64_t)bh * p.nc + c) * C * C + e];
-  for (int e = tid; e < C * R * R; e += kT) {
+  for (int e = tid; e < C * C; e += kTG) seg[e] = p.segsum[((int64_t)bh * p.nc + c) * C * C + e];
+  for (int e = tid; e < C * R * R; e += kTG) {
     const int tg = c * C + e / (R * R);
     qk[e] = tg < p.S ? bf_f(p.qk[((int64_t)bh * p.S + tg) * R * R + e % (R * R)]) : 0.f;
   }
-  for (int e = tid; e < N * P; e += kT) {
+  for (int e = tid; e < N * P; e += kTG) {
     Hc[(e / P) * kLD + e % P] = bf_f(p.states[((int64_t)bh * p.nc + c) * N * P + e]);
     Dn[(e / P) * kLD + e % P] = p.ws_D[((int64_t)bh * p.nc + c) * N * P + e];
   }
@@ -247,13 +253,13 @@ __global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
 
   // ---- A = mask(q_rot k_scaled^T) exp(segsum): selected, never multiplied by
   //      a mask (padded rows and the upper triangle never reach a product)
-  auto tok_ok = [&](int i, int j) { return (i / R) > (j / R) && valid[i / R] != 0.f; };
+  auto tok_ok = [=](int i, int j) { return (i / R) > (j / R) && valid[i / R] != 0.f; };
   {
-    float acc[4][4];
+    float acc[kTM][4];
     zero4(acc);
-    mm4(acc, i0, j0, N, [&](int i, int n) { return Qr[i * kLD + n]; }, [&](int n, int j) { return Kr[j * kLD + n]; });
+    mm4(acc, i0, j0, N, [=](int i, int n) { return Qr[i * kLD + n]; }, [=](int n, int j) { return Kr[j * kLD + n]; });
 #pragma unroll
-    for (int u = 0; u < 4; u++)
+    for (int u = 0; u < kTM; u++)
 #pragma unroll
       for (int v = 0; v < 4; v++) {
         const int i = i0 + u, j = j0 + v;
@@ -266,15 +272,15 @@ __global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
   // ---- dPsiV = A^T dPhiO + k_state D_{c+1} + d dPhiO + gamma qk^T dPhiO (diagonal);
   //      dA = dPhiO PsiV^T
   {
-    float acc[4][4];
+    float acc[kTM][4];
     zero4(acc);
-    mm4(acc, i0, j0, CR, [&](int j, int i) { return M1[i * kLD + j]; }, [&](int i, int pp) { return Gp[i * kLD + pp]; });
-    float acc2[4][4];
+    mm4(acc, i0, j0, CR, [=](int j, int i) { return M1[i * kLD + j]; }, [=](int i, int pp) { return Gp[i * kLD + pp]; });
+    float acc2[kTM][4];
     zero4(acc2);
-    mm4(acc2, i0, j0, N, [&](int j, int n) { return Kr[j * kLD + n]; }, [&](int n, int pp) { return Dn[n * kLD + pp]; });
+    mm4(acc2, i0, j0, N, [=](int j, int n) { return Kr[j * kLD + n]; }, [=](int n, int pp) { return Dn[n * kLD + pp]; });
     const float dv = p.has_d ? p.d[h] : 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; u++)
+    for (int u = 0; u < kTM; u++)
 #pragma unroll
       for (int v = 0; v < 4; v++) {
         const int j = i0 + u, pp = j0 + v;
@@ -287,9 +293,9 @@ __global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
         }
       }
     zero4(acc);
-    mm4(acc, i0, j0, P, [&](int i, int pp) { return Gp[i * kLD + pp]; }, [&](int pp, int j) { return Ps[j * kLD + pp]; });
+    mm4(acc, i0, j0, P, [=](int i, int pp) { return Gp[i * kLD + pp]; }, [=](int pp, int j) { return Ps[j * kLD + pp]; });
 #pragma unroll
-    for (int u = 0; u < 4; u++)
+    for (int u = 0; u < kTM; u++)
 #pragma unroll
       for (int v = 0; v < 4; v++)
         if (i0 + u < CR && j0 + v < CR) M2[(i0 + u) * kLD + j0 + v] = acc[u][v];
@@ -297,7 +303,7 @@ __global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
   __syncthreads();
 
   // ---- DSSDA[ti][tj] = sum over the token pair's rank pairs of dA * A
-  for (int e = tid; e < C * C; e += kT) {
+  for (int e = tid; e < C * C; e += kTG) {
     const int ti = e / C, tj = e % C;
     float s = 0.f;
     if (ti > tj && valid[ti] != 0.f)
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
   }
   __syncthreads();
   // dS = dA exp(segsum) on the causal entries (in place)
-  for (int e = tid; e < CR * CR; e += kT) {
+  for (int e = tid; e < CR * CR; e += kTG) {
     const int i = e / CR, j = e % CR;
     M2[i * kLD + j] = tok_ok(i, j) ? M2[i * kLD + j] * expf(seg[(i / R) * C + j / R]) : 0.f;
   }
@@ -317,172 +323,191 @@ __global__ void __launch_bounds__(kT, 1) grad_kernel(const BBParams p) {
   //      dk_scaled = dS^T q_rot + exp(da_cs_rev) dk_state, dk_state = PsiV Dn^T;
   //      row sums for DDA_CS_REV (dk_state * k_state) and DDA_CS (inter * dPhiO)
   {
-    float acc[4][4];
+    float acc[kTM][4];
     zero4(acc);
-    mm4(acc, i0, j0, CR, [&](int i, int j) { return M2[i * kLD + j] * fac[j / R]; },
-        [&](int j, int n) { return Kr[j * kLD + n]; });
-    float acc2[4][4];
+    mm4(acc, i0, j0, CR, [=](int i, int j) { return M2[i * kLD + j] * fac[j / R]; },
+        [=](int j, int n) { return Kr[j * kLD + n]; });
+    float acc2[kTM][4];
     zero4(acc2);
-    mm4(acc2, i0, j0, P, [&](int i, int pp) { return Gp[i * kLD + pp]; }, [&](int pp, int n) { return Hc[n * kLD + pp]; });
+    mm4(acc2, i0, j0, P, [=](int i, int pp) { return Gp[i * kLD + pp]; }, [=](int pp, int n) { return Hc[n * kLD + pp]; });
 #pragma unroll
-    for (int u = 0; u < 4; u++)
+    for (int u = 0; u < kTM; u++)
 #pragma unroll
       for (int v = 0; v < 4; v++)
         if (i0 + u < CR && j0 + v < N) dQ[(i0 + u) * kLD + j0 + v] = fmaf(ea[(i0 + u) / R], acc2[u][v], acc[u][v]);
-    // dk_state and its row sums with k_state = k_rot * factor * exp(da_cs_rev)
+    // dk_state = PsiV D^T, dk_scaled = dS^T q_rot + exp(da_cs_rev) dk_state, with
+    // row sums for DDA_CS_REV (dk_state * k_state) and DFACTOR (dk_scaled * k_rot)
     zero4(acc);
-    mm4(acc, i0, j0, P, [&](int j, int pp) { return Ps[j * kLD + pp]; }, [&](int pp, int n) { return Dn[n * kLD + pp]; });
+    mm4(acc, i0, j0, P, [=](int j, int pp) { return Ps[j * kLD + pp]; }, [=](int pp, int n) { return Dn[n * kLD + pp]; });
     zero4(acc2);
-    mm4(acc2, i0, j0, CR, [&](int j, int i) { return M2[i * kLD + j]; }, [&](int i, int n) { return Qr[i * kLD + n]; });
+    mm4(acc2, i0, j0, CR, [=](int j, int i) { return M2[i * kLD + j]; }, [=](int i, int n) { return Qr[i * kLD + n]; });
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
+    for (int u = 0; u < kTM; u++) {
       const int j = i0 + u;
-      float rs = 0.f;
+      float r1 = 0.f, r2 = 0.f;
 #pragma unroll
       for (int v = 0; v < 4; v++) {
         const int n = j0 + v;
         if (j < CR && n < N) {
           const int t = j / R;
-          rs = fmaf(acc[u][v], Kr[j * kLD + n] * fac[t] * er[t], rs);
-          dK[j * kLD + n] = fmaf(er[t], acc[u][v], acc2[u][v]);
+          const float kr = Kr[j * kLD + n];
+          r1 = fmaf(acc[u][v], kr * fac[t] * er[t], r1);
+          const float dks = fmaf(er[t], acc[u][v], acc2[u][v]);
+          r2 = fmaf(dks, kr, r2);
+          dK[j * kLD + n] = dks;
         }
       }
-      if (j < kMax) red[j * kRedCols + (tid & 15)] = rs;
+      red[j * kRedCols + (tid & 15)] = r1;
+      red2[j * kRedCols + (tid & 15)] = r2;
     }
   }
-  __syncthreads();
-  for (int t = tid; t < C; t += kT) {  // DDA_CS_REV
-    float s = 0.f;
-    for (int r = 0; r < R; r++)
-      for (int q = 0; q < kRedCols; q++) s += red[(t * R + r) * kRedCols + q];
-    const int tg = c * C + t;
-    if (tg < p.S) p.DDA_CS_REV[(int64_t)bh * p.S + tg] = s;
-  }
-  __syncthreads();
-  {  // inter = exp(da_cs) q_rot Hc and its row sums with dPhiO (DDA_CS)
-    float acc[4][4];
+  {  // inter = exp(da_cs) q_rot Hc: row sums with dPhiO (DDA_CS)
+    float acc[kTM][4];
     zero4(acc);
-    mm4(acc, i0, j0, N, [&](int i, int n) { return Qr[i * kLD + n]; }, [&](int n, int pp) { return Hc[n * kLD + pp]; });
+    mm4(acc, i0, j0, N, [=](int i, int n) { return Qr[i * kLD + n]; }, [=](int n, int pp) { return Hc[n * kLD + pp]; });
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
+    for (int u = 0; u < kTM; u++) {
       const int i = i0 + u;
       float rs = 0.f;
 #pragma unroll
       for (int v = 0; v < 4; v++)
         if (i < CR && j0 + v < P) rs = fmaf(acc[u][v] * ea[i / R], Gp[i * kLD + j0 + v], rs);
-      if (i < kMax) red[i * kRedCols + (tid & 15)] = rs;
+      red3[i * kRedCols + (tid & 15)] = rs;
     }
   }
-  // same-token terms: dot[t,o,r] = dPhiO[(t,o)] . PsiV[(t,r)] -> dqk = gamma dot,
+  // same-token terms: dot[t,o,r] = dPhiO[(t,o)] . PsiV[(t,r)]; dqk = gamma dot,
   // DGAMMA = sum qk * dot
-  for (int e = tid; e < C * R * R; e += kT) {
+  for (int e = tid; e < C * R * R; e += kTG) {
     const int t = e / (R * R), o = (e / R) % R, r = e % R;
     float s = 0.f;
     for (int pp = 0; pp < P; pp++) s = fmaf(Gp[(t * R + o) * kLD + pp], Ps[(t * R + r) * kLD + pp], s);
     dqk[e] = s;  // gamma applied below
   }
-  __syncthreads();
-  for (int t = tid; t < C; t += kT) {
-    float s = 0.f, g = 0.f;
-    for (int r = 0; r < R; r++)
-      for (int q = 0; q < kRedCols; q++) s += red[(t * R + r) * kRedCols + q];
-    for (int e = 0; e < R * R; e++) g = fmaf(qk[t * R * R + e], dqk[t * R * R + e], g);
-    const int tg = c * C + t;
-    if (tg < p.S) {
-      p.DDA_CS[(int64_t)bh * p.S + tg] = s;
-      p.DGAMMA[(int64_t)bh * p.S + tg] = g;
-    }
-  }
-  __syncthreads();
-  for (int e = tid; e < C * R * R; e += kT) dqk[e] *= gam[e / (R * R)];
-  // DFACTOR = sum dk_scaled * k_rot per token
-  for (int t = tid; t < C; t += kT) {
-    float s = 0.f;
-    for (int r = 0; r < R; r++)
-      for (int n = 0; n < N; n++) s = fmaf(dK[(t * R + r) * kLD + n], Kr[(t * R + r) * kLD + n], s);
-    const int tg = c * C + t;
-    if (tg < p.S) p.DFACTOR[(int64_t)bh * p.S + tg] = s;
-  }
-  // DDA at the chunk's last valid token: alpha_c * <Hc, D_{c+1}>; DD partial
-  if (tid < 32) {
+  // DDA (alpha_c <Hc, D_{c+1}> at the chunk's last valid token) and the DD
+  // partial (sum dPhiO * PsiV): block sums in a fixed order
+  {
     float s = 0.f, dd = 0.f;
-    for (int e = tid; e < N * P; e += 32) s = fmaf(Hc[(e / P) * kLD + e % P], Dn[(e / P) * kLD + e % P], s);
-    for (int e = tid; e < CR * P; e += 32) dd = fmaf(Gp[(e / P) * kLD + e % P], Ps[(e / P) * kLD + e % P], dd);
+    for (int e = tid; e < N * P; e += kTG) s = fmaf(Hc[(e / P) * kLD + e % P], Dn[(e / P) * kLD + e % P], s);
+    for (int e = tid; e < CR * P; e += kTG) dd = fmaf(Gp[(e / P) * kLD + e % P], Ps[(e / P) * kLD + e % P], dd);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       s += __shfl_xor_sync(0xffffffffu, s, o);
       dd += __shfl_xor_sync(0xffffffffu, dd, o);
     }
-    if (tid == 0) {
-      const int last = min(c * C + C, p.S) - 1;
-      for (int t = 0; t < C; t++) {
-        const int tg = c * C + t;
-        if (tg < p.S)
-          p.DDA[(int64_t)bh * p.S + tg] = (tg == last) ? p.ws_alpha[(int64_t)bh * p.nc + c] * s : 0.f;
-      }
-      p.ws_dd[(int64_t)bh * p.nc + c] = dd;
+    if ((tid & 31) == 0) {
+      wsum[tid >> 5] = s;
+      wsum[kTG / 32 + (tid >> 5)] = dd;
     }
   }
   __syncthreads();
-
-  // ---- rotary post-pass: DQ / DK (transposed rotation + the diagonal's
-  //      same-token q.k terms on the un-rotated biased rows), DANGLES
-  const int half = N / 2, g = h / (p.H / p.G);
-  for (int e = tid; e < CR * N; e += kT) {
-    const int j = e / N, n = e % N, t = j / R, r = j % R, tg = c * C + t;
-    if (tg >= p.S) continue;
-    int m = -1;
-    bool lo = false;
-    if (n < p.w) { m = n; lo = true; }
-    else if (n >= half && n < half + p.w) { m = n - half; }
-    float dq = dQ[j * kLD + n], dk = dK[j * kLD + n] * fac[t];
-    if (m >= 0) {
-      float sn, cs;
-      sincosf(p.angles[(((int64_t)b * p.S + tg) * p.H + h) * p.w + m], &sn, &cs);
-      const float qlo = dQ[j * kLD + m], qhi = dQ[j * kLD + half + m];
-      const float klo = dK[j * kLD + m] * fac[t], khi = dK[j * kLD + half + m] * fac[t];
-      dq = lo ? cs * qlo + sn * qhi : -sn * qlo + cs * qhi;
-      dk = lo ? cs * klo + sn * khi : -sn * klo + cs * khi;
+  for (int t = tid; t < C; t += kTG) {  // per-token sums
+    float s1 = 0.f, s2 = 0.f, s3 = 0.f, g = 0.f;
+    for (int r = 0; r < R; r++)
+      for (int q = 0; q < kRedCols; q++) {
+        s1 += red[(t * R + r) * kRedCols + q];
+        s2 += red2[(t * R + r) * kRedCols + q];
+        s3 += red3[(t * R + r) * kRedCols + q];
+      }
+    for (int e = 0; e < R * R; e++) g = fmaf(qk[t * R * R + e], dqk[t * R * R + e], g);
+    const int tg = c * C + t;
+    if (tg < p.S) {
+      const int64_t o = (int64_t)bh * p.S + tg;
+      p.DDA_CS_REV[o] = s1;
+      p.DFACTOR[o] = s2;
+      p.DDA_CS[o] = s3;
+      p.DGAMMA[o] = g;
+      float hd = 0.f;
+      for (int w8 = 0; w8 < kTG / 32; w8++) hd += wsum[w8];
+      p.DDA[o] = (tg == min(c * C + C, p.S) - 1) ? p.ws_alpha[(int64_t)bh * p.nc + c] * hd : 0.f;
     }
-    // diagonal: qk[t,o,r] = qh[(t,o)] . kh[(t,r)]
-    for (int x = 0; x < R; x++) {
-      const int64_t src = ((((int64_t)b * p.S + tg) * R + x) * p.G + g) * N + n;
-      const float kh = bf_f(p.k[src]) + p.k_bias[((int64_t)h * R + x) * N + n];
-      const float qh = bf_f(p.q[src]) + p.q_bias[((int64_t)h * R + x) * N + n];
-      dq = fmaf(dqk[(t * R + r) * R + x], kh, dq);   // row j = (t, o = r) of q
-      dk = fmaf(dqk[(t * R + x) * R + r], qh, dk);   // row j = (t, r) of k
-    }
-    const int64_t o = (((int64_t)b * p.S + tg) * R + r) * p.H + h;
-    p.DQ[o * N + n] = dq;
-    p.DK[o * N + n] = dk;
   }
-  for (int e = tid; e < C * p.w; e += kT) {
-    const int t = e / p.w, m = e % p.w, tg = c * C + t;
+  if (tid == 0) {
+    float dd = 0.f;
+    for (int w8 = 0; w8 < kTG / 32; w8++) dd += wsum[kTG / 32 + w8];
+    p.ws_dd[(int64_t)bh * p.nc + c] = dd;
+  }
+  __syncthreads();
+  for (int e = tid; e < C * R * R; e += kTG) dqk[e] *= gam[e / (R * R)];
+
+  // ---- rotary post-pass.  Stage the rotary cos / sin of the chunk and
+  //      mimo_v in M1, v in M2 (both free now); DANGLES from the rotated rows.
+  const int half = N / 2, W = p.w;
+  float* cst = M1;                // cos [C][W]
+  float* snt = M1 + C * W;        // sin [C][W]
+  float* mvs = M1 + 2 * C * W;    // mimo_v [R][P]
+  float* vs = M2;                 // v [C][P]
+  for (int e = tid; e < C * W; e += kTG) {
+    const int t = e / W, m = e % W, tg = c * C + t;
+    float sn = 0.f, cs = 1.f;
+    if (tg < p.S) sincosf(p.angles[(((int64_t)b * p.S + tg) * p.H + h) * W + m], &sn, &cs);
+    cst[e] = cs;
+    snt[e] = sn;
+  }
+  for (int e = tid; e < R * P; e += kTG) mvs[e] = p.mimo_v[(int64_t)h * R * P + e];
+  for (int e = tid; e < C * P; e += kTG) {
+    const int t = e / P, pp = e % P, tg = c * C + t;
+    vs[e] = tg < p.S ? bf_f(p.v[(((int64_t)b * p.S + tg) * p.H + h) * P + pp]) : 0.f;
+  }
+  for (int e = tid; e < C * W; e += kTG) {
+    const int t = e / W, m = e % W, tg = c * C + t;
     if (tg >= p.S) continue;
     float s = 0.f;
     for (int r = 0; r < R; r++) {
       const int j = t * R + r;
       s += dQ[j * kLD + m] * (-Qr[j * kLD + half + m]) + dQ[j * kLD + half + m] * Qr[j * kLD + m];
-      s += dK[j * kLD + m] * fac[t] * (-Kr[j * kLD + half + m]) + dK[j * kLD + half + m] * fac[t] * Kr[j * kLD + m];
+      s += fac[t] * (dK[j * kLD + m] * (-Kr[j * kLD + half + m]) + dK[j * kLD + half + m] * Kr[j * kLD + m]);
     }
-    p.DANGLES[(((int64_t)b * p.S + tg) * p.H + h) * p.w + m] = s;
+    p.DANGLES[(((int64_t)b * p.S + tg) * p.H + h) * W + m] = s;
+  }
+  __syncthreads();
+  // q_rot, k_rot -> the un-rotated biased rows (transposed rotation, in place)
+  for (int e = tid; e < CR * W; e += kTG) {
+    const int j = e / W, m = e % W, t = j / R;
+    const float cs = cst[t * W + m], sn = snt[t * W + m];
+    float lo = Qr[j * kLD + m], hi = Qr[j * kLD + half + m];
+    Qr[j * kLD + m] = cs * lo + sn * hi;
+    Qr[j * kLD + half + m] = -sn * lo + cs * hi;
+    lo = Kr[j * kLD + m];
+    hi = Kr[j * kLD + half + m];
+    Kr[j * kLD + m] = cs * lo + sn * hi;
+    Kr[j * kLD + half + m] = -sn * lo + cs * hi;
   }
   // DV and the DMIMO_V partial of the chunk
-  for (int e = tid; e < C * P; e += kT) {
+  for (int e = tid; e < C * P; e += kTG) {
     const int t = e / P, pp = e % P, tg = c * C + t;
     if (tg >= p.S) continue;
     float s = 0.f;
-    for (int r = 0; r < R; r++) s = fmaf(dP[(t * R + r) * kLD + pp], p.mimo_v[((int64_t)h * R + r) * P + pp], s);
+    for (int r = 0; r < R; r++) s = fmaf(dP[(t * R + r) * kLD + pp], mvs[r * P + pp], s);
     p.DV[(((int64_t)b * p.S + tg) * p.H + h) * P + pp] = s;
   }
-  for (int e = tid; e < R * P; e += kT) {
+  for (int e = tid; e < R * P; e += kTG) {
     const int r = e / P, pp = e % P;
     float s = 0.f;
-    for (int t = 0; t < C; t++) {
-      const int tg = c * C + t;
-      if (tg < p.S) s = fmaf(dP[(t * R + r) * kLD + pp], bf_f(p.v[(((int64_t)b * p.S + tg) * p.H + h) * P + pp]), s);
-    }
+    for (int t = 0; t < C; t++) s = fmaf(dP[(t * R + r) * kLD + pp], vs[t * P + pp], s);
     p.ws_mv[((int64_t)bh * p.nc + c) * R * P + e] = s;
+  }
+  __syncthreads();
+  // DQ / DK: the transposed rotation of the rotated-domain gradients plus the
+  // diagonal's same-token terms, qk[t,o,x] = qh[(t,o)] . kh[(t,x)]
+  for (int e = tid; e < CR * N; e += kTG) {
+    const int j = e / N, n = e % N, t = j / R, r = j % R, tg = c * C + t;
+    if (tg >= p.S) continue;
+    float dq = dQ[j * kLD + n], dk = dK[j * kLD + n] * fac[t];
+    const int m = n < W ? n : (n >= half && n < half + W ? n - half : -1);
+    if (m >= 0) {
+      const float cs = cst[t * W + m], sn = snt[t * W + m];
+      const float qlo = dQ[j * kLD + m], qhi = dQ[j * kLD + half + m];
+      const float klo = dK[j * kLD + m] * fac[t], khi = dK[j * kLD + half + m] * fac[t];
+      dq = n < W ? cs * qlo + sn * qhi : -sn * qlo + cs * qhi;
+      dk = n < W ? cs * klo + sn * khi : -sn * klo + cs * khi;
+    }
+    for (int x = 0; x < R; x++) {
+      dq = fmaf(dqk[(t * R + r) * R + x], Kr[(t * R + x) * kLD + n], dq);  // row (t, o = r) of q
+      dk = fmaf(dqk[(t * R + x) * R + r], Qr[(t * R + x) * kLD + n], dk);  // row (t, r) of k
+    }
+    const int64_t o = (((int64_t)b * p.S + tg) * R + r) * p.H + h;
+    p.DQ[o * N + n] = dq;
+    p.DK[o * N + n] = dk;
   }
 }
 
@@ -504,7 +529,7 @@ __global__ void __launch_bounds__(kT) reduce_kernel(const BBParams p) {
 static const char* const kBBStageNames[4] = {"bb_seed", "bb_scan", "bb_grad", "bb_reduce"};
 
 constexpr size_t kSeedSmem = (2 * kTile + 5 * kMax) * sizeof(float);
-constexpr size_t kGradSmem = (11 * kTile + kSmall + 5 * kMax + kMax * kRedCols) * sizeof(float);
+constexpr size_t kGradSmem = (11 * kTile + kSmall + 5 * kMax + 3 * kMax * kRedCols + 2 * (kTG / 32)) * sizeof(float);
 
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -625,7 +650,7 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
   stage_event(1, 1, st);
   launches++;
   stage_event(2, 0, st);
-  grad_kernel<<<dim3(p.nc, BH), kT, kGradSmem, st>>>(p);
+  grad_kernel<<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
   stage_event(2, 1, st);
   launches++;
   stage_event(3, 0, st);
