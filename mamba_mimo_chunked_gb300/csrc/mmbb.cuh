@@ -150,16 +150,19 @@ __global__ void __launch_bounds__(kT, 2) seed_kernel(const BBParams p) {
   float* Qr = smf;
   float* Gp = Qr + kTile;
   float* tk = Gp + kTile;  // gam, fac, ea, er, valid: 5 x kMax
+  float* ear = tk + 5 * kMax;  // exp(da_cs) per row j = t*R + r
   const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
   load_tokens(p, bh, c, tk, tk + kMax, tk + 2 * kMax, tk + 3 * kMax, tk + 4 * kMax);
   load_dphio(p, b, h, c, Gp);
   load_rotated(p, b, h, c, p.q, p.q_bias, Qr);
   __syncthreads();
   const float* ea = tk + 2 * kMax;
-  const int i0 = (threadIdx.x >> 4) * 4, j0 = (threadIdx.x & 15) * 4, R = p.R;
+  for (int j = threadIdx.x; j < p.CR; j += blockDim.x) ear[j] = ea[j / p.R];
+  __syncthreads();
+  const int i0 = (threadIdx.x >> 4) * 4, j0 = (threadIdx.x & 15) * 4;
   float acc[4][4];
   zero4(acc);
-  mm4(acc, i0, j0, p.CR, [=](int n, int i) { return Qr[i * kLD + n] * ea[i / R]; },
+  mm4(acc, i0, j0, p.CR, [=](int n, int i) { return Qr[i * kLD + n] * ear[i]; },
       [=](int i, int pp) { return Gp[i * kLD + pp]; });
   float* dst = p.ws_D + ((int64_t)bh * p.nc + c) * p.N * p.P;
 #pragma unroll
@@ -222,6 +225,9 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   float* red2 = red + kMax * kRedCols;
   float* red3 = red2 + kMax * kRedCols;
   float* wsum = red3 + kMax * kRedCols;  // [2][kTG / 32] per-warp sums
+  float* facr = wsum + 2 * (kTG / 32);   // factor, exp(da_cs), exp(da_cs_rev) per row j = t*R + r
+  float* ear = facr + kMax;
+  float* err = ear + kMax;
   float* gam = tk;
   float* fac = tk + kMax;
   float* ea = tk + 2 * kMax;
@@ -250,6 +256,12 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   load_rotated(p, b, h, c, p.q, p.q_bias, Qr);
   load_rotated(p, b, h, c, p.k, p.k_bias, Kr);
   __syncthreads();
+  for (int j = tid; j < CR; j += kTG) {
+    facr[j] = fac[j / R];
+    ear[j] = ea[j / R];
+    err[j] = er[j / R];
+  }
+  __syncthreads();
 
   // ---- A = mask(q_rot k_scaled^T) exp(segsum): selected, never multiplied by
   //      a mask (padded rows and the upper triangle never reach a product)
@@ -264,7 +276,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
       for (int v = 0; v < 4; v++) {
         const int i = i0 + u, j = j0 + v;
         if (i < CR && j < CR)
-          M1[i * kLD + j] = tok_ok(i, j) ? acc[u][v] * fac[j / R] * expf(seg[(i / R) * C + j / R]) : 0.f;
+          M1[i * kLD + j] = tok_ok(i, j) ? acc[u][v] * facr[j] * expf(seg[(i / R) * C + j / R]) : 0.f;
       }
   }
   __syncthreads();
@@ -286,7 +298,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
         const int j = i0 + u, pp = j0 + v;
         if (j < CR && pp < P) {
           const int t = j / R, r = j % R;
-          float x = acc[u][v] + acc2[u][v] * fac[t] * er[t] + dv * Gp[j * kLD + pp];
+          float x = acc[u][v] + acc2[u][v] * facr[j] * err[j] + dv * Gp[j * kLD + pp];
           float dg = 0.f;
           for (int o = 0; o < R; o++) dg = fmaf(qk[(t * R + o) * R + r], Gp[(t * R + o) * kLD + pp], dg);
           dP[j * kLD + pp] = fmaf(gam[t], dg, x);
@@ -325,7 +337,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   {
     float acc[kTM][4];
     zero4(acc);
-    mm4(acc, i0, j0, CR, [=](int i, int j) { return M2[i * kLD + j] * fac[j / R]; },
+    mm4(acc, i0, j0, CR, [=](int i, int j) { return M2[i * kLD + j] * facr[j]; },
         [=](int j, int n) { return Kr[j * kLD + n]; });
     float acc2[kTM][4];
     zero4(acc2);
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
     for (int u = 0; u < kTM; u++)
 #pragma unroll
       for (int v = 0; v < 4; v++)
-        if (i0 + u < CR && j0 + v < N) dQ[(i0 + u) * kLD + j0 + v] = fmaf(ea[(i0 + u) / R], acc2[u][v], acc[u][v]);
+        if (i0 + u < CR && j0 + v < N) dQ[(i0 + u) * kLD + j0 + v] = fmaf(ear[i0 + u], acc2[u][v], acc[u][v]);
     // dk_state = PsiV D^T, dk_scaled = dS^T q_rot + exp(da_cs_rev) dk_state, with
     // row sums for DDA_CS_REV (dk_state * k_state) and DFACTOR (dk_scaled * k_rot)
     zero4(acc);
@@ -349,10 +361,9 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
       for (int v = 0; v < 4; v++) {
         const int n = j0 + v;
         if (j < CR && n < N) {
-          const int t = j / R;
           const float kr = Kr[j * kLD + n];
-          r1 = fmaf(acc[u][v], kr * fac[t] * er[t], r1);
-          const float dks = fmaf(er[t], acc[u][v], acc2[u][v]);
+          r1 = fmaf(acc[u][v], kr * facr[j] * err[j], r1);
+          const float dks = fmaf(err[j], acc[u][v], acc2[u][v]);
           r2 = fmaf(dks, kr, r2);
           dK[j * kLD + n] = dks;
         }
@@ -371,7 +382,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
       float rs = 0.f;
 #pragma unroll
       for (int v = 0; v < 4; v++)
-        if (i < CR && j0 + v < P) rs = fmaf(acc[u][v] * ea[i / R], Gp[i * kLD + j0 + v], rs);
+        if (i < CR && j0 + v < P) rs = fmaf(acc[u][v] * ear[i], Gp[i * kLD + j0 + v], rs);
       red3[i * kRedCols + (tid & 15)] = rs;
     }
   }
@@ -528,8 +539,8 @@ __global__ void __launch_bounds__(kT) reduce_kernel(const BBParams p) {
 
 static const char* const kBBStageNames[4] = {"bb_seed", "bb_scan", "bb_grad", "bb_reduce"};
 
-constexpr size_t kSeedSmem = (2 * kTile + 5 * kMax) * sizeof(float);
-constexpr size_t kGradSmem = (11 * kTile + kSmall + 5 * kMax + 3 * kMax * kRedCols + 2 * (kTG / 32)) * sizeof(float);
+constexpr size_t kSeedSmem = (2 * kTile + 6 * kMax) * sizeof(float);
+constexpr size_t kGradSmem = (11 * kTile + kSmall + 8 * kMax + 3 * kMax * kRedCols + 2 * (kTG / 32)) * sizeof(float);
 
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
