@@ -39,7 +39,6 @@ struct BBParams {
 
 constexpr int kT = 256;             // threads per CTA (seed kernel: 4 x 4 blocks of a 64 x 64 product)
 constexpr int kTG = 512;            // threads per CTA of the gradient kernel (2 x 4 blocks)
-constexpr int kTM = 2;              // rows per thread block of the gradient kernel's products
 constexpr int kMax = 64;            // N, P and C*R limit of this path
 constexpr int kLD = kMax + 1;       // FP32 tile row stride
 constexpr int kTile = kMax * kLD;   // floats per tile
@@ -64,6 +63,76 @@ __device__ __forceinline__ void mm4(float (&acc)[TM][TN], int i0, int j0, int K,
     for (int u = 0; u < TM; u++)
 #pragma unroll
       for (int v = 0; v < TN; v++) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+  }
+}
+// FP32 products on the tensor cores with FP32-level accuracy: each operand
+// x = hi + lo with hi = tf32(x) and lo = tf32(x - hi) (round to nearest,
+// |x - hi - lo| <= 2^-22 |x|), and a b = hi_a hi_b + hi_a lo_b + lo_a hi_b
+// (the dropped lo_a lo_b is below 2^-21 relative); FP32 accumulation.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  uint32_t h, l;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
+  const float r = x - __uint_as_float(h);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
+  hi = h;
+  lo = l;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// acc += a b over k < K for this warp's 16 x 16 output tile at (r0, c0):
+// m16n8k8 fragments (A: rows g, g+8 at k = c, c+4; B: column g at k = c,
+// c+4; accumulator nb: rows g, g+8, columns nb*8 + 2c, +1; g = lane / 4,
+// c = lane % 4).  k past K reads as zero.
+template <class FA, class FB>
+__device__ __forceinline__ void mm_tc(float (&acc)[2][4], int r0, int c0, int K, FA a, FB b) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, cq = lane & 3;
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    const int ka = k0 + cq, kb = ka + 4;
+    const bool va = ka < K, vb = kb < K;
+    float af[4];
+    af[0] = va ? a(r0 + g, ka) : 0.f;
+    af[1] = va ? a(r0 + g + 8, ka) : 0.f;
+    af[2] = vb ? a(r0 + g, kb) : 0.f;
+    af[3] = vb ? a(r0 + g + 8, kb) : 0.f;
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) split_tf32(af[q], ah[q], al[q]);
+#pragma unroll
+    for (int nb = 0; nb < 2; nb++) {
+      uint32_t bh0, bl0, bh1, bl1;
+      split_tf32(va ? b(ka, c0 + nb * 8 + g) : 0.f, bh0, bl0);
+      split_tf32(vb ? b(kb, c0 + nb * 8 + g) : 0.f, bh1, bl1);
+      mma_tf32(acc[nb], ah, bl0, bl1);
+      mma_tf32(acc[nb], al, bh0, bh1);
+      mma_tf32(acc[nb], ah, bh0, bh1);
+    }
+  }
+}
+__device__ __forceinline__ void zero_tc(float (&acc)[2][4]) {
+#pragma unroll
+  for (int nb = 0; nb < 2; nb++) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+}
+// Row and column of element e of accumulator nb of this lane's fragments.
+#define TC_ROW(r0, e) ((r0) + ((threadIdx.x & 31) >> 2) + 8 * ((e) >> 1))
+#define TC_COL(c0, nb, e) ((c0) + (nb) * 8 + 2 * (threadIdx.x & 3) + ((e) & 1))
+// Per-row sums of this warp's tile: each lane adds its values of rows g and
+// g+8 (rs[0], rs[1]); the four lanes of a row group combine, and lane c = 0
+// writes the tile's partial to red[row * kRedCols + wc].
+__device__ __forceinline__ void tc_row_sums(float (&rs)[2], float* red, int r0, int wc) {
+#pragma unroll
+  for (int h2 = 0; h2 < 2; h2++) {
+    rs[h2] += __shfl_xor_sync(0xffffffffu, rs[h2], 1);
+    rs[h2] += __shfl_xor_sync(0xffffffffu, rs[h2], 2);
+  }
+  if ((threadIdx.x & 3) == 0) {
+    const int g = (threadIdx.x & 31) >> 2;
+    red[(r0 + g) * kRedCols + wc] = rs[0];
+    red[(r0 + g + 8) * kRedCols + wc] = rs[1];
   }
 }
 template <int TM, int TN>
@@ -238,7 +307,8 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   float* qk = sm + C * C;
   float* dqk = qk + C * R * R;
   const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  const int tid = threadIdx.x, i0 = (tid >> 4) * kTM, j0 = (tid & 15) * 4;
+  const int tid = threadIdx.x, wid = tid >> 5;
+  const int fr0 = (wid >> 2) * 16, fc0 = (wid & 3) * 16, wc = wid & 3;  // this warp's 16 x 16 tile
 
   // ---- inputs of the chunk
   load_tokens(p, bh, c, gam, fac, ea, er, valid);
@@ -267,16 +337,16 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   //      a mask (padded rows and the upper triangle never reach a product)
   auto tok_ok = [=](int i, int j) { return (i / R) > (j / R) && valid[i / R] != 0.f; };
   {
-    float acc[kTM][4];
-    zero4(acc);
-    mm4(acc, i0, j0, N, [=](int i, int n) { return Qr[i * kLD + n]; }, [=](int n, int j) { return Kr[j * kLD + n]; });
+    float acc[2][4];
+    zero_tc(acc);
+    mm_tc(acc, fr0, fc0, N, [=](int i, int n) { return Qr[i * kLD + n]; }, [=](int n, int j) { return Kr[j * kLD + n]; });
 #pragma unroll
-    for (int u = 0; u < kTM; u++)
+    for (int nb = 0; nb < 2; nb++)
 #pragma unroll
-      for (int v = 0; v < 4; v++) {
-        const int i = i0 + u, j = j0 + v;
+      for (int e = 0; e < 4; e++) {
+        const int i = TC_ROW(fr0, e), j = TC_COL(fc0, nb, e);
         if (i < CR && j < CR)
-          M1[i * kLD + j] = tok_ok(i, j) ? acc[u][v] * facr[j] * expf(seg[(i / R) * C + j / R]) : 0.f;
+          M1[i * kLD + j] = tok_ok(i, j) ? acc[nb][e] * facr[j] * expf(seg[(i / R) * C + j / R]) : 0.f;
       }
   }
   __syncthreads();
@@ -284,33 +354,34 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   // ---- dPsiV = A^T dPhiO + k_state D_{c+1} + d dPhiO + gamma qk^T dPhiO (diagonal);
   //      dA = dPhiO PsiV^T
   {
-    float acc[kTM][4];
-    zero4(acc);
-    mm4(acc, i0, j0, CR, [=](int j, int i) { return M1[i * kLD + j]; }, [=](int i, int pp) { return Gp[i * kLD + pp]; });
-    float acc2[kTM][4];
-    zero4(acc2);
-    mm4(acc2, i0, j0, N, [=](int j, int n) { return Kr[j * kLD + n]; }, [=](int n, int pp) { return Dn[n * kLD + pp]; });
+    float acc[2][4], acc2[2][4];
+    zero_tc(acc);
+    mm_tc(acc, fr0, fc0, CR, [=](int j, int i) { return M1[i * kLD + j]; }, [=](int i, int pp) { return Gp[i * kLD + pp]; });
+    zero_tc(acc2);
+    mm_tc(acc2, fr0, fc0, N, [=](int j, int n) { return Kr[j * kLD + n]; }, [=](int n, int pp) { return Dn[n * kLD + pp]; });
     const float dv = p.has_d ? p.d[h] : 0.f;
 #pragma unroll
-    for (int u = 0; u < kTM; u++)
+    for (int nb = 0; nb < 2; nb++)
 #pragma unroll
-      for (int v = 0; v < 4; v++) {
-        const int j = i0 + u, pp = j0 + v;
+      for (int e = 0; e < 4; e++) {
+        const int j = TC_ROW(fr0, e), pp = TC_COL(fc0, nb, e);
         if (j < CR && pp < P) {
           const int t = j / R, r = j % R;
-          float x = acc[u][v] + acc2[u][v] * facr[j] * err[j] + dv * Gp[j * kLD + pp];
+          float x = acc[nb][e] + acc2[nb][e] * facr[j] * err[j] + dv * Gp[j * kLD + pp];
           float dg = 0.f;
           for (int o = 0; o < R; o++) dg = fmaf(qk[(t * R + o) * R + r], Gp[(t * R + o) * kLD + pp], dg);
           dP[j * kLD + pp] = fmaf(gam[t], dg, x);
         }
       }
-    zero4(acc);
-    mm4(acc, i0, j0, P, [=](int i, int pp) { return Gp[i * kLD + pp]; }, [=](int pp, int j) { return Ps[j * kLD + pp]; });
+    zero_tc(acc);
+    mm_tc(acc, fr0, fc0, P, [=](int i, int pp) { return Gp[i * kLD + pp]; }, [=](int pp, int j) { return Ps[j * kLD + pp]; });
 #pragma unroll
-    for (int u = 0; u < kTM; u++)
+    for (int nb = 0; nb < 2; nb++)
 #pragma unroll
-      for (int v = 0; v < 4; v++)
-        if (i0 + u < CR && j0 + v < CR) M2[(i0 + u) * kLD + j0 + v] = acc[u][v];
+      for (int e = 0; e < 4; e++) {
+        const int i = TC_ROW(fr0, e), j = TC_COL(fc0, nb, e);
+        if (i < CR && j < CR) M2[i * kLD + j] = acc[nb][e];
+      }
   }
   __syncthreads();
 
@@ -333,58 +404,54 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
 
   // ---- dq_rot = dS k_scaled + exp(da_cs) dPhiO Hc^T;
   //      dk_scaled = dS^T q_rot + exp(da_cs_rev) dk_state, dk_state = PsiV Dn^T;
-  //      row sums for DDA_CS_REV (dk_state * k_state) and DDA_CS (inter * dPhiO)
+  //      row sums for DDA_CS_REV (dk_state * k_state), DFACTOR (dk_scaled *
+  //      k_rot) and DDA_CS (inter * dPhiO)
   {
-    float acc[kTM][4];
-    zero4(acc);
-    mm4(acc, i0, j0, CR, [=](int i, int j) { return M2[i * kLD + j] * facr[j]; },
-        [=](int j, int n) { return Kr[j * kLD + n]; });
-    float acc2[kTM][4];
-    zero4(acc2);
-    mm4(acc2, i0, j0, P, [=](int i, int pp) { return Gp[i * kLD + pp]; }, [=](int pp, int n) { return Hc[n * kLD + pp]; });
+    float acc[2][4], acc2[2][4];
+    zero_tc(acc);
+    mm_tc(acc, fr0, fc0, CR, [=](int i, int j) { return M2[i * kLD + j] * facr[j]; },
+          [=](int j, int n) { return Kr[j * kLD + n]; });
+    zero_tc(acc2);
+    mm_tc(acc2, fr0, fc0, P, [=](int i, int pp) { return Gp[i * kLD + pp]; }, [=](int pp, int n) { return Hc[n * kLD + pp]; });
 #pragma unroll
-    for (int u = 0; u < kTM; u++)
+    for (int nb = 0; nb < 2; nb++)
 #pragma unroll
-      for (int v = 0; v < 4; v++)
-        if (i0 + u < CR && j0 + v < N) dQ[(i0 + u) * kLD + j0 + v] = fmaf(ear[i0 + u], acc2[u][v], acc[u][v]);
-    // dk_state = PsiV D^T, dk_scaled = dS^T q_rot + exp(da_cs_rev) dk_state, with
-    // row sums for DDA_CS_REV (dk_state * k_state) and DFACTOR (dk_scaled * k_rot)
-    zero4(acc);
-    mm4(acc, i0, j0, P, [=](int j, int pp) { return Ps[j * kLD + pp]; }, [=](int pp, int n) { return Dn[n * kLD + pp]; });
-    zero4(acc2);
-    mm4(acc2, i0, j0, CR, [=](int j, int i) { return M2[i * kLD + j]; }, [=](int i, int n) { return Qr[i * kLD + n]; });
+      for (int e = 0; e < 4; e++) {
+        const int i = TC_ROW(fr0, e), n = TC_COL(fc0, nb, e);
+        if (i < CR && n < N) dQ[i * kLD + n] = fmaf(ear[i], acc2[nb][e], acc[nb][e]);
+      }
+    zero_tc(acc);
+    mm_tc(acc, fr0, fc0, P, [=](int j, int pp) { return Ps[j * kLD + pp]; }, [=](int pp, int n) { return Dn[n * kLD + pp]; });
+    zero_tc(acc2);
+    mm_tc(acc2, fr0, fc0, CR, [=](int j, int i) { return M2[i * kLD + j]; }, [=](int i, int n) { return Qr[i * kLD + n]; });
+    float r1[2] = {0.f, 0.f}, r2[2] = {0.f, 0.f};
 #pragma unroll
-    for (int u = 0; u < kTM; u++) {
-      const int j = i0 + u;
-      float r1 = 0.f, r2 = 0.f;
+    for (int nb = 0; nb < 2; nb++)
 #pragma unroll
-      for (int v = 0; v < 4; v++) {
-        const int n = j0 + v;
+      for (int e = 0; e < 4; e++) {
+        const int j = TC_ROW(fr0, e), n = TC_COL(fc0, nb, e);
         if (j < CR && n < N) {
           const float kr = Kr[j * kLD + n];
-          r1 = fmaf(acc[u][v], kr * facr[j] * err[j], r1);
-          const float dks = fmaf(err[j], acc[u][v], acc2[u][v]);
-          r2 = fmaf(dks, kr, r2);
+          r1[e >> 1] = fmaf(acc[nb][e], kr * facr[j] * err[j], r1[e >> 1]);
+          const float dks = fmaf(err[j], acc[nb][e], acc2[nb][e]);
+          r2[e >> 1] = fmaf(dks, kr, r2[e >> 1]);
           dK[j * kLD + n] = dks;
         }
       }
-      red[j * kRedCols + (tid & 15)] = r1;
-      red2[j * kRedCols + (tid & 15)] = r2;
-    }
-  }
-  {  // inter = exp(da_cs) q_rot Hc: row sums with dPhiO (DDA_CS)
-    float acc[kTM][4];
-    zero4(acc);
-    mm4(acc, i0, j0, N, [=](int i, int n) { return Qr[i * kLD + n]; }, [=](int n, int pp) { return Hc[n * kLD + pp]; });
+    tc_row_sums(r1, red, fr0, wc);
+    tc_row_sums(r2, red2, fr0, wc);
+    // inter = exp(da_cs) q_rot Hc
+    zero_tc(acc);
+    mm_tc(acc, fr0, fc0, N, [=](int i, int n) { return Qr[i * kLD + n]; }, [=](int n, int pp) { return Hc[n * kLD + pp]; });
+    float r3[2] = {0.f, 0.f};
 #pragma unroll
-    for (int u = 0; u < kTM; u++) {
-      const int i = i0 + u;
-      float rs = 0.f;
+    for (int nb = 0; nb < 2; nb++)
 #pragma unroll
-      for (int v = 0; v < 4; v++)
-        if (i < CR && j0 + v < P) rs = fmaf(acc[u][v] * ear[i], Gp[i * kLD + j0 + v], rs);
-      red3[i * kRedCols + (tid & 15)] = rs;
-    }
+      for (int e = 0; e < 4; e++) {
+        const int i = TC_ROW(fr0, e), pp = TC_COL(fc0, nb, e);
+        if (i < CR && pp < P) r3[e >> 1] = fmaf(acc[nb][e] * ear[i], Gp[i * kLD + pp], r3[e >> 1]);
+      }
+    tc_row_sums(r3, red3, fr0, wc);
   }
   // same-token terms: dot[t,o,r] = dPhiO[(t,o)] . PsiV[(t,r)]; dqk = gamma dot,
   // DGAMMA = sum qk * dot
@@ -414,7 +481,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   for (int t = tid; t < C; t += kTG) {  // per-token sums
     float s1 = 0.f, s2 = 0.f, s3 = 0.f, g = 0.f;
     for (int r = 0; r < R; r++)
-      for (int q = 0; q < kRedCols; q++) {
+      for (int q = 0; q < 4; q++) {  // the four column tiles of the row
         s1 += red[(t * R + r) * kRedCols + q];
         s2 += red2[(t * R + r) * kRedCols + q];
         s3 += red3[(t * R + r) * kRedCols + q];
