@@ -13,7 +13,7 @@ its own replica and the slowest rank's time counts.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
 
 ``--op bwd_bwd`` instead times the second backward stage (mamba_mimo_bwd_bwd)
-on the same shape and prints its own line (metric, FP32-ALU roofline of its
+on the same shape and prints its own line (metric, tensor roofline of its
 gradient kernel, CPU-oracle baseline on a sample of heads).
 """
 
@@ -269,11 +269,11 @@ def _prefix(inp, tokens, C):
 
 
 BB_METRIC = "MIMO bwd_bwd tokens/s at B1 S8192 H16 N=P=64 R4 C16"
-FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor throughput of a GB300
 
 
 def bb_grad_flop(wl):
-    """Algorithmic FP32 FLOP of the second stage's gradient kernel per call:
+    """Algorithmic FLOP of the second stage's gradient kernel per call:
     per chunk and (b,h), the five strictly causal products (Q Ks^T, A^T dPhiO,
     dPhiO PsiV^T, dS Ks, dS^T Q: R^2 C(C-1)/2 x (3N + 2P) multiply-adds) and
     the four state products (dPhiO Hc^T, k_state D, PsiV D^T, Q Hc: 4 CR N P)."""
@@ -362,9 +362,11 @@ def run_bwd_bwd(args, world, rank, local):
         if name:
             stage_ms[name.decode()] = statistics.mean(row[2 * k].elapsed_time(row[2 * k + 1]) for row in ev)
     grad_ms = stage_ms["bb_grad"]
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
-    alu_peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    # the products run on the tensor cores in TF32 (three passes per FP32
+    # product): the peak is TF32's, the measured BF16 figure times the
+    # nominal TF32 / BF16 ratio
+    bf16_peak, bf16_kind = measured_bf16_tflops()
+    tc_peak = bf16_peak * TF32_PER_BF16
     flop = bb_grad_flop(wl)
     achieved = flop / (grad_ms * 1e-3) / 1e12
     hbm, hbm_kind = measured_peaks()
@@ -379,10 +381,11 @@ def run_bwd_bwd(args, world, rank, local):
                    "d": True, "caches": "seeded stand-ins for states / qk_dot",
                    "parallelism": f"replicas{world}",
                    "l2": f"{nsets} rotating input+output sets, {nsets * (in_bytes + out_bytes) / 1e6:.0f} MB > 129 MB L2"},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                     "frac": achieved / alu_peak, "traffic": None, "kernel": "bb_grad",
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tc_peak, "traffic": None, "kernel": "bb_grad",
                      "algorithmic_flop_per_launch": flop,
-                     "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {mhz:.0f} MHz"},
+                     "peak_source": f"{bf16_kind} bf16 x nominal tf32/bf16 {TF32_PER_BF16:.3f}",
+                     "path": "mma.sync m16n8k8 tf32, three passes per FP32 product (hi.hi + hi.lo + lo.hi)"},
         "op_hbm_frac": (in_bytes + out_bytes) / (ms_per_step * 1e-3) / 1e9 / hbm,
         "algorithmic_bytes_per_call": in_bytes + out_bytes,
         "stage_ms": stage_ms, "gpu_launches": launches * steps, "clocks": clocks,
