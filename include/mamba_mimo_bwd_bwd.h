@@ -63,8 +63,10 @@
  * rotary_dim_divisor in {2, 4}, N % rotary_dim_divisor == 0) and this
  * build's: N <= 64, P <= 64, C*R <= 64 (MMBF_ERR_UNSUPPORTED otherwise).
  *
- * Numerics: FP32 throughout (products, sums, the reverse scan); results are
- * deterministic (no floating-point atomics).
+ * Numerics: FP32 throughout (sums, the reverse scan); the tile products run
+ * on the tensor cores in TF32 with each FP32 operand split into two TF32
+ * parts and three products per pair, which keeps FP32-level accuracy.
+ * Results are deterministic (no floating-point atomics).
  */
 #ifndef MAMBA_MIMO_BWD_BWD_H
 #define MAMBA_MIMO_BWD_BWD_H

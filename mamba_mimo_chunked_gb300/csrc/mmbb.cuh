@@ -16,10 +16,11 @@
 //   grad_kernel   (chunk, b*h)  every gradient of the chunk from its inputs,
 //                               the state entering it (the states cache) and
 //                               D_{c+1}: 9 products of at most 64 x 64 x 64
-//                               in FP32 tiles in shared memory;
+//                               of FP32 tiles in shared memory, on the tensor
+//                               cores (TF32, three passes per FP32 product);
 //   reduce_kernel (b*h)         DMIMO_V and DD: the chunks' partial sums in
 //                               chunk order.
-// FP32 throughout, deterministic (no floating-point atomics).
+// FP32-level accuracy throughout, deterministic (no floating-point atomics).
 
 #include "mamba_mimo_bwd_bwd.h"
 
