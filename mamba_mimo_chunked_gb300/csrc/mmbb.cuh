@@ -41,7 +41,7 @@ struct BBParams {
 constexpr int kT = 256;             // threads per CTA (seed kernel: 4 x 4 blocks of a 64 x 64 product)
 constexpr int kTG = 512;            // threads per CTA of the gradient kernel (2 x 4 blocks)
 constexpr int kMax = 64;            // N, P and C*R limit of this path
-constexpr int kLD = kMax + 1;       // FP32 tile row stride
+constexpr int kLD = kMax + 4;       // FP32 tile row stride: 4 (mod 32) puts the 32 lanes of every m16n8k8 fragment load on distinct banks
 constexpr int kTile = kMax * kLD;   // floats per tile
 constexpr int kSmall = 4224;        // segsum [C][C], qk [C][R][R], dqk (C*R <= 64, R <= 16)
 constexpr int kRedCols = 16;        // per-row partial sums, one per column block
