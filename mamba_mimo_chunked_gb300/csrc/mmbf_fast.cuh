@@ -13,10 +13,14 @@
 //   four ranks of one token: the rank-ordered BF16 diagonal and dz sums then
 //   need no cross-lane traffic.  The permutation only reorders the summation
 //   index of the contractions; what is computed is unchanged.
-// * Two launches per call: state_kernel (segment sums, the units of a
-//   segment folded inside a thread-block cluster) and output_kernel (each
-//   CTA folds the earlier segments' sums into its entering state; its last
-//   CTA per (b,h) sums the gradient partials).
+// * Three launches per call: state_kernel (segment sums, the units of a
+//   segment folded inside a thread-block cluster), segment_prefix_fast_kernel
+//   (the exclusive scan over segments) and output_kernel (each CTA reads its
+//   entering state; its last CTA per (b,h) sums the gradient partials).
+// * Token scalars (gamma, factor, exp(da_cs), exp(da_cs_rev)) come from a
+//   two-window table filled one token per thread at each window's first
+//   chunk; the epilogue meets BF16 and FP32 values in the mixed-precision
+//   add / fma instructions.
 // * The FP32 state is the transposed tile state^T[p][n], split over the warps
 //   by p-block.  For N = P = 64 it lives in tensor memory as the accumulator
 //   of an M = 64 tcgen05.mma that adds PsiV^T k_state each chunk; otherwise

@@ -27,12 +27,17 @@
 //   grad_reduce_kernel     grid (b*h)
 //       Fixed-order sum of the per-segment dmimo_o / dmimo_z partials.
 //
-// Shapes with specialised kernels (mmbf_fast.cuh) run two launches:
-// fast::state_kernel over state units of LA chunks (the units of a segment
-// form a thread-block cluster and fold their sums into the segment's sum),
-// and fast::output_kernel, whose CTAs fold the earlier segments' sums into
-// their entering state and whose last CTA per (b,h) -- found with an atomic
-// counter -- does the fixed-order gradient sum.
+// Shapes with specialised kernels (mmbf_fast.cuh) run three launches,
+// chained by programmatic dependent launch: fast::state_kernel over state
+// units of LA chunks (the units of a segment form a thread-block cluster and
+// fold their sums into the segment's sum); segment_prefix_fast_kernel, the
+// exclusive scan over segments with one state element per thread; and
+// fast::output_kernel, whose CTAs read their entering state and whose last
+// CTA per (b,h) -- found with an atomic counter -- does the fixed-order
+// gradient sum.
+//
+// The second backward stage (mamba_mimo_bwd_bwd) has its own kernels and
+// entry points in mmbb.cuh, included at the end of this file.
 //
 // Rows of a chunk tile are j = t*R + r (token-major), as in the reference's
 // flatten of the token and rank axes.  BF16 products and sums of two BF16
