@@ -71,6 +71,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--with-y", action="store_true",
                     help="time mamba_mimo_bwd_fwd_y (the op plus the layer's forward output y)")
+    ap.add_argument("--workload", type=int, default=None,
+                    help="index into synthetic_inputs.WORKLOADS (default: the timed shape, 2); other "
+                         "shapes print their own line (no pages' number to compare, no profile traffic)")
     ap.add_argument("--op", choices=["bwd_fwd", "bwd_bwd"], default="bwd_fwd",
                     help="bwd_bwd: time the second backward stage instead (its own JSON line)")
     return ap.parse_args()
@@ -433,13 +436,15 @@ def main():
     torch.cuda.set_device(dev)
     mm.build()
     lib = mm.load_library()
-    wl = si.WORKLOADS[WORKLOAD_INDEX]
+    wi = WORKLOAD_INDEX if args.workload is None else args.workload
+    wl = si.WORKLOADS[wi]
+    timed_shape = wi == WORKLOAD_INDEX
     stream = torch.cuda.current_stream(dev)
 
     # Input/output sets, resident in HBM before timing starts.
     sets = []
     for s in range(args.sets):
-        inp = si.make_inputs(**wl.shape_kwargs(), seed=si.WORKLOAD_SEED_BASE + WORKLOAD_INDEX + 7919 * s
+        inp = si.make_inputs(**wl.shape_kwargs(), seed=si.WORKLOAD_SEED_BASE + wi + 7919 * s
                              + 104729 * rank, device=dev)
         if args.with_y:  # y travels with the outputs (last field)
             out, y = mm.mamba_mimo_bwd_fwd_with_y(*si.args_of(inp))
@@ -602,10 +607,11 @@ def main():
                          "one packed buffer each way per step"}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC if timed_shape else f"MIMO bwd_fwd tokens/s at {wl.name}",
+        "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": value / (PAGES_TOKENS_PER_S * world),
+        "vs_baseline": value / (PAGES_TOKENS_PER_S * world) if timed_shape else None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "H": wl.H, "G": wl.G, "R": wl.R,
                    "N": wl.N, "P": wl.P, "chunk_size": wl.C, "rotary_dim_divisor": wl.div,
@@ -614,7 +620,7 @@ def main():
                    "l2": f"{args.sets} rotating input+output sets, "
                          f"{args.sets * alg_bytes / 1e6:.0f} MB > 129 MB L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profile_traffic(),
+                     "frac": achieved / peak, "traffic": profile_traffic() if timed_shape else None,
                      "kernel": DOMINANT, "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": peak_kind},
         "op_hbm_frac": alg_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
