@@ -317,7 +317,8 @@ def run_bwd_bwd(args, world, rank, local):
     sets = []
     for s in range(nsets):
         a = _bb_inputs(wl, si.WORKLOAD_SEED_BASE + 31 * s + 104729 * rank, dev)
-        outs = mm.mamba_mimo_bwd_bwd(*a[:15], mimo_o=a[15], d=a[16], chunk_size=wl.C, rotary_dim_divisor=wl.div)
+        outs = mm.mamba_mimo_bwd_bwd(*a[:15], mimo_o=a[15], d=a[16], chunk_size=wl.C, rotary_dim_divisor=wl.div,
+                                     output_dtype=torch.float32)  # the pages' example call
         sets.append((a, outs))
     torch.cuda.synchronize(dev)
     in_bytes = sum(nbytes(t) for t in sets[0][0])
@@ -326,7 +327,7 @@ def run_bwd_bwd(args, world, rank, local):
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     dims = mm._Dims(wl.B, wl.S, wl.H, wl.G, wl.R, wl.N, wl.P)
     sh = ctypes.c_void_p(stream.cuda_stream)
-    call_args = [[ctypes.byref(dims)] + [mm._ptr(t) for t in a] + [wl.C, wl.div]
+    call_args = [[ctypes.byref(dims)] + [mm._ptr(t) for t in a] + [wl.C, wl.div, 0]
                  + [mm._ptr(o[n]) for n in mm.BWD_BWD_OUTPUTS] + [mm._ptr(workspace), ws_bytes, sh]
                  for a, o in sets]
     for i in range(args.warmup):

@@ -47,7 +47,8 @@
  *   mimo_o      [H,R,P] or NULL                         fp32   (NULL: dout per rank)
  *   d           [H] or NULL                             fp32
  *
- *   output (all fp32: the pages' call with output_dtype = float32)
+ *   output (fp32; DQ, DK, DV in the dtype `dqkv_dtype` selects: the pages'
+ *   output_dtype, whose default is the inputs' bf16)
  *   DQ, DK      [B,S*R,H,N]   per head (sum over a group's heads for q / k)
  *   DV          [B,S,H,P]
  *   DMIMO_V     [B,H,R,P]     per batch (sum over B for mimo_v)
@@ -85,8 +86,9 @@ mmbf_status mamba_mimo_bwd_bwd_workspace_size(const mmbf_dims* dims, int64_t chu
 
 /* Enqueue the second backward stage on `stream` (a cudaStream_t; NULL for
  * the legacy default stream).  Inputs in the pages' positional order (dout
- * ... angles, mimo_o, d), then chunk_size and rotary_dim_divisor, then the
- * 12 outputs in the pages' order, then the workspace.  Validation failures
+ * ... angles, mimo_o, d), then chunk_size, rotary_dim_divisor and
+ * dqkv_dtype (0: DQ, DK, DV in fp32; 1: in bf16, rounded to nearest even),
+ * then the 12 outputs in the pages' order, then the workspace.  Validation failures
  * enqueue nothing and return an error (message in mamba_mimo_last_error);
  * MMBF_ERR_CUDA reports a launch error.  Asynchronous; calls sharing a
  * workspace must be ordered on one stream.  Four kernels: the per-chunk
@@ -100,8 +102,8 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
                                const float* da_cs, const float* da_cs_rev, const float* dt,
                                const void* trap, const float* segsum, const float* angles,
                                const float* mimo_o, const float* d, int64_t chunk_size,
-                               int64_t rotary_dim_divisor, float* DQ, float* DK, float* DV,
-                               float* DMIMO_V, float* DANGLES, float* DFACTOR, float* DGAMMA,
+                               int64_t rotary_dim_divisor, int dqkv_dtype, void* DQ, void* DK,
+                               void* DV, float* DMIMO_V, float* DANGLES, float* DFACTOR, float* DGAMMA,
                                float* DDA, float* DSSDA, float* DDA_CS_REV, float* DDA_CS, float* DD,
                                void* workspace, size_t workspace_bytes, void* stream);
 

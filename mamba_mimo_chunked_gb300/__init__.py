@@ -91,7 +91,7 @@ def load_library():
         lib.mamba_mimo_stage_name.argtypes = [ctypes.c_int]
         lib.mamba_mimo_bwd_bwd.restype = ctypes.c_int
         lib.mamba_mimo_bwd_bwd.argtypes = (
-            [ctypes.POINTER(_Dims)] + [vp] * 17 + [i64, i64] + [vp] * 12 + [vp, ctypes.c_size_t, vp])
+            [ctypes.POINTER(_Dims)] + [vp] * 17 + [i64, i64, ctypes.c_int] + [vp] * 12 + [vp, ctypes.c_size_t, vp])
         lib.mamba_mimo_bwd_bwd_workspace_size.restype = ctypes.c_int
         lib.mamba_mimo_bwd_bwd_workspace_size.argtypes = [
             ctypes.POINTER(_Dims), i64, i64, ctypes.POINTER(ctypes.c_size_t)]
@@ -325,13 +325,16 @@ def bwd_bwd_workspace_size(B, S, H, G, R, N, P, chunk_size=16, rotary_dim_diviso
 
 def mamba_mimo_bwd_bwd(dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt,
                        trap, segsum, angles, mimo_o=None, d=None, chunk_size: int = 16,
-                       rotary_dim_divisor: int = 4, *, workspace: torch.Tensor | None = None) -> dict:
+                       rotary_dim_divisor: int = 4, output_dtype=None, *,
+                       workspace: torch.Tensor | None = None) -> dict:
     """Second Mamba-3 MIMO backward stage on the current CUDA stream.
 
     Arguments in the pages' order (the first stage's ``states`` and
     ``qk_dot`` caches among them); ``mimo_o`` selects reduce-O ``dout``
-    ([B,S,H,P]), ``d`` adds the D-skip gradient.  Returns a dict of the 12
-    FP32 gradients (``DD`` is None without ``d``)."""
+    ([B,S,H,P]), ``d`` adds the D-skip gradient.  ``output_dtype`` sets the
+    dtype of DQ, DK and DV (None: the inputs' bfloat16, as on the pages; or
+    torch.float32); the other nine gradients are FP32.  Returns a dict of
+    the 12 gradients (``DD`` is None without ``d``)."""
     if q.dim() != 5:
         raise ValueError("q must have shape [B, S, R, G, N]")
     B, S, R, G, N = q.shape
@@ -370,14 +373,18 @@ def mamba_mimo_bwd_bwd(dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da
         _check("dout", dout, (B, S, R, H, P), bf16, dev)
     if d is not None:
         _check("d", d, (H,), f32, dev)
+    if output_dtype is None:
+        output_dtype = q.dtype
+    if output_dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("output_dtype must be None, torch.bfloat16 or torch.float32")
     args = tuple(None if a is None else a.contiguous() for a in (
         dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt, trap, segsum,
         angles, mimo_o, d))
     lib = load_library()
     outs = {
-        "DQ": torch.empty((B, S * R, H, N), dtype=f32, device=dev),
-        "DK": torch.empty((B, S * R, H, N), dtype=f32, device=dev),
-        "DV": torch.empty((B, S, H, P), dtype=f32, device=dev),
+        "DQ": torch.empty((B, S * R, H, N), dtype=output_dtype, device=dev),
+        "DK": torch.empty((B, S * R, H, N), dtype=output_dtype, device=dev),
+        "DV": torch.empty((B, S, H, P), dtype=output_dtype, device=dev),
         "DMIMO_V": torch.empty((B, H, R, P), dtype=f32, device=dev),
         "DANGLES": torch.empty((B, S, H, N // rotary_dim_divisor), dtype=f32, device=dev),
         "DFACTOR": torch.empty((B, H, S), dtype=f32, device=dev),
@@ -395,7 +402,8 @@ def mamba_mimo_bwd_bwd(dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da
     with torch.cuda.device(dev):
         st = lib.mamba_mimo_bwd_bwd(
             ctypes.byref(_Dims(B, S, H, G, R, N, P)), *[_ptr(a) for a in args], chunk_size,
-            rotary_dim_divisor, *[_ptr(outs[n]) for n in BWD_BWD_OUTPUTS], _ptr(workspace),
+            rotary_dim_divisor, int(output_dtype == torch.bfloat16),
+            *[_ptr(outs[n]) for n in BWD_BWD_OUTPUTS], _ptr(workspace),
             workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream))
     if st:
         _raise(lib, st)

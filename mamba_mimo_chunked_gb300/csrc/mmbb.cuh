@@ -29,9 +29,11 @@ namespace bb {
 
 struct BBParams {
   int B, S, H, G, R, N, P, C, w, nc, CR, reduced, has_d;
+  int dqkv_bf16;  // DQ, DK, DV stored as BF16 (else FP32)
   const uint16_t *dout, *q, *k, *v, *states, *qk, *trap;
   const float *q_bias, *k_bias, *mimo_v, *mimo_o, *d, *da_cs, *da_cs_rev, *dt, *segsum, *angles;
-  float *DQ, *DK, *DV, *DMIMO_V, *DANGLES, *DFACTOR, *DGAMMA, *DDA, *DSSDA, *DDA_CS_REV, *DDA_CS, *DD;
+  void *DQ, *DK, *DV;  // FP32 or BF16 (dqkv_bf16)
+  float *DMIMO_V, *DANGLES, *DFACTOR, *DGAMMA, *DDA, *DSSDA, *DDA_CS_REV, *DDA_CS, *DD;
   float* ws_D;      // [BH][nc][N][P]: seeds G_c, then D_{c+1}
   float* ws_alpha;  // [BH][nc]
   float* ws_mv;     // [BH][nc][R][P]: DMIMO_V partials
@@ -47,6 +49,14 @@ constexpr int kSmall = 4224;        // segsum [C][C], qk [C][R][R], dqk (C*R <= 
 constexpr int kRedCols = 16;        // per-row partial sums, one per column block
 
 __device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+// Element i of DQ / DK / DV in the requested dtype (FP32, or BF16 rounded to
+// nearest even).
+__device__ __forceinline__ void store_dqkv(void* base, int64_t i, float x, int bf16) {
+  if (bf16)
+    static_cast<uint16_t*>(base)[i] = f_bf(x);
+  else
+    static_cast<float*>(base)[i] = x;
+}
 
 // acc[u][v] += sum_k a(i0+u, k) * b(k, j0+v): a 4 x 4 block of a product of
 // shared-memory tiles (rows and columns past the operands' extents are
@@ -557,7 +567,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
     if (tg >= p.S) continue;
     float s = 0.f;
     for (int r = 0; r < R; r++) s = fmaf(dP[(t * R + r) * kLD + pp], mvs[r * P + pp], s);
-    p.DV[(((int64_t)b * p.S + tg) * p.H + h) * P + pp] = s;
+    store_dqkv(p.DV, (((int64_t)b * p.S + tg) * p.H + h) * P + pp, s, p.dqkv_bf16);
   }
   for (int e = tid; e < R * P; e += kTG) {
     const int r = e / P, pp = e % P;
@@ -585,8 +595,8 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
       dk = fmaf(dqk[(t * R + x) * R + r], Qr[(t * R + x) * kLD + n], dk);  // row (t, r) of k
     }
     const int64_t o = (((int64_t)b * p.S + tg) * R + r) * p.H + h;
-    p.DQ[o * N + n] = dq;
-    p.DK[o * N + n] = dk;
+    store_dqkv(p.DQ, o * N + n, dq, p.dqkv_bf16);
+    store_dqkv(p.DK, o * N + n, dk, p.dqkv_bf16);
   }
 }
 
@@ -665,8 +675,8 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
                                const float* q_bias, const float* k_bias, const float* mimo_v, const void* states,
                                const void* qk_dot, const float* da_cs, const float* da_cs_rev, const float* dt,
                                const void* trap, const float* segsum, const float* angles, const float* mimo_o,
-                               const float* d, int64_t chunk_size, int64_t rotary_dim_divisor, float* DQ, float* DK,
-                               float* DV, float* DMIMO_V, float* DANGLES, float* DFACTOR, float* DGAMMA, float* DDA,
+                               const float* d, int64_t chunk_size, int64_t rotary_dim_divisor, int dqkv_dtype,
+                               void* DQ, void* DK, void* DV, float* DMIMO_V, float* DANGLES, float* DFACTOR, float* DGAMMA, float* DDA,
                                float* DSSDA, float* DDA_CS_REV, float* DDA_CS, float* DD, void* workspace,
                                size_t workspace_bytes, void* stream) {
   using namespace mmbf::bb;
@@ -678,6 +688,7 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
   for (const void* x : req)
     if (!x) return fail(MMBF_ERR_ARG, "a required pointer is NULL");
   if ((d == nullptr) != (DD == nullptr)) return fail(MMBF_ERR_ARG, "DD must be given exactly when d is");
+  if (dqkv_dtype != 0 && dqkv_dtype != 1) return fail(MMBF_ERR_ARG, "dqkv_dtype must be 0 (fp32) or 1 (bf16)");
   const void* all[] = {dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt, trap, segsum,
                        angles, mimo_o, d, DQ, DK, DV, DMIMO_V, DANGLES, DFACTOR, DGAMMA, DDA, DSSDA, DDA_CS_REV, DDA_CS, DD};
   for (const void* x : all)
@@ -699,7 +710,8 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
   p.da_cs = da_cs; p.da_cs_rev = da_cs_rev; p.dt = dt; p.segsum = segsum; p.angles = angles;
   p.reduced = mimo_o != nullptr;
   p.has_d = d != nullptr;
-  p.DQ = DQ; p.DK = DK; p.DV = DV; p.DMIMO_V = DMIMO_V; p.DANGLES = DANGLES; p.DFACTOR = DFACTOR;
+  p.DQ = DQ; p.DK = DK; p.DV = DV;
+  p.dqkv_bf16 = dqkv_dtype; p.DMIMO_V = DMIMO_V; p.DANGLES = DANGLES; p.DFACTOR = DFACTOR;
   p.DGAMMA = DGAMMA; p.DDA = DDA; p.DSSDA = DSSDA; p.DDA_CS_REV = DDA_CS_REV; p.DDA_CS = DDA_CS; p.DD = DD;
   p.ws_D = reinterpret_cast<float*>(ws + off[0]);
   p.ws_alpha = reinterpret_cast<float*>(ws + off[1]);

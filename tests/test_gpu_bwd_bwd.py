@@ -6,7 +6,10 @@ rest).  The oracle computes in float64, the kernels in FP32 (products of at
 most 64 terms, a reverse scan over chunks with decays below one), so every
 output is held to a relative RMS error below 1e-4; DDA and DANGLES, whose
 entries can sit near zero, also to a max-abs error below 1e-3 of their
-largest entry (the pages' global relative criterion for those two).
+largest entry (the pages' global relative criterion for those two).  Those
+checks take DQ, DK and DV in FP32 (output_dtype=torch.float32); with the
+default BF16 outputs the three must equal the FP32 results rounded to
+nearest even.
 """
 
 import numpy as np
@@ -45,9 +48,9 @@ def _problem(B, S, H, G, R, N, P, C, div=4, reduced=True, has_d=True, seed=0, ca
     return args, kw
 
 
-def _run_gpu(args, kw):
+def _run_gpu(args, kw, output_dtype=torch.float32):
     dev = torch.device("cuda:0")
-    g = mm.mamba_mimo_bwd_bwd(*[a.to(dev) for a in args],
+    g = mm.mamba_mimo_bwd_bwd(*[a.to(dev) for a in args], output_dtype=output_dtype,
                               **{k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in kw.items()})
     torch.cuda.synchronize(dev)
     return g
@@ -102,6 +105,27 @@ def test_deterministic_and_four_launches():
     g2 = _run_gpu(args, kw)
     for name in bb.OUTPUT_NAMES:
         assert torch.equal(g1[name], g2[name]), name
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[1]], ids=["S40_R4", "S33_R2"])
+def test_default_bf16_dq_dk_dv_are_the_rounded_fp32_results(case):
+    args, kw = _problem(**case, seed=23)
+    g32 = _run_gpu(args, kw)
+    g16 = _run_gpu(args, kw, output_dtype=None)
+    for name in bb.OUTPUT_NAMES:
+        if g32[name] is None:
+            assert g16[name] is None
+        elif name in ("DQ", "DK", "DV"):
+            assert g16[name].dtype == torch.bfloat16, name
+            assert torch.equal(g16[name], g32[name].to(torch.bfloat16)), name
+        else:
+            assert g16[name].dtype == torch.float32 and torch.equal(g16[name], g32[name]), name
+    # and against the oracle, within BF16's rounding (at most 2^-9 relative per entry)
+    want = bb.bwd_bwd(*args, **kw)
+    for name in ("DQ", "DK", "DV"):
+        g = g16[name].double().cpu().numpy()
+        err = np.sqrt(np.mean((g - want[name]) ** 2)) / np.sqrt(np.mean(want[name] ** 2))
+        assert err < 2.0 ** -9, f"{name}: relative RMS {err:.3e}"
 
 
 def test_outside_the_envelope_raises():
