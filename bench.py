@@ -327,7 +327,7 @@ def run_bwd_bwd(args, world, rank, local):
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     dims = mm._Dims(wl.B, wl.S, wl.H, wl.G, wl.R, wl.N, wl.P)
     sh = ctypes.c_void_p(stream.cuda_stream)
-    call_args = [[ctypes.byref(dims)] + [mm._ptr(t) for t in a] + [wl.C, wl.div, 0]
+    call_args = [[ctypes.byref(dims)] + [mm._ptr(t) for t in a] + [wl.C, wl.div, 1, 0]
                  + [mm._ptr(o[n]) for n in mm.BWD_BWD_OUTPUTS] + [mm._ptr(workspace), ws_bytes, sh]
                  for a, o in sets]
     for i in range(args.warmup):

@@ -32,23 +32,28 @@
  * tensor; the caller owns all memory (inputs, outputs, workspace); each call
  * only enqueues kernels on `stream`.
  *
+ * dtype codes (act_dtype, dqkv_dtype): 0 fp32, 1 bf16, 2 fp16.  The op page
+ * supports float16, bfloat16 and float32 activations; here one code,
+ * act_dtype, gives the dtype of all seven activation-like inputs (marked
+ * "act" below: those that are BF16 in the first stage, and its two caches).
+ *
  *   input       shape                                   dtype
- *   dout        reduce-O: [B,S,H,P]; per rank: [B,S,R,H,P]  bf16
- *   q, k        [B,S,R,G,N]                             bf16
- *   v           [B,S,H,P]                               bf16
+ *   dout        reduce-O: [B,S,H,P]; per rank: [B,S,R,H,P]  act
+ *   q, k        [B,S,R,G,N]                             act
+ *   v           [B,S,H,P]                               act
  *   q_bias, k_bias [H,R,N]                              fp32
  *   mimo_v      [H,R,P]                                 fp32
- *   states      [B,H,nchunks,N,P]                       bf16   (first stage's output)
- *   qk_dot      [B,H,S,R,R]                             bf16   (first stage's output)
+ *   states      [B,H,nchunks,N,P]                       act    (first stage's output)
+ *   qk_dot      [B,H,S,R,R]                             act    (first stage's output)
  *   da_cs, da_cs_rev, dt  [B,H,S]                       fp32
- *   trap        [B,H,S]                                 bf16
+ *   trap        [B,H,S]                                 act
  *   segsum      [B,H,nchunks,C,C]                       fp32
  *   angles      [B,S,H,RD]                              fp32
  *   mimo_o      [H,R,P] or NULL                         fp32   (NULL: dout per rank)
  *   d           [H] or NULL                             fp32
  *
  *   output (fp32; DQ, DK, DV in the dtype `dqkv_dtype` selects: the pages'
- *   output_dtype, whose default is the inputs' bf16)
+ *   output_dtype, whose default is the inputs' dtype)
  *   DQ, DK      [B,S*R,H,N]   per head (sum over a group's heads for q / k)
  *   DV          [B,S,H,P]
  *   DMIMO_V     [B,H,R,P]     per batch (sum over B for mimo_v)
@@ -64,7 +69,9 @@
  * rotary_dim_divisor in {2, 4}, N % rotary_dim_divisor == 0) and this
  * build's: N <= 64, P <= 64, C*R <= 64 (MMBF_ERR_UNSUPPORTED otherwise).
  *
- * Numerics: FP32 throughout (sums, the reverse scan); the tile products run
+ * Numerics: every input is widened to FP32 exactly; FP32 throughout (sums,
+ * the reverse scan); BF16 / FP16 outputs are the FP32 results rounded to
+ * nearest even.  The tile products run
  * on the tensor cores in TF32 with each FP32 operand split into two TF32
  * parts and three products per pair, which keeps FP32-level accuracy.
  * Results are deterministic (no floating-point atomics).
@@ -86,9 +93,10 @@ mmbf_status mamba_mimo_bwd_bwd_workspace_size(const mmbf_dims* dims, int64_t chu
 
 /* Enqueue the second backward stage on `stream` (a cudaStream_t; NULL for
  * the legacy default stream).  Inputs in the pages' positional order (dout
- * ... angles, mimo_o, d), then chunk_size, rotary_dim_divisor and
- * dqkv_dtype (0: DQ, DK, DV in fp32; 1: in bf16, rounded to nearest even),
- * then the 12 outputs in the pages' order, then the workspace.  Validation failures
+ * ... angles, mimo_o, d), then chunk_size, rotary_dim_divisor, act_dtype
+ * (the activations' dtype code) and dqkv_dtype (the dtype code of DQ, DK,
+ * DV; MMBF_ERR_ARG for a code outside 0..2), then the 12 outputs in the
+ * pages' order, then the workspace.  Validation failures
  * enqueue nothing and return an error (message in mamba_mimo_last_error);
  * MMBF_ERR_CUDA reports a launch error.  Asynchronous; calls sharing a
  * workspace must be ordered on one stream.  Four kernels: the per-chunk
@@ -102,7 +110,7 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
                                const float* da_cs, const float* da_cs_rev, const float* dt,
                                const void* trap, const float* segsum, const float* angles,
                                const float* mimo_o, const float* d, int64_t chunk_size,
-                               int64_t rotary_dim_divisor, int dqkv_dtype, void* DQ, void* DK,
+                               int64_t rotary_dim_divisor, int act_dtype, int dqkv_dtype, void* DQ, void* DK,
                                void* DV, float* DMIMO_V, float* DANGLES, float* DFACTOR, float* DGAMMA,
                                float* DDA, float* DSSDA, float* DDA_CS_REV, float* DDA_CS, float* DD,
                                void* workspace, size_t workspace_bytes, void* stream);

@@ -91,7 +91,7 @@ def load_library():
         lib.mamba_mimo_stage_name.argtypes = [ctypes.c_int]
         lib.mamba_mimo_bwd_bwd.restype = ctypes.c_int
         lib.mamba_mimo_bwd_bwd.argtypes = (
-            [ctypes.POINTER(_Dims)] + [vp] * 17 + [i64, i64, ctypes.c_int] + [vp] * 12 + [vp, ctypes.c_size_t, vp])
+            [ctypes.POINTER(_Dims)] + [vp] * 17 + [i64, i64, ctypes.c_int, ctypes.c_int] + [vp] * 12 + [vp, ctypes.c_size_t, vp])
         lib.mamba_mimo_bwd_bwd_workspace_size.restype = ctypes.c_int
         lib.mamba_mimo_bwd_bwd_workspace_size.argtypes = [
             ctypes.POINTER(_Dims), i64, i64, ctypes.POINTER(ctypes.c_size_t)]
@@ -323,6 +323,10 @@ def bwd_bwd_workspace_size(B, S, H, G, R, N, P, chunk_size=16, rotary_dim_diviso
     return nbytes.value
 
 
+# dtype codes of the second stage's C ABI (act_dtype, dqkv_dtype)
+_BB_DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+
 def mamba_mimo_bwd_bwd(dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt,
                        trap, segsum, angles, mimo_o=None, d=None, chunk_size: int = 16,
                        rotary_dim_divisor: int = 4, output_dtype=None, *,
@@ -331,15 +335,18 @@ def mamba_mimo_bwd_bwd(dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da
 
     Arguments in the pages' order (the first stage's ``states`` and
     ``qk_dot`` caches among them); ``mimo_o`` selects reduce-O ``dout``
-    ([B,S,H,P]), ``d`` adds the D-skip gradient.  ``output_dtype`` sets the
-    dtype of DQ, DK and DV (None: the inputs' bfloat16, as on the pages; or
-    torch.float32); the other nine gradients are FP32.  Returns a dict of
-    the 12 gradients (``DD`` is None without ``d``)."""
+    ([B,S,H,P]), ``d`` adds the D-skip gradient.  dout, q, k, v, states,
+    qk_dot and trap share one dtype (float16, bfloat16 or float32, as on the
+    pages); the other inputs are float32.  ``output_dtype`` sets the dtype
+    of DQ, DK and DV (None: the inputs' dtype, as on the pages); the other
+    nine gradients are FP32.  Returns a dict of the 12 gradients (``DD`` is
+    None without ``d``)."""
     if q.dim() != 5:
         raise ValueError("q must have shape [B, S, R, G, N]")
     B, S, R, G, N = q.shape
-    if q.dtype != torch.bfloat16:
-        raise TypeError("q, k, v, dout, states, qk_dot and trap must use torch.bfloat16")
+    if q.dtype not in _BB_DTYPE_CODES:
+        raise TypeError("q, k, v, dout, states, qk_dot and trap must use torch.float16, torch.bfloat16 "
+                        "or torch.float32")
     if q.device.type != "cuda":
         raise ValueError("mamba_mimo_bwd_bwd requires CUDA tensors")
     if rotary_dim_divisor not in (2, 4):
@@ -352,31 +359,31 @@ def mamba_mimo_bwd_bwd(dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da
     if H % G:
         raise ValueError("H must be divisible by G")
     dev = q.device
-    bf16, f32 = torch.bfloat16, torch.float32
+    act, f32 = q.dtype, torch.float32
     nc = (S + chunk_size - 1) // chunk_size
-    _check("k", k, q.shape, bf16, dev)
-    _check("v", v, (B, S, H, P), bf16, dev)
+    _check("k", k, q.shape, act, dev)
+    _check("v", v, (B, S, H, P), act, dev)
     _check("q_bias", q_bias, (H, R, N), f32, dev)
     _check("k_bias", k_bias, (H, R, N), f32, dev)
     _check("mimo_v", mimo_v, (H, R, P), f32, dev)
-    _check("states", states, (B, H, nc, N, P), bf16, dev)
-    _check("qk_dot", qk_dot, (B, H, S, R, R), bf16, dev)
+    _check("states", states, (B, H, nc, N, P), act, dev)
+    _check("qk_dot", qk_dot, (B, H, S, R, R), act, dev)
     for name, t in (("da_cs", da_cs), ("da_cs_rev", da_cs_rev), ("dt", dt)):
         _check(name, t, (B, H, S), f32, dev)
-    _check("trap", trap, (B, H, S), bf16, dev)
+    _check("trap", trap, (B, H, S), act, dev)
     _check("segsum", segsum, (B, H, nc, chunk_size, chunk_size), f32, dev)
     _check("angles", angles, (B, S, H, N // rotary_dim_divisor), f32, dev)
     if mimo_o is not None:
         _check("mimo_o", mimo_o, (H, R, P), f32, dev)
-        _check("dout", dout, (B, S, H, P), bf16, dev)
+        _check("dout", dout, (B, S, H, P), act, dev)
     else:
-        _check("dout", dout, (B, S, R, H, P), bf16, dev)
+        _check("dout", dout, (B, S, R, H, P), act, dev)
     if d is not None:
         _check("d", d, (H,), f32, dev)
     if output_dtype is None:
         output_dtype = q.dtype
-    if output_dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("output_dtype must be None, torch.bfloat16 or torch.float32")
+    if output_dtype not in _BB_DTYPE_CODES:
+        raise TypeError("output_dtype must be None, torch.float16, torch.bfloat16 or torch.float32")
     args = tuple(None if a is None else a.contiguous() for a in (
         dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt, trap, segsum,
         angles, mimo_o, d))
@@ -402,7 +409,7 @@ def mamba_mimo_bwd_bwd(dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da
     with torch.cuda.device(dev):
         st = lib.mamba_mimo_bwd_bwd(
             ctypes.byref(_Dims(B, S, H, G, R, N, P)), *[_ptr(a) for a in args], chunk_size,
-            rotary_dim_divisor, int(output_dtype == torch.bfloat16),
+            rotary_dim_divisor, _BB_DTYPE_CODES[act], _BB_DTYPE_CODES[output_dtype],
             *[_ptr(outs[n]) for n in BWD_BWD_OUTPUTS], _ptr(workspace),
             workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream))
     if st:

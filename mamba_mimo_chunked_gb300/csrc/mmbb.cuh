@@ -22,6 +22,8 @@
 //                               chunk order.
 // FP32-level accuracy throughout, deterministic (no floating-point atomics).
 
+#include <cuda_fp16.h>
+
 #include "mamba_mimo_bwd_bwd.h"
 
 namespace mmbf {
@@ -29,10 +31,11 @@ namespace bb {
 
 struct BBParams {
   int B, S, H, G, R, N, P, C, w, nc, CR, reduced, has_d;
-  int dqkv_bf16;  // DQ, DK, DV stored as BF16 (else FP32)
-  const uint16_t *dout, *q, *k, *v, *states, *qk, *trap;
+  int act;   // dtype of dout, q, k, v, states, qk_dot, trap: kF32, kBF16 or kF16
+  int dqkv;  // dtype of DQ, DK, DV (same codes)
+  const void *dout, *q, *k, *v, *states, *qk, *trap;
   const float *q_bias, *k_bias, *mimo_v, *mimo_o, *d, *da_cs, *da_cs_rev, *dt, *segsum, *angles;
-  void *DQ, *DK, *DV;  // FP32 or BF16 (dqkv_bf16)
+  void *DQ, *DK, *DV;  // in the dtype dqkv selects
   float *DMIMO_V, *DANGLES, *DFACTOR, *DGAMMA, *DDA, *DSSDA, *DDA_CS_REV, *DDA_CS, *DD;
   float* ws_D;      // [BH][nc][N][P]: seeds G_c, then D_{c+1}
   float* ws_alpha;  // [BH][nc]
@@ -48,12 +51,25 @@ constexpr int kTile = kMax * kLD;   // floats per tile
 constexpr int kSmall = 4224;        // segsum [C][C], qk [C][R][R], dqk (C*R <= 64, R <= 16)
 constexpr int kRedCols = 16;        // per-row partial sums, one per column block
 
+// dtype codes of the ABI (dqkv_dtype / act_dtype)
+constexpr int kF32 = 0, kBF16 = 1, kF16 = 2;
+
 __device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
-// Element i of DQ / DK / DV in the requested dtype (FP32, or BF16 rounded to
-// nearest even).
-__device__ __forceinline__ void store_dqkv(void* base, int64_t i, float x, int bf16) {
-  if (bf16)
+// Element i of an activation tensor of dtype code A, widened to FP32 (exact
+// for all three).  The kernels that read activations are instantiated per A.
+template <int A>
+__device__ __forceinline__ float ld_act(const void* base, int64_t i) {
+  if constexpr (A == kBF16) return bf_f(static_cast<const uint16_t*>(base)[i]);
+  else if constexpr (A == kF16) return __half2float(static_cast<const __half*>(base)[i]);
+  else return static_cast<const float*>(base)[i];
+}
+// Element i of DQ / DK / DV in the requested dtype (FP32, or BF16 / FP16
+// rounded to nearest even).
+__device__ __forceinline__ void store_dqkv(void* base, int64_t i, float x, int dt) {
+  if (dt == kBF16)
     static_cast<uint16_t*>(base)[i] = f_bf(x);
+  else if (dt == kF16)
+    static_cast<__half*>(base)[i] = __float2half_rn(x);
   else
     static_cast<float*>(base)[i] = x;
 }
@@ -156,14 +172,15 @@ __device__ __forceinline__ void zero4(float (&acc)[TM][TN]) {
 
 // Token scalars of chunk c (reading of the op header): gamma, factor,
 // exp(da_cs), exp(da_cs_rev), and whether the token is inside S.
+template <int A>
 __device__ void load_tokens(const BBParams& p, int bh, int c, float* gam, float* fac, float* ea, float* er,
                             float* valid) {
   for (int t = threadIdx.x; t < p.C; t += blockDim.x) {
     const int tg = c * p.C + t;
     const int64_t i = (int64_t)bh * p.S + tg;
     const bool in = tg < p.S, in1 = tg + 1 < p.S;
-    const float dtv = in ? p.dt[i] : 0.f, trv = in ? bf_f(p.trap[i]) : 0.f;
-    const float dtn = in1 ? p.dt[i + 1] : 0.f, trn = in1 ? bf_f(p.trap[i + 1]) : 0.f;
+    const float dtv = in ? p.dt[i] : 0.f, trv = in ? ld_act<A>(p.trap, i) : 0.f;
+    const float dtn = in1 ? p.dt[i + 1] : 0.f, trn = in1 ? ld_act<A>(p.trap, i + 1) : 0.f;
     const float g = dtv * sigm(trv);
     gam[t] = g;
     fac[t] = g + dtn * sigm(-trn);  // 0 shifted part past S and at the last padded position
@@ -176,13 +193,14 @@ __device__ void load_tokens(const BBParams& p, int bh, int c, float* gam, float*
 // Biased rows of q (or k) of chunk c, then the rotary on the pairs (m, N/2+m),
 // m < w, in place: rows j = t*R + r of a [C*R][N] tile (zero input past S,
 // plus the bias, as the padded reference).
-__device__ void load_rotated(const BBParams& p, int b, int h, int c, const uint16_t* src, const float* bias,
+template <int A>
+__device__ void load_rotated(const BBParams& p, int b, int h, int c, const void* src, const float* bias,
                              float* T) {
   const int g = h / (p.H / p.G);
   for (int e = threadIdx.x; e < p.CR * p.N; e += blockDim.x) {
     const int j = e / p.N, n = e % p.N, t = j / p.R, r = j % p.R, tg = c * p.C + t;
     float x = bias[((int64_t)h * p.R + r) * p.N + n];
-    if (tg < p.S) x += bf_f(src[((((int64_t)b * p.S + tg) * p.R + r) * p.G + g) * p.N + n]);
+    if (tg < p.S) x += ld_act<A>(src, ((((int64_t)b * p.S + tg) * p.R + r) * p.G + g) * p.N + n);
     T[j * kLD + n] = x;
   }
   __syncthreads();
@@ -199,32 +217,35 @@ __device__ void load_rotated(const BBParams& p, int b, int h, int c, const uint1
 }
 
 // dPhiO rows [C*R][P] (zero past S) [op document: reduce-O or per rank].
+template <int A>
 __device__ void load_dphio(const BBParams& p, int b, int h, int c, float* T) {
   for (int e = threadIdx.x; e < p.CR * p.P; e += blockDim.x) {
     const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
     float x = 0.f;
     if (tg < p.S) {
       if (p.reduced)
-        x = bf_f(p.dout[(((int64_t)b * p.S + tg) * p.H + h) * p.P + pp]) * p.mimo_o[((int64_t)h * p.R + r) * p.P + pp];
+        x = ld_act<A>(p.dout, (((int64_t)b * p.S + tg) * p.H + h) * p.P + pp) * p.mimo_o[((int64_t)h * p.R + r) * p.P + pp];
       else
-        x = bf_f(p.dout[((((int64_t)b * p.S + tg) * p.R + r) * p.H + h) * p.P + pp]);
+        x = ld_act<A>(p.dout, ((((int64_t)b * p.S + tg) * p.R + r) * p.H + h) * p.P + pp);
     }
     T[j * kLD + pp] = x;
   }
 }
 
 // PsiV rows [C*R][P] = v[t,p] * mimo_v[r,p] (zero past S).
+template <int A>
 __device__ void load_psi(const BBParams& p, int b, int h, int c, float* T) {
   for (int e = threadIdx.x; e < p.CR * p.P; e += blockDim.x) {
     const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
     float x = 0.f;
     if (tg < p.S)
-      x = bf_f(p.v[(((int64_t)b * p.S + tg) * p.H + h) * p.P + pp]) * p.mimo_v[((int64_t)h * p.R + r) * p.P + pp];
+      x = ld_act<A>(p.v, (((int64_t)b * p.S + tg) * p.H + h) * p.P + pp) * p.mimo_v[((int64_t)h * p.R + r) * p.P + pp];
     T[j * kLD + pp] = x;
   }
 }
 
 // ---- 1. seeds: G_c[n][p] = sum_i exp(da_cs[t_i]) q_rot[i][n] dPhiO[i][p]
+template <int A>
 __global__ void __launch_bounds__(kT, 2) seed_kernel(const BBParams p) {
   extern __shared__ float smf[];
   float* Qr = smf;
@@ -232,9 +253,9 @@ __global__ void __launch_bounds__(kT, 2) seed_kernel(const BBParams p) {
   float* tk = Gp + kTile;  // gam, fac, ea, er, valid: 5 x kMax
   float* ear = tk + 5 * kMax;  // exp(da_cs) per row j = t*R + r
   const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  load_tokens(p, bh, c, tk, tk + kMax, tk + 2 * kMax, tk + 3 * kMax, tk + 4 * kMax);
-  load_dphio(p, b, h, c, Gp);
-  load_rotated(p, b, h, c, p.q, p.q_bias, Qr);
+  load_tokens<A>(p, bh, c, tk, tk + kMax, tk + 2 * kMax, tk + 3 * kMax, tk + 4 * kMax);
+  load_dphio<A>(p, b, h, c, Gp);
+  load_rotated<A>(p, b, h, c, p.q, p.q_bias, Qr);
   __syncthreads();
   const float* ea = tk + 2 * kMax;
   for (int j = threadIdx.x; j < p.CR; j += blockDim.x) ear[j] = ea[j / p.R];
@@ -286,6 +307,7 @@ __global__ void __launch_bounds__(128) scan_kernel(const BBParams p) {
 }
 
 // ---- 3. every gradient of one chunk
+template <int A>
 __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   extern __shared__ float smf[];
   float* Qr = smf;              // rotated q rows
@@ -322,20 +344,20 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   const int fr0 = (wid >> 2) * 16, fc0 = (wid & 3) * 16, wc = wid & 3;  // this warp's 16 x 16 tile
 
   // ---- inputs of the chunk
-  load_tokens(p, bh, c, gam, fac, ea, er, valid);
+  load_tokens<A>(p, bh, c, gam, fac, ea, er, valid);
   for (int e = tid; e < C * C; e += kTG) seg[e] = p.segsum[((int64_t)bh * p.nc + c) * C * C + e];
   for (int e = tid; e < C * R * R; e += kTG) {
     const int tg = c * C + e / (R * R);
-    qk[e] = tg < p.S ? bf_f(p.qk[((int64_t)bh * p.S + tg) * R * R + e % (R * R)]) : 0.f;
+    qk[e] = tg < p.S ? ld_act<A>(p.qk, ((int64_t)bh * p.S + tg) * R * R + e % (R * R)) : 0.f;
   }
   for (int e = tid; e < N * P; e += kTG) {
-    Hc[(e / P) * kLD + e % P] = bf_f(p.states[((int64_t)bh * p.nc + c) * N * P + e]);
+    Hc[(e / P) * kLD + e % P] = ld_act<A>(p.states, ((int64_t)bh * p.nc + c) * N * P + e);
     Dn[(e / P) * kLD + e % P] = p.ws_D[((int64_t)bh * p.nc + c) * N * P + e];
   }
-  load_psi(p, b, h, c, Ps);
-  load_dphio(p, b, h, c, Gp);
-  load_rotated(p, b, h, c, p.q, p.q_bias, Qr);
-  load_rotated(p, b, h, c, p.k, p.k_bias, Kr);
+  load_psi<A>(p, b, h, c, Ps);
+  load_dphio<A>(p, b, h, c, Gp);
+  load_rotated<A>(p, b, h, c, p.q, p.q_bias, Qr);
+  load_rotated<A>(p, b, h, c, p.k, p.k_bias, Kr);
   __syncthreads();
   for (int j = tid; j < CR; j += kTG) {
     facr[j] = fac[j / R];
@@ -535,7 +557,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   for (int e = tid; e < R * P; e += kTG) mvs[e] = p.mimo_v[(int64_t)h * R * P + e];
   for (int e = tid; e < C * P; e += kTG) {
     const int t = e / P, pp = e % P, tg = c * C + t;
-    vs[e] = tg < p.S ? bf_f(p.v[(((int64_t)b * p.S + tg) * p.H + h) * P + pp]) : 0.f;
+    vs[e] = tg < p.S ? ld_act<A>(p.v, (((int64_t)b * p.S + tg) * p.H + h) * P + pp) : 0.f;
   }
   for (int e = tid; e < C * W; e += kTG) {
     const int t = e / W, m = e % W, tg = c * C + t;
@@ -567,7 +589,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
     if (tg >= p.S) continue;
     float s = 0.f;
     for (int r = 0; r < R; r++) s = fmaf(dP[(t * R + r) * kLD + pp], mvs[r * P + pp], s);
-    store_dqkv(p.DV, (((int64_t)b * p.S + tg) * p.H + h) * P + pp, s, p.dqkv_bf16);
+    store_dqkv(p.DV, (((int64_t)b * p.S + tg) * p.H + h) * P + pp, s, p.dqkv);
   }
   for (int e = tid; e < R * P; e += kTG) {
     const int r = e / P, pp = e % P;
@@ -595,8 +617,8 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
       dk = fmaf(dqk[(t * R + x) * R + r], Qr[(t * R + x) * kLD + n], dk);  // row (t, r) of k
     }
     const int64_t o = (((int64_t)b * p.S + tg) * R + r) * p.H + h;
-    store_dqkv(p.DQ, o * N + n, dq, p.dqkv_bf16);
-    store_dqkv(p.DK, o * N + n, dk, p.dqkv_bf16);
+    store_dqkv(p.DQ, o * N + n, dq, p.dqkv);
+    store_dqkv(p.DK, o * N + n, dk, p.dqkv);
   }
 }
 
@@ -654,6 +676,36 @@ static mmbf_status bb_plan(const mmbf_dims* dims, int64_t chunk_size, int64_t di
   return MMBF_OK;
 }
 
+// The four launches of one call for activation dtype A (the kernels' shared
+// memory limits are raised once per instantiation).
+template <int A>
+cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
+  static bool smem_set = false;
+  if (!smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(seed_kernel<A>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeedSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grad_kernel<A>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
+    if (e != cudaSuccess) return e;
+    smem_set = true;
+  }
+  const int BH = p.B * p.H;
+  g_stage_names = kBBStageNames;
+  g_stage_names_n = 4;
+  stage_event(0, 0, st);
+  seed_kernel<A><<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
+  stage_event(0, 1, st);
+  stage_event(1, 0, st);
+  scan_kernel<<<dim3((p.N * p.P + 127) / 128, BH), 128, 0, st>>>(p);
+  stage_event(1, 1, st);
+  stage_event(2, 0, st);
+  grad_kernel<A><<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
+  stage_event(2, 1, st);
+  stage_event(3, 0, st);
+  reduce_kernel<<<BH, kT, 0, st>>>(p);
+  stage_event(3, 1, st);
+  return cudaSuccess;
+}
+
 }  // namespace bb
 }  // namespace mmbf
 
@@ -675,7 +727,7 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
                                const float* q_bias, const float* k_bias, const float* mimo_v, const void* states,
                                const void* qk_dot, const float* da_cs, const float* da_cs_rev, const float* dt,
                                const void* trap, const float* segsum, const float* angles, const float* mimo_o,
-                               const float* d, int64_t chunk_size, int64_t rotary_dim_divisor, int dqkv_dtype,
+                               const float* d, int64_t chunk_size, int64_t rotary_dim_divisor, int act_dtype, int dqkv_dtype,
                                void* DQ, void* DK, void* DV, float* DMIMO_V, float* DANGLES, float* DFACTOR, float* DGAMMA, float* DDA,
                                float* DSSDA, float* DDA_CS_REV, float* DDA_CS, float* DD, void* workspace,
                                size_t workspace_bytes, void* stream) {
@@ -688,7 +740,9 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
   for (const void* x : req)
     if (!x) return fail(MMBF_ERR_ARG, "a required pointer is NULL");
   if ((d == nullptr) != (DD == nullptr)) return fail(MMBF_ERR_ARG, "DD must be given exactly when d is");
-  if (dqkv_dtype != 0 && dqkv_dtype != 1) return fail(MMBF_ERR_ARG, "dqkv_dtype must be 0 (fp32) or 1 (bf16)");
+  if (act_dtype < kF32 || act_dtype > kF16) return fail(MMBF_ERR_ARG, "act_dtype must be 0 (fp32), 1 (bf16) or 2 (fp16)");
+  if (dqkv_dtype < kF32 || dqkv_dtype > kF16)
+    return fail(MMBF_ERR_ARG, "dqkv_dtype must be 0 (fp32), 1 (bf16) or 2 (fp16)");
   const void* all[] = {dout, q, k, v, q_bias, k_bias, mimo_v, states, qk_dot, da_cs, da_cs_rev, dt, trap, segsum,
                        angles, mimo_o, d, DQ, DK, DV, DMIMO_V, DANGLES, DFACTOR, DGAMMA, DDA, DSSDA, DDA_CS_REV, DDA_CS, DD};
   for (const void* x : all)
@@ -699,57 +753,26 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
     return fail(MMBF_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need, workspace_bytes);
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(MMBF_ERR_ALIGN, "workspace must be 256-byte aligned");
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  p.dout = static_cast<const uint16_t*>(dout);
-  p.q = static_cast<const uint16_t*>(q);
-  p.k = static_cast<const uint16_t*>(k);
-  p.v = static_cast<const uint16_t*>(v);
-  p.states = static_cast<const uint16_t*>(states);
-  p.qk = static_cast<const uint16_t*>(qk_dot);
-  p.trap = static_cast<const uint16_t*>(trap);
+  p.dout = dout; p.q = q; p.k = k; p.v = v; p.states = states; p.qk = qk_dot; p.trap = trap;
+  p.act = act_dtype;
   p.q_bias = q_bias; p.k_bias = k_bias; p.mimo_v = mimo_v; p.mimo_o = mimo_o; p.d = d;
   p.da_cs = da_cs; p.da_cs_rev = da_cs_rev; p.dt = dt; p.segsum = segsum; p.angles = angles;
   p.reduced = mimo_o != nullptr;
   p.has_d = d != nullptr;
   p.DQ = DQ; p.DK = DK; p.DV = DV;
-  p.dqkv_bf16 = dqkv_dtype; p.DMIMO_V = DMIMO_V; p.DANGLES = DANGLES; p.DFACTOR = DFACTOR;
+  p.dqkv = dqkv_dtype; p.DMIMO_V = DMIMO_V; p.DANGLES = DANGLES; p.DFACTOR = DFACTOR;
   p.DGAMMA = DGAMMA; p.DDA = DDA; p.DSSDA = DSSDA; p.DDA_CS_REV = DDA_CS_REV; p.DDA_CS = DDA_CS; p.DD = DD;
   p.ws_D = reinterpret_cast<float*>(ws + off[0]);
   p.ws_alpha = reinterpret_cast<float*>(ws + off[1]);
   p.ws_mv = reinterpret_cast<float*>(ws + off[2]);
   p.ws_dd = reinterpret_cast<float*>(ws + off[3]);
 
-  static int smem_set = 0;
-  cudaError_t e = cudaSuccess;
-  if (!smem_set) {
-    e = cudaFuncSetAttribute(seed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeedSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
-    if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "shared-memory attribute: %s", cudaGetErrorString(e));
-    smem_set = 1;
-  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int BH = p.B * p.H;
-  int launches = 0;
-  g_stage_names = kBBStageNames;
-  g_stage_names_n = 4;
-  stage_event(0, 0, st);
-  seed_kernel<<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
-  stage_event(0, 1, st);
-  launches++;
-  stage_event(1, 0, st);
-  scan_kernel<<<dim3((p.N * p.P + 127) / 128, BH), 128, 0, st>>>(p);
-  stage_event(1, 1, st);
-  launches++;
-  stage_event(2, 0, st);
-  grad_kernel<<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
-  stage_event(2, 1, st);
-  launches++;
-  stage_event(3, 0, st);
-  reduce_kernel<<<BH, kT, 0, st>>>(p);
-  stage_event(3, 1, st);
-  launches++;
+  cudaError_t e = p.act == kBF16 ? launch_bb<kBF16>(p, st) : p.act == kF16 ? launch_bb<kF16>(p, st)
+                                                                           : launch_bb<kF32>(p, st);
+  if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "shared-memory attribute: %s", cudaGetErrorString(e));
   e = cudaGetLastError();
-  g_launches = launches;
+  g_launches = 4;
   if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "launching the second stage: %s", cudaGetErrorString(e));
   return MMBF_OK;
 }

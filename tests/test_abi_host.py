@@ -170,8 +170,8 @@ def test_bwd_bwd_rejects_bad_pointer_patterns_without_gpu(lib):
     d = dims(S=64, H=2, R=2, N=16, P=16)
     fake = ctypes.c_void_p(0x1000)
 
-    def call(ins, outs, ws_bytes=1 << 30, ws_ptr=fake, dtype=0):
-        return lib.mamba_mimo_bwd_bwd(ctypes.byref(d), *ins, 16, 4, dtype, *outs, ws_ptr, ws_bytes, None)
+    def call(ins, outs, ws_bytes=1 << 30, ws_ptr=fake, dtype=0, act=1):
+        return lib.mamba_mimo_bwd_bwd(ctypes.byref(d), *ins, 16, 4, act, dtype, *outs, ws_ptr, ws_bytes, None)
 
     ins = [fake] * 17
     outs = [fake] * 12
@@ -191,4 +191,5 @@ def test_bwd_bwd_rejects_bad_pointer_patterns_without_gpu(lib):
     assert call(ins, outs, ws_bytes=16) == 5
     assert call(ins, outs, ws_ptr=ctypes.c_void_p(0x1010)) == 4
     # an unknown DQ / DK / DV dtype
-    assert call(ins, outs, dtype=2) == 2 and "dqkv_dtype" in lib.mamba_mimo_last_error().decode()
+    assert call(ins, outs, dtype=3) == 2 and "dqkv_dtype" in lib.mamba_mimo_last_error().decode()
+    assert call(ins, outs, act=-1) == 2 and "act_dtype" in lib.mamba_mimo_last_error().decode()

@@ -8,8 +8,9 @@ output is held to a relative RMS error below 1e-4; DDA and DANGLES, whose
 entries can sit near zero, also to a max-abs error below 1e-3 of their
 largest entry (the pages' global relative criterion for those two).  Those
 checks take DQ, DK and DV in FP32 (output_dtype=torch.float32); with the
-default BF16 outputs the three must equal the FP32 results rounded to
-nearest even.
+default outputs (the inputs' dtype) the three must equal the FP32 results
+rounded to nearest even.  FP16 and FP32 activations (dout, q, k, v, the
+caches, trap) are checked the same way: both sides read the same values.
 """
 
 import numpy as np
@@ -26,9 +27,15 @@ KEYS = ("dout", "q", "k", "v", "q_bias", "k_bias", "mimo_v", "mimo_o", "d", "da_
         "trap", "segsum", "angles")
 
 
-def _problem(B, S, H, G, R, N, P, C, div=4, reduced=True, has_d=True, seed=0, caches="forward"):
+ACT = ("dout", "q", "k", "v", "trap")  # with the two caches: the activation-dtype inputs
+
+
+def _problem(B, S, H, G, R, N, P, C, div=4, reduced=True, has_d=True, seed=0, caches="forward",
+             act=torch.bfloat16):
     inp = si.make_inputs(B=B, S=S, H=H, G=G, R=R, N=N, P=P, C=C, div=div, reduced=reduced, has_z=False,
                          has_d=has_d, seed=seed, recipe="workload")
+    for name in ACT:  # BF16 values, stored in the requested dtype (exact for FP32)
+        inp[name] = inp[name].to(act)
     if caches == "forward":  # the caches a forward pass leaves (float64, stored as BF16)
         a = {k: bb._f64(inp[k]) for k in KEYS}
         nc = (S + C - 1) // C
@@ -38,10 +45,11 @@ def _problem(B, S, H, G, R, N, P, C, div=4, reduced=True, has_d=True, seed=0, ca
             for h in range(H):
                 _, s_, q_, _ = bb.forward(a, b, h, C, div)
                 st[b, h], qk[b, h] = s_, q_[:S]
-        states = torch.from_numpy(st).to(torch.bfloat16)
-        qk_dot = torch.from_numpy(qk).to(torch.bfloat16)
+        states = torch.from_numpy(st).to(act)
+        qk_dot = torch.from_numpy(qk).to(act)
     else:
         states, qk_dot = si.make_stage1_caches(B=B, S=S, H=H, R=R, N=N, P=P, C=C, seed=seed + 1)
+        states, qk_dot = states.to(act), qk_dot.to(act)
     args = (inp["dout"], inp["q"], inp["k"], inp["v"], inp["q_bias"], inp["k_bias"], inp["mimo_v"], states,
             qk_dot, inp["da_cs"], inp["da_cs_rev"], inp["dt"], inp["trap"], inp["segsum"], inp["angles"])
     kw = dict(mimo_o=inp["mimo_o"], d=inp["d"], chunk_size=C, rotary_dim_divisor=div)
@@ -91,6 +99,14 @@ def test_parity_with_forward_caches(case):
     _compare(_run_gpu(args, kw), want)
 
 
+@pytest.mark.parametrize("act", [torch.float16, torch.float32], ids=["f16", "f32"])
+@pytest.mark.parametrize("case", [CASES[0], CASES[1], CASES[5]], ids=["S40_R4", "S33_R2", "GQA"])
+def test_parity_other_activation_dtypes(case, act):
+    args, kw = _problem(**case, seed=29, act=act)
+    want = bb.bwd_bwd(*args, **kw)
+    _compare(_run_gpu(args, kw), want)
+
+
 def test_parity_timed_shape_all_heads():
     # B1 S8192 H16 R4 N=P=64 C16: given caches (seeded stand-ins); every head
     args, kw = _problem(B=1, S=8192, H=16, G=1, R=4, N=64, P=64, C=16, seed=5, caches="random")
@@ -107,25 +123,30 @@ def test_deterministic_and_four_launches():
         assert torch.equal(g1[name], g2[name]), name
 
 
+@pytest.mark.parametrize("act,out", [(torch.bfloat16, None), (torch.float16, None), (torch.bfloat16, torch.float16),
+                                     (torch.float32, torch.bfloat16)], ids=["bf16", "f16", "bf16_to_f16", "f32_to_bf16"])
 @pytest.mark.parametrize("case", [CASES[0], CASES[1]], ids=["S40_R4", "S33_R2"])
-def test_default_bf16_dq_dk_dv_are_the_rounded_fp32_results(case):
-    args, kw = _problem(**case, seed=23)
+def test_lower_precision_dq_dk_dv_are_the_rounded_fp32_results(case, act, out):
+    args, kw = _problem(**case, seed=23, act=act)
     g32 = _run_gpu(args, kw)
-    g16 = _run_gpu(args, kw, output_dtype=None)
+    g16 = _run_gpu(args, kw, output_dtype=out)
+    want_dt = act if out is None else out
     for name in bb.OUTPUT_NAMES:
         if g32[name] is None:
             assert g16[name] is None
         elif name in ("DQ", "DK", "DV"):
-            assert g16[name].dtype == torch.bfloat16, name
-            assert torch.equal(g16[name], g32[name].to(torch.bfloat16)), name
+            assert g16[name].dtype == want_dt, name
+            assert torch.equal(g16[name], g32[name].to(want_dt)), name
         else:
             assert g16[name].dtype == torch.float32 and torch.equal(g16[name], g32[name]), name
-    # and against the oracle, within BF16's rounding (at most 2^-9 relative per entry)
+    # and against the oracle, within the output's rounding: at most 2^-8
+    # relative per entry for BF16 (8 significant bits), 2^-11 for FP16 (11
+    # bits, normal range; below it the absolute step is 2^-24)
     want = bb.bwd_bwd(*args, **kw)
     for name in ("DQ", "DK", "DV"):
         g = g16[name].double().cpu().numpy()
         err = np.sqrt(np.mean((g - want[name]) ** 2)) / np.sqrt(np.mean(want[name] ** 2))
-        assert err < 2.0 ** -9, f"{name}: relative RMS {err:.3e}"
+        assert err < (2.0 ** -8 if want_dt == torch.bfloat16 else 2.0 ** -11), f"{name}: relative RMS {err:.3e}"
 
 
 def test_outside_the_envelope_raises():
