@@ -310,7 +310,7 @@ def run_bwd_bwd(args, world, rank, local):
     torch.cuda.set_device(dev)
     mm.build()
     lib = mm.load_library()
-    wl = si.WORKLOADS[WORKLOAD_INDEX]
+    wl = si.WORKLOADS[WORKLOAD_INDEX if args.workload is None else args.workload]
     stream = torch.cuda.current_stream(dev)
     steps = args.steps if args.steps != 20000 else 300   # the default count is the first stage's
     nsets = 2                                            # each set ~0.45 GB, over the L2

@@ -67,7 +67,11 @@
  *
  * Envelope (checked): the pages' constraints (B..P >= 1, H % G == 0, N even,
  * rotary_dim_divisor in {2, 4}, N % rotary_dim_divisor == 0) and this
- * build's: N <= 64, P <= 64, C*R <= 64 (MMBF_ERR_UNSUPPORTED otherwise).
+ * build's: N <= 256, P <= 128, C*R <= 128, R <= 16 (MMBF_ERR_UNSUPPORTED
+ * otherwise).  Shapes with N, P and C*R all <= 64 run the gradient kernel
+ * with its tiles in shared memory, one chunk per CTA; larger ones run a
+ * persistent kernel (152 CTAs) whose tiles sit in a per-CTA part of the
+ * workspace, which the size query then includes.
  *
  * Numerics: every input is widened to FP32 exactly; FP32 throughout (sums,
  * the reverse scan); BF16 / FP16 outputs are the FP32 results rounded to

@@ -41,6 +41,12 @@ struct BBParams {
   float* ws_alpha;  // [BH][nc]
   float* ws_mv;     // [BH][nc][R][P]: DMIMO_V partials
   float* ws_dd;     // [BH][nc]: DD partials
+  // wide path (N, P or C*R above 64): tiles in a per-CTA FP32 scratch
+  int wide;
+  int LN, LP, LC, CR16, N16;  // tile strides (extents rounded up to 16) and padded row counts
+  int sLN, sLP;               // seed kernel strides (N, P rounded up to 64)
+  int64_t m1sz, m2sz, scr_floats;
+  float* ws_scr;              // [grid][scr_floats]
 };
 
 constexpr int kT = 256;             // threads per CTA (seed kernel: 4 x 4 blocks of a 64 x 64 product)
@@ -49,6 +55,9 @@ constexpr int kMax = 64;            // N, P and C*R limit of this path
 constexpr int kLD = kMax + 4;       // FP32 tile row stride: 4 (mod 32) puts the 32 lanes of every m16n8k8 fragment load on distinct banks
 constexpr int kTile = kMax * kLD;   // floats per tile
 constexpr int kSmall = 4224;        // segsum [C][C], qk [C][R][R], dqk (C*R <= 64, R <= 16)
+constexpr int kMaxW = 128;          // wide path: C*R and P limit (N up to 2 * kMaxW)
+constexpr int kSmallW = 16640;      // segsum, qk, dqk for C*R <= 128, R <= 16
+constexpr int kWideGrid = 152;      // persistent CTAs of the wide gradient kernel
 constexpr int kRedCols = 16;        // per-row partial sums, one per column block
 
 // dtype codes of the ABI (dqkv_dtype / act_dtype)
@@ -173,7 +182,7 @@ __device__ __forceinline__ void zero4(float (&acc)[TM][TN]) {
 // Token scalars of chunk c (reading of the op header): gamma, factor,
 // exp(da_cs), exp(da_cs_rev), and whether the token is inside S.
 template <int A>
-__device__ void load_tokens(const BBParams& p, int bh, int c, float* gam, float* fac, float* ea, float* er,
+__device__ __forceinline__ void load_tokens(const BBParams& p, int bh, int c, float* gam, float* fac, float* ea, float* er,
                             float* valid) {
   for (int t = threadIdx.x; t < p.C; t += blockDim.x) {
     const int tg = c * p.C + t;
@@ -194,14 +203,14 @@ __device__ void load_tokens(const BBParams& p, int bh, int c, float* gam, float*
 // m < w, in place: rows j = t*R + r of a [C*R][N] tile (zero input past S,
 // plus the bias, as the padded reference).
 template <int A>
-__device__ void load_rotated(const BBParams& p, int b, int h, int c, const void* src, const float* bias,
-                             float* T) {
+__device__ __forceinline__ void load_rotated(const BBParams& p, int b, int h, int c, const void* src, const float* bias,
+                             float* T, int ld) {
   const int g = h / (p.H / p.G);
   for (int e = threadIdx.x; e < p.CR * p.N; e += blockDim.x) {
     const int j = e / p.N, n = e % p.N, t = j / p.R, r = j % p.R, tg = c * p.C + t;
     float x = bias[((int64_t)h * p.R + r) * p.N + n];
     if (tg < p.S) x += ld_act<A>(src, ((((int64_t)b * p.S + tg) * p.R + r) * p.G + g) * p.N + n);
-    T[j * kLD + n] = x;
+    T[j * ld + n] = x;
   }
   __syncthreads();
   const int half = p.N / 2;
@@ -210,15 +219,15 @@ __device__ void load_rotated(const BBParams& p, int b, int h, int c, const void*
     const float th = tg < p.S ? p.angles[(((int64_t)b * p.S + tg) * p.H + h) * p.w + m] : 0.f;
     float sn, cs;
     sincosf(th, &sn, &cs);
-    const float lo = T[j * kLD + m], hi = T[j * kLD + half + m];
-    T[j * kLD + m] = cs * lo - sn * hi;
-    T[j * kLD + half + m] = sn * lo + cs * hi;
+    const float lo = T[j * ld + m], hi = T[j * ld + half + m];
+    T[j * ld + m] = cs * lo - sn * hi;
+    T[j * ld + half + m] = sn * lo + cs * hi;
   }
 }
 
 // dPhiO rows [C*R][P] (zero past S) [op document: reduce-O or per rank].
 template <int A>
-__device__ void load_dphio(const BBParams& p, int b, int h, int c, float* T) {
+__device__ __forceinline__ void load_dphio(const BBParams& p, int b, int h, int c, float* T, int ld) {
   for (int e = threadIdx.x; e < p.CR * p.P; e += blockDim.x) {
     const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
     float x = 0.f;
@@ -228,49 +237,61 @@ __device__ void load_dphio(const BBParams& p, int b, int h, int c, float* T) {
       else
         x = ld_act<A>(p.dout, ((((int64_t)b * p.S + tg) * p.R + r) * p.H + h) * p.P + pp);
     }
-    T[j * kLD + pp] = x;
+    T[j * ld + pp] = x;
   }
 }
 
 // PsiV rows [C*R][P] = v[t,p] * mimo_v[r,p] (zero past S).
 template <int A>
-__device__ void load_psi(const BBParams& p, int b, int h, int c, float* T) {
+__device__ __forceinline__ void load_psi(const BBParams& p, int b, int h, int c, float* T, int ld) {
   for (int e = threadIdx.x; e < p.CR * p.P; e += blockDim.x) {
     const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
     float x = 0.f;
     if (tg < p.S)
       x = ld_act<A>(p.v, (((int64_t)b * p.S + tg) * p.H + h) * p.P + pp) * p.mimo_v[((int64_t)h * p.R + r) * p.P + pp];
-    T[j * kLD + pp] = x;
+    T[j * ld + pp] = x;
   }
 }
 
 // ---- 1. seeds: G_c[n][p] = sum_i exp(da_cs[t_i]) q_rot[i][n] dPhiO[i][p]
-template <int A>
-__global__ void __launch_bounds__(kT, 2) seed_kernel(const BBParams p) {
+// The 64-wide path (W = false) keeps [64][kLD] tiles and one 64 x 64 output
+// block; the wide path strides its rows by N and P rounded up to 64 (every
+// 4 x 4 read of a block stays inside its row) and walks the output blocks.
+template <int A, bool W>
+__global__ void __launch_bounds__(kT, W ? 1 : 4) seed_kernel(const BBParams p) {  // 64-wide: 4 CTAs per SM
   extern __shared__ float smf[];
+  const int LN = W ? p.sLN : kLD, LP = W ? p.sLP : kLD, rows = W ? p.CR : kMax, TC = W ? kMaxW : kMax;
   float* Qr = smf;
-  float* Gp = Qr + kTile;
-  float* tk = Gp + kTile;  // gam, fac, ea, er, valid: 5 x kMax
-  float* ear = tk + 5 * kMax;  // exp(da_cs) per row j = t*R + r
+  float* Gp = Qr + rows * LN;
+  float* tk = Gp + rows * LP;  // gam, fac, ea, er, valid: 5 x TC
+  float* ear = tk + 5 * TC;    // exp(da_cs) per row j = t*R + r
   const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  load_tokens<A>(p, bh, c, tk, tk + kMax, tk + 2 * kMax, tk + 3 * kMax, tk + 4 * kMax);
-  load_dphio<A>(p, b, h, c, Gp);
-  load_rotated<A>(p, b, h, c, p.q, p.q_bias, Qr);
+  load_tokens<A>(p, bh, c, tk, tk + TC, tk + 2 * TC, tk + 3 * TC, tk + 4 * TC);
+  load_dphio<A>(p, b, h, c, Gp, LP);
+  load_rotated<A>(p, b, h, c, p.q, p.q_bias, Qr, LN);
   __syncthreads();
-  const float* ea = tk + 2 * kMax;
+  const float* ea = tk + 2 * TC;
   for (int j = threadIdx.x; j < p.CR; j += blockDim.x) ear[j] = ea[j / p.R];
   __syncthreads();
-  const int i0 = (threadIdx.x >> 4) * 4, j0 = (threadIdx.x & 15) * 4;
-  float acc[4][4];
-  zero4(acc);
-  mm4(acc, i0, j0, p.CR, [=](int n, int i) { return Qr[i * kLD + n] * ear[i]; },
-      [=](int i, int pp) { return Gp[i * kLD + pp]; });
   float* dst = p.ws_D + ((int64_t)bh * p.nc + c) * p.N * p.P;
+  auto block = [&](int n0, int p0) {  // the 64 x 64 output block at (n0, p0)
+    const int i0 = n0 + (threadIdx.x >> 4) * 4, j0 = p0 + (threadIdx.x & 15) * 4;
+    float acc[4][4];
+    zero4(acc);
+    mm4(acc, i0, j0, p.CR, [=](int n, int i) { return Qr[i * LN + n] * ear[i]; },
+        [=](int i, int pp) { return Gp[i * LP + pp]; });
 #pragma unroll
-  for (int u = 0; u < 4; u++)
+    for (int u = 0; u < 4; u++)
 #pragma unroll
-    for (int v = 0; v < 4; v++)
-      if (i0 + u < p.N && j0 + v < p.P) dst[(i0 + u) * p.P + j0 + v] = acc[u][v];
+      for (int v = 0; v < 4; v++)
+        if (i0 + u < p.N && j0 + v < p.P) dst[(i0 + u) * p.P + j0 + v] = acc[u][v];
+  };
+  if constexpr (!W) {
+    block(0, 0);
+  } else {
+    for (int n0 = 0; n0 < p.N; n0 += 64)
+      for (int p0 = 0; p0 < p.P; p0 += 64) block(n0, p0);
+  }
   if (threadIdx.x == 0) {
     const int last = min(c * p.C + p.C, p.S) - 1;
     p.ws_alpha[(int64_t)bh * p.nc + c] = expf(p.da_cs[(int64_t)bh * p.S + last]);
@@ -307,41 +328,78 @@ __global__ void __launch_bounds__(128) scan_kernel(const BBParams p) {
 }
 
 // ---- 3. every gradient of one chunk
-template <int A>
-__global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
-  extern __shared__ float smf[];
-  float* Qr = smf;              // rotated q rows
-  float* Kr = Qr + kTile;       // rotated k rows
-  float* Ps = Kr + kTile;       // PsiV
-  float* Gp = Ps + kTile;       // dPhiO
-  float* Hc = Gp + kTile;       // state entering the chunk [N][P]
-  float* Dn = Hc + kTile;       // gradient of the state leaving it [N][P]
-  float* M1 = Dn + kTile;       // A, then (kept) for the segsum gradient
-  float* M2 = M1 + kTile;       // dA, then dS
-  float* dQ = M2 + kTile;       // gradient of q_rot
-  float* dK = dQ + kTile;       // gradient of k_scaled
-  float* dP = dK + kTile;       // gradient of PsiV
-  float* sm = dP + kTile;       // segsum [C][C] | qk [C][R][R] | dqk [C][R][R]
-  float* tk = sm + kSmall;      // gam | fac | ea | er | valid, kMax each
-  float* red = tk + 5 * kMax;   // three [kMax][kRedCols] row-partial buffers
-  float* red2 = red + kMax * kRedCols;
-  float* red3 = red2 + kMax * kRedCols;
-  float* wsum = red3 + kMax * kRedCols;  // [2][kTG / 32] per-warp sums
-  float* facr = wsum + 2 * (kTG / 32);   // factor, exp(da_cs), exp(da_cs_rev) per row j = t*R + r
-  float* ear = facr + kMax;
-  float* err = ear + kMax;
+// This warp's 16 x 16 output tiles of a rows x cols product, f(r0, c0, tile
+// column): on the 64-wide path one tile of the 4 x 4 grid per warp (16
+// warps), on the wide path a strided walk over the grid.
+template <bool W, class F>
+__device__ __forceinline__ void for_tiles(int rows, int cols, F f) {
+  const int wid = threadIdx.x >> 5;
+  if constexpr (!W) {
+    f((wid >> 2) * 16, (wid & 3) * 16, wid & 3);
+  } else {
+    const int nr = (rows + 15) >> 4, ncol = (cols + 15) >> 4;
+    for (int t = wid; t < nr * ncol; t += kTG / 32) f((t / ncol) * 16, (t % ncol) * 16, t % ncol);
+  }
+}
+
+// Tiles: on the 64-wide path eleven [64][kLD] FP32 tiles in shared memory;
+// on the wide path the same tiles in this CTA's global scratch (rows padded
+// to 16 and strides rounded up to 16, so that every fragment read of a
+// 16 x 16 tile stays inside its tile), the small tables in shared memory.
+template <int A, bool WIDE>
+__device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, float* smf, float* scr) {
+  const int LN = WIDE ? p.LN : kLD, LP = WIDE ? p.LP : kLD, LC = WIDE ? p.LC : kLD;
+  const int TC = WIDE ? kMaxW : kMax;
+  float *Qr, *Kr, *Ps, *Gp, *Hc, *Dn, *M1, *M2, *dQ, *dK, *dP, *sm;
+  if constexpr (!WIDE) {
+    Qr = smf;              // rotated q rows
+    Kr = Qr + kTile;       // rotated k rows
+    Ps = Kr + kTile;       // PsiV
+    Gp = Ps + kTile;       // dPhiO
+    Hc = Gp + kTile;       // state entering the chunk [N][P]
+    Dn = Hc + kTile;       // gradient of the state leaving it [N][P]
+    M1 = Dn + kTile;       // A, then (kept) for the segsum gradient
+    M2 = M1 + kTile;       // dA, then dS
+    dQ = M2 + kTile;       // gradient of q_rot
+    dK = dQ + kTile;       // gradient of k_scaled
+    dP = dK + kTile;       // gradient of PsiV
+    sm = dP + kTile;       // segsum [C][C] | qk [C][R][R] | dqk [C][R][R]
+  } else {
+    const int64_t tq = (int64_t)p.CR16 * LN, tp = (int64_t)p.CR16 * LP, th = (int64_t)p.N16 * LP;
+    Qr = scr;
+    Kr = Qr + tq;
+    dQ = Kr + tq;
+    dK = dQ + tq;
+    Ps = dK + tq;
+    Gp = Ps + tp;
+    dP = Gp + tp;
+    Hc = dP + tp;
+    Dn = Hc + th;
+    M1 = Dn + th;
+    M2 = M1 + p.m1sz;
+    sm = smf;
+  }
+  float* tk = sm + (WIDE ? kSmallW : kSmall);  // gam | fac | ea | er | valid, TC each
+  float* red = tk + 5 * TC;                 // three [TC][kRedCols] row-partial buffers
+  float* red2 = red + TC * kRedCols;
+  float* red3 = red2 + TC * kRedCols;
+  float* wsum = red3 + TC * kRedCols;       // [2][kTG / 32] per-warp sums
+  float* facr = wsum + 2 * (kTG / 32);      // factor, exp(da_cs), exp(da_cs_rev) per row j = t*R + r
+  float* ear = facr + TC;
+  float* err = ear + TC;
   float* gam = tk;
-  float* fac = tk + kMax;
-  float* ea = tk + 2 * kMax;
-  float* er = tk + 3 * kMax;
-  float* valid = tk + 4 * kMax;
+  float* fac = tk + TC;
+  float* ea = tk + 2 * TC;
+  float* er = tk + 3 * TC;
+  float* valid = tk + 4 * TC;
   const int C = p.C, R = p.R, N = p.N, P = p.P, CR = p.CR;
   float* seg = sm;
   float* qk = sm + C * C;
   float* dqk = qk + C * R * R;
-  const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  const int tid = threadIdx.x, wid = tid >> 5;
-  const int fr0 = (wid >> 2) * 16, fc0 = (wid & 3) * 16, wc = wid & 3;  // this warp's 16 x 16 tile
+  const int b = bh / p.H, h = bh % p.H;
+  const int tid = threadIdx.x;
+  // column tiles of the N-wide and P-wide row sums
+  const int ctn = WIDE ? (N + 15) >> 4 : 4, ctp = WIDE ? (P + 15) >> 4 : 4;
 
   // ---- inputs of the chunk
   load_tokens<A>(p, bh, c, gam, fac, ea, er, valid);
@@ -351,13 +409,13 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
     qk[e] = tg < p.S ? ld_act<A>(p.qk, ((int64_t)bh * p.S + tg) * R * R + e % (R * R)) : 0.f;
   }
   for (int e = tid; e < N * P; e += kTG) {
-    Hc[(e / P) * kLD + e % P] = ld_act<A>(p.states, ((int64_t)bh * p.nc + c) * N * P + e);
-    Dn[(e / P) * kLD + e % P] = p.ws_D[((int64_t)bh * p.nc + c) * N * P + e];
+    Hc[(e / P) * LP + e % P] = ld_act<A>(p.states, ((int64_t)bh * p.nc + c) * N * P + e);
+    Dn[(e / P) * LP + e % P] = p.ws_D[((int64_t)bh * p.nc + c) * N * P + e];
   }
-  load_psi<A>(p, b, h, c, Ps);
-  load_dphio<A>(p, b, h, c, Gp);
-  load_rotated<A>(p, b, h, c, p.q, p.q_bias, Qr);
-  load_rotated<A>(p, b, h, c, p.k, p.k_bias, Kr);
+  load_psi<A>(p, b, h, c, Ps, LP);
+  load_dphio<A>(p, b, h, c, Gp, LP);
+  load_rotated<A>(p, b, h, c, p.q, p.q_bias, Qr, LN);
+  load_rotated<A>(p, b, h, c, p.k, p.k_bias, Kr, LN);
   __syncthreads();
   for (int j = tid; j < CR; j += kTG) {
     facr[j] = fac[j / R];
@@ -369,30 +427,30 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   // ---- A = mask(q_rot k_scaled^T) exp(segsum): selected, never multiplied by
   //      a mask (padded rows and the upper triangle never reach a product)
   auto tok_ok = [=](int i, int j) { return (i / R) > (j / R) && valid[i / R] != 0.f; };
-  {
+  for_tiles<WIDE>(CR, CR, [&](int fr0, int fc0, int) {
     float acc[2][4];
     zero_tc(acc);
-    mm_tc(acc, fr0, fc0, N, [=](int i, int n) { return Qr[i * kLD + n]; }, [=](int n, int j) { return Kr[j * kLD + n]; });
+    mm_tc(acc, fr0, fc0, N, [=](int i, int n) { return Qr[i * LN + n]; }, [=](int n, int j) { return Kr[j * LN + n]; });
 #pragma unroll
     for (int nb = 0; nb < 2; nb++)
 #pragma unroll
       for (int e = 0; e < 4; e++) {
         const int i = TC_ROW(fr0, e), j = TC_COL(fc0, nb, e);
         if (i < CR && j < CR)
-          M1[i * kLD + j] = tok_ok(i, j) ? acc[nb][e] * facr[j] * expf(seg[(i / R) * C + j / R]) : 0.f;
+          M1[i * LC + j] = tok_ok(i, j) ? acc[nb][e] * facr[j] * expf(seg[(i / R) * C + j / R]) : 0.f;
       }
-  }
+  });
   __syncthreads();
 
   // ---- dPsiV = A^T dPhiO + k_state D_{c+1} + d dPhiO + gamma qk^T dPhiO (diagonal);
   //      dA = dPhiO PsiV^T
-  {
+  const float dv = p.has_d ? p.d[h] : 0.f;
+  for_tiles<WIDE>(CR, P, [&](int fr0, int fc0, int) {
     float acc[2][4], acc2[2][4];
     zero_tc(acc);
-    mm_tc(acc, fr0, fc0, CR, [=](int j, int i) { return M1[i * kLD + j]; }, [=](int i, int pp) { return Gp[i * kLD + pp]; });
+    mm_tc(acc, fr0, fc0, CR, [=](int j, int i) { return M1[i * LC + j]; }, [=](int i, int pp) { return Gp[i * LP + pp]; });
     zero_tc(acc2);
-    mm_tc(acc2, fr0, fc0, N, [=](int j, int n) { return Kr[j * kLD + n]; }, [=](int n, int pp) { return Dn[n * kLD + pp]; });
-    const float dv = p.has_d ? p.d[h] : 0.f;
+    mm_tc(acc2, fr0, fc0, N, [=](int j, int n) { return Kr[j * LN + n]; }, [=](int n, int pp) { return Dn[n * LP + pp]; });
 #pragma unroll
     for (int nb = 0; nb < 2; nb++)
 #pragma unroll
@@ -400,22 +458,25 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
         const int j = TC_ROW(fr0, e), pp = TC_COL(fc0, nb, e);
         if (j < CR && pp < P) {
           const int t = j / R, r = j % R;
-          float x = acc[nb][e] + acc2[nb][e] * facr[j] * err[j] + dv * Gp[j * kLD + pp];
+          float x = acc[nb][e] + acc2[nb][e] * facr[j] * err[j] + dv * Gp[j * LP + pp];
           float dg = 0.f;
-          for (int o = 0; o < R; o++) dg = fmaf(qk[(t * R + o) * R + r], Gp[(t * R + o) * kLD + pp], dg);
-          dP[j * kLD + pp] = fmaf(gam[t], dg, x);
+          for (int o = 0; o < R; o++) dg = fmaf(qk[(t * R + o) * R + r], Gp[(t * R + o) * LP + pp], dg);
+          dP[j * LP + pp] = fmaf(gam[t], dg, x);
         }
       }
+  });
+  for_tiles<WIDE>(CR, CR, [&](int fr0, int fc0, int) {
+    float acc[2][4];
     zero_tc(acc);
-    mm_tc(acc, fr0, fc0, P, [=](int i, int pp) { return Gp[i * kLD + pp]; }, [=](int pp, int j) { return Ps[j * kLD + pp]; });
+    mm_tc(acc, fr0, fc0, P, [=](int i, int pp) { return Gp[i * LP + pp]; }, [=](int pp, int j) { return Ps[j * LP + pp]; });
 #pragma unroll
     for (int nb = 0; nb < 2; nb++)
 #pragma unroll
       for (int e = 0; e < 4; e++) {
         const int i = TC_ROW(fr0, e), j = TC_COL(fc0, nb, e);
-        if (i < CR && j < CR) M2[i * kLD + j] = acc[nb][e];
+        if (i < CR && j < CR) M2[i * LC + j] = acc[nb][e];
       }
-  }
+  });
   __syncthreads();
 
   // ---- DSSDA[ti][tj] = sum over the token pair's rank pairs of dA * A
@@ -424,14 +485,14 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
     float s = 0.f;
     if (ti > tj && valid[ti] != 0.f)
       for (int o = 0; o < R; o++)
-        for (int r = 0; r < R; r++) s = fmaf(M2[(ti * R + o) * kLD + tj * R + r], M1[(ti * R + o) * kLD + tj * R + r], s);
+        for (int r = 0; r < R; r++) s = fmaf(M2[(ti * R + o) * LC + tj * R + r], M1[(ti * R + o) * LC + tj * R + r], s);
     p.DSSDA[((int64_t)bh * p.nc + c) * C * C + e] = (valid[tj] != 0.f) ? s : 0.f;
   }
   __syncthreads();
   // dS = dA exp(segsum) on the causal entries (in place)
   for (int e = tid; e < CR * CR; e += kTG) {
     const int i = e / CR, j = e % CR;
-    M2[i * kLD + j] = tok_ok(i, j) ? M2[i * kLD + j] * expf(seg[(i / R) * C + j / R]) : 0.f;
+    M2[i * LC + j] = tok_ok(i, j) ? M2[i * LC + j] * expf(seg[(i / R) * C + j / R]) : 0.f;
   }
   __syncthreads();
 
@@ -439,24 +500,27 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   //      dk_scaled = dS^T q_rot + exp(da_cs_rev) dk_state, dk_state = PsiV Dn^T;
   //      row sums for DDA_CS_REV (dk_state * k_state), DFACTOR (dk_scaled *
   //      k_rot) and DDA_CS (inter * dPhiO)
-  {
+  for_tiles<WIDE>(CR, N, [&](int fr0, int fc0, int) {
     float acc[2][4], acc2[2][4];
     zero_tc(acc);
-    mm_tc(acc, fr0, fc0, CR, [=](int i, int j) { return M2[i * kLD + j] * facr[j]; },
-          [=](int j, int n) { return Kr[j * kLD + n]; });
+    mm_tc(acc, fr0, fc0, CR, [=](int i, int j) { return M2[i * LC + j] * facr[j]; },
+          [=](int j, int n) { return Kr[j * LN + n]; });
     zero_tc(acc2);
-    mm_tc(acc2, fr0, fc0, P, [=](int i, int pp) { return Gp[i * kLD + pp]; }, [=](int pp, int n) { return Hc[n * kLD + pp]; });
+    mm_tc(acc2, fr0, fc0, P, [=](int i, int pp) { return Gp[i * LP + pp]; }, [=](int pp, int n) { return Hc[n * LP + pp]; });
 #pragma unroll
     for (int nb = 0; nb < 2; nb++)
 #pragma unroll
       for (int e = 0; e < 4; e++) {
         const int i = TC_ROW(fr0, e), n = TC_COL(fc0, nb, e);
-        if (i < CR && n < N) dQ[i * kLD + n] = fmaf(ear[i], acc2[nb][e], acc[nb][e]);
+        if (i < CR && n < N) dQ[i * LN + n] = fmaf(ear[i], acc2[nb][e], acc[nb][e]);
       }
+  });
+  for_tiles<WIDE>(CR, N, [&](int fr0, int fc0, int wc) {
+    float acc[2][4], acc2[2][4];
     zero_tc(acc);
-    mm_tc(acc, fr0, fc0, P, [=](int j, int pp) { return Ps[j * kLD + pp]; }, [=](int pp, int n) { return Dn[n * kLD + pp]; });
+    mm_tc(acc, fr0, fc0, P, [=](int j, int pp) { return Ps[j * LP + pp]; }, [=](int pp, int n) { return Dn[n * LP + pp]; });
     zero_tc(acc2);
-    mm_tc(acc2, fr0, fc0, CR, [=](int j, int i) { return M2[i * kLD + j]; }, [=](int i, int n) { return Qr[i * kLD + n]; });
+    mm_tc(acc2, fr0, fc0, CR, [=](int j, int i) { return M2[i * LC + j]; }, [=](int i, int n) { return Qr[i * LN + n]; });
     float r1[2] = {0.f, 0.f}, r2[2] = {0.f, 0.f};
 #pragma unroll
     for (int nb = 0; nb < 2; nb++)
@@ -464,42 +528,45 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
       for (int e = 0; e < 4; e++) {
         const int j = TC_ROW(fr0, e), n = TC_COL(fc0, nb, e);
         if (j < CR && n < N) {
-          const float kr = Kr[j * kLD + n];
+          const float kr = Kr[j * LN + n];
           r1[e >> 1] = fmaf(acc[nb][e], kr * facr[j] * err[j], r1[e >> 1]);
           const float dks = fmaf(err[j], acc[nb][e], acc2[nb][e]);
           r2[e >> 1] = fmaf(dks, kr, r2[e >> 1]);
-          dK[j * kLD + n] = dks;
+          dK[j * LN + n] = dks;
         }
       }
     tc_row_sums(r1, red, fr0, wc);
     tc_row_sums(r2, red2, fr0, wc);
-    // inter = exp(da_cs) q_rot Hc
+  });
+  // inter = exp(da_cs) q_rot Hc
+  for_tiles<WIDE>(CR, P, [&](int fr0, int fc0, int wc) {
+    float acc[2][4];
     zero_tc(acc);
-    mm_tc(acc, fr0, fc0, N, [=](int i, int n) { return Qr[i * kLD + n]; }, [=](int n, int pp) { return Hc[n * kLD + pp]; });
+    mm_tc(acc, fr0, fc0, N, [=](int i, int n) { return Qr[i * LN + n]; }, [=](int n, int pp) { return Hc[n * LP + pp]; });
     float r3[2] = {0.f, 0.f};
 #pragma unroll
     for (int nb = 0; nb < 2; nb++)
 #pragma unroll
       for (int e = 0; e < 4; e++) {
         const int i = TC_ROW(fr0, e), pp = TC_COL(fc0, nb, e);
-        if (i < CR && pp < P) r3[e >> 1] = fmaf(acc[nb][e] * ear[i], Gp[i * kLD + pp], r3[e >> 1]);
+        if (i < CR && pp < P) r3[e >> 1] = fmaf(acc[nb][e] * ear[i], Gp[i * LP + pp], r3[e >> 1]);
       }
     tc_row_sums(r3, red3, fr0, wc);
-  }
+  });
   // same-token terms: dot[t,o,r] = dPhiO[(t,o)] . PsiV[(t,r)]; dqk = gamma dot,
   // DGAMMA = sum qk * dot
   for (int e = tid; e < C * R * R; e += kTG) {
     const int t = e / (R * R), o = (e / R) % R, r = e % R;
     float s = 0.f;
-    for (int pp = 0; pp < P; pp++) s = fmaf(Gp[(t * R + o) * kLD + pp], Ps[(t * R + r) * kLD + pp], s);
+    for (int pp = 0; pp < P; pp++) s = fmaf(Gp[(t * R + o) * LP + pp], Ps[(t * R + r) * LP + pp], s);
     dqk[e] = s;  // gamma applied below
   }
   // DDA (alpha_c <Hc, D_{c+1}> at the chunk's last valid token) and the DD
   // partial (sum dPhiO * PsiV): block sums in a fixed order
   {
     float s = 0.f, dd = 0.f;
-    for (int e = tid; e < N * P; e += kTG) s = fmaf(Hc[(e / P) * kLD + e % P], Dn[(e / P) * kLD + e % P], s);
-    for (int e = tid; e < CR * P; e += kTG) dd = fmaf(Gp[(e / P) * kLD + e % P], Ps[(e / P) * kLD + e % P], dd);
+    for (int e = tid; e < N * P; e += kTG) s = fmaf(Hc[(e / P) * LP + e % P], Dn[(e / P) * LP + e % P], s);
+    for (int e = tid; e < CR * P; e += kTG) dd = fmaf(Gp[(e / P) * LP + e % P], Ps[(e / P) * LP + e % P], dd);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -513,12 +580,13 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   __syncthreads();
   for (int t = tid; t < C; t += kTG) {  // per-token sums
     float s1 = 0.f, s2 = 0.f, s3 = 0.f, g = 0.f;
-    for (int r = 0; r < R; r++)
-      for (int q = 0; q < 4; q++) {  // the four column tiles of the row
+    for (int r = 0; r < R; r++) {  // the column tiles of the row
+      for (int q = 0; q < ctn; q++) {
         s1 += red[(t * R + r) * kRedCols + q];
         s2 += red2[(t * R + r) * kRedCols + q];
-        s3 += red3[(t * R + r) * kRedCols + q];
       }
+      for (int q = 0; q < ctp; q++) s3 += red3[(t * R + r) * kRedCols + q];
+    }
     for (int e = 0; e < R * R; e++) g = fmaf(qk[t * R * R + e], dqk[t * R * R + e], g);
     const int tg = c * C + t;
     if (tg < p.S) {
@@ -565,8 +633,8 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
     float s = 0.f;
     for (int r = 0; r < R; r++) {
       const int j = t * R + r;
-      s += dQ[j * kLD + m] * (-Qr[j * kLD + half + m]) + dQ[j * kLD + half + m] * Qr[j * kLD + m];
-      s += fac[t] * (dK[j * kLD + m] * (-Kr[j * kLD + half + m]) + dK[j * kLD + half + m] * Kr[j * kLD + m]);
+      s += dQ[j * LN + m] * (-Qr[j * LN + half + m]) + dQ[j * LN + half + m] * Qr[j * LN + m];
+      s += fac[t] * (dK[j * LN + m] * (-Kr[j * LN + half + m]) + dK[j * LN + half + m] * Kr[j * LN + m]);
     }
     p.DANGLES[(((int64_t)b * p.S + tg) * p.H + h) * W + m] = s;
   }
@@ -575,26 +643,26 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   for (int e = tid; e < CR * W; e += kTG) {
     const int j = e / W, m = e % W, t = j / R;
     const float cs = cst[t * W + m], sn = snt[t * W + m];
-    float lo = Qr[j * kLD + m], hi = Qr[j * kLD + half + m];
-    Qr[j * kLD + m] = cs * lo + sn * hi;
-    Qr[j * kLD + half + m] = -sn * lo + cs * hi;
-    lo = Kr[j * kLD + m];
-    hi = Kr[j * kLD + half + m];
-    Kr[j * kLD + m] = cs * lo + sn * hi;
-    Kr[j * kLD + half + m] = -sn * lo + cs * hi;
+    float lo = Qr[j * LN + m], hi = Qr[j * LN + half + m];
+    Qr[j * LN + m] = cs * lo + sn * hi;
+    Qr[j * LN + half + m] = -sn * lo + cs * hi;
+    lo = Kr[j * LN + m];
+    hi = Kr[j * LN + half + m];
+    Kr[j * LN + m] = cs * lo + sn * hi;
+    Kr[j * LN + half + m] = -sn * lo + cs * hi;
   }
   // DV and the DMIMO_V partial of the chunk
   for (int e = tid; e < C * P; e += kTG) {
     const int t = e / P, pp = e % P, tg = c * C + t;
     if (tg >= p.S) continue;
     float s = 0.f;
-    for (int r = 0; r < R; r++) s = fmaf(dP[(t * R + r) * kLD + pp], mvs[r * P + pp], s);
+    for (int r = 0; r < R; r++) s = fmaf(dP[(t * R + r) * LP + pp], mvs[r * P + pp], s);
     store_dqkv(p.DV, (((int64_t)b * p.S + tg) * p.H + h) * P + pp, s, p.dqkv);
   }
   for (int e = tid; e < R * P; e += kTG) {
     const int r = e / P, pp = e % P;
     float s = 0.f;
-    for (int t = 0; t < C; t++) s = fmaf(dP[(t * R + r) * kLD + pp], vs[t * P + pp], s);
+    for (int t = 0; t < C; t++) s = fmaf(dP[(t * R + r) * LP + pp], vs[t * P + pp], s);
     p.ws_mv[((int64_t)bh * p.nc + c) * R * P + e] = s;
   }
   __syncthreads();
@@ -603,22 +671,42 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   for (int e = tid; e < CR * N; e += kTG) {
     const int j = e / N, n = e % N, t = j / R, r = j % R, tg = c * C + t;
     if (tg >= p.S) continue;
-    float dq = dQ[j * kLD + n], dk = dK[j * kLD + n] * fac[t];
+    float dq = dQ[j * LN + n], dk = dK[j * LN + n] * fac[t];
     const int m = n < W ? n : (n >= half && n < half + W ? n - half : -1);
     if (m >= 0) {
       const float cs = cst[t * W + m], sn = snt[t * W + m];
-      const float qlo = dQ[j * kLD + m], qhi = dQ[j * kLD + half + m];
-      const float klo = dK[j * kLD + m] * fac[t], khi = dK[j * kLD + half + m] * fac[t];
+      const float qlo = dQ[j * LN + m], qhi = dQ[j * LN + half + m];
+      const float klo = dK[j * LN + m] * fac[t], khi = dK[j * LN + half + m] * fac[t];
       dq = n < W ? cs * qlo + sn * qhi : -sn * qlo + cs * qhi;
       dk = n < W ? cs * klo + sn * khi : -sn * klo + cs * khi;
     }
     for (int x = 0; x < R; x++) {
-      dq = fmaf(dqk[(t * R + r) * R + x], Kr[(t * R + x) * kLD + n], dq);  // row (t, o = r) of q
-      dk = fmaf(dqk[(t * R + x) * R + r], Qr[(t * R + x) * kLD + n], dk);  // row (t, r) of k
+      dq = fmaf(dqk[(t * R + r) * R + x], Kr[(t * R + x) * LN + n], dq);  // row (t, o = r) of q
+      dk = fmaf(dqk[(t * R + x) * R + r], Qr[(t * R + x) * LN + n], dk);  // row (t, r) of k
     }
     const int64_t o = (((int64_t)b * p.S + tg) * R + r) * p.H + h;
     store_dqkv(p.DQ, o * N + n, dq, p.dqkv);
     store_dqkv(p.DK, o * N + n, dk, p.dqkv);
+  }
+}
+
+// One chunk per CTA (N, P, C*R <= 64).
+template <int A>
+__global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
+  extern __shared__ float smf[];
+  grad_chunk<A, false>(p, blockIdx.x, blockIdx.y, smf, nullptr);
+}
+
+// Wide shapes: a persistent grid walks the (b*h, chunk) items, each CTA
+// reusing its own scratch.
+template <int A>
+__global__ void __launch_bounds__(kTG, 1) grad_kernel_wide(const BBParams p) {
+  extern __shared__ float smf[];
+  float* scr = p.ws_scr + (int64_t)blockIdx.x * p.scr_floats;
+  const int items = p.nc * p.B * p.H;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    grad_chunk<A, true>(p, it % p.nc, it / p.nc, smf, scr);
+    __syncthreads();  // every read of this item's tiles precedes the next item's loads
   }
 }
 
@@ -641,10 +729,18 @@ static const char* const kBBStageNames[4] = {"bb_seed", "bb_scan", "bb_grad", "b
 
 constexpr size_t kSeedSmem = (2 * kTile + 6 * kMax) * sizeof(float);
 constexpr size_t kGradSmem = (11 * kTile + kSmall + 8 * kMax + 3 * kMax * kRedCols + 2 * (kTG / 32)) * sizeof(float);
+// wide path: the seed tiles at their largest (C*R = 128 rows, N = 256, P = 128)
+constexpr size_t kSeedSmemW = (kMaxW * 2 * kMaxW + kMaxW * kMaxW + 6 * kMaxW) * sizeof(float);
+constexpr size_t kGradSmemW = (kSmallW + 8 * kMaxW + 3 * kMaxW * kRedCols + 2 * (kTG / 32)) * sizeof(float);
+static size_t seed_smem_wide(const BBParams& p) {
+  return ((size_t)p.CR * (p.sLN + p.sLP) + 6 * kMaxW) * sizeof(float);
+}
+static int grad_grid_wide(const BBParams& p) { return std::min(p.nc * p.B * p.H, kWideGrid); }
 
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace carve-up (bytes): D, alpha, DMIMO_V partials, DD partials.
+// Workspace carve-up (bytes): D, alpha, DMIMO_V partials, DD partials and,
+// on the wide path, the gradient kernel's per-CTA tile scratch.
 static size_t bb_workspace(const BBParams& p, size_t* off) {
   const size_t BH = (size_t)p.B * p.H, nc = (size_t)p.nc;
   size_t o = 0;
@@ -652,6 +748,7 @@ static size_t bb_workspace(const BBParams& p, size_t* off) {
   off[1] = o; o += a256(BH * nc * 4);
   off[2] = o; o += a256(BH * nc * p.R * p.P * 4);
   off[3] = o; o += a256(BH * nc * 4);
+  off[4] = o; o += p.wide ? a256((size_t)grad_grid_wide(p) * p.scr_floats * 4) : 0;
   return o;
 }
 
@@ -663,8 +760,9 @@ static mmbf_status bb_plan(const mmbf_dims* dims, int64_t chunk_size, int64_t di
   if (d.H % d.G) return fail(MMBF_ERR_SHAPE, "H (%lld) must be a multiple of G (%lld)", (long long)d.H, (long long)d.G);
   if (div != 2 && div != 4) return fail(MMBF_ERR_SHAPE, "rotary_dim_divisor must be 2 or 4");
   if (d.N % 2 || d.N % div) return fail(MMBF_ERR_SHAPE, "N must be even and a multiple of rotary_dim_divisor");
-  if (d.N > kMax || d.P > kMax || chunk_size * d.R > kMax || d.R > 16)
-    return fail(MMBF_ERR_UNSUPPORTED, "this build of the second stage needs N, P, C*R <= %d and R <= 16", kMax);
+  if (d.N > 2 * kMaxW || d.P > kMaxW || chunk_size * d.R > kMaxW || d.R > 16)
+    return fail(MMBF_ERR_UNSUPPORTED, "this build of the second stage needs N <= %d, P, C*R <= %d and R <= 16",
+                2 * kMaxW, kMaxW);
   if (d.S > (1 << 30) || d.B * d.H > 65535) return fail(MMBF_ERR_UNSUPPORTED, "S > 2^30 or B*H > 65535");
   BBParams p = {};
   p.B = (int)d.B; p.S = (int)d.S; p.H = (int)d.H; p.G = (int)d.G; p.R = (int)d.R; p.N = (int)d.N; p.P = (int)d.P;
@@ -672,6 +770,21 @@ static mmbf_status bb_plan(const mmbf_dims* dims, int64_t chunk_size, int64_t di
   p.w = (int)(d.N / div);
   p.nc = (int)((d.S + chunk_size - 1) / chunk_size);
   p.CR = p.C * p.R;
+  p.wide = (p.N > kMax || p.P > kMax || p.CR > kMax) ? 1 : 0;
+  if (p.wide) {
+    auto up = [](int x, int m) { return (x + m - 1) / m * m; };
+    p.LN = up(p.N, 16); p.LP = up(p.P, 16); p.LC = up(p.CR, 16);
+    p.CR16 = p.LC; p.N16 = p.LN;
+    p.sLN = up(p.N, 64); p.sLP = up(p.P, 64);
+    const int64_t cc = (int64_t)p.CR16 * p.LC;
+    p.m1sz = std::max<int64_t>(cc, 2 * (int64_t)p.C * p.w + (int64_t)p.R * p.P);  // A; rotary cos / sin, mimo_v
+    p.m2sz = std::max<int64_t>(cc, (int64_t)p.C * p.P);                              // dA, dS; v
+    auto a64 = [](int64_t x) { return (x + 63) / 64 * 64; };
+    p.m1sz = a64(p.m1sz);
+    p.m2sz = a64(p.m2sz);
+    p.scr_floats = 4 * (int64_t)p.CR16 * p.LN + 3 * (int64_t)p.CR16 * p.LP + 2 * (int64_t)p.N16 * p.LP + p.m1sz + p.m2sz;
+    p.scr_floats = a64(p.scr_floats);
+  }
   *out = p;
   return MMBF_OK;
 }
@@ -682,9 +795,13 @@ template <int A>
 cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
   static bool smem_set = false;
   if (!smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(seed_kernel<A>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeedSmem);
+    cudaError_t e = cudaFuncSetAttribute(seed_kernel<A, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeedSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(grad_kernel<A>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(seed_kernel<A, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeedSmemW);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grad_kernel_wide<A>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmemW);
     if (e != cudaSuccess) return e;
     smem_set = true;
   }
@@ -692,13 +809,19 @@ cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
   g_stage_names = kBBStageNames;
   g_stage_names_n = 4;
   stage_event(0, 0, st);
-  seed_kernel<A><<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
+  if (p.wide)
+    seed_kernel<A, true><<<dim3(p.nc, BH), kT, seed_smem_wide(p), st>>>(p);
+  else
+    seed_kernel<A, false><<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
   stage_event(0, 1, st);
   stage_event(1, 0, st);
   scan_kernel<<<dim3((p.N * p.P + 127) / 128, BH), 128, 0, st>>>(p);
   stage_event(1, 1, st);
   stage_event(2, 0, st);
-  grad_kernel<A><<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
+  if (p.wide)
+    grad_kernel_wide<A><<<grad_grid_wide(p), kTG, kGradSmemW, st>>>(p);
+  else
+    grad_kernel<A><<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
   stage_event(2, 1, st);
   stage_event(3, 0, st);
   reduce_kernel<<<BH, kT, 0, st>>>(p);
@@ -718,7 +841,7 @@ mmbf_status mamba_mimo_bwd_bwd_workspace_size(const mmbf_dims* dims, int64_t chu
   mmbf_status s = bb_plan(dims, chunk_size, rotary_dim_divisor, &p);
   if (s != MMBF_OK) return s;
   if (!bytes) return fail(MMBF_ERR_ARG, "bytes is NULL");
-  size_t off[4];
+  size_t off[5];
   *bytes = bb_workspace(p, off);
   return MMBF_OK;
 }
@@ -747,7 +870,7 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
                        angles, mimo_o, d, DQ, DK, DV, DMIMO_V, DANGLES, DFACTOR, DGAMMA, DDA, DSSDA, DDA_CS_REV, DDA_CS, DD};
   for (const void* x : all)
     if (x && (reinterpret_cast<uintptr_t>(x) & 3)) return fail(MMBF_ERR_ALIGN, "tensor pointers must be 4-byte aligned");
-  size_t off[4];
+  size_t off[5];
   const size_t need = bb_workspace(p, off);
   if (!workspace || workspace_bytes < need)
     return fail(MMBF_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need, workspace_bytes);
@@ -766,6 +889,7 @@ mmbf_status mamba_mimo_bwd_bwd(const mmbf_dims* dims, const void* dout, const vo
   p.ws_alpha = reinterpret_cast<float*>(ws + off[1]);
   p.ws_mv = reinterpret_cast<float*>(ws + off[2]);
   p.ws_dd = reinterpret_cast<float*>(ws + off[3]);
+  p.ws_scr = p.wide ? reinterpret_cast<float*>(ws + off[4]) : nullptr;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = p.act == kBF16 ? launch_bb<kBF16>(p, st) : p.act == kF16 ? launch_bb<kF16>(p, st)

@@ -159,11 +159,41 @@ def test_bwd_bwd_workspace_query_and_envelope(lib):
         (dims(H=6, G=4), 16, 4, 1, "multiple of G"),
         (dims(), 16, 3, 1, "rotary_dim_divisor"),
         (dims(N=66), 16, 4, 1, "N must be even"),
-        (dims(N=128), 16, 4, 3, "N, P, C*R <= 64"),
-        (dims(), 32, 4, 3, "N, P, C*R <= 64"),
+        (dims(N=512), 16, 4, 3, "N <= 256, P, C*R <= 128"),
+        (dims(P=192), 16, 4, 3, "N <= 256, P, C*R <= 128"),
+        (dims(), 64, 4, 3, "N <= 256, P, C*R <= 128"),
+        (dims(R=32, N=16, P=16), 2, 4, 3, "R <= 16"),
     ]:
         st, _, err = bb_ws(lib, d, C, div)
         assert st == code and msg in err, (st, err)
+
+
+def test_bwd_bwd_wide_shapes_add_the_gradient_scratch(lib):
+    # above 64 in N, P or C*R the gradient kernel keeps its FP32 tiles in a
+    # per-CTA scratch (152 persistent CTAs), sized from the padded extents
+    def need(**kw):
+        C = kw.pop("C", 16)
+        st, n, _ = bb_ws(lib, dims(**kw), C, 4)
+        assert st == 0
+        return n
+
+    base = need()
+    for kw, (CR16, LN, LP, N16, C, W, R, P) in [
+        (dict(N=128, P=128), (64, 128, 128, 128, 16, 32, 4, 128)),
+        (dict(C=32), (128, 64, 64, 64, 32, 16, 4, 64)),
+        (dict(N=256, P=72, R=1, C=128), (128, 256, 80, 256, 128, 64, 1, 72)),
+    ]:
+        n = need(**kw)
+        S, H = 8192, 16
+        nc = (S + C - 1) // C
+        Np = kw.get("N", 64)
+        plain = sum((x + 255) // 256 * 256 for x in (H * nc * Np * P * 4, H * nc * 4, H * nc * R * P * 4, H * nc * 4))
+        cc = CR16 * CR16
+        m1 = -(-max(cc, 2 * C * W + R * P) // 64) * 64
+        m2 = -(-max(cc, C * P) // 64) * 64
+        scr = -(-(4 * CR16 * LN + 3 * CR16 * LP + 2 * N16 * LP + m1 + m2) // 64) * 64
+        assert n == plain + (152 * scr * 4 + 255) // 256 * 256, kw
+    assert base < need(N=128, P=128)
 
 
 def test_bwd_bwd_rejects_bad_pointer_patterns_without_gpu(lib):

@@ -91,6 +91,18 @@ CASES = [
     dict(B=1, S=1, H=1, G=1, R=4, N=64, P=64, C=16, div=4, reduced=True, has_d=True),     # one token
 ]
 
+# Shapes past 64 in N, P or C*R (the persistent kernel with tiles in global
+# scratch): the first stage's largest state, the op page's N = 256, C*R =
+# 128 both ways, extents that are not multiples of 16, GQA.
+WIDE = [
+    dict(B=1, S=40, H=2, G=1, R=4, N=128, P=128, C=16, div=4, reduced=True, has_d=True),
+    dict(B=1, S=70, H=1, G=1, R=2, N=256, P=64, C=32, div=2, reduced=True, has_d=True),
+    dict(B=1, S=40, H=2, G=1, R=8, N=64, P=64, C=16, div=4, reduced=False, has_d=True),
+    dict(B=1, S=300, H=1, G=1, R=1, N=16, P=128, C=128, div=4, reduced=True, has_d=False),
+    dict(B=2, S=50, H=2, G=1, R=3, N=80, P=72, C=24, div=4, reduced=True, has_d=True),
+    dict(B=1, S=33, H=4, G=2, R=4, N=128, P=96, C=16, div=2, reduced=True, has_d=True),
+]
+
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"S{c['S']}_R{c['R']}_N{c['N']}_C{c['C']}")
 def test_parity_with_forward_caches(case):
@@ -103,6 +115,20 @@ def test_parity_with_forward_caches(case):
 @pytest.mark.parametrize("case", [CASES[0], CASES[1], CASES[5]], ids=["S40_R4", "S33_R2", "GQA"])
 def test_parity_other_activation_dtypes(case, act):
     args, kw = _problem(**case, seed=29, act=act)
+    want = bb.bwd_bwd(*args, **kw)
+    _compare(_run_gpu(args, kw), want)
+
+
+@pytest.mark.parametrize("case", WIDE, ids=lambda c: f"S{c['S']}_R{c['R']}_N{c['N']}_P{c['P']}_C{c['C']}")
+def test_parity_wide_shapes(case):
+    args, kw = _problem(**case, seed=31)
+    want = bb.bwd_bwd(*args, **kw)
+    _compare(_run_gpu(args, kw), want)
+
+
+def test_wide_shape_more_items_than_persistent_ctas():
+    # 2 x 8 heads x 24 chunks = 384 items on 152 CTAs: each CTA reuses its scratch
+    args, kw = _problem(B=2, S=380, H=8, G=2, R=4, N=128, P=128, C=16, seed=37, caches="random")
     want = bb.bwd_bwd(*args, **kw)
     _compare(_run_gpu(args, kw), want)
 
@@ -150,6 +176,6 @@ def test_lower_precision_dq_dk_dv_are_the_rounded_fp32_results(case, act, out):
 
 
 def test_outside_the_envelope_raises():
-    args, kw = _problem(B=1, S=16, H=1, G=1, R=2, N=128, P=16, C=16, seed=1, caches="random")
+    args, kw = _problem(B=1, S=16, H=1, G=1, R=2, N=512, P=16, C=16, seed=1, caches="random")
     with pytest.raises(NotImplementedError):
         _run_gpu(args, kw)
