@@ -179,13 +179,38 @@ __device__ __forceinline__ void zero4(float (&acc)[TM][TN]) {
     for (int v = 0; v < TN; v++) acc[u][v] = 0.f;
 }
 
+// Problem extents, read from the parameters (ShapeRT) or fixed at compile
+// time for one shape (ShapeCT: the divisions and remainders of the element
+// loops by them become shifts and masks).
+struct ShapeRT {
+  static __device__ __forceinline__ int N(const BBParams& p) { return p.N; }
+  static __device__ __forceinline__ int P(const BBParams& p) { return p.P; }
+  static __device__ __forceinline__ int R(const BBParams& p) { return p.R; }
+  static __device__ __forceinline__ int C(const BBParams& p) { return p.C; }
+  static __device__ __forceinline__ int CR(const BBParams& p) { return p.CR; }
+  static __device__ __forceinline__ int w(const BBParams& p) { return p.w; }
+};
+template <int N_, int P_, int R_, int C_, int W_>
+struct ShapeCT {
+  static __device__ __forceinline__ int N(const BBParams&) { return N_; }
+  static __device__ __forceinline__ int P(const BBParams&) { return P_; }
+  static __device__ __forceinline__ int R(const BBParams&) { return R_; }
+  static __device__ __forceinline__ int C(const BBParams&) { return C_; }
+  static __device__ __forceinline__ int CR(const BBParams&) { return C_ * R_; }
+  static __device__ __forceinline__ int w(const BBParams&) { return W_; }
+  static bool matches(const BBParams& p) { return p.N == N_ && p.P == P_ && p.R == R_ && p.C == C_ && p.w == W_; }
+};
+// the shape with its own instantiation: N = P = 64, R = 4, C = 16, rotary width 16
+using ShapeFast = ShapeCT<64, 64, 4, 16, 16>;
+
 // Token scalars of chunk c (reading of the op header): gamma, factor,
 // exp(da_cs), exp(da_cs_rev), and whether the token is inside S.
-template <int A>
+template <int A, class SH, int NT>
 __device__ __forceinline__ void load_tokens(const BBParams& p, int bh, int c, float* gam, float* fac, float* ea, float* er,
                             float* valid) {
-  for (int t = threadIdx.x; t < p.C; t += blockDim.x) {
-    const int tg = c * p.C + t;
+  #pragma unroll
+  for (int t = threadIdx.x; t < SH::C(p); t += NT) {
+    const int tg = c * SH::C(p) + t;
     const int64_t i = (int64_t)bh * p.S + tg;
     const bool in = tg < p.S, in1 = tg + 1 < p.S;
     const float dtv = in ? p.dt[i] : 0.f, trv = in ? ld_act<A>(p.trap, i) : 0.f;
@@ -202,21 +227,23 @@ __device__ __forceinline__ void load_tokens(const BBParams& p, int bh, int c, fl
 // Biased rows of q (or k) of chunk c, then the rotary on the pairs (m, N/2+m),
 // m < w, in place: rows j = t*R + r of a [C*R][N] tile (zero input past S,
 // plus the bias, as the padded reference).
-template <int A>
+template <int A, class SH, int NT>
 __device__ __forceinline__ void load_rotated(const BBParams& p, int b, int h, int c, const void* src, const float* bias,
                              float* T, int ld) {
   const int g = h / (p.H / p.G);
-  for (int e = threadIdx.x; e < p.CR * p.N; e += blockDim.x) {
-    const int j = e / p.N, n = e % p.N, t = j / p.R, r = j % p.R, tg = c * p.C + t;
-    float x = bias[((int64_t)h * p.R + r) * p.N + n];
-    if (tg < p.S) x += ld_act<A>(src, ((((int64_t)b * p.S + tg) * p.R + r) * p.G + g) * p.N + n);
+  #pragma unroll
+  for (int e = threadIdx.x; e < SH::CR(p) * SH::N(p); e += NT) {
+    const int j = e / SH::N(p), n = e % SH::N(p), t = j / SH::R(p), r = j % SH::R(p), tg = c * SH::C(p) + t;
+    float x = bias[((int64_t)h * SH::R(p) + r) * SH::N(p) + n];
+    if (tg < p.S) x += ld_act<A>(src, ((((int64_t)b * p.S + tg) * SH::R(p) + r) * p.G + g) * SH::N(p) + n);
     T[j * ld + n] = x;
   }
   __syncthreads();
-  const int half = p.N / 2;
-  for (int e = threadIdx.x; e < p.CR * p.w; e += blockDim.x) {
-    const int j = e / p.w, m = e % p.w, t = j / p.R, tg = c * p.C + t;
-    const float th = tg < p.S ? p.angles[(((int64_t)b * p.S + tg) * p.H + h) * p.w + m] : 0.f;
+  const int half = SH::N(p) / 2;
+  #pragma unroll
+  for (int e = threadIdx.x; e < SH::CR(p) * SH::w(p); e += NT) {
+    const int j = e / SH::w(p), m = e % SH::w(p), t = j / SH::R(p), tg = c * SH::C(p) + t;
+    const float th = tg < p.S ? p.angles[(((int64_t)b * p.S + tg) * p.H + h) * SH::w(p) + m] : 0.f;
     float sn, cs;
     sincosf(th, &sn, &cs);
     const float lo = T[j * ld + m], hi = T[j * ld + half + m];
@@ -226,29 +253,31 @@ __device__ __forceinline__ void load_rotated(const BBParams& p, int b, int h, in
 }
 
 // dPhiO rows [C*R][P] (zero past S) [op document: reduce-O or per rank].
-template <int A>
+template <int A, class SH, int NT>
 __device__ __forceinline__ void load_dphio(const BBParams& p, int b, int h, int c, float* T, int ld) {
-  for (int e = threadIdx.x; e < p.CR * p.P; e += blockDim.x) {
-    const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
+  #pragma unroll
+  for (int e = threadIdx.x; e < SH::CR(p) * SH::P(p); e += NT) {
+    const int j = e / SH::P(p), pp = e % SH::P(p), t = j / SH::R(p), r = j % SH::R(p), tg = c * SH::C(p) + t;
     float x = 0.f;
     if (tg < p.S) {
       if (p.reduced)
-        x = ld_act<A>(p.dout, (((int64_t)b * p.S + tg) * p.H + h) * p.P + pp) * p.mimo_o[((int64_t)h * p.R + r) * p.P + pp];
+        x = ld_act<A>(p.dout, (((int64_t)b * p.S + tg) * p.H + h) * SH::P(p) + pp) * p.mimo_o[((int64_t)h * SH::R(p) + r) * SH::P(p) + pp];
       else
-        x = ld_act<A>(p.dout, ((((int64_t)b * p.S + tg) * p.R + r) * p.H + h) * p.P + pp);
+        x = ld_act<A>(p.dout, ((((int64_t)b * p.S + tg) * SH::R(p) + r) * p.H + h) * SH::P(p) + pp);
     }
     T[j * ld + pp] = x;
   }
 }
 
 // PsiV rows [C*R][P] = v[t,p] * mimo_v[r,p] (zero past S).
-template <int A>
+template <int A, class SH, int NT>
 __device__ __forceinline__ void load_psi(const BBParams& p, int b, int h, int c, float* T, int ld) {
-  for (int e = threadIdx.x; e < p.CR * p.P; e += blockDim.x) {
-    const int j = e / p.P, pp = e % p.P, t = j / p.R, r = j % p.R, tg = c * p.C + t;
+  #pragma unroll
+  for (int e = threadIdx.x; e < SH::CR(p) * SH::P(p); e += NT) {
+    const int j = e / SH::P(p), pp = e % SH::P(p), t = j / SH::R(p), r = j % SH::R(p), tg = c * SH::C(p) + t;
     float x = 0.f;
     if (tg < p.S)
-      x = ld_act<A>(p.v, (((int64_t)b * p.S + tg) * p.H + h) * p.P + pp) * p.mimo_v[((int64_t)h * p.R + r) * p.P + pp];
+      x = ld_act<A>(p.v, (((int64_t)b * p.S + tg) * p.H + h) * SH::P(p) + pp) * p.mimo_v[((int64_t)h * SH::R(p) + r) * SH::P(p) + pp];
     T[j * ld + pp] = x;
   }
 }
@@ -257,43 +286,43 @@ __device__ __forceinline__ void load_psi(const BBParams& p, int b, int h, int c,
 // The 64-wide path (W = false) keeps [64][kLD] tiles and one 64 x 64 output
 // block; the wide path strides its rows by N and P rounded up to 64 (every
 // 4 x 4 read of a block stays inside its row) and walks the output blocks.
-template <int A, bool W>
+template <int A, bool W, class SH>
 __global__ void __launch_bounds__(kT, W ? 1 : 4) seed_kernel(const BBParams p) {  // 64-wide: 4 CTAs per SM
   extern __shared__ float smf[];
-  const int LN = W ? p.sLN : kLD, LP = W ? p.sLP : kLD, rows = W ? p.CR : kMax, TC = W ? kMaxW : kMax;
+  const int LN = W ? p.sLN : kLD, LP = W ? p.sLP : kLD, rows = W ? SH::CR(p) : kMax, TC = W ? kMaxW : kMax;
   float* Qr = smf;
   float* Gp = Qr + rows * LN;
   float* tk = Gp + rows * LP;  // gam, fac, ea, er, valid: 5 x TC
   float* ear = tk + 5 * TC;    // exp(da_cs) per row j = t*R + r
   const int c = blockIdx.x, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-  load_tokens<A>(p, bh, c, tk, tk + TC, tk + 2 * TC, tk + 3 * TC, tk + 4 * TC);
-  load_dphio<A>(p, b, h, c, Gp, LP);
-  load_rotated<A>(p, b, h, c, p.q, p.q_bias, Qr, LN);
+  load_tokens<A, SH, kT>(p, bh, c, tk, tk + TC, tk + 2 * TC, tk + 3 * TC, tk + 4 * TC);
+  load_dphio<A, SH, kT>(p, b, h, c, Gp, LP);
+  load_rotated<A, SH, kT>(p, b, h, c, p.q, p.q_bias, Qr, LN);
   __syncthreads();
   const float* ea = tk + 2 * TC;
-  for (int j = threadIdx.x; j < p.CR; j += blockDim.x) ear[j] = ea[j / p.R];
+  for (int j = threadIdx.x; j < SH::CR(p); j += blockDim.x) ear[j] = ea[j / SH::R(p)];
   __syncthreads();
-  float* dst = p.ws_D + ((int64_t)bh * p.nc + c) * p.N * p.P;
+  float* dst = p.ws_D + ((int64_t)bh * p.nc + c) * SH::N(p) * SH::P(p);
   auto block = [&](int n0, int p0) {  // the 64 x 64 output block at (n0, p0)
     const int i0 = n0 + (threadIdx.x >> 4) * 4, j0 = p0 + (threadIdx.x & 15) * 4;
     float acc[4][4];
     zero4(acc);
-    mm4(acc, i0, j0, p.CR, [=](int n, int i) { return Qr[i * LN + n] * ear[i]; },
+    mm4(acc, i0, j0, SH::CR(p), [=](int n, int i) { return Qr[i * LN + n] * ear[i]; },
         [=](int i, int pp) { return Gp[i * LP + pp]; });
 #pragma unroll
     for (int u = 0; u < 4; u++)
 #pragma unroll
       for (int v = 0; v < 4; v++)
-        if (i0 + u < p.N && j0 + v < p.P) dst[(i0 + u) * p.P + j0 + v] = acc[u][v];
+        if (i0 + u < SH::N(p) && j0 + v < SH::P(p)) dst[(i0 + u) * SH::P(p) + j0 + v] = acc[u][v];
   };
   if constexpr (!W) {
     block(0, 0);
   } else {
-    for (int n0 = 0; n0 < p.N; n0 += 64)
-      for (int p0 = 0; p0 < p.P; p0 += 64) block(n0, p0);
+    for (int n0 = 0; n0 < SH::N(p); n0 += 64)
+      for (int p0 = 0; p0 < SH::P(p); p0 += 64) block(n0, p0);
   }
   if (threadIdx.x == 0) {
-    const int last = min(c * p.C + p.C, p.S) - 1;
+    const int last = min(c * SH::C(p) + SH::C(p), p.S) - 1;
     p.ws_alpha[(int64_t)bh * p.nc + c] = expf(p.da_cs[(int64_t)bh * p.S + last]);
   }
 }
@@ -346,7 +375,7 @@ __device__ __forceinline__ void for_tiles(int rows, int cols, F f) {
 // on the wide path the same tiles in this CTA's global scratch (rows padded
 // to 16 and strides rounded up to 16, so that every fragment read of a
 // 16 x 16 tile stays inside its tile), the small tables in shared memory.
-template <int A, bool WIDE>
+template <int A, bool WIDE, class SH>
 __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, float* smf, float* scr) {
   const int LN = WIDE ? p.LN : kLD, LP = WIDE ? p.LP : kLD, LC = WIDE ? p.LC : kLD;
   const int TC = WIDE ? kMaxW : kMax;
@@ -392,7 +421,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   float* ea = tk + 2 * TC;
   float* er = tk + 3 * TC;
   float* valid = tk + 4 * TC;
-  const int C = p.C, R = p.R, N = p.N, P = p.P, CR = p.CR;
+  const int C = SH::C(p), R = SH::R(p), N = SH::N(p), P = SH::P(p), CR = SH::CR(p);
   float* seg = sm;
   float* qk = sm + C * C;
   float* dqk = qk + C * R * R;
@@ -402,20 +431,21 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   const int ctn = WIDE ? (N + 15) >> 4 : 4, ctp = WIDE ? (P + 15) >> 4 : 4;
 
   // ---- inputs of the chunk
-  load_tokens<A>(p, bh, c, gam, fac, ea, er, valid);
+  load_tokens<A, SH, kTG>(p, bh, c, gam, fac, ea, er, valid);
   for (int e = tid; e < C * C; e += kTG) seg[e] = p.segsum[((int64_t)bh * p.nc + c) * C * C + e];
   for (int e = tid; e < C * R * R; e += kTG) {
     const int tg = c * C + e / (R * R);
     qk[e] = tg < p.S ? ld_act<A>(p.qk, ((int64_t)bh * p.S + tg) * R * R + e % (R * R)) : 0.f;
   }
+#pragma unroll
   for (int e = tid; e < N * P; e += kTG) {
     Hc[(e / P) * LP + e % P] = ld_act<A>(p.states, ((int64_t)bh * p.nc + c) * N * P + e);
     Dn[(e / P) * LP + e % P] = p.ws_D[((int64_t)bh * p.nc + c) * N * P + e];
   }
-  load_psi<A>(p, b, h, c, Ps, LP);
-  load_dphio<A>(p, b, h, c, Gp, LP);
-  load_rotated<A>(p, b, h, c, p.q, p.q_bias, Qr, LN);
-  load_rotated<A>(p, b, h, c, p.k, p.k_bias, Kr, LN);
+  load_psi<A, SH, kTG>(p, b, h, c, Ps, LP);
+  load_dphio<A, SH, kTG>(p, b, h, c, Gp, LP);
+  load_rotated<A, SH, kTG>(p, b, h, c, p.q, p.q_bias, Qr, LN);
+  load_rotated<A, SH, kTG>(p, b, h, c, p.k, p.k_bias, Kr, LN);
   __syncthreads();
   for (int j = tid; j < CR; j += kTG) {
     facr[j] = fac[j / R];
@@ -610,7 +640,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
 
   // ---- rotary post-pass.  Stage the rotary cos / sin of the chunk and
   //      mimo_v in M1, v in M2 (both free now); DANGLES from the rotated rows.
-  const int half = N / 2, W = p.w;
+  const int half = N / 2, W = SH::w(p);
   float* cst = M1;                // cos [C][W]
   float* snt = M1 + C * W;        // sin [C][W]
   float* mvs = M1 + 2 * C * W;    // mimo_v [R][P]
@@ -691,10 +721,10 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
 }
 
 // One chunk per CTA (N, P, C*R <= 64).
-template <int A>
+template <int A, class SH>
 __global__ void __launch_bounds__(kTG, 1) grad_kernel(const BBParams p) {
   extern __shared__ float smf[];
-  grad_chunk<A, false>(p, blockIdx.x, blockIdx.y, smf, nullptr);
+  grad_chunk<A, false, SH>(p, blockIdx.x, blockIdx.y, smf, nullptr);
 }
 
 // Wide shapes: a persistent grid walks the (b*h, chunk) items, each CTA
@@ -705,7 +735,7 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel_wide(const BBParams p) {
   float* scr = p.ws_scr + (int64_t)blockIdx.x * p.scr_floats;
   const int items = p.nc * p.B * p.H;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    grad_chunk<A, true>(p, it % p.nc, it / p.nc, smf, scr);
+    grad_chunk<A, true, ShapeRT>(p, it % p.nc, it / p.nc, smf, scr);
     __syncthreads();  // every read of this item's tiles precedes the next item's loads
   }
 }
@@ -793,13 +823,24 @@ static mmbf_status bb_plan(const mmbf_dims* dims, int64_t chunk_size, int64_t di
 // memory limits are raised once per instantiation).
 template <int A>
 cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
+  // the compile-time shape for BF16 activations on its own shape; run-time extents otherwise
+  const bool fast = A == kBF16 && !p.wide && ShapeFast::matches(p);
+  using SF = ShapeFast;
   static bool smem_set = false;
   if (!smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(seed_kernel<A, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeedSmem);
+    cudaError_t e = cudaFuncSetAttribute(seed_kernel<A, false, ShapeRT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSeedSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grad_kernel<A>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
+      e = cudaFuncSetAttribute(grad_kernel<A, ShapeRT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
+    if constexpr (A == kBF16) {
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(seed_kernel<A, false, SF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeedSmem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(grad_kernel<A, SF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
+    }
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(seed_kernel<A, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeedSmemW);
+      e = cudaFuncSetAttribute(seed_kernel<A, true, ShapeRT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSeedSmemW);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(grad_kernel_wide<A>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmemW);
     if (e != cudaSuccess) return e;
@@ -810,9 +851,14 @@ cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
   g_stage_names_n = 4;
   stage_event(0, 0, st);
   if (p.wide)
-    seed_kernel<A, true><<<dim3(p.nc, BH), kT, seed_smem_wide(p), st>>>(p);
-  else
-    seed_kernel<A, false><<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
+    seed_kernel<A, true, ShapeRT><<<dim3(p.nc, BH), kT, seed_smem_wide(p), st>>>(p);
+  else if constexpr (A == kBF16) {
+    if (fast)
+      seed_kernel<A, false, SF><<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
+    else
+      seed_kernel<A, false, ShapeRT><<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
+  } else
+    seed_kernel<A, false, ShapeRT><<<dim3(p.nc, BH), kT, kSeedSmem, st>>>(p);
   stage_event(0, 1, st);
   stage_event(1, 0, st);
   scan_kernel<<<dim3((p.N * p.P + 127) / 128, BH), 128, 0, st>>>(p);
@@ -820,8 +866,13 @@ cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
   stage_event(2, 0, st);
   if (p.wide)
     grad_kernel_wide<A><<<grad_grid_wide(p), kTG, kGradSmemW, st>>>(p);
-  else
-    grad_kernel<A><<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
+  else if constexpr (A == kBF16) {
+    if (fast)
+      grad_kernel<A, SF><<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
+    else
+      grad_kernel<A, ShapeRT><<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
+  } else
+    grad_kernel<A, ShapeRT><<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
   stage_event(2, 1, st);
   stage_event(3, 0, st);
   reduce_kernel<<<BH, kT, 0, st>>>(p);
