@@ -432,7 +432,9 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
 
   // ---- inputs of the chunk
   load_tokens<A, SH, kTG>(p, bh, c, gam, fac, ea, er, valid);
+  #pragma unroll
   for (int e = tid; e < C * C; e += kTG) seg[e] = p.segsum[((int64_t)bh * p.nc + c) * C * C + e];
+  #pragma unroll
   for (int e = tid; e < C * R * R; e += kTG) {
     const int tg = c * C + e / (R * R);
     qk[e] = tg < p.S ? ld_act<A>(p.qk, ((int64_t)bh * p.S + tg) * R * R + e % (R * R)) : 0.f;
@@ -510,6 +512,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   __syncthreads();
 
   // ---- DSSDA[ti][tj] = sum over the token pair's rank pairs of dA * A
+  #pragma unroll
   for (int e = tid; e < C * C; e += kTG) {
     const int ti = e / C, tj = e % C;
     float s = 0.f;
@@ -520,6 +523,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   }
   __syncthreads();
   // dS = dA exp(segsum) on the causal entries (in place)
+  #pragma unroll
   for (int e = tid; e < CR * CR; e += kTG) {
     const int i = e / CR, j = e % CR;
     M2[i * LC + j] = tok_ok(i, j) ? M2[i * LC + j] * expf(seg[(i / R) * C + j / R]) : 0.f;
@@ -585,6 +589,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   });
   // same-token terms: dot[t,o,r] = dPhiO[(t,o)] . PsiV[(t,r)]; dqk = gamma dot,
   // DGAMMA = sum qk * dot
+  #pragma unroll
   for (int e = tid; e < C * R * R; e += kTG) {
     const int t = e / (R * R), o = (e / R) % R, r = e % R;
     float s = 0.f;
@@ -595,7 +600,9 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   // partial (sum dPhiO * PsiV): block sums in a fixed order
   {
     float s = 0.f, dd = 0.f;
+    #pragma unroll
     for (int e = tid; e < N * P; e += kTG) s = fmaf(Hc[(e / P) * LP + e % P], Dn[(e / P) * LP + e % P], s);
+    #pragma unroll
     for (int e = tid; e < CR * P; e += kTG) dd = fmaf(Gp[(e / P) * LP + e % P], Ps[(e / P) * LP + e % P], dd);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -608,6 +615,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
     }
   }
   __syncthreads();
+  #pragma unroll
   for (int t = tid; t < C; t += kTG) {  // per-token sums
     float s1 = 0.f, s2 = 0.f, s3 = 0.f, g = 0.f;
     for (int r = 0; r < R; r++) {  // the column tiles of the row
@@ -636,6 +644,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
     p.ws_dd[(int64_t)bh * p.nc + c] = dd;
   }
   __syncthreads();
+  #pragma unroll
   for (int e = tid; e < C * R * R; e += kTG) dqk[e] *= gam[e / (R * R)];
 
   // ---- rotary post-pass.  Stage the rotary cos / sin of the chunk and
@@ -645,6 +654,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   float* snt = M1 + C * W;        // sin [C][W]
   float* mvs = M1 + 2 * C * W;    // mimo_v [R][P]
   float* vs = M2;                 // v [C][P]
+  #pragma unroll
   for (int e = tid; e < C * W; e += kTG) {
     const int t = e / W, m = e % W, tg = c * C + t;
     float sn = 0.f, cs = 1.f;
@@ -652,11 +662,14 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
     cst[e] = cs;
     snt[e] = sn;
   }
+  #pragma unroll
   for (int e = tid; e < R * P; e += kTG) mvs[e] = p.mimo_v[(int64_t)h * R * P + e];
+  #pragma unroll
   for (int e = tid; e < C * P; e += kTG) {
     const int t = e / P, pp = e % P, tg = c * C + t;
     vs[e] = tg < p.S ? ld_act<A>(p.v, (((int64_t)b * p.S + tg) * p.H + h) * P + pp) : 0.f;
   }
+  #pragma unroll
   for (int e = tid; e < C * W; e += kTG) {
     const int t = e / W, m = e % W, tg = c * C + t;
     if (tg >= p.S) continue;
@@ -670,6 +683,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   }
   __syncthreads();
   // q_rot, k_rot -> the un-rotated biased rows (transposed rotation, in place)
+  #pragma unroll
   for (int e = tid; e < CR * W; e += kTG) {
     const int j = e / W, m = e % W, t = j / R;
     const float cs = cst[t * W + m], sn = snt[t * W + m];
@@ -682,6 +696,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
     Kr[j * LN + half + m] = -sn * lo + cs * hi;
   }
   // DV and the DMIMO_V partial of the chunk
+  #pragma unroll
   for (int e = tid; e < C * P; e += kTG) {
     const int t = e / P, pp = e % P, tg = c * C + t;
     if (tg >= p.S) continue;
@@ -689,6 +704,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
     for (int r = 0; r < R; r++) s = fmaf(dP[(t * R + r) * LP + pp], mvs[r * P + pp], s);
     store_dqkv(p.DV, (((int64_t)b * p.S + tg) * p.H + h) * P + pp, s, p.dqkv);
   }
+  #pragma unroll
   for (int e = tid; e < R * P; e += kTG) {
     const int r = e / P, pp = e % P;
     float s = 0.f;
@@ -698,6 +714,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   __syncthreads();
   // DQ / DK: the transposed rotation of the rotated-domain gradients plus the
   // diagonal's same-token terms, qk[t,o,x] = qh[(t,o)] . kh[(t,x)]
+  #pragma unroll
   for (int e = tid; e < CR * N; e += kTG) {
     const int j = e / N, n = e % N, t = j / R, r = j % R, tg = c * C + t;
     if (tg >= p.S) continue;
