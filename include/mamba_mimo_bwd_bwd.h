@@ -75,10 +75,11 @@
  *
  * Numerics: every input is widened to FP32 exactly; FP32 throughout (sums,
  * the reverse scan); BF16 / FP16 outputs are the FP32 results rounded to
- * nearest even.  The tile products run
- * on the tensor cores in TF32 with each FP32 operand split into two TF32
- * parts and three products per pair, which keeps FP32-level accuracy.
- * Results are deterministic (no floating-point atomics).
+ * nearest even.  The tile products run on the tensor cores in TF32: each
+ * FP32 operand is split into two TF32 parts by truncation and each pair
+ * takes three products, an error below 3 * 2^-20 relative per product
+ * (FP32-level accuracy).  Results are deterministic (no floating-point
+ * atomics).
  */
 #ifndef MAMBA_MIMO_BWD_BWD_H
 #define MAMBA_MIMO_BWD_BWD_H

@@ -102,16 +102,15 @@ __device__ __forceinline__ void mm4(float (&acc)[TM][TN], int i0, int j0, int K,
   }
 }
 // FP32 products on the tensor cores with FP32-level accuracy: each operand
-// x = hi + lo with hi = tf32(x) and lo = tf32(x - hi) (round to nearest,
-// |x - hi - lo| <= 2^-22 |x|), and a b = hi_a hi_b + hi_a lo_b + lo_a hi_b
-// (the dropped lo_a lo_b is below 2^-21 relative); FP32 accumulation.
+// x = hi + lo + e with hi = x truncated to TF32 (the low 13 mantissa bits
+// cleared), lo = (x - hi) truncated the same way (x - hi is exact), so
+// |e| < 2^-20 |x|; a b = hi_a hi_b + hi_a lo_b + lo_a hi_b, whose error
+// (the dropped lo_a lo_b and the two truncations) is below 3 * 2^-20
+// relative; FP32 accumulation.  Bit operations only (finite inputs).
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  uint32_t h, l;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
-  const float r = x - __uint_as_float(h);
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
-  hi = h;
-  lo = l;
+  constexpr uint32_t kTf32 = 0xffffe000u;
+  hi = __float_as_uint(x) & kTf32;
+  lo = __float_as_uint(x - __uint_as_float(hi)) & kTf32;
 }
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
