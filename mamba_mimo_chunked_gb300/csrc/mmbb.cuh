@@ -421,7 +421,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   float* er = tk + 3 * TC;
   float* valid = tk + 4 * TC;
   const int C = SH::C(p), R = SH::R(p), N = SH::N(p), P = SH::P(p), CR = SH::CR(p);
-  float* seg = sm;
+  float* seg = sm;  // exp(segsum) below the diagonal, 0 elsewhere
   float* qk = sm + C * C;
   float* dqk = qk + C * R * R;
   const int b = bh / p.H, h = bh % p.H;
@@ -432,7 +432,10 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   // ---- inputs of the chunk
   load_tokens<A, SH, kTG>(p, bh, c, gam, fac, ea, er, valid);
   #pragma unroll
-  for (int e = tid; e < C * C; e += kTG) seg[e] = p.segsum[((int64_t)bh * p.nc + c) * C * C + e];
+  for (int e = tid; e < C * C; e += kTG) {  // exp(segsum) below the diagonal, once per chunk
+    const float x = p.segsum[((int64_t)bh * p.nc + c) * C * C + e];
+    seg[e] = (e / C > e % C) ? expf(x) : 0.f;
+  }
   #pragma unroll
   for (int e = tid; e < C * R * R; e += kTG) {
     const int tg = c * C + e / (R * R);
@@ -468,7 +471,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
       for (int e = 0; e < 4; e++) {
         const int i = TC_ROW(fr0, e), j = TC_COL(fc0, nb, e);
         if (i < CR && j < CR)
-          M1[i * LC + j] = tok_ok(i, j) ? acc[nb][e] * facr[j] * expf(seg[(i / R) * C + j / R]) : 0.f;
+          M1[i * LC + j] = tok_ok(i, j) ? acc[nb][e] * facr[j] * seg[(i / R) * C + j / R] : 0.f;
       }
   });
   __syncthreads();
@@ -525,7 +528,7 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   #pragma unroll
   for (int e = tid; e < CR * CR; e += kTG) {
     const int i = e / CR, j = e % CR;
-    M2[i * LC + j] = tok_ok(i, j) ? M2[i * LC + j] * expf(seg[(i / R) * C + j / R]) : 0.f;
+    M2[i * LC + j] = tok_ok(i, j) ? M2[i * LC + j] * seg[(i / R) * C + j / R] : 0.f;
   }
   __syncthreads();
 
