@@ -314,8 +314,23 @@ __global__ void __launch_bounds__(kT, W ? 1 : 4) seed_kernel(const BBParams p) {
       for (int v = 0; v < 4; v++)
         if (i0 + u < SH::N(p) && j0 + v < SH::P(p)) dst[(i0 + u) * SH::P(p) + j0 + v] = acc[u][v];
   };
-  if constexpr (!W) {
-    block(0, 0);
+  if constexpr (!W) {  // the 64 x 64 block as 16 x 16 tiles on the tensor cores, two per warp
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int t = warp; t < 16; t += kT / 32) {
+      const int r0 = (t >> 2) * 16, c0 = (t & 3) * 16;
+      float acc[2][4];
+      zero_tc(acc);
+      mm_tc(acc, r0, c0, SH::CR(p), [=](int n, int i) { return Qr[i * LN + n] * ear[i]; },
+            [=](int i, int pp) { return Gp[i * LP + pp]; });
+#pragma unroll
+      for (int nb = 0; nb < 2; nb++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const int n = TC_ROW(r0, e), pp = TC_COL(c0, nb, e);
+          if (n < SH::N(p) && pp < SH::P(p)) dst[n * SH::P(p) + pp] = acc[nb][e];
+        }
+    }
   } else {
     for (int n0 = 0; n0 < SH::N(p); n0 += 64)
       for (int p0 = 0; p0 < SH::P(p); p0 += 64) block(n0, p0);
