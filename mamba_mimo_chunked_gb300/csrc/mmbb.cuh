@@ -860,8 +860,9 @@ cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
   // the compile-time shape for BF16 activations on its own shape; run-time extents otherwise
   const bool fast = A == kBF16 && !p.wide && ShapeFast::matches(p);
   using SF = ShapeFast;
-  static bool smem_set = false;
-  if (!smem_set) {
+  static bool smem_set[kMaxDevices + 1];  // per device: function attributes are
+  const int dev = device_slot();
+  if (!smem_set[dev] || dev == kMaxDevices) {
     cudaError_t e = cudaFuncSetAttribute(seed_kernel<A, false, ShapeRT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSeedSmem);
     if (e == cudaSuccess)
@@ -878,7 +879,7 @@ cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(grad_kernel_wide<A>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmemW);
     if (e != cudaSuccess) return e;
-    smem_set = true;
+    smem_set[dev] = true;
   }
   const int BH = p.B * p.H;
   g_stage_names = kBBStageNames;

@@ -851,7 +851,20 @@ static void stage_event(int i, int which, cudaStream_t s) {
   }
 }
 
-// cudaFuncSetAttribute once per kernel and size (kept out of stream capture).
+// Function attributes are per device: caches of them are kept per device
+// ordinal, the last slot standing for any device past the table (never
+// cached there: its value is reset on every use).
+constexpr int kMaxDevices = 16;
+static int device_slot() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = 0;
+  }
+  return (dev >= 0 && dev < kMaxDevices) ? dev : kMaxDevices;
+}
+
+// cudaFuncSetAttribute once per kernel, size and device (kept out of stream capture).
 template <typename K>
 static cudaError_t ensure_smem(K kern, size_t smem, int* cached) {
   if ((int)smem <= *cached) return cudaSuccess;
@@ -907,18 +920,22 @@ static size_t fast_state_smem(const Params& p) {
   return fast::smem_layout<StateCfg<K>>(false, p.reduced, p.has_z).total;
 }
 
-// Largest dynamic shared memory each fast kernel has been opened for.  The
-// limit is only ever raised (a lower request must never shrink it, or a later
-// launch with a larger layout would fail).
+// Largest dynamic shared memory each fast kernel has been opened for on the
+// current device.  The limit is only ever raised (a lower request must never
+// shrink it, or a later launch with a larger layout would fail).
 template <class K, int MODE = -1>
 static int& fast_out_smem_set() {
-  static int v = 48 * 1024;
-  return v;
+  static int v[kMaxDevices + 1];
+  const int d = device_slot();
+  if (d == kMaxDevices) v[d] = 0;
+  return v[d];
 }
 template <class K>
 static int& fast_state_smem_set() {
-  static int v = 48 * 1024;
-  return v;
+  static int v[kMaxDevices + 1];
+  const int d = device_slot();
+  if (d == kMaxDevices) v[d] = 0;
+  return v[d];
 }
 
 // CTAs of `kern` (NT threads, `smem` dynamic bytes, `tmem_cols` tensor-memory
