@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(128) scan_kernel(const BBParams p) {
   if (e >= NP) return;
   float* base = p.ws_D + (int64_t)bh * p.nc * NP + e;
   const float* al = p.ws_alpha + (int64_t)bh * p.nc;
-  constexpr int GRP = 16;
+  constexpr int GRP = 32;  // chunks whose loads are in flight at once
   float acc = 0.f;
   for (int c1 = p.nc - 1; c1 >= 0; c1 -= GRP) {
     float x[GRP], a[GRP];
@@ -774,18 +774,44 @@ __global__ void __launch_bounds__(kTG, 1) grad_kernel_wide(const BBParams p) {
   }
 }
 
-// ---- 4. DMIMO_V and DD: the chunks' partials in chunk order
-__global__ void __launch_bounds__(kT) reduce_kernel(const BBParams p) {
-  const int bh = blockIdx.x;
-  for (int e = threadIdx.x; e < p.R * p.P; e += kT) {
+// ---- 4. DMIMO_V and DD: the chunks' partials in a fixed order (each of
+//      kRG thread groups sums the chunks c = g (mod kRG) in chunk order, then
+//      the group sums are added in group order: deterministic)
+constexpr int kRG = 4;              // thread groups of the reduce kernel
+constexpr int kTR = kRG * kT;       // its threads
+__global__ void __launch_bounds__(kTR) reduce_kernel(const BBParams p) {
+  __shared__ float part[kRG][kT];
+  __shared__ float dpart[kTR / 32];
+  const int bh = blockIdx.x, grp = threadIdx.x / kT, lt = threadIdx.x % kT;
+  for (int e0 = 0; e0 < p.R * p.P; e0 += kT) {
+    const int e = e0 + lt;
     float s = 0.f;
-    for (int c = 0; c < p.nc; c++) s += p.ws_mv[((int64_t)bh * p.nc + c) * p.R * p.P + e];
-    p.DMIMO_V[(int64_t)bh * p.R * p.P + e] = s;
+    if (e < p.R * p.P) {
+#pragma unroll 8
+      for (int c = grp; c < p.nc; c += kRG) s += p.ws_mv[((int64_t)bh * p.nc + c) * p.R * p.P + e];
+    }
+    part[grp][lt] = s;
+    __syncthreads();
+    if (grp == 0 && e < p.R * p.P) {
+      float t = part[0][lt];
+#pragma unroll
+      for (int g = 1; g < kRG; g++) t += part[g][lt];
+      p.DMIMO_V[(int64_t)bh * p.R * p.P + e] = t;
+    }
+    __syncthreads();
   }
-  if (p.has_d && threadIdx.x == 0) {
+  if (p.has_d) {  // each thread a strided share of the chunks, then warp and block sums in a fixed order
     float s = 0.f;
-    for (int c = 0; c < p.nc; c++) s += p.ws_dd[(int64_t)bh * p.nc + c];
-    p.DD[bh] = s;
+    for (int c = threadIdx.x; c < p.nc; c += kTR) s += p.ws_dd[(int64_t)bh * p.nc + c];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) dpart[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+      for (int w = 0; w < kTR / 32; w++) t += dpart[w];
+      p.DD[bh] = t;
+    }
   }
 }
 
@@ -910,7 +936,7 @@ cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
     grad_kernel<A, ShapeRT><<<dim3(p.nc, BH), kTG, kGradSmem, st>>>(p);
   stage_event(2, 1, st);
   stage_event(3, 0, st);
-  reduce_kernel<<<BH, kT, 0, st>>>(p);
+  reduce_kernel<<<BH, kTR, 0, st>>>(p);
   stage_event(3, 1, st);
   return cudaSuccess;
 }
