@@ -621,14 +621,13 @@ __device__ __forceinline__ void add_bias(uint32_t (&f)[K::NKT][4], const uint16_
 }
 
 // Rotary on the pairs (m, N/2 + m), m < W: both partners sit in the same
-// register slot of k tiles kt and kt + NKT/2.  FP32 with the reference's
-// operation order (products, then sum), each result rounded to BF16.
+// register slot of k tiles kt and kt + NKT/2.  FP32, one product of each
+// sum contracted with the addition into an FMA, each result rounded to BF16.
 template <class K>
 __device__ __forceinline__ void rotate_regs(uint32_t& lo, uint32_t& hi, float2 cs, float2 sn) {
   const float2 a = unpack2(lo), x = unpack2(hi);
-  const float2 sx = __fmul2_rn(sn, x);
-  lo = pack2(__fadd2_rn(__fmul2_rn(cs, a), make_float2(-sx.x, -sx.y)));
-  hi = pack2(__fadd2_rn(__fmul2_rn(sn, a), __fmul2_rn(cs, x)));
+  lo = pack2(__ffma2_rn(cs, a, __fmul2_rn(make_float2(-sn.x, -sn.y), x)));
+  hi = pack2(__ffma2_rn(sn, a, __fmul2_rn(cs, x)));
 }
 // The same rotary with each thread taking the sines and cosines it needs from
 // the chunk's raw angles [C][W] (no shared table, no barrier).  For R = 4 and
@@ -1654,6 +1653,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
             if (HD) x = __ffma2_rn(make_float2(dval, dval), unpack2(pso[k]), x);
             const uint32_t ob = pack2(x);
             float2 pz = make_float2(0.f, 0.f), sg = make_float2(0.5f, 0.5f), mz = make_float2(0.f, 0.f);
+            float2 silu = make_float2(0.f, 0.f);  // pz * sigmoid(pz)
             if (HZ) {
               mz = mzp[(o * NMT + mt) * 8 + g];
               pz = __fmul2_rn(z2, mz);
@@ -1661,12 +1661,13 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
               const float2 den = __fadd2_rn(make_float2(ex2_approx(tq.x), ex2_approx(tq.y)),
                                             make_float2(1.f, 1.f));
               sg = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+              silu = __fmul2_rn(pz, sg);
             }
             uint32_t preb = 0u;
             if (RED) {  // dmimo_o partials: out * dout (exact) * silu(pz)
               if (HZ) {
                 const float2 od = fma_bf2_f32(ob, dob, make_float2(-0.f, -0.f));
-                cdmo[sl] = __ffma2_rn(od, __fmul2_rn(pz, sg), cdmo[sl]);
+                cdmo[sl] = __ffma2_rn(od, silu, cdmo[sl]);
                 preb = bmul2(bmul2(dob, mop[(o * NMT + mt) * 8 + g]), ob);
               } else {
                 cdmo[sl] = fma_bf2_f32(ob, dob, cdmo[sl]);
@@ -1679,7 +1680,7 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
             }
             if (WY) {  // y: out silu(pz), weighted by mimo_o and summed over ranks, or per rank
               const float2 of = unpack2(ob);
-              const float2 og = HZ ? __fmul2_rn(of, __fmul2_rn(pz, sg)) : of;
+              const float2 og = HZ ? __fmul2_rn(of, silu) : of;
               if (RED) {
                 yacc = __ffma2_rn(mof[(o * NMT + mt) * 8 + g], og, yacc);
               } else {
@@ -1699,9 +1700,9 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 :
             prodz[k] = make_float2(0.f, 0.f);
             if (HZ) {
               const float2 pre = unpack2(preb);
+              // sigmoid(pz) (1 + pz (1 - sigmoid(pz))) = sigmoid + silu (1 - sigmoid)
               const float2 om = __fadd2_rn(make_float2(1.f, 1.f), make_float2(-sg.x, -sg.y));
-              const float2 gg = __ffma2_rn(pz, om, make_float2(1.f, 1.f));
-              const float2 gz = __fmul2_rn(__fmul2_rn(pre, sg), gg);
+              const float2 gz = __fmul2_rn(pre, __ffma2_rn(silu, om, sg));
               cdmz[sl] = __ffma2_rn(gz, z2, cdmz[sl]);
               prodz[k] = __fmul2_rn(gz, mz);
             }
