@@ -1,11 +1,14 @@
-"""GB300 (sm_103a) implementation of the first backward stage of the Mamba-3
-MIMO chunked scan, ``mamba_mimo_bwd_fwd``.
+"""GB300 (sm_103a) implementation of the backward stages of the Mamba-3 MIMO
+chunked scan: ``mamba_mimo_bwd_fwd`` (first stage; ``mamba_mimo_bwd_fwd_with_y``
+also writes the forward output y) and ``mamba_mimo_bwd_bwd`` (second stage,
+the reverse scan and its 12 gradients).
 
 This module is a thin binding over the C ABI in
-``include/mamba_mimo_bwd_fwd.h`` (``libmmbf.so``): it checks shapes, dtypes
-and devices the way the PR #125 page's ``_validate_inputs`` does (same
-exception types), allocates outputs and workspace with torch, and passes raw
-device pointers and the current CUDA stream.  Every step of the computation
+``include/mamba_mimo_bwd_fwd.h`` and ``include/mamba_mimo_bwd_bwd.h``
+(``libmmbf.so``): it checks shapes, dtypes and devices the way the PR #125
+page's ``_validate_inputs`` does (same exception types), allocates outputs
+and workspace with torch, and passes raw device pointers and the current
+CUDA stream.  Every step of the computation
 runs in the library's CUDA kernels; there is no fallback of any kind.  If the
 library is missing or cannot load, calls raise.
 """
@@ -21,8 +24,8 @@ import torch
 
 from . import _build
 
-__all__ = ["MambaMimoBwdFwdOutputs", "mamba_mimo_bwd_fwd", "workspace_size", "load_library",
-           "last_launch_count", "build", "mamba_mimo_bwd_bwd", "bwd_bwd_workspace_size",
+__all__ = ["MambaMimoBwdFwdOutputs", "mamba_mimo_bwd_fwd", "mamba_mimo_bwd_fwd_with_y", "workspace_size",
+           "load_library", "last_launch_count", "build", "mamba_mimo_bwd_bwd", "bwd_bwd_workspace_size",
            "BWD_BWD_OUTPUTS"]
 
 build = _build.build
