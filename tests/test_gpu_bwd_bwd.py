@@ -175,6 +175,29 @@ def test_lower_precision_dq_dk_dv_are_the_rounded_fp32_results(case, act, out):
         assert err < (2.0 ** -8 if want_dt == torch.bfloat16 else 2.0 ** -11), f"{name}: relative RMS {err:.3e}"
 
 
+def test_explicit_workspace_reuse_and_non_contiguous_inputs():
+    args, kw = _problem(B=1, S=40, H=2, G=1, R=4, N=64, P=64, C=16, seed=41, caches="random")
+    dev = torch.device("cuda:0")
+    base = _run_gpu(args, kw)
+    B, S, R, G, N = args[1].shape
+    H, P = args[3].shape[2], args[3].shape[3]
+    nbytes = mm.bwd_bwd_workspace_size(B, S, H, G, R, N, P, 16, 4)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dargs = [a.to(dev) for a in args]
+    # the same values through non-contiguous views (the binding makes them dense)
+    dargs[1] = dargs[1].transpose(1, 2).contiguous().transpose(1, 2)
+    dargs[3] = dargs[3].transpose(1, 2).contiguous().transpose(1, 2)
+    assert not dargs[1].is_contiguous() and not dargs[3].is_contiguous()
+    dkw = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
+    for _ in range(2):  # one workspace, two calls
+        g = mm.mamba_mimo_bwd_bwd(*dargs, output_dtype=torch.float32, workspace=ws, **dkw)
+        torch.cuda.synchronize(dev)
+        for name in bb.OUTPUT_NAMES:
+            assert torch.equal(g[name], base[name]), name
+    with pytest.raises(ValueError):
+        mm.mamba_mimo_bwd_bwd(*dargs, output_dtype=torch.float32, workspace=ws[: nbytes - 256], **dkw)
+
+
 def test_outside_the_envelope_raises():
     args, kw = _problem(B=1, S=16, H=1, G=1, R=2, N=512, P=16, C=16, seed=1, caches="random")
     with pytest.raises(NotImplementedError):
