@@ -15,11 +15,18 @@
 //                               D_{c+1}, the gradient of the state leaving it;
 //   grad_kernel   (chunk, b*h)  every gradient of the chunk from its inputs,
 //                               the state entering it (the states cache) and
-//                               D_{c+1}: 9 products of at most 64 x 64 x 64
-//                               of FP32 tiles in shared memory, on the tensor
-//                               cores (TF32, three passes per FP32 product);
-//   reduce_kernel (b*h)         DMIMO_V and DD: the chunks' partial sums in
-//                               chunk order.
+//                               D_{c+1}: 9 products of FP32 tiles on the
+//                               tensor cores (TF32, three passes per FP32
+//                               product).  N, P, C*R <= 64: tiles in shared
+//                               memory, one chunk per CTA; larger shapes:
+//                               grad_kernel_wide, a persistent grid whose
+//                               tiles sit in a per-CTA slice of the workspace;
+//   reduce_kernel (b*h)         DMIMO_V and DD: the chunks' partial sums in a
+//                               fixed order.
+// The kernels that read activations are instantiated per activation dtype
+// (FP32, BF16, FP16) and per shape policy: run-time extents, or compile-time
+// extents for BF16 on N = P = 64, R = 4, C = 16 (shifts instead of the
+// divisions that split flat element indices).
 // FP32-level accuracy throughout, deterministic (no floating-point atomics).
 
 #include <cuda_fp16.h>
