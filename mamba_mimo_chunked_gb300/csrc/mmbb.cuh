@@ -189,6 +189,7 @@ __device__ __forceinline__ void zero4(float (&acc)[TM][TN]) {
 // time for one shape (ShapeCT: the divisions and remainders of the element
 // loops by them become shifts and masks).
 struct ShapeRT {
+  static constexpr bool kVec = false;  // element-wise loads
   static __device__ __forceinline__ int N(const BBParams& p) { return p.N; }
   static __device__ __forceinline__ int P(const BBParams& p) { return p.P; }
   static __device__ __forceinline__ int R(const BBParams& p) { return p.R; }
@@ -196,8 +197,12 @@ struct ShapeRT {
   static __device__ __forceinline__ int CR(const BBParams& p) { return p.CR; }
   static __device__ __forceinline__ int w(const BBParams& p) { return p.w; }
 };
-template <int N_, int P_, int R_, int C_, int W_>
+template <int N_, int P_, int R_, int C_, int W_, bool VEC_>
 struct ShapeCT {
+  // VEC_: BF16 activations with every activation, bias and mimo pointer
+  // 16-byte aligned; rows of 8 elements move with one 16-byte load
+  static constexpr bool kVec = VEC_;
+  static_assert(!VEC_ || (N_ % 8 == 0 && P_ % 8 == 0), "vector loads take rows of 8 elements");
   static __device__ __forceinline__ int N(const BBParams&) { return N_; }
   static __device__ __forceinline__ int P(const BBParams&) { return P_; }
   static __device__ __forceinline__ int R(const BBParams&) { return R_; }
@@ -206,8 +211,29 @@ struct ShapeCT {
   static __device__ __forceinline__ int w(const BBParams&) { return W_; }
   static bool matches(const BBParams& p) { return p.N == N_ && p.P == P_ && p.R == R_ && p.C == C_ && p.w == W_; }
 };
-// the shape with its own instantiation: N = P = 64, R = 4, C = 16, rotary width 16
-using ShapeFast = ShapeCT<64, 64, 4, 16, 16>;
+// the shape with its own instantiation: N = P = 64, R = 4, C = 16, rotary
+// width 16, BF16 activations on 16-byte aligned pointers
+using ShapeFast = ShapeCT<64, 64, 4, 16, 16, true>;
+
+// 8 BF16 values at element i of `base` (16-byte aligned) widened to FP32, and
+// 8 FP32 values to / from 16-byte aligned memory.
+__device__ __forceinline__ void ld8_bf16(const void* base, int64_t i, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + i);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int q = 0; q < 4; q++) {
+    f[2 * q] = bf_lo(w[q]);
+    f[2 * q + 1] = bf_hi(w[q]);
+  }
+}
+__device__ __forceinline__ void ld8_f32(const float* base, int64_t i, float (&f)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(base + i), b = *reinterpret_cast<const float4*>(base + i + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void st8_f32(float* dst, const float (&f)[8]) {
+  *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
+  *reinterpret_cast<float4*>(dst + 4) = make_float4(f[4], f[5], f[6], f[7]);
+}
 
 // Token scalars of chunk c (reading of the op header): gamma, factor,
 // exp(da_cs), exp(da_cs_rev), and whether the token is inside S.
@@ -237,12 +263,28 @@ template <int A, class SH, int NT>
 __device__ __forceinline__ void load_rotated(const BBParams& p, int b, int h, int c, const void* src, const float* bias,
                              float* T, int ld) {
   const int g = h / (p.H / p.G);
-  #pragma unroll
-  for (int e = threadIdx.x; e < SH::CR(p) * SH::N(p); e += NT) {
-    const int j = e / SH::N(p), n = e % SH::N(p), t = j / SH::R(p), r = j % SH::R(p), tg = c * SH::C(p) + t;
-    float x = bias[((int64_t)h * SH::R(p) + r) * SH::N(p) + n];
-    if (tg < p.S) x += ld_act<A>(src, ((((int64_t)b * p.S + tg) * SH::R(p) + r) * p.G + g) * SH::N(p) + n);
-    T[j * ld + n] = x;
+  if constexpr (SH::kVec) {  // 8 consecutive n of one row per step
+#pragma unroll
+    for (int e8 = threadIdx.x; e8 < SH::CR(p) * SH::N(p) / 8; e8 += NT) {
+      const int e = e8 * 8, j = e / SH::N(p), n = e % SH::N(p), t = j / SH::R(p), r = j % SH::R(p),
+                tg = c * SH::C(p) + t;
+      float x[8], y[8];
+      ld8_f32(bias, ((int64_t)h * SH::R(p) + r) * SH::N(p) + n, x);
+      if (tg < p.S) {
+        ld8_bf16(src, ((((int64_t)b * p.S + tg) * SH::R(p) + r) * p.G + g) * SH::N(p) + n, y);
+#pragma unroll
+        for (int q = 0; q < 8; q++) x[q] += y[q];
+      }
+      st8_f32(T + j * ld + n, x);
+    }
+  } else {
+#pragma unroll
+    for (int e = threadIdx.x; e < SH::CR(p) * SH::N(p); e += NT) {
+      const int j = e / SH::N(p), n = e % SH::N(p), t = j / SH::R(p), r = j % SH::R(p), tg = c * SH::C(p) + t;
+      float x = bias[((int64_t)h * SH::R(p) + r) * SH::N(p) + n];
+      if (tg < p.S) x += ld_act<A>(src, ((((int64_t)b * p.S + tg) * SH::R(p) + r) * p.G + g) * SH::N(p) + n);
+      T[j * ld + n] = x;
+    }
   }
   __syncthreads();
   const int half = SH::N(p) / 2;
@@ -261,30 +303,68 @@ __device__ __forceinline__ void load_rotated(const BBParams& p, int b, int h, in
 // dPhiO rows [C*R][P] (zero past S) [op document: reduce-O or per rank].
 template <int A, class SH, int NT>
 __device__ __forceinline__ void load_dphio(const BBParams& p, int b, int h, int c, float* T, int ld) {
-  #pragma unroll
-  for (int e = threadIdx.x; e < SH::CR(p) * SH::P(p); e += NT) {
-    const int j = e / SH::P(p), pp = e % SH::P(p), t = j / SH::R(p), r = j % SH::R(p), tg = c * SH::C(p) + t;
-    float x = 0.f;
-    if (tg < p.S) {
-      if (p.reduced)
-        x = ld_act<A>(p.dout, (((int64_t)b * p.S + tg) * p.H + h) * SH::P(p) + pp) * p.mimo_o[((int64_t)h * SH::R(p) + r) * SH::P(p) + pp];
-      else
-        x = ld_act<A>(p.dout, ((((int64_t)b * p.S + tg) * SH::R(p) + r) * p.H + h) * SH::P(p) + pp);
+  if constexpr (SH::kVec) {  // 8 consecutive p of one row per step
+#pragma unroll
+    for (int e8 = threadIdx.x; e8 < SH::CR(p) * SH::P(p) / 8; e8 += NT) {
+      const int e = e8 * 8, j = e / SH::P(p), pp = e % SH::P(p), t = j / SH::R(p), r = j % SH::R(p),
+                tg = c * SH::C(p) + t;
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (tg < p.S) {
+        if (p.reduced) {
+          float m[8];
+          ld8_bf16(p.dout, (((int64_t)b * p.S + tg) * p.H + h) * SH::P(p) + pp, x);
+          ld8_f32(p.mimo_o, ((int64_t)h * SH::R(p) + r) * SH::P(p) + pp, m);
+#pragma unroll
+          for (int q = 0; q < 8; q++) x[q] *= m[q];
+        } else {
+          ld8_bf16(p.dout, ((((int64_t)b * p.S + tg) * SH::R(p) + r) * p.H + h) * SH::P(p) + pp, x);
+        }
+      }
+      st8_f32(T + j * ld + pp, x);
     }
-    T[j * ld + pp] = x;
+  } else {
+#pragma unroll
+    for (int e = threadIdx.x; e < SH::CR(p) * SH::P(p); e += NT) {
+      const int j = e / SH::P(p), pp = e % SH::P(p), t = j / SH::R(p), r = j % SH::R(p), tg = c * SH::C(p) + t;
+      float x = 0.f;
+      if (tg < p.S) {
+        if (p.reduced)
+          x = ld_act<A>(p.dout, (((int64_t)b * p.S + tg) * p.H + h) * SH::P(p) + pp) * p.mimo_o[((int64_t)h * SH::R(p) + r) * SH::P(p) + pp];
+        else
+          x = ld_act<A>(p.dout, ((((int64_t)b * p.S + tg) * SH::R(p) + r) * p.H + h) * SH::P(p) + pp);
+      }
+      T[j * ld + pp] = x;
+    }
   }
 }
 
 // PsiV rows [C*R][P] = v[t,p] * mimo_v[r,p] (zero past S).
 template <int A, class SH, int NT>
 __device__ __forceinline__ void load_psi(const BBParams& p, int b, int h, int c, float* T, int ld) {
-  #pragma unroll
-  for (int e = threadIdx.x; e < SH::CR(p) * SH::P(p); e += NT) {
-    const int j = e / SH::P(p), pp = e % SH::P(p), t = j / SH::R(p), r = j % SH::R(p), tg = c * SH::C(p) + t;
-    float x = 0.f;
-    if (tg < p.S)
-      x = ld_act<A>(p.v, (((int64_t)b * p.S + tg) * p.H + h) * SH::P(p) + pp) * p.mimo_v[((int64_t)h * SH::R(p) + r) * SH::P(p) + pp];
-    T[j * ld + pp] = x;
+  if constexpr (SH::kVec) {  // 8 consecutive p of one row per step
+#pragma unroll
+    for (int e8 = threadIdx.x; e8 < SH::CR(p) * SH::P(p) / 8; e8 += NT) {
+      const int e = e8 * 8, j = e / SH::P(p), pp = e % SH::P(p), t = j / SH::R(p), r = j % SH::R(p),
+                tg = c * SH::C(p) + t;
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (tg < p.S) {
+        float m[8];
+        ld8_bf16(p.v, (((int64_t)b * p.S + tg) * p.H + h) * SH::P(p) + pp, x);
+        ld8_f32(p.mimo_v, ((int64_t)h * SH::R(p) + r) * SH::P(p) + pp, m);
+#pragma unroll
+        for (int q = 0; q < 8; q++) x[q] *= m[q];
+      }
+      st8_f32(T + j * ld + pp, x);
+    }
+  } else {
+#pragma unroll
+    for (int e = threadIdx.x; e < SH::CR(p) * SH::P(p); e += NT) {
+      const int j = e / SH::P(p), pp = e % SH::P(p), t = j / SH::R(p), r = j % SH::R(p), tg = c * SH::C(p) + t;
+      float x = 0.f;
+      if (tg < p.S)
+        x = ld_act<A>(p.v, (((int64_t)b * p.S + tg) * p.H + h) * SH::P(p) + pp) * p.mimo_v[((int64_t)h * SH::R(p) + r) * SH::P(p) + pp];
+      T[j * ld + pp] = x;
+    }
   }
 }
 
@@ -463,10 +543,22 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
     const int tg = c * C + e / (R * R);
     qk[e] = tg < p.S ? ld_act<A>(p.qk, ((int64_t)bh * p.S + tg) * R * R + e % (R * R)) : 0.f;
   }
+  if constexpr (SH::kVec) {  // 8 consecutive p of one state row per step
 #pragma unroll
-  for (int e = tid; e < N * P; e += kTG) {
-    Hc[(e / P) * LP + e % P] = ld_act<A>(p.states, ((int64_t)bh * p.nc + c) * N * P + e);
-    Dn[(e / P) * LP + e % P] = p.ws_D[((int64_t)bh * p.nc + c) * N * P + e];
+    for (int e8 = tid; e8 < N * P / 8; e8 += kTG) {
+      const int e = e8 * 8;
+      float x[8];
+      ld8_bf16(p.states, ((int64_t)bh * p.nc + c) * N * P + e, x);
+      st8_f32(Hc + (e / P) * LP + e % P, x);
+      ld8_f32(p.ws_D, ((int64_t)bh * p.nc + c) * N * P + e, x);
+      st8_f32(Dn + (e / P) * LP + e % P, x);
+    }
+  } else {
+#pragma unroll
+    for (int e = tid; e < N * P; e += kTG) {
+      Hc[(e / P) * LP + e % P] = ld_act<A>(p.states, ((int64_t)bh * p.nc + c) * N * P + e);
+      Dn[(e / P) * LP + e % P] = p.ws_D[((int64_t)bh * p.nc + c) * N * P + e];
+    }
   }
   load_psi<A, SH, kTG>(p, b, h, c, Ps, LP);
   load_dphio<A, SH, kTG>(p, b, h, c, Gp, LP);
@@ -891,7 +983,10 @@ static mmbf_status bb_plan(const mmbf_dims* dims, int64_t chunk_size, int64_t di
 template <int A>
 cudaError_t launch_bb(const BBParams& p, cudaStream_t st) {
   // the compile-time shape for BF16 activations on its own shape; run-time extents otherwise
-  const bool fast = A == kBF16 && !p.wide && ShapeFast::matches(p);
+  auto a16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+  const bool fast = A == kBF16 && !p.wide && ShapeFast::matches(p) && a16(p.q) && a16(p.k) && a16(p.v) &&
+                    a16(p.dout) && a16(p.states) && a16(p.q_bias) && a16(p.k_bias) && a16(p.mimo_v) &&
+                    (!p.reduced || a16(p.mimo_o));
   using SF = ShapeFast;
   static bool smem_set[kMaxDevices + 1];  // per device: function attributes are
   const int dev = device_slot();

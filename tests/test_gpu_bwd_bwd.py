@@ -198,6 +198,25 @@ def test_explicit_workspace_reuse_and_non_contiguous_inputs():
         mm.mamba_mimo_bwd_bwd(*dargs, output_dtype=torch.float32, workspace=ws[: nbytes - 256], **dkw)
 
 
+def test_unaligned_activation_takes_the_element_wise_loads():
+    # q 4-byte aligned but not 16-byte aligned (a valid ABI call): the
+    # 16-byte vector loads of the timed-shape instantiation must not be used
+    args, kw = _problem(B=1, S=40, H=2, G=1, R=4, N=64, P=64, C=16, seed=43)
+    want = bb.bwd_bwd(*args, **kw)
+    dev = torch.device("cuda:0")
+    q = args[1].to(dev)
+    buf = torch.empty(q.numel() + 2, dtype=q.dtype, device=dev)
+    buf[2:].copy_(q.flatten())
+    q_off = buf[2:].view(q.shape)
+    assert q_off.data_ptr() % 16 == 4
+    dargs = [a.to(dev) for a in args]
+    dargs[1] = q_off
+    g = mm.mamba_mimo_bwd_bwd(*dargs, output_dtype=torch.float32,
+                              **{k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in kw.items()})
+    torch.cuda.synchronize(dev)
+    _compare(g, want)
+
+
 def test_outside_the_envelope_raises():
     args, kw = _problem(B=1, S=16, H=1, G=1, R=2, N=512, P=16, C=16, seed=1, caches="random")
     with pytest.raises(NotImplementedError):
