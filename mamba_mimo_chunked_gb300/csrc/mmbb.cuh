@@ -389,18 +389,6 @@ __global__ void __launch_bounds__(kT, W ? 1 : 4) seed_kernel(const BBParams p) {
   for (int j = threadIdx.x; j < SH::CR(p); j += blockDim.x) ear[j] = ea[j / SH::R(p)];
   __syncthreads();
   float* dst = p.ws_D + ((int64_t)bh * p.nc + c) * SH::N(p) * SH::P(p);
-  auto block = [&](int n0, int p0) {  // the 64 x 64 output block at (n0, p0)
-    const int i0 = n0 + (threadIdx.x >> 4) * 4, j0 = p0 + (threadIdx.x & 15) * 4;
-    float acc[4][4];
-    zero4(acc);
-    mm4(acc, i0, j0, SH::CR(p), [=](int n, int i) { return Qr[i * LN + n] * ear[i]; },
-        [=](int i, int pp) { return Gp[i * LP + pp]; });
-#pragma unroll
-    for (int u = 0; u < 4; u++)
-#pragma unroll
-      for (int v = 0; v < 4; v++)
-        if (i0 + u < SH::N(p) && j0 + v < SH::P(p)) dst[(i0 + u) * SH::P(p) + j0 + v] = acc[u][v];
-  };
   if constexpr (!W) {  // the 64 x 64 block as 16 x 16 tiles on the tensor cores, two per warp
     const int warp = threadIdx.x >> 5;
 #pragma unroll
@@ -418,9 +406,20 @@ __global__ void __launch_bounds__(kT, W ? 1 : 4) seed_kernel(const BBParams p) {
           if (n < SH::N(p) && pp < SH::P(p)) dst[n * SH::P(p) + pp] = acc[nb][e];
         }
     }
-  } else {
+  } else {  // FP32 FMAs, 4 x 4 outputs per thread, over the 64 x 64 output blocks
     for (int n0 = 0; n0 < SH::N(p); n0 += 64)
-      for (int p0 = 0; p0 < SH::P(p); p0 += 64) block(n0, p0);
+      for (int p0 = 0; p0 < SH::P(p); p0 += 64) {
+        const int i0 = n0 + (threadIdx.x >> 4) * 4, j0 = p0 + (threadIdx.x & 15) * 4;
+        float acc[4][4];
+        zero4(acc);
+        mm4(acc, i0, j0, SH::CR(p), [=](int n, int i) { return Qr[i * LN + n] * ear[i]; },
+            [=](int i, int pp) { return Gp[i * LP + pp]; });
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+#pragma unroll
+          for (int v = 0; v < 4; v++)
+            if (i0 + u < SH::N(p) && j0 + v < SH::P(p)) dst[(i0 + u) * SH::P(p) + j0 + v] = acc[u][v];
+      }
   }
   if (threadIdx.x == 0) {
     const int last = min(c * SH::C(p) + SH::C(p), p.S) - 1;
