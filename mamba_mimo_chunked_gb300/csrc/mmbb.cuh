@@ -865,9 +865,9 @@ template <int A>
 __global__ void __launch_bounds__(kTG, 1) grad_kernel_wide(const BBParams p) {
   extern __shared__ float smf[];
   float* scr = p.ws_scr + (int64_t)blockIdx.x * p.scr_floats;
-  const int items = p.nc * p.B * p.H;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    grad_chunk<A, true, ShapeRT>(p, it % p.nc, it / p.nc, smf, scr);
+  const int64_t items = (int64_t)p.nc * p.B * p.H;
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    grad_chunk<A, true, ShapeRT>(p, (int)(it % p.nc), (int)(it / p.nc), smf, scr);
     __syncthreads();  // every read of this item's tiles precedes the next item's loads
   }
 }
@@ -923,7 +923,9 @@ constexpr size_t kGradSmemW = (kSmallW + 8 * kMaxW + 3 * kMaxW * kRedCols + 2 * 
 static size_t seed_smem_wide(const BBParams& p) {
   return ((size_t)p.CR * (p.sLN + p.sLP) + 6 * kMaxW) * sizeof(float);
 }
-static int grad_grid_wide(const BBParams& p) { return std::min(p.nc * p.B * p.H, kWideGrid); }
+static int grad_grid_wide(const BBParams& p) {
+  return (int)std::min<int64_t>((int64_t)p.nc * p.B * p.H, kWideGrid);
+}
 
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
