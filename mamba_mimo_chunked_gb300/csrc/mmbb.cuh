@@ -130,7 +130,9 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 // m16n8k8 fragments (A: rows g, g+8 at k = c, c+4; B: column g at k = c,
 // c+4; accumulator nb: rows g, g+8, columns nb*8 + 2c, +1; g = lane / 4,
 // c = lane % 4).  k past K reads as zero.
-template <class FA, class FB>
+// BEXACT: every b value is exactly a TF32 number (a widened BF16 or FP16
+// value), so b needs no split and a b = hi_a b + lo_a b takes two products.
+template <bool BEXACT = false, class FA, class FB>
 __device__ __forceinline__ void mm_tc(float (&acc)[2][4], int r0, int c0, int K, FA a, FB b) {
   const int lane = threadIdx.x & 31, g = lane >> 2, cq = lane & 3;
   for (int k0 = 0; k0 < K; k0 += 8) {
@@ -146,12 +148,19 @@ __device__ __forceinline__ void mm_tc(float (&acc)[2][4], int r0, int c0, int K,
     for (int q = 0; q < 4; q++) split_tf32(af[q], ah[q], al[q]);
 #pragma unroll
     for (int nb = 0; nb < 2; nb++) {
-      uint32_t bh0, bl0, bh1, bl1;
-      split_tf32(va ? b(ka, c0 + nb * 8 + g) : 0.f, bh0, bl0);
-      split_tf32(vb ? b(kb, c0 + nb * 8 + g) : 0.f, bh1, bl1);
-      mma_tf32(acc[nb], ah, bl0, bl1);
-      mma_tf32(acc[nb], al, bh0, bh1);
-      mma_tf32(acc[nb], ah, bh0, bh1);
+      if constexpr (BEXACT) {
+        const uint32_t b0 = __float_as_uint(va ? b(ka, c0 + nb * 8 + g) : 0.f);
+        const uint32_t b1 = __float_as_uint(vb ? b(kb, c0 + nb * 8 + g) : 0.f);
+        mma_tf32(acc[nb], al, b0, b1);
+        mma_tf32(acc[nb], ah, b0, b1);
+      } else {
+        uint32_t bh0, bl0, bh1, bl1;
+        split_tf32(va ? b(ka, c0 + nb * 8 + g) : 0.f, bh0, bl0);
+        split_tf32(vb ? b(kb, c0 + nb * 8 + g) : 0.f, bh1, bl1);
+        mma_tf32(acc[nb], ah, bl0, bl1);
+        mma_tf32(acc[nb], al, bh0, bh1);
+        mma_tf32(acc[nb], ah, bh0, bh1);
+      }
     }
   }
 }
@@ -655,7 +664,9 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
     mm_tc(acc, fr0, fc0, CR, [=](int i, int j) { return M2[i * LC + j] * facr[j]; },
           [=](int j, int n) { return Kr[j * LN + n]; });
     zero_tc(acc2);
-    mm_tc(acc2, fr0, fc0, P, [=](int i, int pp) { return Gp[i * LP + pp]; }, [=](int pp, int n) { return Hc[n * LP + pp]; });
+    // Hc holds widened BF16 / FP16 cache values: exact TF32 operands
+    mm_tc<A != kF32>(acc2, fr0, fc0, P, [=](int i, int pp) { return Gp[i * LP + pp]; },
+                     [=](int pp, int n) { return Hc[n * LP + pp]; });
 #pragma unroll
     for (int nb = 0; nb < 2; nb++)
 #pragma unroll
@@ -691,7 +702,8 @@ __device__ __forceinline__ void grad_chunk(const BBParams& p, int c, int bh, flo
   for_tiles<WIDE>(CR, P, [&](int fr0, int fc0, int wc) {
     float acc[2][4];
     zero_tc(acc);
-    mm_tc(acc, fr0, fc0, N, [=](int i, int n) { return Qr[i * LN + n]; }, [=](int n, int pp) { return Hc[n * LP + pp]; });
+    mm_tc<A != kF32>(acc, fr0, fc0, N, [=](int i, int n) { return Qr[i * LN + n]; },
+                     [=](int n, int pp) { return Hc[n * LP + pp]; });
     float r3[2] = {0.f, 0.f};
 #pragma unroll
     for (int nb = 0; nb < 2; nb++)
