@@ -77,7 +77,8 @@
  * the reverse scan); BF16 / FP16 outputs are the FP32 results rounded to
  * nearest even.  The tile products run on the tensor cores in TF32: each
  * FP32 operand is split into two TF32 parts by truncation and each pair
- * takes three products, an error below 3 * 2^-20 relative per product
+ * takes three products (two where one operand is the BF16 / FP16 states
+ * cache, exact in TF32), an error below 3 * 2^-20 relative per product
  * (FP32-level accuracy).  Results are deterministic (no floating-point
  * atomics).
  */
