@@ -297,15 +297,19 @@ __device__ __forceinline__ void load_rotated(const BBParams& p, int b, int h, in
   }
   __syncthreads();
   const int half = SH::N(p) / 2;
+  // one angle per (token, pair), applied to the token's R rank rows
   #pragma unroll
-  for (int e = threadIdx.x; e < SH::CR(p) * SH::w(p); e += NT) {
-    const int j = e / SH::w(p), m = e % SH::w(p), t = j / SH::R(p), tg = c * SH::C(p) + t;
+  for (int e = threadIdx.x; e < SH::C(p) * SH::w(p); e += NT) {
+    const int t = e / SH::w(p), m = e % SH::w(p), tg = c * SH::C(p) + t;
     const float th = tg < p.S ? p.angles[(((int64_t)b * p.S + tg) * p.H + h) * SH::w(p) + m] : 0.f;
     float sn, cs;
     sincosf(th, &sn, &cs);
-    const float lo = T[j * ld + m], hi = T[j * ld + half + m];
-    T[j * ld + m] = cs * lo - sn * hi;
-    T[j * ld + half + m] = sn * lo + cs * hi;
+    for (int r = 0; r < SH::R(p); r++) {
+      const int j = t * SH::R(p) + r;
+      const float lo = T[j * ld + m], hi = T[j * ld + half + m];
+      T[j * ld + m] = cs * lo - sn * hi;
+      T[j * ld + half + m] = sn * lo + cs * hi;
+    }
   }
 }
 
