@@ -119,6 +119,23 @@ def test_parity_other_activation_dtypes(case, act):
     _compare(_run_gpu(args, kw), want)
 
 
+@pytest.mark.parametrize("act", [torch.float16, torch.float32], ids=["f16", "f32"])
+@pytest.mark.parametrize("case", [WIDE[0], WIDE[4]], ids=["N128_P128", "N80_P72"])
+def test_parity_wide_shapes_other_activation_dtypes(case, act):
+    # the persistent kernel's FP16 / FP32 instantiations, with FP16 DQ / DK /
+    # DV for FP16 activations (the default output dtype)
+    args, kw = _problem(**case, seed=47, act=act)
+    want = bb.bwd_bwd(*args, **kw)
+    _compare(_run_gpu(args, kw), want)
+    if act == torch.float16:
+        g16 = _run_gpu(args, kw, output_dtype=None)
+        for name in ("DQ", "DK", "DV"):
+            assert g16[name].dtype == torch.float16
+            w = want[name]
+            err = np.sqrt(np.mean((g16[name].double().cpu().numpy() - w) ** 2)) / np.sqrt(np.mean(w ** 2))
+            assert err < 2.0 ** -11, f"{name}: relative RMS {err:.3e}"
+
+
 @pytest.mark.parametrize("case", WIDE, ids=lambda c: f"S{c['S']}_R{c['R']}_N{c['N']}_P{c['P']}_C{c['C']}")
 def test_parity_wide_shapes(case):
     args, kw = _problem(**case, seed=31)
