@@ -56,9 +56,9 @@ struct BBParams {
   float* ws_scr;              // [grid][scr_floats]
 };
 
-constexpr int kT = 256;             // threads per CTA (seed kernel: 4 x 4 blocks of a 64 x 64 product)
-constexpr int kTG = 512;            // threads per CTA of the gradient kernel (2 x 4 blocks)
-constexpr int kMax = 64;            // N, P and C*R limit of this path
+constexpr int kT = 256;             // threads per CTA of the seed and reduce kernels' thread groups
+constexpr int kTG = 512;            // threads per CTA of the gradient kernel (16 warps, 16 x 16 output tiles)
+constexpr int kMax = 64;            // N, P and C*R limit of the 64-wide path (tiles in shared memory)
 constexpr int kLD = kMax + 4;       // FP32 tile row stride: 4 (mod 32) puts the 32 lanes of every m16n8k8 fragment load on distinct banks
 constexpr int kTile = kMax * kLD;   // floats per tile
 constexpr int kSmall = 4224;        // segsum [C][C], qk [C][R][R], dqk (C*R <= 64, R <= 16)
