@@ -477,9 +477,11 @@ def main():
             mm._raise(lib, st)
     launches_per_call = lib.mamba_mimo_last_launch_count()
 
-    # Per-kernel events on sampled steps of the timed region.
-    every = max(1, args.steps // 400)
-    n_samples = (args.steps + every - 1) // every
+    # Per-kernel CUDA events are taken in a separate, untimed pass after the
+    # timed region: an event recorded between two kernels of a call keeps the
+    # next kernel from launching early (programmatic dependent launch), so
+    # timed steps carry no events.
+    n_samples = 200
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n_samples)]
     for row in ev:                      # torch creates the CUDA event on first record
         for e in row:
@@ -488,21 +490,29 @@ def main():
     ev_arrays = [(ctypes.c_void_p * 8)(*[ctypes.c_void_p(e.cuda_event) for e in row]) for row in ev]
     assert all(e.cuda_event for row in ev for e in row)
 
+    # The clock sampler runs across a stretch of untimed steps (about half a
+    # second) directly before the timed region and across the timed region
+    # itself, so a short timed region still has samples under load.
     sampler = ClockSampler(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
     sampler.start()
-    time.sleep(0.3)
+    t_load = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_load < 0.6:
+        for _ in range(64):
+            bad = call(*call_args[i % len(call_args)])
+            i += 1
+            if bad:
+                mm._raise(lib, bad)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
     start.record(stream)
     bad = 0
     for i in range(args.steps):
-        if i % every == 0:
-            lib.mamba_mimo_set_stage_events(ev_arrays[i // every], 8)
-            bad |= call(*call_args[i % len(call_args)])
-            lib.mamba_mimo_set_stage_events(None, 0)
-        else:
-            bad |= call(*call_args[i % len(call_args)])
+        bad |= call(*call_args[i % len(call_args)])
     end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
@@ -510,6 +520,14 @@ def main():
     if bad:
         raise RuntimeError("a timed call failed")
     elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, dev)
+
+    for i in range(n_samples):          # untimed: per-kernel durations
+        lib.mamba_mimo_set_stage_events(ev_arrays[i], 8)
+        st = call(*call_args[i % len(call_args)])
+        lib.mamba_mimo_set_stage_events(None, 0)
+        if st:
+            mm._raise(lib, st)
+    torch.cuda.synchronize(dev)
 
     stage_ms = {}
     for k in range(min(4, launches_per_call)):
