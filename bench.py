@@ -74,6 +74,9 @@ def parse_args():
     ap.add_argument("--workload", type=int, default=None,
                     help="index into synthetic_inputs.WORKLOADS (default: the timed shape, 2); other "
                          "shapes print their own line (no pages' number to compare, no profile traffic)")
+    ap.add_argument("--quick", action="store_true",
+                    help="warm-up and timed steps only (no clock-load stretch, per-kernel event pass, "
+                         "end-to-end pass or CPU baseline): the short command ncu captures run")
     ap.add_argument("--op", choices=["bwd_fwd", "bwd_bwd"], default="bwd_fwd",
                     help="bwd_bwd: time the second backward stage instead (its own JSON line)")
     return ap.parse_args()
@@ -500,7 +503,7 @@ def main():
     sampler.start()
     t_load = time.perf_counter()
     i = 0
-    while time.perf_counter() - t_load < 0.6:
+    while not args.quick and time.perf_counter() - t_load < 0.6:
         for _ in range(64):
             bad = call(*call_args[i % len(call_args)])
             i += 1
@@ -521,7 +524,7 @@ def main():
         raise RuntimeError("a timed call failed")
     elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, dev)
 
-    for i in range(n_samples):          # untimed: per-kernel durations
+    for i in range(0 if args.quick else n_samples):  # untimed: per-kernel durations
         lib.mamba_mimo_set_stage_events(ev_arrays[i], 8)
         st = call(*call_args[i % len(call_args)])
         lib.mamba_mimo_set_stage_events(None, 0)
@@ -529,6 +532,13 @@ def main():
             mm._raise(lib, st)
     torch.cuda.synchronize(dev)
 
+    if args.quick:  # the short run ncu captures: timing only
+        if rank == 0:
+            print(json.dumps({"metric": METRIC if timed_shape else f"MIMO bwd_fwd tokens/s at {wl.name}",
+                              "quick": True, "ms_per_step": elapsed_s * 1e3 / args.steps,
+                              "value": wl.B * wl.S * args.steps * world / elapsed_s, "unit": "tokens/s",
+                              "config": {"workload": wl.name}}), flush=True)
+        return
     stage_ms = {}
     for k in range(min(4, launches_per_call)):
         name = lib.mamba_mimo_stage_name(k)

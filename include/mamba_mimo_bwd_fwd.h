@@ -163,7 +163,10 @@ mmbf_status mamba_mimo_bwd_fwd_y(const mmbf_dims* dims, const void* dout, const 
  * larger is rejected with MMBF_ERR_WORKSPACE and nothing is enqueued.  This
  * call allocates nothing.  Its first call on a device looks up the array's
  * device address on the current device (cudaGetSymbolAddress); make that
- * first call before any stream capture.  Every call on a device shares the
+ * first call before any stream capture.  The address is kept with the CUDA
+ * context it was looked up in; after the device's context is destroyed and
+ * created again (cudaDeviceReset) the next call looks it up anew, so make
+ * that call before capture too.  Every call on a device shares the
  * one array and leaves its contents behind; nothing in it needs to start at
  * zero.  Calls whose kernels overlap on the GPU (different streams without
  * ordering between them) race on the array and give wrong results: order
@@ -196,8 +199,10 @@ int mamba_mimo_last_launch_count(void);
 void mamba_mimo_set_stage_events(void* const* events, int count);
 
 /* Kernel family the last successful mamba_mimo_bwd_fwd call on this thread
- * used: -1 for the generic kernels (any shape of the envelope), k >= 0 for
- * the k-th shape-specialised family. */
+ * used: -1 for the generic kernels (any shape of the envelope); 0, 1, 2 for
+ * the shape-specialised families R4 C16 N=P=64, R8 C16 N=P=64 and R4 C16
+ * N=P=32; 3 for the warp-specialised tensor-core family (R4 C16 N=P=64 with
+ * reduced dout and without y: every chunk contraction on tcgen05.mma). */
 int mamba_mimo_last_kernel_variant(void);
 
 /* Failure detection for the last mamba_mimo_bwd_fwd call on this thread.
@@ -218,6 +223,24 @@ mmbf_status mamba_mimo_device_status(void* stream);
  * mamba_mimo_device_status.  Nothing faults or hangs; outputs of such a
  * call are incomplete.  For tests of the failure path only. */
 void mamba_mimo_set_test_hooks(int flags);
+
+/* Test hook: evaluates, on the device, the approximate math the shape-
+ * specialised kernels use, so tests can bound its error (the pages have no
+ * counterpart: these are this library's own fast paths for the rotary
+ * sin/cos, exp(segsum) and the gate sigmoid).  x: n FP32 inputs, out: 4n
+ * FP32 results, both device pointers owned by the caller; enqueued on
+ * `stream`.  For input i, out[4i] and out[4i+1] are the fast path's values,
+ * out[4i+2] and out[4i+3] the same quantities from CUDA's accurate sinf /
+ * cosf / expf:
+ *   which = 0: sin(x), cos(x) (reduction by 2*pi in two FP32 parts, then the
+ *              sin.approx / cos.approx instructions);
+ *   which = 1: exp(x) as 2^(x log2 e) by ex2.approx (second slot 0);
+ *   which = 2: sigmoid(x) = rcp.approx(ex2.approx(-x log2 e) + 1) (second
+ *              slot 0).
+ * Returns MMBF_ERR_ARG for a bad `which`, a NULL pointer or n < 0,
+ * MMBF_ERR_ALIGN if out is not 16-byte aligned, and MMBF_ERR_CUDA if the
+ * launch fails. */
+mmbf_status mamba_mimo_probe_fast_math(int which, const float* x, float* out, int n, void* stream);
 
 /* Launch plan of the last successful mamba_mimo_bwd_fwd call on this thread
  * (diagnostic): writes min(n, 5) ints to out -- chunks per segment, segments

@@ -158,6 +158,7 @@ struct Params {
   int nc, CR, MP, NP, PS, npslice, L, nseg;
   int reduced, has_z, has_d, vec_p;  // vec_p: P even (pairs of p are 4-byte aligned)
   int fast;                          // index of the shape-specialised kernels, or -1
+  int tc;                            // 1: the warp-specialised tensor-core output kernel (mmbf_tc.cuh)
   int UA, LA, nunit;                 // state units per segment, chunks per unit, units per head
   const uint16_t *dout, *q, *k, *v, *z, *trap;
   const float *q_bias, *k_bias, *mimo_v, *mimo_o, *mimo_z, *angles, *da_cs, *da_cs_rev, *dt,
@@ -811,6 +812,7 @@ __global__ void grad_reduce_kernel(Params p) {
 }
 
 #include "mmbf_fast.cuh"
+#include "mmbf_tc.cuh"
 
 // ---------------------------------------------------------------------------
 // Host side: planning, validation, launch.
@@ -839,6 +841,7 @@ static unsigned int next_call_tag() {
 static const char* const kStageNames[4] = {"segment_state", "segment_prefix", "chunk_output",
                                            "grad_reduce"};
 static const char* const kFastStageNames[3] = {"segment_state", "segment_prefix", "chunk_output"};
+static const char* const kTcStageNames[2] = {"segment_state", "chunk_output"};
 static thread_local const char* const* g_stage_names = kStageNames;  // kernels of the last call
 static thread_local int g_stage_names_n = 4;
 
@@ -896,7 +899,6 @@ static const size_t kSmemLimit = 227 * 1024;
 using FastA = fast::Cfg<4, 16, 64, 64, 4, 1>;  // R4 C16 N=P=64 (the pages' timed and unit-test shape)
 using FastB = fast::Cfg<8, 16, 64, 64, 4, 2>;  // R8 C16 N=P=64
 using FastC = fast::Cfg<4, 16, 32, 32, 4, 1>;  // R4 C16 N=P=32
-constexpr int kNumFast = 3;
 
 template <class K>
 static bool fast_fits(const Params& p) {
@@ -938,101 +940,44 @@ static int& fast_state_smem_set() {
   return v[d];
 }
 
-// CTAs of `kern` (NT threads, `smem` dynamic bytes, `tmem_cols` tensor-memory
-// columns each) resident on one SM of device `dev`, from the function's
-// register count and the SM's limits: registers per scheduler (a warp's
-// registers rounded to 256), shared memory incl. the per-CTA reservation,
-// threads, CTAs, and the 512 tensor-memory columns.  (The runtime occupancy
-// query reports one CTA per SM for kernels that allocate tensor memory, which
-// is not what the hardware runs.)
-template <typename Kern>
-static int resident_ctas(Kern kern, int dev, int NT, size_t smem, int tmem_cols) {
-  cudaFuncAttributes fa;
-  int regs_sm = 0, smem_sm = 0, reserved = 0, thr_sm = 0, blk_sm = 0;
-  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess ||
-      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 1;
-  }
-  const int warps = (NT + 31) / 32;
-  const int regs_warp = ((std::max(fa.numRegs, 1) * 32 + 255) / 256) * 256;
-  const int warps_smsp = (regs_sm / 4) / regs_warp;
-  int n = std::min(4 * warps_smsp / warps, blk_sm);
-  n = std::min(n, (int)(smem_sm / (smem + fa.sharedSizeBytes + (size_t)reserved)));
-  n = std::min(n, thr_sm / NT);
+// The launch plan is a pure function of the problem (shape and branches):
+// the workspace size query and the call agree on any device, with or without
+// a device current.  It assumes a GB300's 152 SMs and each kernel's resident
+// CTAs per SM as fixed by its launch bounds, shared memory (plus the 1 KB per-
+// CTA reservation, 228 KB per SM) and tensor-memory columns (512 per SM).  On
+// another device the plan is still correct, only its wave count may differ.
+constexpr int kPlanSms = 152;
+constexpr size_t kSmemPerSm = 228 * 1024, kSmemReserved = 1024;
+static int per_sm(int launch_bound_ctas, size_t smem, int tmem_cols) {
+  int n = launch_bound_ctas;
+  n = std::min(n, (int)(kSmemPerSm / (smem + kSmemReserved)));
   if (tmem_cols > 0) n = std::min(n, 512 / tmem_cols);
   return std::max(n, 1);
 }
-
-// Resident output-kernel CTAs on the current device (SMs x CTAs per SM), or a
-// GB300-sized default when no device can be queried.
+// Resident output-kernel CTAs (all SMs) of the shape-specialised family.
 template <class K>
 static int fast_slots_of(const Params& p) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 2 * 152;
-  }
-  const size_t smem = fast_out_smem<K>(p);
-  if (ensure_smem(fast::output_kernel<K, -1>, smem, &fast_out_smem_set<K>()) != cudaSuccess)
-    cudaGetLastError();
-  return sms * resident_ctas(fast::output_kernel<K, -1>, dev, K::NT, smem, K::TM_COLS);
+  return kPlanSms * per_sm(K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 : 1), fast_out_smem<K>(p), K::TM_COLS);
 }
-// Resident state-kernel CTAs on the current device.
+// Resident state-kernel CTAs (all SMs).
 template <class K>
 static int fast_state_slots_of(const Params& p) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 4 * 152;
-  }
-  const size_t smem = fast_state_smem<K>(p);
-  if (ensure_smem(fast::state_kernel<StateCfg<K>>, smem, &fast_state_smem_set<K>()) != cudaSuccess)
-    cudaGetLastError();
-  return sms * resident_ctas(fast::state_kernel<StateCfg<K>>, dev, StateCfg<K>::NT, smem, K::UMMA ? 64 : 0);
+  return kPlanSms * per_sm(StateCfg<K>::NT <= 128 ? 6 : 1, fast_state_smem<K>(p), K::UMMA ? 64 : 0);
 }
 static int fast_state_slots(const Params& p) {
-  static int cache[16][kNumFast];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    dev = 0;
-  }
-  int* slot = (dev >= 0 && dev < 16) ? &cache[dev][p.fast] : nullptr;
-  if (slot && *slot > 0) return *slot;
-  int v;
   switch (p.fast) {
-    case 0: v = fast_state_slots_of<FastA>(p); break;
-    case 1: v = fast_state_slots_of<FastB>(p); break;
-    default: v = fast_state_slots_of<FastC>(p); break;
+    case 0: return fast_state_slots_of<FastA>(p);
+    case 1: return fast_state_slots_of<FastB>(p);
+    default: return fast_state_slots_of<FastC>(p);
   }
-  if (slot) *slot = v;
-  return v;
 }
 static int fast_slots(const Params& p) {
-  // cached per device and specialisation (the occupancy query is not free)
-  static int cache[16][kNumFast][2][2][2];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    dev = 0;
-  }
-  int* slot = (dev >= 0 && dev < 16) ? &cache[dev][p.fast][p.reduced][p.has_z][p.want_y ? 1 : 0] : nullptr;
-  if (slot && *slot > 0) return *slot;
-  int v;
+  if (p.tc) return kPlanSms;  // one warp-specialised CTA per SM (all of its tensor memory)
   switch (p.fast) {
-    case 0: v = fast_slots_of<FastA>(p); break;
-    case 1: v = fast_slots_of<FastB>(p); break;
-    default: v = fast_slots_of<FastC>(p); break;
+    case 0: return fast_slots_of<FastA>(p);
+    case 1: return fast_slots_of<FastB>(p);
+    default: return fast_slots_of<FastC>(p);
   }
-  if (slot) *slot = v;
-  return v;
 }
 // Chunks per segment: the length that minimises (waves x (L + per-CTA setup)),
 // with every segment a CTA of the output kernel.
@@ -1061,7 +1006,7 @@ static int fast_segment_length(const Params& p, int slots) {
 // Shape validation (the pages' checks in their order, then this build's
 // envelope) and the launch plan: tile sizes, p-slices, segment length.
 static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduced, int has_z,
-                        Params* out) {
+                        int want_y, Params* out) {
   if (!dims) return fail(MMBF_ERR_ARG, "dims is NULL");
   const int64_t B = dims->B, S = dims->S, H = dims->H, G = dims->G, R = dims->R, N = dims->N,
                 P = dims->P;
@@ -1105,6 +1050,10 @@ static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduc
   p.LA = p.L;
   p.nunit = p.nseg;
   p.fast = fast_index(p);
+  p.want_y = want_y ? 1 : 0;
+  // the warp-specialised tensor-core output kernel: R4 C16 N=P=64, reduced
+  // dout (mimo_o given), without the forward output y
+  p.tc = (p.fast == 0 && p.reduced && !p.want_y) ? 1 : 0;
   if (p.fast >= 0) {
     p.L = fast_segment_length(p, fast_slots(p));
     p.nseg = (p.nc + p.L - 1) / p.L;
@@ -1117,7 +1066,9 @@ static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduc
     const int64_t sslots = fast_state_slots(p);
     int ua = 1;
     double best = 1e300;
-    for (int u = 1; u <= std::min(2, p.L); u++) {
+    // (the tensor-core output kernel runs one long segment per SM: its state
+    // units come in clusters of up to eight)
+    for (int u = 1; u <= std::min(p.tc ? 8 : 2, p.L); u++) {
       const int la = (p.L + u - 1) / u;
       const int64_t ctas = heads * p.nseg * ((p.L + la - 1) / la);
       const double cost = (double)((ctas + sslots - 1) / sslots) * (la + 2.0);
@@ -1315,13 +1266,99 @@ static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) 
   return e;  // the output kernel's last CTA per (b,h) also sums the dmimo partials
 }
 
+// Device-side evaluation of the specialised kernels' approximate math next to
+// CUDA's accurate functions (mamba_mimo_probe_fast_math).
+__global__ void probe_fast_math_kernel(int which, const float* x, float* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float v = x[i];
+  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (which == 0) {
+    fast::sincos_fast(v, &r.x, &r.y);
+    r.z = sinf(v);
+    r.w = cosf(v);
+  } else if (which == 1) {
+    r.x = fast::exp_fast(v);
+    r.z = expf(v);
+  } else {
+    r.x = fast::rcp_approx(fast::ex2_approx(v * -fast::kLog2e) + 1.f);
+    r.z = 1.f / (1.f + expf(-v));
+  }
+  reinterpret_cast<float4*>(out)[i] = r;
+}
+
+// The timed shape family with reduced dout: the state-sum kernel (clusters of
+// up to eight units per segment), then the warp-specialised tensor-core output
+// kernel, which folds the earlier segments' sums itself (no prefix kernel).
+template <int MODE>
+static int& tc_smem_set() {
+  static int v[kMaxDevices + 1];
+  const int d = device_slot();
+  if (d == kMaxDevices) v[d] = 0;
+  return v[d];
+}
+static cudaError_t launch_tc(const Params& p, cudaStream_t st, int* launches) {
+  using T = tc::TCfg<4>;
+  using KS = StateCfg<FastA>;
+  const size_t ss = fast_state_smem<FastA>(p);
+  const int mode = (p.has_z && p.has_d) ? 7 : -1;
+  cudaError_t e = ensure_smem(fast::state_kernel<KS>, ss, &fast_state_smem_set<FastA>());
+  if (e == cudaSuccess)
+    e = mode == 7 ? ensure_smem(tc::out_kernel<T, 7>, T::SMEM, &tc_smem_set<7>())
+                  : ensure_smem(tc::out_kernel<T, -1>, T::SMEM, &tc_smem_set<-1>());
+  if (e != cudaSuccess) return e;
+  g_stage_names = kTcStageNames;
+  g_stage_names_n = 2;
+  g_failed_stage = 0;
+  stage_event(0, 0, st);
+  e = launch_ex(fast::state_kernel<KS>, dim3(p.B * p.H, p.nunit), dim3(KS::NT), ss, st, false, p, p.UA);
+  stage_event(0, 1, st);
+  (*launches)++;
+  if (e != cudaSuccess) return e;
+  g_failed_stage = 1;
+  stage_event(1, 0, st);
+  const dim3 og(p.B * p.H, p.nseg);
+  e = mode == 7 ? launch_ex(tc::out_kernel<T, 7>, og, dim3(T::NT), T::SMEM, st, true, p)
+                : launch_ex(tc::out_kernel<T, -1>, og, dim3(T::NT), T::SMEM, st, true, p);
+  stage_event(1, 1, st);
+  (*launches)++;
+  return e;
+}
+
 // Built-in scratch area of mamba_mimo_bwd_fwd_fixed_scratch: a file-scope
 // device array (every GPU that loads the library holds it until exit).  Host
 // code must not use the name as an address; the device address is looked up
-// once per device with that device current.
+// with the device current, once per device and CUDA context: a context torn
+// down and created again (cudaDeviceReset) maps the array at a new address,
+// so the cached address is kept with the context it belongs to and looked up
+// again when the current context differs.
 static __device__ __align__(256) unsigned char g_fixed_scratch[MAMBA_MIMO_FIXED_SCRATCH_BYTES];
 static std::mutex g_fixed_scratch_mu;
-static void* g_fixed_scratch_addr[256];
+struct FixedScratchSlot {
+  CUcontext ctx;
+  void* addr;
+};
+static FixedScratchSlot g_fixed_scratch_slot[256];
+
+// The calling thread's current CUDA context (NULL if none is current yet or
+// the driver entry point is unavailable); no stream work, no allocation.
+static CUcontext current_context() {
+  using Fn = CUresult (*)(CUcontext*);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(f);
+    else
+      cudaGetLastError();
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 static mmbf_status fixed_scratch_address(void** out) {
   int dev = -1;
@@ -1329,15 +1366,18 @@ static mmbf_status fixed_scratch_address(void** out) {
   if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= 256) return fail(MMBF_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_fixed_scratch_mu);
-  if (!g_fixed_scratch_addr[dev]) {
+  FixedScratchSlot& slot = g_fixed_scratch_slot[dev];
+  const CUcontext ctx = current_context();
+  if (!slot.addr || !ctx || slot.ctx != ctx) {
     void* addr = nullptr;
     e = cudaGetSymbolAddress(&addr, g_fixed_scratch);
     if (e != cudaSuccess || addr == nullptr)
       return fail(MMBF_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch area: %s",
                   cudaGetErrorString(e));
-    g_fixed_scratch_addr[dev] = addr;
+    slot.addr = addr;
+    slot.ctx = current_context();  // the symbol lookup made the device's context current
   }
-  *out = g_fixed_scratch_addr[dev];
+  *out = slot.addr;
   return MMBF_OK;
 }
 
@@ -1350,11 +1390,17 @@ extern "C" {
 mmbf_status mamba_mimo_bwd_fwd_workspace_size(const mmbf_dims* dims, int64_t chunk_size,
                                               int64_t rotary_dim_divisor, int reduced_dout,
                                               int has_z, size_t* bytes) {
-  Params p;
-  mmbf_status s = plan(dims, chunk_size, rotary_dim_divisor, reduced_dout, has_z, &p);
-  if (s != MMBF_OK) return s;
+  // one size serves the op with and without the forward output y (their
+  // plans may differ)
+  size_t need = 0;
+  for (int want_y = 0; want_y < 2; want_y++) {
+    Params p;
+    mmbf_status s = plan(dims, chunk_size, rotary_dim_divisor, reduced_dout, has_z, want_y, &p);
+    if (s != MMBF_OK) return s;
+    need = std::max(need, workspace_bytes_of(p));
+  }
   if (!bytes) return fail(MMBF_ERR_ARG, "bytes is NULL");
-  *bytes = workspace_bytes_of(p);
+  *bytes = need;
   return MMBF_OK;
 }
 
@@ -1371,7 +1417,7 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
                           void* y, void* workspace, size_t workspace_bytes, void* stream) {
   g_err[0] = '\0';
   Params p;
-  mmbf_status s = plan(dims, chunk_size, rotary_dim_divisor, mimo_o != nullptr, z != nullptr, &p);
+  mmbf_status s = plan(dims, chunk_size, rotary_dim_divisor, mimo_o != nullptr, z != nullptr, y != nullptr, &p);
   if (s != MMBF_OK) return s;
   if (!dout || !q || !k || !v || !q_bias || !k_bias || !mimo_v || !angles || !da_cs ||
       !da_cs_rev || !dt || !trap || !segsum)
@@ -1389,7 +1435,10 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
   for (const void* x : ptrs)
     if (x && (reinterpret_cast<uintptr_t>(x) & 3))
       return fail(MMBF_ERR_ALIGN, "tensor pointers must be 4-byte aligned");
-  const size_t need = workspace_bytes_of(p);
+  size_t need = 0;
+  s = mamba_mimo_bwd_fwd_workspace_size(dims, chunk_size, rotary_dim_divisor, mimo_o != nullptr, z != nullptr,
+                                        &need);
+  if (s != MMBF_OK) return s;
   if (!workspace || workspace_bytes < need)
     return fail(MMBF_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
   if (reinterpret_cast<uintptr_t>(workspace) & 255)
@@ -1397,7 +1446,6 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
 
   p.has_d = d != nullptr;
   p.y = static_cast<uint16_t*>(y);
-  p.want_y = y != nullptr;
   p.dout = static_cast<const uint16_t*>(dout);
   p.q = static_cast<const uint16_t*>(q);
   p.k = static_cast<const uint16_t*>(k);
@@ -1441,16 +1489,20 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
     }
   }
   if (fast_ok) {
-    switch (p.fast) {
-      case 0: e = launch_fast<FastA>(p, st, &launches); break;
-      case 1: e = launch_fast<FastB>(p, st, &launches); break;
-      default: e = launch_fast<FastC>(p, st, &launches); break;
+    if (p.tc) {
+      e = launch_tc(p, st, &launches);
+    } else {
+      switch (p.fast) {
+        case 0: e = launch_fast<FastA>(p, st, &launches); break;
+        case 1: e = launch_fast<FastB>(p, st, &launches); break;
+        default: e = launch_fast<FastC>(p, st, &launches); break;
+      }
     }
     if (e == cudaSuccess && g_stage_error != cudaSuccess) {
       e = g_stage_error;
       g_stage_error = cudaSuccess;
     }
-    g_variant = p.fast;
+    g_variant = p.tc ? 3 : p.fast;
     g_plan[0] = p.L; g_plan[1] = p.nseg; g_plan[2] = p.UA; g_plan[3] = p.LA; g_plan[4] = fast_slots(p);
     if (e != cudaSuccess)
       return fail(MMBF_ERR_CUDA, "CUDA error in %s (fast %d, grid %d x %d/%d): %s",
@@ -1594,6 +1646,18 @@ int mamba_mimo_last_launch_count(void) { return g_launches; }
 int mamba_mimo_last_kernel_variant(void) { return g_variant; }
 
 void mamba_mimo_set_test_hooks(int flags) { g_test_flags = flags; }
+
+mmbf_status mamba_mimo_probe_fast_math(int which, const float* x, float* out, int n, void* stream) {
+  g_err[0] = '\0';
+  if (which < 0 || which > 2) return fail(MMBF_ERR_ARG, "which must be 0, 1 or 2");
+  if (n < 0 || (n > 0 && (!x || !out))) return fail(MMBF_ERR_ARG, "x and out must be device pointers, n >= 0");
+  if (n == 0) return MMBF_OK;
+  if (reinterpret_cast<uintptr_t>(out) & 15) return fail(MMBF_ERR_ALIGN, "out must be 16-byte aligned");
+  probe_fast_math_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(which, x, out, n);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "probe launch: %s", cudaGetErrorString(e));
+  return MMBF_OK;
+}
 
 mmbf_status mamba_mimo_device_status(void* stream) {
   if (!g_last_err_word) return MMBF_OK;

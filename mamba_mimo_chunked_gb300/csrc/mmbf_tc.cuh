@@ -1,0 +1,746 @@
+// Warp-specialised output kernel of mamba_mimo_bwd_fwd for the pages' timed
+// shape family: R = 4, C = 16, N = P = 64, reduced dout (mimo_o given), Z and
+// D optional (included by mmbf_kernels.cu inside namespace mmbf, after
+// mmbf_fast.cuh, whose TMA, mbarrier, fragment and tensor-memory helpers it
+// uses).
+//
+// What one chunk computes is the op document's chunk output (page "feat: add
+// Triton-Ascend implementation of Mamba-3 mamba_mimo_bwd_fwd #125", section
+// "Triton 实现", items 5-7, and the BF16 reference): every rounding point of
+// the BF16 reference is kept, as in the other kernel families.  How it is
+// computed here:
+//
+// * One CTA per (b*h, segment) and SM (all 512 tensor-memory columns); it
+//   walks its segment's chunks with the FP32 state in registers.
+// * Every contraction of a chunk is a 64x64x64 BF16 tcgen05.mma with an FP32
+//   accumulator in tensor memory (M = 64 layout: row m at lane 32(m/16) +
+//   m%16), double-buffered across chunks:
+//     S       = Q_rot Ks^T              (the causal scores, rows and columns j)
+//     U       = PsiV^T k_state          (the chunk's state contribution, [p][n])
+//     inter^T = bf16(state)^T Q_rot^T   ([p][j])
+//     intra^T = PsiV^T A^T              ([p][j], A = bf16(mask(S) exp(segsum)))
+//   Rows j of the chunk are stored in the fragment order of fast::perm() inside
+//   each 16-row block, so a thread that reads inter^T / intra^T as 16x256b
+//   fragments holds all four ranks of one token for a pair of p values (p,
+//   p+8): the rank-ordered BF16 diagonal and dz need no cross-lane traffic.
+// * Warp roles (16 warps):
+//     0-7   epilogue: warp w reads p-block w%4 and the j-columns of tokens
+//           8(w/4)..8(w/4)+7; diagonal, out, Z branch, dmimo partials, dz;
+//     8-11  prologue: one 16-row j-block each; biased Q/K, same-token qk_dot
+//           (mma.sync on the diagonal tiles), rotary, k_scaled, k_state,
+//           PsiV, exp(segsum) below the diagonal, the token-scalar table;
+//     12-15 state: the FP32 state (p-block w%4, all n) in registers, folded
+//           with U each chunk; bf16(state) for inter and the states output;
+//           the causal matrix A from S.  Warp 12's first thread issues the
+//           MMAs and the TMA loads of q, k, v, angles and segsum; warp 13's
+//           stores states.
+//   Warp 0's first thread also stores dz (TMA) and loads dout and z.
+// * Two TMA rings: ring I (q, k, v, angles, segsum; the prologue writes Q_rot
+//   and k_scaled over the raw q and k rows, k_state beside them) is freed when
+//   the chunk's MMAs complete; ring O (PsiV, dout, z -> dz, the qk table) when
+//   the epilogue is done and dz has left.  Four slots each.
+// * All hand-offs are mbarriers.  Every wait is bounded (about a second of
+//   %globaltimer); a wait that runs out records the tagged error word and sets
+//   a CTA abort flag that ends every other wait at once, so the CTA drains its
+//   copies in flight and leaves.
+
+namespace tc {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int DIV_>
+struct TCfg {
+  using K = fast::Cfg<4, 16, 64, 64, DIV_, 1>;  // the shared prologue helpers' view
+  static constexpr int R = 4, C = 16, N = 64, P = 64, CR = 64, DIV = DIV_, W = N / DIV_;
+  static constexpr int NI = 4, NO = 4;            // ring depths
+  static constexpr int TW = 8, TS = 4 * C;        // token table: window of 8 chunks, 64 floats per chunk
+  static constexpr int QKS = K::QKS;              // words per token in the qk table
+  static constexpr int NWARP = 16, NT = NWARP * 32;
+  static constexpr int WP = 8, WS = 12;           // first prologue / state warp
+  // ring I slot
+  static constexpr uint32_t I_Q = 0, I_K = 8192, I_KST = 16384, I_V = 24576, I_ANG = 26624, I_SEG = 28672,
+                            I_BYTES = 29696;
+  // ring O slot
+  static constexpr uint32_t O_PSI = 0, O_DOUT = 8192, O_Z = 10240, O_QKD = 12288, O_BYTES = 14336;
+  // CTA layout (offsets from the 1024-byte aligned base)
+  static constexpr uint32_t RI = 0, RO = NI * I_BYTES, SBT = RO + NO * O_BYTES, ATT = SBT + 2 * 8192,
+                            TOK = ATT + 2 * 8192, MVB = TOK + 2 * TW * TS * 4, QBS = MVB + R * P * 2,
+                            KBS = QBS + R * K::LDB * 2, MZP = KBS + R * K::LDB * 2, MOP = MZP + R * 4 * 8 * 8,
+                            BAR = MOP + R * 4 * 8 * 4;
+  // barriers: full / pdone / ofree / fullO per ring slot, the rest per TMEM / tile buffer
+  enum : uint32_t {
+    B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_M1 = 16, B_M2 = 18, B_SBR = 20, B_SBFREE = 22,
+    B_AR = 24, B_SUFREE = 26, B_XFREE = 28, B_ED = 30, B_TOKW = 32, NBAR = 34
+  };
+  static constexpr uint32_t MISC = BAR + NBAR * 8;  // tmem slot, abort flag, last-CTA flag
+  static constexpr uint32_t SMEM = MISC + 16 + 1024;  // + alignment slack of the base
+  // tensor-memory columns (two buffers of 64 each)
+  static constexpr uint32_t T_S = 0, T_U = 128, T_I = 256, T_X = 384;
+  static_assert(I_ANG + C * W * 4 <= I_SEG && I_SEG + C * C * 4 <= I_BYTES, "ring I slot");
+  static_assert(O_QKD + C * QKS * 4 <= O_BYTES, "ring O slot");
+  static_assert(I_BYTES % 1024 == 0 && O_BYTES % 1024 == 0 && RO % 1024 == 0 && SBT % 1024 == 0, "alignment");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+__device__ __forceinline__ void arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// Bounded wait for phase `parity`; false if the CTA is aborting or the wait
+// ran out (then the abort flag is set and the error word recorded).
+__device__ __forceinline__ bool wait_b(const Params& p, uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                       uint32_t code) {
+  if (fast::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = fast::global_ns();
+  while (true) {
+    if (fast::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (fast::global_ns() - t0 > fast::kWaitLimitNs) {
+      *abort_flag = 1u;
+      atomicExch(p.ws_err, (p.tag << 8) | code);
+      return false;
+    }
+  }
+}
+
+// 64x64x64 BF16 MMA, FP32 accumulator in tensor memory (M = N = 64).  A is
+// [M][K] (K-major: rows of 128 bytes along K) or [K][M] (MN-major); B is [N][K]
+// (K-major) or [K][N] (MN-major); 128-byte swizzled tiles, 1024-byte aligned.
+// A K-step of 16 advances 32 bytes inside a K-major row, 16 rows (2048 bytes)
+// of an MN-major tile.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void mma64(uint32_t tmem_d, uint32_t a_saddr, uint32_t b_saddr) {
+  constexpr uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (A_MN ? (1u << 15) : 0u) |
+                             (B_MN ? (1u << 16) : 0u) | ((64u >> 3) << 17) | ((64u >> 4) << 24);
+#pragma unroll
+  for (int ks = 0; ks < 4; ks++) {
+    const uint64_t da = fast::umma_desc_mn128(a_saddr + ks * (A_MN ? 2048u : 32u));
+    const uint64_t db = fast::umma_desc_mn128(b_saddr + ks * (B_MN ? 2048u : 32u));
+    const uint32_t acc = ks > 0 ? 1u : 0u;
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(da), "l"(db), "r"(idesc), "r"(acc)
+        : "memory");
+  }
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+               : "memory");
+}
+
+// Token of physical row i (0..63) of a chunk tile: rows are in perm<4> order
+// inside each 16-row block.
+__device__ __forceinline__ int token_of(int i) { return 4 * (i >> 4) + ((i & 7) >> 1); }
+
+// Raw token inputs of the window starting at chunk cw, one token per
+// prologue thread (pt = 0..127: token cw*C + pt).
+template <class T>
+__device__ __forceinline__ fast::TokRaw tok_load(const Params& p, int bh, int cw, int pt) {
+  fast::TokRaw r = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int tg = cw * T::C + pt;
+  const int64_t i = (int64_t)bh * p.S + tg;
+  if (tg < p.S) {
+    r.dt = __ldg(p.dt + i);
+    r.tr = bf_f(__ldg(p.trap + i));
+    r.a = __ldg(p.da_cs + i);
+    r.ar = __ldg(p.da_cs_rev + i);
+  }
+  if (tg + 1 < p.S) {
+    r.dtn = __ldg(p.dt + i + 1);
+    r.trn = bf_f(__ldg(p.trap + i + 1));
+  }
+  return r;
+}
+// Token scalars of one token into the window table (same arithmetic as
+// fast::token_window): gamma = bf16(dt) sigmoid(trap); factor = bf16(gamma +
+// bf16(bf16(dt[t+1]) sigmoid(-trap[t+1]))) (0 shifted term at the last padded
+// position) as a BF16 pair; exp(da_cs); exp(da_cs_rev).
+template <class T>
+__device__ __forceinline__ void tok_fill(const Params& p, const fast::TokRaw& v, float* tab, int cw, int pt) {
+  const int tg = cw * T::C + pt;
+  float* tok = tab + (pt / T::C) * T::TS;
+  const int t = pt % T::C;
+  const float gam = __fmul_rn(round_bf(v.dt), sigmoid_f(v.tr));
+  float sh = 0.f;
+  if (tg + 1 < p.nc * T::C) sh = round_bf(__fmul_rn(round_bf(v.dtn), 1.0f / (1.0f + expf(v.trn))));
+  tok[t] = gam;
+  reinterpret_cast<uint32_t*>(tok)[T::C + t] = fast::dup_bf(__fadd_rn(gam, sh));
+  tok[2 * T::C + t] = expf(v.a);
+  tok[3 * T::C + t] = expf(v.ar);
+}
+
+template <class T, int MODE>
+__global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ Params p) {
+  using K = typename T::K;
+  constexpr int R = T::R, C = T::C, N = T::N, P = T::P;
+  const bool HZ = MODE >= 0 ? (MODE & 2) != 0 : p.has_z != 0;
+  const bool HD = MODE >= 0 ? (MODE & 4) != 0 : p.has_d != 0;
+  extern __shared__ __align__(128) unsigned char sm_raw[];
+  unsigned char* sm;
+  {
+    const uint32_t a = smem_u32(sm_raw);
+    sm = sm_raw + (((a + 1023u) & ~1023u) - a);
+  }
+  const uint32_t sb = smem_u32(sm);
+  const int bh = blockIdx.x, seg = blockIdx.y;
+  const int b = bh / p.H, h = bh % p.H, grp = h / (p.H / p.G);
+  const int c0 = seg * p.L, c1 = min(p.nc, c0 + p.L), n = c1 - c0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, cq = lane & 3, mi = lane >> 3, li = lane & 7;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + T::MISC + 4);
+  auto bar = [&](uint32_t i) { return sb + T::BAR + 8u * i; };
+
+  // ---- set-up: barriers, tensor memory, parameter tables
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 4; i++) {
+      fast::mbar_init(bar(T::B_FULLI + i), 1);
+      fast::mbar_init(bar(T::B_FULLO + i), 1);
+      fast::mbar_init(bar(T::B_PDONE + i), 4);
+      fast::mbar_init(bar(T::B_OFREE + i), 1);
+    }
+    for (int i = 0; i < 2; i++) {
+      fast::mbar_init(bar(T::B_M1 + i), 1);
+      fast::mbar_init(bar(T::B_M2 + i), 1);
+      fast::mbar_init(bar(T::B_SBR + i), 4);
+      fast::mbar_init(bar(T::B_SBFREE + i), 1);
+      fast::mbar_init(bar(T::B_AR + i), 4);
+      fast::mbar_init(bar(T::B_SUFREE + i), 4);
+      fast::mbar_init(bar(T::B_XFREE + i), 8);
+      fast::mbar_init(bar(T::B_ED + i), 8);
+      fast::mbar_init(bar(T::B_TOKW + i), 4);
+    }
+    *abort_flag = 0u;
+    fast::mbar_fence_init();
+  }
+  uint32_t* tm_slot = reinterpret_cast<uint32_t*>(sm + T::MISC);
+  if (warp == T::WS) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tm_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  {
+    uint16_t* mvb = reinterpret_cast<uint16_t*>(sm + T::MVB);
+    uint16_t* qbs = reinterpret_cast<uint16_t*>(sm + T::QBS);
+    uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + T::KBS);
+    for (int e = threadIdx.x; e < R * P; e += T::NT) mvb[e] = f_bf(p.mimo_v[(int64_t)h * R * P + e]);
+    for (int e = threadIdx.x; e < R * N; e += T::NT) {
+      const int at = (e / N) * K::LDB + e % N;
+      qbs[at] = f_bf(p.q_bias[(int64_t)h * R * N + e]);
+      kbs[at] = f_bf(p.k_bias[(int64_t)h * R * N + e]);
+    }
+    float2* mzp = reinterpret_cast<float2*>(sm + T::MZP);
+    uint32_t* mop = reinterpret_cast<uint32_t*>(sm + T::MOP);
+    for (int e = threadIdx.x; e < R * 4 * 8; e += T::NT) {
+      const int o = e / 32, mt = (e / 8) % 4, gg = e % 8;
+      const float* mo = p.mimo_o + ((int64_t)h * R + o) * P + mt * 16 + gg;
+      mop[e] = (uint32_t)f_bf(mo[0]) | ((uint32_t)f_bf(mo[8]) << 16);
+      if (HZ) {
+        const float* mz = p.mimo_z + ((int64_t)h * R + o) * P + mt * 16 + gg;
+        mzp[e] = make_float2(mz[0], mz[8]);
+      }
+    }
+  }
+  fast::tm_fence_before();
+  __syncthreads();
+  fast::tm_fence_after();
+  const uint32_t tmem = *tm_slot;
+
+  // TMA loads of chunk c0 + i into its ring slots (one thread each ring)
+  auto load_I = [&](int i) {
+    const int c = c0 + i, s = i % T::NI;
+    const uint32_t base = sb + T::RI + s * T::I_BYTES, full = bar(T::B_FULLI + s);
+    const int t0 = c * C;
+    uint32_t bytes = 2 * 8192 + C * P * 2 + C * T::W * 4 + C * C * 4;
+    if (i == 0 && (p.test_flags & 1)) bytes += 16;  // test hook: this wait runs out (nothing faults)
+    fast::mbar_expect_tx(full, bytes);
+    fast::tma_load_5d(base + T::I_Q, &p.tm_q, 0, grp, 0, t0, b, full);
+    fast::tma_load_5d(base + T::I_K, &p.tm_k, 0, grp, 0, t0, b, full);
+    fast::tma_load_4d(base + T::I_V, &p.tm_v, 0, h, t0, b, full);
+    fast::tma_load_4d(base + T::I_ANG, &p.tm_ang, 0, h, t0, b, full);
+    fast::bulk_load(base + T::I_SEG, p.segsum + ((int64_t)bh * p.nc + c) * C * C, C * C * 4, full);
+  };
+  auto load_O = [&](int i) {
+    const int c = c0 + i, s = i % T::NO;
+    const uint32_t base = sb + T::RO + s * T::O_BYTES, full = bar(T::B_FULLO + s);
+    const int t0 = c * C;
+    fast::mbar_expect_tx(full, C * P * 2 * (HZ ? 2 : 1));
+    fast::tma_load_4d(base + T::O_DOUT, &p.tm_dout, 0, h, t0, b, full);
+    if (HZ) fast::tma_load_4d(base + T::O_Z, &p.tm_z, 0, h, t0, b, full);
+  };
+  if (threadIdx.x == T::WS * 32)
+    for (int i = 0; i < min(T::NI - 1, n); i++) load_I(i);
+  if (threadIdx.x == 0)
+    for (int i = 0; i < min(T::NO - 1, n); i++) load_O(i);
+
+  // ---- the state entering this segment: the segment sums of the earlier
+  //      segments of (b,h) folded in order (acc = acc * decay_s + sum_s),
+  //      every thread below 512 eight consecutive elements
+  fast::pdl_wait();
+  float* xs = reinterpret_cast<float*>(sm + T::SBT);  // 16 KB scratch (SB and A tiles are unused yet)
+  if (threadIdx.x < 512) {
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    const float* base = p.ws_state + (int64_t)bh * p.nseg * N * P + threadIdx.x * 8;
+    const float* dec = p.ws_decay + (int64_t)bh * p.nseg;
+    for (int s0 = 0; s0 < seg; s0 += 8) {
+      float4 x0[8], x1[8];
+      float d[8];
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        if (s0 + q < seg) {
+          const float4* src = reinterpret_cast<const float4*>(base + (int64_t)(s0 + q) * N * P);
+          x0[q] = __ldcg(src);
+          x1[q] = __ldcg(src + 1);
+          d[q] = __ldcg(dec + s0 + q);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        if (s0 + q < seg) {
+          a0 = make_float4(fmaf(a0.x, d[q], x0[q].x), fmaf(a0.y, d[q], x0[q].y), fmaf(a0.z, d[q], x0[q].z),
+                           fmaf(a0.w, d[q], x0[q].w));
+          a1 = make_float4(fmaf(a1.x, d[q], x1[q].x), fmaf(a1.y, d[q], x1[q].y), fmaf(a1.z, d[q], x1[q].z),
+                           fmaf(a1.w, d[q], x1[q].w));
+        }
+      }
+    }
+    reinterpret_cast<float4*>(xs)[2 * threadIdx.x] = a0;
+    reinterpret_cast<float4*>(xs)[2 * threadIdx.x + 1] = a1;
+  }
+  __syncthreads();
+  // State warps: their FP32 state^T slice (p-block q, all n) in the 16x256b
+  // fragment layout: st[nn][e] = state[n = 8nn + 2cq + (e&1)][p = 16q + g + 8(e>>1)].
+  float st[8][4];
+  if (warp >= T::WS) {
+    const int q = warp - T::WS;
+#pragma unroll
+    for (int nn = 0; nn < 8; nn++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) st[nn][e] = xs[(8 * nn + 2 * cq + (e & 1)) * P + 16 * q + g + 8 * (e >> 1)];
+  }
+  __syncthreads();  // the scratch is read before any tile is written
+
+  float* tokb = reinterpret_cast<float*>(sm + T::TOK);
+  auto tok_of = [&](int i) { return tokb + (i % (2 * T::TW)) * T::TS; };
+  auto decay_of = [&](int i) {  // exp(da_cs[last valid token of chunk c0 + i])
+    const int c = c0 + i;
+    return tok_of(i)[2 * C + min(c * C + C, p.S) - 1 - c * C];
+  };
+
+  int loaded_o = min(T::NO - 1, n);  // ring O chunks issued (thread 0)
+  if (warp < T::WP) {
+    // =====================================================================
+    // Epilogue warps
+    // =====================================================================
+    const int q = warp & 3, hc = warp >> 2;
+    const uint32_t tl_lane = (uint32_t)(32 * q) << 16;
+    float2 mzr[4];
+    uint32_t mor[4];
+    {
+      const float2* mzp = reinterpret_cast<const float2*>(sm + T::MZP);
+      const uint32_t* mop = reinterpret_cast<const uint32_t*>(sm + T::MOP);
+#pragma unroll
+      for (int o = 0; o < 4; o++) {
+        mzr[o] = HZ ? mzp[(o * 4 + q) * 8 + g] : make_float2(0.f, 0.f);
+        mor[o] = mop[(o * 4 + q) * 8 + g];
+      }
+    }
+    const float dval = HD ? p.d[h] : 0.f;
+    float2 cdmo[4], cdmz[4];
+#pragma unroll
+    for (int o = 0; o < 4; o++) cdmo[o] = cdmz[o] = make_float2(0.f, 0.f);
+    for (int i = 0; i < n; i++) {
+      const int c = c0 + i, so = i % T::NO, s2 = i & 1;
+      const uint32_t obase = sb + T::RO + so * T::O_BYTES;
+      unsigned char* op = sm + T::RO + so * T::O_BYTES;
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_M2 + s2), (i >> 1) & 1, abort_flag, 3))) break;
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + i % T::NI), (i / T::NI) & 1, abort_flag, 3))) break;
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLO + so), (i / T::NO) & 1, abort_flag, 1))) break;
+      fast::tm_fence_after();
+      float vi[4][4], vx[4][4];
+      fast::tm_ld_frag<4>(tmem + tl_lane + T::T_I + 64 * s2 + 32 * hc, vi);
+      fast::tm_ld_frag<4>(tmem + tl_lane + T::T_X + 64 * s2 + 32 * hc, vx);
+      fast::tm_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_XFREE + s2));
+      const float* tok = tok_of(i);
+      const uint16_t* psi = reinterpret_cast<const uint16_t*>(op + T::O_PSI);
+      const uint32_t* qkd = reinterpret_cast<const uint32_t*>(op + T::O_QKD);
+      uint16_t* zt = reinterpret_cast<uint16_t*>(op + T::O_Z);
+      const uint16_t* dt_ = reinterpret_cast<const uint16_t*>(op + T::O_DOUT);
+#pragma unroll
+      for (int tt = 0; tt < 2; tt++) {
+        const int jb = 2 * hc + tt, tl = 4 * jb + cq;
+        const float gam = tok[tl], ed = tok[2 * C + tl];
+        const float2 gam2 = make_float2(gam, gam), ed2 = make_float2(ed, ed);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(a0, a1, a2, a3, psi + fast::swz128(16 * jb + (mi >> 1) * 8 + li, 16 * q + (mi & 1) * 8));
+        uint32_t ps[4];  // PsiV of rank o at (p, p + 8)
+        ps[0] = fast::lo_lo(a0, a1);
+        ps[1] = fast::hi_hi(a0, a1);
+        ps[2] = fast::lo_lo(a2, a3);
+        ps[3] = fast::hi_hi(a2, a3);
+        uint32_t qr[4][4];  // same-token bf16(qh . kh)[o][r], both halves
+#pragma unroll
+        for (int o = 0; o < 4; o++) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qkd + tl * T::QKS + o * 4);
+          qr[o][0] = v.x; qr[o][1] = v.y; qr[o][2] = v.z; qr[o][3] = v.w;
+        }
+        const int pr = 16 * q + g;
+        float2 z2 = make_float2(0.f, 0.f);
+        if (HZ) z2 = fast::unpack2((uint32_t)zt[fast::swz128(tl, pr)] | ((uint32_t)zt[fast::swz128(tl, pr + 8)] << 16));
+        const uint32_t dob =
+            (uint32_t)dt_[fast::swz128(tl, pr)] | ((uint32_t)dt_[fast::swz128(tl, pr + 8)] << 16);
+        uint32_t dzacc = 0u;
+#pragma unroll
+        for (int o = 0; o < 4; o++) {
+          const int kk = 2 * tt + (o >> 1), bb = o & 1;
+          // diagonal: rank-ordered BF16 products and sums, then * gamma, rounded
+          uint32_t dacc = bmul2(qr[o][0], ps[0]);
+#pragma unroll
+          for (int r = 1; r < R; r++) dacc = badd2(dacc, bmul2(qr[o][r], ps[r]));
+          const uint32_t dgb = fast::pack2(__fmul2_rn(fast::unpack2(dacc), gam2));
+          // out = bf16(inter * exp(da_cs) + intra + diag + d * PsiV)
+          float2 x = __ffma2_rn(make_float2(vi[kk][bb], vi[kk][bb + 2]), ed2, make_float2(vx[kk][bb], vx[kk][bb + 2]));
+          x = fast::add_bf2_f32(dgb, x);
+          if (HD) x = __ffma2_rn(make_float2(dval, dval), fast::unpack2(ps[o]), x);
+          const uint32_t ob = fast::pack2(x);
+          if (HZ) {
+            const float2 mz = mzr[o];
+            const float2 pz = __fmul2_rn(z2, mz);
+            const float2 tq = __fmul2_rn(pz, make_float2(-fast::kLog2e, -fast::kLog2e));
+            const float2 den =
+                __fadd2_rn(make_float2(fast::ex2_approx(tq.x), fast::ex2_approx(tq.y)), make_float2(1.f, 1.f));
+            const float2 sg = make_float2(fast::rcp_approx(den.x), fast::rcp_approx(den.y));
+            const float2 silu = __fmul2_rn(pz, sg);
+            // dmimo_o partials: out * dout (exact) * silu(pz)
+            const float2 od = fast::fma_bf2_f32(ob, dob, make_float2(-0.f, -0.f));
+            cdmo[o] = __ffma2_rn(od, silu, cdmo[o]);
+            const uint32_t preb = bmul2(bmul2(dob, mor[o]), ob);
+            const float2 pre = fast::unpack2(preb);
+            // sigmoid(pz) (1 + pz (1 - sigmoid(pz))) = sigmoid + silu (1 - sigmoid)
+            const float2 om = __fadd2_rn(make_float2(1.f, 1.f), make_float2(-sg.x, -sg.y));
+            const float2 gz = __fmul2_rn(pre, __ffma2_rn(silu, om, sg));
+            cdmz[o] = __ffma2_rn(gz, z2, cdmz[o]);
+            // dz: BF16 running sum over the ranks in order
+            dzacc = fast::pack2(fast::add_bf2_f32(dzacc, __fmul2_rn(gz, mz)));
+          } else {
+            cdmo[o] = fast::fma_bf2_f32(ob, dob, cdmo[o]);
+          }
+        }
+        if (HZ) {  // dz over the z values this thread has read; stored by TMA
+          zt[fast::swz128(tl, pr)] = (uint16_t)(dzacc & 0xffffu);
+          zt[fast::swz128(tl, pr + 8)] = (uint16_t)(dzacc >> 16);
+        }
+      }
+      // dz of chunk c leaves by TMA once all epilogue warps wrote it; then the
+      // ring O slot of chunk c - 1 is free (its dz store has read it) and
+      // takes chunk c - 1 + NO
+      // (every epilogue warp arrives, with or without dz: the slot refill
+      // below must not overtake a warp still reading chunk c - 1)
+      if (HZ) fast::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_ED + s2));
+      bool ok = true;
+      if (threadIdx.x == 0) {
+        ok = wait_b(p, bar(T::B_ED + s2), (i >> 1) & 1, abort_flag, 3);
+        if (ok) {
+          if (HZ) {
+            fast::tma_store_4d(&p.tm_dz, obase + T::O_Z, 0, h, c * C, b);
+            asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
+          }
+          if (i >= 1) arrive(bar(T::B_OFREE + (i - 1) % T::NO));
+          if (i + T::NO - 1 < n) {
+            fast::fence_proxy_async();
+            load_O(i + T::NO - 1);
+            loaded_o = i + T::NO;
+          }
+        }
+      }
+      if (!__all_sync(kFull, ok)) break;
+    }
+    if (threadIdx.x == 0) fast::tma_store_wait_all();
+    // ---- fixed-order reduction of the dmimo partials of this segment:
+    //      the four lanes of a row group (tokens), then the two warps of a
+    //      p-block (token halves)
+#pragma unroll
+    for (int o = 0; o < 4; o++) {
+#pragma unroll
+      for (int m = 1; m <= 2; m <<= 1) {
+        cdmo[o].x += __shfl_xor_sync(0xffffffffu, cdmo[o].x, m);
+        cdmo[o].y += __shfl_xor_sync(0xffffffffu, cdmo[o].y, m);
+        cdmz[o].x += __shfl_xor_sync(0xffffffffu, cdmz[o].x, m);
+        cdmz[o].y += __shfl_xor_sync(0xffffffffu, cdmz[o].y, m);
+      }
+    }
+    // red[hc][which][o][p] (FP32, 2 x 2 x 4 x 64) in ring I slot 0 (idle now)
+    // after the final barrier below
+    __syncwarp();
+    fast::tm_fence_before();
+    __syncthreads();  // (A) every role has left its loop
+    float* red = reinterpret_cast<float*>(sm + T::RI);
+    if (cq == 0) {
+#pragma unroll
+      for (int o = 0; o < 4; o++) {
+        const int pr = 16 * q + g;
+        red[((hc * 2 + 0) * 4 + o) * P + pr] = cdmo[o].x;
+        red[((hc * 2 + 0) * 4 + o) * P + pr + 8] = cdmo[o].y;
+        red[((hc * 2 + 1) * 4 + o) * P + pr] = cdmz[o].x;
+        red[((hc * 2 + 1) * 4 + o) * P + pr + 8] = cdmz[o].y;
+      }
+    }
+  } else if (warp < T::WS) {
+    // =====================================================================
+    // Prologue warps: one 16-row j-block each
+    // =====================================================================
+    const int jw = warp - T::WP, j0 = 16 * jw, pt = threadIdx.x - T::WP * 32;
+    const uint16_t* qbs = reinterpret_cast<const uint16_t*>(sm + T::QBS);
+    const uint16_t* kbs = reinterpret_cast<const uint16_t*>(sm + T::KBS);
+    const uint16_t* mvb = reinterpret_cast<const uint16_t*>(sm + T::MVB);
+    fast::TokRaw traw = tok_load<T>(p, bh, c0, pt);
+    for (int i = 0; i < n; i++) {
+      const int c = c0 + i, si = i % T::NI, so = i % T::NO;
+      unsigned char* ip = sm + T::RI + si * T::I_BYTES;
+      unsigned char* op = sm + T::RO + so * T::O_BYTES;
+      if (i % T::TW == 0) {  // token scalars of the window starting at chunk c
+        const int wi = i / T::TW;
+        tok_fill<T>(p, traw, tokb + (wi & 1) * T::TW * T::TS, c, pt);
+        if (c + T::TW < c1) traw = tok_load<T>(p, bh, c + T::TW, pt);
+        __syncwarp();
+        if (lane == 0) arrive(bar(T::B_TOKW + (wi & 1)));
+        if (!__all_sync(kFull, wait_b(p, bar(T::B_TOKW + (wi & 1)), (wi >> 1) & 1, abort_flag, 4))) break;
+      }
+      const float* tok = tok_of(i);
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLI + si), (i / T::NI) & 1, abort_flag, 1))) break;
+      if (!__all_sync(kFull, i < T::NO || wait_b(p, bar(T::B_OFREE + so), ((i / T::NO) - 1) & 1, abort_flag, 4)))
+        break;
+      uint16_t* qt = reinterpret_cast<uint16_t*>(ip + T::I_Q);
+      uint16_t* kt = reinterpret_cast<uint16_t*>(ip + T::I_K);
+      uint32_t qf[4][4], kf[4][4];
+      fast::load_rows<K>(qf, qt, j0);
+      fast::load_rows<K>(kf, kt, j0);
+      fast::add_bias<K>(qf, qbs);
+      fast::add_bias<K>(kf, kbs);
+      {  // same-token qk_dot from the diagonal 16x16 tile of Qh Kh^T
+        uint32_t* qkd = reinterpret_cast<uint32_t*>(op + T::O_QKD);
+        float qa[2][4];
+#pragma unroll
+        for (int ht = 0; ht < 2; ht++) qa[ht][0] = qa[ht][1] = qa[ht][2] = qa[ht][3] = 0.f;
+#pragma unroll
+        for (int k4 = 0; k4 < 4; k4++) {
+          mma16816(qa[0], qf[k4][0], qf[k4][1], qf[k4][2], qf[k4][3], kf[k4][0], kf[k4][2]);
+          mma16816(qa[1], qf[k4][0], qf[k4][1], qf[k4][2], qf[k4][3], kf[k4][1], kf[k4][3]);
+        }
+#pragma unroll
+        for (int ht = 0; ht < 2; ht++)
+#pragma unroll
+          for (int hh = 0; hh < 2; hh++) {
+            const int pi = fast::perm<R>(g + 8 * hh), pi2 = fast::perm<R>(ht * 8 + 2 * cq);
+            if (pi / R == pi2 / R) {
+              const int tl = (j0 + pi) / R, o = pi % R, s0 = pi2 % R;
+              const float v0 = round_bf(qa[ht][2 * hh]), v1 = round_bf(qa[ht][2 * hh + 1]);
+              qkd[tl * T::QKS + o * R + s0] = fast::dup_bf(v0);
+              qkd[tl * T::QKS + o * R + s0 + 1] = fast::dup_bf(v1);
+              const int tg = c * C + tl;
+              if (tg < p.S)
+                *reinterpret_cast<uint32_t*>(p.qk_dot + (((int64_t)bh * p.S + tg) * R + o) * R + s0) =
+                    (uint32_t)f_bf(v0) | ((uint32_t)f_bf(v1) << 16);
+            }
+          }
+      }
+      fast::rotate_direct<K, true>(qf, kf, reinterpret_cast<const float*>(ip + T::I_ANG), j0);
+      __syncwarp();  // this warp's raw q / k rows are read before they are overwritten
+      fast::store_rows<K, true>(qf, qt, j0);  // Q_rot, rows in fragment order
+      fast::scale_k<K>(kf, reinterpret_cast<const uint32_t*>(tok) + C, j0);
+      fast::store_rows<K, true>(kf, kt, j0);  // k_scaled
+      fast::k_state<K>(kf, tok + 3 * C, j0);
+      fast::store_rows<K, true>(kf, reinterpret_cast<uint16_t*>(ip + T::I_KST), j0);
+      fast::psi_rows<K>(reinterpret_cast<const uint16_t*>(ip + T::I_V), mvb,
+                        reinterpret_cast<uint16_t*>(op + T::O_PSI), j0);
+      {  // exp(segsum) strictly below the diagonal, 0 elsewhere (a select), in place
+        float* sg = reinterpret_cast<float*>(ip + T::I_SEG);
+#pragma unroll
+        for (int e = pt; e < C * C; e += 128) sg[e] = ((e % C) < (e / C)) ? fast::exp_fast(sg[e]) : 0.f;
+      }
+      fast::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_PDONE + si));
+    }
+    __syncwarp();
+    fast::tm_fence_before();
+    __syncthreads();  // (A)
+  } else {
+    // =====================================================================
+    // State warps: p-block q of the state; the causal matrix rows of block q.
+    // The first thread of warp 12 issues the MMAs and the ring I loads, the
+    // first of warp 13 stores states.
+    // =====================================================================
+    const int q = warp - T::WS;
+    const uint32_t tl_lane = (uint32_t)(32 * q) << 16;
+    const bool issuer = threadIdx.x == T::WS * 32;
+    const bool store_thread = threadIdx.x == T::WS * 32 + 32;
+    int loaded_i = min(T::NI - 1, n);  // ring I chunks issued (issuer)
+    int commits = 0;                   // tcgen05.commit issued (the last one covers every MMA)
+    uint32_t last_bar = 0, last_par = 0;
+    for (int i = 0; i < n; i++) {
+      const int c = c0 + i, s2 = i & 1, si = i % T::NI, so = i % T::NO;
+      const uint32_t ib = sb + T::RI + si * T::I_BYTES, ob = sb + T::RO + so * T::O_BYTES;
+      if (i >= 1) {  // state = state * exp(da_cs[last of chunk c-1]) + U_{c-1}
+        fast::tm_fence_after();
+        fast::fold_u<K>(st, tmem + tl_lane + T::T_U + 64 * ((i - 1) & 1), decay_of(i - 1));
+        fast::tm_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive(bar(T::B_SUFREE + ((i - 1) & 1)));
+      }
+      bool ok = true;
+      if (issuer) {  // S = Q_rot Ks^T and U = PsiV^T k_state of chunk c
+        ok = wait_b(p, bar(T::B_PDONE + si), (i / T::NI) & 1, abort_flag, 2) &&
+             (i < 2 || wait_b(p, bar(T::B_SUFREE + s2), ((i - 2) >> 1) & 1, abort_flag, 2));
+        if (ok) {
+          fast::tm_fence_after();
+          mma64<false, false>(tmem + T::T_S + 64 * s2, ib + T::I_Q, ib + T::I_K);
+          mma64<true, true>(tmem + T::T_U + 64 * s2, ob + T::O_PSI, ib + T::I_KST);
+          mma_commit(bar(T::B_M1 + s2));
+          commits++; last_bar = bar(T::B_M1 + s2); last_par = (i >> 1) & 1;
+        }
+      }
+      if (!__all_sync(kFull, ok)) break;
+      // bf16(state) -> SB tile [n][p] (inter's operand and states[c])
+      if (i >= 2) {
+        if (!__all_sync(kFull, wait_b(p, bar(T::B_M2 + s2), ((i - 2) >> 1) & 1, abort_flag, 2))) break;
+        if (!__all_sync(kFull, wait_b(p, bar(T::B_SBFREE + s2), ((i - 2) >> 1) & 1, abort_flag, 2))) break;
+      }
+      uint16_t* sbt = reinterpret_cast<uint16_t*>(sm + T::SBT + s2 * 8192);
+#pragma unroll
+      for (int nn = 0; nn < 4; nn++) {
+        const uint32_t r0 = fast::pack2(make_float2(st[2 * nn][0], st[2 * nn][1]));
+        const uint32_t r1 = fast::pack2(make_float2(st[2 * nn][2], st[2 * nn][3]));
+        const uint32_t r2 = fast::pack2(make_float2(st[2 * nn + 1][0], st[2 * nn + 1][1]));
+        const uint32_t r3 = fast::pack2(make_float2(st[2 * nn + 1][2], st[2 * nn + 1][3]));
+        fast::stsm_x4_t(sbt + fast::swz128(nn * 16 + (mi >> 1) * 8 + li, q * 16 + (mi & 1) * 8), r0, r1, r2, r3);
+      }
+      fast::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_SBR + s2));
+      if (store_thread) {  // states[c] = bf16(state entering chunk c): one tile store
+        ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2);
+        if (ok) {
+          fast::tma_store_2d(&p.tm_states, sb + T::SBT + s2 * 8192, 0, (int)(((int64_t)bh * p.nc + c) * N));
+          if (i >= 1) {
+            asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
+            arrive(bar(T::B_SBFREE + ((i - 1) & 1)));
+          }
+        }
+      }
+      if (!__all_sync(kFull, ok)) break;
+      // A = bf16(S * exp(segsum)) strictly below the token diagonal, 0 elsewhere
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + si), (i / T::NI) & 1, abort_flag, 2))) break;
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_M1 + s2), (i >> 1) & 1, abort_flag, 2))) break;
+      fast::tm_fence_after();
+      float sv[8][4];
+      fast::tm_ld_frag<8>(tmem + tl_lane + T::T_S + 64 * s2, sv);
+      const float* es = reinterpret_cast<const float*>(sm + T::RI + si * T::I_BYTES + T::I_SEG);
+      const int trow = 4 * q + (g >> 1);
+      uint16_t* at = reinterpret_cast<uint16_t*>(sm + T::ATT + s2 * 8192);
+#pragma unroll
+      for (int kb = 0; kb < 4; kb++) {  // 16 columns (one j-block) per stsm
+        const float e = es[trow * C + 4 * kb + cq];
+        const float2 e2 = make_float2(e, e);
+        const uint32_t r0 = fast::pack2(__fmul2_rn(make_float2(sv[2 * kb][0], sv[2 * kb][1]), e2));
+        const uint32_t r1 = fast::pack2(__fmul2_rn(make_float2(sv[2 * kb][2], sv[2 * kb][3]), e2));
+        const uint32_t r2 = fast::pack2(__fmul2_rn(make_float2(sv[2 * kb + 1][0], sv[2 * kb + 1][1]), e2));
+        const uint32_t r3 = fast::pack2(__fmul2_rn(make_float2(sv[2 * kb + 1][2], sv[2 * kb + 1][3]), e2));
+        fast::stsm_x4(at + fast::swz128(16 * q + li + 8 * (mi & 1), 16 * kb + 8 * (mi >> 1)), r0, r1, r2, r3);
+      }
+      fast::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_AR + s2));
+      if (issuer) {  // inter^T and intra^T of chunk c; then the ring I refill
+        ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2) &&
+             wait_b(p, bar(T::B_AR + s2), (i >> 1) & 1, abort_flag, 2) &&
+             (i < 2 || wait_b(p, bar(T::B_XFREE + s2), ((i - 2) >> 1) & 1, abort_flag, 2));
+        if (ok) {
+          fast::tm_fence_after();
+          mma64<true, false>(tmem + T::T_I + 64 * s2, sb + T::SBT + s2 * 8192, ib + T::I_Q);
+          mma64<true, false>(tmem + T::T_X + 64 * s2, ob + T::O_PSI, sb + T::ATT + s2 * 8192);
+          mma_commit(bar(T::B_M2 + s2));
+          commits++; last_bar = bar(T::B_M2 + s2); last_par = (i >> 1) & 1;
+          // chunk i + NI - 1 into the ring I slot of chunk i - 1 once its MMAs are done
+          if (i + T::NI - 1 < n) {
+            ok = i < 1 || wait_b(p, bar(T::B_M2 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag, 2);
+            if (ok) {
+              load_I(i + T::NI - 1);
+              loaded_i = i + T::NI;
+            }
+          }
+        }
+      }
+      if (!__all_sync(kFull, ok)) break;
+    }
+    __syncwarp();
+    if (issuer) {
+      // every MMA completes before tensor memory is released (bounded)
+      if (commits > 0) {
+        const uint64_t t0 = fast::global_ns();
+        while (!fast::mbar_try_wait(last_bar, last_par))
+          if (fast::global_ns() - t0 > fast::kWaitLimitNs) break;
+      }
+      // after an abort: the ring I loads in flight land first (the last NI
+      // issued are the latest use of their slots)
+      if (*abort_flag)
+        for (int i = max(0, loaded_i - T::NI); i < loaded_i; i++) {
+          const uint32_t bf = bar(T::B_FULLI + i % T::NI), ph = (i / T::NI) & 1;
+          const uint64_t t0 = fast::global_ns();
+          while (!fast::mbar_try_wait(bf, ph))
+            if (fast::global_ns() - t0 > fast::kWaitLimitNs) break;
+        }
+    }
+    if (store_thread) fast::tma_store_wait_all();
+    __syncwarp();
+    fast::tm_fence_before();
+    __syncthreads();  // (A)
+  }
+
+  // ---- (after barrier A) after an abort the ring O loads in flight land
+  //      before the CTA leaves; then the dmimo partials of this segment and
+  //      the release of tensor memory
+  if (threadIdx.x == 0 && *abort_flag) {
+    for (int i = max(0, loaded_o - T::NO); i < loaded_o; i++) {
+      const uint32_t bf = bar(T::B_FULLO + i % T::NO), ph = (i / T::NO) & 1;
+      const uint64_t t0 = fast::global_ns();
+      while (!fast::mbar_try_wait(bf, ph))
+        if (fast::global_ns() - t0 > fast::kWaitLimitNs) break;
+    }
+  }
+  __syncthreads();  // (B) red[] complete
+  if (warp == T::WS) {
+    fast::tm_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
+  }
+  const float* red = reinterpret_cast<const float*>(sm + T::RI);
+  float* dst = p.ws_grad + ((int64_t)bh * p.nseg + seg) * 2 * R * P;
+  for (int e = threadIdx.x; e < 2 * R * P; e += T::NT) {
+    // e = which * R * P + o * P + pp; token halves summed in order
+    dst[e] = red[e] + red[2 * R * P + e];
+  }
+  // The last CTA of this (b,h) to finish sums the segments' partials in
+  // segment order (the result does not depend on which CTA is last).
+  __threadfence();
+  __syncthreads();
+  unsigned int* last = reinterpret_cast<unsigned int*>(sm + T::MISC + 8);
+  if (threadIdx.x == 0) *last = (atomicAdd(p.ws_count + bh, 1u) == (unsigned int)p.nseg - 1u) ? 1u : 0u;
+  __syncthreads();
+  if (*last) {
+    __threadfence();
+    for (int e = threadIdx.x; e < 2 * R * P; e += T::NT) {
+      const float* src = p.ws_grad + (int64_t)bh * p.nseg * 2 * R * P + e;
+      float sum = 0.f;
+      for (int s = 0; s < p.nseg; s++) sum += __ldcg(src + (int64_t)s * 2 * R * P);
+      const int which = e / (R * P), x = e % (R * P);
+      if (which == 0) p.dmimo_o[(int64_t)bh * R * P + x] = sum;
+      if (which == 1 && HZ) p.dmimo_z[(int64_t)bh * R * P + x] = sum;
+    }
+  }
+}
+
+}  // namespace tc

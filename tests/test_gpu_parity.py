@@ -150,6 +150,8 @@ def sampled_heads(index, pairs):
     variant = mm.last_kernel_variant()
     if index in (2, 4):   # shapes with specialised kernels must use them
         assert variant >= 0, f"{wl.name} ran the generic kernels"
+    if index == 2:        # the timed shape runs the warp-specialised tensor-core kernel
+        assert variant == 3, f"{wl.name} ran kernel family {variant}"
     for (b, h) in pairs:
         sl = si.head_slice(inp, b, h)
         sl_cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in sl.items()}
@@ -165,8 +167,19 @@ def sampled_heads(index, pairs):
     torch.cuda.empty_cache()
 
 
-def test_timed_workload_sampled_heads():
-    sampled_heads(2, [(0, 0), (0, 7), (0, 15)])
+def test_timed_workload_all_heads():
+    # every output element of all 16 heads of the pages' timed shape, in the
+    # benchmark's launch configuration (the oracle runs all heads at once)
+    wl = si.WORKLOADS[2]
+    inp = si.make_inputs(**wl.shape_kwargs(), seed=si.WORKLOAD_SEED_BASE + 2, device="cuda")
+    got = mm.mamba_mimo_bwd_fwd(*si.args_of(inp))
+    torch.cuda.synchronize()
+    assert mm.last_kernel_variant() == 3
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    want = oracle.bwd_fwd(*si.args_of(cpu))
+    compare(got, want, wl.name)
+    del inp, got
+    torch.cuda.empty_cache()
 
 
 def test_wide_state_workload_sampled_heads():
@@ -233,5 +246,83 @@ def test_device_status_clean_after_calls():
     wl = si.WORKLOADS[2]
     inp = si.make_inputs(**wl.shape_kwargs(), seed=7, device="cuda")
     mm.mamba_mimo_bwd_fwd(*si.args_of(inp))
-    assert mm.last_kernel_variant() == 0
+    assert mm.last_kernel_variant() == 3
     mm.device_status()
+
+
+# --- inputs outside the workload ranges --------------------------------------
+
+# one case per kernel family: the warp-specialised tensor-core kernel (R4 C16
+# N=P=64, reduced dout), the specialised kernels with per-rank dout, R = 8,
+# N = P = 32, and the generic kernels
+FAMILIES = [
+    dict(seqlen=70, heads=2, reduce_o=True, has_z=True, has_d=True),
+    dict(seqlen=70, heads=2, reduce_o=False, has_z=True, has_d=True),
+    dict(seqlen=45, heads=2, rank=8, reduce_o=True, has_z=True, has_d=True),
+    dict(seqlen=50, heads=2, state_dim=32, value_dim=32, reduce_o=True, has_z=True, has_d=True),
+    dict(seqlen=37, heads=2, rank=3, chunk_size=6, state_dim=24, value_dim=20, reduce_o=True, has_z=True,
+         has_d=True),
+]
+
+
+def poison_segsum(inp):
+    """+inf and NaN on and above the diagonal of every segsum block: entries
+    the strictly causal mask excludes.  The mask must be a select, so none of
+    them may reach an output (a mask applied by multiplication would turn
+    them into NaN)."""
+    seg = inp["segsum"].clone()
+    C = seg.shape[-1]
+    i = torch.arange(C)
+    upper = i[None, :] >= i[:, None]
+    pattern = torch.where((i[None, :] + i[:, None]) % 2 == 0, torch.tensor(float("inf")),
+                          torch.tensor(float("nan")))
+    seg[..., upper] = pattern[upper]
+    out = dict(inp)
+    out["segsum"] = seg
+    return out
+
+
+@pytest.mark.parametrize("kw", FAMILIES)
+def test_segsum_inf_nan_above_diagonal(kw):
+    inp = poison_segsum(unit_inputs(recipe="workload", **kw))
+    assert torch.isnan(inp["segsum"]).any() and torch.isposinf(inp["segsum"]).any()
+    check(inp, str(kw))
+
+
+@pytest.mark.parametrize("kw", FAMILIES)
+def test_large_rotary_angles(kw):
+    # rotary angles of real models reach the thousands; the specialised
+    # kernels reduce them by 2 pi before sin.approx / cos.approx
+    inp = unit_inputs(recipe="workload", **kw)
+    g = torch.Generator().manual_seed(2024)
+    inp["angles"] = (torch.rand(inp["angles"].shape, generator=g, dtype=torch.float64) * 4e4 - 2e4).float()
+    check(inp, str(kw))
+
+
+def test_workspace_size_independent_of_device():
+    # The launch plan is a function of the problem only: the size queried with
+    # a GPU current equals the size queried in a process that sees no GPU, so a
+    # workspace sized anywhere is accepted by every call.
+    import json
+    import os
+    import subprocess
+    import sys
+    shapes = [(1, 8192, 16, 1, 4, 64, 64, 16, 4, 1, 1), (2, 16384, 32, 4, 4, 128, 64, 32, 2, 1, 1),
+              (8, 32768, 32, 8, 8, 64, 64, 16, 4, 1, 1), (2, 1000, 8, 2, 4, 32, 32, 16, 4, 0, 0),
+              (1, 200, 2, 1, 4, 64, 64, 16, 4, 0, 1)]
+    code = (
+        "import ctypes, json, sys; sys.path.insert(0, %r)\n"
+        "import mamba_mimo_chunked_gb300 as mm\n"
+        "lib = mm.load_library(); out = []\n"
+        "for B, S, H, G, R, N, P, C, div, red, z in %r:\n"
+        "    d = mm._Dims(B, S, H, G, R, N, P); n = ctypes.c_size_t(0)\n"
+        "    assert lib.mamba_mimo_bwd_fwd_workspace_size(ctypes.byref(d), C, div, red, z, ctypes.byref(n)) == 0\n"
+        "    out.append(n.value)\n"
+        "print(json.dumps(out))\n") % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))), shapes)
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    no_gpu = json.loads(subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                                       check=True).stdout)
+    here = []
+    for B, S, H, G, R, N, P, C, div, red, z in shapes:
+        here.append(mm.workspace_size(B, S, H, G, R, N, P, C, div, bool(red), bool(z)))
+    assert here == no_gpu

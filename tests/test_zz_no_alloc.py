@@ -17,6 +17,7 @@ import pytest
 import torch
 
 import mamba_mimo_chunked_gb300 as mm
+import oracle
 import synthetic_inputs as si
 
 pytestmark = pytest.mark.gpu
@@ -77,8 +78,35 @@ def test_fixed_scratch_refuses_problems_larger_than_its_area(cuda_lib):
     need = mm.workspace_size(wl.B, wl.S, wl.H, wl.G, wl.R, wl.N, wl.P, wl.C, wl.div, wl.reduced,
                              wl.has_z)
     assert need > FIXED_SCRATCH_BYTES
-    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the size check comes first
-    st = fn(ctypes.byref(mm._Dims(wl.B, wl.S, wl.H, wl.G, wl.R, wl.N, wl.P)), *([fake] * 17),
-            wl.C, wl.div, *([fake] * 5), None)
+    # Every tensor pointer is NULL: the size check refuses the problem first;
+    # were that check ever to come later, the NULL inputs would be refused as
+    # invalid arguments (a different status) -- no kernel can be launched.
+    st = fn(ctypes.byref(mm._Dims(wl.B, wl.S, wl.H, wl.G, wl.R, wl.N, wl.P)), *([None] * 17),
+            wl.C, wl.div, *([None] * 5), None)
     assert st == 5
     assert "built-in scratch area" in lib.mamba_mimo_last_error().decode()
+
+
+def test_fixed_scratch_matches_the_oracle(cuda_lib):
+    # the tail+GQA workload (ragged last chunk, grouped heads, per-rank dout)
+    # through the allocation-free entry point, element by element against the
+    # CPU oracle
+    lib = mm.load_library()
+    fn = _entry(lib)
+    inp = si.workload_inputs(1)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    like = mm.mamba_mimo_bwd_fwd(*si.args_of(dev))
+    torch.cuda.synchronize()
+    st, got = _call_fixed(fn, dev, like)
+    assert st == 0, lib.mamba_mimo_last_error().decode()
+    torch.cuda.synchronize()
+    want = oracle.bwd_fwd(*si.args_of(inp))
+    for name, g in zip(oracle.OUTPUT_NAMES, got):
+        w = want[name]
+        assert (g is None) == (w is None), name
+        if g is None:
+            continue
+        gn = g.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(gn)), name
+        err = np.sqrt(np.mean((gn - w) ** 2)) / max(np.sqrt(np.mean(w ** 2)), 1e-30)
+        assert err < TOL, (name, err)
