@@ -221,7 +221,9 @@ mmbf_status mamba_mimo_device_status(void* stream);
  * expects 16 bytes more than its loads deliver, so its bounded wait runs
  * out and the call reports MMBF_ERR_DEVICE_TIMEOUT through
  * mamba_mimo_device_status.  Nothing faults or hangs; outputs of such a
- * call are incomplete.  For tests of the failure path only. */
+ * call are incomplete.  Bit 1: the warp-specialised family takes its two-
+ * kernel form (a separate state-sum kernel) where it would run as a single
+ * kernel, so tests cover both forms.  For tests only. */
 void mamba_mimo_set_test_hooks(int flags);
 
 /* Test hook: evaluates, on the device, the approximate math the shape-
@@ -243,10 +245,16 @@ void mamba_mimo_set_test_hooks(int flags);
 mmbf_status mamba_mimo_probe_fast_math(int which, const float* x, float* out, int n, void* stream);
 
 /* Launch plan of the last successful mamba_mimo_bwd_fwd call on this thread
- * (diagnostic): writes min(n, 5) ints to out -- chunks per segment, segments
- * per (b,h), state units per segment, chunks per unit, and the resident
+ * (diagnostic): writes min(n, 7) ints to out -- chunks per segment, segments
+ * per (b,h), state units per segment, chunks per unit, the resident
  * output-kernel CTAs the segment length was sized for (0 for the generic
- * kernels) -- and returns how many it wrote (0 if out is NULL or n < 0). */
+ * kernels), 1 if the call ran as a single kernel (the warp-specialised
+ * family computing each segment's state sum itself, all CTAs resident at
+ * once), and the CUDA error code with which the device refused that single
+ * launch when the call fell back to two kernels (else 0) -- and returns how
+ * many it wrote (0 if out is NULL or n < 0).  The
+ * plan is a function of the problem alone (shape and branches), so the
+ * workspace size query agrees with every call on any device. */
 int mamba_mimo_last_plan(int* out, int n);
 
 /* Name of the i-th kernel the last mamba_mimo_bwd_fwd call on this thread

@@ -127,9 +127,10 @@ def device_status(stream=None) -> None:
 
 def last_plan() -> dict:
     """Launch plan of the last successful call on this thread."""
-    buf = (ctypes.c_int * 5)()
-    n = load_library().mamba_mimo_last_plan(buf, 5)
-    keys = ("chunks_per_segment", "segments", "units_per_segment", "chunks_per_unit", "output_slots")
+    buf = (ctypes.c_int * 7)()
+    n = load_library().mamba_mimo_last_plan(buf, 7)
+    keys = ("chunks_per_segment", "segments", "units_per_segment", "chunks_per_unit", "output_slots",
+            "single_kernel", "single_kernel_refused")
     return dict(zip(keys, list(buf)[:n]))
 
 

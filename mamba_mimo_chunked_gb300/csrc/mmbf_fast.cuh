@@ -150,14 +150,24 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 // Wait for phase `parity` of the barrier for at most about a second; false
-// if it did not complete (the caller reports the error and stops).
+// if it did not complete (the caller reports the error and stops).  After a
+// first check the thread sleeps in try_wait (suspend-time hint of 20 us: it
+// resumes as soon as the phase completes) instead of spinning, so waiting
+// warps take no issue slots from the warps they wait for.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    if (ok) return true;
     if (global_ns() - t0 > kWaitLimitNs) return false;
-  return true;
+  }
 }
 // Generic-proxy shared-memory writes before later async-proxy (TMA) writes
 // to the same bytes.

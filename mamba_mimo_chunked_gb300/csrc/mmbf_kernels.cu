@@ -159,6 +159,7 @@ struct Params {
   int reduced, has_z, has_d, vec_p;  // vec_p: P even (pairs of p are 4-byte aligned)
   int fast;                          // index of the shape-specialised kernels, or -1
   int tc;                            // 1: the warp-specialised tensor-core output kernel (mmbf_tc.cuh)
+  int fused;                         // 1: its single-kernel form (phase A in the kernel, cooperative launch)
   int UA, LA, nunit;                 // state units per segment, chunks per unit, units per head
   const uint16_t *dout, *q, *k, *v, *z, *trap;
   const float *q_bias, *k_bias, *mimo_v, *mimo_o, *mimo_z, *angles, *da_cs, *da_cs_rev, *dt,
@@ -169,6 +170,7 @@ struct Params {
   int want_y;
   float *ws_state, *ws_decay, *ws_grad;
   unsigned int* ws_count;  // per (b,h): output CTAs done (specialised kernels)
+  unsigned int* ws_flag;   // per (b,h) and segment: its sum is published (single-kernel form)
   unsigned int* ws_err;    // device-side error word: (tag << 8) | code of the failing call
   unsigned int tag;        // call tag (24 bits) for ws_err
   int test_flags;          // test hooks (mamba_mimo_set_test_hooks); 0 in normal use
@@ -824,7 +826,8 @@ static thread_local int g_stage_count = 0;
 static thread_local cudaError_t g_stage_error = cudaSuccess;
 static thread_local int g_failed_stage = -1;  // kernel index of a failed launch
 static thread_local int g_variant = -1;       // kernel family of the last call
-static thread_local int g_plan[5] = {0, 0, 0, 0, 0};  // L, nseg, UA, LA, resident output CTAs
+static thread_local int g_plan[7] = {0, 0, 0, 0, 0, 0, 0};  // L, nseg, UA, LA, output slots, single kernel, refusal
+static thread_local int g_fused_refused = 0;  // error code of a refused single-kernel launch (diagnostic)
 static thread_local unsigned int g_last_tag = 0;           // tag of this thread's last call
 static thread_local int g_test_flags = 0;                  // mamba_mimo_set_test_hooks
 static thread_local const unsigned int* g_last_err_word = nullptr;
@@ -842,6 +845,7 @@ static const char* const kStageNames[4] = {"segment_state", "segment_prefix", "c
                                            "grad_reduce"};
 static const char* const kFastStageNames[3] = {"segment_state", "segment_prefix", "chunk_output"};
 static const char* const kTcStageNames[2] = {"segment_state", "chunk_output"};
+static const char* const kTcFusedStageNames[1] = {"chunk_output"};
 static thread_local const char* const* g_stage_names = kStageNames;  // kernels of the last call
 static thread_local int g_stage_names_n = 4;
 
@@ -1054,8 +1058,18 @@ static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduc
   // the warp-specialised tensor-core output kernel: R4 C16 N=P=64, reduced
   // dout (mimo_o given), without the forward output y
   p.tc = (p.fast == 0 && p.reduced && !p.want_y) ? 1 : 0;
+  p.fused = 0;
   if (p.fast >= 0) {
     p.L = fast_segment_length(p, fast_slots(p));
+    if (p.tc) {
+      // the single-kernel form: one wave of one CTA per SM (every CTA resident
+      // at once), the shortest segments that allow it
+      const int64_t per_head = kPlanSms / ((int64_t)p.B * p.H);
+      if (per_head >= 1) {
+        const int64_t L1 = (p.nc + per_head - 1) / per_head;
+        if (L1 <= tc::TCfg<4>::LMAX) p.L = (int)L1;
+      }
+    }
     p.nseg = (p.nc + p.L - 1) / p.L;
     // The state-sum kernel works on units of about L/UA chunks, the UA units
     // of a segment one thread-block cluster: more CTAs in flight, shorter
@@ -1080,6 +1094,9 @@ static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduc
     p.LA = (p.L + ua - 1) / ua;
     p.UA = (p.L + p.LA - 1) / p.LA;
     p.nunit = p.nseg * p.UA;
+    // single-kernel form: every CTA resident at once (one per SM) and the
+    // segment's token scalars in shared memory
+    p.fused = (p.tc && (int64_t)p.B * p.H * p.nseg <= kPlanSms && p.L <= tc::TCfg<4>::LMAX) ? 1 : 0;
   }
   *out = p;
   return MMBF_OK;
@@ -1104,7 +1121,8 @@ static size_t workspace_bytes_of(const Params& p) {
   const size_t dec = align16((size_t)p.B * p.H * n * 4);
   const size_t gr = align16((size_t)p.B * p.H * n * 2 * p.R * p.P * 4);
   const size_t cnt = align16((size_t)p.B * p.H * 4);
-  return kWsHeader + st + dec + gr + cnt + 256;
+  const size_t flg = align16((size_t)p.B * p.H * n * 4);
+  return kWsHeader + st + dec + gr + cnt + flg + 256;
 }
 
 // ---- tensor maps of the TMA kernels (cuTensorMapEncodeTiled through the
@@ -1297,15 +1315,44 @@ static int& tc_smem_set() {
   if (d == kMaxDevices) v[d] = 0;
   return v[d];
 }
-static cudaError_t launch_tc(const Params& p, cudaStream_t st, int* launches) {
+static cudaError_t launch_tc(Params& p, cudaStream_t st, int* launches) {
   using T = tc::TCfg<4>;
   using KS = StateCfg<FastA>;
   const size_t ss = fast_state_smem<FastA>(p);
   const int mode = (p.has_z && p.has_d) ? 7 : -1;
-  cudaError_t e = ensure_smem(fast::state_kernel<KS>, ss, &fast_state_smem_set<FastA>());
-  if (e == cudaSuccess)
-    e = mode == 7 ? ensure_smem(tc::out_kernel<T, 7>, T::SMEM, &tc_smem_set<7>())
-                  : ensure_smem(tc::out_kernel<T, -1>, T::SMEM, &tc_smem_set<-1>());
+  cudaError_t e = mode == 7 ? ensure_smem(tc::out_kernel<T, 7>, T::SMEM, &tc_smem_set<7>())
+                            : ensure_smem(tc::out_kernel<T, -1>, T::SMEM, &tc_smem_set<-1>());
+  if (e != cudaSuccess) return e;
+  if (p.fused && !(p.test_flags & 2)) {
+    // single kernel, all CTAs resident at once (they wait for their head's
+    // earlier segments); a device that cannot hold the grid takes the two-
+    // kernel form below
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B * p.H, p.nseg);
+    cfg.blockDim = dim3(T::NT);
+    cfg.dynamicSmemBytes = T::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    g_stage_names = kTcFusedStageNames;
+    g_stage_names_n = 1;
+    g_failed_stage = 0;
+    stage_event(0, 0, st);
+    e = mode == 7 ? cudaLaunchKernelEx(&cfg, tc::out_kernel<T, 7>, p) : cudaLaunchKernelEx(&cfg, tc::out_kernel<T, -1>, p);
+    stage_event(0, 1, st);
+    if (e == cudaSuccess) {
+      (*launches)++;
+      return e;
+    }
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    cudaGetLastError();
+    g_fused_refused = (int)e;
+  }
+  p.fused = 0;
+  e = ensure_smem(fast::state_kernel<KS>, ss, &fast_state_smem_set<FastA>());
   if (e != cudaSuccess) return e;
   g_stage_names = kTcStageNames;
   g_stage_names_n = 2;
@@ -1470,6 +1517,8 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
   p.ws_grad = reinterpret_cast<float*>(ws);
   ws += align16((size_t)p.B * p.H * wsn * 2 * p.R * p.P * 4);
   p.ws_count = reinterpret_cast<unsigned int*>(ws);
+  ws += align16((size_t)p.B * p.H * 4);
+  p.ws_flag = reinterpret_cast<unsigned int*>(ws);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int launches = 0;
@@ -1490,7 +1539,7 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
   }
   if (fast_ok) {
     if (p.tc) {
-      e = launch_tc(p, st, &launches);
+      e = launch_tc(p, st, &launches);  // (clears p.fused if it takes the two-kernel form)
     } else {
       switch (p.fast) {
         case 0: e = launch_fast<FastA>(p, st, &launches); break;
@@ -1504,6 +1553,9 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
     }
     g_variant = p.tc ? 3 : p.fast;
     g_plan[0] = p.L; g_plan[1] = p.nseg; g_plan[2] = p.UA; g_plan[3] = p.LA; g_plan[4] = fast_slots(p);
+    g_plan[5] = p.fused;
+    g_plan[6] = g_fused_refused;
+    g_fused_refused = 0;
     if (e != cudaSuccess)
       return fail(MMBF_ERR_CUDA, "CUDA error in %s (fast %d, grid %d x %d/%d): %s",
                   g_failed_stage >= 0 ? g_stage_names[g_failed_stage] : "setup", p.fast, p.B * p.H,
@@ -1576,7 +1628,7 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
                 out_layout(p).total, cudaGetErrorString(e));
   g_launches = launches;
   g_variant = -1;
-  g_plan[0] = p.L; g_plan[1] = p.nseg; g_plan[2] = 1; g_plan[3] = p.L; g_plan[4] = 0;
+  g_plan[0] = p.L; g_plan[1] = p.nseg; g_plan[2] = 1; g_plan[3] = p.L; g_plan[4] = 0; g_plan[5] = 0; g_plan[6] = 0;
   return MMBF_OK;
 }
 
@@ -1674,7 +1726,7 @@ mmbf_status mamba_mimo_device_status(void* stream) {
 
 int mamba_mimo_last_plan(int* out, int n) {
   if (!out || n < 0) return 0;
-  const int k = n < 5 ? n : 5;
+  const int k = n < 7 ? n : 7;
   for (int i = 0; i < k; i++) out[i] = g_plan[i];
   return k;
 }

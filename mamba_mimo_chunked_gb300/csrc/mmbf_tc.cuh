@@ -29,12 +29,18 @@
 //     8-11  prologue: one 16-row j-block each; biased Q/K, same-token qk_dot
 //           (mma.sync on the diagonal tiles), rotary, k_scaled, k_state,
 //           PsiV, exp(segsum) below the diagonal, the token-scalar table;
-//     12-15 state: the FP32 state (p-block w%4, all n) in registers, folded
-//           with U each chunk; bf16(state) for inter and the states output;
-//           the causal matrix A from S.  Warp 12's first thread issues the
-//           MMAs and the TMA loads of q, k, v, angles and segsum; warp 13's
-//           stores states.
-//   Warp 0's first thread also stores dz (TMA) and loads dout and z.
+//     12-15 state: the causal matrix A of the previous chunk from S; the
+//           FP32 state (p-block w%4, all n) in registers, folded with U each
+//           chunk; bf16(state) for inter and the states output (warp 13's
+//           first thread stores it).  Only the fold and bf16(state) are
+//           serial from chunk to chunk.
+//   The MMAs of a chunk are issued by the warps that wait for their results
+//   anyway, alternating by chunk parity so that no warp carries every issue
+//   (an issue can stall while the tensor pipe works through earlier MMAs):
+//   S and U by warp 12 / 13 one state iteration ahead, inter^T and intra^T
+//   by warp 0 / 4 one epilogue step ahead.
+//   Warp 0's first thread refills ring I once a chunk's MMAs are done; warp
+//   8's loads dout and z (ring O).
 // * Two TMA rings: ring I (q, k, v, angles, segsum; the prologue writes Q_rot
 //   and k_scaled over the raw q and k rows, k_state beside them) is freed when
 //   the chunk's MMAs complete; ring O (PsiV, dout, z -> dz, the qk table) when
@@ -56,7 +62,7 @@ struct TCfg {
   static constexpr int TW = 8, TS = 4 * C;        // token table: window of 8 chunks, 64 floats per chunk
   static constexpr int QKS = K::QKS;              // words per token in the qk table
   static constexpr int NWARP = 16, NT = NWARP * 32;
-  static constexpr int WP = 8, WS = 12;           // first prologue / state warp
+  static constexpr int WP = 8, WS = 12, WM = 16;  // first prologue / state warp, end of the state warps
   // ring I slot
   static constexpr uint32_t I_Q = 0, I_K = 8192, I_KST = 16384, I_V = 24576, I_ANG = 26624, I_SEG = 28672,
                             I_BYTES = 29696;
@@ -70,8 +76,20 @@ struct TCfg {
   // barriers: full / pdone / ofree / fullO per ring slot, the rest per TMEM / tile buffer
   enum : uint32_t {
     B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_M1 = 16, B_M2 = 18, B_SBR = 20, B_SBFREE = 22,
-    B_AR = 24, B_SUFREE = 26, B_XFREE = 28, B_ED = 30, B_TOKW = 32, NBAR = 34
+    B_AR = 24, B_SUFREE = 26, B_XFREE = 28, B_TOKW = 30,
+    // phase A of the single-kernel form: per group TMA (3 buffers), prologue done, MMA done (2 buffers)
+    B_AFULL = 32, B_APA = 44, B_AUA = 48, NBAR = 56
   };
+  // Phase A (the segment's own state sum, single-kernel form), laid over the
+  // ring and tile regions before phase C uses them: per group of four warps
+  // three staging buffers of raw k (k_state is written over it), v and
+  // angles, one PsiV tile per group; the segment's token scalars (factor,
+  // exp(da_cs_rev)) and chunk weights in the A-tile region.
+  static constexpr uint32_t A_K = 0, A_V = 8192, A_ANG = 10240, A_BUF = 12288;
+  static constexpr uint32_t A_RAW = 0, A_PSI = 12 * A_BUF;
+  static constexpr int LMAX = 64;  // longest segment of the single-kernel form
+  static constexpr uint32_t A_FAC = ATT, A_EDR = ATT + LMAX * C * 4, A_GAM = A_EDR + LMAX * C * 4,
+                            A_ALP = A_GAM + LMAX * 4, A_DEC = A_ALP + LMAX * 4;
   static constexpr uint32_t MISC = BAR + NBAR * 8;  // tmem slot, abort flag, last-CTA flag
   static constexpr uint32_t SMEM = MISC + 16 + 1024;  // + alignment slack of the base
   // tensor-memory columns (two buffers of 64 each)
@@ -80,10 +98,36 @@ struct TCfg {
   static_assert(O_QKD + C * QKS * 4 <= O_BYTES, "ring O slot");
   static_assert(I_BYTES % 1024 == 0 && O_BYTES % 1024 == 0 && RO % 1024 == 0 && SBT % 1024 == 0, "alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(A_PSI + 4 * 8192 <= ATT && A_DEC + 16 <= TOK, "phase A layout");
+  static_assert(A_BUF % 1024 == 0 && A_PSI % 1024 == 0 && 4 * 4096 * 4 <= A_PSI, "phase A alignment, reduction scratch");
 };
 
 __device__ __forceinline__ void arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `ns` nanoseconds pass (it does not spin meanwhile, so a
+// waiting warp takes no issue slots from the warps it waits for).
+__device__ __forceinline__ bool try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSleepNs = 20000;  // bound and abort flag are checked every ~20 us of waiting
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // Bounded wait for phase `parity`; false if the CTA is aborting or the wait
@@ -93,7 +137,7 @@ __device__ __forceinline__ bool wait_b(const Params& p, uint32_t bar, uint32_t p
   if (fast::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = fast::global_ns();
   while (true) {
-    if (fast::mbar_try_wait(bar, parity)) return true;
+    if (try_wait_sleep(bar, parity, kSleepNs)) return true;
     if (*abort_flag) return false;
     if (fast::global_ns() - t0 > fast::kWaitLimitNs) {
       *abort_flag = 1u;
@@ -101,6 +145,12 @@ __device__ __forceinline__ bool wait_b(const Params& p, uint32_t bar, uint32_t p
       return false;
     }
   }
+}
+// Bounded wait without the abort protocol (draining copies in flight).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = fast::global_ns();
+  while (!try_wait_sleep(bar, parity, kSleepNs))
+    if (fast::global_ns() - t0 > fast::kWaitLimitNs) break;
 }
 
 // 64x64x64 BF16 MMA, FP32 accumulator in tensor memory (M = N = 64).  A is
@@ -185,7 +235,8 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
   const uint32_t sb = smem_u32(sm);
   const int bh = blockIdx.x, seg = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H, grp = h / (p.H / p.G);
-  const int c0 = seg * p.L, c1 = min(p.nc, c0 + p.L), n = c1 - c0;
+  const int c0 = seg * p.L, c1 = min(p.nc, c0 + p.L);
+  int n = c1 - c0;  // chunks of phase C (0 if phase A stopped)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, cq = lane & 3, mi = lane >> 3, li = lane & 7;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + T::MISC + 4);
@@ -197,8 +248,11 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::mbar_init(bar(T::B_FULLI + i), 1);
       fast::mbar_init(bar(T::B_FULLO + i), 1);
       fast::mbar_init(bar(T::B_PDONE + i), 4);
-      fast::mbar_init(bar(T::B_OFREE + i), 1);
+      fast::mbar_init(bar(T::B_OFREE + i), 8);
     }
+    for (int i = 0; i < 12; i++) fast::mbar_init(bar(T::B_AFULL + i), 1);
+    for (int i = 0; i < 4; i++) fast::mbar_init(bar(T::B_APA + i), 4);
+    for (int i = 0; i < 4; i++) fast::mbar_init(bar(T::B_AUA + i), 4);
     for (int i = 0; i < 2; i++) {
       fast::mbar_init(bar(T::B_M1 + i), 1);
       fast::mbar_init(bar(T::B_M2 + i), 1);
@@ -207,7 +261,6 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::mbar_init(bar(T::B_AR + i), 4);
       fast::mbar_init(bar(T::B_SUFREE + i), 4);
       fast::mbar_init(bar(T::B_XFREE + i), 8);
-      fast::mbar_init(bar(T::B_ED + i), 8);
       fast::mbar_init(bar(T::B_TOKW + i), 4);
     }
     *abort_flag = 0u;
@@ -268,15 +321,195 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     fast::tma_load_4d(base + T::O_DOUT, &p.tm_dout, 0, h, t0, b, full);
     if (HZ) fast::tma_load_4d(base + T::O_Z, &p.tm_z, 0, h, t0, b, full);
   };
-  if (threadIdx.x == T::WS * 32)
-    for (int i = 0; i < min(T::NI - 1, n); i++) load_I(i);
-  if (threadIdx.x == 0)
-    for (int i = 0; i < min(T::NO - 1, n); i++) load_O(i);
+  const unsigned int flag_value = (p.tag << 8) | 0x5au;
+  if (p.fused) {
+    // =====================================================================
+    // Phase A (single-kernel form): this segment's own state sum
+    //   sum = sum_c gamma_c U_c,  gamma_c = prod_{c' > c in the segment} alpha_c',
+    // U_c = PsiV_c^T k_state_c (tcgen05.mma), alpha_c = exp(da_cs[last valid
+    // token of c]) -- the chunk recurrence state = alpha state + U unrolled
+    // over the segment -- and its decay prod alpha_c, published for the
+    // later segments of (b,h).  Four groups of four warps take every fourth
+    // chunk (warp 4w + q: j-block q and tensor-memory lane quarter q of
+    // group w); each keeps its partial sum in registers.
+    // =====================================================================
+    const int na = c1 - c0;
+    uint32_t* afac = reinterpret_cast<uint32_t*>(sm + T::A_FAC);
+    float* aedr = reinterpret_cast<float*>(sm + T::A_EDR);
+    float* agam = reinterpret_cast<float*>(sm + T::A_GAM);
+    float* aalp = reinterpret_cast<float*>(sm + T::A_ALP);
+    float* adec = reinterpret_cast<float*>(sm + T::A_DEC);
+    // token scalars of the segment (the arithmetic of tok_fill)
+    for (int e = threadIdx.x; e < na * C; e += T::NT) {
+      const int tg = c0 * C + e;
+      const int64_t ix = (int64_t)bh * p.S + tg;
+      float dtv = 0.f, trv = 0.f, dtn = 0.f, trn = 0.f, arv = 0.f;
+      if (tg < p.S) {
+        dtv = __ldg(p.dt + ix);
+        trv = bf_f(__ldg(p.trap + ix));
+        arv = __ldg(p.da_cs_rev + ix);
+      }
+      if (tg + 1 < p.S) {
+        dtn = __ldg(p.dt + ix + 1);
+        trn = bf_f(__ldg(p.trap + ix + 1));
+      }
+      const float gam = __fmul_rn(round_bf(dtv), sigmoid_f(trv));
+      float sh = 0.f;
+      if (tg + 1 < p.nc * C) sh = round_bf(__fmul_rn(round_bf(dtn), 1.0f / (1.0f + expf(trn))));
+      afac[e] = fast::dup_bf(__fadd_rn(gam, sh));
+      aedr[e] = expf(arv);
+    }
+    for (int e = threadIdx.x; e < na; e += T::NT) {
+      const int c = c0 + e;
+      aalp[e] = expf(__ldg(p.da_cs + (int64_t)bh * p.S + min(c * C + C, p.S) - 1));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // suffix products gamma_c, and the segment decay
+      float gg = 1.f;
+      for (int e = na - 1; e >= 0; e--) {
+        agam[e] = gg;
+        gg *= aalp[e];
+      }
+      *adec = gg;
+    }
+    __syncthreads();
+    const int w = warp >> 2, q = warp & 3;
+    const int kw = na > w ? (na - w + 3) / 4 : 0;  // chunks of group w: w + 4k
+    const bool gl = (q == 0) && lane == 0;         // the group's TMA thread
+    const uint16_t* kbs = reinterpret_cast<const uint16_t*>(sm + T::KBS);
+    const uint16_t* mvb = reinterpret_cast<const uint16_t*>(sm + T::MVB);
+    const uint16_t* psa = reinterpret_cast<const uint16_t*>(sm + T::A_PSI + w * 8192);
+    auto abuf = [&](int k) { return (uint32_t)(T::A_RAW + (w * 3 + k % 3) * T::A_BUF); };
+    auto load_A = [&](int k) {
+      const int t0 = (c0 + w + 4 * k) * C;
+      const uint32_t dst = sb + abuf(k), full = bar(T::B_AFULL + w * 3 + k % 3);
+      uint32_t bytes = 8192 + C * P * 2 + C * T::W * 4;
+      if (w == 0 && k == 0 && (p.test_flags & 1)) bytes += 16;  // test hook: this wait runs out
+      fast::mbar_expect_tx(full, bytes);
+      fast::tma_load_5d(dst + T::A_K, &p.tm_k, 0, grp, 0, t0, b, full);
+      fast::tma_load_4d(dst + T::A_V, &p.tm_v, 0, h, t0, b, full);
+      fast::tma_load_4d(dst + T::A_ANG, &p.tm_ang, 0, h, t0, b, full);
+    };
+    int loaded_a = 0;
+    if (gl) {
+      loaded_a = min(3, kw);
+      for (int k = 0; k < loaded_a; k++) load_A(k);
+    }
+    // acc: the group's running sum over its chunks c_0 < c_1 < ... (stride 4),
+    // acc = (prod of alpha over (c_{k-1}, c_k]) acc + U_{c_k}, so that at the
+    // end gamma_{c_last} acc = sum_k gamma_{c_k} U_{c_k}
+    float acc[8][4];
+#pragma unroll
+    for (int nn = 0; nn < 8; nn++) acc[nn][0] = acc[nn][1] = acc[nn][2] = acc[nn][3] = 0.f;
+    for (int k = 0; k < kw; k++) {
+      const int i = w + 4 * k;
+      unsigned char* bp = sm + abuf(k);
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_AFULL + w * 3 + k % 3), (k / 3) & 1, abort_flag, 1))) break;
+      uint32_t kf[4][4];
+      fast::load_rows<K>(kf, reinterpret_cast<const uint16_t*>(bp + T::A_K), 16 * q);
+      fast::add_bias<K>(kf, kbs);
+      fast::rotate_direct<K, false>(kf, kf, reinterpret_cast<const float*>(bp + T::A_ANG), 16 * q);
+      fast::scale_k<K>(kf, afac + i * C, 16 * q);
+      fast::k_state<K>(kf, aedr + i * C, 16 * q);
+      __syncwarp();  // this warp's raw k rows are read before k_state overwrites them
+      fast::store_rows<K, true>(kf, reinterpret_cast<uint16_t*>(bp + T::A_K), 16 * q);
+      // the group's PsiV tile and chunk k - 1's staging buffer are free once
+      // every warp of the group has added chunk k - 1; the buffer takes chunk k + 2
+      if (k >= 1 && !__all_sync(kFull, wait_b(p, bar(T::B_AUA + w), (k - 1) & 1, abort_flag, 4))) break;
+      if (gl && k >= 1 && k + 2 < kw) {
+        load_A(k + 2);
+        loaded_a = k + 3;
+      }
+      fast::psi_rows<K>(reinterpret_cast<const uint16_t*>(bp + T::A_V), mvb, const_cast<uint16_t*>(psa), 16 * q);
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_APA + w));
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_APA + w), k & 1, abort_flag, 4))) break;
+      // decay from the group's previous chunk through this one: prod of alpha over (c_{k-1}, c_k]
+      const float dk = k >= 1 ? ((aalp[i - 3] * aalp[i - 2]) * aalp[i - 1]) * aalp[i] : 1.f;
+      fast::state_mma<K>(acc, psa, reinterpret_cast<const uint16_t*>(bp + T::A_K), dk, q, 0);
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_AUA + w));
+    }
+    if (kw > 0) {
+      const float gl_last = agam[w + 4 * (kw - 1)];
+#pragma unroll
+      for (int nn = 0; nn < 8; nn++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) acc[nn][e] *= gl_last;
+    }
+    __syncwarp();
+    if (gl && *abort_flag)  // every staging load landed before the area is reused
+      for (int k = max(0, loaded_a - 3); k < loaded_a; k++) drain_wait(bar(T::B_AFULL + w * 3 + k % 3), (k / 3) & 1);
+    __syncthreads();
+    // the four group partials, summed in group order, published with a flag
+    float* red4 = reinterpret_cast<float*>(sm + T::A_RAW);  // [4][N][P] FP32 over the staging area
+    {
+#pragma unroll
+      for (int nn = 0; nn < 8; nn++)
+#pragma unroll
+        for (int e = 0; e < 4; e++)
+          red4[w * N * P + (8 * nn + 2 * cq + (e & 1)) * P + 16 * q + g + 8 * (e >> 1)] = acc[nn][e];
+    }
+    __syncthreads();
+    if (!*abort_flag) {
+      if (seg + 1 < p.nseg) {  // (the last segment's sum is never needed)
+        float* dsts = p.ws_state + ((int64_t)bh * p.nseg + seg) * N * P;
+        for (int e = threadIdx.x; e < N * P; e += T::NT)
+          dsts[e] = ((red4[e] + red4[N * P + e]) + red4[2 * N * P + e]) + red4[3 * N * P + e];
+      }
+      if (threadIdx.x == 0) {
+        p.ws_decay[(int64_t)bh * p.nseg + seg] = *adec;
+        if (seg == 0) p.ws_count[bh] = 0u;  // read by this head's CTAs after they saw this flag
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0)
+        asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p.ws_flag + (int64_t)bh * p.nseg + seg),
+                     "r"(flag_value)
+                     : "memory");
+    }
+    __syncthreads();
+    if (*abort_flag) n = 0;  // phase A stopped: no phase C (the error word is set)
+  }
+  const int first_i = min(T::NI, n), first_o = min(T::NO, n);  // loads issued below (thread 0)
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < first_i; i++) load_I(i);
+    for (int i = 0; i < first_o; i++) load_O(i);
+  }
 
   // ---- the state entering this segment: the segment sums of the earlier
   //      segments of (b,h) folded in order (acc = acc * decay_s + sum_s),
   //      every thread below 512 eight consecutive elements
-  fast::pdl_wait();
+  if (p.fused) {
+    // the earlier segments of this head have published their sums (all CTAs
+    // of a single-kernel launch are resident at once: a cooperative launch)
+    for (int s2 = threadIdx.x; n > 0 && s2 < seg; s2 += T::NT) {
+      const unsigned int* f = p.ws_flag + (int64_t)bh * p.nseg + s2;
+      const uint64_t t0 = fast::global_ns();
+      while (true) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(f) : "memory");
+        if (v == flag_value) break;
+        if (*abort_flag) break;
+        if (fast::global_ns() - t0 > fast::kWaitLimitNs) {
+          *abort_flag = 1u;
+          atomicExch(p.ws_err, (p.tag << 8) | 5u);
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    __syncthreads();
+    if (*abort_flag) {  // a wait ran out: no phase C; the first loads land before the CTA leaves
+      if (threadIdx.x == 0) {
+        for (int i = 0; i < first_i; i++) drain_wait(bar(T::B_FULLI + i), 0);
+        for (int i = 0; i < first_o; i++) drain_wait(bar(T::B_FULLO + i), 0);
+      }
+      n = 0;
+    }
+  } else {
+    fast::pdl_wait();
+  }
   float* xs = reinterpret_cast<float*>(sm + T::SBT);  // 16 KB scratch (SB and A tiles are unused yet)
   if (threadIdx.x < 512) {
     float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
@@ -311,7 +544,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
   // State warps: their FP32 state^T slice (p-block q, all n) in the 16x256b
   // fragment layout: st[nn][e] = state[n = 8nn + 2cq + (e&1)][p = 16q + g + 8(e>>1)].
   float st[8][4];
-  if (warp >= T::WS) {
+  if (warp >= T::WS && warp < T::WM) {
     const int q = warp - T::WS;
 #pragma unroll
     for (int nn = 0; nn < 8; nn++)
@@ -327,10 +560,10 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     return tok_of(i)[2 * C + min(c * C + C, p.S) - 1 - c * C];
   };
 
-  int loaded_o = min(T::NO - 1, n);  // ring O chunks issued (thread 0)
   if (warp < T::WP) {
     // =====================================================================
-    // Epilogue warps
+    // Epilogue warps: pure compute on chunks whose inter^T / intra^T are in
+    // tensor memory; dz goes straight to global memory.
     // =====================================================================
     const int q = warp & 3, hc = warp >> 2;
     const uint32_t tl_lane = (uint32_t)(32 * q) << 16;
@@ -349,13 +582,19 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     float2 cdmo[4], cdmz[4];
 #pragma unroll
     for (int o = 0; o < 4; o++) cdmo[o] = cdmz[o] = make_float2(0.f, 0.f);
+    int loaded_i = min(T::NI, n);  // ring I chunks issued (thread 0)
     for (int i = 0; i < n; i++) {
       const int c = c0 + i, so = i % T::NO, s2 = i & 1;
-      const uint32_t obase = sb + T::RO + so * T::O_BYTES;
       unsigned char* op = sm + T::RO + so * T::O_BYTES;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_M2 + s2), (i >> 1) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + i % T::NI), (i / T::NI) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLO + so), (i / T::NO) & 1, abort_flag, 1))) break;
+      // every MMA of chunk c is done (and the prologue and A-step before it):
+      // its ring I slot takes chunk c + NI
+      if (threadIdx.x == 0 && i + T::NI < n) {
+        load_I(i + T::NI);
+        loaded_i = i + T::NI + 1;
+      }
       fast::tm_fence_after();
       float vi[4][4], vx[4][4];
       fast::tm_ld_frag<4>(tmem + tl_lane + T::T_I + 64 * s2 + 32 * hc, vi);
@@ -366,7 +605,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       const float* tok = tok_of(i);
       const uint16_t* psi = reinterpret_cast<const uint16_t*>(op + T::O_PSI);
       const uint32_t* qkd = reinterpret_cast<const uint32_t*>(op + T::O_QKD);
-      uint16_t* zt = reinterpret_cast<uint16_t*>(op + T::O_Z);
+      const uint16_t* zt = reinterpret_cast<const uint16_t*>(op + T::O_Z);
       const uint16_t* dt_ = reinterpret_cast<const uint16_t*>(op + T::O_DOUT);
 #pragma unroll
       for (int tt = 0; tt < 2; tt++) {
@@ -428,38 +667,22 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
             cdmo[o] = fast::fma_bf2_f32(ob, dob, cdmo[o]);
           }
         }
-        if (HZ) {  // dz over the z values this thread has read; stored by TMA
-          zt[fast::swz128(tl, pr)] = (uint16_t)(dzacc & 0xffffu);
-          zt[fast::swz128(tl, pr + 8)] = (uint16_t)(dzacc >> 16);
+        const int tg = c * C + tl;
+        if (HZ && tg < p.S) {  // dz[b, t, h, p] and [.., p + 8]
+          uint16_t* dzp = p.dz + (((int64_t)b * p.S + tg) * p.H + h) * P + pr;
+          dzp[0] = (uint16_t)(dzacc & 0xffffu);
+          dzp[8] = (uint16_t)(dzacc >> 16);
         }
       }
-      // dz of chunk c leaves by TMA once all epilogue warps wrote it; then the
-      // ring O slot of chunk c - 1 is free (its dz store has read it) and
-      // takes chunk c - 1 + NO
-      // (every epilogue warp arrives, with or without dz: the slot refill
-      // below must not overtake a warp still reading chunk c - 1)
-      if (HZ) fast::fence_proxy_async();
+      // this warp is done with the chunk's ring O slot
       __syncwarp();
-      if (lane == 0) arrive(bar(T::B_ED + s2));
-      bool ok = true;
-      if (threadIdx.x == 0) {
-        ok = wait_b(p, bar(T::B_ED + s2), (i >> 1) & 1, abort_flag, 3);
-        if (ok) {
-          if (HZ) {
-            fast::tma_store_4d(&p.tm_dz, obase + T::O_Z, 0, h, c * C, b);
-            asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
-          }
-          if (i >= 1) arrive(bar(T::B_OFREE + (i - 1) % T::NO));
-          if (i + T::NO - 1 < n) {
-            fast::fence_proxy_async();
-            load_O(i + T::NO - 1);
-            loaded_o = i + T::NO;
-          }
-        }
-      }
-      if (!__all_sync(kFull, ok)) break;
+      if (lane == 0) arrive(bar(T::B_OFREE + so));
     }
-    if (threadIdx.x == 0) fast::tma_store_wait_all();
+    if (threadIdx.x == 0 && *abort_flag)  // after an abort: the ring I loads in flight land first
+      for (int i = max(0, loaded_i - T::NI); i < loaded_i; i++) {
+        const uint32_t bf = bar(T::B_FULLI + i % T::NI), ph = (i / T::NI) & 1;
+        drain_wait(bf, ph);
+      }
     // ---- fixed-order reduction of the dmimo partials of this segment:
     //      the four lanes of a row group (tokens), then the two warps of a
     //      p-block (token halves)
@@ -474,7 +697,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       }
     }
     // red[hc][which][o][p] (FP32, 2 x 2 x 4 x 64) in ring I slot 0 (idle now)
-    // after the final barrier below
+    // after the barrier below
     __syncwarp();
     fast::tm_fence_before();
     __syncthreads();  // (A) every role has left its loop
@@ -491,11 +714,15 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     }
   } else if (warp < T::WS) {
     // =====================================================================
-    // Prologue warps: one 16-row j-block each
+    // Prologue warps: one 16-row j-block each.  Thread 0 of warp 8 also
+    // loads dout and z into ring O slots the epilogue has released.
     // =====================================================================
     const int jw = warp - T::WP, j0 = 16 * jw, pt = threadIdx.x - T::WP * 32;
+    const bool load_thread = pt == 0;  // issues the ring O loads
+    int loaded_o = min(T::NO, n);
     const uint16_t* qbs = reinterpret_cast<const uint16_t*>(sm + T::QBS);
     const uint16_t* kbs = reinterpret_cast<const uint16_t*>(sm + T::KBS);
+
     const uint16_t* mvb = reinterpret_cast<const uint16_t*>(sm + T::MVB);
     fast::TokRaw traw = tok_load<T>(p, bh, c0, pt);
     for (int i = 0; i < n; i++) {
@@ -508,18 +735,25 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
         if (c + T::TW < c1) traw = tok_load<T>(p, bh, c + T::TW, pt);
         __syncwarp();
         if (lane == 0) arrive(bar(T::B_TOKW + (wi & 1)));
-        if (!__all_sync(kFull, wait_b(p, bar(T::B_TOKW + (wi & 1)), (wi >> 1) & 1, abort_flag, 4))) break;
+        if (!__all_sync(kFull, wait_b(p, bar(T::B_TOKW + (wi & 1)), (wi >> 1) & 1, abort_flag, 4)))
+          break;
       }
       const float* tok = tok_of(i);
-      if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLI + si), (i / T::NI) & 1, abort_flag, 1))) break;
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLI + si), (i / T::NI) & 1, abort_flag, 1)))
+        break;
       if (!__all_sync(kFull, i < T::NO || wait_b(p, bar(T::B_OFREE + so), ((i / T::NO) - 1) & 1, abort_flag, 4)))
         break;
+      if (load_thread && i >= T::NO) {  // the epilogue is done with this ring O slot: dout, z of chunk c
+        fast::fence_proxy_async();
+        load_O(i);
+        loaded_o = i + 1;
+      }
       uint16_t* qt = reinterpret_cast<uint16_t*>(ip + T::I_Q);
       uint16_t* kt = reinterpret_cast<uint16_t*>(ip + T::I_K);
       uint32_t qf[4][4], kf[4][4];
       fast::load_rows<K>(qf, qt, j0);
       fast::load_rows<K>(kf, kt, j0);
-      fast::add_bias<K>(qf, qbs);
+      fast::add_bias<K>(qf, qbs);  // bf16(q + bf16(bias)), bf16(k + bf16(bias))
       fast::add_bias<K>(kf, kbs);
       {  // same-token qk_dot from the diagonal 16x16 tile of Qh Kh^T
         uint32_t* qkd = reinterpret_cast<uint32_t*>(op + T::O_QKD);
@@ -567,45 +801,45 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       if (lane == 0) arrive(bar(T::B_PDONE + si));
     }
     __syncwarp();
+    if (load_thread && *abort_flag)  // after an abort: the ring O loads in flight land first
+      for (int i = max(0, loaded_o - T::NO); i < loaded_o; i++) {
+        const uint32_t bf = bar(T::B_FULLO + i % T::NO), ph = (i / T::NO) & 1;
+        drain_wait(bf, ph);
+      }
+    __syncwarp();
     fast::tm_fence_before();
     __syncthreads();  // (A)
-  } else {
+  } else if (warp < T::WM) {
     // =====================================================================
-    // State warps: p-block q of the state; the causal matrix rows of block q.
-    // The first thread of warp 12 issues the MMAs and the ring I loads, the
-    // first of warp 13 stores states.
+    // State warps: p-block q of the FP32 state in registers and rows 16q..
+    // of the causal matrix.  Per chunk: bf16(state entering the chunk) for
+    // inter^T and the states output; A = bf16(mask(Q_rot Ks^T) exp(segsum))
+    // for j-block q (mma.sync on the prologue's tiles, causal blocks only);
+    // the fold state = alpha state + PsiV^T k_state (mma.sync into the
+    // register state).  Then one thread issues inter^T and intra^T on
+    // tcgen05.mma (warp 12's for even chunks, warp 13's for odd ones: an
+    // issue can stall while the tensor pipe works), and warp 14's stores
+    // states.
     // =====================================================================
     const int q = warp - T::WS;
-    const uint32_t tl_lane = (uint32_t)(32 * q) << 16;
-    const bool issuer = threadIdx.x == T::WS * 32;
-    const bool store_thread = threadIdx.x == T::WS * 32 + 32;
-    int loaded_i = min(T::NI - 1, n);  // ring I chunks issued (issuer)
-    int commits = 0;                   // tcgen05.commit issued (the last one covers every MMA)
-    uint32_t last_bar = 0, last_par = 0;
+    const bool store_thread = threadIdx.x == T::WS * 32 + 64;
+    const bool mma_even = threadIdx.x == T::WS * 32, mma_odd = threadIdx.x == T::WS * 32 + 32;
+    int last_m2 = -1;  // last chunk whose inter^T / intra^T this thread committed
+    {  // blocks of A above the token-block diagonal stay 0 (both buffers)
+      uint16_t* at = reinterpret_cast<uint16_t*>(sm + T::ATT);
+      for (int e = lane; e < 2 * 16 * 8; e += 32) {  // 2 buffers x 16 rows x 8 chunks of 16 bytes
+        const int bf = e / 128, r = (e / 8) % 16, ch = e % 8;
+        if (ch >= 2 * (q + 1))
+          *reinterpret_cast<uint4*>(at + bf * 4096 + fast::swz128(16 * q + r, ch * 8)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    bool alive = true;
     for (int i = 0; i < n; i++) {
       const int c = c0 + i, s2 = i & 1, si = i % T::NI, so = i % T::NO;
-      const uint32_t ib = sb + T::RI + si * T::I_BYTES, ob = sb + T::RO + so * T::O_BYTES;
-      if (i >= 1) {  // state = state * exp(da_cs[last of chunk c-1]) + U_{c-1}
-        fast::tm_fence_after();
-        fast::fold_u<K>(st, tmem + tl_lane + T::T_U + 64 * ((i - 1) & 1), decay_of(i - 1));
-        fast::tm_fence_before();
-        __syncwarp();
-        if (lane == 0) arrive(bar(T::B_SUFREE + ((i - 1) & 1)));
-      }
-      bool ok = true;
-      if (issuer) {  // S = Q_rot Ks^T and U = PsiV^T k_state of chunk c
-        ok = wait_b(p, bar(T::B_PDONE + si), (i / T::NI) & 1, abort_flag, 2) &&
-             (i < 2 || wait_b(p, bar(T::B_SUFREE + s2), ((i - 2) >> 1) & 1, abort_flag, 2));
-        if (ok) {
-          fast::tm_fence_after();
-          mma64<false, false>(tmem + T::T_S + 64 * s2, ib + T::I_Q, ib + T::I_K);
-          mma64<true, true>(tmem + T::T_U + 64 * s2, ob + T::O_PSI, ib + T::I_KST);
-          mma_commit(bar(T::B_M1 + s2));
-          commits++; last_bar = bar(T::B_M1 + s2); last_par = (i >> 1) & 1;
-        }
-      }
-      if (!__all_sync(kFull, ok)) break;
-      // bf16(state) -> SB tile [n][p] (inter's operand and states[c])
+      unsigned char* ip = sm + T::RI + si * T::I_BYTES;
+      unsigned char* op = sm + T::RO + so * T::O_BYTES;
+      // bf16(state entering chunk c) -> SB tile [n][p]; its buffer and the A
+      // buffer are free once chunk c - 2's inter^T / intra^T are done
       if (i >= 2) {
         if (!__all_sync(kFull, wait_b(p, bar(T::B_M2 + s2), ((i - 2) >> 1) & 1, abort_flag, 2))) break;
         if (!__all_sync(kFull, wait_b(p, bar(T::B_SBFREE + s2), ((i - 2) >> 1) & 1, abort_flag, 2))) break;
@@ -619,9 +853,58 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
         const uint32_t r3 = fast::pack2(make_float2(st[2 * nn + 1][2], st[2 * nn + 1][3]));
         fast::stsm_x4_t(sbt + fast::swz128(nn * 16 + (mi >> 1) * 8 + li, q * 16 + (mi & 1) * 8), r0, r1, r2, r3);
       }
-      fast::fence_proxy_async();
+      // the chunk's operands (Q_rot, k_scaled, k_state, PsiV, exp(segsum))
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + si), (i / T::NI) & 1, abort_flag, 2))) break;
+      {  // A rows 16q..: S = Q_rot Ks^T on causal blocks jb <= q, rows and columns in tile order
+        const uint16_t* qt = reinterpret_cast<const uint16_t*>(ip + T::I_Q);
+        const uint16_t* kt = reinterpret_cast<const uint16_t*>(ip + T::I_K);
+        const float* es = reinterpret_cast<const float*>(ip + T::I_SEG);
+        uint16_t* at = reinterpret_cast<uint16_t*>(sm + T::ATT + s2 * 8192);
+        uint32_t qf[4][4];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; k4++)
+          ldsm_x4(qf[k4][0], qf[k4][1], qf[k4][2], qf[k4][3],
+                  qt + fast::swz128(16 * q + (lane & 15), k4 * 16 + (lane >> 4) * 8));
+        const int trow = 4 * q + (g >> 1);
+        for (int jb = 0; jb <= q; jb++) {
+          float sa[2][4];
+#pragma unroll
+          for (int ht = 0; ht < 2; ht++) sa[ht][0] = sa[ht][1] = sa[ht][2] = sa[ht][3] = 0.f;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; k4++) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(b0, b1, b2, b3, kt + fast::swz128(16 * jb + (mi >> 1) * 8 + li, k4 * 16 + (mi & 1) * 8));
+            mma16816(sa[0], qf[k4][0], qf[k4][1], qf[k4][2], qf[k4][3], b0, b1);
+            mma16816(sa[1], qf[k4][0], qf[k4][1], qf[k4][2], qf[k4][3], b2, b3);
+          }
+          // exp(segsum) of (row token, column token): 0 unless the row's token is later
+          const float e = es[trow * C + 4 * jb + cq];
+          const float2 e2 = make_float2(e, e);
+          const uint32_t r0 = fast::pack2(__fmul2_rn(make_float2(sa[0][0], sa[0][1]), e2));
+          const uint32_t r1 = fast::pack2(__fmul2_rn(make_float2(sa[0][2], sa[0][3]), e2));
+          const uint32_t r2 = fast::pack2(__fmul2_rn(make_float2(sa[1][0], sa[1][1]), e2));
+          const uint32_t r3 = fast::pack2(__fmul2_rn(make_float2(sa[1][2], sa[1][3]), e2));
+          fast::stsm_x4(at + fast::swz128(16 * q + li + 8 * (mi & 1), 16 * jb + 8 * (mi >> 1)), r0, r1, r2, r3);
+        }
+      }
+      // state = state * exp(da_cs[last of chunk c]) + PsiV^T k_state
+      fast::state_mma<K>(st, reinterpret_cast<const uint16_t*>(op + T::O_PSI),
+                         reinterpret_cast<const uint16_t*>(ip + T::I_KST), decay_of(i), q, 0);
+      fast::fence_proxy_async();  // SB and A tiles before the MMAs read them
       __syncwarp();
       if (lane == 0) arrive(bar(T::B_SBR + s2));
+      bool ok = true;
+      if ((i & 1) ? mma_odd : mma_even) {  // inter^T and intra^T of chunk c
+        ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2) &&
+             (i < 2 || wait_b(p, bar(T::B_XFREE + s2), ((i - 2) >> 1) & 1, abort_flag, 2));
+        if (ok) {
+          fast::tm_fence_after();
+          mma64<true, false>(tmem + T::T_I + 64 * s2, sb + T::SBT + s2 * 8192, sb + T::RI + si * T::I_BYTES + T::I_Q);
+          mma64<true, false>(tmem + T::T_X + 64 * s2, sb + T::RO + so * T::O_BYTES + T::O_PSI, sb + T::ATT + s2 * 8192);
+          mma_commit(bar(T::B_M2 + s2));
+          last_m2 = i;
+        }
+      }
       if (store_thread) {  // states[c] = bf16(state entering chunk c): one tile store
         ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2);
         if (ok) {
@@ -632,86 +915,21 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
           }
         }
       }
-      if (!__all_sync(kFull, ok)) break;
-      // A = bf16(S * exp(segsum)) strictly below the token diagonal, 0 elsewhere
-      if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + si), (i / T::NI) & 1, abort_flag, 2))) break;
-      if (!__all_sync(kFull, wait_b(p, bar(T::B_M1 + s2), (i >> 1) & 1, abort_flag, 2))) break;
-      fast::tm_fence_after();
-      float sv[8][4];
-      fast::tm_ld_frag<8>(tmem + tl_lane + T::T_S + 64 * s2, sv);
-      const float* es = reinterpret_cast<const float*>(sm + T::RI + si * T::I_BYTES + T::I_SEG);
-      const int trow = 4 * q + (g >> 1);
-      uint16_t* at = reinterpret_cast<uint16_t*>(sm + T::ATT + s2 * 8192);
-#pragma unroll
-      for (int kb = 0; kb < 4; kb++) {  // 16 columns (one j-block) per stsm
-        const float e = es[trow * C + 4 * kb + cq];
-        const float2 e2 = make_float2(e, e);
-        const uint32_t r0 = fast::pack2(__fmul2_rn(make_float2(sv[2 * kb][0], sv[2 * kb][1]), e2));
-        const uint32_t r1 = fast::pack2(__fmul2_rn(make_float2(sv[2 * kb][2], sv[2 * kb][3]), e2));
-        const uint32_t r2 = fast::pack2(__fmul2_rn(make_float2(sv[2 * kb + 1][0], sv[2 * kb + 1][1]), e2));
-        const uint32_t r3 = fast::pack2(__fmul2_rn(make_float2(sv[2 * kb + 1][2], sv[2 * kb + 1][3]), e2));
-        fast::stsm_x4(at + fast::swz128(16 * q + li + 8 * (mi & 1), 16 * kb + 8 * (mi >> 1)), r0, r1, r2, r3);
+      if (!__all_sync(kFull, ok)) {
+        alive = false;
+        break;
       }
-      fast::fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) arrive(bar(T::B_AR + s2));
-      if (issuer) {  // inter^T and intra^T of chunk c; then the ring I refill
-        ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2) &&
-             wait_b(p, bar(T::B_AR + s2), (i >> 1) & 1, abort_flag, 2) &&
-             (i < 2 || wait_b(p, bar(T::B_XFREE + s2), ((i - 2) >> 1) & 1, abort_flag, 2));
-        if (ok) {
-          fast::tm_fence_after();
-          mma64<true, false>(tmem + T::T_I + 64 * s2, sb + T::SBT + s2 * 8192, ib + T::I_Q);
-          mma64<true, false>(tmem + T::T_X + 64 * s2, ob + T::O_PSI, sb + T::ATT + s2 * 8192);
-          mma_commit(bar(T::B_M2 + s2));
-          commits++; last_bar = bar(T::B_M2 + s2); last_par = (i >> 1) & 1;
-          // chunk i + NI - 1 into the ring I slot of chunk i - 1 once its MMAs are done
-          if (i + T::NI - 1 < n) {
-            ok = i < 1 || wait_b(p, bar(T::B_M2 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag, 2);
-            if (ok) {
-              load_I(i + T::NI - 1);
-              loaded_i = i + T::NI;
-            }
-          }
-        }
-      }
-      if (!__all_sync(kFull, ok)) break;
     }
     __syncwarp();
-    if (issuer) {
-      // every MMA completes before tensor memory is released (bounded)
-      if (commits > 0) {
-        const uint64_t t0 = fast::global_ns();
-        while (!fast::mbar_try_wait(last_bar, last_par))
-          if (fast::global_ns() - t0 > fast::kWaitLimitNs) break;
-      }
-      // after an abort: the ring I loads in flight land first (the last NI
-      // issued are the latest use of their slots)
-      if (*abort_flag)
-        for (int i = max(0, loaded_i - T::NI); i < loaded_i; i++) {
-          const uint32_t bf = bar(T::B_FULLI + i % T::NI), ph = (i / T::NI) & 1;
-          const uint64_t t0 = fast::global_ns();
-          while (!fast::mbar_try_wait(bf, ph))
-            if (fast::global_ns() - t0 > fast::kWaitLimitNs) break;
-        }
-    }
     if (store_thread) fast::tma_store_wait_all();
+    if ((mma_even || mma_odd) && last_m2 >= 0)  // its MMAs complete before tensor memory is released
+      drain_wait(bar(T::B_M2 + (last_m2 & 1)), (last_m2 >> 1) & 1);
     __syncwarp();
     fast::tm_fence_before();
     __syncthreads();  // (A)
   }
 
-  // ---- (after barrier A) after an abort the ring O loads in flight land
-  //      before the CTA leaves; then the dmimo partials of this segment and
-  //      the release of tensor memory
-  if (threadIdx.x == 0 && *abort_flag) {
-    for (int i = max(0, loaded_o - T::NO); i < loaded_o; i++) {
-      const uint32_t bf = bar(T::B_FULLO + i % T::NO), ph = (i / T::NO) & 1;
-      const uint64_t t0 = fast::global_ns();
-      while (!fast::mbar_try_wait(bf, ph))
-        if (fast::global_ns() - t0 > fast::kWaitLimitNs) break;
-    }
-  }
+  // ---- (after barrier A) the dmimo partials of this segment; tensor memory released
   __syncthreads();  // (B) red[] complete
   if (warp == T::WS) {
     fast::tm_fence_after();

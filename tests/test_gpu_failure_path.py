@@ -30,13 +30,15 @@ def rel_rms(a, b):
     return float(np.sqrt(np.mean((a - b) ** 2)) / np.sqrt(np.mean(b ** 2)))
 
 
-def test_bounded_wait_reports_timeout_and_context_recovers(cuda_lib):
+@pytest.mark.parametrize("form", [0, 2])  # the single-kernel form, the two-kernel form
+def test_bounded_wait_reports_timeout_and_context_recovers(cuda_lib, form):
     lib = mm.load_library()
     inp = tma_shape_inputs(5)
-    lib.mamba_mimo_set_test_hooks(1)
+    lib.mamba_mimo_set_test_hooks(1 | form)
     try:
         mm.mamba_mimo_bwd_fwd(*dev(inp))
         assert mm.last_kernel_variant() == 3
+        assert mm.last_plan()["single_kernel"] == (0 if form else 1)
         with pytest.raises(TimeoutError, match="barrier wait ran out"):
             mm.device_status()
     finally:

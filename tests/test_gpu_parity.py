@@ -174,7 +174,7 @@ def test_timed_workload_all_heads():
     inp = si.make_inputs(**wl.shape_kwargs(), seed=si.WORKLOAD_SEED_BASE + 2, device="cuda")
     got = mm.mamba_mimo_bwd_fwd(*si.args_of(inp))
     torch.cuda.synchronize()
-    assert mm.last_kernel_variant() == 3
+    assert mm.last_kernel_variant() == 3 and mm.last_plan()["single_kernel"] == 1
     cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     want = oracle.bwd_fwd(*si.args_of(cpu))
     compare(got, want, wl.name)
@@ -326,3 +326,36 @@ def test_workspace_size_independent_of_device():
     for B, S, H, G, R, N, P, C, div, red, z in shapes:
         here.append(mm.workspace_size(B, S, H, G, R, N, P, C, div, bool(red), bool(z)))
     assert here == no_gpu
+
+
+# --- both forms of the warp-specialised tensor-core family -------------------
+
+@pytest.mark.parametrize("two_kernel", [False, True])
+@pytest.mark.parametrize("kw", [
+    dict(seqlen=200, heads=2, has_z=True, has_d=True),                  # several segments
+    dict(seqlen=1000, heads=3, groups=1, has_z=True, has_d=False),      # ragged tail
+    dict(seqlen=64, batch=2, heads=4, groups=2, has_z=False, has_d=True),
+    dict(seqlen=16, heads=1, has_z=True, has_d=True),                   # one chunk
+])
+def test_tensor_core_family_forms(kw, two_kernel):
+    lib = mm.load_library()
+    lib.mamba_mimo_set_test_hooks(2 if two_kernel else 0)
+    try:
+        inp = unit_inputs(recipe="workload", **kw)
+        got = run_gpu(inp)
+        assert mm.last_kernel_variant() == 3
+        assert mm.last_plan()["single_kernel"] == (0 if two_kernel else 1)
+        assert mm.last_launch_count() == (2 if two_kernel else 1)
+    finally:
+        lib.mamba_mimo_set_test_hooks(0)
+    compare(got, oracle.bwd_fwd(*si.args_of(inp)), str(kw))
+
+
+def test_timed_workload_two_kernel_form_sampled_heads():
+    lib = mm.load_library()
+    lib.mamba_mimo_set_test_hooks(2)
+    try:
+        sampled_heads(2, [(0, 0), (0, 9)])
+        assert mm.last_plan()["single_kernel"] == 0
+    finally:
+        lib.mamba_mimo_set_test_hooks(0)
