@@ -76,7 +76,7 @@ struct TCfg {
   // barriers: full / pdone / ofree / fullO per ring slot, the rest per TMEM / tile buffer
   enum : uint32_t {
     B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_M1 = 16, B_M2 = 18, B_SBR = 20, B_SBFREE = 22,
-    B_AR = 24, B_SUFREE = 26, B_XFREE = 28, B_TOKW = 30,
+    B_PSI = 24, B_XFREE = 28, B_TOKW = 30,
     // phase A of the single-kernel form: per group TMA (3 buffers), prologue done, MMA done (2 buffers)
     B_AFULL = 32, B_APA = 44, B_AUA = 48, NBAR = 56
   };
@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::mbar_init(bar(T::B_FULLI + i), 1);
       fast::mbar_init(bar(T::B_FULLO + i), 1);
       fast::mbar_init(bar(T::B_PDONE + i), 4);
+      fast::mbar_init(bar(T::B_PSI + i), 8);
       fast::mbar_init(bar(T::B_OFREE + i), 8);
     }
     for (int i = 0; i < 12; i++) fast::mbar_init(bar(T::B_AFULL + i), 1);
@@ -258,8 +259,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::mbar_init(bar(T::B_M2 + i), 1);
       fast::mbar_init(bar(T::B_SBR + i), 4);
       fast::mbar_init(bar(T::B_SBFREE + i), 1);
-      fast::mbar_init(bar(T::B_AR + i), 4);
-      fast::mbar_init(bar(T::B_SUFREE + i), 4);
+
       fast::mbar_init(bar(T::B_XFREE + i), 8);
       fast::mbar_init(bar(T::B_TOKW + i), 4);
     }
@@ -404,6 +404,13 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     for (int k = 0; k < kw; k++) {
       const int i = w + 4 * k;
       unsigned char* bp = sm + abuf(k);
+      // chunk k - 1 is done by every warp of the group: its staging buffer
+      // takes chunk k + 2 (and the group's PsiV tile is free)
+      if (k >= 1 && !__all_sync(kFull, wait_b(p, bar(T::B_AUA + w), (k - 1) & 1, abort_flag, 4))) break;
+      if (gl && k >= 1 && k + 2 < kw) {
+        load_A(k + 2);
+        loaded_a = k + 3;
+      }
       if (!__all_sync(kFull, wait_b(p, bar(T::B_AFULL + w * 3 + k % 3), (k / 3) & 1, abort_flag, 1))) break;
       uint32_t kf[4][4];
       fast::load_rows<K>(kf, reinterpret_cast<const uint16_t*>(bp + T::A_K), 16 * q);
@@ -413,13 +420,6 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::k_state<K>(kf, aedr + i * C, 16 * q);
       __syncwarp();  // this warp's raw k rows are read before k_state overwrites them
       fast::store_rows<K, true>(kf, reinterpret_cast<uint16_t*>(bp + T::A_K), 16 * q);
-      // the group's PsiV tile and chunk k - 1's staging buffer are free once
-      // every warp of the group has added chunk k - 1; the buffer takes chunk k + 2
-      if (k >= 1 && !__all_sync(kFull, wait_b(p, bar(T::B_AUA + w), (k - 1) & 1, abort_flag, 4))) break;
-      if (gl && k >= 1 && k + 2 < kw) {
-        load_A(k + 2);
-        loaded_a = k + 3;
-      }
       fast::psi_rows<K>(reinterpret_cast<const uint16_t*>(bp + T::A_V), mvb, const_cast<uint16_t*>(psa), 16 * q);
       __syncwarp();
       if (lane == 0) arrive(bar(T::B_APA + w));
@@ -583,9 +583,28 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
 #pragma unroll
     for (int o = 0; o < 4; o++) cdmo[o] = cdmz[o] = make_float2(0.f, 0.f);
     int loaded_i = min(T::NI, n);  // ring I chunks issued (thread 0)
-    for (int i = 0; i < n; i++) {
+    // PsiV = bf16(v * bf16(mimo_v)) of chunk j, rows 8w.. of the tile, into
+    // its ring O slot (free once chunk j - NO is done by every epilogue warp)
+    const uint16_t* mvb = reinterpret_cast<const uint16_t*>(sm + T::MVB);
+    auto psi_step = [&](int j) -> bool {
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLI + j % T::NI), (j / T::NI) & 1, abort_flag, 1))) return false;
+      if (!__all_sync(kFull, j < T::NO ||
+                                 wait_b(p, bar(T::B_OFREE + j % T::NO), ((j / T::NO) - 1) & 1, abort_flag, 3)))
+        return false;
+      fast::psi_rows<K, 8>(reinterpret_cast<const uint16_t*>(sm + T::RI + (j % T::NI) * T::I_BYTES + T::I_V), mvb,
+                           reinterpret_cast<uint16_t*>(sm + T::RO + (j % T::NO) * T::O_BYTES + T::O_PSI), 8 * warp);
+      fast::fence_proxy_async();  // the MMAs read PsiV
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_PSI + j % T::NO));
+      return true;
+    };
+    bool alive = true;
+    for (int j = 0; alive && j < min(2, n); j++) alive = psi_step(j);
+    for (int i = 0; alive && i < n; i++) {
       const int c = c0 + i, so = i % T::NO, s2 = i & 1;
       unsigned char* op = sm + T::RO + so * T::O_BYTES;
+      if (i + 2 < n && !psi_step(i + 2)) break;
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_PSI + so), (i / T::NO) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_M2 + s2), (i >> 1) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + i % T::NI), (i / T::NI) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLO + so), (i / T::NO) & 1, abort_flag, 1))) break;
@@ -789,13 +808,6 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::store_rows<K, true>(kf, kt, j0);  // k_scaled
       fast::k_state<K>(kf, tok + 3 * C, j0);
       fast::store_rows<K, true>(kf, reinterpret_cast<uint16_t*>(ip + T::I_KST), j0);
-      fast::psi_rows<K>(reinterpret_cast<const uint16_t*>(ip + T::I_V), mvb,
-                        reinterpret_cast<uint16_t*>(op + T::O_PSI), j0);
-      {  // exp(segsum) strictly below the diagonal, 0 elsewhere (a select), in place
-        float* sg = reinterpret_cast<float*>(ip + T::I_SEG);
-#pragma unroll
-        for (int e = pt; e < C * C; e += 128) sg[e] = ((e % C) < (e / C)) ? fast::exp_fast(sg[e]) : 0.f;
-      }
       fast::fence_proxy_async();
       __syncwarp();
       if (lane == 0) arrive(bar(T::B_PDONE + si));
@@ -877,8 +889,11 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
             mma16816(sa[0], qf[k4][0], qf[k4][1], qf[k4][2], qf[k4][3], b0, b1);
             mma16816(sa[1], qf[k4][0], qf[k4][1], qf[k4][2], qf[k4][3], b2, b3);
           }
-          // exp(segsum) of (row token, column token): 0 unless the row's token is later
-          const float e = es[trow * C + 4 * jb + cq];
+          // exp(segsum) of (row token, column token) if the row's token is
+          // later, else 0 (a select: the entries on and above the diagonal
+          // are never read)
+          const int tcol = 4 * jb + cq;
+          const float e = trow > tcol ? fast::exp_fast(es[trow * C + tcol]) : 0.f;
           const float2 e2 = make_float2(e, e);
           const uint32_t r0 = fast::pack2(__fmul2_rn(make_float2(sa[0][0], sa[0][1]), e2));
           const uint32_t r1 = fast::pack2(__fmul2_rn(make_float2(sa[0][2], sa[0][3]), e2));
@@ -887,7 +902,9 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
           fast::stsm_x4(at + fast::swz128(16 * q + li + 8 * (mi & 1), 16 * jb + 8 * (mi >> 1)), r0, r1, r2, r3);
         }
       }
-      // state = state * exp(da_cs[last of chunk c]) + PsiV^T k_state
+      // state = state * exp(da_cs[last of chunk c]) + PsiV^T k_state (PsiV
+      // comes from the epilogue warps)
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_PSI + so), (i / T::NO) & 1, abort_flag, 2))) break;
       fast::state_mma<K>(st, reinterpret_cast<const uint16_t*>(op + T::O_PSI),
                          reinterpret_cast<const uint16_t*>(ip + T::I_KST), decay_of(i), q, 0);
       fast::fence_proxy_async();  // SB and A tiles before the MMAs read them
