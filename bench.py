@@ -48,7 +48,7 @@ KERNEL_DIR = os.path.join(ROOT, "mamba_mimo_chunked_gb300", "csrc")
 # The sources of the first stage's kernels (the dominant kernel's traffic in
 # profiles/ is valid while these are unchanged; the second stage's kernels
 # live in mmbb.cuh).
-FIRST_STAGE_SOURCES = ("mmbf_fast.cuh", "mmbf_kernels.cu")
+FIRST_STAGE_SOURCES = ("mmbf_fast.cuh", "mmbf_tc.cuh", "mmbf_kernels.cu")
 
 
 def kernel_source_sha256():
@@ -57,6 +57,12 @@ def kernel_source_sha256():
     for name in FIRST_STAGE_SOURCES:
         h.update(open(os.path.join(KERNEL_DIR, name), "rb").read())
     return h.hexdigest()
+# Tensor instructions of each first-stage kernel family (by its variant number)
+TENSOR_PATHS = {
+    3: "tcgen05.mma kind::f16 M=64 N=64 K=16, TMEM accumulators (inter, intra); "
+       "mma.sync m16n8k16 bf16 (causal scores, state fold, same-token qk_dot)",
+    0: "mma.sync m16n8k16 bf16 (inter, scores, intra, qk_dot); tcgen05.mma state sums",
+}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -479,6 +485,7 @@ def main():
         if st:
             mm._raise(lib, st)
     launches_per_call = lib.mamba_mimo_last_launch_count()
+    variant = lib.mamba_mimo_last_kernel_variant()
 
     # Per-kernel CUDA events are taken in a separate, untimed pass after the
     # timed region: an event recorded between two kernels of a call keeps the
@@ -655,7 +662,7 @@ def main():
         "op_hbm_frac": alg_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
         "tensor": {"achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
                    "kernel": DOMINANT, "algorithmic_flop_per_launch": alg_flop,
-                   "peak_source": tpeak_kind, "path": "mma.sync m16n8k16 bf16"},
+                   "peak_source": tpeak_kind, "path": TENSOR_PATHS.get(variant, "mma.sync m16n8k16 bf16")},
         "stage_ms": stage_ms,
         "gpu_launches": launches_per_call * args.steps,
         "e2e": e2e,

@@ -490,6 +490,19 @@ template <class K>
 __device__ __forceinline__ int kst_off(int row, int col) {
   return K::UMMA ? swz128(op_row<K>(row), col) : swz<K::LDN>(row, col);
 }
+// The same tiles indexed by physical row, for a contraction over all rows
+// (the state update): both operands share the row order, so the sum may
+// visit rows as stored.  Eight consecutive physical rows are eight different
+// swizzle chunks (conflict-free matrix loads); eight consecutive logical rows
+// of the fragment order are not.
+template <class K>
+__device__ __forceinline__ int psi_off_phys(int row, int col) {
+  return K::UMMA ? swz128(row, col) : swz<K::LDP>(row, col);
+}
+template <class K>
+__device__ __forceinline__ int kst_off_phys(int row, int col) {
+  return K::UMMA ? swz128(row, col) : swz<K::LDN>(row, col);
+}
 
 // Offset of (n, p) in the BF16 state tile [N][P]: the TMA swizzle when it is
 // stored by TMA, else the conflict-free swizzle.
@@ -727,12 +740,12 @@ __device__ __forceinline__ void state_mma(float (&st)[K::NN8][4], const uint16_t
 #pragma unroll
   for (int kb = 0; kb < K::NWJ; kb++) {
     uint32_t a0, a1, a2_, a3;
-    ldsm_x4_t(a0, a1, a2_, a3, Psi + psi_off<K>(kb * 16 + (mi >> 1) * 8 + li, pm * 16 + (mi & 1) * 8));
+    ldsm_x4_t(a0, a1, a2_, a3, Psi + psi_off_phys<K>(kb * 16 + (mi >> 1) * 8 + li, pm * 16 + (mi & 1) * 8));
 #pragma unroll
     for (int nn = 0; nn < K::NN8 / 2; nn++) {
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(b0, b1, b2, b3,
-                Kst + kst_off<K>(kb * 16 + (mi & 1) * 8 + li, nbase + nn * 16 + (mi >> 1) * 8));
+                Kst + kst_off_phys<K>(kb * 16 + (mi & 1) * 8 + li, nbase + nn * 16 + (mi >> 1) * 8));
       mma16816(st[2 * nn], a0, a1, a2_, a3, b0, b1);
       mma16816(st[2 * nn + 1], a0, a1, a2_, a3, b2, b3);
     }

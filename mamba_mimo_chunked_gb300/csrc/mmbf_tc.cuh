@@ -73,13 +73,14 @@ struct TCfg {
                             TOK = ATT + 2 * 8192, MVB = TOK + 2 * TW * TS * 4, QBS = MVB + R * P * 2,
                             KBS = QBS + R * K::LDB * 2, MZP = KBS + R * K::LDB * 2, MOP = MZP + R * 4 * 8 * 8,
                             BAR = MOP + R * 4 * 8 * 4;
-  // barriers: full / pdone / ofree / fullO per ring slot, the rest per TMEM / tile buffer
+  // barriers: full / pdone / ofree / fullO / PsiV per ring slot, the rest
+  // per tensor-memory / tile buffer (two) or one
   enum : uint32_t {
-    B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_M1 = 16, B_M2 = 18, B_SBR = 20, B_SBFREE = 22,
-    B_PSI = 24, B_XFREE = 28, B_TOKW = 30,
+    B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_PSI = 16, B_M1 = 20, B_M2 = 21, B_SBR = 23, B_TOKW = 25,
     // phase A of the single-kernel form: per group TMA (3 buffers), prologue done, MMA done (2 buffers)
-    B_AFULL = 32, B_APA = 44, B_AUA = 48, NBAR = 56
+    B_AFULL = 27, B_APA = 39, B_AUA = 43, NBAR = 47
   };
+
   // Phase A (the segment's own state sum, single-kernel form), laid over the
   // ring and tile regions before phase C uses them: per group of four warps
   // three staging buffers of raw k (k_state is written over it), v and
@@ -90,7 +91,7 @@ struct TCfg {
   static constexpr int LMAX = 64;  // longest segment of the single-kernel form
   static constexpr uint32_t A_FAC = ATT, A_EDR = ATT + LMAX * C * 4, A_GAM = A_EDR + LMAX * C * 4,
                             A_ALP = A_GAM + LMAX * 4, A_DEC = A_ALP + LMAX * 4;
-  static constexpr uint32_t MISC = BAR + NBAR * 8;  // tmem slot, abort flag, last-CTA flag
+  static constexpr uint32_t MISC = BAR + ((NBAR * 8 + 15) & ~15u);  // tmem slot, abort flag, last-CTA flag
   static constexpr uint32_t SMEM = MISC + 16 + 1024;  // + alignment slack of the base
   // tensor-memory columns (two buffers of 64 each)
   static constexpr uint32_t T_S = 0, T_U = 128, T_I = 256, T_X = 384;
@@ -254,13 +255,12 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     for (int i = 0; i < 12; i++) fast::mbar_init(bar(T::B_AFULL + i), 1);
     for (int i = 0; i < 4; i++) fast::mbar_init(bar(T::B_APA + i), 4);
     for (int i = 0; i < 4; i++) fast::mbar_init(bar(T::B_AUA + i), 4);
+    fast::mbar_init(bar(T::B_M1), 1);
     for (int i = 0; i < 2; i++) {
-      fast::mbar_init(bar(T::B_M1 + i), 1);
       fast::mbar_init(bar(T::B_M2 + i), 1);
-      fast::mbar_init(bar(T::B_SBR + i), 4);
-      fast::mbar_init(bar(T::B_SBFREE + i), 1);
-
-      fast::mbar_init(bar(T::B_XFREE + i), 8);
+      // chunk c's issue: the four state warps, the eight epilogue warps
+      // done with chunk c - 2's products, and the eight writers of PsiV of c + 1
+      fast::mbar_init(bar(T::B_SBR + i), 4 + 8 + 8);
       fast::mbar_init(bar(T::B_TOKW + i), 4);
     }
     *abort_flag = 0u;
@@ -595,15 +595,31 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
                            reinterpret_cast<uint16_t*>(sm + T::RO + (j % T::NO) * T::O_BYTES + T::O_PSI), 8 * warp);
       fast::fence_proxy_async();  // the MMAs read PsiV
       __syncwarp();
-      if (lane == 0) arrive(bar(T::B_PSI + j % T::NO));
+      if (lane == 0) {
+        arrive(bar(T::B_PSI + j % T::NO));
+        if (j >= 1) arrive(bar(T::B_SBR + ((j - 1) & 1)));  // U_j goes out with chunk j - 1's products
+      }
       return true;
     };
+    // PsiV of chunk j (j < n); at j = n only the share of the last chunk's
+    // issue barrier that PsiV of a next chunk would have given
+    auto psi_or_last = [&](int j) -> bool {
+      if (j < n) return psi_step(j);
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_SBR + ((n - 1) & 1)));
+      return true;
+    };
+    // the first two chunks' tensor-memory buffers are free from the start
+    if (lane == 0) {
+      if (n > 0) arrive(bar(T::B_SBR));
+      if (n > 1) arrive(bar(T::B_SBR + 1));
+    }
     bool alive = true;
-    for (int j = 0; alive && j < min(2, n); j++) alive = psi_step(j);
+    for (int j = 0; alive && n > 0 && j <= min(1, n); j++) alive = psi_or_last(j);
     for (int i = 0; alive && i < n; i++) {
       const int c = c0 + i, so = i % T::NO, s2 = i & 1;
       unsigned char* op = sm + T::RO + so * T::O_BYTES;
-      if (i + 2 < n && !psi_step(i + 2)) break;
+      if (i + 2 <= n && !psi_or_last(i + 2)) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_PSI + so), (i / T::NO) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_M2 + s2), (i >> 1) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + i % T::NI), (i / T::NI) & 1, abort_flag, 3))) break;
@@ -620,7 +636,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::tm_ld_frag<4>(tmem + tl_lane + T::T_X + 64 * s2 + 32 * hc, vx);
       fast::tm_fence_before();
       __syncwarp();
-      if (lane == 0) arrive(bar(T::B_XFREE + s2));
+      if (lane == 0 && i + 2 < n) arrive(bar(T::B_SBR + s2));  // this parity's buffers take chunk c + 2
       const float* tok = tok_of(i);
       const uint16_t* psi = reinterpret_cast<const uint16_t*>(op + T::O_PSI);
       const uint32_t* qkd = reinterpret_cast<const uint32_t*>(op + T::O_QKD);
@@ -824,19 +840,20 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
   } else if (warp < T::WM) {
     // =====================================================================
     // State warps: p-block q of the FP32 state in registers and rows 16q..
-    // of the causal matrix.  Per chunk: bf16(state entering the chunk) for
-    // inter^T and the states output; A = bf16(mask(Q_rot Ks^T) exp(segsum))
-    // for j-block q (mma.sync on the prologue's tiles, causal blocks only);
-    // the fold state = alpha state + PsiV^T k_state (mma.sync into the
-    // register state).  Then one thread issues inter^T and intra^T on
-    // tcgen05.mma (warp 12's for even chunks, warp 13's for odd ones: an
-    // issue can stall while the tensor pipe works), and warp 14's stores
-    // states.
+    // of the causal matrix.  Per chunk c: the state entering c, folded from
+    // the one entering c - 1 and U of chunk c - 1 (tensor memory; its MMA
+    // went out with chunk c - 2's products, so it is long done); bf16 of it
+    // for inter^T and the states output; A = bf16(mask(Q_rot Ks^T)
+    // exp(segsum)) for j-block q (mma.sync on the prologue's tiles, causal
+    // blocks only).  Then one thread (warp 12's for even chunks, warp 13's
+    // for odd ones) stores states[c] and issues inter^T, intra^T of c and U
+    // of c + 1 on tcgen05.mma.  Only the fold is serial from chunk to chunk.
     // =====================================================================
     const int q = warp - T::WS;
-    const bool store_thread = threadIdx.x == T::WS * 32 + 64;
     const bool mma_even = threadIdx.x == T::WS * 32, mma_odd = threadIdx.x == T::WS * 32 + 32;
-    int last_m2 = -1;  // last chunk whose inter^T / intra^T this thread committed
+    const uint32_t tl_lane = (uint32_t)(32 * q) << 16;
+    int last_m2 = -1;  // last chunk whose MMAs this thread committed
+    bool u0 = false;   // U of the first chunk issued (committed to B_M1)
     {  // blocks of A above the token-block diagonal stay 0 (both buffers)
       uint16_t* at = reinterpret_cast<uint16_t*>(sm + T::ATT);
       for (int e = lane; e < 2 * 16 * 8; e += 32) {  // 2 buffers x 16 rows x 8 chunks of 16 bytes
@@ -845,16 +862,39 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
           *reinterpret_cast<uint4*>(at + bf * 4096 + fast::swz128(16 * q + r, ch * 8)) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+    // U of the first chunk: PsiV^T k_state, into tensor-memory buffer 0
     bool alive = true;
-    for (int i = 0; i < n; i++) {
+    if (mma_even && n > 0) {
+      alive = wait_b(p, bar(T::B_PSI), 0, abort_flag, 2) && wait_b(p, bar(T::B_PDONE), 0, abort_flag, 2);
+      if (alive) {
+        fast::tm_fence_after();
+        mma64<true, true>(tmem + T::T_U, sb + T::RO + T::O_PSI, sb + T::RI + T::I_KST);
+        mma_commit(bar(T::B_M1));
+        u0 = true;
+      }
+    }
+    alive = __all_sync(kFull, alive);
+    for (int i = 0; alive && i < n; i++) {
       const int c = c0 + i, s2 = i & 1, si = i % T::NI, so = i % T::NO;
       unsigned char* ip = sm + T::RI + si * T::I_BYTES;
-      unsigned char* op = sm + T::RO + so * T::O_BYTES;
-      // bf16(state entering chunk c) -> SB tile [n][p]; its buffer and the A
-      // buffer are free once chunk c - 2's inter^T / intra^T are done
-      if (i >= 2) {
-        if (!__all_sync(kFull, wait_b(p, bar(T::B_M2 + s2), ((i - 2) >> 1) & 1, abort_flag, 2))) break;
-        if (!__all_sync(kFull, wait_b(p, bar(T::B_SBFREE + s2), ((i - 2) >> 1) & 1, abort_flag, 2))) break;
+      // state entering chunk c = round(state * alpha_{c-1}) + U_{c-1} (FP32).
+      // Chunk c - 2's MMAs are done: U_{c-1} is ready and the SB / A buffers
+      // of this parity are free (and so is the states store that read SB).
+      if (i >= 1) {
+        if (!__all_sync(kFull, i >= 2 ? wait_b(p, bar(T::B_M2 + s2), ((i - 2) >> 1) & 1, abort_flag, 2)
+                                      : wait_b(p, bar(T::B_M1), 0, abort_flag, 2)))
+          break;
+        fast::tm_fence_after();
+        float u[8][4];
+        fast::tm_ld_frag<8>(tmem + tl_lane + T::T_U + 64 * ((i - 1) & 1), u);
+        const float a = decay_of(i - 1);
+        const float2 a2 = make_float2(a, a);
+#pragma unroll
+        for (int nn = 0; nn < 8; nn++) {
+          const float2 x = __fadd2_rn(__fmul2_rn(make_float2(st[nn][0], st[nn][1]), a2), make_float2(u[nn][0], u[nn][1]));
+          const float2 y = __fadd2_rn(__fmul2_rn(make_float2(st[nn][2], st[nn][3]), a2), make_float2(u[nn][2], u[nn][3]));
+          st[nn][0] = x.x; st[nn][1] = x.y; st[nn][2] = y.x; st[nn][3] = y.y;
+        }
       }
       uint16_t* sbt = reinterpret_cast<uint16_t*>(sm + T::SBT + s2 * 8192);
 #pragma unroll
@@ -865,8 +905,12 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
         const uint32_t r3 = fast::pack2(make_float2(st[2 * nn + 1][2], st[2 * nn + 1][3]));
         fast::stsm_x4_t(sbt + fast::swz128(nn * 16 + (mi >> 1) * 8 + li, q * 16 + (mi & 1) * 8), r0, r1, r2, r3);
       }
-      // the chunk's operands (Q_rot, k_scaled, k_state, PsiV, exp(segsum))
-      if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + si), (i / T::NI) & 1, abort_flag, 2))) break;
+      // the prologue of chunk c + 1 is done (and so that of c): Q_rot,
+      // k_scaled of c for A, k_state of c + 1 for U_{c+1}
+      {
+        const int jn = min(i + 1, n - 1);
+        if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + jn % T::NI), (jn / T::NI) & 1, abort_flag, 2))) break;
+      }
       {  // A rows 16q..: S = Q_rot Ks^T on causal blocks jb <= q, rows and columns in tile order
         const uint16_t* qt = reinterpret_cast<const uint16_t*>(ip + T::I_Q);
         const uint16_t* kt = reinterpret_cast<const uint16_t*>(ip + T::I_K);
@@ -902,34 +946,28 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
           fast::stsm_x4(at + fast::swz128(16 * q + li + 8 * (mi & 1), 16 * jb + 8 * (mi >> 1)), r0, r1, r2, r3);
         }
       }
-      // state = state * exp(da_cs[last of chunk c]) + PsiV^T k_state (PsiV
-      // comes from the epilogue warps)
-      if (!__all_sync(kFull, wait_b(p, bar(T::B_PSI + so), (i / T::NO) & 1, abort_flag, 2))) break;
-      fast::state_mma<K>(st, reinterpret_cast<const uint16_t*>(op + T::O_PSI),
-                         reinterpret_cast<const uint16_t*>(ip + T::I_KST), decay_of(i), q, 0);
-      fast::fence_proxy_async();  // SB and A tiles before the MMAs read them
+      fast::tm_fence_before();    // U_{c-1} is read before its buffer takes U_{c+1}
+      fast::fence_proxy_async();  // SB and A tiles before the MMAs and the store read them
       __syncwarp();
       if (lane == 0) arrive(bar(T::B_SBR + s2));
       bool ok = true;
-      if ((i & 1) ? mma_odd : mma_even) {  // inter^T and intra^T of chunk c
-        ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2) &&
-             (i < 2 || wait_b(p, bar(T::B_XFREE + s2), ((i - 2) >> 1) & 1, abort_flag, 2));
-        if (ok) {
-          fast::tm_fence_after();
-          mma64<true, false>(tmem + T::T_I + 64 * s2, sb + T::SBT + s2 * 8192, sb + T::RI + si * T::I_BYTES + T::I_Q);
-          mma64<true, false>(tmem + T::T_X + 64 * s2, sb + T::RO + so * T::O_BYTES + T::O_PSI, sb + T::ATT + s2 * 8192);
-          mma_commit(bar(T::B_M2 + s2));
-          last_m2 = i;
-        }
-      }
-      if (store_thread) {  // states[c] = bf16(state entering chunk c): one tile store
+      if ((i & 1) ? mma_odd : mma_even) {
+        // every state warp is done with chunk c, the epilogue has read chunk
+        // c - 2's products, and PsiV of chunk c + 1 is written
         ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2);
         if (ok) {
+          fast::tm_fence_after();
+          // states[c] = bf16(state entering chunk c): one tile store, issued
+          // first so that its read of SB overlaps the MMA issue
           fast::tma_store_2d(&p.tm_states, sb + T::SBT + s2 * 8192, 0, (int)(((int64_t)bh * p.nc + c) * N));
-          if (i >= 1) {
-            asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
-            arrive(bar(T::B_SBFREE + ((i - 1) & 1)));
-          }
+          mma64<true, false>(tmem + T::T_I + 64 * s2, sb + T::SBT + s2 * 8192, sb + T::RI + si * T::I_BYTES + T::I_Q);
+          mma64<true, false>(tmem + T::T_X + 64 * s2, sb + T::RO + so * T::O_BYTES + T::O_PSI, sb + T::ATT + s2 * 8192);
+          if (i + 1 < n)  // U_{c+1} = PsiV_{c+1}^T k_state_{c+1}
+            mma64<true, true>(tmem + T::T_U + 64 * ((i + 1) & 1), sb + T::RO + ((i + 1) % T::NO) * T::O_BYTES + T::O_PSI,
+                              sb + T::RI + ((i + 1) % T::NI) * T::I_BYTES + T::I_KST);
+          asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");  // SB read before the buffer is released
+          mma_commit(bar(T::B_M2 + s2));
+          last_m2 = i;
         }
       }
       if (!__all_sync(kFull, ok)) {
@@ -938,9 +976,12 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       }
     }
     __syncwarp();
-    if (store_thread) fast::tma_store_wait_all();
-    if ((mma_even || mma_odd) && last_m2 >= 0)  // its MMAs complete before tensor memory is released
-      drain_wait(bar(T::B_M2 + (last_m2 & 1)), (last_m2 >> 1) & 1);
+    if (mma_even || mma_odd) {
+      fast::tma_store_wait_all();
+      if (last_m2 >= 0)  // its MMAs complete before tensor memory is released
+        drain_wait(bar(T::B_M2 + (last_m2 & 1)), (last_m2 >> 1) & 1);
+      if (u0) drain_wait(bar(T::B_M1), 0);
+    }
     __syncwarp();
     fast::tm_fence_before();
     __syncthreads();  // (A)
