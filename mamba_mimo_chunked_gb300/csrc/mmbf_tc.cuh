@@ -76,9 +76,9 @@ struct TCfg {
   // barriers: full / pdone / ofree / fullO / PsiV per ring slot, the rest
   // per tensor-memory / tile buffer (two) or one
   enum : uint32_t {
-    B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_PSI = 16, B_M1 = 20, B_M2 = 21, B_SBR = 23, B_TOKW = 25,
+    B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_M1 = 16, B_M2 = 17, B_SBR = 19, B_TOKW = 21,
     // phase A of the single-kernel form: per group TMA (3 buffers), prologue done, MMA done (2 buffers)
-    B_AFULL = 27, B_APA = 39, B_AUA = 43, NBAR = 47
+    B_AFULL = 23, B_APA = 35, B_AUA = 39, NBAR = 43
   };
 
   // Phase A (the segment's own state sum, single-kernel form), laid over the
@@ -99,6 +99,7 @@ struct TCfg {
   static_assert(O_QKD + C * QKS * 4 <= O_BYTES, "ring O slot");
   static_assert(I_BYTES % 1024 == 0 && O_BYTES % 1024 == 0 && RO % 1024 == 0 && SBT % 1024 == 0, "alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(W == 16, "register prologue: N / rotary_dim_divisor = 16 rotated pairs");
   static_assert(A_PSI + 4 * 8192 <= ATT && A_DEC + 16 <= TOK, "phase A layout");
   static_assert(A_BUF % 1024 == 0 && A_PSI % 1024 == 0 && 4 * 4096 * 4 <= A_PSI, "phase A alignment, reduction scratch");
 };
@@ -163,17 +164,20 @@ template <bool A_MN, bool B_MN>
 __device__ __forceinline__ void mma64(uint32_t tmem_d, uint32_t a_saddr, uint32_t b_saddr) {
   constexpr uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (A_MN ? (1u << 15) : 0u) |
                              (B_MN ? (1u << 16) : 0u) | ((64u >> 3) << 17) | ((64u >> 4) << 24);
-#pragma unroll
-  for (int ks = 0; ks < 4; ks++) {
-    const uint64_t da = fast::umma_desc_mn128(a_saddr + ks * (A_MN ? 2048u : 32u));
-    const uint64_t db = fast::umma_desc_mn128(b_saddr + ks * (B_MN ? 2048u : 32u));
-    const uint32_t acc = ks > 0 ? 1u : 0u;
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(da), "l"(db), "r"(idesc), "r"(acc)
-        : "memory");
-  }
+  // A K-step moves the start address (descriptor bits 0-13, in 16-byte units)
+  // by 32 bytes (K-major) or 2048 bytes (MN-major); shared-memory addresses
+  // stay below 256 KB, so the field never carries into the bits above it.
+  constexpr uint64_t da = A_MN ? 2048 / 16 : 32 / 16, dbs = B_MN ? 2048 / 16 : 32 / 16;
+  const uint64_t a0 = fast::umma_desc_mn128(a_saddr), b0 = fast::umma_desc_mn128(b_saddr);
+  asm volatile(
+      "{\n .reg .pred p0, p1;\n setp.ne.b32 p0, %9, 0;\n setp.eq.b32 p1, %9, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %5, %3, p1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %7, %3, p1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %10, %3, p1;\n}\n" ::"r"(tmem_d),
+      "l"(a0), "l"(b0), "r"(idesc), "l"(a0 + da), "l"(b0 + dbs), "l"(a0 + 2 * da), "l"(b0 + 2 * dbs),
+      "l"(a0 + 3 * da), "r"(0u), "l"(b0 + 3 * dbs)
+      : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
@@ -183,6 +187,67 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 // Token of physical row i (0..63) of a chunk tile: rows are in perm<4> order
 // inside each 16-row block.
 __device__ __forceinline__ int token_of(int i) { return 4 * (i >> 4) + ((i & 7) >> 1); }
+
+// The prologue of one 16-row j-block with its operands in registers.  With
+// R = 4 every fragment row of a thread (rows perm(g), perm(g + 8) of the
+// block) belongs to token j0/4 + g/2, and the bias row of fragment register
+// e is rank 2(e & 1) + (g & 1).
+template <class T>
+struct RowRegs {
+  // bf16(bias) pairs of the 16 fragment registers
+  uint32_t b[4][4];
+  __device__ __forceinline__ void load(const uint16_t* bias) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c2 = 2 * (lane & 3);
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const int r = 2 * (e & 1) + (g & 1);
+#pragma unroll
+      for (int kt = 0; kt < 4; kt++)
+        b[kt][e] = *reinterpret_cast<const uint32_t*>(bias + r * T::K::LDB + kt * 16 + 8 * (e >> 1) + c2);
+    }
+  }
+};
+// x = bf16(x + bf16(bias)) on every fragment register.
+__device__ __forceinline__ void add_bias_r(uint32_t (&f)[4][4], const uint32_t (&b)[4][4]) {
+#pragma unroll
+  for (int kt = 0; kt < 4; kt++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) f[kt][e] = badd2(f[kt][e], b[kt][e]);
+}
+// Rotary (N = 64, N/4 = 16 rotated pairs (m, 32 + m)): the thread's columns
+// m = 2(lane & 3) + {0, 1} (registers e = 0, 1) and 8 + the same (e = 2, 3)
+// of tile 0 pair with tile 2; a0 / a1 are the token's angles at those
+// columns.  Same arithmetic as the shared-table form.
+template <class K>
+__device__ __forceinline__ void rotate_r(uint32_t (&fq)[4][4], uint32_t (&fk)[4][4], bool with_q, float2 a0,
+                                         float2 a1) {
+  float2 sn0, cs0, sn1, cs1;
+  fast::sincos_fast(a0.x, &sn0.x, &cs0.x);
+  fast::sincos_fast(a0.y, &sn0.y, &cs0.y);
+  fast::sincos_fast(a1.x, &sn1.x, &cs1.x);
+  fast::sincos_fast(a1.y, &sn1.y, &cs1.y);
+#pragma unroll
+  for (int e = 0; e < 4; e++) {
+    const float2 cs = (e >> 1) ? cs1 : cs0, sn = (e >> 1) ? sn1 : sn0;
+    if (with_q) fast::rotate_regs<K>(fq[0][e], fq[2][e], cs, sn);
+    fast::rotate_regs<K>(fk[0][e], fk[2][e], cs, sn);
+  }
+}
+// k_scaled = bf16(k_rot * factor) (BF16 x BF16), factor of the thread's token.
+__device__ __forceinline__ void scale_r(uint32_t (&f)[4][4], uint32_t fd) {
+#pragma unroll
+  for (int kt = 0; kt < 4; kt++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) f[kt][e] = bmul2(f[kt][e], fd);
+}
+// k_state = bf16(k_scaled * exp(da_cs_rev)) (FP32 product), the thread's token.
+__device__ __forceinline__ void kstate_r(uint32_t (&f)[4][4], float x) {
+  const float2 x2 = make_float2(x, x);
+#pragma unroll
+  for (int kt = 0; kt < 4; kt++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) f[kt][e] = fast::pack2(__fmul2_rn(fast::unpack2(f[kt][e]), x2));
+}
 
 // Raw token inputs of the window starting at chunk cw, one token per
 // prologue thread (pt = 0..127: token cw*C + pt).
@@ -249,7 +314,6 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::mbar_init(bar(T::B_FULLI + i), 1);
       fast::mbar_init(bar(T::B_FULLO + i), 1);
       fast::mbar_init(bar(T::B_PDONE + i), 4);
-      fast::mbar_init(bar(T::B_PSI + i), 8);
       fast::mbar_init(bar(T::B_OFREE + i), 8);
     }
     for (int i = 0; i < 12; i++) fast::mbar_init(bar(T::B_AFULL + i), 1);
@@ -257,10 +321,10 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     for (int i = 0; i < 4; i++) fast::mbar_init(bar(T::B_AUA + i), 4);
     fast::mbar_init(bar(T::B_M1), 1);
     for (int i = 0; i < 2; i++) {
-      fast::mbar_init(bar(T::B_M2 + i), 1);
-      // chunk c's issue: the four state warps, the eight epilogue warps
-      // done with chunk c - 2's products, and the eight writers of PsiV of c + 1
-      fast::mbar_init(bar(T::B_SBR + i), 4 + 8 + 8);
+      fast::mbar_init(bar(T::B_M2 + i), 3);  // three issuing threads
+      // chunk c's issue: the four state warps and the eight epilogue warps
+      // done with chunk c - 2's products
+      fast::mbar_init(bar(T::B_SBR + i), 4 + 8);
       fast::mbar_init(bar(T::B_TOKW + i), 4);
     }
     *abort_flag = 0u;
@@ -582,54 +646,59 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     float2 cdmo[4], cdmz[4];
 #pragma unroll
     for (int o = 0; o < 4; o++) cdmo[o] = cdmz[o] = make_float2(0.f, 0.f);
-    int loaded_i = min(T::NI, n);  // ring I chunks issued (thread 0)
-    // PsiV = bf16(v * bf16(mimo_v)) of chunk j, rows 8w.. of the tile, into
-    // its ring O slot (free once chunk j - NO is done by every epilogue warp)
-    const uint16_t* mvb = reinterpret_cast<const uint16_t*>(sm + T::MVB);
-    auto psi_step = [&](int j) -> bool {
-      if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLI + j % T::NI), (j / T::NI) & 1, abort_flag, 1))) return false;
-      if (!__all_sync(kFull, j < T::NO ||
-                                 wait_b(p, bar(T::B_OFREE + j % T::NO), ((j / T::NO) - 1) & 1, abort_flag, 3)))
-        return false;
-      fast::psi_rows<K, 8>(reinterpret_cast<const uint16_t*>(sm + T::RI + (j % T::NI) * T::I_BYTES + T::I_V), mvb,
-                           reinterpret_cast<uint16_t*>(sm + T::RO + (j % T::NO) * T::O_BYTES + T::O_PSI), 8 * warp);
-      fast::fence_proxy_async();  // the MMAs read PsiV
-      __syncwarp();
-      if (lane == 0) {
-        arrive(bar(T::B_PSI + j % T::NO));
-        if (j >= 1) arrive(bar(T::B_SBR + ((j - 1) & 1)));  // U_j goes out with chunk j - 1's products
-      }
-      return true;
-    };
-    // PsiV of chunk j (j < n); at j = n only the share of the last chunk's
-    // issue barrier that PsiV of a next chunk would have given
-    auto psi_or_last = [&](int j) -> bool {
-      if (j < n) return psi_step(j);
-      __syncwarp();
-      if (lane == 0) arrive(bar(T::B_SBR + ((n - 1) & 1)));
-      return true;
-    };
+    // The chunk's MMAs, one accumulator per issuing thread (each issue
+    // stalls its thread for about the MMA's run time, so the three run side
+    // by side): warp 0's first thread inter^T (and the states store), warp
+    // 4's intra^T, warp 2's U of the next chunk (U of the first chunk before
+    // the loop).  Each commits to the chunk's MMA barrier.
+    const int mma_role = lane != 0 ? -1 : warp == 0 ? 0 : warp == 4 ? 1 : warp == 2 ? 2 : -1;
+    int last_m2 = -1;  // last chunk whose MMAs this thread committed
+    bool u0 = false;   // U of the first chunk issued (committed to B_M1)
+    if (mma_role == 2 && n > 0 && wait_b(p, bar(T::B_PDONE), 0, abort_flag, 2)) {
+      fast::tm_fence_after();
+      mma64<true, true>(tmem + T::T_U, sb + T::RO + T::O_PSI, sb + T::RI + T::I_KST);
+      mma_commit(bar(T::B_M1));
+      u0 = true;
+    }
     // the first two chunks' tensor-memory buffers are free from the start
     if (lane == 0) {
       if (n > 0) arrive(bar(T::B_SBR));
       if (n > 1) arrive(bar(T::B_SBR + 1));
     }
-    bool alive = true;
-    for (int j = 0; alive && n > 0 && j <= min(1, n); j++) alive = psi_or_last(j);
-    for (int i = 0; alive && i < n; i++) {
-      const int c = c0 + i, so = i % T::NO, s2 = i & 1;
+    for (int i = 0; i < n; i++) {
+      const int c = c0 + i, so = i % T::NO, s2 = i & 1, si = i % T::NI;
       unsigned char* op = sm + T::RO + so * T::O_BYTES;
-      if (i + 2 <= n && !psi_or_last(i + 2)) break;
-      if (!__all_sync(kFull, wait_b(p, bar(T::B_PSI + so), (i / T::NO) & 1, abort_flag, 3))) break;
+      bool ok = true;
+      if (mma_role >= 0) {
+        // every state warp is done with chunk c (SB, A) and the epilogue has
+        // read chunk c - 2's products
+        ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2);
+        if (ok) {
+          fast::tm_fence_after();
+          if (mma_role == 0) {
+            // states[c] = bf16(state entering chunk c): one tile store
+            fast::tma_store_2d(&p.tm_states, sb + T::SBT + s2 * 8192, 0, (int)(((int64_t)bh * p.nc + c) * N));
+            mma64<true, false>(tmem + T::T_I + 64 * s2, sb + T::SBT + s2 * 8192,
+                               sb + T::RI + si * T::I_BYTES + T::I_Q);
+            asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");  // SB read before it is released
+          } else if (mma_role == 1) {
+            mma64<true, false>(tmem + T::T_X + 64 * s2, sb + T::RO + so * T::O_BYTES + T::O_PSI,
+                               sb + T::ATT + s2 * 8192);
+          } else if (i + 1 < n && (ok = wait_b(p, bar(T::B_PDONE + (i + 1) % T::NI), ((i + 1) / T::NI) & 1,
+                                                abort_flag, 2))) {
+            // U_{c+1} = PsiV_{c+1}^T k_state_{c+1} (their prologue is done)
+            fast::tm_fence_after();
+            mma64<true, true>(tmem + T::T_U + 64 * ((i + 1) & 1), sb + T::RO + ((i + 1) % T::NO) * T::O_BYTES + T::O_PSI,
+                              sb + T::RI + ((i + 1) % T::NI) * T::I_BYTES + T::I_KST);
+          }
+          mma_commit(bar(T::B_M2 + s2));
+          last_m2 = i;
+        }
+      }
+      if (!__all_sync(kFull, ok)) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_M2 + s2), (i >> 1) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + i % T::NI), (i / T::NI) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLO + so), (i / T::NO) & 1, abort_flag, 1))) break;
-      // every MMA of chunk c is done (and the prologue and A-step before it):
-      // its ring I slot takes chunk c + NI
-      if (threadIdx.x == 0 && i + T::NI < n) {
-        load_I(i + T::NI);
-        loaded_i = i + T::NI + 1;
-      }
       fast::tm_fence_after();
       float vi[4][4], vx[4][4];
       fast::tm_ld_frag<4>(tmem + tl_lane + T::T_I + 64 * s2 + 32 * hc, vi);
@@ -713,11 +782,13 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       __syncwarp();
       if (lane == 0) arrive(bar(T::B_OFREE + so));
     }
-    if (threadIdx.x == 0 && *abort_flag)  // after an abort: the ring I loads in flight land first
-      for (int i = max(0, loaded_i - T::NI); i < loaded_i; i++) {
-        const uint32_t bf = bar(T::B_FULLI + i % T::NI), ph = (i / T::NI) & 1;
-        drain_wait(bf, ph);
-      }
+    if (mma_role >= 0) {
+      if (mma_role == 0) fast::tma_store_wait_all();
+      if (last_m2 >= 0)  // its MMAs complete before tensor memory is released
+        drain_wait(bar(T::B_M2 + (last_m2 & 1)), (last_m2 >> 1) & 1);
+      if (u0) drain_wait(bar(T::B_M1), 0);
+    }
+    __syncwarp();
     // ---- fixed-order reduction of the dmimo partials of this segment:
     //      the four lanes of a row group (tokens), then the two warps of a
     //      p-block (token halves)
@@ -755,8 +826,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     const int jw = warp - T::WP, j0 = 16 * jw, pt = threadIdx.x - T::WP * 32;
     const bool load_thread = pt == 0;  // issues the ring O loads
     int loaded_o = min(T::NO, n);
-    const uint16_t* qbs = reinterpret_cast<const uint16_t*>(sm + T::QBS);
-    const uint16_t* kbs = reinterpret_cast<const uint16_t*>(sm + T::KBS);
+    const int tq = (j0 >> 2) + (g >> 1);  // the token (within a chunk) of this thread's fragment rows
 
     const uint16_t* mvb = reinterpret_cast<const uint16_t*>(sm + T::MVB);
     fast::TokRaw traw = tok_load<T>(p, bh, c0, pt);
@@ -785,11 +855,20 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       }
       uint16_t* qt = reinterpret_cast<uint16_t*>(ip + T::I_Q);
       uint16_t* kt = reinterpret_cast<uint16_t*>(ip + T::I_K);
+      // every per-chunk scalar in one shared-memory round trip: the biases,
+      // the token's angles, factor and exp(da_cs_rev)
+      RowRegs<T> qb, kb;
+      qb.load(reinterpret_cast<const uint16_t*>(sm + T::QBS));
+      kb.load(reinterpret_cast<const uint16_t*>(sm + T::KBS));
+      const float* ang = reinterpret_cast<const float*>(ip + T::I_ANG) + tq * T::W + 2 * cq;
+      const float2 an0 = *reinterpret_cast<const float2*>(ang), an1 = *reinterpret_cast<const float2*>(ang + 8);
+      const uint32_t fd = reinterpret_cast<const uint32_t*>(tok)[C + tq];
+      const float ed = tok[3 * C + tq];
       uint32_t qf[4][4], kf[4][4];
       fast::load_rows<K>(qf, qt, j0);
       fast::load_rows<K>(kf, kt, j0);
-      fast::add_bias<K>(qf, qbs);  // bf16(q + bf16(bias)), bf16(k + bf16(bias))
-      fast::add_bias<K>(kf, kbs);
+      add_bias_r(qf, qb.b);  // bf16(q + bf16(bias)), bf16(k + bf16(bias))
+      add_bias_r(kf, kb.b);
       {  // same-token qk_dot from the diagonal 16x16 tile of Qh Kh^T
         uint32_t* qkd = reinterpret_cast<uint32_t*>(op + T::O_QKD);
         float qa[2][4];
@@ -817,13 +896,16 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
             }
           }
       }
-      fast::rotate_direct<K, true>(qf, kf, reinterpret_cast<const float*>(ip + T::I_ANG), j0);
+      rotate_r<K>(qf, kf, true, an0, an1);
       __syncwarp();  // this warp's raw q / k rows are read before they are overwritten
       fast::store_rows<K, true>(qf, qt, j0);  // Q_rot, rows in fragment order
-      fast::scale_k<K>(kf, reinterpret_cast<const uint32_t*>(tok) + C, j0);
+      scale_r(kf, fd);
       fast::store_rows<K, true>(kf, kt, j0);  // k_scaled
-      fast::k_state<K>(kf, tok + 3 * C, j0);
+      kstate_r(kf, ed);
       fast::store_rows<K, true>(kf, reinterpret_cast<uint16_t*>(ip + T::I_KST), j0);
+      // PsiV = bf16(v * bf16(mimo_v)), this warp's rows, into the ring O slot
+      fast::psi_rows<K, 16>(reinterpret_cast<const uint16_t*>(ip + T::I_V), mvb,
+                            reinterpret_cast<uint16_t*>(op + T::O_PSI), j0);
       fast::fence_proxy_async();
       __syncwarp();
       if (lane == 0) arrive(bar(T::B_PDONE + si));
@@ -845,15 +927,13 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     // went out with chunk c - 2's products, so it is long done); bf16 of it
     // for inter^T and the states output; A = bf16(mask(Q_rot Ks^T)
     // exp(segsum)) for j-block q (mma.sync on the prologue's tiles, causal
-    // blocks only).  Then one thread (warp 12's for even chunks, warp 13's
-    // for odd ones) stores states[c] and issues inter^T, intra^T of c and U
-    // of c + 1 on tcgen05.mma.  Only the fold is serial from chunk to chunk.
+    // blocks only).  The epilogue warps issue the chunk's MMAs.  Only the
+    // fold is serial from chunk to chunk.
     // =====================================================================
     const int q = warp - T::WS;
-    const bool mma_even = threadIdx.x == T::WS * 32, mma_odd = threadIdx.x == T::WS * 32 + 32;
+    const bool loader = threadIdx.x == T::WS * 32 + 96;  // refills ring I
+    int loaded_i = min(T::NI, n);                        // ring I chunks issued
     const uint32_t tl_lane = (uint32_t)(32 * q) << 16;
-    int last_m2 = -1;  // last chunk whose MMAs this thread committed
-    bool u0 = false;   // U of the first chunk issued (committed to B_M1)
     {  // blocks of A above the token-block diagonal stay 0 (both buffers)
       uint16_t* at = reinterpret_cast<uint16_t*>(sm + T::ATT);
       for (int e = lane; e < 2 * 16 * 8; e += 32) {  // 2 buffers x 16 rows x 8 chunks of 16 bytes
@@ -862,20 +942,8 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
           *reinterpret_cast<uint4*>(at + bf * 4096 + fast::swz128(16 * q + r, ch * 8)) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    // U of the first chunk: PsiV^T k_state, into tensor-memory buffer 0
-    bool alive = true;
-    if (mma_even && n > 0) {
-      alive = wait_b(p, bar(T::B_PSI), 0, abort_flag, 2) && wait_b(p, bar(T::B_PDONE), 0, abort_flag, 2);
-      if (alive) {
-        fast::tm_fence_after();
-        mma64<true, true>(tmem + T::T_U, sb + T::RO + T::O_PSI, sb + T::RI + T::I_KST);
-        mma_commit(bar(T::B_M1));
-        u0 = true;
-      }
-    }
-    alive = __all_sync(kFull, alive);
-    for (int i = 0; alive && i < n; i++) {
-      const int c = c0 + i, s2 = i & 1, si = i % T::NI, so = i % T::NO;
+    for (int i = 0; i < n; i++) {
+      const int s2 = i & 1, si = i % T::NI;
       unsigned char* ip = sm + T::RI + si * T::I_BYTES;
       // state entering chunk c = round(state * alpha_{c-1}) + U_{c-1} (FP32).
       // Chunk c - 2's MMAs are done: U_{c-1} is ready and the SB / A buffers
@@ -884,6 +952,12 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
         if (!__all_sync(kFull, i >= 2 ? wait_b(p, bar(T::B_M2 + s2), ((i - 2) >> 1) & 1, abort_flag, 2)
                                       : wait_b(p, bar(T::B_M1), 0, abort_flag, 2)))
           break;
+        // chunk c - 2 is done with its ring I slot (prologue, A, every MMA):
+        // it takes chunk c + 2
+        if (loader && i >= 2 && i + 2 < n) {
+          load_I(i + 2);
+          loaded_i = i + 3;
+        }
         fast::tm_fence_after();
         float u[8][4];
         fast::tm_ld_frag<8>(tmem + tl_lane + T::T_U + 64 * ((i - 1) & 1), u);
@@ -905,12 +979,8 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
         const uint32_t r3 = fast::pack2(make_float2(st[2 * nn + 1][2], st[2 * nn + 1][3]));
         fast::stsm_x4_t(sbt + fast::swz128(nn * 16 + (mi >> 1) * 8 + li, q * 16 + (mi & 1) * 8), r0, r1, r2, r3);
       }
-      // the prologue of chunk c + 1 is done (and so that of c): Q_rot,
-      // k_scaled of c for A, k_state of c + 1 for U_{c+1}
-      {
-        const int jn = min(i + 1, n - 1);
-        if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + jn % T::NI), (jn / T::NI) & 1, abort_flag, 2))) break;
-      }
+      // the prologue of chunk c is done: Q_rot, k_scaled for A
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + si), (i / T::NI) & 1, abort_flag, 2))) break;
       {  // A rows 16q..: S = Q_rot Ks^T on causal blocks jb <= q, rows and columns in tile order
         const uint16_t* qt = reinterpret_cast<const uint16_t*>(ip + T::I_Q);
         const uint16_t* kt = reinterpret_cast<const uint16_t*>(ip + T::I_K);
@@ -950,38 +1020,10 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::fence_proxy_async();  // SB and A tiles before the MMAs and the store read them
       __syncwarp();
       if (lane == 0) arrive(bar(T::B_SBR + s2));
-      bool ok = true;
-      if ((i & 1) ? mma_odd : mma_even) {
-        // every state warp is done with chunk c, the epilogue has read chunk
-        // c - 2's products, and PsiV of chunk c + 1 is written
-        ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2);
-        if (ok) {
-          fast::tm_fence_after();
-          // states[c] = bf16(state entering chunk c): one tile store, issued
-          // first so that its read of SB overlaps the MMA issue
-          fast::tma_store_2d(&p.tm_states, sb + T::SBT + s2 * 8192, 0, (int)(((int64_t)bh * p.nc + c) * N));
-          mma64<true, false>(tmem + T::T_I + 64 * s2, sb + T::SBT + s2 * 8192, sb + T::RI + si * T::I_BYTES + T::I_Q);
-          mma64<true, false>(tmem + T::T_X + 64 * s2, sb + T::RO + so * T::O_BYTES + T::O_PSI, sb + T::ATT + s2 * 8192);
-          if (i + 1 < n)  // U_{c+1} = PsiV_{c+1}^T k_state_{c+1}
-            mma64<true, true>(tmem + T::T_U + 64 * ((i + 1) & 1), sb + T::RO + ((i + 1) % T::NO) * T::O_BYTES + T::O_PSI,
-                              sb + T::RI + ((i + 1) % T::NI) * T::I_BYTES + T::I_KST);
-          asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");  // SB read before the buffer is released
-          mma_commit(bar(T::B_M2 + s2));
-          last_m2 = i;
-        }
-      }
-      if (!__all_sync(kFull, ok)) {
-        alive = false;
-        break;
-      }
     }
     __syncwarp();
-    if (mma_even || mma_odd) {
-      fast::tma_store_wait_all();
-      if (last_m2 >= 0)  // its MMAs complete before tensor memory is released
-        drain_wait(bar(T::B_M2 + (last_m2 & 1)), (last_m2 >> 1) & 1);
-      if (u0) drain_wait(bar(T::B_M1), 0);
-    }
+    if (loader && *abort_flag)  // after an abort: the ring I loads in flight land first
+      for (int i = max(0, loaded_i - T::NI); i < loaded_i; i++) drain_wait(bar(T::B_FULLI + i % T::NI), (i / T::NI) & 1);
     __syncwarp();
     fast::tm_fence_before();
     __syncthreads();  // (A)
