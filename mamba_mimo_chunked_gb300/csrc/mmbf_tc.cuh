@@ -78,21 +78,21 @@ struct TCfg {
   enum : uint32_t {
     B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_M1 = 16, B_M2 = 17, B_SBR = 19, B_TOKW = 21,
     // phase A of the single-kernel form: per group TMA (3 buffers), prologue done, MMA done (2 buffers)
-    B_AFULL = 23, B_APA = 35, B_AUA = 39, NBAR = 43
+    B_AFULL = 23, B_APA = 35, B_AU = 39, B_AUF = 47, NBAR = 55
   };
 
+  static constexpr uint32_t MISC = BAR + ((NBAR * 8 + 15) & ~15u);  // tmem slot, abort flag, last-CTA flag
   // Phase A (the segment's own state sum, single-kernel form), laid over the
-  // ring and tile regions before phase C uses them: per group of four warps
-  // three staging buffers of raw k (k_state is written over it), v and
-  // angles, one PsiV tile per group; the segment's token scalars (factor,
-  // exp(da_cs_rev)) and chunk weights in the A-tile region.
+  // ring and tile regions before phase C uses them (below the parameter
+  // tables): per group of four warps three staging buffers of raw k (k_state
+  // is written over it), v and angles, and two PsiV tiles; the segment's
+  // token scalars (factor, exp(da_cs_rev)) and chunk weights after MISC.
   static constexpr uint32_t A_K = 0, A_V = 8192, A_ANG = 10240, A_BUF = 12288;
   static constexpr uint32_t A_RAW = 0, A_PSI = 12 * A_BUF;
   static constexpr int LMAX = 64;  // longest segment of the single-kernel form
-  static constexpr uint32_t A_FAC = ATT, A_EDR = ATT + LMAX * C * 4, A_GAM = A_EDR + LMAX * C * 4,
-                            A_ALP = A_GAM + LMAX * 4, A_DEC = A_ALP + LMAX * 4;
-  static constexpr uint32_t MISC = BAR + ((NBAR * 8 + 15) & ~15u);  // tmem slot, abort flag, last-CTA flag
-  static constexpr uint32_t SMEM = MISC + 16 + 1024;  // + alignment slack of the base
+  static constexpr uint32_t A_FAC = (MISC + 16 + 127) & ~127u, A_EDR = A_FAC + LMAX * C * 4,
+                            A_GAM = A_EDR + LMAX * C * 4, A_ALP = A_GAM + LMAX * 4, A_DEC = A_ALP + LMAX * 4;
+  static constexpr uint32_t SMEM = A_DEC + 16 + 1024;  // + alignment slack of the base
   // tensor-memory columns (two buffers of 64 each)
   static constexpr uint32_t T_S = 0, T_U = 128, T_I = 256, T_X = 384;
   static_assert(I_ANG + C * W * 4 <= I_SEG && I_SEG + C * C * 4 <= I_BYTES, "ring I slot");
@@ -100,7 +100,7 @@ struct TCfg {
   static_assert(I_BYTES % 1024 == 0 && O_BYTES % 1024 == 0 && RO % 1024 == 0 && SBT % 1024 == 0, "alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(W == 16, "register prologue: N / rotary_dim_divisor = 16 rotated pairs");
-  static_assert(A_PSI + 4 * 8192 <= ATT && A_DEC + 16 <= TOK, "phase A layout");
+  static_assert(A_PSI + 8 * 8192 <= MVB, "phase A layout");
   static_assert(A_BUF % 1024 == 0 && A_PSI % 1024 == 0 && 4 * 4096 * 4 <= A_PSI, "phase A alignment, reduction scratch");
 };
 
@@ -318,7 +318,10 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     }
     for (int i = 0; i < 12; i++) fast::mbar_init(bar(T::B_AFULL + i), 1);
     for (int i = 0; i < 4; i++) fast::mbar_init(bar(T::B_APA + i), 4);
-    for (int i = 0; i < 4; i++) fast::mbar_init(bar(T::B_AUA + i), 4);
+    for (int i = 0; i < 8; i++) {
+      fast::mbar_init(bar(T::B_AU + i), 1);   // a group's U MMA done (per tensor-memory buffer)
+      fast::mbar_init(bar(T::B_AUF + i), 4);  // the group's four warps folded that buffer
+    }
     fast::mbar_init(bar(T::B_M1), 1);
     for (int i = 0; i < 2; i++) {
       fast::mbar_init(bar(T::B_M2 + i), 3);  // three issuing threads
@@ -395,7 +398,11 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     // over the segment -- and its decay prod alpha_c, published for the
     // later segments of (b,h).  Four groups of four warps take every fourth
     // chunk (warp 4w + q: j-block q and tensor-memory lane quarter q of
-    // group w); each keeps its partial sum in registers.
+    // group w); each keeps its partial sum in registers.  U_k is a
+    // tcgen05.mma into the group's tensor-memory buffer k & 1 (columns
+    // 64 (2w + (k & 1))), issued by the group's first thread once the four
+    // warps wrote k_state and PsiV; the warps fold it one chunk later, so the
+    // MMA runs under the next chunk's prologue.
     // =====================================================================
     const int na = c1 - c0;
     uint32_t* afac = reinterpret_cast<uint32_t*>(sm + T::A_FAC);
@@ -440,10 +447,13 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     const int w = warp >> 2, q = warp & 3;
     const int kw = na > w ? (na - w + 3) / 4 : 0;  // chunks of group w: w + 4k
     const bool gl = (q == 0) && lane == 0;         // the group's TMA thread
-    const uint16_t* kbs = reinterpret_cast<const uint16_t*>(sm + T::KBS);
     const uint16_t* mvb = reinterpret_cast<const uint16_t*>(sm + T::MVB);
-    const uint16_t* psa = reinterpret_cast<const uint16_t*>(sm + T::A_PSI + w * 8192);
+    RowRegs<T> kb;  // k bias pairs in registers
+    kb.load(reinterpret_cast<const uint16_t*>(sm + T::KBS));
+    const int tq = 4 * q + (g >> 1);  // the token (within a chunk) of this thread's fragment rows
     auto abuf = [&](int k) { return (uint32_t)(T::A_RAW + (w * 3 + k % 3) * T::A_BUF); };
+    auto apsi = [&](int k) { return (uint32_t)(T::A_PSI + (w * 2 + (k & 1)) * 8192); };
+    const uint32_t tl_lane = (uint32_t)(32 * q) << 16;
     auto load_A = [&](int k) {
       const int t0 = (c0 + w + 4 * k) * C;
       const uint32_t dst = sb + abuf(k), full = bar(T::B_AFULL + w * 3 + k % 3);
@@ -454,7 +464,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::tma_load_4d(dst + T::A_V, &p.tm_v, 0, h, t0, b, full);
       fast::tma_load_4d(dst + T::A_ANG, &p.tm_ang, 0, h, t0, b, full);
     };
-    int loaded_a = 0;
+    int loaded_a = 0, issued_a = 0;  // staging loads, U MMAs (group leader)
     if (gl) {
       loaded_a = min(3, kw);
       for (int k = 0; k < loaded_a; k++) load_A(k);
@@ -465,35 +475,73 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     float acc[8][4];
 #pragma unroll
     for (int nn = 0; nn < 8; nn++) acc[nn][0] = acc[nn][1] = acc[nn][2] = acc[nn][3] = 0.f;
-    for (int k = 0; k < kw; k++) {
-      const int i = w + 4 * k;
-      unsigned char* bp = sm + abuf(k);
-      // chunk k - 1 is done by every warp of the group: its staging buffer
-      // takes chunk k + 2 (and the group's PsiV tile is free)
-      if (k >= 1 && !__all_sync(kFull, wait_b(p, bar(T::B_AUA + w), (k - 1) & 1, abort_flag, 4))) break;
-      if (gl && k >= 1 && k + 2 < kw) {
-        load_A(k + 2);
-        loaded_a = k + 3;
+    // fold U_k into acc: round(acc * decay) + U_k; then the buffer is free
+    auto fold = [&](int k) -> bool {
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_AU + w * 2 + (k & 1)), (k >> 1) & 1, abort_flag, 4))) return false;
+      // U_k is done: chunk k's staging buffer takes chunk k + 3
+      if (gl && k + 3 < kw) {
+        load_A(k + 3);
+        loaded_a = k + 4;
       }
-      if (!__all_sync(kFull, wait_b(p, bar(T::B_AFULL + w * 3 + k % 3), (k / 3) & 1, abort_flag, 1))) break;
-      uint32_t kf[4][4];
-      fast::load_rows<K>(kf, reinterpret_cast<const uint16_t*>(bp + T::A_K), 16 * q);
-      fast::add_bias<K>(kf, kbs);
-      fast::rotate_direct<K, false>(kf, kf, reinterpret_cast<const float*>(bp + T::A_ANG), 16 * q);
-      fast::scale_k<K>(kf, afac + i * C, 16 * q);
-      fast::k_state<K>(kf, aedr + i * C, 16 * q);
-      __syncwarp();  // this warp's raw k rows are read before k_state overwrites them
-      fast::store_rows<K, true>(kf, reinterpret_cast<uint16_t*>(bp + T::A_K), 16 * q);
-      fast::psi_rows<K>(reinterpret_cast<const uint16_t*>(bp + T::A_V), mvb, const_cast<uint16_t*>(psa), 16 * q);
-      __syncwarp();
-      if (lane == 0) arrive(bar(T::B_APA + w));
-      if (!__all_sync(kFull, wait_b(p, bar(T::B_APA + w), k & 1, abort_flag, 4))) break;
+      const int i = w + 4 * k;
       // decay from the group's previous chunk through this one: prod of alpha over (c_{k-1}, c_k]
       const float dk = k >= 1 ? ((aalp[i - 3] * aalp[i - 2]) * aalp[i - 1]) * aalp[i] : 1.f;
-      fast::state_mma<K>(acc, psa, reinterpret_cast<const uint16_t*>(bp + T::A_K), dk, q, 0);
+      fast::tm_fence_after();
+      float u[8][4];
+      fast::tm_ld_frag<8>(tmem + tl_lane + 64 * (w * 2 + (k & 1)), u);
+      const float2 d2 = make_float2(dk, dk);
+#pragma unroll
+      for (int nn = 0; nn < 8; nn++) {
+        const float2 x = __fadd2_rn(__fmul2_rn(make_float2(acc[nn][0], acc[nn][1]), d2), make_float2(u[nn][0], u[nn][1]));
+        const float2 y = __fadd2_rn(__fmul2_rn(make_float2(acc[nn][2], acc[nn][3]), d2), make_float2(u[nn][2], u[nn][3]));
+        acc[nn][0] = x.x; acc[nn][1] = x.y; acc[nn][2] = y.x; acc[nn][3] = y.y;
+      }
+      fast::tm_fence_before();
       __syncwarp();
-      if (lane == 0) arrive(bar(T::B_AUA + w));
+      if (lane == 0) arrive(bar(T::B_AUF + w * 2 + (k & 1)));
+      return true;
+    };
+    bool aok = true;
+    for (int k = 0; aok && k < kw; k++) {
+      const int i = w + 4 * k;
+      unsigned char* bp = sm + abuf(k);
+      if (!__all_sync(kFull, wait_b(p, bar(T::B_AFULL + w * 3 + k % 3), (k / 3) & 1, abort_flag, 1))) break;
+      // the token's angles, factor and exp(da_cs_rev) in one round trip
+      const float* ang = reinterpret_cast<const float*>(bp + T::A_ANG) + tq * T::W + 2 * cq;
+      const float2 an0 = *reinterpret_cast<const float2*>(ang), an1 = *reinterpret_cast<const float2*>(ang + 8);
+      const uint32_t fd = afac[i * C + tq];
+      const float ed = aedr[i * C + tq];
+      uint32_t kf[4][4];
+      fast::load_rows<K>(kf, reinterpret_cast<const uint16_t*>(bp + T::A_K), 16 * q);
+      add_bias_r(kf, kb.b);
+      rotate_r<K>(kf, kf, false, an0, an1);
+      scale_r(kf, fd);
+      kstate_r(kf, ed);
+      __syncwarp();  // this warp's raw k rows are read before k_state overwrites them
+      fast::store_rows<K, true>(kf, reinterpret_cast<uint16_t*>(bp + T::A_K), 16 * q);
+      // PsiV tile k & 1 was read by U_{k-2}, which the fold of k - 2 waited for
+      fast::psi_rows<K>(reinterpret_cast<const uint16_t*>(bp + T::A_V), mvb,
+                        reinterpret_cast<uint16_t*>(sm + apsi(k)), 16 * q);
+      fast::fence_proxy_async();  // the MMA reads k_state and PsiV
+      __syncwarp();
+      if (lane == 0) arrive(bar(T::B_APA + w));
+      if (gl) {  // U_k, once the group's four warps are done and buffer k & 1 is folded
+        aok = wait_b(p, bar(T::B_APA + w), k & 1, abort_flag, 4) &&
+              (k < 2 || wait_b(p, bar(T::B_AUF + w * 2 + (k & 1)), ((k - 2) >> 1) & 1, abort_flag, 4));
+        if (aok) {
+          fast::tm_fence_after();
+          mma64<true, true>(tmem + 64 * (w * 2 + (k & 1)), sb + apsi(k), sb + abuf(k) + T::A_K);
+          mma_commit(bar(T::B_AU + w * 2 + (k & 1)));
+          issued_a = k + 1;
+        }
+      }
+      aok = __all_sync(kFull, aok);
+      if (aok && k >= 1) aok = fold(k - 1);
     }
+    if (aok && kw > 0) aok = fold(kw - 1);
+    __syncwarp();
+    if (gl && issued_a > 0)  // the group's last MMA completes before the area and tensor memory are reused
+      drain_wait(bar(T::B_AU + w * 2 + ((issued_a - 1) & 1)), ((issued_a - 1) >> 1) & 1);
     if (kw > 0) {
       const float gl_last = agam[w + 4 * (kw - 1)];
 #pragma unroll
