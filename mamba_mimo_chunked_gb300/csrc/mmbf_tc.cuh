@@ -96,7 +96,7 @@ struct TCfg {
   // tensor-memory columns (two buffers of 64 each)
   static constexpr uint32_t T_S = 0, T_U = 128, T_I = 256, T_X = 384;
   static_assert(I_ANG + C * W * 4 <= I_SEG && I_SEG + C * C * 4 <= I_BYTES, "ring I slot");
-  static_assert(O_QKD + C * QKS * 4 <= O_BYTES, "ring O slot");
+  static_assert(O_QKD + C * QKS * 4 <= O_BYTES && QKS % 4 == 0 && O_QKD % 16 == 0, "ring O slot, qk table rows");
   static_assert(I_BYTES % 1024 == 0 && O_BYTES % 1024 == 0 && RO % 1024 == 0 && SBT % 1024 == 0, "alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(W == 16, "register prologue: N / rotary_dim_divisor = 16 rotated pairs");
@@ -927,22 +927,27 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
           mma16816(qa[0], qf[k4][0], qf[k4][1], qf[k4][2], qf[k4][3], kf[k4][0], kf[k4][2]);
           mma16816(qa[1], qf[k4][0], qf[k4][1], qf[k4][2], qf[k4][3], kf[k4][1], kf[k4][3]);
         }
-#pragma unroll
-        for (int ht = 0; ht < 2; ht++)
+        // Fragment rows g, g + 8 are ranks 2hh + (g & 1) of token g / 2 of the
+        // block, columns 2 cq, 2 cq + 1 of tile ht ranks 2ht, 2ht + 1 of token
+        // cq: the lanes with g / 2 = cq hold token 4 jw + cq's qk values, ranks
+        // o = (g & 1) and 2 + (g & 1), all four columns.  Each writes two rows
+        // of the token's [R][R] block: the BF16 table for the epilogue (both
+        // halves), and the output.
+        if ((g >> 1) == cq) {
+          const int tl = 4 * jw + cq;
+          const bool inb = c * C + tl < p.S;
+          uint32_t* qrow = qkd + tl * T::QKS;
+          uint2* grow = reinterpret_cast<uint2*>(p.qk_dot + ((int64_t)bh * p.S + c * C + tl) * (R * R));
 #pragma unroll
           for (int hh = 0; hh < 2; hh++) {
-            const int pi = fast::perm<R>(g + 8 * hh), pi2 = fast::perm<R>(ht * 8 + 2 * cq);
-            if (pi / R == pi2 / R) {
-              const int tl = (j0 + pi) / R, o = pi % R, s0 = pi2 % R;
-              const float v0 = round_bf(qa[ht][2 * hh]), v1 = round_bf(qa[ht][2 * hh + 1]);
-              qkd[tl * T::QKS + o * R + s0] = fast::dup_bf(v0);
-              qkd[tl * T::QKS + o * R + s0 + 1] = fast::dup_bf(v1);
-              const int tg = c * C + tl;
-              if (tg < p.S)
-                *reinterpret_cast<uint32_t*>(p.qk_dot + (((int64_t)bh * p.S + tg) * R + o) * R + s0) =
-                    (uint32_t)f_bf(v0) | ((uint32_t)f_bf(v1) << 16);
-            }
+            const int o = 2 * hh + (g & 1);
+            const uint32_t v0 = f_bf(qa[0][2 * hh]), v1 = f_bf(qa[0][2 * hh + 1]);
+            const uint32_t v2 = f_bf(qa[1][2 * hh]), v3 = f_bf(qa[1][2 * hh + 1]);
+            *reinterpret_cast<uint4*>(qrow + o * R) =
+                make_uint4(v0 | (v0 << 16), v1 | (v1 << 16), v2 | (v2 << 16), v3 | (v3 << 16));
+            if (inb) grow[o] = make_uint2(v0 | (v1 << 16), v2 | (v3 << 16));
           }
+        }
       }
       rotate_r<K>(qf, kf, true, an0, an1);
       __syncwarp();  // this warp's raw q / k rows are read before they are overwritten
