@@ -76,9 +76,9 @@ struct TCfg {
   // barriers: full / pdone / ofree / fullO / PsiV per ring slot, the rest
   // per tensor-memory / tile buffer (two) or one
   enum : uint32_t {
-    B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_M1 = 16, B_M2 = 17, B_SBR = 19, B_TOKW = 21,
+    B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_U = 16, B_M2 = 18, B_SBR = 20, B_TOKW = 22,
     // phase A of the single-kernel form: per group TMA (3 buffers), prologue done, MMA done (2 buffers)
-    B_AFULL = 23, B_APA = 35, B_AU = 39, B_AUF = 47, NBAR = 55
+    B_AFULL = 24, B_APA = 36, B_AU = 40, B_AUF = 48, NBAR = 56
   };
 
   static constexpr uint32_t MISC = BAR + ((NBAR * 8 + 15) & ~15u);  // tmem slot, abort flag, last-CTA flag
@@ -322,9 +322,9 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::mbar_init(bar(T::B_AU + i), 1);   // a group's U MMA done (per tensor-memory buffer)
       fast::mbar_init(bar(T::B_AUF + i), 4);  // the group's four warps folded that buffer
     }
-    fast::mbar_init(bar(T::B_M1), 1);
     for (int i = 0; i < 2; i++) {
-      fast::mbar_init(bar(T::B_M2 + i), 3);  // three issuing threads
+      fast::mbar_init(bar(T::B_U + i), 1);
+      fast::mbar_init(bar(T::B_M2 + i), 2);  // inter^T and intra^T, two issuing threads
       // chunk c's issue: the four state warps and the eight epilogue warps
       // done with chunk c - 2's products
       fast::mbar_init(bar(T::B_SBR + i), 4 + 8);
@@ -694,56 +694,14 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     float2 cdmo[4], cdmz[4];
 #pragma unroll
     for (int o = 0; o < 4; o++) cdmo[o] = cdmz[o] = make_float2(0.f, 0.f);
-    // The chunk's MMAs, one accumulator per issuing thread (each issue
-    // stalls its thread for about the MMA's run time, so the three run side
-    // by side): warp 0's first thread inter^T (and the states store), warp
-    // 4's intra^T, warp 2's U of the next chunk (U of the first chunk before
-    // the loop).  Each commits to the chunk's MMA barrier.
-    const int mma_role = lane != 0 ? -1 : warp == 0 ? 0 : warp == 4 ? 1 : warp == 2 ? 2 : -1;
-    int last_m2 = -1;  // last chunk whose MMAs this thread committed
-    bool u0 = false;   // U of the first chunk issued (committed to B_M1)
-    if (mma_role == 2 && n > 0 && wait_b(p, bar(T::B_PDONE), 0, abort_flag, 2)) {
-      fast::tm_fence_after();
-      mma64<true, true>(tmem + T::T_U, sb + T::RO + T::O_PSI, sb + T::RI + T::I_KST);
-      mma_commit(bar(T::B_M1));
-      u0 = true;
-    }
     // the first two chunks' tensor-memory buffers are free from the start
     if (lane == 0) {
       if (n > 0) arrive(bar(T::B_SBR));
       if (n > 1) arrive(bar(T::B_SBR + 1));
     }
     for (int i = 0; i < n; i++) {
-      const int c = c0 + i, so = i % T::NO, s2 = i & 1, si = i % T::NI;
+      const int c = c0 + i, so = i % T::NO, s2 = i & 1;
       unsigned char* op = sm + T::RO + so * T::O_BYTES;
-      bool ok = true;
-      if (mma_role >= 0) {
-        // every state warp is done with chunk c (SB, A) and the epilogue has
-        // read chunk c - 2's products
-        ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2);
-        if (ok) {
-          fast::tm_fence_after();
-          if (mma_role == 0) {
-            // states[c] = bf16(state entering chunk c): one tile store
-            fast::tma_store_2d(&p.tm_states, sb + T::SBT + s2 * 8192, 0, (int)(((int64_t)bh * p.nc + c) * N));
-            mma64<true, false>(tmem + T::T_I + 64 * s2, sb + T::SBT + s2 * 8192,
-                               sb + T::RI + si * T::I_BYTES + T::I_Q);
-            asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");  // SB read before it is released
-          } else if (mma_role == 1) {
-            mma64<true, false>(tmem + T::T_X + 64 * s2, sb + T::RO + so * T::O_BYTES + T::O_PSI,
-                               sb + T::ATT + s2 * 8192);
-          } else if (i + 1 < n && (ok = wait_b(p, bar(T::B_PDONE + (i + 1) % T::NI), ((i + 1) / T::NI) & 1,
-                                                abort_flag, 2))) {
-            // U_{c+1} = PsiV_{c+1}^T k_state_{c+1} (their prologue is done)
-            fast::tm_fence_after();
-            mma64<true, true>(tmem + T::T_U + 64 * ((i + 1) & 1), sb + T::RO + ((i + 1) % T::NO) * T::O_BYTES + T::O_PSI,
-                              sb + T::RI + ((i + 1) % T::NI) * T::I_BYTES + T::I_KST);
-          }
-          mma_commit(bar(T::B_M2 + s2));
-          last_m2 = i;
-        }
-      }
-      if (!__all_sync(kFull, ok)) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_M2 + s2), (i >> 1) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_PDONE + i % T::NI), (i / T::NI) & 1, abort_flag, 3))) break;
       if (!__all_sync(kFull, wait_b(p, bar(T::B_FULLO + so), (i / T::NO) & 1, abort_flag, 1))) break;
@@ -830,13 +788,6 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       __syncwarp();
       if (lane == 0) arrive(bar(T::B_OFREE + so));
     }
-    if (mma_role >= 0) {
-      if (mma_role == 0) fast::tma_store_wait_all();
-      if (last_m2 >= 0)  // its MMAs complete before tensor memory is released
-        drain_wait(bar(T::B_M2 + (last_m2 & 1)), (last_m2 >> 1) & 1);
-      if (u0) drain_wait(bar(T::B_M1), 0);
-    }
-    __syncwarp();
     // ---- fixed-order reduction of the dmimo partials of this segment:
     //      the four lanes of a row group (tokens), then the two warps of a
     //      p-block (token halves)
@@ -980,10 +931,16 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     // went out with chunk c - 2's products, so it is long done); bf16 of it
     // for inter^T and the states output; A = bf16(mask(Q_rot Ks^T)
     // exp(segsum)) for j-block q (mma.sync on the prologue's tiles, causal
-    // blocks only).  The epilogue warps issue the chunk's MMAs.  Only the
-    // fold is serial from chunk to chunk.
+    // blocks only).  Then the chunk's MMAs go out from the two warps with the
+    // fewest A blocks, one accumulator per issuing thread (an issue stalls
+    // its thread for about the MMA's run time): warp 12's first thread the
+    // states store, inter^T, then U of the next chunk (its own barrier, so
+    // that the epilogue of c never waits for the prologue of c + 1), warp
+    // 13's intra^T.  Only the fold is serial from chunk to chunk.
     // =====================================================================
     const int q = warp - T::WS;
+    const int mma_role = lane != 0 ? -1 : q < 2 ? q : -1;  // 0 store, inter, U; 1 intra
+    int last_m = -1, last_u = -1;  // last chunk this thread committed products / U for
     const bool loader = threadIdx.x == T::WS * 32 + 96;  // refills ring I
     int loaded_i = min(T::NI, n);                        // ring I chunks issued
     const uint32_t tl_lane = (uint32_t)(32 * q) << 16;
@@ -995,15 +952,27 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
           *reinterpret_cast<uint4*>(at + bf * 4096 + fast::swz128(16 * q + r, ch * 8)) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    for (int i = 0; i < n; i++) {
-      const int s2 = i & 1, si = i % T::NI;
+    // U of the first chunk: PsiV^T k_state, into tensor-memory buffer 0
+    bool alive = true;
+    if (mma_role == 0 && n > 0) {
+      alive = wait_b(p, bar(T::B_PDONE), 0, abort_flag, 2);
+      if (alive) {
+        fast::tm_fence_after();
+        mma64<true, true>(tmem + T::T_U, sb + T::RO + T::O_PSI, sb + T::RI + T::I_KST);
+        mma_commit(bar(T::B_U));
+        last_u = 0;
+      }
+    }
+    alive = __all_sync(kFull, alive);
+    for (int i = 0; alive && i < n; i++) {
+      const int c = c0 + i, s2 = i & 1, si = i % T::NI, so = i % T::NO;
       unsigned char* ip = sm + T::RI + si * T::I_BYTES;
       // state entering chunk c = round(state * alpha_{c-1}) + U_{c-1} (FP32).
       // Chunk c - 2's MMAs are done: U_{c-1} is ready and the SB / A buffers
       // of this parity are free (and so is the states store that read SB).
       if (i >= 1) {
-        if (!__all_sync(kFull, i >= 2 ? wait_b(p, bar(T::B_M2 + s2), ((i - 2) >> 1) & 1, abort_flag, 2)
-                                      : wait_b(p, bar(T::B_M1), 0, abort_flag, 2)))
+        if (!__all_sync(kFull, (i < 2 || wait_b(p, bar(T::B_M2 + s2), ((i - 2) >> 1) & 1, abort_flag, 2)) &&
+                                   wait_b(p, bar(T::B_U + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag, 2)))
           break;
         // chunk c - 2 is done with its ring I slot (prologue, A, every MMA):
         // it takes chunk c + 2
@@ -1073,7 +1042,46 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::fence_proxy_async();  // SB and A tiles before the MMAs and the store read them
       __syncwarp();
       if (lane == 0) arrive(bar(T::B_SBR + s2));
+      bool ok = true;
+      if (mma_role >= 0) {
+        // every state warp is done with chunk c (SB, A, U_{c-1} folded) and
+        // the epilogue has read chunk c - 2's products
+        ok = wait_b(p, bar(T::B_SBR + s2), (i >> 1) & 1, abort_flag, 2);
+        if (ok) {
+          fast::tm_fence_after();
+          if (mma_role == 0) {
+            // states[c] = bf16(state entering chunk c): one tile store
+            fast::tma_store_2d(&p.tm_states, sb + T::SBT + s2 * 8192, 0, (int)(((int64_t)bh * p.nc + c) * N));
+            mma64<true, false>(tmem + T::T_I + 64 * s2, sb + T::SBT + s2 * 8192,
+                               sb + T::RI + si * T::I_BYTES + T::I_Q);
+            asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");  // SB read before it is released
+            mma_commit(bar(T::B_M2 + s2));
+            last_m = i;
+            if (i + 1 < n && (ok = wait_b(p, bar(T::B_PDONE + (i + 1) % T::NI), ((i + 1) / T::NI) & 1,
+                                          abort_flag, 2))) {
+              // U_{c+1} = PsiV_{c+1}^T k_state_{c+1} (their prologue is done)
+              fast::tm_fence_after();
+              mma64<true, true>(tmem + T::T_U + 64 * ((i + 1) & 1),
+                                sb + T::RO + ((i + 1) % T::NO) * T::O_BYTES + T::O_PSI,
+                                sb + T::RI + ((i + 1) % T::NI) * T::I_BYTES + T::I_KST);
+              mma_commit(bar(T::B_U + ((i + 1) & 1)));
+              last_u = i + 1;
+            }
+          } else {
+            mma64<true, false>(tmem + T::T_X + 64 * s2, sb + T::RO + so * T::O_BYTES + T::O_PSI,
+                               sb + T::ATT + s2 * 8192);
+            mma_commit(bar(T::B_M2 + s2));
+            last_m = i;
+          }
+        }
+      }
+      if (!__all_sync(kFull, ok)) break;
     }
+    __syncwarp();
+    if (mma_role == 0) fast::tma_store_wait_all();
+    if (last_m >= 0)  // this thread's MMAs complete before tensor memory is released
+      drain_wait(bar(T::B_M2 + (last_m & 1)), (last_m >> 1) & 1);
+    if (last_u >= 0) drain_wait(bar(T::B_U + (last_u & 1)), (last_u >> 1) & 1);
     __syncwarp();
     if (loader && *abort_flag)  // after an abort: the ring I loads in flight land first
       for (int i = max(0, loaded_i - T::NI); i < loaded_i; i++) drain_wait(bar(T::B_FULLI + i % T::NI), (i / T::NI) & 1);
