@@ -10,37 +10,40 @@
 // the BF16 reference is kept, as in the other kernel families.  How it is
 // computed here:
 //
-// * One CTA per (b*h, segment) and SM (all 512 tensor-memory columns); it
-//   walks its segment's chunks with the FP32 state in registers.
-// * Every contraction of a chunk is a 64x64x64 BF16 tcgen05.mma with an FP32
-//   accumulator in tensor memory (M = 64 layout: row m at lane 32(m/16) +
-//   m%16), double-buffered across chunks:
-//     S       = Q_rot Ks^T              (the causal scores, rows and columns j)
+// * One CTA per (b*h, segment) and SM (all 512 tensor-memory columns), all
+//   resident at once (a cooperative launch).  Phase A: the CTA sums its own
+//   segment's state contributions (U of every chunk on tcgen05.mma, each
+//   group of four warps folding its chunks with their decays) and publishes
+//   the sum with a release flag.  Then it folds the sums of the earlier
+//   segments of its (b,h) (acquire, bounded spin) into the state entering
+//   the segment.  Phase C: it walks the segment's chunks with the FP32 state
+//   in registers.
+// * Contractions of a chunk on tcgen05.mma (64x64x64 BF16, FP32 accumulator
+//   in tensor memory, M = 64 layout: row m at lane 32(m/16) + m%16,
+//   double-buffered across chunks):
 //     U       = PsiV^T k_state          (the chunk's state contribution, [p][n])
 //     inter^T = bf16(state)^T Q_rot^T   ([p][j])
 //     intra^T = PsiV^T A^T              ([p][j], A = bf16(mask(S) exp(segsum)))
-//   Rows j of the chunk are stored in the fragment order of fast::perm() inside
-//   each 16-row block, so a thread that reads inter^T / intra^T as 16x256b
-//   fragments holds all four ranks of one token for a pair of p values (p,
-//   p+8): the rank-ordered BF16 diagonal and dz need no cross-lane traffic.
-// * Warp roles (16 warps):
+//   and on mma.sync (register fragments): S = Q_rot Ks^T on the causal 16x16
+//   blocks, the same-token qk_dot on the diagonal blocks.  Rows j of the
+//   chunk are stored in the fragment order of fast::perm() inside each 16-row
+//   block, so a thread that reads inter^T / intra^T as 16x256b fragments
+//   holds all four ranks of one token for a pair of p values (p, p+8): the
+//   rank-ordered BF16 diagonal and dz need no cross-lane traffic.
+// * Warp roles in phase C (16 warps, 4 per scheduler):
 //     0-7   epilogue: warp w reads p-block w%4 and the j-columns of tokens
 //           8(w/4)..8(w/4)+7; diagonal, out, Z branch, dmimo partials, dz;
-//     8-11  prologue: one 16-row j-block each; biased Q/K, same-token qk_dot
-//           (mma.sync on the diagonal tiles), rotary, k_scaled, k_state,
-//           PsiV, exp(segsum) below the diagonal, the token-scalar table;
-//     12-15 state: the causal matrix A of the previous chunk from S; the
-//           FP32 state (p-block w%4, all n) in registers, folded with U each
-//           chunk; bf16(state) for inter and the states output (warp 13's
-//           first thread stores it).  Only the fold and bf16(state) are
-//           serial from chunk to chunk.
-//   The MMAs of a chunk are issued by the warps that wait for their results
-//   anyway, alternating by chunk parity so that no warp carries every issue
-//   (an issue can stall while the tensor pipe works through earlier MMAs):
-//   S and U by warp 12 / 13 one state iteration ahead, inter^T and intra^T
-//   by warp 0 / 4 one epilogue step ahead.
-//   Warp 0's first thread refills ring I once a chunk's MMAs are done; warp
-//   8's loads dout and z (ring O).
+//     8-11  prologue: one 16-row j-block each; biased Q/K, same-token qk_dot,
+//           rotary, k_scaled, k_state, PsiV, the token-scalar table; warp 8's
+//           first thread loads dout and z (ring O);
+//     12-15 state: p-block w%4 of the FP32 state, folded with U of the
+//           previous chunk (tensor memory, issued a chunk ahead); bf16(state)
+//           for inter^T and the states output; the causal rows 16(w%4).. of
+//           A.  Warp 12's first thread issues inter^T and U of the next chunk,
+//           warp 13's intra^T (an issue stalls its thread for about the MMA's
+//           run time, so the accumulators go out from different threads);
+//           warp 12's also stores states, warp 15's refills ring I.  Only the
+//           fold is serial from chunk to chunk.
 // * Two TMA rings: ring I (q, k, v, angles, segsum; the prologue writes Q_rot
 //   and k_scaled over the raw q and k rows, k_state beside them) is freed when
 //   the chunk's MMAs complete; ring O (PsiV, dout, z -> dz, the qk table) when
