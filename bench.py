@@ -52,7 +52,7 @@ FIRST_STAGE_SOURCES = ("mmbf_fast.cuh", "mmbf_tc.cuh", "mmbf_kernels.cu")
 
 
 def kernel_source_sha256():
-    """sha256 over the first stage's CUDA sources (in name order, concatenated)."""
+    """sha256 over the first stage's CUDA sources (in the order listed, concatenated)."""
     h = hashlib.sha256()
     for name in FIRST_STAGE_SOURCES:
         h.update(open(os.path.join(KERNEL_DIR, name), "rb").read())
