@@ -336,6 +336,8 @@ def test_workspace_size_independent_of_device():
     dict(seqlen=1000, heads=3, groups=1, has_z=True, has_d=False),      # ragged tail
     dict(seqlen=64, batch=2, heads=4, groups=2, has_z=False, has_d=True),
     dict(seqlen=16, heads=1, has_z=True, has_d=True),                   # one chunk
+    dict(seqlen=2005, heads=16, has_z=True, has_d=True),                # 14-chunk segments, ragged tail
+    dict(seqlen=3000, batch=2, heads=8, groups=2, has_z=True, has_d=True),  # 21 / 20-chunk segments, GQA
 ])
 def test_tensor_core_family_forms(kw, two_kernel):
     lib = mm.load_library()
