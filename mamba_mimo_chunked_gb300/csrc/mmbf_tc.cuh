@@ -94,7 +94,8 @@ struct TCfg {
   static constexpr uint32_t A_RAW = 0, A_PSI = 12 * A_BUF;
   static constexpr int LMAX = 64;  // longest segment of the single-kernel form
   static constexpr uint32_t A_FAC = (MISC + 16 + 127) & ~127u, A_EDR = A_FAC + LMAX * C * 4,
-                            A_GAM = A_EDR + LMAX * C * 4, A_ALP = A_GAM + LMAX * 4, A_DEC = A_ALP + LMAX * 4;
+                            A_GAM = A_EDR + LMAX * C * 4, A_ALP = A_GAM + LMAX * 4, A_D4 = A_ALP + LMAX * 4,
+                            A_DEC = A_D4 + LMAX * 4;
   static constexpr uint32_t SMEM = A_DEC + 16 + 1024;  // + alignment slack of the base
   // tensor-memory columns (two buffers of 64 each)
   static constexpr uint32_t T_S = 0, T_U = 128, T_I = 256, T_X = 384;
@@ -413,6 +414,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     float* agam = reinterpret_cast<float*>(sm + T::A_GAM);
     float* aalp = reinterpret_cast<float*>(sm + T::A_ALP);
     float* adec = reinterpret_cast<float*>(sm + T::A_DEC);
+    float* ad4 = reinterpret_cast<float*>(sm + T::A_D4);
     // token scalars of the segment (the arithmetic of tok_fill)
     for (int e = threadIdx.x; e < na * C; e += T::NT) {
       const int tg = c0 * C + e;
@@ -446,10 +448,14 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       }
       *adec = gg;
     }
+    // decay from a group's previous chunk through chunk e: prod of alpha over (e - 4, e]
+    for (int e = threadIdx.x; e < na; e += T::NT)
+      ad4[e] = e >= 4 ? ((aalp[e - 3] * aalp[e - 2]) * aalp[e - 1]) * aalp[e] : 1.f;
     __syncthreads();
     const int w = warp >> 2, q = warp & 3;
     const int kw = na > w ? (na - w + 3) / 4 : 0;  // chunks of group w: w + 4k
-    const bool gl = (q == 0) && lane == 0;         // the group's TMA thread
+    const bool gl = (q == 0) && lane == 0;         // the group's MMA thread
+    const bool gt = (q == 1) && lane == 0;         // the group's TMA thread
     const uint16_t* mvb = reinterpret_cast<const uint16_t*>(sm + T::MVB);
     RowRegs<T> kb;  // k bias pairs in registers
     kb.load(reinterpret_cast<const uint16_t*>(sm + T::KBS));
@@ -467,8 +473,8 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::tma_load_4d(dst + T::A_V, &p.tm_v, 0, h, t0, b, full);
       fast::tma_load_4d(dst + T::A_ANG, &p.tm_ang, 0, h, t0, b, full);
     };
-    int loaded_a = 0, issued_a = 0;  // staging loads, U MMAs (group leader)
-    if (gl) {
+    int loaded_a = 0, issued_a = 0;  // staging loads (TMA thread), U MMAs (MMA thread)
+    if (gt) {
       loaded_a = min(3, kw);
       for (int k = 0; k < loaded_a; k++) load_A(k);
     }
@@ -482,13 +488,13 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
     auto fold = [&](int k) -> bool {
       if (!__all_sync(kFull, wait_b(p, bar(T::B_AU + w * 2 + (k & 1)), (k >> 1) & 1, abort_flag, 4))) return false;
       // U_k is done: chunk k's staging buffer takes chunk k + 3
-      if (gl && k + 3 < kw) {
+      if (gt && k + 3 < kw) {
         load_A(k + 3);
         loaded_a = k + 4;
       }
       const int i = w + 4 * k;
       // decay from the group's previous chunk through this one: prod of alpha over (c_{k-1}, c_k]
-      const float dk = k >= 1 ? ((aalp[i - 3] * aalp[i - 2]) * aalp[i - 1]) * aalp[i] : 1.f;
+      const float dk = ad4[i];  // 1 for the group's first chunk (i < 4)
       fast::tm_fence_after();
       float u[8][4];
       fast::tm_ld_frag<8>(tmem + tl_lane + 64 * (w * 2 + (k & 1)), u);
@@ -553,7 +559,7 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
         for (int e = 0; e < 4; e++) acc[nn][e] *= gl_last;
     }
     __syncwarp();
-    if (gl && *abort_flag)  // every staging load landed before the area is reused
+    if (gt && *abort_flag)  // every staging load landed before the area is reused
       for (int k = max(0, loaded_a - 3); k < loaded_a; k++) drain_wait(bar(T::B_AFULL + w * 3 + k % 3), (k / 3) & 1);
     __syncthreads();
     // the four group partials, summed in group order, published with a flag
