@@ -223,7 +223,10 @@ mmbf_status mamba_mimo_device_status(void* stream);
  * mamba_mimo_device_status.  Nothing faults or hangs; outputs of such a
  * call are incomplete.  Bit 1: the warp-specialised family takes its two-
  * kernel form (a separate state-sum kernel) where it would run as a single
- * kernel, so tests cover both forms.  For tests only. */
+ * kernel, so tests cover both forms.  Bit 2: in its single-kernel form the
+ * first segment of every (b,h) does not publish its segment sum, so the later
+ * segments' bounded look-back runs out and the call reports
+ * MMBF_ERR_DEVICE_TIMEOUT (after about a second).  For tests only. */
 void mamba_mimo_set_test_hooks(int flags);
 
 /* Test hook: evaluates, on the device, the approximate math the shape-

@@ -1719,8 +1719,9 @@ mmbf_status mamba_mimo_device_status(void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return fail(MMBF_ERR_CUDA, "reading the device status: %s", cudaGetErrorString(e));
   if ((w >> 8) == g_last_tag && (w & 0xffu) != 0)
-    return fail(MMBF_ERR_DEVICE_TIMEOUT, "a kernel of the last call stopped: a shared-memory barrier wait ran out (code %u)",
-                w & 0xffu);
+    return fail(MMBF_ERR_DEVICE_TIMEOUT, "a kernel of the last call stopped: a bounded wait ran out (code %u: %s)",
+                w & 0xffu,
+                (w & 0xffu) == 5u ? "the look-back on an earlier segment's published sum" : "a shared-memory barrier");
   return MMBF_OK;
 }
 
