@@ -81,7 +81,7 @@ struct TCfg {
   enum : uint32_t {
     B_FULLI = 0, B_FULLO = 4, B_PDONE = 8, B_OFREE = 12, B_U = 16, B_M2 = 18, B_SBR = 20, B_TOKW = 22,
     // phase A of the single-kernel form: per group TMA (3 buffers), prologue done, MMA done (2 buffers)
-    B_AFULL = 24, B_APA = 36, B_AU = 40, B_AUF = 48, NBAR = 56
+    B_AFULL = 24, B_APA = 36, B_AU = 44, B_AUF = 52, NBAR = 60
   };
 
   static constexpr uint32_t MISC = BAR + ((NBAR * 8 + 15) & ~15u);  // tmem slot, abort flag, last-CTA flag
@@ -321,7 +321,12 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
       fast::mbar_init(bar(T::B_OFREE + i), 8);
     }
     for (int i = 0; i < 12; i++) fast::mbar_init(bar(T::B_AFULL + i), 1);
-    for (int i = 0; i < 4; i++) fast::mbar_init(bar(T::B_APA + i), 4);
+    // a group's chunk prologue done, per chunk parity: only the MMA thread
+    // waits, so a warp may arrive for chunk k + 1 before a slower one has
+    // arrived for k; with one barrier per parity that arrival cannot complete
+    // chunk k's phase (and none for k + 2 comes before U_k has gone out,
+    // since the warp's fold of k waits for it)
+    for (int i = 0; i < 8; i++) fast::mbar_init(bar(T::B_APA + i), 4);
     for (int i = 0; i < 8; i++) {
       fast::mbar_init(bar(T::B_AU + i), 1);   // a group's U MMA done (per tensor-memory buffer)
       fast::mbar_init(bar(T::B_AUF + i), 4);  // the group's four warps folded that buffer
@@ -533,9 +538,9 @@ __global__ void __launch_bounds__(T::NT, 1) out_kernel(const __grid_constant__ P
                         reinterpret_cast<uint16_t*>(sm + apsi(k)), 16 * q);
       fast::fence_proxy_async();  // the MMA reads k_state and PsiV
       __syncwarp();
-      if (lane == 0) arrive(bar(T::B_APA + w));
+      if (lane == 0) arrive(bar(T::B_APA + w * 2 + (k & 1)));
       if (gl) {  // U_k, once the group's four warps are done and buffer k & 1 is folded
-        aok = wait_b(p, bar(T::B_APA + w), k & 1, abort_flag, 4) &&
+        aok = wait_b(p, bar(T::B_APA + w * 2 + (k & 1)), (k >> 1) & 1, abort_flag, 4) &&
               (k < 2 || wait_b(p, bar(T::B_AUF + w * 2 + (k & 1)), ((k - 2) >> 1) & 1, abort_flag, 4));
         if (aok) {
           fast::tm_fence_after();
