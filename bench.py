@@ -62,6 +62,7 @@ TENSOR_PATHS = {
     3: "tcgen05.mma kind::f16 M=64 N=64 K=16, TMEM accumulators (inter, intra); "
        "mma.sync m16n8k16 bf16 (causal scores, state fold, same-token qk_dot)",
     0: "mma.sync m16n8k16 bf16 (inter, scores, intra, qk_dot); tcgen05.mma state sums",
+    4: "mma.sync m16n8k16 bf16 (inter, scores, intra, qk_dot, state sums and updates)",
 }
 FALLBACK_HBM_GBS = 6800.0
 

@@ -202,7 +202,9 @@ void mamba_mimo_set_stage_events(void* const* events, int count);
  * used: -1 for the generic kernels (any shape of the envelope); 0, 1, 2 for
  * the shape-specialised families R4 C16 N=P=64, R8 C16 N=P=64 and R4 C16
  * N=P=32; 3 for the warp-specialised tensor-core family (R4 C16 N=P=64 with
- * reduced dout and without y: every chunk contraction on tcgen05.mma). */
+ * reduced dout and without y: every chunk contraction on tcgen05.mma); 4 for
+ * the shape-specialised wide-state family R4 C32 N=128 P=64 with rotary
+ * divisor 2. */
 int mamba_mimo_last_kernel_variant(void);
 
 /* Failure detection for the last mamba_mimo_bwd_fwd call on this thread.

@@ -11,6 +11,7 @@ SOURCES = [os.path.join(PKG_DIR, "csrc", "mmbf_kernels.cu")]
 HEADERS = [os.path.join(REPO_DIR, "include", "mamba_mimo_bwd_fwd.h"),
            os.path.join(REPO_DIR, "include", "mamba_mimo_bwd_bwd.h"),
            os.path.join(PKG_DIR, "csrc", "mmbf_fast.cuh"),
+           os.path.join(PKG_DIR, "csrc", "mmbf_tc.cuh"),
            os.path.join(PKG_DIR, "csrc", "mmbb.cuh")]
 LIB_PATH = os.path.join(PKG_DIR, "libmmbf.so")
 NVCC_FLAGS = [

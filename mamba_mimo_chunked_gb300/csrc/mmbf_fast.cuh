@@ -45,8 +45,9 @@ struct Cfg {
   static constexpr int NKT = N / 16;          // 16-wide k tiles over N
   static constexpr int NMT = P / 16;          // 16-row p blocks of X^T / state^T
   static constexpr int NMTH = NMT / SPLIT;    // p blocks per warp in the output stage
-  // smem row strides (elements): 128-byte rows unpadded, others padded by 8
-  static constexpr int LDN = (N == 64) ? 64 : N + 8;
+  // smem row strides (elements): 128- and 256-byte rows unpadded, others
+  // padded by 8
+  static constexpr int LDN = (N == 64 || N == 128) ? N : N + 8;
   static constexpr int LDP = (P == 64) ? 64 : P + 8;
   // one warp per j-block: k_scaled / k_state go over the warp's own rows of
   // the raw k / q stage tiles (output kernel), k_state over raw k (state kernel)
@@ -61,9 +62,15 @@ struct Cfg {
   static constexpr int NCW = N / WPM;         // state columns (n) per warp
   static constexpr int NN8 = NCW / 8;         // n8 tiles of the state per warp
   static constexpr int SLOTS = 4;             // X^T columns per thread: (tile nt, bit b)
+  // output-kernel CTAs per SM the launch bounds aim at (a 256-byte-row tile
+  // set takes most of an SM's shared memory: one CTA, all registers)
+  static constexpr int OUT_CTAS = NT <= 128 ? 3 : (NT <= 256 && N <= 64 ? 2 : 1);
   // token tables: a window of TW chunks, one token per thread, filled at the
   // window's first chunk; two windows in shared memory (TS floats per chunk)
-  static constexpr int TW = (NT / C < 8) ? NT / C : 8;
+  // (at most 128 tokens a window: two windows of C = 32 chunks fit beside
+  // the 256-byte-row stage tiles)
+  static constexpr int TW_T = (NT / C < 8) ? NT / C : 8;
+  static constexpr int TW = (TW_T * C > 128) ? 128 / C : TW_T;
   static constexpr int TS = 4 * C;
   // padded strides of small tables (bank spread): bias rows [R][N + 8] BF16,
   // same-token qk_dot [C][R*R + QKP] words
@@ -115,13 +122,15 @@ __device__ __forceinline__ int perm_inv(int r) {
 
 // Element offset of (row, col) in a row-major BF16 tile with row stride LD
 // whose 16-byte chunks are XOR-swizzled (the XOR touches col bits 3..5 only).
-// LD = 64 (128-byte rows, no padding): chunk ^ ((row & 7) ^ (bit 3 of row
-// moved to bit 1)).  Padded strides (LD = width + 8): chunk ^ (bit 3 of row).
-// Either way any 8 consecutive rows, and the row sets {0,1,4,5,8,9,12,13} and
-// {2,3,6,7,10,11,14,15} that perm() visits, hit 8 different bank groups.
+// LD = 64 or 128 (128- or 256-byte rows, no padding): chunk ^ ((row & 7) ^
+// (bit 3 of row moved to bit 1)); a chunk's bank group is the low three bits
+// of its swizzled index in both.  Padded strides (LD = width + 8): chunk ^
+// (bit 3 of row).  Either way any 8 consecutive rows, and the row sets
+// {0,1,4,5,8,9,12,13} and {2,3,6,7,10,11,14,15} that perm() visits, hit 8
+// different bank groups.
 template <int LD>
 __device__ __forceinline__ int swz(int row, int col) {
-  if (LD == 64) return row * 64 + (col ^ ((((row & 7) ^ ((row >> 2) & 2))) << 3));
+  if (LD == 64 || LD == 128) return row * LD + (col ^ ((((row & 7) ^ ((row >> 2) & 2))) << 3));
   return row * LD + (col ^ ((row & 8) << 1));
 }
 
@@ -1272,7 +1281,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // MODE >= 0 fixes the branches at compile time (bit 0: reduced dout, bit 1: z,
 // bit 2: d, bit 3: the forward output y); MODE = -1 reads them from Params.
 template <class K, int MODE>
-__global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 : 1)))
+__global__ void __launch_bounds__(K::NT, K::OUT_CTAS)
     output_kernel(const __grid_constant__ Params p) {
   const bool RED = MODE >= 0 ? (MODE & 1) != 0 : p.reduced != 0;
   const bool HZ = MODE >= 0 ? (MODE & 2) != 0 : p.has_z != 0;

@@ -903,17 +903,8 @@ static const size_t kSmemLimit = 227 * 1024;
 using FastA = fast::Cfg<4, 16, 64, 64, 4, 1>;  // R4 C16 N=P=64 (the pages' timed and unit-test shape)
 using FastB = fast::Cfg<8, 16, 64, 64, 4, 2>;  // R8 C16 N=P=64
 using FastC = fast::Cfg<4, 16, 32, 32, 4, 1>;  // R4 C16 N=P=32
+using FastD = fast::Cfg<4, 32, 128, 64, 2, 1>;  // R4 C32 N=128 P=64, rotary on all of N (wide state)
 
-template <class K>
-static bool fast_fits(const Params& p) {
-  return p.R == K::R && p.C == K::C && p.N == K::N && p.P == K::P && p.div == K::DIV;
-}
-static int fast_index(const Params& p) {
-  if (fast_fits<FastA>(p)) return 0;
-  if (fast_fits<FastB>(p)) return 1;
-  if (fast_fits<FastC>(p)) return 2;
-  return -1;
-}
 template <class K>
 static size_t fast_out_smem(const Params& p) {
   return fast::smem_layout<K>(true, p.reduced, p.has_z, p.want_y).total;
@@ -924,6 +915,25 @@ using StateCfg = fast::Cfg<K::R, K::C, K::N, K::P, K::DIV, 1>;
 template <class K>
 static size_t fast_state_smem(const Params& p) {
   return fast::smem_layout<StateCfg<K>>(false, p.reduced, p.has_z).total;
+}
+// A family takes the shape when its tile set fits in shared memory for the
+// call's branches both without and with the forward output y, so the two
+// entry points run the same kernels (the wide-state tiles leave no room for
+// per-rank dout).
+template <class K>
+static bool fast_fits(const Params& p) {
+  Params py = p;
+  py.want_y = 1;
+  return p.R == K::R && p.C == K::C && p.N == K::N && p.P == K::P && p.div == K::DIV &&
+         fast_out_smem<K>(p) <= kSmemLimit && fast_out_smem<K>(py) <= kSmemLimit &&
+         fast_state_smem<K>(p) <= kSmemLimit;
+}
+static int fast_index(const Params& p) {
+  if (fast_fits<FastA>(p)) return 0;
+  if (fast_fits<FastB>(p)) return 1;
+  if (fast_fits<FastC>(p)) return 2;
+  if (fast_fits<FastD>(p)) return 3;
+  return -1;
 }
 
 // Largest dynamic shared memory each fast kernel has been opened for on the
@@ -961,7 +971,7 @@ static int per_sm(int launch_bound_ctas, size_t smem, int tmem_cols) {
 // Resident output-kernel CTAs (all SMs) of the shape-specialised family.
 template <class K>
 static int fast_slots_of(const Params& p) {
-  return kPlanSms * per_sm(K::NT <= 128 ? 3 : (K::NT <= 256 ? 2 : 1), fast_out_smem<K>(p), K::TM_COLS);
+  return kPlanSms * per_sm(K::OUT_CTAS, fast_out_smem<K>(p), K::TM_COLS);
 }
 // Resident state-kernel CTAs (all SMs).
 template <class K>
@@ -972,7 +982,8 @@ static int fast_state_slots(const Params& p) {
   switch (p.fast) {
     case 0: return fast_state_slots_of<FastA>(p);
     case 1: return fast_state_slots_of<FastB>(p);
-    default: return fast_state_slots_of<FastC>(p);
+    case 2: return fast_state_slots_of<FastC>(p);
+    default: return fast_state_slots_of<FastD>(p);
   }
 }
 static int fast_slots(const Params& p) {
@@ -980,7 +991,8 @@ static int fast_slots(const Params& p) {
   switch (p.fast) {
     case 0: return fast_slots_of<FastA>(p);
     case 1: return fast_slots_of<FastB>(p);
-    default: return fast_slots_of<FastC>(p);
+    case 2: return fast_slots_of<FastC>(p);
+    default: return fast_slots_of<FastD>(p);
   }
 }
 // Chunks per segment: the length that minimises (waves x (L + per-CTA setup)),
@@ -1053,8 +1065,8 @@ static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduc
   p.UA = 1;
   p.LA = p.L;
   p.nunit = p.nseg;
-  p.fast = fast_index(p);
   p.want_y = want_y ? 1 : 0;
+  p.fast = fast_index(p);
   // the warp-specialised tensor-core output kernel: R4 C16 N=P=64, reduced
   // dout (mimo_o given), without the forward output y
   p.tc = (p.fast == 0 && p.reduced && !p.want_y) ? 1 : 0;
@@ -1534,7 +1546,8 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
     switch (p.fast) {
       case 0: fast_ok = encode_stage_maps<FastA>(p); break;
       case 1: fast_ok = encode_stage_maps<FastB>(p); break;
-      default: fast_ok = encode_stage_maps<FastC>(p); break;
+      case 2: fast_ok = encode_stage_maps<FastC>(p); break;
+      default: fast_ok = encode_stage_maps<FastD>(p); break;
     }
   }
   if (fast_ok) {
@@ -1544,14 +1557,15 @@ static mmbf_status run_op(const mmbf_dims* dims, const void* dout, const void* q
       switch (p.fast) {
         case 0: e = launch_fast<FastA>(p, st, &launches); break;
         case 1: e = launch_fast<FastB>(p, st, &launches); break;
-        default: e = launch_fast<FastC>(p, st, &launches); break;
+        case 2: e = launch_fast<FastC>(p, st, &launches); break;
+        default: e = launch_fast<FastD>(p, st, &launches); break;
       }
     }
     if (e == cudaSuccess && g_stage_error != cudaSuccess) {
       e = g_stage_error;
       g_stage_error = cudaSuccess;
     }
-    g_variant = p.tc ? 3 : p.fast;
+    g_variant = p.tc ? 3 : (p.fast == 3 ? 4 : p.fast);  // (the wide-state family reports 4)
     g_plan[0] = p.L; g_plan[1] = p.nseg; g_plan[2] = p.UA; g_plan[3] = p.LA; g_plan[4] = fast_slots(p);
     g_plan[5] = p.fused;
     g_plan[6] = g_fused_refused;

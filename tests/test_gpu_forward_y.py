@@ -57,7 +57,8 @@ def _lib(cuda_lib):
 @pytest.mark.parametrize("reduced,has_z,has_d", [(True, True, True), (True, False, True),
                                                  (False, True, False), (False, False, False),
                                                  (True, True, False)])
-@pytest.mark.parametrize("shape", [dict(), dict(R=8), dict(N=32, P=32), dict(R=3, N=12, P=5, C=6, div=2)])
+@pytest.mark.parametrize("shape", [dict(), dict(R=8), dict(N=32, P=32), dict(R=3, N=12, P=5, C=6, div=2),
+                                   dict(N=128, C=32, div=2, S=80)])
 def test_forward_y_branches_and_families(reduced, has_z, has_d, shape):
     check(unit(reduced=reduced, has_z=has_z, has_d=has_d, **shape), f"{shape} {reduced}{has_z}{has_d}")
 

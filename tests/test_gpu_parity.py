@@ -148,10 +148,12 @@ def sampled_heads(index, pairs):
     got = mm.mamba_mimo_bwd_fwd(*si.args_of(inp))
     torch.cuda.synchronize()
     variant = mm.last_kernel_variant()
-    if index in (2, 4):   # shapes with specialised kernels must use them
+    if index in (2, 3, 4):   # shapes with specialised kernels must use them
         assert variant >= 0, f"{wl.name} ran the generic kernels"
     if index == 2:        # the timed shape runs the warp-specialised tensor-core kernel
         assert variant == 3, f"{wl.name} ran kernel family {variant}"
+    if index == 3:        # the wide-state family (256-byte N rows, C*R = 128)
+        assert variant == 4, f"{wl.name} ran kernel family {variant}"
     for (b, h) in pairs:
         sl = si.head_slice(inp, b, h)
         sl_cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in sl.items()}
@@ -361,3 +363,24 @@ def test_timed_workload_two_kernel_form_sampled_heads():
         assert mm.last_plan()["single_kernel"] == 0
     finally:
         lib.mamba_mimo_set_test_hooks(0)
+
+
+# --- the wide-state family: R4 C32 N=128 P=64, rotary on all of N -------------
+
+@pytest.mark.parametrize("branches", [(True, True, True), (True, False, False), (False, True, True),
+                                      (False, False, True)])
+@pytest.mark.parametrize("kw", [
+    dict(seqlen=200, heads=2),                         # ragged tail, several segments
+    dict(seqlen=1000, batch=2, heads=4, groups=2),     # GQA, B = 2, multi-segment prefix
+    dict(seqlen=32, heads=1),                          # one full chunk
+    dict(seqlen=5, heads=1),                           # one partial chunk
+])
+def test_wide_state_family(kw, branches):
+    r, z, d = branches
+    inp = unit_inputs(state_dim=128, value_dim=64, rank=4, chunk_size=32, div=2, reduce_o=r, has_z=z,
+                      has_d=d, recipe="workload", **kw)
+    got = run_gpu(inp)
+    # per-rank dout is a [C*R][P] stage tile the wide family has no room for:
+    # those calls run the generic kernels
+    assert mm.last_kernel_variant() == (4 if r else -1)
+    compare(got, oracle.bwd_fwd(*si.args_of(inp)), f"{kw} {branches}")
