@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import os
@@ -84,6 +85,9 @@ def parse_args():
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only (no clock-load stretch, per-kernel event pass, "
                          "end-to-end pass or CPU baseline): the short command ncu captures run")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="with --quick: the workload with H heads (G capped at H) instead of its own "
+                         "count, the same per-head shape; a smaller case of the same kernels for ncu")
     ap.add_argument("--op", choices=["bwd_fwd", "bwd_bwd"], default="bwd_fwd",
                     help="bwd_bwd: time the second backward stage instead (its own JSON line)")
     return ap.parse_args()
@@ -450,6 +454,14 @@ def main():
     wi = WORKLOAD_INDEX if args.workload is None else args.workload
     wl = si.WORKLOADS[wi]
     timed_shape = wi == WORKLOAD_INDEX
+    if args.heads is not None:
+        if not args.quick:
+            raise SystemExit("--heads is for the short capture runs (--quick) only")
+        g = min(wl.G, args.heads)
+        if args.heads < 1 or args.heads % g:
+            raise SystemExit(f"--heads {args.heads}: H must be a positive multiple of G = {g}")
+        wl = dataclasses.replace(wl, name=f"{wl.name}_h{args.heads}", H=args.heads, G=g)
+        timed_shape = False
     stream = torch.cuda.current_stream(dev)
 
     # Input/output sets, resident in HBM before timing starts.

@@ -65,6 +65,8 @@ struct Cfg {
   // output-kernel CTAs per SM the launch bounds aim at (a 256-byte-row tile
   // set takes most of an SM's shared memory: one CTA, all registers)
   static constexpr int OUT_CTAS = NT <= 128 ? 3 : (NT <= 256 && N <= 64 ? 2 : 1);
+  // state-sum kernel CTAs per SM the launch bounds aim at
+  static constexpr int STATE_CTAS = NT <= 128 ? 6 : (NT <= 256 ? 2 : 1);
   // token tables: a window of TW chunks, one token per thread, filled at the
   // window's first chunk; two windows in shared memory (TS floats per chunk)
   // (at most 128 tokens a window: two windows of C = 32 chunks fit beside
@@ -1020,7 +1022,7 @@ __device__ __forceinline__ void fold_u(float (&st)[K::NN8][4], uint32_t taddr, f
 
 // Segment-local state sums (fast path of segment_state_kernel).
 template <class K>
-__global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(K::NT, K::STATE_CTAS) state_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char sm_raw[];
   unsigned char* sm = smem_base<K>(sm_raw);
   const Smem L = smem_layout<K>(false, p.reduced, p.has_z);
@@ -1039,6 +1041,10 @@ __global__ void __launch_bounds__(K::NT, (K::NT <= 128 ? 6 : 1)) state_kernel(co
   uint16_t* kbs = reinterpret_cast<uint16_t*>(sm + L.kbs);
 
   if (unit == 0 && threadIdx.x == 0) p.ws_count[bh] = 0u;  // read by this call's output kernel
+  if (seg == p.nseg - 1) {  // no later segment reads the last one's sum (launched only when nseg = 1)
+    pdl_trigger();
+    return;
+  }
   stage_init<K>(L, sm);
   if (c0 < c1) stage_issue<K>(p, L, sm, 0, bh, c0, false, false, true);
   cp_commit();
@@ -1259,7 +1265,7 @@ __global__ void __launch_bounds__(128) segment_prefix_fast_kernel(Params p) {
     float x[GRP], d[GRP];
 #pragma unroll
     for (int q = 0; q < GRP; q++) {
-      const bool in = s0 + q < p.nseg;
+      const bool in = s0 + q < p.nseg - 1;  // (the last segment's sum is not computed)
       x[q] = in ? __ldcg(base + (int64_t)(s0 + q) * NPe) : 0.f;
       d[q] = in ? __ldcg(dec + s0 + q) : 1.f;
     }

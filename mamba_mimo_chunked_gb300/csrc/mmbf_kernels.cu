@@ -976,7 +976,7 @@ static int fast_slots_of(const Params& p) {
 // Resident state-kernel CTAs (all SMs).
 template <class K>
 static int fast_state_slots_of(const Params& p) {
-  return kPlanSms * per_sm(StateCfg<K>::NT <= 128 ? 6 : 1, fast_state_smem<K>(p), K::UMMA ? 64 : 0);
+  return kPlanSms * per_sm(StateCfg<K>::STATE_CTAS, fast_state_smem<K>(p), K::UMMA ? 64 : 0);
 }
 static int fast_state_slots(const Params& p) {
   switch (p.fast) {
@@ -1088,15 +1088,18 @@ static mmbf_status plan(const mmbf_dims* dims, int64_t C, int64_t div, int reduc
     // chains.  UA minimises (waves x (chunks per unit + setup)) over the
     // resident state CTAs; clusters of more than two CTAs measured slower
     // (co-scheduling of the whole cluster leaves slots idle).
+    // Only the sums of segments 0 .. nseg-2 are computed: no segment reads
+    // the last one's.
     const int64_t heads = (int64_t)p.B * p.H;
     const int64_t sslots = fast_state_slots(p);
+    const int64_t nsum = std::max(1, p.nseg - 1);
     int ua = 1;
     double best = 1e300;
     // (the tensor-core output kernel runs one long segment per SM: its state
     // units come in clusters of up to eight)
     for (int u = 1; u <= std::min(p.tc ? 8 : 2, p.L); u++) {
       const int la = (p.L + u - 1) / u;
-      const int64_t ctas = heads * p.nseg * ((p.L + la - 1) / la);
+      const int64_t ctas = heads * nsum * ((p.L + la - 1) / la);
       const double cost = (double)((ctas + sslots - 1) / sslots) * (la + 2.0);
       if (cost < best - 1e-9) {
         best = cost;
@@ -1252,6 +1255,11 @@ static cudaError_t launch_ex(Kern kern, dim3 grid, dim3 block, size_t smem, cuda
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// State-sum units launched: those of segments 0 .. nseg-2 (the last segment's
+// sum is read by no one); with one segment, one cluster that only resets the
+// gradient counter.
+static int state_units(const Params& p) { return std::max(1, p.nseg - 1) * p.UA; }
+
 static bool aligned16(const void* x) { return x == nullptr || (reinterpret_cast<uintptr_t>(x) & 15) == 0; }
 
 template <class K>
@@ -1272,7 +1280,7 @@ static cudaError_t launch_fast(const Params& p, cudaStream_t st, int* launches) 
   g_failed_stage = 0;
   stage_event(0, 0, st);
   // the UA units of a segment form one cluster (UA <= 8)
-  e = launch_ex(fast::state_kernel<StateCfg<K>>, dim3(p.B * p.H, p.nunit), dim3(StateCfg<K>::NT), ss,
+  e = launch_ex(fast::state_kernel<StateCfg<K>>, dim3(p.B * p.H, state_units(p)), dim3(StateCfg<K>::NT), ss,
                 st, false, p, p.UA);
   stage_event(0, 1, st);
   (*launches)++;
@@ -1370,7 +1378,7 @@ static cudaError_t launch_tc(Params& p, cudaStream_t st, int* launches) {
   g_stage_names_n = 2;
   g_failed_stage = 0;
   stage_event(0, 0, st);
-  e = launch_ex(fast::state_kernel<KS>, dim3(p.B * p.H, p.nunit), dim3(KS::NT), ss, st, false, p, p.UA);
+  e = launch_ex(fast::state_kernel<KS>, dim3(p.B * p.H, state_units(p)), dim3(KS::NT), ss, st, false, p, p.UA);
   stage_event(0, 1, st);
   (*launches)++;
   if (e != cudaSuccess) return e;
